@@ -1,0 +1,266 @@
+/*
+ * FP64 CPU oracle for causal grouped-query softmax attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plainly written
+ * definition that the CUDA path is checked against.  It shares no code,
+ * header or constant with the CUDA library, and only the test suite, the
+ * smoke check and the benchmark's CPU-baseline / reference arm may load it.
+ * The product path never calls it and has no CPU fallback.
+ *
+ * What is computed (one query row at a time, every quantity in double):
+ *
+ *   TileOPs "Attention Operators", GQADenseFwdOp, stages 1, 4, 5, 7:
+ *     r(h)  = floor(h / g),  g = Hq / Hkv           (head grouping)
+ *     p_i   = i + Skv - Sq                          (bottom-right alignment)
+ *     z_j   = scale * <q_i,h , k_j,r(h)>            (scores)
+ *     V_i   = { j : (!causal || j <= p_i) }         (visibility)
+ *     O_i,h = sum_{j in V_i} softmax_j(z) * v_j,r(h)
+ *   RL-Kernel "Standard Softmax Attention", Tensor Contract / Accuracy:
+ *     key_padding_mask[b, j] == 0 removes key j from V_i for every head and
+ *     query (the column becomes -inf); scale None -> 1/sqrt(D) is resolved by
+ *     the caller, any explicit value (0.0 included) is used as given.
+ *   TileOPs "Attention Operators", MHADecodePagedWithKVCacheFwdOp and
+ *   GQAPagedFwdOp:  a row with no visible key outputs zeros; paged K/V of
+ *     request b at logical position t live in physical page
+ *     block_table[b, t / page_size], slot t % page_size.
+ *   MATE "QSA", Core Attention: the log-sum-exp is natural-log, of the
+ *     scaled logits, and -inf for a row with no visible key.
+ *
+ * softmax_j(z) is written out as its definition: with M = max_{j in V_i} z_j
+ * and Z = sum_{j in V_i} exp(z_j - M), weight_j = exp(z_j - M) / Z and
+ * LSE = M + log Z.  Subtracting M changes nothing mathematically; it only
+ * keeps exp() finite.
+ *
+ * Inputs may be given as IEEE double or as bfloat16 bit patterns (uint16);
+ * a bfloat16 value widens to double exactly (its bits are the top half of a
+ * float).  Outputs are always double.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fopenmp -fPIC -shared (OpenMP optional).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_F64 = 0, ORACLE_BF16 = 1 };
+
+/* Exact widening of one element of an input array to double. */
+static double load_elem(const void* base, size_t idx, int dtype) {
+    if (dtype == ORACLE_F64) return ((const double*)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/*
+ * One query row of the dense definition.
+ *   q      : [B, Sq, Hq, D]      k, v : [B, Skv, Hkv, D]      (BSHD)
+ *   mask   : [B, Skv] bytes, nonzero = keep, or NULL
+ *   z      : scratch of Skv doubles
+ *   out    : D doubles; *lse_out : the row's log-sum-exp
+ */
+static void dense_row(const void* q, const void* k, const void* v, int dtype,
+                      const uint8_t* mask, int Hq, int Hkv, int Sq, int Skv,
+                      int D, int causal, double scale, int b, int i, int h,
+                      double* z, double* out, double* lse_out) {
+    const int g = Hq / Hkv;
+    const int r = h / g;                       /* KV head of query head h */
+    const long p = (long)i + Skv - Sq;         /* query position on the key axis */
+    const size_t q_off = (((size_t)b * Sq + i) * Hq + h) * (size_t)D;
+
+    int any = 0;
+    double M = -INFINITY;
+    for (int j = 0; j < Skv; ++j) {
+        int visible = (!causal || (long)j <= p) &&
+                      (mask == NULL || mask[(size_t)b * Skv + j] != 0);
+        if (!visible) { z[j] = -INFINITY; continue; }
+        const size_t k_off = (((size_t)b * Skv + j) * Hkv + r) * (size_t)D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += load_elem(q, q_off + d, dtype) * load_elem(k, k_off + d, dtype);
+        z[j] = scale * dot;
+        if (!any || z[j] > M) M = z[j];
+        any = 1;
+    }
+
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (!any) {                                /* no visible key: zeros, -inf */
+        *lse_out = -INFINITY;
+        return;
+    }
+    double Z = 0.0;
+    for (int j = 0; j < Skv; ++j)
+        if (z[j] != -INFINITY) Z += exp(z[j] - M);
+    for (int j = 0; j < Skv; ++j) {
+        if (z[j] == -INFINITY) continue;
+        const double w = exp(z[j] - M) / Z;
+        const size_t v_off = (((size_t)b * Skv + j) * Hkv + r) * (size_t)D;
+        for (int d = 0; d < D; ++d) out[d] += w * load_elem(v, v_off + d, dtype);
+    }
+    *lse_out = M + log(Z);
+}
+
+static int check_dense_args(int B, int Hq, int Hkv, int Sq, int Skv, int D) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv < 0 || D <= 0) return -1;
+    if (Hq % Hkv != 0) return -2;              /* GQA needs Hq divisible by Hkv */
+    return 0;
+}
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/* Number of threads the next parallel region would use (1 without OpenMP). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Dense attention over every row.  o: [B, Sq, Hq, D]; lse: [B, Sq, Hq].
+ * Returns 0, -1 for a bad size, -2 when Hq is not a multiple of Hkv,
+ * -3 when scratch memory cannot be had.
+ */
+int oracle_attn_dense(const void* q, const void* k, const void* v, int dtype,
+                      const uint8_t* mask, double* o, double* lse, int B,
+                      int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                      double scale, int nthreads) {
+    int rc = check_dense_args(B, Hq, Hkv, Sq, Skv, D);
+    if (rc) return rc;
+    set_threads(nthreads);
+    const long nrows = (long)B * Sq * Hq;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* z = (double*)malloc(sizeof(double) * (size_t)(Skv > 0 ? Skv : 1));
+        if (!z) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (long row = 0; row < nrows; ++row) {
+                const int h = (int)(row % Hq);
+                const int i = (int)((row / Hq) % Sq);
+                const int b = (int)(row / ((long)Hq * Sq));
+                dense_row(q, k, v, dtype, mask, Hq, Hkv, Sq, Skv, D, causal,
+                          scale, b, i, h, z, o + (size_t)row * D, lse + row);
+            }
+            free(z);
+        }
+    }
+    return failed ? -3 : 0;
+}
+
+/*
+ * Dense attention for a list of rows only.  rows: nrows triples (b, i, h);
+ * o_rows: [nrows, D]; lse_rows: [nrows].  Same return codes, plus -4 for a
+ * row index out of range.
+ */
+int oracle_attn_dense_rows(const void* q, const void* k, const void* v,
+                           int dtype, const uint8_t* mask, const int32_t* rows,
+                           int nrows, double* o_rows, double* lse_rows, int B,
+                           int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                           double scale, int nthreads) {
+    int rc = check_dense_args(B, Hq, Hkv, Sq, Skv, D);
+    if (rc) return rc;
+    for (int n = 0; n < nrows; ++n) {
+        if (rows[3 * n] < 0 || rows[3 * n] >= B || rows[3 * n + 1] < 0 ||
+            rows[3 * n + 1] >= Sq || rows[3 * n + 2] < 0 || rows[3 * n + 2] >= Hq)
+            return -4;
+    }
+    set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* z = (double*)malloc(sizeof(double) * (size_t)(Skv > 0 ? Skv : 1));
+        if (!z) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int n = 0; n < nrows; ++n)
+                dense_row(q, k, v, dtype, mask, Hq, Hkv, Sq, Skv, D, causal,
+                          scale, rows[3 * n], rows[3 * n + 1], rows[3 * n + 2],
+                          z, o_rows + (size_t)n * D, lse_rows + n);
+            free(z);
+        }
+    }
+    return failed ? -3 : 0;
+}
+
+/*
+ * Paged attention, written as "gather the request's cache into a dense
+ * sequence, then apply the dense definition" (the paged ops on the TileOPs
+ * page read the same logical sequence through block_table).
+ *
+ *   q            : [B, Sq, Hq, D]
+ *   k_cache, v_cache : [num_pages, page_size, Hkv, D]
+ *   seqlens      : [B] logical cache length L_b, the Sq query tokens included
+ *   block_table  : [B, max_pages] physical page of each logical page
+ *   req_mask     : [B] bytes, nonzero = compute request b (NULL = all)
+ *   o            : [B, Sq, Hq, D]; lse : [B, Sq, Hq]; rows of requests left
+ *                  out by req_mask are not written.
+ *
+ * Query i of request b sits at key position i + L_b - Sq (end-aligned).
+ * Returns 0; -1 bad size; -2 Hq % Hkv != 0; -3 out of memory; -5 a length
+ * outside [0, max_pages * page_size]; -6 a needed block_table entry outside
+ * [0, num_pages).
+ */
+int oracle_attn_paged(const void* q, const void* k_cache, const void* v_cache,
+                      int dtype, const int32_t* seqlens,
+                      const int32_t* block_table, int page_size,
+                      const uint8_t* req_mask, double* o, double* lse, int B,
+                      int Sq, int Hq, int Hkv, int D, int num_pages,
+                      int max_pages, int causal, double scale, int nthreads) {
+    int rc = check_dense_args(B, Hq, Hkv, Sq, 0, D);
+    if (rc) return rc;
+    if (page_size <= 0 || num_pages < 0 || max_pages < 0) return -1;
+    for (int b = 0; b < B; ++b) {
+        if (req_mask && !req_mask[b]) continue;
+        const int L = seqlens[b];
+        if (L < 0 || (long)L > (long)max_pages * page_size) return -5;
+        const int npages = (L + page_size - 1) / page_size;
+        for (int lp = 0; lp < npages; ++lp) {
+            const int32_t phys = block_table[(size_t)b * max_pages + lp];
+            if (phys < 0 || phys >= num_pages) return -6;
+        }
+    }
+    const size_t es = dtype == ORACLE_F64 ? sizeof(double) : sizeof(uint16_t);
+    for (int b = 0; b < B; ++b) {
+        if (req_mask && !req_mask[b]) continue;
+        const int L = seqlens[b];
+        /* Gather request b's keys and values, token by token, into the dense
+         * layout [1, L, Hkv, D]. */
+        const size_t tok_elems = (size_t)Hkv * D;
+        char* kd = (char*)malloc(es * tok_elems * (size_t)(L > 0 ? L : 1));
+        char* vd = (char*)malloc(es * tok_elems * (size_t)(L > 0 ? L : 1));
+        if (!kd || !vd) { free(kd); free(vd); return -3; }
+        for (int t = 0; t < L; ++t) {
+            const int32_t phys = block_table[(size_t)b * max_pages + t / page_size];
+            const size_t src = ((size_t)phys * page_size + t % page_size) * tok_elems;
+            memcpy(kd + (size_t)t * tok_elems * es, (const char*)k_cache + src * es,
+                   tok_elems * es);
+            memcpy(vd + (size_t)t * tok_elems * es, (const char*)v_cache + src * es,
+                   tok_elems * es);
+        }
+        const char* qb = (const char*)q + (size_t)b * Sq * Hq * D * es;
+        rc = oracle_attn_dense(qb, kd, vd, dtype, NULL,
+                               o + (size_t)b * Sq * Hq * D, lse + (size_t)b * Sq * Hq,
+                               1, Hq, Hkv, Sq, L, D, causal, scale, nthreads);
+        free(kd);
+        free(vd);
+        if (rc) return rc;
+    }
+    return 0;
+}
