@@ -1,0 +1,148 @@
+"""Python entry points with the C ABI's names; torch supplies memory and streams.
+
+Every step of the computation runs in libgqa_attn.so.  These functions check
+dtypes and devices, make inputs contiguous (TileOPs GQADenseFwdOp, forward:
+non-contiguous inputs are copied first), resolve ``scale=None`` to 1/sqrt(D)
+(RL-Kernel Tensor Contract), allocate outputs with torch and pass raw pointers
+plus the current CUDA stream.  A non-OK status raises: ``ValueError`` for
+argument problems (naming the refused limit), ``RuntimeError`` for CUDA errors.
+"""
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+
+_ARG_ERRORS = {1, 2, 3, 4}
+
+
+def _raise(status: int, what: str):
+    name = _lib.status_name(status)
+    msg = "%s: %s (%s)" % (what, _lib.load().gqa_status_string(status).decode(), name)
+    if status in _ARG_ERRORS:
+        raise ValueError(msg)
+    raise RuntimeError(msg)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_bf16_cuda(name, t, ndim):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != torch.bfloat16:
+        raise ValueError("%s must be bfloat16, got %s" % (name, t.dtype))
+    if t.dim() != ndim:
+        raise ValueError("%s must have %d dimensions, got %d" % (name, ndim, t.dim()))
+
+
+def resolve_scale(scale, D):
+    """None -> 1/sqrt(D); an explicit value (0.0 included) is used verbatim."""
+    return 1.0 / math.sqrt(D) if scale is None else float(scale)
+
+
+def attn_fwd_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, out=None, lse=None):
+    """Dense / chunked-prefill GQA attention.
+
+    q [B,Sq,Hq,D], k/v [B,Skv,Hkv,D] bfloat16 CUDA tensors (BSHD);
+    key_padding_mask [B,Skv] bool (True = keep) or None.
+    Returns (o [B,Sq,Hq,D] bf16, lse [B,Sq,Hq] float32, natural log).
+    """
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16_cuda(n, t, 4)
+    B, Sq, Hq, D = q.shape
+    Bk, Skv, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch: q %s, k %s, v %s" % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    if Hq % Hkv != 0:
+        raise ValueError("Hq (%d) must be divisible by Hkv (%d)" % (Hq, Hkv))
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    m = None
+    if key_padding_mask is not None:
+        if tuple(key_padding_mask.shape) != (B, Skv):
+            raise ValueError("key_padding_mask must be [B, Skv] = [%d, %d]" % (B, Skv))
+        m = key_padding_mask.to(device=q.device, dtype=torch.bool).contiguous().view(torch.uint8)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device)
+    st = _lib.load().attn_fwd_dense(_ptr(q), _ptr(k), _ptr(v), _ptr(m), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
+                                    Skv, D, int(bool(causal)), resolve_scale(scale, D), _stream(q.device))
+    if st != 0:
+        _raise(st, "attn_fwd_dense")
+    return out, lse
+
+
+def attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, page_size, max_pages):
+    """Workspace bytes attn_decode_paged needs on the current device."""
+    return int(_lib.load().attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, page_size, max_pages))
+
+
+def attn_decode_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=True, scale=None,
+                      workspace=None, out=None, lse=None):
+    """Paged decode.
+
+    q [B,Sq,Hq,D] bf16; k_cache/v_cache [num_pages,page_size,Hkv,D] bf16;
+    real_seqlen_kv [B] int32 (query tokens included); block_table [B,max_pages] int32.
+    workspace: optional uint8 CUDA tensor of at least attn_decode_paged_workspace_size bytes.
+    Returns (o [B,Sq,Hq,D] bf16, lse [B,Sq,Hq] float32).
+    """
+    _check_bf16_cuda("q", q, 4)
+    _check_bf16_cuda("k_cache", k_cache, 4)
+    _check_bf16_cuda("v_cache", v_cache, 4)
+    B, Sq, Hq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shape mismatch: k %s, v %s, D %d" % (tuple(k_cache.shape), tuple(v_cache.shape), D))
+    if Hq % Hkv != 0:
+        raise ValueError("Hq (%d) must be divisible by Hkv (%d)" % (Hq, Hkv))
+    for n, t in (("real_seqlen_kv", real_seqlen_kv), ("block_table", block_table)):
+        if not t.is_cuda or t.dtype != torch.int32:
+            raise ValueError("%s must be an int32 CUDA tensor" % n)
+    if tuple(real_seqlen_kv.shape) != (B,) or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("real_seqlen_kv must be [B] and block_table [B, max_pages]")
+    max_pages = block_table.shape[1]
+    q, k_cache, v_cache = q.contiguous(), k_cache.contiguous(), v_cache.contiguous()
+    sl, bt = real_seqlen_kv.contiguous(), block_table.contiguous()
+    need = attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, page_size, max_pages)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device)
+    st = _lib.load().attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sl), _ptr(bt), page_size,
+                                       _ptr(out), _ptr(lse), B, Sq, Hq, Hkv, D, num_pages, max_pages,
+                                       int(bool(causal)), resolve_scale(scale, D), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(q.device))
+    if st != 0:
+        _raise(st, "attn_decode_paged")
+    return out, lse
+
+
+def attn_validate_paged(real_seqlen_kv, block_table, Sq, page_size, num_pages, causal=True):
+    """Host-side range check of paged metadata (synchronises the stream)."""
+    B, max_pages = block_table.shape
+    st = _lib.load().attn_validate_paged(_ptr(real_seqlen_kv.contiguous()), _ptr(block_table.contiguous()), B, Sq,
+                                         page_size, num_pages, max_pages, int(bool(causal)),
+                                         _stream(block_table.device))
+    if st != 0:
+        _raise(st, "attn_validate_paged")
+
+
+def gqa_device_error():
+    """Raise if a kernel recorded a timed-out wait since the last check (synchronises)."""
+    st = _lib.load().gqa_device_error()
+    if st != 0:
+        _raise(st, "gqa_device_error")
+
+
+# Short aliases in the style of the pages' op APIs.
+attention = attn_fwd_dense
+decode_paged = attn_decode_paged

@@ -1,0 +1,189 @@
+// C ABI of the library (include/gqa_attn.h): argument checks, launch
+// planning, TMA tensor-map encoding and kernel launches.  No device memory is
+// allocated and no device data is read back on the attention paths.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "gqa_attn.h"
+#include "internal.h"
+
+namespace {
+
+using gqa::DecodeArgs;
+using gqa::DecodePlan;
+using gqa::PrefillArgs;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [B, S, H, D] bf16, D contiguous, as a 4-D tensor map {D, S, H, B} with a
+// {64, 128, 1, 1} box and 128-byte swizzle.  Rows past S read as zero.
+bool make_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)H * D * 2, (cuuint64_t)D * 2, (cuuint64_t)S * H * D * 2};
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static int cache[64] = {0};
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
+
+constexpr long kMaxSeq = 1L << 30;
+
+}  // namespace
+
+extern "C" {
+
+gqa_status attn_fwd_dense(const void* q, const void* k, const void* v, const uint8_t* key_padding_mask,
+                          void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                          float scale, gqa_stream_t stream) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Sq < 0 || Skv < 0) return GQA_ERR_INVALID_ARG;
+    if (Sq >= kMaxSeq || Skv >= kMaxSeq) return GQA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+    if (!head_dim_ok(D) || D == 256) return GQA_ERR_UNSUPPORTED;
+    if (Sq == 0) return GQA_OK;
+    if (!q || !o || (Skv > 0 && (!k || !v))) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o) || (Skv > 0 && (!aligned16(k) || !aligned16(v)))) return GQA_ERR_MISALIGNED;
+    if (lse && !aligned4(lse)) return GQA_ERR_MISALIGNED;
+    const long n_qtiles = ((long)Sq + 127) / 128;
+    if (n_qtiles * B * Hq >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    if (Skv == 0)
+        return gqa::launch_empty_rows(o, lse, (long)B * Sq * Hq, D, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+
+    CUtensorMap tq, tk, tv;
+    if (!make_bshd_map(&tq, q, B, Sq, Hq, D) || !make_bshd_map(&tk, k, B, Skv, Hkv, D) ||
+        !make_bshd_map(&tv, v, B, Skv, Hkv, D))
+        return GQA_ERR_CUDA;
+    PrefillArgs a;
+    a.mask = key_padding_mask;
+    a.o = o;
+    a.lse = lse;
+    a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = Sq; a.Skv = Skv; a.D = D;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    return gqa::launch_prefill(tq, tk, tv, a, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+size_t attn_decode_paged_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_pages) {
+    if (!head_dim_ok(D)) return 0;
+    DecodePlan p;
+    if (!gqa::plan_decode(B, Sq, Hq, Hkv, D, page_size, max_pages, sm_count(), &p)) return 0;
+    return p.workspace_bytes;
+}
+
+gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* real_seqlen_kv,
+                             const int32_t* block_table, int page_size, void* o, float* lse, int B, int Sq, int Hq,
+                             int Hkv, int D, int num_pages, int max_pages, int causal, float scale,
+                             void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
+    if (B <= 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || page_size <= 0 || num_pages < 0 || max_pages <= 0)
+        return GQA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+    if ((long)max_pages * page_size >= kMaxSeq) return GQA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+    if (!head_dim_ok(D)) return GQA_ERR_UNSUPPORTED;
+    if (Sq == 0) return GQA_OK;
+    if (!q || !k_cache || !v_cache || !real_seqlen_kv || !block_table || !o) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return GQA_ERR_MISALIGNED;
+    if (!aligned4(real_seqlen_kv) || !aligned4(block_table) || (lse && !aligned4(lse))) return GQA_ERR_MISALIGNED;
+    DecodePlan p;
+    if (!gqa::plan_decode(B, Sq, Hq, Hkv, D, page_size, max_pages, sm_count(), &p)) return GQA_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < p.workspace_bytes) return GQA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GQA_ERR_MISALIGNED;
+
+    DecodeArgs a;
+    a.q = q; a.k_cache = k_cache; a.v_cache = v_cache;
+    a.seqlens = real_seqlen_kv; a.table = block_table;
+    a.o = o; a.lse = lse;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + (p.part_o_bytes + 255) / 256 * 256);
+    a.B = B; a.Sq = Sq; a.Hq = Hq; a.Hkv = Hkv; a.D = D;
+    a.page_size = page_size; a.max_pages = max_pages; a.num_pages = num_pages; a.causal = causal ? 1 : 0;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    a.chunk = p.chunk;
+    a.max_splits = p.max_splits;
+    return gqa::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status attn_validate_paged(const int32_t* real_seqlen_kv, const int32_t* block_table, int B, int Sq,
+                               int page_size, int num_pages, int max_pages, int causal, gqa_stream_t stream) {
+    (void)causal;
+    if (B <= 0 || Sq < 0 || page_size <= 0 || num_pages < 0 || max_pages <= 0) return GQA_ERR_INVALID_ARG;
+    if (!real_seqlen_kv || !block_table) return GQA_ERR_INVALID_ARG;
+    std::vector<int32_t> lens(B), table((size_t)B * max_pages);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(lens.data(), real_seqlen_kv, sizeof(int32_t) * B, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(table.data(), block_table, sizeof(int32_t) * table.size(), cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    for (int b = 0; b < B; ++b) {
+        const long L = lens[b];
+        if (L < 0 || L > (long)max_pages * page_size) return GQA_ERR_INVALID_ARG;
+        const long need = (L + page_size - 1) / page_size;
+        for (long p = 0; p < need; ++p) {
+            const int32_t phys = table[(size_t)b * max_pages + p];
+            if (phys < 0 || phys >= num_pages) return GQA_ERR_INVALID_ARG;
+        }
+    }
+    return GQA_OK;
+}
+
+const char* gqa_status_string(gqa_status s) {
+    switch (s) {
+        case GQA_OK: return "ok";
+        case GQA_ERR_INVALID_ARG: return "invalid argument";
+        case GQA_ERR_UNSUPPORTED: return "unsupported combination";
+        case GQA_ERR_MISALIGNED: return "pointer not aligned";
+        case GQA_ERR_WORKSPACE: return "workspace missing or too small";
+        case GQA_ERR_CUDA: return "CUDA error";
+        case GQA_ERR_TIMEOUT: return "a kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+gqa_status gqa_device_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
+    const int e = gqa::prefill_take_device_error();
+    if (e < 0) return GQA_ERR_CUDA;
+    return e ? GQA_ERR_TIMEOUT : GQA_OK;
+}
+
+const char* gqa_version(void) { return "gqa_attn 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace gqa {
+
+struct PrefillArgs {
+    const uint8_t* mask;  // [B, Skv] or nullptr
+    void* o;              // [B, Sq, Hq, D] bf16
+    float* lse;           // [B, Sq, Hq] or nullptr
+    int B, Hq, Hkv, Sq, Skv, D;
+    int causal;
+    float scale_log2;     // scale * log2(e)
+};
+
+// Launches the tcgen05 prefill kernel.  The tensor maps describe q, k, v as
+// 4-D [B, S, H, D] bf16 tensors with a {64, 128, 1, 1} box and 128-byte swizzle.
+cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                           const CUtensorMap& tm_v, const PrefillArgs& a, cudaStream_t stream);
+// Rows with no key at all (Skv == 0): O = 0, LSE = -inf.
+cudaError_t launch_empty_rows(void* o, float* lse, long rows, int D, cudaStream_t stream);
+int prefill_take_device_error();
+
+struct DecodeArgs {
+    const void* q;          // [B, Sq, Hq, D]
+    const void* k_cache;    // [P, ps, Hkv, D]
+    const void* v_cache;
+    const int32_t* seqlens; // [B]
+    const int32_t* table;   // [B, max_pages]
+    void* o;                // [B, Sq, Hq, D]
+    float* lse;             // [B, Sq, Hq] or nullptr
+    float* part_o;          // [B, Hkv, max_splits, R, D]
+    float* part_lse;        // [B, Hkv, max_splits, R]  (log2 units)
+    int B, Sq, Hq, Hkv, D, page_size, max_pages, num_pages, causal;
+    float scale_log2;
+    int chunk;              // tokens per split (multiple of the key tile)
+    int max_splits;
+};
+
+struct DecodePlan {
+    int chunk;
+    int max_splits;
+    int rows;               // g * Sq rows per KV head
+    size_t part_o_bytes;
+    size_t part_lse_bytes;
+    size_t workspace_bytes;
+};
+
+bool plan_decode(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
+                 DecodePlan* plan);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace gqa

@@ -1,0 +1,149 @@
+/*
+ * gqa_attn.h — C ABI of the GB300 (sm_103a) grouped-query softmax attention
+ * forward library, libgqa_attn.so.
+ *
+ * Operation (TileOPs "Attention Operators", GQADenseFwdOp, stages 1-7, and
+ * RL-Kernel "Standard Softmax Attention", Accuracy):
+ *
+ *     O[b,i,h,:] = sum_{j in V(b,i)} softmax_j( scale * <q[b,i,h,:], k[b,j,r,:]> ) * v[b,j,r,:]
+ *
+ *   r = h / (Hq / Hkv)                     query head h reads KV head r
+ *   p_i = i + Skv - Sq                     queries aligned to the end of the keys
+ *   V(b,i) = { j < Skv : (!causal || j <= p_i) && key_padding_mask[b,j] != 0 }
+ *
+ * Accumulation is FP32; O is written as bfloat16 (round to nearest even).  A row
+ * whose V(b,i) is empty gets O = 0 exactly and LSE = -inf (TileOPs
+ * MHADecodePagedWithKVCacheFwdOp / GQAPagedFwdOp: "outputs zeros"; MATE "QSA",
+ * Core Attention: empty rows give -inf LSE).  LSE is the natural-log
+ * log-sum-exp of the scaled logits of the row, FP32 (MATE "QSA", Core
+ * Attention: natural-log LSE shaped like the query without its last axis).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *     row-major, contiguous, in BSHD order (batch, sequence, head, head_dim),
+ *     head_dim contiguous (TileOPs GQADenseFwdOp, forward).  bfloat16 data is
+ *     passed as raw 16-bit storage (void*).
+ *   - q, k, v, o must be 16-byte aligned; paged caches too.
+ *   - The caller owns every buffer (inputs, outputs, workspace).  The library
+ *     allocates no device memory on these paths and never reads device data
+ *     back to the host; work is enqueued on `stream` and returns immediately.
+ *   - Inputs are read only (RL-Kernel: "no in-place mutation").
+ *   - Argument checks run on the host before any launch; a failed check
+ *     launches nothing and returns the status.  A launch failure returns
+ *     GQA_ERR_CUDA.
+ *   - D (head_dim) must be 64, 128 or 256; Hq must be a multiple of Hkv
+ *     (RL-Kernel, Known Limitations: ValueError otherwise).
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime and driver stream handle types are the same). */
+typedef struct CUstream_st* gqa_stream_t;
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = 1,  /* a size or pointer argument is out of range */
+    GQA_ERR_UNSUPPORTED = 2,  /* a valid combination this build has no kernel for */
+    GQA_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+    GQA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
+    GQA_ERR_CUDA = 5,         /* a CUDA call or kernel launch failed */
+    GQA_ERR_TIMEOUT = 6       /* a kernel gave up waiting (see gqa_device_error) */
+} gqa_status;
+
+/*
+ * Dense prefill / chunked prefill (TileOPs GQADenseFwdOp; RL-Kernel
+ * "Prefill / Decode / KV-cache Shared Contract": one expression covers
+ * Sq == Skv, chunked prefill and Sq < Skv).
+ *
+ *   q    [B, Sq,  Hq,  D] bf16        k, v [B, Skv, Hkv, D] bf16
+ *   key_padding_mask  [B, Skv] bytes, nonzero = keep, or NULL for none
+ *                     (RL-Kernel Tensor Contract: False columns become -inf)
+ *   o    [B, Sq, Hq, D] bf16 (written)
+ *   lse  [B, Sq, Hq] float (written), or NULL to skip it
+ *   causal  nonzero applies the end-aligned causal mask
+ *   scale   the score multiplier; the library takes it as given (0.0 included);
+ *           callers wanting the default pass 1/sqrt(D)
+ *
+ * B, Hq, Hkv, D > 0; Sq >= 0, Skv >= 0.  Sq > Skv with causal is accepted:
+ * rows i < Sq - Skv see no key and get zeros.  Skv == 0 gives all-zero O.
+ * D == 256 is not yet served here (GQA_ERR_UNSUPPORTED).
+ */
+gqa_status attn_fwd_dense(const void* q, const void* k, const void* v,
+                          const uint8_t* key_padding_mask, void* o, float* lse,
+                          int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                          int causal, float scale, gqa_stream_t stream);
+
+/*
+ * Paged decode (TileOPs MHADecodePagedWithKVCacheFwdOp and GQAPagedFwdOp;
+ * split-KV with an LSE merge as in MATE "QSA", Core Attention).
+ *
+ *   q        [B, Sq, Hq, D] bf16  (Sq new query tokens per request)
+ *   k_cache, v_cache  [num_pages, page_size, Hkv, D] bf16
+ *   real_seqlen_kv    [B] int32: request b's cache length L_b, its Sq query
+ *                     tokens included; 0 <= L_b <= max_pages * page_size
+ *   block_table       [B, max_pages] int32: logical page p of request b lives
+ *                     in physical page block_table[b, p]; token t is slot
+ *                     t % page_size of page block_table[b, t / page_size]
+ *   o        [B, Sq, Hq, D] bf16 (written); lse [B, Sq, Hq] float or NULL
+ *   causal   nonzero: query i sees keys t <= i + L_b - Sq
+ *   workspace / workspace_bytes: device scratch of at least
+ *            attn_decode_paged_workspace_size(...) bytes, 256-byte aligned;
+ *            its contents on entry do not matter; calls that share one
+ *            workspace must not overlap on the GPU.
+ *
+ * Caller obligations (not checked on the device; see attn_validate_paged):
+ * the entries block_table[b, 0 .. ceil(L_b / page_size) - 1] lie in
+ * [0, num_pages); later entries are never read (-1 is fine there).
+ */
+gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* real_seqlen_kv, const int32_t* block_table,
+                             int page_size, void* o, float* lse,
+                             int B, int Sq, int Hq, int Hkv, int D,
+                             int num_pages, int max_pages, int causal, float scale,
+                             void* workspace, size_t workspace_bytes,
+                             gqa_stream_t stream);
+
+/*
+ * Bytes of workspace attn_decode_paged needs for these sizes on the current
+ * device (0 for invalid sizes).  A pure function of its arguments and the
+ * device's SM count.
+ */
+size_t attn_decode_paged_workspace_size(int B, int Sq, int Hq, int Hkv, int D,
+                                        int page_size, int max_pages);
+
+/*
+ * Optional host-side check of the paged metadata (the TileOPs
+ * validate_inputs=True analogue).  Copies real_seqlen_kv and block_table to
+ * the host (synchronising `stream`) and checks every length and every needed
+ * table entry.  Returns GQA_OK or GQA_ERR_INVALID_ARG.  Not for the hot path.
+ */
+gqa_status attn_validate_paged(const int32_t* real_seqlen_kv, const int32_t* block_table,
+                               int B, int Sq, int page_size, int num_pages, int max_pages,
+                               int causal, gqa_stream_t stream);
+
+/* Static description of a status code. */
+const char* gqa_status_string(gqa_status status);
+
+/*
+ * Every wait inside the kernels is bounded; a wait that runs out records a
+ * code in a device-side word and the kernel returns early.  This call
+ * synchronises the device, returns GQA_ERR_TIMEOUT if the word is set
+ * (clearing it) and GQA_OK otherwise.  Diagnostic, not for the hot path.
+ */
+gqa_status gqa_device_error(void);
+
+/* Library version string. */
+const char* gqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

@@ -1,0 +1,104 @@
+"""The C-ABI library on the CPU side: it builds, loads, exports every symbol
+include/gqa_attn.h declares, and its host-side argument checks return the
+documented status before anything reaches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gqa_softmax_attention_gb300 import _lib, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gqa_attn.h")
+OK, INVALID, UNSUPPORTED, MISALIGNED, WORKSPACE = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s+\**\s*([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd_dense", "attn_decode_paged", "attn_decode_paged_workspace_size", "attn_validate_paged",
+              "gqa_status_string", "gqa_device_error", "gqa_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.gqa_status_string(code)
+    assert b"sm_103a" in lib.gqa_version()
+
+
+A16 = ctypes.c_void_p(1 << 20)         # 16-byte aligned stand-in pointers; never dereferenced
+A16b = ctypes.c_void_p(2 << 20)
+MIS = ctypes.c_void_p((1 << 20) + 2)   # misaligned
+
+
+def dense(lib, q=A16, k=A16, v=A16, o=A16b, B=1, Hq=4, Hkv=2, Sq=8, Skv=8, D=64, scale=0.125, lse=None):
+    return lib.attn_fwd_dense(q, k, v, None, o, lse, B, Hq, Hkv, Sq, Skv, D, 1, scale, None)
+
+
+def test_dense_argument_checks(lib):
+    assert dense(lib, B=0) == INVALID
+    assert dense(lib, Hq=6, Hkv=4) == INVALID                   # Hq % Hkv != 0
+    assert dense(lib, Sq=-1) == INVALID
+    assert dense(lib, Skv=-3) == INVALID
+    assert dense(lib, D=96) == UNSUPPORTED
+    assert dense(lib, D=256) == UNSUPPORTED                      # dense D=256 not served yet
+    assert dense(lib, scale=float("nan")) == INVALID
+    assert dense(lib, scale=float("inf")) == INVALID
+    assert dense(lib, q=MIS) == MISALIGNED
+    assert dense(lib, o=MIS) == MISALIGNED
+    assert dense(lib, lse=ctypes.c_void_p((1 << 20) + 1)) == MISALIGNED
+    assert dense(lib, q=None) == INVALID
+    assert dense(lib, Sq=0) == OK                                # nothing to do, nothing launched
+
+
+def paged(lib, ws=None, ws_bytes=0, q=A16, B=2, Sq=1, Hq=8, Hkv=2, D=128, ps=16, num_pages=10, max_pages=4,
+          seq=A16, table=A16):
+    return lib.attn_decode_paged(q, A16, A16, seq, table, ps, A16b, None, B, Sq, Hq, Hkv, D, num_pages, max_pages,
+                                 1, 0.1, ws, ws_bytes, None)
+
+
+def test_paged_argument_checks(lib):
+    assert paged(lib, B=0) == INVALID
+    assert paged(lib, Hq=6, Hkv=4) == INVALID
+    assert paged(lib, ps=0) == INVALID
+    assert paged(lib, max_pages=0) == INVALID
+    assert paged(lib, D=80) == UNSUPPORTED
+    assert paged(lib, q=MIS) == MISALIGNED
+    assert paged(lib, seq=ctypes.c_void_p((1 << 20) + 2)) == MISALIGNED
+    assert paged(lib, ws=None, ws_bytes=0) == WORKSPACE          # workspace is required
+    assert paged(lib, ws=A16, ws_bytes=16) == WORKSPACE          # and must be large enough
+    assert paged(lib, Sq=0) == OK
+
+
+def test_workspace_size_is_positive_and_monotone(lib):
+    small = lib.attn_decode_paged_workspace_size(4, 1, 32, 8, 128, 64, 16)
+    big = lib.attn_decode_paged_workspace_size(64, 1, 32, 8, 128, 64, 256)
+    assert 0 < small < big
+    assert lib.attn_decode_paged_workspace_size(4, 1, 30, 8, 128, 64, 16) == 0   # Hq % Hkv
+    assert lib.attn_decode_paged_workspace_size(4, 1, 32, 8, 96, 64, 16) == 0    # D
+
+
+def test_python_layer_rejects_cpu_tensors():
+    import torch
+    import gqa_softmax_attention_gb300 as g
+    q = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        g.attention(q, q, q)
