@@ -7,6 +7,7 @@ marshals arguments.  The shared library is loaded on first use and its absence
 is an error: there is no CPU fallback.
 """
 
-from .api import (attention, attn_decode_paged, attn_decode_paged_workspace_size,  # noqa: F401
+from .api import (attention, attn_decode_paged, attn_decode_paged_noalloc,  # noqa: F401
+                  attn_decode_paged_workspace_size,
                   attn_fwd_dense, attn_validate_paged, decode_paged, gqa_device_error,
                   resolve_scale)

@@ -43,6 +43,10 @@ def load() -> ctypes.CDLL:
     lib.attn_decode_paged.restype = i
     lib.attn_decode_paged_workspace_size.argtypes = [i] * 7
     lib.attn_decode_paged_workspace_size.restype = sz
+    lib.attn_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, i, vp, vp] + [i] * 8 + [f, vp]
+    lib.attn_decode_paged_noalloc.restype = i
+    lib.attn_decode_paged_noalloc_max_workspace.argtypes = []
+    lib.attn_decode_paged_noalloc_max_workspace.restype = sz
     lib.attn_validate_paged.argtypes = [vp, vp] + [i] * 6 + [vp]
     lib.attn_validate_paged.restype = i
     lib.gqa_status_string.argtypes = [i]

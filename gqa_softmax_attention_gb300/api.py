@@ -126,6 +126,35 @@ def attn_decode_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=T
     return out, lse
 
 
+def attn_decode_paged_noalloc(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=True, scale=None, out=None,
+                              lse=None):
+    """Paged decode through the entry point that allocates nothing in the library.
+
+    For callers that cannot allocate device memory or supply a workspace: the
+    split partials go to a fixed 32 MiB array inside the library, shared by all
+    calls (calls overlapping on the GPU race).  Sizes whose partials do not fit
+    raise ValueError.  Outputs are allocated here only when not passed in.
+    """
+    _check_bf16_cuda("q", q, 4)
+    _check_bf16_cuda("k_cache", k_cache, 4)
+    _check_bf16_cuda("v_cache", v_cache, 4)
+    B, Sq, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    max_pages = block_table.shape[1]
+    if out is None:
+        out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device)
+    st = _lib.load().attn_decode_paged_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(real_seqlen_kv),
+                                               _ptr(block_table), page_size, _ptr(out), _ptr(lse), B, Sq, Hq, Hkv,
+                                               D, num_pages, max_pages, int(bool(causal)),
+                                               resolve_scale(scale, D), _stream(q.device))
+    if st != 0:
+        _raise(st, "attn_decode_paged_noalloc (static scratch %d bytes)"
+               % _lib.load().attn_decode_paged_noalloc_max_workspace())
+    return out, lse
+
+
 def attn_validate_paged(real_seqlen_kv, block_table, Sq, page_size, num_pages, causal=True):
     """Host-side range check of paged metadata (synchronises the stream)."""
     B, max_pages = block_table.shape

@@ -26,7 +26,9 @@
 // This path is bound by HBM bandwidth; the MMAs are small and hidden under the
 // gathers, so warp-level mma.sync is used rather than tcgen05.
 #include <cmath>
+#include <mutex>
 
+#include "gqa_attn.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -458,3 +460,59 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace gqa
+
+// ---------------------------------------------------------------------------
+// Paged decode for callers that cannot allocate device memory.
+//
+// Some callers have no way to hand this library a workspace: a serving
+// engine whose device memory is entirely pre-reserved by its own pool, a
+// plugin loaded into a host framework that forbids allocation while it
+// executes, or a latency-critical loop that cannot pay for cudaMalloc's
+// implicit synchronisation.  For them attn_decode_paged_noalloc keeps the
+// split-KV partials in the fixed array below instead of a caller workspace.
+//
+// The array lives in this library's device image: every GPU that loads the
+// library holds kStaticScratchBytes of it until the process exits.  Its
+// device address is looked up once per device (the first call on a device,
+// with that device current) and cached.  Every call shares the array and it
+// keeps whatever the last call wrote; nothing in it needs to start at zero,
+// because each call writes every partial it later reads.  Two calls whose
+// kernels overlap on the GPU (for example on two streams) race on it.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // 32 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_static_scratch on the current device, or nullptr.
+void* static_scratch_address() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (!g_static_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+        g_static_scratch_ptr[dev] = p;
+    }
+    return g_static_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" size_t attn_decode_paged_noalloc_max_workspace(void) { return kStaticScratchBytes; }
+
+extern "C" gqa_status attn_decode_paged_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                                const int32_t* real_seqlen_kv, const int32_t* block_table,
+                                                int page_size, void* o, float* lse, int B, int Sq, int Hq, int Hkv,
+                                                int D, int num_pages, int max_pages, int causal, float scale,
+                                                gqa_stream_t stream) {
+    void* scratch = static_scratch_address();
+    if (!scratch) return GQA_ERR_CUDA;
+    // Sizes whose partials exceed the array are refused with GQA_ERR_WORKSPACE
+    // by the same check attn_decode_paged applies to a caller workspace.
+    return attn_decode_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, page_size, o, lse, B, Sq, Hq, Hkv,
+                             D, num_pages, max_pages, causal, scale, scratch, kStaticScratchBytes, stream);
+}

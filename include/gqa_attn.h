@@ -119,6 +119,36 @@ size_t attn_decode_paged_workspace_size(int B, int Sq, int Hq, int Hkv, int D,
                                         int page_size, int max_pages);
 
 /*
+ * Paged decode that allocates nothing and takes no workspace.  The pages this
+ * library follows have no counterpart of it; it exists for callers that
+ * cannot allocate device memory or hand over a workspace (a serving engine
+ * whose memory is all pre-reserved by its own pool, a plugin inside a host
+ * framework that forbids allocation while it runs, a latency-critical loop
+ * that cannot pay for cudaMalloc's implicit synchronisation).
+ *
+ * Same arguments, semantics and checks as attn_decode_paged, without
+ * `workspace` / `workspace_bytes`: the split-KV partials live in a fixed
+ * device array inside the library of attn_decode_paged_noalloc_max_workspace()
+ * bytes (32 MiB), which every GPU that loads the library holds until the
+ * process exits.  Sizes needing more than that (see
+ * attn_decode_paged_workspace_size) return GQA_ERR_WORKSPACE and launch
+ * nothing.  The first call on a device looks up the array's device address
+ * with that device current; make that first call before any stream capture.
+ * All calls share the array: calls whose kernels overlap on the GPU (for
+ * example on two streams) race; nothing in it needs clearing between calls.
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+gqa_status attn_decode_paged_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* real_seqlen_kv, const int32_t* block_table,
+                                     int page_size, void* o, float* lse,
+                                     int B, int Sq, int Hq, int Hkv, int D,
+                                     int num_pages, int max_pages, int causal, float scale,
+                                     gqa_stream_t stream);
+
+/* Bytes of the fixed device array attn_decode_paged_noalloc uses. */
+size_t attn_decode_paged_noalloc_max_workspace(void);
+
+/*
  * Optional host-side check of the paged metadata (the TileOPs
  * validate_inputs=True analogue).  Copies real_seqlen_kv and block_table to
  * the host (synchronising `stream`) and checks every length and every needed
