@@ -46,6 +46,21 @@ bool make_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D
     return r == CUDA_SUCCESS;
 }
 
+// Paged cache [pages * page_size, Hkv, D] bf16 as a 3-D map {D, Hkv, rows}
+// with a {64, 1, box_tokens} box and 128-byte swizzle.
+bool make_cache_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D, int box_tokens) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_tokens};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -115,6 +130,7 @@ gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_c
         return GQA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
     if ((long)max_pages * page_size >= kMaxSeq) return GQA_ERR_INVALID_ARG;
+    if ((long)num_pages * page_size >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
     if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
     if (!head_dim_ok(D)) return GQA_ERR_UNSUPPORTED;
     if (Sq == 0) return GQA_OK;
@@ -137,7 +153,17 @@ gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_c
     a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     a.chunk = p.chunk;
     a.max_splits = p.max_splits;
-    return gqa::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    // Pages that cut into 8-row multiples of the key tile are loaded by TMA;
+    // other page sizes are gathered row by row.
+    const int box = gqa::decode_box_tokens(D, page_size);
+    CUtensorMap tk, tv;
+    const bool use_tma = box > 0 && num_pages > 0 &&
+                         make_cache_map(&tk, k_cache, (long)num_pages * page_size, Hkv, D, box) &&
+                         make_cache_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, box);
+    return gqa::launch_decode(a, use_tma ? &tk : nullptr, use_tma ? &tv : nullptr, box,
+                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GQA_OK
+               : GQA_ERR_CUDA;
 }
 
 gqa_status attn_validate_paged(const int32_t* real_seqlen_kv, const int32_t* block_table, int B, int Sq,
@@ -180,8 +206,9 @@ const char* gqa_status_string(gqa_status s) {
 gqa_status gqa_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
     const int e = gqa::prefill_take_device_error();
-    if (e < 0) return GQA_ERR_CUDA;
-    return e ? GQA_ERR_TIMEOUT : GQA_OK;
+    const int d = gqa::decode_take_device_error();
+    if (e < 0 || d < 0) return GQA_ERR_CUDA;
+    return (e || d) ? GQA_ERR_TIMEOUT : GQA_OK;
 }
 
 const char* gqa_version(void) { return "gqa_attn 0.1 sm_103a"; }

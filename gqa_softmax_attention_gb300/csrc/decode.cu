@@ -10,21 +10,29 @@
 // log-sum-exps without recomputing QK or PV (MATE "QSA", Core Attention,
 // SplitKV).
 //
-// decode_split_kernel: one CTA per (split, KV head, request, row block).  All
-//   g * Sq query rows that read this KV head are packed into the M dimension
-//   of m16n8k16 tensor-core MMAs (rows padded to 16 * MF).  Key/value rows of
-//   64 tokens are gathered page by page with 16-byte cp.async copies (each
-//   token row is D * 2 contiguous bytes) into a multi-stage shared-memory ring;
-//   slots past the request's length are zero-filled, never read.  Warps split
-//   the keys of a tile for S = Q K^T (each warp keeps its rows of Q in
-//   registers), rows are softmaxed by thread groups in shared memory, and the
-//   warps split the head dimension for O += P V.  Each split writes its
-//   normalised FP32 partial O and its base-2 LSE to the workspace.
+// One CTA per (split, KV head, request, row block).  All g * Sq query rows
+// that read this KV head are packed into the M dimension of m16n8k16
+// tensor-core MMAs (rows padded to 16 * MF).  Keys are processed in tiles of
+// TK tokens held in a multi-stage shared-memory ring laid out as 64-column
+// sub-tiles with 128-byte rows (16-byte chunks XOR-swizzled by row % 8):
+//   decode_tma_kernel     one producer warp fills the ring with TMA: each page
+//                         of a KV head is a strided 3-D box {64 cols, 1 head,
+//                         page tokens}; consumer warps only wait on mbarriers.
+//                         Used when pages cut into 8-row multiples of the tile.
+//   decode_gather_kernel  every thread gathers token rows with 16-byte
+//                         cp.async copies (any page size).
+// In both, consumer warps split the keys of a tile for S = Q K^T (each warp
+// keeps its rows of Q in registers), rows are softmaxed by thread groups in
+// shared memory (running max and sum, base 2), and the warps split the head
+// dimension for O += P V.  Slots past the request's length never contribute:
+// their scores are -inf and their value rows are zero in shared memory (never
+// 0 * garbage).  Each split writes its normalised FP32 partial O and its base-2
+// LSE to the workspace.
 // decode_combine_kernel: one warp per output row; weights exp(lse_s - max),
 //   normalised; a row no split saw gets O = 0 and LSE = -inf.
 //
-// This path is bound by HBM bandwidth; the MMAs are small and hidden under the
-// gathers, so warp-level mma.sync is used rather than tcgen05.
+// The path is bound by HBM bandwidth; the MMAs are small and hidden under the
+// loads, so warp-level mma.sync is used rather than tcgen05.
 #include <cmath>
 #include <mutex>
 
@@ -35,165 +43,150 @@
 namespace gqa {
 namespace {
 
-constexpr int TK = 64;   // tokens per key tile
+__device__ int g_decode_error;
+
 constexpr float kLn2 = 0.693147180559945309f;
 
-template <int D, int MF>
+constexpr int key_tile(int D) { return D == 256 ? 32 : 64; }
+
+template <int D, int MF, bool TMA>
 struct DCfg {
-    static constexpr int KSPLIT = MF == 1 ? 4 : 2;           // warps per 16-row fragment
-    static constexpr int NWARPS = MF * KSPLIT;
-    static constexpr int NT = NWARPS * 32;
+    static constexpr int TK = key_tile(D);                   // tokens per key tile
+    static constexpr int KSPLIT = (MF == 1 && TK == 64) ? 4 : 2;   // consumer warps per 16-row fragment
+    static constexpr int NC = MF * KSPLIT;                   // consumer warps
+    static constexpr int NCT = NC * 32;                      // consumer threads
+    static constexpr int NT = NCT + (TMA ? 32 : 0);          // + producer warp
     static constexpr int ROWS = 16 * MF;                     // padded rows per CTA
-    static constexpr int ROW_BYTES = D * 2;                  // one token's K (or V) row
-    static constexpr int CHUNKS = D / 8;                     // 16-byte chunks per row
-    static constexpr int NS = D == 64 ? 4 : (D == 128 ? 3 : 2);
-    static constexpr int KV_TILE = TK * ROW_BYTES;
+    static constexpr int NSUB = D / 64;                      // 64-column sub-tiles
+    static constexpr int SUB_BYTES = TK * 128;               // one sub-tile of a K (or V) tile
+    static constexpr int KV_TILE = NSUB * SUB_BYTES;
     static constexpr int KEYS_PER_WARP = TK / KSPLIT;
     static constexpr int NFK = KEYS_PER_WARP / 8;            // n8 fragments per warp in S = Q K^T
     static constexpr int DSL = D / KSPLIT;                   // head-dim slice per warp in O += P V
     static constexpr int NFD = DSL / 8;
     static constexpr int KSTEPS = D / 16;
-    static constexpr int S_STRIDE = TK + 4;                  // floats per score row in smem
-    static constexpr int TPR = NT / ROWS;                    // threads per row in the softmax
+    static constexpr int S_STRIDE = TK + 4;                  // floats per score row
+    static constexpr int TPR = NCT / ROWS;                   // threads per row in the softmax
     static constexpr int KPT = TK / TPR;                     // keys per thread in the softmax
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + ROWS * ROW_BYTES;
-    static constexpr int OFF_V = OFF_K + NS * KV_TILE;
-    static constexpr int OFF_S = OFF_V + NS * KV_TILE;
+    static constexpr int Q_BYTES = ROWS * D * 2;
+    static constexpr int FIXED = Q_BYTES + ROWS * S_STRIDE * 4 + ROWS * 128 + 3 * ROWS * 4 + 1024 + 256;
+    // as many stages as fit next to the fixed part, capped
+    static constexpr int NS_FIT = (227 * 1024 - FIXED) / (2 * KV_TILE);
+    static constexpr int NS_CAP = D == 256 ? 4 : (D == 128 ? 3 : 6);
+    static constexpr int NS = NS_FIT < NS_CAP ? NS_FIT : NS_CAP;
+    static constexpr int OFF_KV = 0;                          // 1024-aligned stage ring first
+    static constexpr int OFF_Q = OFF_KV + NS * 2 * KV_TILE;
+    static constexpr int OFF_S = OFF_Q + Q_BYTES;
     static constexpr int OFF_P = OFF_S + ROWS * S_STRIDE * 4;
-    static constexpr int OFF_A = OFF_P + ROWS * TK * 2;
+    static constexpr int OFF_A = OFF_P + ROWS * 128;
     static constexpr int OFF_L = OFF_A + ROWS * 4;
     static constexpr int OFF_M = OFF_L + ROWS * 4;
-    static constexpr int SMEM = OFF_M + ROWS * 4;
+    static constexpr int OFF_BAR = OFF_M + ROWS * 4;         // full[NS], empty[NS]
+    static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
+    static constexpr int SMEM = OFF_FLAG + 16 + 1024;        // + alignment slack
+    static_assert(NS >= 2, "pipeline depth");
     static_assert(NFK % 2 == 0 && NFD % 2 == 0, "fragments are loaded in pairs");
-    static_assert(KPT % 8 == 0, "softmax writes whole 16-byte chunks of P");
+    static_assert(KPT % 8 == 0 && TK * 2 <= 128, "softmax writes whole 16-byte chunks of a 128-byte P row");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, int MF>
-__global__ void __launch_bounds__(DCfg<D, MF>::NT)
-decode_split_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
-    using C = DCfg<D, MF>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    const uint32_t sb = smem_u32(smem);
-    const int split = blockIdx.x;
-    const int hkv = blockIdx.y;
-    const int b = blockIdx.z / n_rowblk;
-    const int rb = blockIdx.z % n_rowblk;
+// Byte offset of 16-byte chunk c of row r in a [D/64][rows][128 B] tile.
+__device__ __forceinline__ uint32_t sw_off(int r, int c, int sub_bytes) {
+    return (uint32_t)((c >> 3) * sub_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+struct Work {
+    int split, hkv, b, rb, L, t_begin, t_end, n_tiles, row0, rows_here;
+};
+
+template <class C>
+__device__ __forceinline__ bool work_of(const DecodeArgs& a, int R, int n_rowblk, Work& w) {
+    w.split = blockIdx.x;
+    w.hkv = blockIdx.y;
+    w.b = blockIdx.z / n_rowblk;
+    w.rb = blockIdx.z % n_rowblk;
     // Lengths are clamped to the table's capacity so a bad length cannot send
-    // the gather past block_table.
-    const int L = min(max(a.seqlens[b], 0), a.max_pages * a.page_size);
-    const int t_begin = split * a.chunk;
-    if (t_begin >= L) return;                      // nothing here; the combine skips it
-    const int t_end = min(L, t_begin + a.chunk);
-    const int n_tiles = (t_end - t_begin + TK - 1) / TK;
-    const int row0 = rb * C::ROWS;
-    const int rows_here = min(C::ROWS, R - row0);
+    // a load past block_table.
+    w.L = min(max(a.seqlens[w.b], 0), a.max_pages * a.page_size);
+    w.t_begin = w.split * a.chunk;
+    if (w.t_begin >= w.L) return false;            // nothing here; the combine skips it
+    w.t_end = min(w.L, w.t_begin + a.chunk);
+    w.n_tiles = (w.t_end - w.t_begin + C::TK - 1) / C::TK;
+    w.row0 = w.rb * C::ROWS;
+    w.rows_here = min(C::ROWS, R - w.row0);
+    return true;
+}
 
-    const int tid = threadIdx.x;
-    const int warp = tid / 32;
-    const int lane = tid % 32;
-    const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
-    const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
-    const int32_t* trow = a.table + (size_t)b * a.max_pages;
+// Consumer-side state and the per-tile steps shared by both kernels.
+template <class C>
+struct Consumer {
+    static constexpr int CHUNKS = C::NSUB * 8;   // 16-byte chunks per row of D
+    uint32_t sb;            // shared-memory base (1024-aligned)
+    uint8_t* smem;
+    int ctid, warp, lane, mf, wk, srow, ssub;
+    int lim[2];             // exclusive visibility limit of the two fragment rows this lane holds
+    uint32_t qf[C::KSTEPS][4];
+    float m_run, l_run;
+    float acc[C::NFD][4];
 
-    // Q rows r = i * g + hl (query i, head hkv * g + hl); padded rows are zero.
-    for (int idx = tid; idx < C::ROWS * C::CHUNKS; idx += C::NT) {
-        const int rr = idx / C::CHUNKS, c = idx % C::CHUNKS;
-        const uint32_t dst = sb + C::OFF_Q + rr * C::ROW_BYTES + ((c ^ (rr & 7)) << 4);
-        if (rr < rows_here) {
-            const int r = row0 + rr;
-            const int i = r / g, hl = r % g;
-            cp_async16(dst, qg + (((size_t)b * a.Sq + i) * a.Hq + hkv * g + hl) * D + c * 8, 16);
-        } else {
-            cp_async16(dst, qg, 0);
-        }
-    }
-    cp_async_commit();
-
-    auto load_tile = [&](int tile, int stage) {
-        const int t0 = t_begin + tile * TK;
-        for (int idx = tid; idx < TK * C::CHUNKS; idx += C::NT) {
-            const int tok = idx / C::CHUNKS, c = idx % C::CHUNKS;
-            const int t = t0 + tok;
-            const uint32_t off = tok * C::ROW_BYTES + ((c ^ (tok & 7)) << 4);
-            const uint32_t dk = sb + C::OFF_K + stage * C::KV_TILE + off;
-            const uint32_t dv = sb + C::OFF_V + stage * C::KV_TILE + off;
-            const int page = t < t_end ? trow[t / a.page_size] : -1;
-            // A page id outside the pool (a caller error) is read as zeros, never dereferenced.
-            if (page >= 0 && page < a.num_pages) {
-                const size_t e = (((size_t)page * a.page_size + t % a.page_size) * a.Hkv + hkv) * D + c * 8;
-                cp_async16(dk, kc + e, 16);
-                cp_async16(dv, vc + e, 16);
+    __device__ void init(uint8_t* s, uint32_t base, const DecodeArgs& a, const Work& w, int g) {
+        smem = s;
+        sb = base;
+        ctid = threadIdx.x;
+        warp = ctid / 32;
+        lane = ctid % 32;
+        mf = warp / C::KSPLIT;
+        wk = warp % C::KSPLIT;
+        srow = ctid / C::TPR;
+        ssub = ctid % C::TPR;
+        m_run = -INFINITY;
+        l_run = 0.f;
+#pragma unroll
+        for (int n = 0; n < C::NFD; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int rl = mf * 16 + (lane >> 2) + 8 * h;
+            const int r = w.row0 + rl;
+            if (rl >= w.rows_here) {
+                lim[h] = -1;
+            } else if (a.causal) {
+                const long p = (long)(r / g) + w.L - a.Sq;          // key position of query r / g
+                lim[h] = (int)min((long)w.t_end, p + 1);
             } else {
-                cp_async16(dk, kc, 0);   // zero-fill: 0 * P stays 0 in O += P V
-                cp_async16(dv, vc, 0);
+                lim[h] = w.t_end;
             }
         }
-    };
+    }
 
-#pragma unroll
-    for (int s = 0; s < C::NS - 1; ++s) {
-        if (s < n_tiles) load_tile(s, s);
+    // Q rows r = i * g + hl (query i, head hkv * g + hl) -> shared memory with
+    // cp.async (padded rows zero), then into registers.  `bar` syncs consumers.
+    template <class Bar>
+    __device__ void load_q(const DecodeArgs& a, const Work& w, int g, Bar bar) {
+        const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(a.q);
+        for (int idx = ctid; idx < C::ROWS * CHUNKS; idx += C::NCT) {
+            const int rr = idx / CHUNKS, c = idx % CHUNKS;
+            const uint32_t dst = sb + C::OFF_Q + sw_off(rr, c, C::ROWS * 128);
+            if (rr < w.rows_here) {
+                const int r = w.row0 + rr;
+                const int i = r / g, hl = r % g;
+                cp_async16(dst, qg + (((size_t)w.b * a.Sq + i) * a.Hq + w.hkv * g + hl) * (CHUNKS * 8) + c * 8, 16);
+            } else {
+                cp_async16(dst, qg, 0);
+            }
+        }
         cp_async_commit();
-    }
-    cp_async_wait<C::NS - 1>();                    // the Q group has landed
-    __syncthreads();
-
-    const int mf = warp / C::KSPLIT;               // this warp's 16-row fragment
-    const int wk = warp % C::KSPLIT;               // key part (S) / head-dim part (PV)
-    uint32_t qf[C::KSTEPS][4];
+        cp_async_wait<0>();
+        bar();
 #pragma unroll
-    for (int kk = 0; kk < C::KSTEPS; ++kk) {
-        const int row = mf * 16 + (lane & 15);
-        const int chunk = kk * 2 + (lane >> 4);
-        ldsm_x4(sb + C::OFF_Q + row * C::ROW_BYTES + ((chunk ^ (row & 7)) << 4), qf[kk][0], qf[kk][1],
-                qf[kk][2], qf[kk][3]);
-    }
-
-    // Visibility limit (exclusive) of the two rows this lane holds in S fragments.
-    int lim[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int rl = mf * 16 + (lane >> 2) + 8 * h;
-        const int r = row0 + rl;
-        if (rl >= rows_here) {
-            lim[h] = -1;
-        } else if (a.causal) {
-            const long p = (long)(r / g) + L - a.Sq;       // key position of query r / g
-            lim[h] = (int)min((long)t_end, p + 1);
-        } else {
-            lim[h] = t_end;
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            const int row = mf * 16 + (lane & 15);
+            const int chunk = kk * 2 + (lane >> 4);
+            ldsm_x4(sb + C::OFF_Q + sw_off(row, chunk, C::ROWS * 128), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
         }
     }
 
-    // Softmax row ownership: TPR consecutive threads share a row.
-    const int srow = tid / C::TPR;
-    const int ssub = tid % C::TPR;
-    float m_run = -INFINITY, l_run = 0.f;
-    float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
-    float* sAlpha = reinterpret_cast<float*>(smem + C::OFF_A);
-    const float sl = a.scale_log2;
-
-    float acc[C::NFD][4];
-#pragma unroll
-    for (int n = 0; n < C::NFD; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-
-    for (int it = 0; it < n_tiles; ++it) {
-        cp_async_wait<C::NS - 2>();
-        __syncthreads();
-        {
-            const int nt = it + C::NS - 1;
-            if (nt < n_tiles) load_tile(nt, nt % C::NS);
-            cp_async_commit();
-        }
-        const int stage = it % C::NS;
-        const int t0 = t_begin + it * TK;
-        const uint32_t sK = sb + C::OFF_K + stage * C::KV_TILE;
-        const uint32_t sV = sb + C::OFF_V + stage * C::KV_TILE;
-
-        // ---- S = Q K^T for this warp's rows and keys
+    // S = Q K^T for this warp's rows and keys, scaled and masked, into smem.
+    __device__ void qk(uint32_t sK, int t0, float sl) {
         float sacc[C::NFK][4];
 #pragma unroll
         for (int n = 0; n < C::NFK; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
@@ -204,11 +197,12 @@ decode_split_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
                 const int key = wk * C::KEYS_PER_WARP + np * 16 + (lane & 7) + ((lane >> 4) << 3);
                 const int chunk = kk * 2 + ((lane >> 3) & 1);
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(sK + key * C::ROW_BYTES + ((chunk ^ (key & 7)) << 4), b0, b1, b2, b3);
+                ldsm_x4(sK + sw_off(key, chunk, C::SUB_BYTES), b0, b1, b2, b3);
                 mma_16816(sacc[2 * np], qf[kk], b0, b1);
                 mma_16816(sacc[2 * np + 1], qf[kk], b2, b3);
             }
         }
+        float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
 #pragma unroll
         for (int n = 0; n < C::NFK; ++n) {
 #pragma unroll
@@ -217,111 +211,295 @@ decode_split_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
                 const int kl = wk * C::KEYS_PER_WARP + n * 8 + 2 * (lane & 3);
                 const int t = t0 + kl;
                 float2 v;
-                v.x = t < lim[h] ? sacc[n][2 * h] * sl : -INFINITY;
+                v.x = t < lim[h] ? sacc[n][2 * h] * sl : -INFINITY;        // the select drops stale rows
                 v.y = t + 1 < lim[h] ? sacc[n][2 * h + 1] * sl : -INFINITY;
                 *reinterpret_cast<float2*>(sS + rl * C::S_STRIDE + kl) = v;
             }
         }
-        __syncthreads();
+    }
 
-        // ---- online softmax, TPR threads per row
-        {
-            float x[C::KPT];
-            const float* src = sS + srow * C::S_STRIDE + ssub * C::KPT;
+    // Online softmax over the tile, TPR threads per row; P (bf16) and the
+    // rescale factor alpha go to smem.
+    __device__ void softmax() {
+        const float* sS = reinterpret_cast<const float*>(smem + C::OFF_S);
+        float* sAlpha = reinterpret_cast<float*>(smem + C::OFF_A);
+        float x[C::KPT];
+        const float* src = sS + srow * C::S_STRIDE + ssub * C::KPT;
 #pragma unroll
-            for (int e = 0; e < C::KPT; e += 4) {
-                const float4 f = *reinterpret_cast<const float4*>(src + e);
-                x[e] = f.x; x[e + 1] = f.y; x[e + 2] = f.z; x[e + 3] = f.w;
-            }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < C::KPT; ++e) mx = fmaxf(mx, x[e]);
-#pragma unroll
-            for (int o = C::TPR / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float m_new = fmaxf(m_run, mx);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = fast_exp2(m_run - m_use);
-            float sum = 0.f;
-            uint32_t pk[C::KPT / 2];
-#pragma unroll
-            for (int e = 0; e < C::KPT / 2; ++e) {
-                const float p0 = fast_exp2(x[2 * e] - m_use);
-                const float p1 = fast_exp2(x[2 * e + 1] - m_use);
-                sum += p0 + p1;
-                pk[e] = pack_bf16x2(p0, p1);
-            }
-#pragma unroll
-            for (int o = C::TPR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            l_run = l_run * alpha + sum;
-            m_run = m_new;
-#pragma unroll
-            for (int q = 0; q < C::KPT / 8; ++q) {
-                const int chunk = ssub * (C::KPT / 8) + q;
-                uint4* dst = reinterpret_cast<uint4*>(smem + C::OFF_P + srow * (TK * 2) +
-                                                      ((chunk ^ (srow & 7)) << 4));
-                *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
-            if (ssub == 0) sAlpha[srow] = alpha;
+        for (int e = 0; e < C::KPT; e += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(src + e);
+            x[e] = f.x; x[e + 1] = f.y; x[e + 2] = f.z; x[e + 3] = f.w;
         }
-        __syncthreads();
-
-        // ---- O = O * alpha + P V for this warp's rows and head-dim slice
-        {
-            const float a0 = sAlpha[mf * 16 + (lane >> 2)];
-            const float a1 = sAlpha[mf * 16 + (lane >> 2) + 8];
+        float mx = -INFINITY;
 #pragma unroll
-            for (int n = 0; n < C::NFD; ++n) {
-                acc[n][0] *= a0; acc[n][1] *= a0;
-                acc[n][2] *= a1; acc[n][3] *= a1;
+        for (int e = 0; e < C::KPT; ++e) mx = fmaxf(mx, x[e]);
+#pragma unroll
+        for (int o = C::TPR / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - m_use);
+        float sum = 0.f;
+        uint32_t pk[C::KPT / 2];
+#pragma unroll
+        for (int e = 0; e < C::KPT / 2; ++e) {
+            const float p0 = fast_exp2(x[2 * e] - m_use);
+            const float p1 = fast_exp2(x[2 * e + 1] - m_use);
+            sum += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+#pragma unroll
+        for (int o = C::TPR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        l_run = l_run * alpha + sum;
+        m_run = m_new;
+#pragma unroll
+        for (int q = 0; q < C::KPT / 8; ++q) {
+            const int chunk = ssub * (C::KPT / 8) + q;
+            *reinterpret_cast<uint4*>(smem + C::OFF_P + srow * 128 + ((chunk ^ (srow & 7)) << 4)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+        if (ssub == 0) sAlpha[srow] = alpha;
+    }
+
+    // O = O * alpha + P V for this warp's rows and head-dim slice.
+    __device__ void pv(uint32_t sV) {
+        const float* sAlpha = reinterpret_cast<const float*>(smem + C::OFF_A);
+        const float a0 = sAlpha[mf * 16 + (lane >> 2)];
+        const float a1 = sAlpha[mf * 16 + (lane >> 2) + 8];
+#pragma unroll
+        for (int n = 0; n < C::NFD; ++n) {
+            acc[n][0] *= a0; acc[n][1] *= a0;
+            acc[n][2] *= a1; acc[n][3] *= a1;
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::TK / 16; ++kk) {
+            uint32_t pa[4];
+            {
+                const int row = mf * 16 + (lane & 15);
+                const int chunk = kk * 2 + (lane >> 4);
+                ldsm_x4(sb + C::OFF_P + row * 128 + ((chunk ^ (row & 7)) << 4), pa[0], pa[1], pa[2], pa[3]);
             }
 #pragma unroll
-            for (int kk = 0; kk < TK / 16; ++kk) {
-                uint32_t pa[4];
-                {
-                    const int row = mf * 16 + (lane & 15);
-                    const int chunk = kk * 2 + (lane >> 4);
-                    ldsm_x4(sb + C::OFF_P + row * (TK * 2) + ((chunk ^ (row & 7)) << 4), pa[0], pa[1],
-                            pa[2], pa[3]);
-                }
-#pragma unroll
-                for (int np = 0; np < C::NFD / 2; ++np) {
-                    const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                    const int dchunk = (wk * C::DSL + np * 16) / 8 + (lane >> 4);
-                    uint32_t v0, v1, v2, v3;
-                    ldsm_x4_t(sV + key * C::ROW_BYTES + ((dchunk ^ (key & 7)) << 4), v0, v1, v2, v3);
-                    mma_16816(acc[2 * np], pa, v0, v1);
-                    mma_16816(acc[2 * np + 1], pa, v2, v3);
-                }
+            for (int np = 0; np < C::NFD / 2; ++np) {
+                const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int dchunk = (wk * C::DSL + np * 16) / 8 + (lane >> 4);
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(sV + sw_off(key, dchunk, C::SUB_BYTES), v0, v1, v2, v3);
+                mma_16816(acc[2 * np], pa, v0, v1);
+                mma_16816(acc[2 * np + 1], pa, v2, v3);
             }
         }
     }
-    cp_async_wait<0>();
 
-    float* sL = reinterpret_cast<float*>(smem + C::OFF_L);
-    float* sM = reinterpret_cast<float*>(smem + C::OFF_M);
-    if (ssub == 0) {
-        sL[srow] = l_run;
-        sM[srow] = m_run;
+    // Normalised partial O (FP32) and base-2 LSE of this split.  `bar` syncs consumers.
+    template <class Bar>
+    __device__ void store(const DecodeArgs& a, const Work& w, int R, Bar bar) {
+        float* sL = reinterpret_cast<float*>(smem + C::OFF_L);
+        float* sM = reinterpret_cast<float*>(smem + C::OFF_M);
+        if (ssub == 0) {
+            sL[srow] = l_run;
+            sM[srow] = m_run;
+        }
+        bar();
+        const size_t part_row0 = ((size_t)(w.b * a.Hkv + w.hkv) * a.max_splits + w.split) * R + w.row0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int rl = mf * 16 + (lane >> 2) + 8 * h;
+            if (rl < w.rows_here) {
+                const float l = sL[rl];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                float* dst = a.part_o + (part_row0 + rl) * (CHUNKS * 8) + wk * C::DSL + 2 * (lane & 3);
+#pragma unroll
+                for (int n = 0; n < C::NFD; ++n)
+                    *reinterpret_cast<float2*>(dst + n * 8) =
+                        make_float2(acc[n][2 * h] * inv, acc[n][2 * h + 1] * inv);
+            }
+        }
+        if (ctid < w.rows_here) {
+            const float l = sL[ctid];
+            a.part_lse[part_row0 + ctid] = l > 0.f ? sM[ctid] + log2f(l) : -INFINITY;
+        }
+    }
+};
+
+template <int D, int MF>
+__global__ void __launch_bounds__(DCfg<D, MF, true>::NT)
+decode_tma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DecodeArgs a, int R, int g, int n_rowblk, int box_tokens) {
+    using C = DCfg<D, MF, true>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+    Work w;
+    if (!work_of<C>(a, R, n_rowblk, w)) return;
+
+    const uint32_t bar0 = sb + C::OFF_BAR;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (C::NS + s); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), C::NC);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
     }
     __syncthreads();
 
-    const size_t part_row0 = ((size_t)(b * a.Hkv + hkv) * a.max_splits + split) * R + row0;
+    const int warp = threadIdx.x / 32;
+    if (warp == C::NC) {
+        // ------------------------------------------------------------ TMA producer
+        if ((threadIdx.x & 31) == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            const int32_t* trow = a.table + (size_t)w.b * a.max_pages;
+            const int nbox = C::TK / box_tokens;
+            const uint32_t box_bytes = (uint32_t)box_tokens * 128;
+            int issued = 0;
+            for (int it = 0; it < w.n_tiles; ++it) {
+                const int s = it % C::NS;
+                if (!mbar_wait(empty(s), ((it / C::NS) & 1) ^ 1, abort_flag)) break;
+                const int t0 = w.t_begin + it * C::TK;
+                int rows[8];        // first cache row of each box, or -1
+                int n = 0;
+                for (int i = 0; i < nbox; ++i) {
+                    const int t = t0 + i * box_tokens;
+                    int row = -1;
+                    if (t < w.t_end) {
+                        const int page = trow[t / a.page_size];
+                        // a page id outside the pool (a caller error) is not loaded
+                        if (page >= 0 && page < a.num_pages) row = page * a.page_size + t % a.page_size;
+                    }
+                    rows[i] = row;
+                    n += row >= 0;
+                }
+                mbar_arrive_expect_tx(full(s), (uint32_t)n * box_bytes * C::NSUB * 2);
+                const uint32_t sK = sb + C::OFF_KV + s * 2 * C::KV_TILE;
+                const uint32_t sV = sK + C::KV_TILE;
+                for (int i = 0; i < nbox; ++i) {
+                    if (rows[i] < 0) continue;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int rl = mf * 16 + (lane >> 2) + 8 * h;
-        if (rl < rows_here) {
-            const float l = sL[rl];
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            float* dst = a.part_o + (part_row0 + rl) * D + wk * C::DSL + 2 * (lane & 3);
-#pragma unroll
-            for (int n = 0; n < C::NFD; ++n)
-                *reinterpret_cast<float2*>(dst + n * 8) = make_float2(acc[n][2 * h] * inv, acc[n][2 * h + 1] * inv);
+                    for (int sub = 0; sub < C::NSUB; ++sub) {
+                        const uint32_t off = sub * C::SUB_BYTES + i * box_tokens * 128;
+                        tma_load_3d(sK + off, &tm_k, full(s), sub * 64, w.hkv, rows[i]);
+                        tma_load_3d(sV + off, &tm_v, full(s), sub * 64, w.hkv, rows[i]);
+                    }
+                }
+                issued = it + 1;
+            }
+            if (*abort_flag) {
+                // let copies already in flight land before the CTA goes away
+                for (int it = issued - C::NS > 0 ? issued - C::NS : 0; it < issued; ++it)
+                    mbar_drain(full(it % C::NS), (it / C::NS) & 1);
+            }
         }
+    } else {
+        // ------------------------------------------------------------ consumers
+        Consumer<C> c;
+        c.init(smem, sb, a, w, g);
+        auto bar = [] { named_bar_sync(1, C::NCT); };
+        c.load_q(a, w, g, bar);
+        const float sl = a.scale_log2;
+        for (int it = 0; it < w.n_tiles; ++it) {
+            const int s = it % C::NS;
+            const int t0 = w.t_begin + it * C::TK;
+            const uint32_t sK = sb + C::OFF_KV + s * 2 * C::KV_TILE;
+            const uint32_t sV = sK + C::KV_TILE;
+            const bool ok = mbar_wait(full(s), (it / C::NS) & 1, abort_flag);
+            if (ok) {
+                const int nvalid = w.t_end - t0;
+                if (nvalid < C::TK) {
+                    // Value rows past the request's end hold stale data: zero them.
+                    const int per_sub = (C::TK - nvalid) * 8;
+                    for (int idx = c.ctid; idx < per_sub * C::NSUB; idx += C::NCT) {
+                        const int sub = idx / per_sub;
+                        const int rem = idx % per_sub;
+                        *reinterpret_cast<uint4*>(smem + (sV - sb) + sub * C::SUB_BYTES +
+                                                  (nvalid + rem / 8) * 128 + (rem % 8) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                c.qk(sK, t0, sl);
+            }
+            if (!named_bar_and(1, C::NCT, ok)) break;   // every consumer leaves together
+            c.softmax();
+            named_bar_sync(1, C::NCT);
+            c.pv(sV);
+            __syncwarp();
+            if (c.lane == 0) mbar_arrive(empty(s));
+        }
+        c.store(a, w, R, bar);
     }
-    if (tid < rows_here) {
-        const float l = sL[tid];
-        a.part_lse[part_row0 + tid] = l > 0.f ? sM[tid] + log2f(l) : -INFINITY;
+    if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_decode_error, (int)kErrDecodeWait);
+}
+
+template <int D, int MF>
+__global__ void __launch_bounds__(DCfg<D, MF, false>::NT)
+decode_gather_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
+    using C = DCfg<D, MF, false>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+    Work w;
+    if (!work_of<C>(a, R, n_rowblk, w)) return;
+    const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
+    const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
+    const int32_t* trow = a.table + (size_t)w.b * a.max_pages;
+    const int tid = threadIdx.x;
+
+    auto load_tile = [&](int tile, int stage) {
+        const int t0 = w.t_begin + tile * C::TK;
+        const uint32_t sK = sb + C::OFF_KV + stage * 2 * C::KV_TILE;
+        const uint32_t sV = sK + C::KV_TILE;
+        constexpr int CH = C::NSUB * 8;
+        for (int idx = tid; idx < C::TK * CH; idx += C::NT) {
+            const int tok = idx / CH, ch = idx % CH;
+            const int t = t0 + tok;
+            const uint32_t off = sw_off(tok, ch, C::SUB_BYTES);
+            const int page = t < w.t_end ? trow[t / a.page_size] : -1;
+            // A page id outside the pool (a caller error) is read as zeros, never dereferenced.
+            if (page >= 0 && page < a.num_pages) {
+                const size_t e = (((size_t)page * a.page_size + t % a.page_size) * a.Hkv + w.hkv) * D + ch * 8;
+                cp_async16(sK + off, kc + e, 16);
+                cp_async16(sV + off, vc + e, 16);
+            } else {
+                cp_async16(sK + off, kc, 0);    // zero-fill: value rows past the end stay 0
+                cp_async16(sV + off, vc, 0);
+            }
+        }
+    };
+
+    Consumer<C> c;
+    c.init(smem, sb, a, w, g);
+    auto bar = [] { __syncthreads(); };
+    c.load_q(a, w, g, bar);
+#pragma unroll
+    for (int s = 0; s < C::NS - 1; ++s) {
+        if (s < w.n_tiles) load_tile(s, s);
+        cp_async_commit();
     }
+    const float sl = a.scale_log2;
+    for (int it = 0; it < w.n_tiles; ++it) {
+        cp_async_wait<C::NS - 2>();
+        __syncthreads();
+        {
+            const int nt = it + C::NS - 1;
+            if (nt < w.n_tiles) load_tile(nt, nt % C::NS);
+            cp_async_commit();
+        }
+        const int s = it % C::NS;
+        const uint32_t sK = sb + C::OFF_KV + s * 2 * C::KV_TILE;
+        c.qk(sK, w.t_begin + it * C::TK, sl);
+        __syncthreads();
+        c.softmax();
+        __syncthreads();
+        c.pv(sK + C::KV_TILE);
+    }
+    cp_async_wait<0>();
+    c.store(a, w, R, bar);
 }
 
 template <int D>
@@ -387,28 +565,38 @@ int choose_mf(int R) {
 }
 
 template <int D, int MF>
-cudaError_t launch_split(const DecodeArgs& a, int R, int g, int n_rowblk, cudaStream_t stream) {
-    using C = DCfg<D, MF>;
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, MF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
-    if (e != cudaSuccess) return e;
+cudaError_t launch_split(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int box_tokens,
+                         int R, int g, int n_rowblk, cudaStream_t stream) {
     dim3 grid(a.max_splits, a.Hkv, a.B * n_rowblk);
-    decode_split_kernel<D, MF><<<grid, C::NT, C::SMEM, stream>>>(a, R, g, n_rowblk);
+    if (tm_k) {
+        using C = DCfg<D, MF, true>;
+        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<D, MF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM);
+        if (e != cudaSuccess) return e;
+        decode_tma_kernel<D, MF><<<grid, C::NT, C::SMEM, stream>>>(*tm_k, *tm_v, a, R, g, n_rowblk, box_tokens);
+    } else {
+        using C = DCfg<D, MF, false>;
+        cudaError_t e = cudaFuncSetAttribute(decode_gather_kernel<D, MF>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        decode_gather_kernel<D, MF><<<grid, C::NT, C::SMEM, stream>>>(a, R, g, n_rowblk);
+    }
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_d(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int box_tokens,
+                     cudaStream_t stream) {
     const int g = a.Hq / a.Hkv;
     const int R = g * a.Sq;
     const int mf = choose_mf(R);
     const int n_rowblk = (R + 16 * mf - 1) / (16 * mf);
     cudaError_t e;
     switch (mf) {
-        case 1: e = launch_split<D, 1>(a, R, g, n_rowblk, stream); break;
-        case 2: e = launch_split<D, 2>(a, R, g, n_rowblk, stream); break;
-        case 3: e = launch_split<D, 3>(a, R, g, n_rowblk, stream); break;
-        default: e = launch_split<D, 4>(a, R, g, n_rowblk, stream); break;
+        case 1: e = launch_split<D, 1>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        case 2: e = launch_split<D, 2>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        case 3: e = launch_split<D, 3>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        default: e = launch_split<D, 4>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
     }
     if (e != cudaSuccess) return e;
     const long rows = (long)a.B * a.Sq * a.Hq;
@@ -418,10 +606,18 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+int decode_box_tokens(int D, int page_size) {
+    const int tk = key_tile(D);
+    const int bt = page_size < tk ? page_size : tk;
+    if (bt % 8 != 0 || page_size % bt != 0 || tk % bt != 0) return 0;
+    return bt;
+}
+
 bool plan_decode(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
                  DecodePlan* plan) {
     if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || page_size <= 0 || max_pages <= 0)
         return false;
+    const int TK = key_tile(D);
     const int g = Hq / Hkv;
     const long R = (long)g * Sq;
     const int mf = choose_mf((int)R);
@@ -450,13 +646,24 @@ bool plan_decode(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_p
     return true;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int box_tokens,
+                          cudaStream_t stream) {
     switch (a.D) {
-        case 64: return launch_d<64>(a, stream);
-        case 128: return launch_d<128>(a, stream);
-        case 256: return launch_d<256>(a, stream);
+        case 64: return launch_d<64>(a, tm_k, tm_v, box_tokens, stream);
+        case 128: return launch_d<128>(a, tm_k, tm_v, box_tokens, stream);
+        case 256: return launch_d<256>(a, tm_k, tm_v, box_tokens, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+int decode_take_device_error() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_error, sizeof(int)) != cudaSuccess) return -1;
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(int));
+    }
+    return v;
 }
 
 }  // namespace gqa

@@ -51,6 +51,13 @@ struct DecodePlan {
 
 bool plan_decode(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
                  DecodePlan* plan);
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// Tokens per TMA box for this page size (a multiple of 8 dividing both the
+// page and the key tile), or 0 when pages must be gathered row by row.
+int decode_box_tokens(int D, int page_size);
+// tm_k / tm_v: 3-D maps {D, Hkv, pages * page_size} with a {64, 1, box_tokens}
+// box, or nullptr for the cp.async gather kernel.
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int box_tokens,
+                          cudaStream_t stream);
+int decode_take_device_error();
 
 }  // namespace gqa
