@@ -9,18 +9,33 @@
 // never stored, and the per-row log-sum-exp is returned in natural-log units
 // (MATE "QSA", Core Attention).
 //
-// One CTA owns one 128-row query tile of one (b, h) and is warp-specialised:
-//   warp 4     TMA producer: Q once, then K_j and V_j tiles through two
+// One CTA owns two 128-row query tiles (Q0, Q1) of one (b, h); both read the
+// same K/V tiles.  Warp roles:
+//   warp 8     TMA producer: Q0 and Q1 once, then K_j and V_j tiles through two
 //              shared-memory rings (128-byte swizzle, 64-column boxes);
-//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into TMEM (two S
-//              buffers), then O += P_j V_j with P read from TMEM;
-//   warps 0-3  softmax: thread t owns query row t; it reads its S row from
-//              TMEM, folds the causal / padding mask, updates the running
-//              max and sum, writes P (bf16) back to TMEM, rescales O when the
-//              max grows, and finally normalises O and writes O and LSE.
+//   warp 9     MMA issuer (one thread): S_k = Q_k K_j^T into TMEM, then
+//              O_k += P_k V_j with P_k read from TMEM, alternating k = 0, 1 so
+//              the tensor core works on one tile while the other is softmaxed;
+//   warps 0-3  softmax of Q0, warps 4-7 softmax of Q1: thread t owns row t; it
+//              reads its S row from TMEM, folds the causal / padding mask,
+//              updates the running max and sum, writes P (bf16) back over its
+//              S row, rescales its O row when needed, and finally normalises O
+//              and writes O and LSE.
+// Warps 10-11 only complete the third warpgroup (register rebalancing works
+// per warpgroup).  TMEM (512 columns): S0 | S1 | O0 | O1; P_k occupies the
+// first 64 columns of S_k.
+//
+// The O rescale is lazy: the reference max of a row only moves when the tile
+// max exceeds it by more than kRescaleThreshold (log2 units), so P stays below
+// 2^threshold and most tiles touch no O at all.  The result is exact: O and l
+// are accumulated against the same reference max.  A rescale of O_k before PV
+// of tile i needs PV of tile i-1 complete; that is implied by S_k of tile i
+// having landed, since its commit follows that PV in the MMA thread's order.
+//
 // Key tiles holding no visible key (beyond the causal bound or fully padded)
-// are never loaded.  Every wait is bounded (ptx.cuh); on a timeout the CTA
-// stops issuing work, drains what is in flight, frees TMEM and returns.
+// are never loaded, and tiles past Q0's causal bound are skipped for Q0.
+// Every wait is bounded (ptx.cuh); on a timeout the CTA stops issuing work,
+// drains what is in flight, frees TMEM and returns.
 #include <cmath>
 
 #include "internal.h"
@@ -31,56 +46,66 @@ namespace {
 
 __device__ int g_prefill_error;
 
-constexpr int BM = 128;            // query rows per CTA (= TMEM lanes)
+constexpr int BM = 128;            // query rows per Q tile (= TMEM lanes)
+constexpr int NQ = 2;              // Q tiles per CTA
 constexpr int BN = 128;            // keys per tile
-constexpr int NUM_THREADS = 192;   // warps 0-3 softmax, 4 producer, 5 MMA
-constexpr int WARP_LOAD = 4;
-constexpr int WARP_MMA = 5;
+constexpr int NUM_THREADS = 384;   // warps 0-7 softmax, 8 producer, 9 MMA, 10-11 idle
+constexpr int WARP_LOAD = 8;
+constexpr int WARP_MMA = 9;
+// Registers per thread: the launch gives 168 to all 384 threads (64,512); the
+// producer/MMA warpgroup gives back 80 each, which the two softmax
+// warpgroups take: 208 * 256 + 88 * 128 = 64,512, the launch total.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsOther = 88;
+static_assert(kRegsSoftmax * 256 + kRegsOther * 128 <= kRegsLaunch * NUM_THREADS, "register split");
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleThreshold = 8.f;   // log2 units: P <= 256 between rescales
 
 template <int D>
 struct Cfg {
     static constexpr int KSUB = D / 64;                 // 64-column (128-byte) boxes per row
     static constexpr int SUB_BYTES = BN * 128;          // one box: 128 rows x 128 bytes
     static constexpr int TILE_BYTES = KSUB * SUB_BYTES; // one Q, K or V tile
-    static constexpr int NK = D == 64 ? 3 : 2;          // K ring depth
-    static constexpr int NV = D == 64 ? 3 : 2;          // V ring depth
+    static constexpr int NK = D == 64 ? 4 : 2;          // K ring depth
+    static constexpr int NV = D == 64 ? 4 : 2;          // V ring depth
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+    static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
     static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_V + NV * TILE_BYTES;
-    // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done, drain
-    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 1 + 1;
+    // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_final
+    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     // 1 KB alignment slack; at least 120 KB so that one CTA holds an SM (it
     // takes all 512 TMEM columns).
     static constexpr int SMEM_BYTES = SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
-    // TMEM columns (32-bit each): two S buffers, O, two P buffers (bf16 pairs).
-    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
-    static constexpr uint32_t COL_P0 = 256 + D, COL_P1 = 256 + D + 64;
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128;
+    static constexpr uint32_t COL_O0 = 256, COL_O1 = 256 + D;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t IDESC_QK = make_idesc_bf16(BM, BN, false, false);
     static constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, D, false, true);
-    static_assert(COL_P1 + 64 <= TMEM_COLS, "TMEM budget");
+    static_assert(COL_O1 + D <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
 struct TileInfo {
     int q0;          // first query row of the tile
-    int rows_valid;  // rows of the tile that exist (ragged tail)
+    int rows_valid;  // rows of the tile that exist (ragged tail; may be 0)
     int lim_first;   // keys [0, lim_first) are causally visible to every row of the tile
     int kv_end;      // no row of the tile sees a key >= kv_end
-    int n_tiles;     // key tiles to visit
+    int n_tiles;     // key tiles in [0, kv_end)
 };
 
-__device__ __forceinline__ TileInfo tile_info(int qtile, int Sq, int Skv, int causal) {
+__device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causal) {
     TileInfo t;
-    t.q0 = qtile * BM;
-    t.rows_valid = min(BM, Sq - t.q0);
-    const long p_first = (long)t.q0 + Skv - Sq;              // key position of the first row
-    const long p_last = (long)t.q0 + t.rows_valid - 1 + Skv - Sq;
-    if (causal) {
+    t.q0 = q0;
+    t.rows_valid = max(0, min(BM, Sq - q0));
+    if (t.rows_valid == 0) {
+        t.kv_end = t.lim_first = 0;
+    } else if (causal) {
+        const long p_first = (long)q0 + Skv - Sq;        // key position of the first row
+        const long p_last = p_first + t.rows_valid - 1;
         t.kv_end = (int)max(0L, min((long)Skv, p_last + 1));
         t.lim_first = (int)max(0L, min((long)Skv, p_first + 1));
     } else {
@@ -102,7 +127,7 @@ __device__ __forceinline__ uint32_t mask_word(const uint8_t* mrow, int key0, int
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a, int n_qtiles) {
+               const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a, int n_qpairs) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -114,7 +139,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     // Heaviest (last) query tiles first; adjacent CTAs share a KV head.
     const int bh = a.B * a.Hq;
-    const int qtile = n_qtiles - 1 - (int)(blockIdx.x / bh);
+    const int qp = n_qpairs - 1 - (int)(blockIdx.x / bh);
     const int rem = (int)(blockIdx.x % bh);
     const int hq = rem % a.Hq;
     const int b = rem / a.Hq;
@@ -126,10 +151,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto k_empty = [&](int i) { return bar0 + 8u * (1 + C::NK + i); };
     auto v_full = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + i); };
     auto v_empty = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + C::NV + i); };
-    auto s_full = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + i); };
-    auto p_full = [&](int i) { return bar0 + 8u * (3 + 2 * C::NK + 2 * C::NV + i); };
-    const uint32_t o_done = bar0 + 8u * (5 + 2 * C::NK + 2 * C::NV);
-    const uint32_t drain = bar0 + 8u * (6 + 2 * C::NK + 2 * C::NV);
+    auto s_full = [&](int k) { return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + k); };
+    auto p_full = [&](int k) { return bar0 + 8u * (3 + 2 * C::NK + 2 * C::NV + k); };
+    const uint32_t o_final = bar0 + 8u * (5 + 2 * C::NK + 2 * C::NV);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -137,9 +161,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(q_full, 1);
         for (int i = 0; i < C::NK; ++i) { mbar_init(k_full(i), 1); mbar_init(k_empty(i), 1); }
         for (int i = 0; i < C::NV; ++i) { mbar_init(v_full(i), 1); mbar_init(v_empty(i), 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(s_full(i), 1); mbar_init(p_full(i), BM); }
-        mbar_init(o_done, 1);
-        mbar_init(drain, 1);
+        for (int k = 0; k < NQ; ++k) { mbar_init(s_full(k), 1); mbar_init(p_full(k), BM); }
+        mbar_init(o_final, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -152,7 +175,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const TileInfo ti = tile_info(qtile, a.Sq, a.Skv, a.causal);
+    const int q0 = qp * (NQ * BM);
+    const TileInfo t0 = tile_info(q0, a.Sq, a.Skv, a.causal);
+    const TileInfo t1 = tile_info(q0 + BM, a.Sq, a.Skv, a.causal);
+    const int n_all = max(t0.n_tiles, t1.n_tiles);
+    const int kv_end_all = max(t0.kv_end, t1.kv_end);
     const uint8_t* mrow = a.mask ? a.mask + (size_t)b * a.Skv : nullptr;
 
     // Warp-collective: does key tile j hold no key the padding mask keeps?
@@ -160,136 +187,167 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!mrow) return false;
         uint32_t any = 0;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) any |= mask_word(mrow, j * BN + w * 32, ti.kv_end, lane);
+        for (int w = 0; w < 4; ++w) any |= mask_word(mrow, j * BN + w * 32, kv_end_all, lane);
         return any == 0;
     };
 
-    if (warp == WARP_LOAD) {
-        // ------------------------------------------------------------ producer
-        if (ti.n_tiles > 0) {
-            int nk = 0, nv = 0;   // K and V tile loads issued so far
-            bool q_issued = false;
-            if (lane == 0) {
-                tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(&tm_k);
-                tma_prefetch_desc(&tm_v);
-                mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
-#pragma unroll
-                for (int s = 0; s < C::KSUB; ++s)
-                    tma_load_4d(sb + C::OFF_Q + s * C::SUB_BYTES, &tm_q, q_full, s * 64, ti.q0, hq, b);
-                q_issued = true;
-            }
-            for (int j = 0; j < ti.n_tiles; ++j) {
-                if (tile_empty(j)) continue;
-                bool ok = true;
+    // Each role ends on its own (no shared tail), so register limits apply per
+    // role: the MMA warp frees TMEM once the softmax warps have arrived on
+    // barrier 2 after their last TMEM access.
+    if (warp >= 8) {
+        regs_dec<kRegsOther>();
+        if (warp == WARP_LOAD) {
+            // ------------------------------------------------------------ producer
+            if (n_all > 0) {
+                int nk = 0, nv = 0;   // K and V tile loads issued so far
+                bool q_issued = false;
                 if (lane == 0) {
-                    const int ks = nk % C::NK;
-                    ok = mbar_wait(k_empty(ks), ((nk / C::NK) & 1) ^ 1, abort_flag);
-                    if (ok) {
-                        mbar_arrive_expect_tx(k_full(ks), C::TILE_BYTES);
+                    tma_prefetch_desc(&tm_q);
+                    tma_prefetch_desc(&tm_k);
+                    tma_prefetch_desc(&tm_v);
+                    mbar_arrive_expect_tx(q_full, NQ * C::TILE_BYTES);
+#pragma unroll
+                    for (int k = 0; k < NQ; ++k)
 #pragma unroll
                         for (int s = 0; s < C::KSUB; ++s)
-                            tma_load_4d(sb + C::OFF_K + ks * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k,
-                                        k_full(ks), s * 64, j * BN, hkv, b);
-                        ++nk;
-                        const int vs = nv % C::NV;
-                        ok = mbar_wait(v_empty(vs), ((nv / C::NV) & 1) ^ 1, abort_flag);
+                            tma_load_4d(sb + C::OFF_Q + k * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, q_full, s * 64,
+                                        q0 + k * BM, hq, b);
+                    q_issued = true;
+                }
+                for (int j = 0; j < n_all; ++j) {
+                    if (tile_empty(j)) continue;
+                    bool ok = true;
+                    if (lane == 0) {
+                        const int ks = nk % C::NK;
+                        ok = mbar_wait(k_empty(ks), ((nk / C::NK) & 1) ^ 1, abort_flag);
                         if (ok) {
-                            mbar_arrive_expect_tx(v_full(vs), C::TILE_BYTES);
+                            mbar_arrive_expect_tx(k_full(ks), C::TILE_BYTES);
 #pragma unroll
                             for (int s = 0; s < C::KSUB; ++s)
-                                tma_load_4d(sb + C::OFF_V + vs * C::TILE_BYTES + s * C::SUB_BYTES,
-                                            &tm_v, v_full(vs), s * 64, j * BN, hkv, b);
-                            ++nv;
+                                tma_load_4d(sb + C::OFF_K + ks * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k,
+                                            k_full(ks), s * 64, j * BN, hkv, b);
+                            ++nk;
+                            const int vs = nv % C::NV;
+                            ok = mbar_wait(v_empty(vs), ((nv / C::NV) & 1) ^ 1, abort_flag);
+                            if (ok) {
+                                mbar_arrive_expect_tx(v_full(vs), C::TILE_BYTES);
+#pragma unroll
+                                for (int s = 0; s < C::KSUB; ++s)
+                                    tma_load_4d(sb + C::OFF_V + vs * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v,
+                                                v_full(vs), s * 64, j * BN, hkv, b);
+                                ++nv;
+                            }
                         }
                     }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                // The Q load may have no consumer (every key tile masked out):
+                // never leave it in flight.
+                if (lane == 0 && q_issued) mbar_drain(q_full, 0);
+                if (lane == 0 && *abort_flag) {
+                    // Let copies already in flight land before the CTA goes away:
+                    // wait for the last load issued into each slot.
+                    for (int s = 0; s < C::NK && s < nk; ++s) {
+                        const int last = nk - 1 - ((nk - 1 - s) % C::NK);
+                        mbar_drain(k_full(s), (last / C::NK) & 1);
+                    }
+                    for (int s = 0; s < C::NV && s < nv; ++s) {
+                        const int last = nv - 1 - ((nv - 1 - s) % C::NV);
+                        mbar_drain(v_full(s), (last / C::NV) & 1);
+                    }
+                }
             }
-            if (lane == 0 && *abort_flag) {
-                // Let copies already in flight land before the CTA goes away:
-                // wait for the last load issued into each slot.
-                if (q_issued) mbar_drain(q_full, 0);
-                for (int s = 0; s < C::NK && s < nk; ++s) {
-                    const int last = nk - 1 - ((nk - 1 - s) % C::NK);
-                    mbar_drain(k_full(s), (last / C::NK) & 1);
-                }
-                for (int s = 0; s < C::NV && s < nv; ++s) {
-                    const int last = nv - 1 - ((nv - 1 - s) % C::NV);
-                    mbar_drain(v_full(s), (last / C::NV) & 1);
-                }
-            }
-        }
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------------------ MMA issuer
-        if (ti.n_tiles > 0) {
-            auto issue_pv = [&](int t) -> bool {
-                const int pb = t & 1;
-                if (!mbar_wait(p_full(pb), (t >> 1) & 1, abort_flag)) return false;
-                const int vs = t % C::NV;
-                if (!mbar_wait(v_full(vs), (t / C::NV) & 1, abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t pcol = pb ? C::COL_P1 : C::COL_P0;
-                const uint32_t vbase = sb + C::OFF_V + vs * C::TILE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // keys 16kk..16kk+15 of V: rows 16kk.. of every 64-column box
-                    const uint64_t bdesc = make_sdesc_sw128(vbase + kk * 16 * 128, C::SUB_BYTES, 1024);
-                    mma_bf16_ts(tmem + C::COL_O, tmem + pcol + kk * 8, bdesc, C::IDESC_PV,
-                                (t > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(o_done);
-                mma_commit(v_empty(vs));
-                return true;
-            };
-
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(q_full, 0, abort_flag);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            int it = 0;
-            for (int j = 0; j < ti.n_tiles && ok; ++j) {
+        } else if (warp == WARP_MMA) {
+            // ------------------------------------------------------------ MMA issuer
+            // Visited key tiles (non-empty, below kv_end of either Q tile) are
+            // numbered i = 0, 1, ...; Q_k takes part in the first c_k of them.
+            int c0 = 0, c1 = 0, c_all = 0;
+            for (int j = 0; j < n_all; ++j) {
                 if (tile_empty(j)) continue;
-                if (lane == 0) {
-                    const int ks = it % C::NK;
-                    ok = mbar_wait(k_full(ks), (it / C::NK) & 1, abort_flag);
-                    if (ok) {
-                        tc_fence_after();
-                        const uint32_t d = tmem + ((it & 1) ? C::COL_S1 : C::COL_S0);
-                        const uint32_t kbase = sb + C::OFF_K + ks * C::TILE_BYTES;
+                c0 += j < t0.n_tiles;
+                c1 += j < t1.n_tiles;
+                ++c_all;
+            }
+            if (c_all > 0 && lane == 0) {
+                auto issue_s = [&](int k, int i) {
+                    const uint32_t kbase = sb + C::OFF_K + (i % C::NK) * C::TILE_BYTES;
+                    const uint32_t qbase = sb + C::OFF_Q + k * C::TILE_BYTES;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t koff = (kk / 4) * C::SUB_BYTES + (kk % 4) * 32;
-                            const uint64_t adesc = make_sdesc_sw128(sb + C::OFF_Q + koff, 16, 1024);
-                            const uint64_t bdesc = make_sdesc_sw128(kbase + koff, 16, 1024);
-                            mma_bf16_ss(d, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(s_full(it & 1));
-                        mma_commit(k_empty(ks));
-                        if (it > 0) ok = issue_pv(it - 1);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = (kk / 4) * C::SUB_BYTES + (kk % 4) * 32;
+                        mma_bf16_ss(tmem + (k == 0 ? C::COL_S0 : C::COL_S1), make_sdesc_sw128(qbase + koff, 16, 1024),
+                                    make_sdesc_sw128(kbase + koff, 16, 1024), C::IDESC_QK, kk > 0 ? 1u : 0u);
                     }
+                    mma_commit(s_full(k));
+                };
+                auto issue_pv = [&](int k, int i) {
+                    const uint32_t vbase = sb + C::OFF_V + (i % C::NV) * C::TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        // keys 16kk..16kk+15 of V: rows 16kk.. of every 64-column box
+                        const uint64_t bdesc = make_sdesc_sw128(vbase + kk * 16 * 128, C::SUB_BYTES, 1024);
+                        mma_bf16_ts(tmem + (k == 0 ? C::COL_O0 : C::COL_O1), tmem + (k == 0 ? C::COL_S0 : C::COL_S1) + kk * 8,
+                                    bdesc, C::IDESC_PV,
+                                    (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                };
+                bool ok = mbar_wait(q_full, 0, abort_flag) && mbar_wait(k_full(0), 0, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    if (c0 > 0) issue_s(0, 0);
+                    if (c1 > 0) issue_s(1, 0);
+                    mma_commit(k_empty(0));
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                ++it;
+                for (int i = 0; i < c_all && ok; ++i) {
+                    ok = mbar_wait(v_full(i % C::NV), (i / C::NV) & 1, abort_flag);
+                    if (!ok) break;
+                    const bool more = i + 1 < c_all;
+                    for (int k = 0; k < NQ && ok; ++k) {
+                        const int cnt = k == 0 ? c0 : c1;
+                        if (i < cnt) {
+                            ok = mbar_wait(p_full(k), i & 1, abort_flag);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_pv(k, i);
+                        }
+                        if (more) {
+                            if (k == 0) {
+                                ok = mbar_wait(k_full((i + 1) % C::NK), ((i + 1) / C::NK) & 1, abort_flag);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            // S_k of tile i+1 overwrites P_k of tile i: issued after its PV.
+                            if (i + 1 < cnt) issue_s(k, i + 1);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(v_empty(i % C::NV));
+                    if (more) mma_commit(k_empty((i + 1) % C::NK));
+                }
+                // Arrives once every MMA issued above has completed.
+                mma_commit(o_final);
+                if (!ok) mbar_drain(o_final, 0);
             }
-            if (ok && it > 0 && lane == 0) issue_pv(it - 1);
             __syncwarp();
-            if (lane == 0) {
-                // Every MMA issued above has completed once this arrives.
-                mma_commit(drain);
-                mbar_drain(drain, 0);
-            }
-            __syncwarp();
+            named_bar_sync(2, 8 * 32 + 32);          // softmax warps are done with TMEM
+            tc_fence_after();
+            tmem_dealloc(tmem, C::TMEM_COLS);
         }
     } else {
-        // ------------------------------------------------------------ softmax warps 0-3
-        const int r = warp * 32 + lane;                       // row of the tile == TMEM lane
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        regs_inc<kRegsSoftmax>();
+        // ------------------------------------------------------------ softmax warps 0-7
+        const int k = warp / 4;                                // Q tile of this warpgroup
+        const TileInfo ti = k == 0 ? t0 : t1;
+        const int r = (warp % 4) * 32 + lane;                  // row of the tile == TMEM lane
+        const uint32_t lane_addr = (uint32_t)((warp % 4) * 32) << 16;
+        const uint32_t col_s = k == 0 ? C::COL_S0 : C::COL_S1;
+        const uint32_t col_o = k == 0 ? C::COL_O0 : C::COL_O1;
         const int row_q = ti.q0 + r;
         const long p_row = (long)row_q + a.Skv - a.Sq;
         const int lim = a.causal ? (int)max(0L, min((long)a.Skv, p_row + 1)) : a.Skv;
         const float sl = a.scale_log2;
-        float m_run = -INFINITY;
+        float m_ref = -INFINITY;     // reference max (log2 units, scaled)
         float l_run = 0.f;
         bool ok = true;
         int it = 0;
@@ -300,7 +358,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 uint32_t any = 0;
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    mw[w] = mask_word(mrow, j * BN + w * 32, ti.kv_end, lane);
+                    mw[w] = mask_word(mrow, j * BN + w * 32, kv_end_all, lane);
                     any |= mw[w];
                     all_kept = all_kept && (mw[w] == 0xffffffffu);
                 }
@@ -309,13 +367,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const int kbase = j * BN;
             const bool need_mask = (kbase + BN > ti.lim_first) || !all_kept;
 
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full(it & 1), (it >> 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full(k), it & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t scol = (it & 1) ? C::COL_S1 : C::COL_S0;
-            float s[BN];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem + lane_addr + scol + 32 * c, s + 32 * c);
+            uint32_t sr[BN];
+            tmem_ld128(tmem + lane_addr + col_s, sr);
+            float* s = reinterpret_cast<float*>(sr);
 
             float mx = -INFINITY;
             if (need_mask) {
@@ -332,9 +389,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     mx = fmaxf(mx, s[c]);
                 }
             }
-            const float m_new = fmaxf(m_run, mx);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;   // no -inf - -inf
-            const float alpha = fast_exp2(m_run - m_use);
+            // Lazy rescale: move the reference max only when the tile max
+            // exceeds it by more than the threshold.
+            float alpha = 1.f;
+            if (mx > m_ref + kRescaleThreshold) {
+                alpha = fast_exp2(m_ref - mx);                  // 0 when m_ref is -inf
+                m_ref = mx;
+            }
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;   // no -inf - -inf
             float rs = 0.f;
             uint32_t pk[BN / 2];
 #pragma unroll
@@ -344,35 +406,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 rs += p0 + p1;
                 pk[c] = pack_bf16x2(p0, p1);
             }
-            const uint32_t pcol = (it & 1) ? C::COL_P1 : C::COL_P0;
-            tmem_st32(tmem + lane_addr + pcol, pk);
-            tmem_st32(tmem + lane_addr + pcol + 32, pk + 32);
+            tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
             l_run = l_run * alpha + rs;
-            m_run = m_new;
 
-            if (it > 0) {
-                // O must hold P_{it-1} V_{it-1} before it is rescaled.
-                ok = __all_sync(0xffffffffu, mbar_wait(o_done, (it - 1) & 1, abort_flag));
-                if (!ok) break;
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            // PV of the previous tile is complete (S of this tile landed after
+            // it), so O may be rescaled here, before PV of this tile.
+            if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tmem + lane_addr + C::COL_O + 32 * c, o);
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_addr + col_o + 32 * c, o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st32(tmem + lane_addr + C::COL_O + 32 * c, reinterpret_cast<uint32_t*>(o));
-                    }
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tmem_st32(tmem + lane_addr + col_o + 32 * c, reinterpret_cast<uint32_t*>(o));
                 }
             }
             tc_fence_before();
-            mbar_arrive(p_full(it & 1));
+            mbar_arrive(p_full(k));
             ++it;
         }
 
         if (ok && it > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(o_done, (it - 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0, abort_flag));
             if (ok) tc_fence_after();
         }
         const bool row_ok = r < ti.rows_valid;
@@ -383,7 +438,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];
-                tmem_ld32(tmem + lane_addr + C::COL_O + 32 * c, o);
+                tmem_ld32(tmem + lane_addr + col_o + 32 * c, o);
                 if (row_ok) {
                     uint32_t w[16];
 #pragma unroll
@@ -401,16 +456,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         if (row_ok && a.lse)
             a.lse[((size_t)b * a.Sq + row_q) * a.Hq + hq] =
-                l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+                l_run > 0.f ? (m_ref + log2f(l_run)) * kLn2 : -INFINITY;
+        tc_fence_before();
+        named_bar_arrive(2, 8 * 32 + 32);
+        if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_prefill_error, (int)kErrPrefillWait);
     }
 
-    tc_fence_before();
-    __syncthreads();
-    if (warp == WARP_MMA) {
-        tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
-    }
-    if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_prefill_error, (int)kErrPrefillWait);
 }
 
 __global__ void empty_rows_kernel(__nv_bfloat16* o, float* lse, long rows, int D) {
@@ -428,9 +479,9 @@ cudaError_t launch_prefill_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int n_qtiles = (a.Sq + BM - 1) / BM;
-    const long grid = (long)n_qtiles * a.B * a.Hq;
-    prefill_kernel<D><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, a, n_qtiles);
+    const int n_qpairs = (a.Sq + NQ * BM - 1) / (NQ * BM);
+    const long grid = (long)n_qpairs * a.B * a.Hq;
+    prefill_kernel<D><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, a, n_qpairs);
     return cudaGetLastError();
 }
 
