@@ -116,12 +116,57 @@ __device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causa
     return t;
 }
 
-// Bit `lane` of the result: key key0 + lane is below kv_end and kept by the
-// padding mask.  Warp-collective.
-__device__ __forceinline__ uint32_t mask_word(const uint8_t* mrow, int key0, int kv_end, int lane) {
-    const int key = key0 + lane;
-    const bool keep = key < kv_end && mrow[key] != 0;
-    return __ballot_sync(0xffffffffu, keep);
+// Warp-collective.  Bit l of the result is set when key tile 32 * chunk + l
+// (below n_tiles) holds a key below kv_end that the padding mask keeps; lane l
+// scans that tile, so 32 tiles cost one pass.  Without a mask every tile
+// below n_tiles counts.
+__device__ __forceinline__ uint32_t tile_flags(const uint8_t* mrow, int chunk, int n_tiles, int kv_end, int lane) {
+    const int j = chunk * 32 + lane;
+    bool any = j < n_tiles;
+    if (mrow && any) {
+        const int k0 = j * BN, k1 = min(k0 + BN, kv_end);
+        const uint8_t* p = mrow + k0;
+        any = false;
+        if (k1 - k0 == BN && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+            const uint4* q = reinterpret_cast<const uint4*>(p);
+            uint32_t acc = 0;
+#pragma unroll
+            for (int e = 0; e < BN / 16; ++e) {
+                const uint4 v = __ldg(q + e);
+                acc |= v.x | v.y | v.z | v.w;
+            }
+            any = acc != 0;
+        } else {
+            for (int k = 0; k < k1 - k0 && !any; ++k) any = p[k] != 0;
+        }
+    }
+    return __ballot_sync(0xffffffffu, any);
+}
+
+// Walks the visited key tiles (non-empty ones below n_tiles) in increasing
+// order, 32 tiles per scan.  Warp-collective; every lane sees the same tiles.
+struct TileIter {
+    const uint8_t* mrow;
+    int n_tiles, kv_end, lane, chunk;
+    uint32_t f;
+    __device__ __forceinline__ TileIter(const uint8_t* m, int n, int e, int l)
+        : mrow(m), n_tiles(n), kv_end(e), lane(l), chunk(-1), f(0) {}
+    __device__ __forceinline__ int next() {   // next visited tile, or -1
+        while (f == 0) {
+            ++chunk;
+            if (chunk * 32 >= n_tiles) return -1;
+            f = tile_flags(mrow, chunk, n_tiles, kv_end, lane);
+        }
+        const int l = __ffs(f) - 1;
+        f &= f - 1;
+        return chunk * 32 + l;
+    }
+};
+
+// Bits of the tiles of chunk `chunk` whose index is below n.
+__device__ __forceinline__ uint32_t below_bits(int n, int chunk) {
+    const int rel = n - chunk * 32;
+    return rel >= 32 ? 0xffffffffu : (rel <= 0 ? 0u : ((1u << rel) - 1u));
 }
 
 template <int D>
@@ -182,15 +227,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int kv_end_all = max(t0.kv_end, t1.kv_end);
     const uint8_t* mrow = a.mask ? a.mask + (size_t)b * a.Skv : nullptr;
 
-    // Warp-collective: does key tile j hold no key the padding mask keeps?
-    auto tile_empty = [&](int j) -> bool {
-        if (!mrow) return false;
-        uint32_t any = 0;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) any |= mask_word(mrow, j * BN + w * 32, kv_end_all, lane);
-        return any == 0;
-    };
-
     // Each role ends on its own (no shared tail), so register limits apply per
     // role: the MMA warp frees TMEM once the softmax warps have arrived on
     // barrier 2 after their last TMEM access.
@@ -214,8 +250,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                         q0 + k * BM, hq, b);
                     q_issued = true;
                 }
-                for (int j = 0; j < n_all; ++j) {
-                    if (tile_empty(j)) continue;
+                TileIter tiles(mrow, n_all, kv_end_all, lane);
+                for (int j = tiles.next(); j >= 0; j = tiles.next()) {
                     bool ok = true;
                     if (lane == 0) {
                         const int ks = nk % C::NK;
@@ -263,11 +299,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // Visited key tiles (non-empty, below kv_end of either Q tile) are
             // numbered i = 0, 1, ...; Q_k takes part in the first c_k of them.
             int c0 = 0, c1 = 0, c_all = 0;
-            for (int j = 0; j < n_all; ++j) {
-                if (tile_empty(j)) continue;
-                c0 += j < t0.n_tiles;
-                c1 += j < t1.n_tiles;
-                ++c_all;
+            for (int chunk = 0; chunk * 32 < n_all; ++chunk) {
+                const uint32_t f = tile_flags(mrow, chunk, n_all, kv_end_all, lane);
+                c_all += __popc(f);
+                c0 += __popc(f & below_bits(t0.n_tiles, chunk));
+                c1 += __popc(f & below_bits(t1.n_tiles, chunk));
             }
             if (c_all > 0 && lane == 0) {
                 auto issue_s = [&](int k, int i) {
@@ -351,18 +387,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         float l_run = 0.f;
         bool ok = true;
         int it = 0;
-        for (int j = 0; j < ti.n_tiles; ++j) {
-            uint32_t mw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-            bool all_kept = true;
-            if (mrow) {
-                uint32_t any = 0;
+        // The mask bytes of the next visited tile are fetched one tile ahead.
+        TileIter tiles(mrow, n_all, kv_end_all, lane);
+        auto fetch = [&](int j, uint8_t* mb) {
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    mw[w] = mask_word(mrow, j * BN + w * 32, kv_end_all, lane);
-                    any |= mw[w];
-                    all_kept = all_kept && (mw[w] == 0xffffffffu);
-                }
-                if (any == 0) continue;                         // skipped by every role
+            for (int w = 0; w < 4; ++w) {
+                const int key = j * BN + w * 32 + lane;
+                mb[w] = (mrow && j >= 0 && key < kv_end_all) ? mrow[key] : (uint8_t)(mrow ? 0 : 1);
+            }
+        };
+        int j = tiles.next();
+        uint8_t mb[4];
+        fetch(j, mb);
+        for (; j >= 0 && j < ti.n_tiles;) {
+            const int jn = tiles.next();
+            uint8_t mbn[4];
+            fetch(jn, mbn);
+            uint32_t mw[4];
+            bool all_kept = true;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                mw[w] = __ballot_sync(0xffffffffu, mb[w] != 0);
+                all_kept = all_kept && (mw[w] == 0xffffffffu);
             }
             const int kbase = j * BN;
             const bool need_mask = (kbase + BN > ti.lim_first) || !all_kept;
@@ -374,21 +420,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tmem_ld128(tmem + lane_addr + col_s, sr);
             float* s = reinterpret_cast<float*>(sr);
 
-            float mx = -INFINITY;
-            if (need_mask) {
+            // Row max over 8 independent chains (short dependency chains).
+            // Fast path (no mask in this tile, positive scale): the max is taken
+            // on raw scores and the scale is folded into the exp2 argument;
+            // otherwise scores are scaled first and masked ones set to -inf.
+            const bool fast = !need_mask && sl > 0.f;
+            float mx8[8];
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const bool vis = (kbase + c < lim) && ((mw[c >> 5] >> (c & 31)) & 1u);
-                    s[c] = vis ? s[c] * sl : -INFINITY;
-                    mx = fmaxf(mx, s[c]);
-                }
+            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+            if (fast) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
             } else {
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    s[c] *= sl;
-                    mx = fmaxf(mx, s[c]);
+                for (int w = 0; w < 4; ++w) {
+                    // keys of this 32-column group below the row's causal limit
+                    const int rel = lim - (kbase + 32 * w);
+                    const uint32_t below = rel >= 32 ? 0xffffffffu : (rel <= 0 ? 0u : ((1u << rel) - 1u));
+                    const uint32_t vis = mw[w] & below;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float x = ((vis >> c) & 1u) ? s[32 * w + c] * sl : -INFINITY;
+                        s[32 * w + c] = x;
+                        mx8[c & 7] = fmaxf(mx8[c & 7], x);
+                    }
                 }
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + 4]);
+            const float mx_raw = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+            const float mx = fast ? mx_raw * sl : mx_raw;          // scaled (log2 units)
             // Lazy rescale: move the reference max only when the tile max
             // exceeds it by more than the threshold.
             float alpha = 1.f;
@@ -397,15 +458,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 m_ref = mx;
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;   // no -inf - -inf
-            float rs = 0.f;
+            // exp2 argument: s * fa - m_use (fa = scale on the fast path, 1 otherwise)
+            const float fa = fast ? sl : 1.f;
+            float rs8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
             uint32_t pk[BN / 2];
 #pragma unroll
             for (int c = 0; c < BN / 2; ++c) {
-                const float p0 = fast_exp2(s[2 * c] - m_use);
-                const float p1 = fast_exp2(s[2 * c + 1] - m_use);
-                rs += p0 + p1;
+                const float p0 = fast_exp2(fmaf(s[2 * c], fa, -m_use));
+                const float p1 = fast_exp2(fmaf(s[2 * c + 1], fa, -m_use));
+                rs8[(2 * c) & 7] += p0;
+                rs8[(2 * c + 1) & 7] += p1;
                 pk[c] = pack_bf16x2(p0, p1);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) rs8[e] += rs8[e + 4];
+            const float rs = (rs8[0] + rs8[1]) + (rs8[2] + rs8[3]);
             tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
             l_run = l_run * alpha + rs;
 
@@ -424,6 +493,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_before();
             mbar_arrive(p_full(k));
             ++it;
+            j = jn;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) mb[w] = mbn[w];
         }
 
         if (ok && it > 0) {
