@@ -430,7 +430,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
             if (fast) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                for (int c = 0; c < BN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
             } else {
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
@@ -460,21 +460,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;   // no -inf - -inf
             // exp2 argument: s * fa - m_use (fa = scale on the fast path, 1 otherwise)
             const float fa = fast ? sl : 1.f;
-            float rs8[8];
+            // p = 2^(s * fa - m_use), two columns per paired FMA / add.
+            const uint64_t fa2 = f32x2(fa, fa);
+            const uint64_t nm2 = f32x2(-m_use, -m_use);
+            uint64_t rs4[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
+            for (int e = 0; e < 4; ++e) rs4[e] = f32x2(0.f, 0.f);
             uint32_t pk[BN / 2];
 #pragma unroll
             for (int c = 0; c < BN / 2; ++c) {
-                const float p0 = fast_exp2(fmaf(s[2 * c], fa, -m_use));
-                const float p1 = fast_exp2(fmaf(s[2 * c + 1], fa, -m_use));
-                rs8[(2 * c) & 7] += p0;
-                rs8[(2 * c + 1) & 7] += p1;
+                float x0, x1;
+                f32x2_split(ffma2(f32x2(s[2 * c], s[2 * c + 1]), fa2, nm2), x0, x1);
+                const float p0 = fast_exp2(x0);
+                const float p1 = fast_exp2(x1);
+                rs4[c & 3] = fadd2(rs4[c & 3], f32x2(p0, p1));
                 pk[c] = pack_bf16x2(p0, p1);
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) rs8[e] += rs8[e + 4];
-            const float rs = (rs8[0] + rs8[1]) + (rs8[2] + rs8[3]);
+            rs4[0] = fadd2(rs4[0], rs4[2]);
+            rs4[1] = fadd2(rs4[1], rs4[3]);
+            float r0, r1, r2, r3;
+            f32x2_split(rs4[0], r0, r1);
+            f32x2_split(rs4[1], r2, r3);
+            const float rs = (r0 + r1) + (r2 + r3);
             tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
             l_run = l_run * alpha + rs;
 
