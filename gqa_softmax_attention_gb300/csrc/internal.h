@@ -23,6 +23,8 @@ cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
 // Rows with no key at all (Skv == 0): O = 0, LSE = -inf.
 cudaError_t launch_empty_rows(void* o, float* lse, long rows, int D, cudaStream_t stream);
 int prefill_take_device_error();
+// y[i] = 2^x[i] by the prefill kernel's FMA-pipe exp2 (diagnostic).
+cudaError_t launch_exp2_poly(const float* x, float* y, long n, cudaStream_t stream);
 
 struct DecodeArgs {
     const void* q;          // [B, Sq, Hq, D]

@@ -61,6 +61,9 @@ constexpr int kRegsOther = 88;
 static_assert(kRegsSoftmax * 256 + kRegsOther * 128 <= kRegsLaunch * NUM_THREADS, "register split");
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P <= 256 between rescales
+// One exponential pair in kPolyEvery goes to the FMA-pipe exp2 on unmasked
+// tiles (0: all on the MUFU).
+constexpr int kPolyEvery = 0;
 
 template <int D>
 struct Cfg {
@@ -167,6 +170,37 @@ struct TileIter {
 __device__ __forceinline__ uint32_t below_bits(int n, int chunk) {
     const int rel = n - chunk * 32;
     return rel >= 32 ? 0xffffffffu : (rel <= 0 ? 0u : ((1u << rel) - 1u));
+}
+
+// p[c] = 2^(s[c] * fa - m_use) for one 128-column row: P packed to bf16x2 in
+// pk, the row sum returned.  Two columns per paired FMA / add; with POLY > 0,
+// one column pair in POLY is evaluated on the FMA pipe instead of the MUFU.
+template <int POLY>
+__device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, uint32_t* pk) {
+    const uint64_t fa2 = f32x2(fa, fa);
+    const uint64_t nm2 = f32x2(-m_use, -m_use);
+    uint64_t rs4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) rs4[e] = f32x2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < BN / 2; ++c) {
+        float x0, x1, p0, p1;
+        f32x2_split(ffma2(f32x2(s[2 * c], s[2 * c + 1]), fa2, nm2), x0, x1);
+        if (POLY > 0 && c % (POLY > 0 ? POLY : 1) == (POLY > 0 ? POLY : 1) - 1) {
+            exp2_poly_x2(x0, x1, p0, p1);
+        } else {
+            p0 = fast_exp2(x0);
+            p1 = fast_exp2(x1);
+        }
+        rs4[c & 3] = fadd2(rs4[c & 3], f32x2(p0, p1));
+        pk[c] = pack_bf16x2(p0, p1);
+    }
+    rs4[0] = fadd2(rs4[0], rs4[2]);
+    rs4[1] = fadd2(rs4[1], rs4[3]);
+    float r0, r1, r2, r3;
+    f32x2_split(rs4[0], r0, r1);
+    f32x2_split(rs4[1], r2, r3);
+    return (r0 + r1) + (r2 + r3);
 }
 
 template <int D>
@@ -460,28 +494,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;   // no -inf - -inf
             // exp2 argument: s * fa - m_use (fa = scale on the fast path, 1 otherwise)
             const float fa = fast ? sl : 1.f;
-            // p = 2^(s * fa - m_use), two columns per paired FMA / add.
-            const uint64_t fa2 = f32x2(fa, fa);
-            const uint64_t nm2 = f32x2(-m_use, -m_use);
-            uint64_t rs4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) rs4[e] = f32x2(0.f, 0.f);
             uint32_t pk[BN / 2];
-#pragma unroll
-            for (int c = 0; c < BN / 2; ++c) {
-                float x0, x1;
-                f32x2_split(ffma2(f32x2(s[2 * c], s[2 * c + 1]), fa2, nm2), x0, x1);
-                const float p0 = fast_exp2(x0);
-                const float p1 = fast_exp2(x1);
-                rs4[c & 3] = fadd2(rs4[c & 3], f32x2(p0, p1));
-                pk[c] = pack_bf16x2(p0, p1);
-            }
-            rs4[0] = fadd2(rs4[0], rs4[2]);
-            rs4[1] = fadd2(rs4[1], rs4[3]);
-            float r0, r1, r2, r3;
-            f32x2_split(rs4[0], r0, r1);
-            f32x2_split(rs4[1], r2, r3);
-            const float rs = (r0 + r1) + (r2 + r3);
+            float rs;
+            if (fast) rs = exp_row<kPolyEvery>(s, fa, m_use, pk);
+            else rs = exp_row<0>(s, fa, m_use, pk);
             tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
             l_run = l_run * alpha + rs;
 
@@ -543,6 +559,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
 }
 
+__global__ void exp2_poly_kernel(const float* x, float* y, long n) {
+    const long i = 2 * ((long)blockIdx.x * blockDim.x + threadIdx.x);
+    if (i >= n) return;
+    float y0, y1;
+    exp2_poly_x2(x[i], i + 1 < n ? x[i + 1] : 0.f, y0, y1);
+    y[i] = y0;
+    if (i + 1 < n) y[i + 1] = y1;
+}
+
 __global__ void empty_rows_kernel(__nv_bfloat16* o, float* lse, long rows, int D) {
     const long n = rows * D;
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -582,6 +607,13 @@ cudaError_t launch_empty_rows(void* o, float* lse, long rows, int D, cudaStream_
     const long blocks = (n + threads - 1) / threads < 4096 ? (n + threads - 1) / threads : 4096;
     empty_rows_kernel<<<(unsigned)blocks, threads, 0, stream>>>(reinterpret_cast<__nv_bfloat16*>(o), lse,
                                                                  rows, D);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_exp2_poly(const float* x, float* y, long n, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const long pairs = (n + 1) / 2;
+    exp2_poly_kernel<<<(unsigned)((pairs + 255) / 256), 256, 0, stream>>>(x, y, n);
     return cudaGetLastError();
 }
 

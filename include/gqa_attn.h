@@ -98,9 +98,14 @@ gqa_status attn_fwd_dense(const void* q, const void* k, const void* v,
  *            its contents on entry do not matter; calls that share one
  *            workspace must not overlap on the GPU.
  *
- * Caller obligations (not checked on the device; see attn_validate_paged):
- * the entries block_table[b, 0 .. ceil(L_b / page_size) - 1] lie in
- * [0, num_pages); later entries are never read (-1 is fine there).
+ * Caller obligations (attn_validate_paged checks them on the host): the
+ * entries block_table[b, 0 .. ceil(L_b / page_size) - 1] lie in
+ * [0, num_pages); later entries are never read (-1 is fine there).  The
+ * device does not report violations, but it never dereferences a page id
+ * outside [0, num_pages) (such rows read as zeros) and clamps lengths to
+ * [0, max_pages * page_size], so no memory outside the pool is touched; the
+ * results of such requests are unspecified.  num_pages * page_size must stay
+ * below 2^31 (GQA_ERR_UNSUPPORTED otherwise).
  */
 gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                              const int32_t* real_seqlen_kv, const int32_t* block_table,
@@ -168,6 +173,16 @@ const char* gqa_status_string(gqa_status status);
  * (clearing it) and GQA_OK otherwise.  Diagnostic, not for the hot path.
  */
 gqa_status gqa_device_error(void);
+
+/*
+ * Diagnostic: y[i] = 2^x[i] (device arrays of n floats) computed by the
+ * FMA-pipe exp2 routine the prefill kernel uses for part of its softmax
+ * exponentials (base-2 Cody-Waite reduction plus a fitted degree-4 minimax
+ * polynomial; relative error <= 2.7e-6 for x in [-125, 127], arguments below
+ * -126 clamped).  Exposed so the routine can be checked against exp2f; not
+ * part of the attention path.
+ */
+gqa_status gqa_exp2_poly(const float* x, float* y, long n, gqa_stream_t stream);
 
 /* Library version string. */
 const char* gqa_version(void);
