@@ -233,6 +233,12 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+def job_value(ideal_s_per_rank, step_s_max, world):
+    """Whole-job value: every rank ran the same step (replicas), so the job did
+    `world` times the work of one rank in the slowest rank's time."""
+    return 100.0 * world * ideal_s_per_rank / step_s_max
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -284,7 +290,7 @@ def bench_ours(args, world, rank, local):
     step_s = sum(statistics.mean(x) for x in per_part)
     step_s_max = max_over_ranks(step_s, world)
     ideal = sum(p.ideal_s(peaks) for p in parts)
-    value = 100.0 * world * ideal / step_s_max
+    value = job_value(ideal, step_s_max, world)
 
     detail = {}
     dom, dom_t = None, -1.0
@@ -349,7 +355,7 @@ def bench_e2e(args, parts, peaks, dev, stream, world):
             times.append(e0.elapsed_time(e1) / 1e3)
     t = max_over_ranks(statistics.mean(times), world)
     ideal = sum(p.ideal_s(peaks) for p in parts)
-    return dict(value=100.0 * world * ideal / t, unit=UNIT, ms_per_step=1e3 * t, h2d_bytes_per_step=h2d,
+    return dict(value=job_value(ideal, t, world), unit=UNIT, ms_per_step=1e3 * t, h2d_bytes_per_step=h2d,
                 d2h_bytes_per_step=d2h, steps=steps)
 
 

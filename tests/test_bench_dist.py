@@ -1,0 +1,66 @@
+"""The benchmark's multi-rank logic on CPU ranks (gloo, world size 2): the
+max-over-ranks timing, the barrier and the whole-job aggregation that
+`bench.py` uses when launched under torchrun.  No GPU."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w, r, lr = bench.dist_env()
+        assert (w, r, lr) == (world, rank, rank)
+        bench.barrier(world)
+        local = 0.010 + 0.005 * rank            # rank 1 is the slow one
+        t = bench.max_over_ranks(local, world)
+        out[rank] = t
+        out[world + rank] = bench.job_value(0.004, t, world)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_slowest_time():
+    world = 2
+    ctx = mp.get_context("spawn")
+    out = ctx.Array("d", 2 * world)
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, world, port, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == pytest.approx(0.015) and out[1] == pytest.approx(0.015)
+    # two replicas did twice the work of one in the slower rank's time
+    assert out[2] == pytest.approx(100.0 * 2 * 0.004 / 0.015)
+    assert out[2] == out[3]
+
+
+def test_single_rank_defaults():
+    assert bench.max_over_ranks(0.5, 1) == 0.5
+    assert bench.job_value(1.0, 2.0, 1) == pytest.approx(50.0)
+
+
+def test_visible_pairs_brute_force():
+    g = torch.Generator().manual_seed(0)
+    m = torch.rand(2, 37, generator=g) < 0.6
+    for causal in (True, False):
+        for Sq, Skv in ((37, 37), (10, 37), (40, 37)):
+            bf = sum(1 for b in range(2) for i in range(Sq) for j in range(Skv)
+                     if (not causal or j <= i + Skv - Sq) and m[b, j])
+            assert bf == bench.visible_pairs(2, Sq, Skv, causal, m[:, :Skv])
