@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libgqa_attn.so")
-SOURCES = ["api.cu", "prefill.cu", "decode.cu"]
+SOURCES = ["api.cu", "prefill.cu", "decode.cu", "decode_tc.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

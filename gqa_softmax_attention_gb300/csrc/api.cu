@@ -61,6 +61,27 @@ bool make_cache_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D
     return r == CUDA_SUCCESS;
 }
 
+// Paged cache as a 5-D map {64, 8, D / 64, pages * page_size / 8, Hkv}: the
+// token axis is split into 8-row groups, and the 64-column slices (128-byte
+// stride) sit between the row-in-group and group axes.  A {64, 8, D / 64,
+// box_tokens / 8, 1} box brings one page block of one head whole and lands in
+// shared memory as [group][slice][8 rows][128 bytes] (128-byte swizzle), so
+// consecutive boxes of a tile keep one uniform 8-row-group stride (D / 64 KB)
+// for every slice, which lets one MMA descriptor span the tile's 64 keys.
+bool make_cache_page_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D, int box_tokens) {
+    auto fn = encode_fn();
+    if (!fn || rows % 8 != 0 || box_tokens % 8 != 0) return false;
+    const cuuint64_t row_bytes = (cuuint64_t)Hkv * D * 2;
+    const cuuint64_t dims[5] = {64, 8, (cuuint64_t)(D / 64), (cuuint64_t)(rows / 8), (cuuint64_t)Hkv};
+    const cuuint64_t strides[4] = {row_bytes, 128, 8 * row_bytes, (cuuint64_t)D * 2};
+    const cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), (cuuint32_t)(box_tokens / 8), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -153,6 +174,16 @@ gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_c
     a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     a.chunk = p.chunk;
     a.max_splits = p.max_splits;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // KV groups of 32..128 query rows run on the tensor-core decode kernel.
+    const int g = Hq / Hkv;
+    if (num_pages > 0 && gqa::decode_tc_eligible(D, g * Sq, page_size)) {
+        const int tbox = gqa::decode_tc_box_tokens(page_size);
+        CUtensorMap tk, tv;
+        if (make_cache_page_map(&tk, k_cache, (long)num_pages * page_size, Hkv, D, tbox) &&
+            make_cache_page_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, tbox))
+            return gqa::launch_decode_tc(tk, tv, a, tbox, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    }
     // Pages that cut into 8-row multiples of the key tile are loaded by TMA;
     // other page sizes are gathered row by row.
     const int box = gqa::decode_box_tokens(D, page_size);
@@ -160,8 +191,7 @@ gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_c
     const bool use_tma = box > 0 && num_pages > 0 &&
                          make_cache_map(&tk, k_cache, (long)num_pages * page_size, Hkv, D, box) &&
                          make_cache_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, box);
-    return gqa::launch_decode(a, use_tma ? &tk : nullptr, use_tma ? &tv : nullptr, box,
-                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+    return gqa::launch_decode(a, use_tma ? &tk : nullptr, use_tma ? &tv : nullptr, box, st) == cudaSuccess
                ? GQA_OK
                : GQA_ERR_CUDA;
 }
@@ -207,8 +237,9 @@ gqa_status gqa_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
     const int e = gqa::prefill_take_device_error();
     const int d = gqa::decode_take_device_error();
-    if (e < 0 || d < 0) return GQA_ERR_CUDA;
-    return (e || d) ? GQA_ERR_TIMEOUT : GQA_OK;
+    const int t = gqa::decode_tc_take_device_error();
+    if (e < 0 || d < 0 || t < 0) return GQA_ERR_CUDA;
+    return (e || d || t) ? GQA_ERR_TIMEOUT : GQA_OK;
 }
 
 gqa_status gqa_exp2_poly(const float* x, float* y, long n, gqa_stream_t stream) {

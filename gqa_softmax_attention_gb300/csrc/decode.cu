@@ -599,9 +599,7 @@ cudaError_t launch_d(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtenso
         default: e = launch_split<D, 4>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
     }
     if (e != cudaSuccess) return e;
-    const long rows = (long)a.B * a.Sq * a.Hq;
-    decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(a, R, g);
-    return cudaGetLastError();
+    return launch_decode_combine(a, stream);
 }
 
 }  // namespace
@@ -617,7 +615,10 @@ bool plan_decode(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_p
                  DecodePlan* plan) {
     if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || page_size <= 0 || max_pages <= 0)
         return false;
-    const int TK = key_tile(D);
+    // Splits start on multiples of 64 tokens for every head dimension, so the
+    // 64-key tiles of decode_tc_kernel never straddle a page boundary.
+    const int TK = 64;
+    (void)D;
     const int g = Hq / Hkv;
     const long R = (long)g * Sq;
     const int mf = choose_mf((int)R);
@@ -644,6 +645,20 @@ bool plan_decode(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_p
     plan->part_lse_bytes = (size_t)B * Hkv * plan->max_splits * R * sizeof(float);
     plan->workspace_bytes = (plan->part_o_bytes + 255) / 256 * 256 + (plan->part_lse_bytes + 255) / 256 * 256;
     return true;
+}
+
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream) {
+    const int g = a.Hq / a.Hkv;
+    const int R = g * a.Sq;
+    const long rows = (long)a.B * a.Sq * a.Hq;
+    const unsigned blocks = (unsigned)((rows + 3) / 4);
+    switch (a.D) {
+        case 64: decode_combine_kernel<64><<<blocks, 128, 0, stream>>>(a, R, g); break;
+        case 128: decode_combine_kernel<128><<<blocks, 128, 0, stream>>>(a, R, g); break;
+        case 256: decode_combine_kernel<256><<<blocks, 128, 0, stream>>>(a, R, g); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int box_tokens,

@@ -1,0 +1,485 @@
+// Paged-KV decode on the 5th-generation tensor cores, for KV groups with many
+// query rows (g * Sq from 32 to 128 rows per KV head, e.g. the 24/2/D256
+// multi-query geometry of MATE "QSA").
+//
+// Same contract and workspace as the split kernels in decode.cu: request b's
+// logical token t lives in slot t % page_size of page block_table[b, t /
+// page_size]; query i sits at key position i + L_b - Sq (TileOPs "Attention
+// Operators", GQAPagedFwdOp / MHADecodePagedWithKVCacheFwdOp); each CTA
+// handles one split of one (request, KV head) and writes a normalised FP32
+// partial O and a base-2 LSE that decode_combine_kernel merges (MATE "QSA",
+// Core Attention, SplitKV).
+//
+// With 48 query rows and D = 256, warp-level MMAs need Q in registers split by
+// 16-row fragment, so every K and V element is read from shared memory once
+// per fragment; here the tensor core reads each operand once instead:
+//   warps 0-3  first copy the group's Q rows (packed i * g + hl, padding rows
+//              zero) from global memory into TMEM, where they are the A
+//              operand of S = Q K^T, so shared memory holds only the K/V rings;
+//   warp 4     TMA producer: 64-key K and V tiles, one 5-D box per page
+//              block (min(page tokens, 64) tokens, all D columns), each issued
+//              by its own lane: a single thread issuing many small boxes is
+//              the limit at small page sizes, and one box per block brings
+//              D / 64 times fewer boxes than one per 64-column slice.  Tiles
+//              are issued in the order the MMAs consume them (K0, K1, V0, K2,
+//              V1, ...) through 3-4 deep K and 4-6 deep V rings (about 200 KB
+//              in flight, which the memory latency at full bandwidth needs);
+//              block-table entries are read 32 at a time by the warp;
+//   warp 5     MMA issuer: S = Q K^T (M = 128 rows, N = 64 keys, Q from TMEM)
+//              into one of two TMEM buffers, O += P V with P read from TMEM
+//              (N = D, 16 keys per step); the descriptors are formed once per
+//              tile and stepped by constants, so issuing keeps pace with the
+//              tensor pipe;
+//   warps 0-3  then softmax, one row per thread (only warps holding a query
+//              row): running max and sum in base 2 with a lazy reference max
+//              (moved only when a tile max exceeds it by more than 2^8), P
+//              written over its S row, O rescaled when needed, then O / l and
+//              the LSE written to the workspace.
+// Rows past g * Sq in the 128-row M dimension are padding; their results are
+// never stored.  Value rows past the request's end are zeroed in shared
+// memory before P V reads them.  Every wait is bounded (ptx.cuh).
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace {
+
+__device__ int g_decode_tc_error;
+
+constexpr int BM = 128;            // TMEM lanes = padded query rows
+constexpr int BN = 64;             // keys per tile
+constexpr int NUM_THREADS = 192;   // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int WARP_LOAD = 4;
+constexpr int WARP_MMA = 5;
+constexpr float kRescaleThreshold = 8.f;
+
+template <int D>
+struct TCfg {
+    static constexpr int NSUB = D / 64;
+    // Shared-memory layout of a 64-key K or V tile: [8-key group][64-column
+    // slice][8 keys][128 bytes] (128-byte swizzle), as the 5-D page-block
+    // boxes land: the 8-row atoms of one slice are GROUP_STRIDE apart across
+    // the whole tile, whatever the page size.
+    static constexpr int GROUP_STRIDE = NSUB * 1024;
+    static constexpr int KV_TILE = NSUB * BN * 128;
+    // Q is held in TMEM, so shared memory is all K/V ring: about 200 KB in
+    // flight per SM covers the memory latency at full bandwidth.  V tiles are
+    // consumed about two tiles after their K (P V follows the softmax), so the
+    // V ring is deeper.
+    static constexpr int NK = D == 256 ? 3 : 4;
+    static constexpr int NV = D == 256 ? 4 : 6;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + NK * KV_TILE;
+    static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
+    // q_ready, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done, drain
+    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 1 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    // TMEM: S0 | S1 | O | Q (Q rows as bf16 pairs, the A operand of S = Q K^T)
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN, COL_Q = 2 * BN + D;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t IDESC_QK = make_idesc_bf16(BM, BN, false, false);
+    static constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, D, false, true);
+    static_assert(COL_Q + D / 2 <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// One 64-column row per thread (two loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+    tmem_ld32(taddr, v);
+    tmem_ld32(taddr + 32, v + 32);
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 const DecodeArgs a, int R, int g, int box_tokens) {
+    using C = TCfg<D>;
+    const int split = blockIdx.x;
+    const int hkv = blockIdx.y;
+    const int b = blockIdx.z;
+    const int L = min(max(a.seqlens[b], 0), a.max_pages * a.page_size);
+    const int t_begin = split * a.chunk;
+    if (t_begin >= L) return;                      // nothing here; the combine skips it
+    const int t_end = min(L, t_begin + a.chunk);
+    const int n_tiles = (t_end - t_begin + BN - 1) / BN;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int n_sm_warps = (R + 31) / 32;          // softmax warps that hold a query row
+
+    const uint32_t bar0 = sb + C::OFF_BAR;
+    const uint32_t q_ready = bar0;
+    auto k_full = [&](int i) { return bar0 + 8u * (1 + i); };
+    auto k_empty = [&](int i) { return bar0 + 8u * (1 + C::NK + i); };
+    auto v_full = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + i); };
+    auto v_empty = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + C::NV + i); };
+    auto s_full = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + i); };
+    auto p_full = [&](int i) { return bar0 + 8u * (3 + 2 * C::NK + 2 * C::NV + i); };
+    const uint32_t o_done = bar0 + 8u * (5 + 2 * C::NK + 2 * C::NV);
+    const uint32_t drain = bar0 + 8u * (6 + 2 * C::NK + 2 * C::NV);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_ready, BM);
+        for (int i = 0; i < C::NK; ++i) { mbar_init(k_full(i), 1); mbar_init(k_empty(i), 1); }
+        for (int i = 0; i < C::NV; ++i) { mbar_init(v_full(i), 1); mbar_init(v_empty(i), 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(s_full(i), 1); mbar_init(p_full(i), 32 * n_sm_warps); }
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == WARP_LOAD) {
+        // ------------------------------------------------------------ producer
+        const int32_t* trow = a.table + (size_t)b * a.max_pages;
+        const int nbox = BN / box_tokens;          // page blocks per tile; lane i loads block i
+        const uint32_t blk_bytes = (uint32_t)box_tokens * 128 * C::NSUB;
+        int win = -(1 << 30), pid = -1;            // block-table window: entry win + lane
+        int nk = 0, nv = 0;
+        bool ok = true;
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+        }
+        // Loads are issued in the order the MMAs consume them: K0, K1, V0, K2,
+        // V1, ...  Lane i finds the first cache row of page block i of a tile
+        // when the tile's K is issued (-1: not loaded) and keeps it, for two
+        // tiles, for the tile's V.
+        int row_ring0 = -1, row_ring1 = -1, n_ring0 = 0, n_ring1 = 0;
+        auto find_rows = [&](int it) {
+            const int t = t_begin + it * BN + lane * box_tokens;
+            const int lp = t / a.page_size;
+            const int lp_first = __shfl_sync(0xffffffffu, lp, 0);
+            const int lp_last = __shfl_sync(0xffffffffu, lp, nbox - 1);
+            if (lp_last - win >= 32 || lp_first < win) {   // warp-uniform refill of the window
+                win = lp_first;
+                pid = win + lane < a.max_pages ? trow[win + lane] : -1;
+            }
+            const int page = __shfl_sync(0xffffffffu, pid, (lp - win) & 31);
+            int row = -1;
+            // a page id outside the pool (a caller error) is not loaded
+            if (lane < nbox && t < t_end && page >= 0 && page < a.num_pages)
+                row = page * a.page_size + t % a.page_size;
+            const int n = __popc(__ballot_sync(0xffffffffu, row >= 0));
+            if (it & 1) { row_ring1 = row; n_ring1 = n; } else { row_ring0 = row; n_ring0 = n; }
+        };
+        auto load = [&](int it, bool is_v) -> bool {   // whole warp
+            const int row = (it & 1) ? row_ring1 : row_ring0;
+            const int n = (it & 1) ? n_ring1 : n_ring0;
+            const int cnt = is_v ? nv : nk;
+            const int ring = is_v ? C::NV : C::NK;
+            const int slot = cnt % ring;
+            const uint32_t empty_bar = is_v ? v_empty(slot) : k_empty(slot);
+            const uint32_t full_bar = is_v ? v_full(slot) : k_full(slot);
+            bool ok = true;
+            if (lane == 0) {
+                ok = mbar_wait(empty_bar, ((cnt / ring) & 1) ^ 1, abort_flag);
+                if (ok) mbar_arrive_expect_tx(full_bar, (uint32_t)n * blk_bytes);
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+            __syncwarp();                          // the expect-tx precedes every lane's copy
+            const uint32_t dst = sb + (is_v ? C::OFF_V : C::OFF_K) + slot * C::KV_TILE + lane * blk_bytes;
+            const void* map = is_v ? (const void*)&tm_v : (const void*)&tm_k;
+            if (row >= 0) tma_load_5d(dst, map, full_bar, 0, 0, 0, row / 8, hkv);
+            if (is_v) ++nv; else ++nk;
+            return true;
+        };
+        find_rows(0);
+        ok = load(0, false);
+        for (int it = 0; it < n_tiles && ok; ++it) {
+            if (it + 1 < n_tiles) {
+                find_rows(it + 1);
+                ok = load(it + 1, false);
+                if (!ok) break;
+            }
+            ok = load(it, true);
+        }
+        if (lane == 0) {
+            if (*abort_flag) {
+                for (int s = 0; s < C::NK && s < nk; ++s) {
+                    const int last = nk - 1 - ((nk - 1 - s) % C::NK);
+                    mbar_drain(k_full(s), (last / C::NK) & 1);
+                }
+                for (int s = 0; s < C::NV && s < nv; ++s) {
+                    const int last = nv - 1 - ((nv - 1 - s) % C::NV);
+                    mbar_drain(v_full(s), (last / C::NV) & 1);
+                }
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------------------ MMA issuer (lane 0 issues)
+        auto issue_qk = [&](int i) -> bool {
+            const int ks = i % C::NK;
+            if (!__all_sync(0xffffffffu, mbar_wait(k_full(ks), (i / C::NK) & 1, abort_flag))) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t d = tmem + ((i & 1) ? C::COL_S1 : C::COL_S0);
+                // K-major B: 8-key atoms GROUP_STRIDE apart; step kk moves 32 bytes
+                // within a slice, every fourth step to the next slice (1 KB on)
+                const uint64_t kdesc = make_sdesc_sw128(sb + C::OFF_K + ks * C::KV_TILE, 16, C::GROUP_STRIDE);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16_ts(d, tmem + C::COL_Q + kk * 8,
+                                kdesc + (uint64_t)((((kk / 4) * 1024 + (kk % 4) * 32)) >> 4), C::IDESC_QK,
+                                kk > 0 ? 1u : 0u);
+                mma_commit(s_full(i & 1));
+                mma_commit(k_empty(ks));
+            }
+            __syncwarp();
+            return true;
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag));
+        if (ok) tc_fence_after();
+        if (ok) ok = issue_qk(0);
+        if (ok && n_tiles > 1) ok = issue_qk(1);
+        for (int i = 0; i < n_tiles && ok; ++i) {
+            ok = __all_sync(0xffffffffu, mbar_wait(p_full(i & 1), (i >> 1) & 1, abort_flag));
+            if (!ok) break;
+            const int vs = i % C::NV;
+            ok = __all_sync(0xffffffffu, mbar_wait(v_full(vs), (i / C::NV) & 1, abort_flag));
+            if (!ok) break;
+            const uint32_t vb = sb + C::OFF_V + vs * C::KV_TILE;
+            const int nvalid = t_end - (t_begin + i * BN);
+            if (nvalid < BN) {
+                // Value rows past the request's end hold stale data: zero them
+                // before the tensor core reads the tile.
+                for (int idx = lane; idx < (BN - nvalid) * 8 * C::NSUB; idx += 32) {
+                    const int key = nvalid + idx / (8 * C::NSUB);
+                    const int s = (idx / 8) % C::NSUB, chunk = idx % 8;
+                    *reinterpret_cast<uint4*>(smem + (vb - sb) + (key / 8) * C::GROUP_STRIDE + s * 1024 +
+                                              (key % 8) * 128 + chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t pcol = (i & 1) ? C::COL_S1 : C::COL_S0;
+                // MN-major B: 64-column slices 1 KB apart, 8-key atoms GROUP_STRIDE
+                // apart; step kk takes keys 16kk..16kk+15 (two atoms)
+                const uint64_t vdesc = make_sdesc_sw128(vb, 1024, C::GROUP_STRIDE);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_bf16_ts(tmem + C::COL_O, tmem + pcol + kk * 8,
+                                vdesc + (uint64_t)((2 * kk * C::GROUP_STRIDE) >> 4), C::IDESC_PV,
+                                (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(o_done);
+                mma_commit(v_empty(vs));
+            }
+            __syncwarp();
+            // S of tile i+2 overwrites P of tile i: issued after its P V.
+            if (i + 2 < n_tiles) ok = issue_qk(i + 2);
+        }
+        if (lane == 0) {
+            mma_commit(drain);                    // every MMA issued above has completed once this arrives
+            mbar_drain(drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ warps 0-3: Q rows into TMEM
+        // Row r = i * g + hl is query i of head hkv * g + hl; rows past g * Sq are zero.
+        {
+            const int r = warp * 32 + lane;
+            const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+            const uint4* src = nullptr;
+            if (r < R)
+                src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                                     (((size_t)b * a.Sq + r / g) * a.Hq + hkv * g + r % g) * D);
+#pragma unroll 1
+            for (int c = 0; c < D / 64; ++c) {          // 32 columns (64 values) at a time
+                uint32_t w[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint4 v = src ? __ldg(src + 8 * c + e) : make_uint4(0u, 0u, 0u, 0u);
+                    w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
+                }
+                tmem_st32(tmem + lane_addr + C::COL_Q + 32 * c, w);
+            }
+            tc_fence_before();
+            mbar_arrive(q_ready);
+        }
+    }
+    if (warp < n_sm_warps) {
+        // ------------------------------------------------------------ softmax warps
+        const int r = warp * 32 + lane;            // padded row == TMEM lane
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const bool row_ok = r < R;
+        int lim = 0;                               // exclusive visibility limit of this row
+        if (row_ok) lim = a.causal ? (int)min((long)t_end, (long)(r / g) + L - a.Sq + 1) : t_end;
+        // keys below lim_first are visible to every row of the group
+        const int lim_first = a.causal ? (int)max((long)t_begin, min((long)t_end, (long)L - a.Sq + 1)) : t_end;
+        const float sl = a.scale_log2;
+        float m_ref = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int it = 0; it < n_tiles; ++it) {
+            const int t0 = t_begin + it * BN;
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full(it & 1), (it >> 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t scol = (it & 1) ? C::COL_S1 : C::COL_S0;
+            float s[BN];
+            tmem_ld64(tmem + lane_addr + scol, s);
+            const bool fast = t0 + BN <= lim_first && sl > 0.f;
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+            if (fast) {
+#pragma unroll
+                for (int c = 0; c < BN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const float x = t0 + c < lim ? s[c] * sl : -INFINITY;   // the select drops stale rows
+                    s[c] = x;
+                    mx8[c & 7] = fmaxf(mx8[c & 7], x);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + 4]);
+            const float mx_raw = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+            const float mx = fast ? mx_raw * sl : mx_raw;
+            float alpha = 1.f;
+            if (mx > m_ref + kRescaleThreshold) {
+                alpha = fast_exp2(m_ref - mx);
+                m_ref = mx;
+            }
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            const uint64_t fa2 = f32x2(fast ? sl : 1.f, fast ? sl : 1.f);
+            const uint64_t nm2 = f32x2(-m_use, -m_use);
+            uint64_t rs4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) rs4[e] = f32x2(0.f, 0.f);
+            uint32_t pk[BN / 2];
+#pragma unroll
+            for (int c = 0; c < BN / 2; ++c) {
+                float x0, x1;
+                f32x2_split(ffma2(f32x2(s[2 * c], s[2 * c + 1]), fa2, nm2), x0, x1);
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                rs4[c & 3] = fadd2(rs4[c & 3], f32x2(p0, p1));
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            rs4[0] = fadd2(rs4[0], rs4[2]);
+            rs4[1] = fadd2(rs4[1], rs4[3]);
+            float r0, r1, r2, r3;
+            f32x2_split(rs4[0], r0, r1);
+            f32x2_split(rs4[1], r2, r3);
+            l_run = l_run * alpha + ((r0 + r1) + (r2 + r3));
+            tmem_st32(tmem + lane_addr + scol, pk);          // P over the first 32 columns of S
+            if (it > 0) {
+                // O must hold P V of the previous tile before it is rescaled
+                ok = __all_sync(0xffffffffu, mbar_wait(o_done, (it - 1) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(tmem + lane_addr + C::COL_O + 32 * c, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(tmem + lane_addr + C::COL_O + 32 * c, reinterpret_cast<uint32_t*>(o));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(p_full(it & 1));
+        }
+        if (ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait(o_done, (n_tiles - 1) & 1, abort_flag));
+            if (ok) tc_fence_after();
+        }
+        const size_t part_row = ((size_t)(b * a.Hkv + hkv) * a.max_splits + split) * R + r;
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            if (ok) tmem_ld32(tmem + lane_addr + C::COL_O + 32 * c, o);
+            if (row_ok) {
+                float4* dst = reinterpret_cast<float4*>(a.part_o + part_row * D + 32 * c);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = ok ? make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv,
+                                              o[4 * e + 3] * inv)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        if (row_ok) a.part_lse[part_row] = (ok && l_run > 0.f) ? m_ref + log2f(l_run) : -INFINITY;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_decode_tc_error, (int)kErrDecodeWait);
+}
+
+template <int D>
+cudaError_t launch_t(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecodeArgs& a,
+                     int box_tokens, cudaStream_t stream) {
+    using C = TCfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int g = a.Hq / a.Hkv;
+    const int R = g * a.Sq;
+    dim3 grid(a.max_splits, a.Hkv, a.B);
+    decode_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_k, tm_v, a, R, g, box_tokens);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tc_eligible(int D, int R, int page_size) {
+    return (D == 128 || D == 256) && R >= 32 && R <= BM && decode_tc_box_tokens(page_size) > 0;
+}
+
+int decode_tc_box_tokens(int page_size) {
+    // page blocks of 8..64 tokens (whole 8-row groups) that tile both a page
+    // and a 64-key tile
+    const int bt = page_size < BN ? page_size : BN;
+    if (bt % 8 != 0 || page_size % bt != 0 || BN % bt != 0) return 0;
+    return bt;
+}
+
+cudaError_t launch_decode_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                             const DecodeArgs& a, int box_tokens, cudaStream_t stream) {
+    cudaError_t e;
+    switch (a.D) {
+        case 128: e = launch_t<128>(tm_k, tm_v, a, box_tokens, stream); break;
+        case 256: e = launch_t<256>(tm_k, tm_v, a, box_tokens, stream); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    return launch_decode_combine(a, stream);
+}
+
+int decode_tc_take_device_error() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_tc_error, sizeof(int)) != cudaSuccess) return -1;
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_decode_tc_error, &zero, sizeof(int));
+    }
+    return v;
+}
+
+}  // namespace gqa

@@ -61,5 +61,16 @@ int decode_box_tokens(int D, int page_size);
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int box_tokens,
                           cudaStream_t stream);
 int decode_take_device_error();
+// Merge of the split partials (decode_combine_kernel).
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream);
+
+// Tensor-core decode (decode_tc.cu) for 32..128 packed query rows per KV head.
+bool decode_tc_eligible(int D, int R, int page_size);
+int decode_tc_box_tokens(int page_size);
+// tm_k / tm_v: the caches as {64, 8, D / 64, pages * page_size / 8, Hkv} with a
+// {64, 8, D / 64, box_tokens / 8, 1} box (one page block of one head per box).
+cudaError_t launch_decode_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecodeArgs& a,
+                             int box_tokens, cudaStream_t stream);
+int decode_tc_take_device_error();
 
 }  // namespace gqa

@@ -53,6 +53,11 @@ SMALL = [
     (2, 5, 16, 1, 64, 8, [90, 260]),                 # 80 rows: two row blocks
     (1, 1, 2, 1, 256, 32, [5000]),                   # one long request, many splits
     (3, 3, 6, 2, 128, 16, [2, 3, 4]),                # 9 rows, L around Sq
+    # 32..128 packed rows per KV head: the tensor-core decode kernel
+    (3, 4, 16, 2, 128, 32, [4100, 3, 700]),          # 32 rows, L < Sq, ragged tail
+    (2, 4, 32, 1, 128, 16, [129, 2000]),             # 128 rows
+    (4, 2, 48, 1, 256, 64, [64, 65, 0, 999]),        # 96 rows, empty request, one-key tile
+    (2, 4, 24, 2, 256, 8, [1, 5000]),                # 48 rows, 8-token pages
 ]
 
 
@@ -66,8 +71,10 @@ def test_small_shapes(g, case):
     compare(o, lse, ro, rl, str(case))
 
 
-def test_non_causal_and_scale(g):
-    p = W.paged_inputs(3, 4, 8, 2, 128, 16, lengths=[10, 0, 77], seed=3)
+@pytest.mark.parametrize("shape", [(3, 4, 8, 2, 128, 16), (2, 4, 24, 2, 256, 16)], ids=["rows16", "rows48"])
+def test_non_causal_and_scale(g, shape):
+    B, Sq, Hq, Hkv, D, ps = shape
+    p = W.paged_inputs(B, Sq, Hq, Hkv, D, ps, lengths=[10, 0, 77][:B] if B == 3 else [300, 17], seed=3)
     o, lse = run(g, p, causal=False, scale=0.05)
     ro, rl = oracle.attn_paged(p["q"], p["k_cache"], p["v_cache"], p["real_seqlen_kv"], p["block_table"],
                                causal=False, scale=0.05)
