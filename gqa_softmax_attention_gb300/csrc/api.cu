@@ -174,15 +174,27 @@ gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_c
     a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     a.chunk = p.chunk;
     a.max_splits = p.max_splits;
+    a.seg_table = nullptr;
+    a.n_part = 0;
+    a.tc_grid = 0;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // KV groups of 32..128 query rows run on the tensor-core decode kernel.
-    const int g = Hq / Hkv;
-    if (num_pages > 0 && gqa::decode_tc_eligible(D, g * Sq, page_size)) {
+    // KV groups of 32..128 query rows run on the balanced tensor-core decode
+    // kernel, whose workspace holds per-piece partials and the segment table.
+    if (num_pages > 0 && p.tc) {
         const int tbox = gqa::decode_tc_box_tokens(page_size);
         CUtensorMap tk, tv;
         if (make_cache_page_map(&tk, k_cache, (long)num_pages * page_size, Hkv, D, tbox) &&
-            make_cache_page_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, tbox))
+            make_cache_page_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, tbox)) {
+            char* ws = static_cast<char*>(workspace);
+            const size_t o_bytes = (p.tc_part_o_bytes + 255) / 256 * 256;
+            const size_t l_bytes = (p.tc_part_lse_bytes + 255) / 256 * 256;
+            a.part_o = reinterpret_cast<float*>(ws);
+            a.part_lse = reinterpret_cast<float*>(ws + o_bytes);
+            a.seg_table = reinterpret_cast<int*>(ws + o_bytes + l_bytes);
+            a.n_part = p.n_part;
+            a.tc_grid = p.tc_grid;
             return gqa::launch_decode_tc(tk, tv, a, tbox, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+        }
     }
     // Pages that cut into 8-row multiples of the key tile are loaded by TMA;
     // other page sizes are gathered row by row.

@@ -513,8 +513,25 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
     const int b = (int)(row / ((long)a.Hq * a.Sq));
     const int hkv = h / g, r = i * g + h % g;
     const int L = min(max(a.seqlens[b], 0), a.max_pages * a.page_size);
-    const int n = L > 0 ? (L + a.chunk - 1) / a.chunk : 0;
-    const size_t base = (size_t)(b * a.Hkv + hkv) * a.max_splits * R + r;
+    int n;
+    size_t base;
+    if (a.seg_table) {
+        // balanced path: the segment's pieces have consecutive ids (entries
+        // outside the partial slots, possible only after a kernel gave up
+        // waiting, read as no pieces)
+        const int s = b * a.Hkv + hkv;
+        int id0 = 0;
+        n = 0;
+        if (L > 0) {
+            id0 = a.seg_table[2 * s];
+            n = a.seg_table[2 * s + 1];
+            if (id0 < 0 || n < 0 || (long)id0 + n > a.n_part) id0 = n = 0;
+        }
+        base = (size_t)id0 * R + r;
+    } else {
+        n = L > 0 ? (L + a.chunk - 1) / a.chunk : 0;
+        base = (size_t)(b * a.Hkv + hkv) * a.max_splits * R + r;
+    }
 
     float M = -INFINITY;
     for (int s = lane; s < n; s += 32) M = fmaxf(M, a.part_lse[base + (size_t)s * R]);
@@ -644,6 +661,21 @@ bool plan_decode(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_p
     plan->part_o_bytes = (size_t)B * Hkv * plan->max_splits * R * D * sizeof(float);
     plan->part_lse_bytes = (size_t)B * Hkv * plan->max_splits * R * sizeof(float);
     plan->workspace_bytes = (plan->part_o_bytes + 255) / 256 * 256 + (plan->part_lse_bytes + 255) / 256 * 256;
+    // The balanced tensor-core path: one partial per (segment, CTA) piece, at
+    // most B * Hkv + grid of them, and a 2-int entry per segment.
+    plan->tc = decode_tc_eligible(D, (int)R, page_size) &&
+               (long)B * Hkv * ((cap + 63) / 64) < (1L << 31) && (long)B * Hkv + num_sms < (1L << 24);
+    if (plan->tc) {
+        plan->tc_grid = num_sms > 0 ? num_sms : 148;
+        plan->n_part = B * Hkv + plan->tc_grid;
+        plan->tc_part_o_bytes = (size_t)plan->n_part * R * D * sizeof(float);
+        plan->tc_part_lse_bytes = (size_t)plan->n_part * R * sizeof(float);
+        plan->tc_table_bytes = (size_t)B * Hkv * 2 * sizeof(int);
+        const size_t tc_bytes = (plan->tc_part_o_bytes + 255) / 256 * 256 +
+                                (plan->tc_part_lse_bytes + 255) / 256 * 256 +
+                                (plan->tc_table_bytes + 255) / 256 * 256;
+        if (tc_bytes > plan->workspace_bytes) plan->workspace_bytes = tc_bytes;
+    }
     return true;
 }
 

@@ -2,18 +2,30 @@
 // query rows (g * Sq from 32 to 128 rows per KV head, e.g. the 24/2/D256
 // multi-query geometry of MATE "QSA").
 //
-// Same contract and workspace as the split kernels in decode.cu: request b's
-// logical token t lives in slot t % page_size of page block_table[b, t /
-// page_size]; query i sits at key position i + L_b - Sq (TileOPs "Attention
-// Operators", GQAPagedFwdOp / MHADecodePagedWithKVCacheFwdOp); each CTA
-// handles one split of one (request, KV head) and writes a normalised FP32
-// partial O and a base-2 LSE that decode_combine_kernel merges (MATE "QSA",
-// Core Attention, SplitKV).
+// Contract as in decode.cu: request b's logical token t lives in slot
+// t % page_size of page block_table[b, t / page_size]; query i sits at key
+// position i + L_b - Sq (TileOPs "Attention Operators", GQAPagedFwdOp /
+// MHADecodePagedWithKVCacheFwdOp).  Partial results are merged by their LSE
+// as in MATE "QSA", Core Attention, SplitKV.
+//
+// Work is balanced, not split per request: the (request, KV head) segments,
+// request-major, are laid end to end as one sequence of 64-key tiles, and a
+// persistent grid of one CTA per SM takes equal contiguous ranges of it.  A
+// CTA's range crosses segment boundaries; the K/V pipeline runs straight
+// through them, and only the query rows, the running softmax state and the
+// output accumulator change.  Each (segment, CTA) piece writes a normalised
+// FP32 partial O and a base-2 LSE under partial id segment + CTA (unique: the
+// pieces form a staircase), and the CTA that holds a segment's first tile
+// records the segment's first id and piece count for decode_combine_kernel.
+// One CTA per SM means no refill of the pipeline between work units and no
+// partly filled last wave.
 //
 // With 48 query rows and D = 256, warp-level MMAs need Q in registers split by
 // 16-row fragment, so every K and V element is read from shared memory once
 // per fragment; here the tensor core reads each operand once instead:
-//   warps 0-3  first copy the group's Q rows (packed i * g + hl, padding rows
+//   warp 4     (before the main loop) sums the tiles of all segments and finds
+//              where this CTA's range starts;
+//   warps 0-3  copy the first piece's Q rows (packed i * g + hl, padding rows
 //              zero) from global memory into TMEM, where they are the A
 //              operand of S = Q K^T, so shared memory holds only the K/V rings;
 //   warp 4     TMA producer: 64-key K and V tiles, one 5-D box per page
@@ -27,17 +39,18 @@
 //              block-table entries are read 32 at a time by the warp;
 //   warp 5     MMA issuer: S = Q K^T (M = 128 rows, N = 64 keys, Q from TMEM)
 //              into one of two TMEM buffers, O += P V with P read from TMEM
-//              (N = D, 16 keys per step); the descriptors are formed once per
-//              tile and stepped by constants, so issuing keeps pace with the
-//              tensor pipe;
-//   warps 0-3  then softmax, one row per thread (only warps holding a query
-//              row): running max and sum in base 2 with a lazy reference max
-//              (moved only when a tile max exceeds it by more than 2^8), P
-//              written over its S row, O rescaled when needed, then O / l and
-//              the LSE written to the workspace.
+//              (N = D, 16 keys per step, a fresh accumulator at each piece);
+//              the descriptors are formed once per tile and stepped by
+//              constants, so issuing keeps pace with the tensor pipe;
+//   warps 0-3  softmax, one row per thread (only warps holding a query row):
+//              running max and sum in base 2 with a lazy reference max (moved
+//              only when a tile max exceeds it by more than 2^8), P written
+//              over its S row, O rescaled when needed; at the end of a piece
+//              the next piece's Q rows go into TMEM (prefetched to L2 one tile
+//              earlier), then O / l and the LSE are written to the workspace.
 // Rows past g * Sq in the 128-row M dimension are padding; their results are
-// never stored.  Value rows past the request's end are zeroed in shared
-// memory before P V reads them.  Every wait is bounded (ptx.cuh).
+// never stored.  Value rows past a request's end are zeroed in shared memory
+// before P V reads them.  Every wait is bounded (ptx.cuh).
 #include <cmath>
 
 #include "internal.h"
@@ -73,10 +86,11 @@ struct TCfg {
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + NK * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
-    // q_ready, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done, drain
-    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 1 + 1;
+    // q_ready, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
+    // p_full[2], o_done, drain, q_next
+    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 1 + 1 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
     // TMEM: S0 | S1 | O | Q (Q rows as bf16 pairs, the A operand of S = Q K^T)
     static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN, COL_Q = 2 * BN + D;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -86,10 +100,62 @@ struct TCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
+// Where this CTA's range of the tile sequence starts and ends (shared memory).
+struct Range {
+    int g0, n;        // first global tile, tiles in the range
+    int per;          // tiles per CTA
+    int s0, lt0;      // segment and tile within it of the first tile
+};
+
+// A position in the tile sequence: segment s = b * Hkv + h holds
+// ceil(L_b / 64) tiles; lt is the tile within the segment.
+struct Cursor {
+    int s, b, h, L, nt, lt;
+    __device__ __forceinline__ void set(const DecodeArgs& a, int seg) {
+        s = seg;
+        b = seg / a.Hkv;
+        h = seg % a.Hkv;
+        L = seg < a.B * a.Hkv ? min(max(a.seqlens[b], 0), a.max_pages * a.page_size) : 0;
+        nt = (L + BN - 1) / BN;
+    }
+    // The next tile, skipping empty segments (never past the last segment).
+    __device__ __forceinline__ void next(const DecodeArgs& a) {
+        if (++lt < nt) return;
+        lt = 0;
+        const int n_seg = a.B * a.Hkv;
+        do {
+            set(a, s + 1);
+        } while (nt == 0 && s + 1 < n_seg);
+    }
+};
+
 // One 64-column row per thread (two loads, one wait).
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
     tmem_ld32(taddr, v);
     tmem_ld32(taddr + 32, v + 32);
+}
+
+__device__ __forceinline__ int request_tiles(const DecodeArgs& a, int b) {
+    return b < a.B ? (min(max(a.seqlens[b], 0), a.max_pages * a.page_size) + BN - 1) / BN : 0;
+}
+
+// Query row r of (b, h) (bf16 [B, Sq, Hq, D]) into this thread's TMEM lane,
+// columns COL_Q.., zeros for padding rows; the whole warp calls it.
+template <int D>
+__device__ __forceinline__ void q_row_to_tmem(const DecodeArgs& a, uint32_t taddr, int r, int R, int g, int b,
+                                              int h) {
+    const uint4* src = nullptr;
+    if (r < R)
+        src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                             (((size_t)b * a.Sq + r / g) * a.Hq + h * g + r % g) * D);
+    uint32_t w[D / 2];
+#pragma unroll
+    for (int e = 0; e < D / 8; ++e) {
+        const uint4 v = src ? __ldg(src + e) : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
+    }
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) tmem_st32(taddr + 32 * c, w + 32 * c);
 }
 
 template <int D>
@@ -97,14 +163,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const DecodeArgs a, int R, int g, int box_tokens) {
     using C = TCfg<D>;
-    const int split = blockIdx.x;
-    const int hkv = blockIdx.y;
-    const int b = blockIdx.z;
-    const int L = min(max(a.seqlens[b], 0), a.max_pages * a.page_size);
-    const int t_begin = split * a.chunk;
-    if (t_begin >= L) return;                      // nothing here; the combine skips it
-    const int t_end = min(L, t_begin + a.chunk);
-    const int n_tiles = (t_end - t_begin + BN - 1) / BN;
+    const int cta = blockIdx.x;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -124,8 +183,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     auto p_full = [&](int i) { return bar0 + 8u * (3 + 2 * C::NK + 2 * C::NV + i); };
     const uint32_t o_done = bar0 + 8u * (5 + 2 * C::NK + 2 * C::NV);
     const uint32_t drain = bar0 + 8u * (6 + 2 * C::NK + 2 * C::NV);
+    const uint32_t q_next = bar0 + 8u * (7 + 2 * C::NK + 2 * C::NV);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    Range* range = reinterpret_cast<Range*>(smem + C::OFF_MISC + 16);
 
     if (threadIdx.x == 0) {
         mbar_init(q_ready, BM);
@@ -134,9 +195,54 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         for (int i = 0; i < 2; ++i) { mbar_init(s_full(i), 1); mbar_init(p_full(i), 32 * n_sm_warps); }
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
+        mbar_init(q_next, 32 * n_sm_warps);
         *abort_flag = 0;
         fence_mbar_init();
     }
+    if (warp == WARP_LOAD) {
+        // This CTA's range: tiles [cta * per, min((cta + 1) * per, T)) of the T
+        // tiles of all segments, per = ceil(T / grid).
+        long T = 0;
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+            int n = request_tiles(a, b0 + lane);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+            T += n;
+        }
+        T *= a.Hkv;
+        const long per = (T + gridDim.x - 1) / gridDim.x;
+        const long g0 = (long)cta * per;
+        const long g1 = min(g0 + per, T);
+        Range rg{(int)g0, (int)max(0L, g1 - g0), (int)per, 0, 0};
+        if (g1 > g0) {
+            long before = 0;   // tiles of the requests before b0, all heads
+            for (int b0 = 0; b0 < a.B; b0 += 32) {
+                const int n = request_tiles(a, b0 + lane);
+                int incl = n;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const unsigned hit = __ballot_sync(0xffffffffu, before + (long)incl * a.Hkv > g0);
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    const int nb = __shfl_sync(0xffffffffu, n, l);
+                    const long start = before + (long)(__shfl_sync(0xffffffffu, incl, l) - nb) * a.Hkv;
+                    const int off = (int)(g0 - start);
+                    rg.s0 = (b0 + l) * a.Hkv + off / nb;
+                    rg.lt0 = off % nb;
+                    break;
+                }
+                before += (long)__shfl_sync(0xffffffffu, incl, 31) * a.Hkv;
+            }
+        }
+        if (lane == 0) *range = rg;
+    }
+    __syncthreads();
+    const Range rg = *range;
+    const int n = rg.n;
+    if (n == 0) return;                            // nothing here (uniform)
     if (warp == WARP_MMA) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
@@ -148,23 +254,30 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     if (warp == WARP_LOAD) {
         // ------------------------------------------------------------ producer
-        const int32_t* trow = a.table + (size_t)b * a.max_pages;
         const int nbox = BN / box_tokens;          // page blocks per tile; lane i loads block i
         const uint32_t blk_bytes = (uint32_t)box_tokens * 128 * C::NSUB;
-        int win = -(1 << 30), pid = -1;            // block-table window: entry win + lane
+        int win = -(1 << 30), pid = -1, win_b = -1;   // block-table window of request win_b
         int nk = 0, nv = 0;
         bool ok = true;
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
         }
+        Cursor cur;
+        cur.set(a, rg.s0);
+        cur.lt = rg.lt0;
         // Loads are issued in the order the MMAs consume them: K0, K1, V0, K2,
         // V1, ...  Lane i finds the first cache row of page block i of a tile
         // when the tile's K is issued (-1: not loaded) and keeps it, for two
-        // tiles, for the tile's V.
-        int row_ring0 = -1, row_ring1 = -1, n_ring0 = 0, n_ring1 = 0;
-        auto find_rows = [&](int it) {
-            const int t = t_begin + it * BN + lane * box_tokens;
+        // tiles, for the tile's V, with the tile's KV head.
+        int row_ring0 = -1, row_ring1 = -1, n_ring0 = 0, n_ring1 = 0, h_ring0 = 0, h_ring1 = 0;
+        auto find_rows = [&](int it) {             // tile `it` is at `cur`
+            if (cur.b != win_b) {
+                win_b = cur.b;
+                win = -(1 << 30);
+            }
+            const int32_t* trow = a.table + (size_t)cur.b * a.max_pages;
+            const int t = cur.lt * BN + lane * box_tokens;
             const int lp = t / a.page_size;
             const int lp_first = __shfl_sync(0xffffffffu, lp, 0);
             const int lp_last = __shfl_sync(0xffffffffu, lp, nbox - 1);
@@ -175,14 +288,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const int page = __shfl_sync(0xffffffffu, pid, (lp - win) & 31);
             int row = -1;
             // a page id outside the pool (a caller error) is not loaded
-            if (lane < nbox && t < t_end && page >= 0 && page < a.num_pages)
+            if (lane < nbox && t < cur.L && page >= 0 && page < a.num_pages)
                 row = page * a.page_size + t % a.page_size;
-            const int n = __popc(__ballot_sync(0xffffffffu, row >= 0));
-            if (it & 1) { row_ring1 = row; n_ring1 = n; } else { row_ring0 = row; n_ring0 = n; }
+            const int cnt = __popc(__ballot_sync(0xffffffffu, row >= 0));
+            if (it & 1) { row_ring1 = row; n_ring1 = cnt; h_ring1 = cur.h; }
+            else { row_ring0 = row; n_ring0 = cnt; h_ring0 = cur.h; }
+            if (it + 1 < n) cur.next(a);
         };
         auto load = [&](int it, bool is_v) -> bool {   // whole warp
             const int row = (it & 1) ? row_ring1 : row_ring0;
-            const int n = (it & 1) ? n_ring1 : n_ring0;
+            const int cnt_rows = (it & 1) ? n_ring1 : n_ring0;
+            const int h = (it & 1) ? h_ring1 : h_ring0;
             const int cnt = is_v ? nv : nk;
             const int ring = is_v ? C::NV : C::NK;
             const int slot = cnt % ring;
@@ -191,20 +307,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             bool ok = true;
             if (lane == 0) {
                 ok = mbar_wait(empty_bar, ((cnt / ring) & 1) ^ 1, abort_flag);
-                if (ok) mbar_arrive_expect_tx(full_bar, (uint32_t)n * blk_bytes);
+                if (ok) mbar_arrive_expect_tx(full_bar, (uint32_t)cnt_rows * blk_bytes);
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
             __syncwarp();                          // the expect-tx precedes every lane's copy
             const uint32_t dst = sb + (is_v ? C::OFF_V : C::OFF_K) + slot * C::KV_TILE + lane * blk_bytes;
             const void* map = is_v ? (const void*)&tm_v : (const void*)&tm_k;
-            if (row >= 0) tma_load_5d(dst, map, full_bar, 0, 0, 0, row / 8, hkv);
+            if (row >= 0) tma_load_5d(dst, map, full_bar, 0, 0, 0, row / 8, h);
             if (is_v) ++nv; else ++nk;
             return true;
         };
         find_rows(0);
         ok = load(0, false);
-        for (int it = 0; it < n_tiles && ok; ++it) {
-            if (it + 1 < n_tiles) {
+        for (int it = 0; it < n && ok; ++it) {
+            if (it + 1 < n) {
                 find_rows(it + 1);
                 ok = load(it + 1, false);
                 if (!ok) break;
@@ -225,7 +341,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer (lane 0 issues)
-        auto issue_qk = [&](int i) -> bool {
+        Cursor cq, cp;                             // tiles of the next S = Q K^T and the next P V
+        cq.set(a, rg.s0);
+        cq.lt = rg.lt0;
+        cp = cq;
+        int q_pieces = 0;                          // later pieces whose Q has been waited for
+        auto issue_qk = [&](int i) -> bool {       // tile i is at cq
+            if (i > 0 && cq.lt == 0) {
+                // first tile of a later piece: its Q rows replace the previous ones
+                if (!__all_sync(0xffffffffu, mbar_wait(q_next, q_pieces & 1, abort_flag))) return false;
+                ++q_pieces;
+            }
             const int ks = i % C::NK;
             if (!__all_sync(0xffffffffu, mbar_wait(k_full(ks), (i / C::NK) & 1, abort_flag))) return false;
             tc_fence_after();
@@ -243,20 +369,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 mma_commit(k_empty(ks));
             }
             __syncwarp();
+            if (i + 1 < n) cq.next(a);
             return true;
         };
         bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag));
         if (ok) tc_fence_after();
         if (ok) ok = issue_qk(0);
-        if (ok && n_tiles > 1) ok = issue_qk(1);
-        for (int i = 0; i < n_tiles && ok; ++i) {
+        if (ok && n > 1) ok = issue_qk(1);
+        for (int i = 0; i < n && ok; ++i) {
             ok = __all_sync(0xffffffffu, mbar_wait(p_full(i & 1), (i >> 1) & 1, abort_flag));
             if (!ok) break;
             const int vs = i % C::NV;
             ok = __all_sync(0xffffffffu, mbar_wait(v_full(vs), (i / C::NV) & 1, abort_flag));
             if (!ok) break;
             const uint32_t vb = sb + C::OFF_V + vs * C::KV_TILE;
-            const int nvalid = t_end - (t_begin + i * BN);
+            const bool fresh = i == 0 || cp.lt == 0;   // first tile of a piece: O starts over
+            const int nvalid = min(BN, cp.L - cp.lt * BN);
             if (nvalid < BN) {
                 // Value rows past the request's end hold stale data: zero them
                 // before the tensor core reads the tile.
@@ -279,13 +407,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_bf16_ts(tmem + C::COL_O, tmem + pcol + kk * 8,
                                 vdesc + (uint64_t)((2 * kk * C::GROUP_STRIDE) >> 4), C::IDESC_PV,
-                                (i > 0 || kk > 0) ? 1u : 0u);
+                                (!fresh || kk > 0) ? 1u : 0u);
                 mma_commit(o_done);
                 mma_commit(v_empty(vs));
             }
             __syncwarp();
+            if (i + 1 < n) cp.next(a);
             // S of tile i+2 overwrites P of tile i: issued after its P V.
-            if (i + 2 < n_tiles) ok = issue_qk(i + 2);
+            if (i + 2 < n) ok = issue_qk(i + 2);
         }
         if (lane == 0) {
             mma_commit(drain);                    // every MMA issued above has completed once this arrives
@@ -293,43 +422,49 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ warps 0-3: Q rows into TMEM
-        // Row r = i * g + hl is query i of head hkv * g + hl; rows past g * Sq are zero.
-        {
-            const int r = warp * 32 + lane;
-            const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-            const uint4* src = nullptr;
-            if (r < R)
-                src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q) +
-                                                     (((size_t)b * a.Sq + r / g) * a.Hq + hkv * g + r % g) * D);
-#pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {          // 32 columns (64 values) at a time
-                uint32_t w[32];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint4 v = src ? __ldg(src + 8 * c + e) : make_uint4(0u, 0u, 0u, 0u);
-                    w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
-                }
-                tmem_st32(tmem + lane_addr + C::COL_Q + 32 * c, w);
-            }
-            tc_fence_before();
-            mbar_arrive(q_ready);
-        }
+        // ------------------------------------------------------------ warps 0-3: first Q rows into TMEM
+        // Row r = i * g + hl is query i of head h * g + hl; rows past g * Sq are zero.
+        Cursor c0;
+        c0.set(a, rg.s0);
+        q_row_to_tmem<D>(a, tmem + ((uint32_t)(warp * 32) << 16) + C::COL_Q, warp * 32 + lane, R, g, c0.b, c0.h);
+        tc_fence_before();
+        mbar_arrive(q_ready);
     }
     if (warp < n_sm_warps) {
         // ------------------------------------------------------------ softmax warps
         const int r = warp * 32 + lane;            // padded row == TMEM lane
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
         const bool row_ok = r < R;
-        int lim = 0;                               // exclusive visibility limit of this row
-        if (row_ok) lim = a.causal ? (int)min((long)t_end, (long)(r / g) + L - a.Sq + 1) : t_end;
-        // keys below lim_first are visible to every row of the group
-        const int lim_first = a.causal ? (int)max((long)t_begin, min((long)t_end, (long)L - a.Sq + 1)) : t_end;
         const float sl = a.scale_log2;
+        Cursor c;
+        c.set(a, rg.s0);
+        c.lt = rg.lt0;
+        int lim = 0, lim_first = 0;                // visibility limit of this row / of every row
+        auto piece_setup = [&]() {
+            const int L = c.L;
+            lim = row_ok ? (a.causal ? (int)min((long)L, (long)(r / g) + L - a.Sq + 1) : L) : 0;
+            lim_first = a.causal ? max(0, min(L, L - a.Sq + 1)) : L;
+        };
+        piece_setup();
+        int piece_lt0 = rg.lt0;                    // tile of the segment the piece starts at
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int it = 0; it < n_tiles; ++it) {
-            const int t0 = t_begin + it * BN;
+        for (int it = 0; it < n; ++it) {
+            const int t0 = c.lt * BN;
+            const bool first = it == 0 || c.lt == 0;
+            const bool last = c.lt == c.nt - 1 || it == n - 1;
+            Cursor nx = c;
+            if (last && it + 1 < n) {
+                // the next piece's Q row: into L2 now, into TMEM after this tile
+                nx.next(a);
+                if (row_ok) {
+                    const char* p = reinterpret_cast<const char*>(a.q) +
+                                    (((size_t)nx.b * a.Sq + r / g) * a.Hq + nx.h * g + r % g) * D * 2;
+#pragma unroll
+                    for (int e = 0; e < D * 2 / 128; ++e)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128 * e));
+                }
+            }
             ok = __all_sync(0xffffffffu, mbar_wait(s_full(it & 1), (it >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -342,13 +477,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
             if (fast) {
 #pragma unroll
-                for (int c = 0; c < BN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
+                for (int cc = 0; cc < BN; cc += 2) mx8[(cc >> 1) & 7] = fmax3(mx8[(cc >> 1) & 7], s[cc], s[cc + 1]);
             } else {
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const float x = t0 + c < lim ? s[c] * sl : -INFINITY;   // the select drops stale rows
-                    s[c] = x;
-                    mx8[c & 7] = fmaxf(mx8[c & 7], x);
+                for (int cc = 0; cc < BN; ++cc) {
+                    const float x = t0 + cc < lim ? s[cc] * sl : -INFINITY;   // the select drops stale rows
+                    s[cc] = x;
+                    mx8[cc & 7] = fmaxf(mx8[cc & 7], x);
                 }
             }
 #pragma unroll
@@ -368,12 +503,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             for (int e = 0; e < 4; ++e) rs4[e] = f32x2(0.f, 0.f);
             uint32_t pk[BN / 2];
 #pragma unroll
-            for (int c = 0; c < BN / 2; ++c) {
+            for (int cc = 0; cc < BN / 2; ++cc) {
                 float x0, x1;
-                f32x2_split(ffma2(f32x2(s[2 * c], s[2 * c + 1]), fa2, nm2), x0, x1);
+                f32x2_split(ffma2(f32x2(s[2 * cc], s[2 * cc + 1]), fa2, nm2), x0, x1);
                 const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                rs4[c & 3] = fadd2(rs4[c & 3], f32x2(p0, p1));
-                pk[c] = pack_bf16x2(p0, p1);
+                rs4[cc & 3] = fadd2(rs4[cc & 3], f32x2(p0, p1));
+                pk[cc] = pack_bf16x2(p0, p1);
             }
             rs4[0] = fadd2(rs4[0], rs4[2]);
             rs4[1] = fadd2(rs4[1], rs4[3]);
@@ -382,45 +517,71 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             f32x2_split(rs4[1], r2, r3);
             l_run = l_run * alpha + ((r0 + r1) + (r2 + r3));
             tmem_st32(tmem + lane_addr + scol, pk);          // P over the first 32 columns of S
-            if (it > 0) {
-                // O must hold P V of the previous tile before it is rescaled
+            if (!first) {
+                // O must hold P V of the previous tile before it is rescaled (the
+                // first tile of a piece starts a fresh O)
                 ok = __all_sync(0xffffffffu, mbar_wait(o_done, (it - 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int cc = 0; cc < D / 32; ++cc) {
                         float o[32];
-                        tmem_ld32(tmem + lane_addr + C::COL_O + 32 * c, o);
+                        tmem_ld32(tmem + lane_addr + C::COL_O + 32 * cc, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st32(tmem + lane_addr + C::COL_O + 32 * c, reinterpret_cast<uint32_t*>(o));
+                        tmem_st32(tmem + lane_addr + C::COL_O + 32 * cc, reinterpret_cast<uint32_t*>(o));
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(p_full(it & 1));
-        }
-        if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(o_done, (n_tiles - 1) & 1, abort_flag));
-            if (ok) tc_fence_after();
-        }
-        const size_t part_row = ((size_t)(b * a.Hkv + hkv) * a.max_splits + split) * R + r;
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            if (last) {
+                if (it + 1 < n) {
+                    // S of this tile is done, so Q is free: the next piece's rows
+                    q_row_to_tmem<D>(a, tmem + lane_addr + C::COL_Q, r, R, g, nx.b, nx.h);
+                    tc_fence_before();
+                    mbar_arrive(q_next);
+                }
+                // ---- epilogue of the piece: O / l and the LSE
+                ok = __all_sync(0xffffffffu, mbar_wait(o_done, it & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                const int id = c.s + cta;                  // partial id of this piece
+                const size_t part_row = (size_t)id * R + r;
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            if (ok) tmem_ld32(tmem + lane_addr + C::COL_O + 32 * c, o);
-            if (row_ok) {
-                float4* dst = reinterpret_cast<float4*>(a.part_o + part_row * D + 32 * c);
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_addr + C::COL_O + 32 * cc, o);
+                    if (row_ok) {
+                        float4* dst = reinterpret_cast<float4*>(a.part_o + part_row * D + 32 * cc);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    dst[e] = ok ? make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv,
-                                              o[4 * e + 3] * inv)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv,
+                                                 o[4 * e + 3] * inv);
+                    }
+                }
+                if (row_ok) a.part_lse[part_row] = l_run > 0.f ? m_ref + log2f(l_run) : -INFINITY;
+                if (piece_lt0 == 0 && r == 0) {
+                    // this CTA holds the segment's first tile: record its pieces
+                    const long seg_start = (long)rg.g0 + it - c.lt;
+                    const int c_last = (int)((seg_start + c.nt - 1) / rg.per);
+                    a.seg_table[2 * c.s] = id;
+                    a.seg_table[2 * c.s + 1] = c_last - cta + 1;
+                }
+                m_ref = -INFINITY;
+                l_run = 0.f;
+                tc_fence_before();
+            }
+            if (it + 1 < n) {
+                c.next(a);
+                if (c.lt == 0) {
+                    piece_setup();
+                    piece_lt0 = 0;
+                }
             }
         }
-        if (row_ok) a.part_lse[part_row] = (ok && l_run > 0.f) ? m_ref + log2f(l_run) : -INFINITY;
     }
 
     tc_fence_before();
@@ -441,8 +602,7 @@ cudaError_t launch_t(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const Dec
     if (e != cudaSuccess) return e;
     const int g = a.Hq / a.Hkv;
     const int R = g * a.Sq;
-    dim3 grid(a.max_splits, a.Hkv, a.B);
-    decode_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_k, tm_v, a, R, g, box_tokens);
+    decode_tc_kernel<D><<<a.tc_grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_k, tm_v, a, R, g, box_tokens);
     return cudaGetLastError();
 }
 

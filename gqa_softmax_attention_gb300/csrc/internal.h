@@ -40,6 +40,12 @@ struct DecodeArgs {
     float scale_log2;
     int chunk;              // tokens per split (multiple of the key tile)
     int max_splits;
+    // Balanced tensor-core path: partials are indexed by piece id, and
+    // seg_table[2s], seg_table[2s + 1] hold segment s's first id and piece
+    // count; nullptr on the split path.
+    int* seg_table;         // [B * Hkv, 2]
+    int n_part;             // partial slots in part_o / part_lse
+    int tc_grid;            // persistent CTAs (one per SM)
 };
 
 struct DecodePlan {
@@ -48,7 +54,12 @@ struct DecodePlan {
     int rows;               // g * Sq rows per KV head
     size_t part_o_bytes;
     size_t part_lse_bytes;
-    size_t workspace_bytes;
+    size_t workspace_bytes; // enough for whichever path the sizes select
+    // balanced tensor-core path (tc set when the sizes select it)
+    bool tc;
+    int tc_grid;
+    int n_part;             // B * Hkv + tc_grid partial slots
+    size_t tc_part_o_bytes, tc_part_lse_bytes, tc_table_bytes;
 };
 
 bool plan_decode(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
