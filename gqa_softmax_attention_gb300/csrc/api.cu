@@ -122,9 +122,9 @@ gqa_status attn_fwd_dense(const void* q, const void* k, const void* v, const uin
     if (Skv == 0)
         return gqa::launch_empty_rows(o, lse, (long)B * Sq * Hq, D, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!make_bshd_map(&tq, q, B, Sq, Hq, D) || !make_bshd_map(&tk, k, B, Skv, Hkv, D) ||
-        !make_bshd_map(&tv, v, B, Skv, Hkv, D))
+        !make_bshd_map(&tv, v, B, Skv, Hkv, D) || !make_bshd_map(&to, o, B, Sq, Hq, D))
         return GQA_ERR_CUDA;
     PrefillArgs a;
     a.mask = key_padding_mask;
@@ -133,7 +133,7 @@ gqa_status attn_fwd_dense(const void* q, const void* k, const void* v, const uin
     a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = Sq; a.Skv = Skv; a.D = D;
     a.causal = causal ? 1 : 0;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
-    return gqa::launch_prefill(tq, tk, tv, a, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    return gqa::launch_prefill(tq, tk, tv, to, a, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 size_t attn_decode_paged_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_pages) {

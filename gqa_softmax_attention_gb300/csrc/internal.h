@@ -19,7 +19,8 @@ struct PrefillArgs {
 // Launches the tcgen05 prefill kernel.  The tensor maps describe q, k, v as
 // 4-D [B, S, H, D] bf16 tensors with a {64, 128, 1, 1} box and 128-byte swizzle.
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                           const CUtensorMap& tm_v, const PrefillArgs& a, cudaStream_t stream);
+                           const CUtensorMap& tm_v, const CUtensorMap& tm_o, const PrefillArgs& a,
+                           cudaStream_t stream);
 // Rows with no key at all (Skv == 0): O = 0, LSE = -inf.
 cudaError_t launch_empty_rows(void* o, float* lse, long rows, int D, cudaStream_t stream);
 int prefill_take_device_error();

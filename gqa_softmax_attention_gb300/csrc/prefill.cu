@@ -20,7 +20,8 @@
 //              reads its S row from TMEM, folds the causal / padding mask,
 //              updates the running max and sum, writes P (bf16) back over its
 //              S row, rescales its O row when needed, and finally normalises O
-//              and writes O and LSE.
+//              into its Q tile's shared-memory buffer, from which one thread
+//              stores the tile with TMA, and writes the LSE.
 // Warps 10-11 only complete the third warpgroup (register rebalancing works
 // per warpgroup).  TMEM (512 columns): S0 | S1 | O0 | O1; P_k occupies the
 // first 64 columns of S_k.
@@ -206,7 +207,8 @@ __device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, 
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a, int n_qpairs) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const PrefillArgs a, int n_qpairs) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -526,26 +528,44 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (ok) tc_fence_after();
         }
         const bool row_ok = r < ti.rows_valid;
-        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) +
-                              (((size_t)b * a.Sq + row_q) * a.Hq + hq) * D;
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        if (ok && it > 0) {
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                tmem_ld32(tmem + lane_addr + col_o + 32 * c, o);
-                if (row_ok) {
-                    uint32_t w[16];
+        // O / l as bf16 goes into this tile's Q buffer (its S products are all
+        // done once o_final has arrived) in the 128-byte-swizzled box layout of
+        // the output map, and one thread stores the tile with TMA: whole
+        // 128-byte rows instead of 16-byte pieces strided by Hq * D.  Rows past
+        // Sq lie outside the map and are not written.  A tile with no visited
+        // key (its Q load may still be landing) or a wait that gave up writes
+        // zeros directly.
+        const bool staged = named_bar_and(3 + k, BM, ok && it > 0);
+        if (staged) {
+            const uint32_t obuf = sb + C::OFF_Q + k * C::TILE_BYTES;
+            uint32_t ow[D];
+            if constexpr (D == 128) {
+                tmem_ld128(tmem + lane_addr + col_o, ow);
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+                for (int c = 0; c < D / 32; ++c)
+                    tmem_ld32(tmem + lane_addr + col_o + 32 * c, reinterpret_cast<float*>(ow + 32 * c));
+            }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-                }
+            for (int q = 0; q < D / 8; ++q) {          // 16-byte chunk q of the row
+                const float* f = reinterpret_cast<const float*>(ow + 8 * q);
+                st_shared_v4(obuf + (q / 8) * C::SUB_BYTES + r * 128 + (((q % 8) ^ (r & 7)) << 4),
+                             pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                             pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(3 + k, BM);
+            if (r == 0) {
+#pragma unroll
+                for (int sub = 0; sub < C::KSUB; ++sub)
+                    tma_store_4d(&tm_o, obuf + sub * C::SUB_BYTES, sub * 64, ti.q0, hq, b);
+                bulk_commit_group();
+                bulk_wait_read_all();
             }
         } else if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
+                                                  (((size_t)b * a.Sq + row_q) * a.Hq + hq) * D);
 #pragma unroll
             for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -578,24 +598,24 @@ __global__ void empty_rows_kernel(__nv_bfloat16* o, float* lse, long rows, int D
 
 template <int D>
 cudaError_t launch_prefill_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                             const PrefillArgs& a, cudaStream_t stream) {
+                             const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream) {
     using C = Cfg<D>;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_qpairs = (a.Sq + NQ * BM - 1) / (NQ * BM);
     const long grid = (long)n_qpairs * a.B * a.Hq;
-    prefill_kernel<D><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, a, n_qpairs);
+    prefill_kernel<D><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, tm_o, a, n_qpairs);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                           const PrefillArgs& a, cudaStream_t stream) {
+                           const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream) {
     switch (a.D) {
-        case 64: return launch_prefill_t<64>(tm_q, tm_k, tm_v, a, stream);
-        case 128: return launch_prefill_t<128>(tm_q, tm_k, tm_v, a, stream);
+        case 64: return launch_prefill_t<64>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 128: return launch_prefill_t<128>(tm_q, tm_k, tm_v, tm_o, a, stream);
         default: return cudaErrorInvalidValue;
     }
 }
