@@ -133,6 +133,7 @@ gqa_status attn_fwd_dense(const void* q, const void* k, const void* v, const uin
     a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = Sq; a.Skv = Skv; a.D = D;
     a.causal = causal ? 1 : 0;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    a.num_sms = sm_count();
     return gqa::launch_prefill(tq, tk, tv, to, a, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 

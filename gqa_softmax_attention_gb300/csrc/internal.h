@@ -14,6 +14,7 @@ struct PrefillArgs {
     int B, Hq, Hkv, Sq, Skv, D;
     int causal;
     float scale_log2;     // scale * log2(e)
+    int num_sms;          // persistent grid size
 };
 
 // Launches the tcgen05 prefill kernel.  The tensor maps describe q, k, v as

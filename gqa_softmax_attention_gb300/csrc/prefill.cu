@@ -76,9 +76,11 @@ struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
     static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_V + NV * TILE_BYTES;
-    // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_final
-    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 1;
+    static constexpr int OFF_STAGE = OFF_V + NV * TILE_BYTES;   // one 64-column output box per Q tile
+    static constexpr int OFF_BAR = OFF_STAGE + NQ * SUB_BYTES;
+    // q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
+    // s_full[2], p_full[2], o_final[2], drain
+    static constexpr int NBAR = 4 + 2 * NK + 2 * NV + 6 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     // 1 KB alignment slack; at least 120 KB so that one CTA holds an SM (it
@@ -218,32 +220,76 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    // Heaviest (last) query tiles first; adjacent CTAs share a KV head.
+    // Work items w = 0 .. n_items-1, heaviest (last) query tiles first and
+    // adjacent items on one KV head; round r of this persistent CTA takes
+    // item r * G + cta (even r) or r * G + G - 1 - cta (odd r), so heavy and
+    // light items alternate across rounds.
     const int bh = a.B * a.Hq;
-    const int qp = n_qpairs - 1 - (int)(blockIdx.x / bh);
-    const int rem = (int)(blockIdx.x % bh);
-    const int hq = rem % a.Hq;
-    const int b = rem / a.Hq;
-    const int hkv = hq / (a.Hq / a.Hkv);
+    const int n_items = n_qpairs * bh;
+    const int G = gridDim.x;
+    const int cta = blockIdx.x;
+    auto item_of = [&](int r) -> int {
+        const long w = (long)r * G + ((r & 1) ? G - 1 - cta : cta);
+        return w < n_items ? (int)w : -1;
+    };
+    struct Item {
+        int b, hq, hkv, q0, n_all, kv_end_all;
+        TileInfo t0, t1;
+        const uint8_t* mrow;
+    };
+    auto describe = [&](int w) {
+        Item it;
+        const int qp = n_qpairs - 1 - w / bh;
+        const int rem = w % bh;
+        it.hq = rem % a.Hq;
+        it.b = rem / a.Hq;
+        it.hkv = it.hq / (a.Hq / a.Hkv);
+        it.q0 = qp * (NQ * BM);
+        it.t0 = tile_info(it.q0, a.Sq, a.Skv, a.causal);
+        it.t1 = tile_info(it.q0 + BM, a.Sq, a.Skv, a.causal);
+        it.n_all = max(it.t0.n_tiles, it.t1.n_tiles);
+        it.kv_end_all = max(it.t0.kv_end, it.t1.kv_end);
+        it.mrow = a.mask ? a.mask + (size_t)it.b * a.Skv : nullptr;
+        return it;
+    };
+    // Visited key tiles of an item (non-empty, below kv_end of either Q tile)
+    // are numbered i = 0, 1, ...; Q_k takes part in the first c_k of them.
+    // Warp-collective.
+    auto count_tiles = [&](const Item& it, int& c0, int& c1, int& c_all) {
+        c0 = c1 = c_all = 0;
+        for (int chunk = 0; chunk * 32 < it.n_all; ++chunk) {
+            const uint32_t f = tile_flags(it.mrow, chunk, it.n_all, it.kv_end_all, lane);
+            c_all += __popc(f);
+            c0 += __popc(f & below_bits(it.t0.n_tiles, chunk));
+            c1 += __popc(f & below_bits(it.t1.n_tiles, chunk));
+        }
+    };
 
     const uint32_t bar0 = sb + C::OFF_BAR;
-    const uint32_t q_full = bar0;
-    auto k_full = [&](int i) { return bar0 + 8u * (1 + i); };
-    auto k_empty = [&](int i) { return bar0 + 8u * (1 + C::NK + i); };
-    auto v_full = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + i); };
-    auto v_empty = [&](int i) { return bar0 + 8u * (1 + 2 * C::NK + C::NV + i); };
-    auto s_full = [&](int k) { return bar0 + 8u * (1 + 2 * C::NK + 2 * C::NV + k); };
-    auto p_full = [&](int k) { return bar0 + 8u * (3 + 2 * C::NK + 2 * C::NV + k); };
-    const uint32_t o_final = bar0 + 8u * (5 + 2 * C::NK + 2 * C::NV);
+    auto q_full = [&](int k) { return bar0 + 8u * k; };
+    auto q_empty = [&](int k) { return bar0 + 8u * (2 + k); };
+    auto k_full = [&](int i) { return bar0 + 8u * (4 + i); };
+    auto k_empty = [&](int i) { return bar0 + 8u * (4 + C::NK + i); };
+    auto v_full = [&](int i) { return bar0 + 8u * (4 + 2 * C::NK + i); };
+    auto v_empty = [&](int i) { return bar0 + 8u * (4 + 2 * C::NK + C::NV + i); };
+    auto s_full = [&](int k) { return bar0 + 8u * (4 + 2 * C::NK + 2 * C::NV + k); };
+    auto p_full = [&](int k) { return bar0 + 8u * (6 + 2 * C::NK + 2 * C::NV + k); };
+    auto o_final = [&](int k) { return bar0 + 8u * (8 + 2 * C::NK + 2 * C::NV + k); };
+    const uint32_t drain = bar0 + 8u * (10 + 2 * C::NK + 2 * C::NV);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
+        for (int k = 0; k < NQ; ++k) {
+            mbar_init(q_full(k), 1);
+            mbar_init(q_empty(k), 1);
+            mbar_init(s_full(k), 1);
+            mbar_init(p_full(k), BM);
+            mbar_init(o_final(k), 1);
+        }
         for (int i = 0; i < C::NK; ++i) { mbar_init(k_full(i), 1); mbar_init(k_empty(i), 1); }
         for (int i = 0; i < C::NV; ++i) { mbar_init(v_full(i), 1); mbar_init(v_empty(i), 1); }
-        for (int k = 0; k < NQ; ++k) { mbar_init(s_full(k), 1); mbar_init(p_full(k), BM); }
-        mbar_init(o_final, 1);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -256,13 +302,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int q0 = qp * (NQ * BM);
-    const TileInfo t0 = tile_info(q0, a.Sq, a.Skv, a.causal);
-    const TileInfo t1 = tile_info(q0 + BM, a.Sq, a.Skv, a.causal);
-    const int n_all = max(t0.n_tiles, t1.n_tiles);
-    const int kv_end_all = max(t0.kv_end, t1.kv_end);
-    const uint8_t* mrow = a.mask ? a.mask + (size_t)b * a.Skv : nullptr;
-
     // Each role ends on its own (no shared tail), so register limits apply per
     // role: the MMA warp frees TMEM once the softmax warps have arrived on
     // barrier 2 after their last TMEM access.
@@ -270,25 +309,43 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         regs_dec<kRegsOther>();
         if (warp == WARP_LOAD) {
             // ------------------------------------------------------------ producer
-            if (n_all > 0) {
-                int nk = 0, nv = 0;   // K and V tile loads issued so far
-                bool q_issued = false;
+            int nk = 0, nv = 0, nq0 = 0, nq1 = 0;   // loads issued so far
+            bool ok = true;
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+            }
+            for (int r = 0; ok; ++r) {
+                const int w = item_of(r);
+                if (w < 0) break;
+                const Item it = describe(w);
+                int c0, c1, c_all;
+                count_tiles(it, c0, c1, c_all);
+                if (c_all == 0) continue;
                 if (lane == 0) {
-                    tma_prefetch_desc(&tm_q);
-                    tma_prefetch_desc(&tm_k);
-                    tma_prefetch_desc(&tm_v);
-                    mbar_arrive_expect_tx(q_full, NQ * C::TILE_BYTES);
+                    // Q_k of this item once the last S of the previous Q_k is done
 #pragma unroll
-                    for (int k = 0; k < NQ; ++k)
+                    for (int k = 0; k < NQ; ++k) {
+                        const int ck = k == 0 ? c0 : c1;
+                        const int nq = k == 0 ? nq0 : nq1;
+                        if (ck == 0 || !ok) continue;
+                        ok = mbar_wait(q_empty(k), (nq & 1) ^ 1, abort_flag);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(q_full(k), C::TILE_BYTES);
 #pragma unroll
                         for (int s = 0; s < C::KSUB; ++s)
-                            tma_load_4d(sb + C::OFF_Q + k * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, q_full, s * 64,
-                                        q0 + k * BM, hq, b);
-                    q_issued = true;
+                            tma_load_4d(sb + C::OFF_Q + k * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, q_full(k),
+                                        s * 64, it.q0 + k * BM, it.hq, it.b);
+                        if (k == 0) ++nq0; else ++nq1;
+                    }
                 }
-                TileIter tiles(mrow, n_all, kv_end_all, lane);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                nq0 = __shfl_sync(0xffffffffu, nq0, 0);
+                nq1 = __shfl_sync(0xffffffffu, nq1, 0);
+                if (!ok) break;
+                TileIter tiles(it.mrow, it.n_all, it.kv_end_all, lane);
                 for (int j = tiles.next(); j >= 0; j = tiles.next()) {
-                    bool ok = true;
                     if (lane == 0) {
                         const int ks = nk % C::NK;
                         ok = mbar_wait(k_empty(ks), ((nk / C::NK) & 1) ^ 1, abort_flag);
@@ -297,7 +354,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                             for (int s = 0; s < C::KSUB; ++s)
                                 tma_load_4d(sb + C::OFF_K + ks * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k,
-                                            k_full(ks), s * 64, j * BN, hkv, b);
+                                            k_full(ks), s * 64, j * BN, it.hkv, it.b);
                             ++nk;
                             const int vs = nv % C::NV;
                             ok = mbar_wait(v_empty(vs), ((nv / C::NV) & 1) ^ 1, abort_flag);
@@ -306,7 +363,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                                 for (int s = 0; s < C::KSUB; ++s)
                                     tma_load_4d(sb + C::OFF_V + vs * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v,
-                                                v_full(vs), s * 64, j * BN, hkv, b);
+                                                v_full(vs), s * 64, j * BN, it.hkv, it.b);
                                 ++nv;
                             }
                         }
@@ -314,92 +371,130 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                 }
-                // The Q load may have no consumer (every key tile masked out):
-                // never leave it in flight.
-                if (lane == 0 && q_issued) mbar_drain(q_full, 0);
-                if (lane == 0 && *abort_flag) {
-                    // Let copies already in flight land before the CTA goes away:
-                    // wait for the last load issued into each slot.
-                    for (int s = 0; s < C::NK && s < nk; ++s) {
-                        const int last = nk - 1 - ((nk - 1 - s) % C::NK);
-                        mbar_drain(k_full(s), (last / C::NK) & 1);
-                    }
-                    for (int s = 0; s < C::NV && s < nv; ++s) {
-                        const int last = nv - 1 - ((nv - 1 - s) % C::NV);
-                        mbar_drain(v_full(s), (last / C::NV) & 1);
-                    }
+            }
+            if (lane == 0 && *abort_flag) {
+                // Let copies already in flight land before the CTA goes away:
+                // wait for the last load issued into each slot.
+                for (int s = 0; s < C::NK && s < nk; ++s) {
+                    const int last = nk - 1 - ((nk - 1 - s) % C::NK);
+                    mbar_drain(k_full(s), (last / C::NK) & 1);
                 }
+                for (int s = 0; s < C::NV && s < nv; ++s) {
+                    const int last = nv - 1 - ((nv - 1 - s) % C::NV);
+                    mbar_drain(v_full(s), (last / C::NV) & 1);
+                }
+                if (nq0 > 0) mbar_drain(q_full(0), (nq0 - 1) & 1);
+                if (nq1 > 0) mbar_drain(q_full(1), (nq1 - 1) & 1);
             }
         } else if (warp == WARP_MMA) {
             // ------------------------------------------------------------ MMA issuer
-            // Visited key tiles (non-empty, below kv_end of either Q tile) are
-            // numbered i = 0, 1, ...; Q_k takes part in the first c_k of them.
-            int c0 = 0, c1 = 0, c_all = 0;
-            for (int chunk = 0; chunk * 32 < n_all; ++chunk) {
-                const uint32_t f = tile_flags(mrow, chunk, n_all, kv_end_all, lane);
-                c_all += __popc(f);
-                c0 += __popc(f & below_bits(t0.n_tiles, chunk));
-                c1 += __popc(f & below_bits(t1.n_tiles, chunk));
-            }
-            if (c_all > 0 && lane == 0) {
-                auto issue_s = [&](int k, int i) {
-                    const uint32_t kbase = sb + C::OFF_K + (i % C::NK) * C::TILE_BYTES;
-                    const uint32_t qbase = sb + C::OFF_Q + k * C::TILE_BYTES;
+            int kt = 0, vt = 0;                    // K and V tiles consumed by earlier items
+            int nq0 = 0, nq1 = 0, pc0 = 0, pc1 = 0;   // Q loads consumed, P tiles taken
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int w = item_of(r);
+                if (w < 0) break;
+                const Item it = describe(w);
+                int c0, c1, c_all;
+                count_tiles(it, c0, c1, c_all);
+                if (lane == 0 && c_all > 0) {
+                    auto issue_s = [&](int k, int slot) {
+                        const uint32_t kbase = sb + C::OFF_K + slot * C::TILE_BYTES;
+                        const uint32_t qbase = sb + C::OFF_Q + k * C::TILE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (kk / 4) * C::SUB_BYTES + (kk % 4) * 32;
-                        mma_bf16_ss(tmem + (k == 0 ? C::COL_S0 : C::COL_S1), make_sdesc_sw128(qbase + koff, 16, 1024),
-                                    make_sdesc_sw128(kbase + koff, 16, 1024), C::IDESC_QK, kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(s_full(k));
-                };
-                auto issue_pv = [&](int k, int i) {
-                    const uint32_t vbase = sb + C::OFF_V + (i % C::NV) * C::TILE_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        // keys 16kk..16kk+15 of V: rows 16kk.. of every 64-column box
-                        const uint64_t bdesc = make_sdesc_sw128(vbase + kk * 16 * 128, C::SUB_BYTES, 1024);
-                        mma_bf16_ts(tmem + (k == 0 ? C::COL_O0 : C::COL_O1), tmem + (k == 0 ? C::COL_S0 : C::COL_S1) + kk * 8,
-                                    bdesc, C::IDESC_PV,
-                                    (i > 0 || kk > 0) ? 1u : 0u);
-                    }
-                };
-                bool ok = mbar_wait(q_full, 0, abort_flag) && mbar_wait(k_full(0), 0, abort_flag);
-                if (ok) {
-                    tc_fence_after();
-                    if (c0 > 0) issue_s(0, 0);
-                    if (c1 > 0) issue_s(1, 0);
-                    mma_commit(k_empty(0));
-                }
-                for (int i = 0; i < c_all && ok; ++i) {
-                    ok = mbar_wait(v_full(i % C::NV), (i / C::NV) & 1, abort_flag);
-                    if (!ok) break;
-                    const bool more = i + 1 < c_all;
-                    for (int k = 0; k < NQ && ok; ++k) {
-                        const int cnt = k == 0 ? c0 : c1;
-                        if (i < cnt) {
-                            ok = mbar_wait(p_full(k), i & 1, abort_flag);
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_pv(k, i);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t koff = (kk / 4) * C::SUB_BYTES + (kk % 4) * 32;
+                            mma_bf16_ss(tmem + (k == 0 ? C::COL_S0 : C::COL_S1),
+                                        make_sdesc_sw128(qbase + koff, 16, 1024),
+                                        make_sdesc_sw128(kbase + koff, 16, 1024), C::IDESC_QK, kk > 0 ? 1u : 0u);
                         }
-                        if (more) {
+                        mma_commit(s_full(k));
+                    };
+                    auto issue_pv = [&](int k, int slot, int i) {
+                        const uint32_t vbase = sb + C::OFF_V + slot * C::TILE_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            // keys 16kk..16kk+15 of V: rows 16kk.. of every 64-column box
+                            const uint64_t bdesc = make_sdesc_sw128(vbase + kk * 16 * 128, C::SUB_BYTES, 1024);
+                            mma_bf16_ts(tmem + (k == 0 ? C::COL_O0 : C::COL_O1),
+                                        tmem + (k == 0 ? C::COL_S0 : C::COL_S1) + kk * 8, bdesc, C::IDESC_PV,
+                                        (i > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    };
+                    if (c0 > 0) ok = mbar_wait(q_full(0), nq0++ & 1, abort_flag);
+                    if (ok && c1 > 0) ok = mbar_wait(q_full(1), nq1++ & 1, abort_flag);
+                    if (ok) ok = mbar_wait(k_full(kt % C::NK), (kt / C::NK) & 1, abort_flag);
+                    if (ok) {
+                        tc_fence_after();
+                        if (c0 > 0) issue_s(0, kt % C::NK);
+                        if (c1 > 0) issue_s(1, kt % C::NK);
+                        mma_commit(k_empty(kt % C::NK));
+                    }
+                    // Visited tiles 0 .. c_all-2: P V of tile i, then S of tile i+1.
+                    // The item's commits of q_empty / o_final come after the loop:
+                    // conditional commits inside it slowed the steady state.
+                    for (int i = 0; i + 1 < c_all && ok; ++i) {
+                        const int vs = (vt + i) % C::NV;
+                        ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
+                        if (!ok) break;
+                        const int kn = kt + i + 1;     // K tile of visited tile i+1
+                        for (int k = 0; k < NQ && ok; ++k) {
+                            const int cnt = k == 0 ? c0 : c1;
+                            if (i < cnt) {
+                                const int pc = k == 0 ? pc0++ : pc1++;
+                                ok = mbar_wait(p_full(k), pc & 1, abort_flag);
+                                if (!ok) break;
+                                tc_fence_after();
+                                issue_pv(k, vs, i);
+                            }
                             if (k == 0) {
-                                ok = mbar_wait(k_full((i + 1) % C::NK), ((i + 1) / C::NK) & 1, abort_flag);
+                                ok = mbar_wait(k_full(kn % C::NK), (kn / C::NK) & 1, abort_flag);
                                 if (!ok) break;
                                 tc_fence_after();
                             }
                             // S_k of tile i+1 overwrites P_k of tile i: issued after its PV.
-                            if (i + 1 < cnt) issue_s(k, i + 1);
+                            if (i + 1 < cnt) issue_s(k, kn % C::NK);
                         }
+                        if (!ok) break;
+                        mma_commit(v_empty(vs));
+                        mma_commit(k_empty(kn % C::NK));
                     }
-                    if (!ok) break;
-                    mma_commit(v_empty(i % C::NV));
-                    if (more) mma_commit(k_empty((i + 1) % C::NK));
+                    // every S of the item is issued: its Q tiles may be replaced
+                    if (ok) {
+                        if (c0 > 0) mma_commit(q_empty(0));
+                        if (c1 > 0) mma_commit(q_empty(1));
+                    }
+                    // the last visited tile: P V only
+                    if (ok) {
+                        const int i = c_all - 1;
+                        const int vs = (vt + i) % C::NV;
+                        ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
+                        for (int k = 0; k < NQ && ok; ++k) {
+                            const int cnt = k == 0 ? c0 : c1;
+                            if (i < cnt) {
+                                const int pc = k == 0 ? pc0++ : pc1++;
+                                ok = mbar_wait(p_full(k), pc & 1, abort_flag);
+                                if (!ok) break;
+                                tc_fence_after();
+                                issue_pv(k, vs, i);
+                            }
+                        }
+                        if (ok) mma_commit(v_empty(vs));
+                    }
+                    kt += c_all;
+                    vt += c_all;
                 }
-                // Arrives once every MMA issued above has completed.
-                mma_commit(o_final);
-                if (!ok) mbar_drain(o_final, 0);
+                // one o_final phase per Q tile and item (also for a tile with no key):
+                // arrives when every MMA of the item has completed
+                if (lane == 0 && ok) {
+                    mma_commit(o_final(0));
+                    mma_commit(o_final(1));
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+            if (lane == 0) {
+                mma_commit(drain);                // every MMA issued above has completed once this arrives
+                mbar_drain(drain, 0);
             }
             __syncwarp();
             named_bar_sync(2, 8 * 32 + 32);          // softmax warps are done with TMEM
@@ -410,173 +505,186 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         regs_inc<kRegsSoftmax>();
         // ------------------------------------------------------------ softmax warps 0-7
         const int k = warp / 4;                                // Q tile of this warpgroup
-        const TileInfo ti = k == 0 ? t0 : t1;
         const int r = (warp % 4) * 32 + lane;                  // row of the tile == TMEM lane
         const uint32_t lane_addr = (uint32_t)((warp % 4) * 32) << 16;
         const uint32_t col_s = k == 0 ? C::COL_S0 : C::COL_S1;
         const uint32_t col_o = k == 0 ? C::COL_O0 : C::COL_O1;
-        const int row_q = ti.q0 + r;
-        const long p_row = (long)row_q + a.Skv - a.Sq;
-        const int lim = a.causal ? (int)max(0L, min((long)a.Skv, p_row + 1)) : a.Skv;
+        const uint32_t stage = sb + C::OFF_STAGE + k * C::SUB_BYTES;   // this warpgroup's output box
         const float sl = a.scale_log2;
-        float m_ref = -INFINITY;     // reference max (log2 units, scaled)
-        float l_run = 0.f;
+        int sf = 0;                  // S tiles taken so far (s_full parity)
+        int n_done = 0;              // items finished (o_final parity)
         bool ok = true;
-        int it = 0;
-        // The mask bytes of the next visited tile are fetched one tile ahead.
-        TileIter tiles(mrow, n_all, kv_end_all, lane);
-        auto fetch = [&](int j, uint8_t* mb) {
+        for (int rr = 0;; ++rr) {
+            const int w = item_of(rr);
+            if (w < 0) break;
+            const Item itm = describe(w);
+            const TileInfo ti = k == 0 ? itm.t0 : itm.t1;
+            const uint8_t* mrow = itm.mrow;
+            const int row_q = ti.q0 + r;
+            const long p_row = (long)row_q + a.Skv - a.Sq;
+            const int lim = a.causal ? (int)max(0L, min((long)a.Skv, p_row + 1)) : a.Skv;
+            float m_ref = -INFINITY;     // reference max (log2 units, scaled)
+            float l_run = 0.f;
+            int it = 0;
+            // The mask bytes of the next visited tile are fetched one tile ahead.
+            TileIter tiles(mrow, itm.n_all, itm.kv_end_all, lane);
+            auto fetch = [&](int j, uint8_t* mb) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int key = j * BN + w * 32 + lane;
-                mb[w] = (mrow && j >= 0 && key < kv_end_all) ? mrow[key] : (uint8_t)(mrow ? 0 : 1);
-            }
-        };
-        int j = tiles.next();
-        uint8_t mb[4];
-        fetch(j, mb);
-        for (; j >= 0 && j < ti.n_tiles;) {
-            const int jn = tiles.next();
-            uint8_t mbn[4];
-            fetch(jn, mbn);
-            uint32_t mw[4];
-            bool all_kept = true;
+                for (int q = 0; q < 4; ++q) {
+                    const int key = j * BN + q * 32 + lane;
+                    mb[q] = (mrow && j >= 0 && key < itm.kv_end_all) ? mrow[key] : (uint8_t)(mrow ? 0 : 1);
+                }
+            };
+            int j = tiles.next();
+            uint8_t mb[4];
+            fetch(j, mb);
+            for (; j >= 0 && j < ti.n_tiles;) {
+                const int jn = tiles.next();
+                uint8_t mbn[4];
+                fetch(jn, mbn);
+                uint32_t mw[4];
+                bool all_kept = true;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                mw[w] = __ballot_sync(0xffffffffu, mb[w] != 0);
-                all_kept = all_kept && (mw[w] == 0xffffffffu);
-            }
-            const int kbase = j * BN;
-            const bool need_mask = (kbase + BN > ti.lim_first) || !all_kept;
+                for (int q = 0; q < 4; ++q) {
+                    mw[q] = __ballot_sync(0xffffffffu, mb[q] != 0);
+                    all_kept = all_kept && (mw[q] == 0xffffffffu);
+                }
+                const int kbase = j * BN;
+                const bool need_mask = (kbase + BN > ti.lim_first) || !all_kept;
 
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full(k), it & 1, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sr[BN];
-            tmem_ld128(tmem + lane_addr + col_s, sr);
-            float* s = reinterpret_cast<float*>(sr);
+                ok = __all_sync(0xffffffffu, mbar_wait(s_full(k), sf & 1, abort_flag));
+                ++sf;
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sr[BN];
+                tmem_ld128(tmem + lane_addr + col_s, sr);
+                float* s = reinterpret_cast<float*>(sr);
 
-            // Row max over 8 independent chains (short dependency chains).
-            // Fast path (no mask in this tile, positive scale): the max is taken
-            // on raw scores and the scale is folded into the exp2 argument;
-            // otherwise scores are scaled first and masked ones set to -inf.
-            const bool fast = !need_mask && sl > 0.f;
-            float mx8[8];
+                // Row max over 8 independent chains (short dependency chains).
+                // Fast path (no mask in this tile, positive scale): the max is taken
+                // on raw scores and the scale is folded into the exp2 argument;
+                // otherwise scores are scaled first and masked ones set to -inf.
+                const bool fast = !need_mask && sl > 0.f;
+                float mx8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-            if (fast) {
+                for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+                if (fast) {
 #pragma unroll
-                for (int c = 0; c < BN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
-            } else {
+                    for (int c = 0; c < BN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
+                } else {
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    // keys of this 32-column group below the row's causal limit
-                    const int rel = lim - (kbase + 32 * w);
-                    const uint32_t below = rel >= 32 ? 0xffffffffu : (rel <= 0 ? 0u : ((1u << rel) - 1u));
-                    const uint32_t vis = mw[w] & below;
+                    for (int q = 0; q < 4; ++q) {
+                        // keys of this 32-column group below the row's causal limit
+                        const int rel = lim - (kbase + 32 * q);
+                        const uint32_t below = rel >= 32 ? 0xffffffffu : (rel <= 0 ? 0u : ((1u << rel) - 1u));
+                        const uint32_t vis = mw[q] & below;
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float x = ((vis >> c) & 1u) ? s[32 * w + c] * sl : -INFINITY;
-                        s[32 * w + c] = x;
-                        mx8[c & 7] = fmaxf(mx8[c & 7], x);
+                        for (int c = 0; c < 32; ++c) {
+                            const float x = ((vis >> c) & 1u) ? s[32 * q + c] * sl : -INFINITY;
+                            s[32 * q + c] = x;
+                            mx8[c & 7] = fmaxf(mx8[c & 7], x);
+                        }
                     }
                 }
-            }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + 4]);
-            const float mx_raw = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
-            const float mx = fast ? mx_raw * sl : mx_raw;          // scaled (log2 units)
-            // Lazy rescale: move the reference max only when the tile max
-            // exceeds it by more than the threshold.
-            float alpha = 1.f;
-            if (mx > m_ref + kRescaleThreshold) {
-                alpha = fast_exp2(m_ref - mx);                  // 0 when m_ref is -inf
-                m_ref = mx;
-            }
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;   // no -inf - -inf
-            // exp2 argument: s * fa - m_use (fa = scale on the fast path, 1 otherwise)
-            const float fa = fast ? sl : 1.f;
-            uint32_t pk[BN / 2];
-            float rs;
-            if (fast) rs = exp_row<kPolyEvery>(s, fa, m_use, pk);
-            else rs = exp_row<0>(s, fa, m_use, pk);
-            tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
-            l_run = l_run * alpha + rs;
-
-            // PV of the previous tile is complete (S of this tile landed after
-            // it), so O may be rescaled here, before PV of this tile.
-            if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(tmem + lane_addr + col_o + 32 * c, o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tmem_st32(tmem + lane_addr + col_o + 32 * c, reinterpret_cast<uint32_t*>(o));
+                for (int e = 0; e < 4; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + 4]);
+                const float mx_raw = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+                const float mx = fast ? mx_raw * sl : mx_raw;          // scaled (log2 units)
+                // Lazy rescale: move the reference max only when the tile max
+                // exceeds it by more than the threshold.
+                float alpha = 1.f;
+                if (mx > m_ref + kRescaleThreshold) {
+                    alpha = fast_exp2(m_ref - mx);                  // 0 when m_ref is -inf
+                    m_ref = mx;
                 }
-            }
-            tc_fence_before();
-            mbar_arrive(p_full(k));
-            ++it;
-            j = jn;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) mb[w] = mbn[w];
-        }
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;   // no -inf - -inf
+                // exp2 argument: s * fa - m_use (fa = scale on the fast path, 1 otherwise)
+                const float fa = fast ? sl : 1.f;
+                uint32_t pk[BN / 2];
+                float rs;
+                if (fast) rs = exp_row<kPolyEvery>(s, fa, m_use, pk);
+                else rs = exp_row<0>(s, fa, m_use, pk);
+                tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
+                l_run = l_run * alpha + rs;
 
-        if (ok && it > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0, abort_flag));
-            if (ok) tc_fence_after();
+                // PV of the previous tile is complete (S of this tile landed after
+                // it), so O may be rescaled here, before PV of this tile.
+                if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(tmem + lane_addr + col_o + 32 * c, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(tmem + lane_addr + col_o + 32 * c, reinterpret_cast<uint32_t*>(o));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(p_full(k));
+                ++it;
+                j = jn;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mb[q] = mbn[q];
+            }
+            // ---- epilogue of this Q tile: the last P V done.  It runs even after
+            // a wait gave up, so that the warpgroup's named barriers below see
+            // all four warps.
+            if (ok) {
+                ok = __all_sync(0xffffffffu, mbar_wait(o_final(k), n_done & 1, abort_flag));
+                if (ok) tc_fence_after();
+            }
+            ++n_done;
+            const bool row_ok = r < ti.rows_valid;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            // O / l as bf16 goes, one 64-column box at a time, into this
+            // warpgroup's staging buffer in the 128-byte-swizzled box layout of
+            // the output map, and one thread stores each box with TMA: whole
+            // 128-byte rows instead of 16-byte pieces strided by Hq * D.  Rows
+            // past Sq lie outside the map and are not written.  A tile with no
+            // visited key, or a wait that gave up, writes zeros directly.
+            const bool staged = named_bar_and(3 + k, BM, ok && it > 0);
+            if (staged) {
+                uint32_t ow[D];
+                if constexpr (D == 128) {
+                    tmem_ld128(tmem + lane_addr + col_o, ow);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c)
+                        tmem_ld32(tmem + lane_addr + col_o + 32 * c, reinterpret_cast<float*>(ow + 32 * c));
+                }
+#pragma unroll
+                for (int sub = 0; sub < C::KSUB; ++sub) {
+                    if (sub > 0) named_bar_sync(3 + k, BM);   // the previous box has been read out
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {              // 16-byte chunk q of the box row
+                        const float* f = reinterpret_cast<const float*>(ow + 64 * sub + 8 * q);
+                        st_shared_v4(stage + r * 128 + ((q ^ (r & 7)) << 4), pack_bf16x2(f[0] * inv, f[1] * inv),
+                                     pack_bf16x2(f[2] * inv, f[3] * inv), pack_bf16x2(f[4] * inv, f[5] * inv),
+                                     pack_bf16x2(f[6] * inv, f[7] * inv));
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(3 + k, BM);
+                    if (r == 0) {
+                        tma_store_4d(&tm_o, stage, sub * 64, ti.q0, itm.hq, itm.b);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                    }
+                }
+            } else if (row_ok) {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
+                                                      (((size_t)itm.b * a.Sq + row_q) * a.Hq + itm.hq) * D);
+#pragma unroll
+                for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (row_ok && a.lse)
+                a.lse[((size_t)itm.b * a.Sq + row_q) * a.Hq + itm.hq] =
+                    l_run > 0.f ? (m_ref + log2f(l_run)) * kLn2 : -INFINITY;
+            tc_fence_before();
+            if (!named_bar_and(3 + k, BM, ok)) break;     // the whole warpgroup stops together
         }
-        const bool row_ok = r < ti.rows_valid;
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        // O / l as bf16 goes into this tile's Q buffer (its S products are all
-        // done once o_final has arrived) in the 128-byte-swizzled box layout of
-        // the output map, and one thread stores the tile with TMA: whole
-        // 128-byte rows instead of 16-byte pieces strided by Hq * D.  Rows past
-        // Sq lie outside the map and are not written.  A tile with no visited
-        // key (its Q load may still be landing) or a wait that gave up writes
-        // zeros directly.
-        const bool staged = named_bar_and(3 + k, BM, ok && it > 0);
-        if (staged) {
-            const uint32_t obuf = sb + C::OFF_Q + k * C::TILE_BYTES;
-            uint32_t ow[D];
-            if constexpr (D == 128) {
-                tmem_ld128(tmem + lane_addr + col_o, ow);
-            } else {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c)
-                    tmem_ld32(tmem + lane_addr + col_o + 32 * c, reinterpret_cast<float*>(ow + 32 * c));
-            }
-#pragma unroll
-            for (int q = 0; q < D / 8; ++q) {          // 16-byte chunk q of the row
-                const float* f = reinterpret_cast<const float*>(ow + 8 * q);
-                st_shared_v4(obuf + (q / 8) * C::SUB_BYTES + r * 128 + (((q % 8) ^ (r & 7)) << 4),
-                             pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                             pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(3 + k, BM);
-            if (r == 0) {
-#pragma unroll
-                for (int sub = 0; sub < C::KSUB; ++sub)
-                    tma_store_4d(&tm_o, obuf + sub * C::SUB_BYTES, sub * 64, ti.q0, hq, b);
-                bulk_commit_group();
-                bulk_wait_read_all();
-            }
-        } else if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
-                                                  (((size_t)b * a.Sq + row_q) * a.Hq + hq) * D);
-#pragma unroll
-            for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (row_ok && a.lse)
-            a.lse[((size_t)b * a.Sq + row_q) * a.Hq + hq] =
-                l_run > 0.f ? (m_ref + log2f(l_run)) * kLn2 : -INFINITY;
-        tc_fence_before();
         named_bar_arrive(2, 8 * 32 + 32);
         if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_prefill_error, (int)kErrPrefillWait);
     }
-
 }
 
 __global__ void exp2_poly_kernel(const float* x, float* y, long n) {
@@ -604,7 +712,9 @@ cudaError_t launch_prefill_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_qpairs = (a.Sq + NQ * BM - 1) / (NQ * BM);
-    const long grid = (long)n_qpairs * a.B * a.Hq;
+    const long n_items = (long)n_qpairs * a.B * a.Hq;
+    const long sms = a.num_sms > 0 ? a.num_sms : 148;
+    const long grid = n_items < sms ? n_items : sms;    // persistent: one CTA per SM
     prefill_kernel<D><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, tm_o, a, n_qpairs);
     return cudaGetLastError();
 }
