@@ -75,6 +75,24 @@ def load_peaks():
 
 
 # --------------------------------------------------------------------------- workload
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
+# kernel, taken once with ncu on the kernel as it stands: for the decode
+# workloads as a ratio to the algorithmic K/V bytes (their captures ran at a
+# reduced batch), for the prefill as bytes per launch of the same workload.
+TRAFFIC = {
+    "paged_decode": ("ratio", (559.396864 + 5.465344) / 556.916736),
+    "wide_group_decode": ("ratio", (233.606656 + 4.270080) / 232.683520),
+    "qwen3_8b_prefill": ("bytes", (93.515776 + 30.323200) * 1e6),
+}
+
+
+def traffic_per_launch(part):
+    t = TRAFFIC.get(part.name)
+    if t is None:
+        return None
+    return t[1] * part.bytes if t[0] == "ratio" else t[1]
+
+
 class Part:
     """One piece of the step: a dense prefill or a paged decode."""
 
@@ -310,11 +328,17 @@ def bench_ours(args, world, rank, local):
         ach = dom.flops / dom_t / 1e12
         roof = dict(kernel="prefill_kernel<128> (" + dom.name + ")", bound="tensor", achieved=ach,
                     peak=peaks["bf16_tflops"], unit="TFLOP/s", frac=ach / peaks["bf16_tflops"],
-                    traffic=None, peak_source=peaks["source"] + " bf16 burst")
+                    traffic=traffic_per_launch(dom), peak_source=peaks["source"] + " bf16 burst")
     else:
         ach = dom.bytes / dom_t / 1e9
-        roof = dict(kernel="decode_split_kernel + decode_combine_kernel (" + dom.name + ")", bound="hbm",
-                    achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s", frac=ach / peaks["hbm_gbs"], traffic=None,
+        c = dom.data["config"]
+        rows = c["Hq"] // c["Hkv"] * c["Sq"]
+        tc = c["D"] in (128, 256) and 32 <= rows <= 128 and c["page_size"] % 8 == 0 and (
+            c["page_size"] >= 64 or 64 % c["page_size"] == 0)
+        split = "decode_tc_kernel<%d>" % c["D"] if tc else "decode_tma_kernel<%d,%d>" % (c["D"], min(4, (rows + 15) // 16))
+        roof = dict(kernel=split + " + decode_combine_kernel<%d> (%s)" % (c["D"], dom.name), bound="hbm",
+                    achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s", frac=ach / peaks["hbm_gbs"],
+                    traffic=traffic_per_launch(dom),
                     peak_source=peaks["source"] + " copy bandwidth")
 
     e2e = bench_e2e(args, parts, peaks, dev, stream, world)
