@@ -33,6 +33,15 @@ def _bind(lib):
     lib.oracle_attn_paged.argtypes = ([vp] * 3 + [ip] + [vp] * 2 + [ip] + [vp] * 3 + [ip] * 8
                                       + [ctypes.c_double, ip])
     lib.oracle_attn_paged.restype = ip
+    lp, dp = ctypes.c_long, ctypes.c_double
+    lib.oracle_attn_dense_ex.argtypes = ([vp] * 3 + [ip] + [vp] * 3 + [ip] * 7 + [dp, lp, lp, dp, vp, ip])
+    lib.oracle_attn_dense_ex.restype = ip
+    lib.oracle_attn_dense_rows_ex.argtypes = ([vp] * 3 + [ip] + [vp] * 2 + [ip] + [vp] * 2 + [ip] * 7
+                                              + [dp, lp, lp, dp, vp, ip])
+    lib.oracle_attn_dense_rows_ex.restype = ip
+    lib.oracle_attn_paged_ex.argtypes = ([vp] * 3 + [ip] + [vp] * 2 + [ip] + [vp] * 3 + [ip] * 8
+                                         + [dp, lp, lp, dp, vp, ip])
+    lib.oracle_attn_paged_ex.restype = ip
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ip
     return lib
@@ -81,6 +90,8 @@ _ERRORS = {
     -4: "row index out of range",
     -5: "a request length lies outside [0, max_pages * page_size]",
     -6: "a block_table entry for a used page lies outside [0, num_pages)",
+    -7: "a window size below -1",
+    -8: "softcap must be finite and >= 0",
 }
 
 
@@ -128,13 +139,29 @@ def _mask_in(mask):
     return np.ascontiguousarray(mask, dtype=np.uint8)
 
 
+def _opts(window_left, window_right, softcap, sinks, Hq):
+    """The optional terms as C arguments: (wl, wr, softcap, sinks array or None)."""
+    sk = None
+    if sinks is not None:
+        sk = np.ascontiguousarray(torch.as_tensor(sinks).detach().cpu().to(torch.float64).numpy().reshape(-1))
+        if sk.shape[0] != Hq:
+            raise ValueError("oracle: sinks must hold one value per query head")
+    return int(window_left), int(window_right), float(0.0 if softcap is None else softcap), sk
+
+
 def default_scale(D: int) -> float:
     """Scale used when the caller passes None: 1/sqrt(D)."""
     return 1.0 / math.sqrt(D)
 
 
-def attn_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, nthreads=0):
-    """Dense GQA attention in double.  q: [B,Sq,Hq,D]; k, v: [B,Skv,Hkv,D]."""
+def attn_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, nthreads=0,
+               window_left=-1, window_right=-1, softcap=0.0, sinks=None):
+    """Dense GQA attention in double.  q: [B,Sq,Hq,D]; k, v: [B,Skv,Hkv,D].
+
+    window_left / window_right: keys admitted left / right of the query's key
+    position (-1 unlimited); softcap: c > 0 caps each scaled score to
+    c*tanh(z/c) (0 or None off); sinks: [Hq] logits added to the softmax
+    denominator only, or None."""
     B, Sq, Hq, D = q.shape
     _, Skv, Hkv, _ = k.shape
     if scale is None:
@@ -143,14 +170,16 @@ def attn_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, nthreads
     m = _mask_in(key_padding_mask)
     o = np.zeros((B, Sq, Hq, D), dtype=np.float64)
     lse = np.zeros((B, Sq, Hq), dtype=np.float64)
-    rc = _load().oracle_attn_dense(_ptr(qa), _ptr(ka), _ptr(va), c, _ptr(m), _ptr(o), _ptr(lse),
-                                   B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
-                                   int(nthreads))
+    wl, wr, cap, sk = _opts(window_left, window_right, softcap, sinks, Hq)
+    rc = _load().oracle_attn_dense_ex(_ptr(qa), _ptr(ka), _ptr(va), c, _ptr(m), _ptr(o), _ptr(lse),
+                                      B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
+                                      wl, wr, cap, _ptr(sk), int(nthreads))
     _check(rc)
     return torch.from_numpy(o), torch.from_numpy(lse)
 
 
-def attn_dense_rows(q, k, v, rows, key_padding_mask=None, causal=True, scale=None, nthreads=0):
+def attn_dense_rows(q, k, v, rows, key_padding_mask=None, causal=True, scale=None, nthreads=0,
+                    window_left=-1, window_right=-1, softcap=0.0, sinks=None):
     """Dense attention for the listed rows only.
 
     rows: integer array [n, 3] of (b, i, h).  Returns o_rows [n, D], lse_rows [n].
@@ -165,15 +194,17 @@ def attn_dense_rows(q, k, v, rows, key_padding_mask=None, causal=True, scale=Non
     n = r.shape[0]
     o = np.zeros((n, D), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
-    rc = _load().oracle_attn_dense_rows(_ptr(qa), _ptr(ka), _ptr(va), c, _ptr(m), _ptr(r), n,
-                                        _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
-                                        int(bool(causal)), float(scale), int(nthreads))
+    wl, wr, cap, sk = _opts(window_left, window_right, softcap, sinks, Hq)
+    rc = _load().oracle_attn_dense_rows_ex(_ptr(qa), _ptr(ka), _ptr(va), c, _ptr(m), _ptr(r), n,
+                                           _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
+                                           int(bool(causal)), float(scale), wl, wr, cap, _ptr(sk),
+                                           int(nthreads))
     _check(rc)
     return torch.from_numpy(o), torch.from_numpy(lse)
 
 
 def attn_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=True, scale=None,
-               requests=None, nthreads=0):
+               requests=None, nthreads=0, window_left=-1, window_right=-1, softcap=0.0, sinks=None):
     """Paged GQA attention in double.
 
     q: [B,Sq,Hq,D]; k_cache, v_cache: [num_pages, page_size, Hkv, D];
@@ -195,8 +226,10 @@ def attn_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=True, sc
         req[np.asarray(list(requests), dtype=np.int64)] = 1
     o = np.zeros((B, Sq, Hq, D), dtype=np.float64)
     lse = np.zeros((B, Sq, Hq), dtype=np.float64)
-    rc = _load().oracle_attn_paged(_ptr(qa), _ptr(ka), _ptr(va), c, _ptr(sl), _ptr(bt), page_size,
-                                   _ptr(req), _ptr(o), _ptr(lse), B, Sq, Hq, Hkv, D, num_pages,
-                                   max_pages, int(bool(causal)), float(scale), int(nthreads))
+    wl, wr, cap, sk = _opts(window_left, window_right, softcap, sinks, Hq)
+    rc = _load().oracle_attn_paged_ex(_ptr(qa), _ptr(ka), _ptr(va), c, _ptr(sl), _ptr(bt), page_size,
+                                      _ptr(req), _ptr(o), _ptr(lse), B, Sq, Hq, Hkv, D, num_pages,
+                                      max_pages, int(bool(causal)), float(scale), wl, wr, cap,
+                                      _ptr(sk), int(nthreads))
     _check(rc)
     return torch.from_numpy(o), torch.from_numpy(lse)

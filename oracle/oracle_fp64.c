@@ -26,6 +26,22 @@
  *   MATE "QSA", Core Attention: the log-sum-exp is natural-log, of the
  *     scaled logits, and -inf for a row with no visible key.
  *
+ * Optional terms (TileOPs "Attention Operators", GQADenseFwdOp stages 5 and
+ * 6, and GQAPagedFwdOp's sinks):
+ *   window:  with wL = window_left and wR = window_right (negative =
+ *            unlimited), key j is visible to row i only if j >= p_i - wL and
+ *            j <= p_i + wR, on top of the causal and padding conditions;
+ *   softcap: with c > 0 every visible logit z becomes c * tanh(z / c); c = 0
+ *            leaves it unchanged;
+ *   sinks:   a logit s_h per query head joins the softmax denominator only
+ *            (no value, not scaled, not capped): weight_j = exp(z_j) /
+ *            (sum_{j in V_i} exp(z_j) + exp(s_h)), and the log-sum-exp
+ *            includes exp(s_h).  s_h = -inf adds nothing; s_h = +inf makes
+ *            the row's output zero (and its log-sum-exp +inf).  A row with no
+ *            visible key still outputs zeros with log-sum-exp -inf (the pages
+ *            fix the zero output; -inf keeps "zero row <=> -inf" whether a
+ *            sink is given or not).
+ *
  * softmax_j(z) is written out as its definition: with M = max_{j in V_i} z_j
  * and Z = sum_{j in V_i} exp(z_j - M), weight_j = exp(z_j - M) / Z and
  * LSE = M + log Z.  Subtracting M changes nothing mathematically; it only
@@ -63,10 +79,19 @@ static double load_elem(const void* base, size_t idx, int dtype) {
  *   z      : scratch of Skv doubles
  *   out    : D doubles; *lse_out : the row's log-sum-exp
  */
+/* Optional terms of one call (see the header). */
+typedef struct {
+    long window_left, window_right;            /* negative = unlimited */
+    double softcap;                            /* 0 = off */
+    const double* sinks;                       /* [Hq] or NULL */
+} oracle_opts;
+
+static const oracle_opts NO_OPTS = {-1, -1, 0.0, NULL};
+
 static void dense_row(const void* q, const void* k, const void* v, int dtype,
                       const uint8_t* mask, int Hq, int Hkv, int Sq, int Skv,
-                      int D, int causal, double scale, int b, int i, int h,
-                      double* z, double* out, double* lse_out) {
+                      int D, int causal, double scale, const oracle_opts* opt,
+                      int b, int i, int h, double* z, double* out, double* lse_out) {
     const int g = Hq / Hkv;
     const int r = h / g;                       /* KV head of query head h */
     const long p = (long)i + Skv - Sq;         /* query position on the key axis */
@@ -76,6 +101,8 @@ static void dense_row(const void* q, const void* k, const void* v, int dtype,
     double M = -INFINITY;
     for (int j = 0; j < Skv; ++j) {
         int visible = (!causal || (long)j <= p) &&
+                      (opt->window_left < 0 || (long)j >= p - opt->window_left) &&
+                      (opt->window_right < 0 || (long)j <= p + opt->window_right) &&
                       (mask == NULL || mask[(size_t)b * Skv + j] != 0);
         if (!visible) { z[j] = -INFINITY; continue; }
         const size_t k_off = (((size_t)b * Skv + j) * Hkv + r) * (size_t)D;
@@ -83,6 +110,7 @@ static void dense_row(const void* q, const void* k, const void* v, int dtype,
         for (int d = 0; d < D; ++d)
             dot += load_elem(q, q_off + d, dtype) * load_elem(k, k_off + d, dtype);
         z[j] = scale * dot;
+        if (opt->softcap > 0.0) z[j] = opt->softcap * tanh(z[j] / opt->softcap);
         if (!any || z[j] > M) M = z[j];
         any = 1;
     }
@@ -92,7 +120,15 @@ static void dense_row(const void* q, const void* k, const void* v, int dtype,
         *lse_out = -INFINITY;
         return;
     }
-    double Z = 0.0;
+    /* A sink joins the denominator: it takes part in the maximum that keeps
+     * exp() finite, and adds exp(s - M) to Z. */
+    const double sink = opt->sinks ? opt->sinks[h] : -INFINITY;
+    if (sink == INFINITY) {                    /* the sink takes all the weight */
+        *lse_out = INFINITY;
+        return;
+    }
+    if (sink > M) M = sink;
+    double Z = sink == -INFINITY ? 0.0 : exp(sink - M);
     for (int j = 0; j < Skv; ++j)
         if (z[j] != -INFINITY) Z += exp(z[j] - M);
     for (int j = 0; j < Skv; ++j) {
@@ -132,10 +168,10 @@ int oracle_max_threads(void) {
  * Returns 0, -1 for a bad size, -2 when Hq is not a multiple of Hkv,
  * -3 when scratch memory cannot be had.
  */
-int oracle_attn_dense(const void* q, const void* k, const void* v, int dtype,
-                      const uint8_t* mask, double* o, double* lse, int B,
-                      int Hq, int Hkv, int Sq, int Skv, int D, int causal,
-                      double scale, int nthreads) {
+static int dense_all(const void* q, const void* k, const void* v, int dtype,
+                     const uint8_t* mask, double* o, double* lse, int B,
+                     int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                     double scale, const oracle_opts* opt, int nthreads) {
     int rc = check_dense_args(B, Hq, Hkv, Sq, Skv, D);
     if (rc) return rc;
     set_threads(nthreads);
@@ -154,7 +190,7 @@ int oracle_attn_dense(const void* q, const void* k, const void* v, int dtype,
                 const int i = (int)((row / Hq) % Sq);
                 const int b = (int)(row / ((long)Hq * Sq));
                 dense_row(q, k, v, dtype, mask, Hq, Hkv, Sq, Skv, D, causal,
-                          scale, b, i, h, z, o + (size_t)row * D, lse + row);
+                          scale, opt, b, i, h, z, o + (size_t)row * D, lse + row);
             }
             free(z);
         }
@@ -162,16 +198,48 @@ int oracle_attn_dense(const void* q, const void* k, const void* v, int dtype,
     return failed ? -3 : 0;
 }
 
+static int check_opts(long window_left, long window_right, double softcap) {
+    if (window_left < -1 || window_right < -1) return -7;
+    if (!(softcap >= 0.0) || softcap == INFINITY) return -8;
+    return 0;
+}
+
+int oracle_attn_dense(const void* q, const void* k, const void* v, int dtype,
+                      const uint8_t* mask, double* o, double* lse, int B,
+                      int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                      double scale, int nthreads) {
+    return dense_all(q, k, v, dtype, mask, o, lse, B, Hq, Hkv, Sq, Skv, D, causal,
+                     scale, &NO_OPTS, nthreads);
+}
+
+/*
+ * oracle_attn_dense with the optional terms: window_left / window_right
+ * (-1 = unlimited), softcap (0 = off), sinks ([Hq] doubles or NULL).
+ * Also returns -7 for a window below -1 and -8 for a negative or non-finite
+ * softcap.
+ */
+int oracle_attn_dense_ex(const void* q, const void* k, const void* v, int dtype,
+                         const uint8_t* mask, double* o, double* lse, int B,
+                         int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                         double scale, long window_left, long window_right,
+                         double softcap, const double* sinks, int nthreads) {
+    int rc = check_opts(window_left, window_right, softcap);
+    if (rc) return rc;
+    const oracle_opts opt = {window_left, window_right, softcap, sinks};
+    return dense_all(q, k, v, dtype, mask, o, lse, B, Hq, Hkv, Sq, Skv, D, causal,
+                     scale, &opt, nthreads);
+}
+
 /*
  * Dense attention for a list of rows only.  rows: nrows triples (b, i, h);
  * o_rows: [nrows, D]; lse_rows: [nrows].  Same return codes, plus -4 for a
  * row index out of range.
  */
-int oracle_attn_dense_rows(const void* q, const void* k, const void* v,
-                           int dtype, const uint8_t* mask, const int32_t* rows,
-                           int nrows, double* o_rows, double* lse_rows, int B,
-                           int Hq, int Hkv, int Sq, int Skv, int D, int causal,
-                           double scale, int nthreads) {
+static int dense_rows(const void* q, const void* k, const void* v,
+                      int dtype, const uint8_t* mask, const int32_t* rows,
+                      int nrows, double* o_rows, double* lse_rows, int B,
+                      int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                      double scale, const oracle_opts* opt, int nthreads) {
     int rc = check_dense_args(B, Hq, Hkv, Sq, Skv, D);
     if (rc) return rc;
     for (int n = 0; n < nrows; ++n) {
@@ -191,12 +259,35 @@ int oracle_attn_dense_rows(const void* q, const void* k, const void* v,
 #pragma omp for schedule(dynamic, 1)
             for (int n = 0; n < nrows; ++n)
                 dense_row(q, k, v, dtype, mask, Hq, Hkv, Sq, Skv, D, causal,
-                          scale, rows[3 * n], rows[3 * n + 1], rows[3 * n + 2],
+                          scale, opt, rows[3 * n], rows[3 * n + 1], rows[3 * n + 2],
                           z, o_rows + (size_t)n * D, lse_rows + n);
             free(z);
         }
     }
     return failed ? -3 : 0;
+}
+
+int oracle_attn_dense_rows(const void* q, const void* k, const void* v,
+                           int dtype, const uint8_t* mask, const int32_t* rows,
+                           int nrows, double* o_rows, double* lse_rows, int B,
+                           int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                           double scale, int nthreads) {
+    return dense_rows(q, k, v, dtype, mask, rows, nrows, o_rows, lse_rows, B, Hq, Hkv,
+                      Sq, Skv, D, causal, scale, &NO_OPTS, nthreads);
+}
+
+/* oracle_attn_dense_rows with the optional terms (as oracle_attn_dense_ex). */
+int oracle_attn_dense_rows_ex(const void* q, const void* k, const void* v,
+                              int dtype, const uint8_t* mask, const int32_t* rows,
+                              int nrows, double* o_rows, double* lse_rows, int B,
+                              int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                              double scale, long window_left, long window_right,
+                              double softcap, const double* sinks, int nthreads) {
+    int rc = check_opts(window_left, window_right, softcap);
+    if (rc) return rc;
+    const oracle_opts opt = {window_left, window_right, softcap, sinks};
+    return dense_rows(q, k, v, dtype, mask, rows, nrows, o_rows, lse_rows, B, Hq, Hkv,
+                      Sq, Skv, D, causal, scale, &opt, nthreads);
 }
 
 /*
@@ -217,12 +308,13 @@ int oracle_attn_dense_rows(const void* q, const void* k, const void* v,
  * outside [0, max_pages * page_size]; -6 a needed block_table entry outside
  * [0, num_pages).
  */
-int oracle_attn_paged(const void* q, const void* k_cache, const void* v_cache,
-                      int dtype, const int32_t* seqlens,
-                      const int32_t* block_table, int page_size,
-                      const uint8_t* req_mask, double* o, double* lse, int B,
-                      int Sq, int Hq, int Hkv, int D, int num_pages,
-                      int max_pages, int causal, double scale, int nthreads) {
+static int paged_all(const void* q, const void* k_cache, const void* v_cache,
+                     int dtype, const int32_t* seqlens,
+                     const int32_t* block_table, int page_size,
+                     const uint8_t* req_mask, double* o, double* lse, int B,
+                     int Sq, int Hq, int Hkv, int D, int num_pages,
+                     int max_pages, int causal, double scale, const oracle_opts* opt,
+                     int nthreads) {
     int rc = check_dense_args(B, Hq, Hkv, Sq, 0, D);
     if (rc) return rc;
     if (page_size <= 0 || num_pages < 0 || max_pages < 0) return -1;
@@ -255,12 +347,40 @@ int oracle_attn_paged(const void* q, const void* k_cache, const void* v_cache,
                    tok_elems * es);
         }
         const char* qb = (const char*)q + (size_t)b * Sq * Hq * D * es;
-        rc = oracle_attn_dense(qb, kd, vd, dtype, NULL,
-                               o + (size_t)b * Sq * Hq * D, lse + (size_t)b * Sq * Hq,
-                               1, Hq, Hkv, Sq, L, D, causal, scale, nthreads);
+        rc = dense_all(qb, kd, vd, dtype, NULL,
+                       o + (size_t)b * Sq * Hq * D, lse + (size_t)b * Sq * Hq,
+                       1, Hq, Hkv, Sq, L, D, causal, scale, opt, nthreads);
         free(kd);
         free(vd);
         if (rc) return rc;
     }
     return 0;
+}
+
+int oracle_attn_paged(const void* q, const void* k_cache, const void* v_cache,
+                      int dtype, const int32_t* seqlens,
+                      const int32_t* block_table, int page_size,
+                      const uint8_t* req_mask, double* o, double* lse, int B,
+                      int Sq, int Hq, int Hkv, int D, int num_pages,
+                      int max_pages, int causal, double scale, int nthreads) {
+    return paged_all(q, k_cache, v_cache, dtype, seqlens, block_table, page_size, req_mask,
+                     o, lse, B, Sq, Hq, Hkv, D, num_pages, max_pages, causal, scale,
+                     &NO_OPTS, nthreads);
+}
+
+/* oracle_attn_paged with the optional terms (as oracle_attn_dense_ex). */
+int oracle_attn_paged_ex(const void* q, const void* k_cache, const void* v_cache,
+                         int dtype, const int32_t* seqlens,
+                         const int32_t* block_table, int page_size,
+                         const uint8_t* req_mask, double* o, double* lse, int B,
+                         int Sq, int Hq, int Hkv, int D, int num_pages,
+                         int max_pages, int causal, double scale, long window_left,
+                         long window_right, double softcap, const double* sinks,
+                         int nthreads) {
+    int rc = check_opts(window_left, window_right, softcap);
+    if (rc) return rc;
+    const oracle_opts opt = {window_left, window_right, softcap, sinks};
+    return paged_all(q, k_cache, v_cache, dtype, seqlens, block_table, page_size, req_mask,
+                     o, lse, B, Sq, Hq, Hkv, D, num_pages, max_pages, causal, scale, &opt,
+                     nthreads);
 }

@@ -6,8 +6,13 @@ logsumexp in float64, exact special cases (one visible key, q = 0, scale = 0,
 rows with no visible key), structural identities (GQA equals MHA with
 repeat_interleaved K/V, paged equals dense after scattering the cache through a
 random block table, chunked prefill equals full prefill, row independence) and
-invariants (convex hull, translation of V).  The last test plants mistakes in
-copies of the oracle and checks that the pins catch every one.
+invariants (convex hull, translation of V).  The optional terms are pinned the
+same way: a zero left window leaves one key (exact value), a window equals the
+plain definition over the sliced keys, softcap has closed forms for two keys
+(tanh 40 = 1; 2 tanh(ln(3)/2) = 1) and vanishes for a huge cap, sinks obey the
+denominator identity O_s = O / (1 + exp(s - LSE)), and paged equals dense with
+all three.  The last test plants mistakes in copies of the oracle and checks
+that the pins catch every one.
 """
 import math
 import os
@@ -315,11 +320,131 @@ def pin_high_precision_rows():
         assert abs(float(mpmath.log(den)) - lse[0, i, h].item()) < 1e-14
 
 
+# ----------------------------------------------------------------------------- optional terms
+# TileOPs "Attention Operators", GQADenseFwdOp stages 5 and 6 (window, softcap)
+# and GQAPagedFwdOp's sinks.
+def pin_window_single_key_exact():
+    # causal with window_left = 0: row i sees key p_i only -> O = V[p_i] exactly,
+    # LSE = scale <q_i, k_{p_i}>; the same with a cap (one key takes all the weight)
+    q, k, v, _ = _rand_case(2, 4, 2, 5, 9, 8, seed=21)
+    scale = 0.25
+    for cap in (0.0, 0.3):
+        o, lse = oracle.attn_dense(q, k, v, causal=True, scale=scale, window_left=0, softcap=cap)
+        for b in range(2):
+            for i in range(5):
+                p = i + 9 - 5
+                for h in range(4):
+                    r = h // 2
+                    assert torch.equal(o[b, i, h], v[b, p, r].double())
+                    if cap == 0.0:
+                        dot = math.fsum(float(a) * float(c) for a, c in zip(q[b, i, h].double(),
+                                                                           k[b, p, r].double()))
+                        assert abs(lse[b, i, h].item() - scale * dot) <= 1e-15 * max(1.0, abs(scale * dot))
+
+
+def pin_window_equals_key_slice():
+    # a window only removes keys: row i equals the plain non-causal definition over
+    # keys [max(0, p_i - wL), min(Skv - 1, p_i (causal), p_i + wR)] alone
+    B, Hq, Hkv, Sq, Skv, D = 1, 4, 2, 6, 14, 8
+    q, k, v, mask = _rand_case(B, Hq, Hkv, Sq, Skv, D, seed=22, mask_p=0.8)
+    for causal, wl, wr in ((True, 3, -1), (False, 2, 4), (False, 0, 0), (True, 20, -1), (False, -1, 1)):
+        o, lse = oracle.attn_dense(q, k, v, key_padding_mask=mask, causal=causal, window_left=wl,
+                                   window_right=wr)
+        for i in range(Sq):
+            p = i + Skv - Sq
+            lo = 0 if wl < 0 else max(0, p - wl)
+            hi = Skv - 1
+            if causal:
+                hi = min(hi, p)
+            if wr >= 0:
+                hi = min(hi, p + wr)
+            if lo > hi or not bool(mask[0, lo:hi + 1].any()):
+                assert torch.equal(o[0, i], torch.zeros(Hq, D, dtype=torch.float64))
+                assert bool(torch.all(lse[0, i] == float("-inf")))
+                continue
+            ro, rl = oracle.attn_dense(q[:, i:i + 1], k[:, lo:hi + 1], v[:, lo:hi + 1],
+                                       key_padding_mask=mask[:, lo:hi + 1], causal=False)
+            assert (o[0, i] - ro[0, 0]).abs().max().item() < 1e-13
+            assert (lse[0, i] - rl[0, 0]).abs().max().item() < 1e-13
+
+
+def pin_softcap_closed_forms():
+    # two visible keys, scaled scores z = (40, 0) and cap 1: logits (tanh 40 = 1, 0), so
+    # the weights are e/(e+1), 1/(e+1) and LSE = log(e + 1); scores (ln 3, 0) and cap 2
+    # give logits (2 tanh(ln(3)/2) = 1, 0): the same weights
+    D = 4
+    v = torch.tensor([[1.0, -2.0, 0.5, 3.0], [-1.0, 4.0, 2.0, 0.0]], dtype=torch.float64).view(1, 2, 1, D)
+    w0 = math.e / (math.e + 1.0)
+    want = w0 * v[0, 0, 0] + (1.0 - w0) * v[0, 1, 0]
+    for z0, cap in ((40.0, 1.0), (math.log(3.0), 2.0)):
+        q = torch.zeros(1, 1, 1, D, dtype=torch.float64)
+        q[0, 0, 0, 0] = z0
+        k = torch.zeros(1, 2, 1, D, dtype=torch.float64)
+        k[0, 0, 0, 0] = 1.0
+        o, lse = oracle.attn_dense(q, k, v, causal=False, scale=1.0, softcap=cap)
+        assert (o[0, 0, 0] - want).abs().max().item() < 1e-14
+        assert abs(lse[0, 0, 0].item() - math.log(math.e + 1.0)) < 1e-14
+
+
+def pin_softcap_large_cap_limit():
+    # c tanh(z / c) = z - z^3 / (3 c^2) + ...: a cap of 1e9 leaves the result unchanged
+    q, k, v, mask = _rand_case(2, 4, 2, 5, 11, 8, seed=23, mask_p=0.7)
+    o0, l0 = oracle.attn_dense(q, k, v, key_padding_mask=mask, causal=True)
+    o1, l1 = oracle.attn_dense(q, k, v, key_padding_mask=mask, causal=True, softcap=1e9)
+    assert (o0 - o1).abs().max().item() < 1e-12
+    fin = torch.isfinite(l0)
+    assert torch.equal(fin, torch.isfinite(l1))
+    assert (l0[fin] - l1[fin]).abs().max().item() < 1e-12
+
+
+def pin_sinks_identity():
+    # a sink adds exp(s_h) to the denominator only: O_s = O exp(LSE) / (exp(LSE) + exp(s)),
+    # LSE_s = log(exp(LSE) + exp(s)); s = -inf changes nothing, s = +inf zeroes the
+    # output (LSE +inf); a row with no visible key stays zero with LSE -inf
+    q, k, v, mask = _rand_case(2, 4, 2, 5, 7, 8, seed=24, mask_p=0.6)
+    o0, l0 = oracle.attn_dense(q, k, v, key_padding_mask=mask, causal=True)
+    inf = float("inf")
+    sinks = torch.tensor([0.3, -1.5, 4.0, -inf], dtype=torch.float64)
+    o1, l1 = oracle.attn_dense(q, k, v, key_padding_mask=mask, causal=True, sinks=sinks)
+    for b in range(2):
+        for i in range(5):
+            for h in range(4):
+                base, s = l0[b, i, h].item(), sinks[h].item()
+                if base == -inf:
+                    assert torch.equal(o1[b, i, h], torch.zeros(8, dtype=torch.float64))
+                    assert l1[b, i, h].item() == -inf
+                    continue
+                frac = 1.0 / (1.0 + math.exp(s - base)) if s != -inf else 1.0
+                assert (o1[b, i, h] - o0[b, i, h] * frac).abs().max().item() < 1e-13
+                want = base if s == -inf else max(base, s) + math.log1p(math.exp(-abs(base - s)))
+                assert abs(l1[b, i, h].item() - want) < 1e-13
+    o2, l2 = oracle.attn_dense(q, k, v, key_padding_mask=mask, causal=True,
+                               sinks=torch.tensor([inf, 0.0, 0.0, 0.0], dtype=torch.float64))
+    has = torch.isfinite(l0[:, :, 0])
+    assert bool(torch.all(o2[:, :, 0] == 0.0))
+    assert bool(torch.all(l2[:, :, 0][has] == inf)) and bool(torch.all(l2[:, :, 0][~has] == -inf))
+
+
+def pin_options_paged_equals_dense():
+    # the optional terms act on the logical sequence: paged with window, cap and
+    # sinks equals dense on the gathered cache
+    q, k, v, _ = _rand_case(1, 4, 2, 3, 40, 8, seed=25)
+    kc, vc, table = _scatter_to_pages(k, v, [40], 8, seed=5)
+    sinks = torch.tensor([0.5, -0.5, 1.0, -2.0], dtype=torch.float64)
+    od, ld = oracle.attn_dense(q, k, v, causal=True, window_left=9, softcap=5.0, sinks=sinks)
+    op, lp = oracle.attn_paged(q, kc, vc, torch.tensor([40], dtype=torch.int32), table, causal=True,
+                               window_left=9, softcap=5.0, sinks=sinks)
+    assert (od - op).abs().max().item() < 1e-14
+    assert (ld - lp).abs().max().item() < 1e-14
+
+
 PINS = [pin_golden_closed_form, pin_matches_torch_sdpa, pin_lse_matches_torch_logsumexp,
         pin_single_visible_key_exact, pin_zero_query_is_mean_of_visible_values,
         pin_gqa_equals_repeat_interleave_mha, pin_paged_equals_dense,
         pin_rows_without_visible_keys, pin_invariants, pin_chunked_prefill_and_row_independence,
-        pin_noncausal_key_permutation, pin_high_precision_rows]
+        pin_noncausal_key_permutation, pin_high_precision_rows, pin_window_single_key_exact,
+        pin_window_equals_key_slice, pin_softcap_closed_forms, pin_softcap_large_cap_limit,
+        pin_sinks_identity, pin_options_paged_equals_dense]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -362,7 +487,12 @@ def test_workload_generator_is_deterministic():
 MUTANTS = {
     "head_map_modulo": ("const int r = h / g;", "const int r = h % Hkv;"),
     "causal_top_left": ("const long p = (long)i + Skv - Sq;", "const long p = (long)i;"),
-    "causal_off_by_one": ("(long)j <= p", "(long)j < p"),
+    "causal_off_by_one": ("(!causal || (long)j <= p)", "(!causal || (long)j < p)"),
+    "window_left_off_by_one": ("(long)j >= p - opt->window_left", "(long)j > p - opt->window_left"),
+    "window_right_ignored": ("(opt->window_right < 0 || (long)j <= p + opt->window_right)", "1"),
+    "softcap_scale_dropped": ("opt->softcap * tanh(z[j] / opt->softcap)", "tanh(z[j] / opt->softcap)"),
+    "sink_ignored": ("double Z = sink == -INFINITY ? 0.0 : exp(sink - M);", "double Z = 0.0;"),
+    "sink_plus_inf_unhandled": ("if (sink == INFINITY) {", "if (0) {"),
     "mask_ignored": ("mask[(size_t)b * Skv + j] != 0", "1"),
     "scale_dropped": ("z[j] = scale * dot;", "z[j] = dot;"),
     "lse_missing_log": ("*lse_out = M + log(Z);", "*lse_out = M + Z;"),
