@@ -41,6 +41,10 @@ def load() -> ctypes.CDLL:
     lib.attn_fwd_dense.restype = i
     lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, i, vp, vp] + [i] * 8 + [f, vp, sz, vp]
     lib.attn_decode_paged.restype = i
+    lib.attn_fwd_dense_ex.argtypes = [vp, vp, vp, vp, vp, vp] + [i] * 7 + [f, vp, vp]
+    lib.attn_fwd_dense_ex.restype = i
+    lib.attn_decode_paged_ex.argtypes = [vp, vp, vp, vp, vp, i, vp, vp] + [i] * 8 + [f, vp, vp, sz, vp]
+    lib.attn_decode_paged_ex.restype = i
     lib.attn_decode_paged_workspace_size.argtypes = [i] * 7
     lib.attn_decode_paged_workspace_size.restype = sz
     lib.attn_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, i, vp, vp] + [i] * 8 + [f, vp]
@@ -59,6 +63,12 @@ def load() -> ctypes.CDLL:
     lib.gqa_version.restype = ctypes.c_char_p
     _handle = lib
     return lib
+
+
+class Options(ctypes.Structure):
+    """gqa_options of include/gqa_attn.h."""
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int), ("softcap", ctypes.c_float),
+                ("sinks", ctypes.c_void_p)]
 
 
 def status_name(code: int) -> str:

@@ -47,11 +47,36 @@ def resolve_scale(scale, D):
     return 1.0 / math.sqrt(D) if scale is None else float(scale)
 
 
-def attn_fwd_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, out=None, lse=None):
+def _options(window_left, window_right, softcap, sinks, Hq, device):
+    """gqa_options for the optional terms, or None when none is set (the sinks
+    tensor is returned too, to keep it alive for the call)."""
+    if window_left == -1 and window_right == -1 and not softcap and sinks is None:
+        return None, None
+    for n, w in (("window_left", window_left), ("window_right", window_right)):
+        if int(w) < -1:
+            raise ValueError("%s must be -1 (unlimited) or >= 0, got %d" % (n, int(w)))
+    cap = 0.0 if softcap is None else float(softcap)
+    if not math.isfinite(cap) or cap < 0.0:
+        raise ValueError("softcap must be finite and >= 0, got %r" % (softcap,))
+    sk = None
+    if sinks is not None:
+        sk = torch.as_tensor(sinks).to(device=device, dtype=torch.float32).contiguous()
+        if tuple(sk.shape) != (Hq,):
+            raise ValueError("sinks must be [Hq] = [%d]" % Hq)
+    opt = _lib.Options(int(window_left), int(window_right), cap, sk.data_ptr() if sk is not None else None)
+    return opt, sk
+
+
+def attn_fwd_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, out=None, lse=None,
+                   window_left=-1, window_right=-1, softcap=None, sinks=None):
     """Dense / chunked-prefill GQA attention.
 
     q [B,Sq,Hq,D], k/v [B,Skv,Hkv,D] bfloat16 CUDA tensors (BSHD);
     key_padding_mask [B,Skv] bool (True = keep) or None.
+    window_left / window_right: keys admitted left / right of each query's key
+    position (-1 unlimited); softcap: c > 0 caps each scaled score to
+    c*tanh(z/c) (None or 0 off); sinks: [Hq] float32 logits joining the
+    softmax denominator only, or None.
     Returns (o [B,Sq,Hq,D] bf16, lse [B,Sq,Hq] float32, natural log).
     """
     for n, t in (("q", q), ("k", k), ("v", v)):
@@ -72,8 +97,15 @@ def attn_fwd_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, out=
         out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device)
-    st = _lib.load().attn_fwd_dense(_ptr(q), _ptr(k), _ptr(v), _ptr(m), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
-                                    Skv, D, int(bool(causal)), resolve_scale(scale, D), _stream(q.device))
+    opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device)
+    lib = _lib.load()
+    if opt is None:
+        st = lib.attn_fwd_dense(_ptr(q), _ptr(k), _ptr(v), _ptr(m), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
+                                int(bool(causal)), resolve_scale(scale, D), _stream(q.device))
+    else:
+        st = lib.attn_fwd_dense_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(m), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv,
+                                   D, int(bool(causal)), resolve_scale(scale, D), ctypes.byref(opt),
+                                   _stream(q.device))
     if st != 0:
         _raise(st, "attn_fwd_dense")
     return out, lse
@@ -85,12 +117,14 @@ def attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, page_size, max_pages):
 
 
 def attn_decode_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=True, scale=None,
-                      workspace=None, out=None, lse=None):
+                      workspace=None, out=None, lse=None, window_left=-1, window_right=-1, softcap=None,
+                      sinks=None):
     """Paged decode.
 
     q [B,Sq,Hq,D] bf16; k_cache/v_cache [num_pages,page_size,Hkv,D] bf16;
     real_seqlen_kv [B] int32 (query tokens included); block_table [B,max_pages] int32.
     workspace: optional uint8 CUDA tensor of at least attn_decode_paged_workspace_size bytes.
+    window_left / window_right / softcap / sinks as in attn_fwd_dense.
     Returns (o [B,Sq,Hq,D] bf16, lse [B,Sq,Hq] float32).
     """
     _check_bf16_cuda("q", q, 4)
@@ -117,10 +151,19 @@ def attn_decode_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=T
         out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device)
-    st = _lib.load().attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sl), _ptr(bt), page_size,
-                                       _ptr(out), _ptr(lse), B, Sq, Hq, Hkv, D, num_pages, max_pages,
-                                       int(bool(causal)), resolve_scale(scale, D), _ptr(workspace),
-                                       workspace.numel() * workspace.element_size(), _stream(q.device))
+    opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device)
+    lib = _lib.load()
+    wsb = workspace.numel() * workspace.element_size()
+    if opt is None:
+        st = lib.attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sl), _ptr(bt), page_size,
+                                   _ptr(out), _ptr(lse), B, Sq, Hq, Hkv, D, num_pages, max_pages,
+                                   int(bool(causal)), resolve_scale(scale, D), _ptr(workspace), wsb,
+                                   _stream(q.device))
+    else:
+        st = lib.attn_decode_paged_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sl), _ptr(bt), page_size,
+                                      _ptr(out), _ptr(lse), B, Sq, Hq, Hkv, D, num_pages, max_pages,
+                                      int(bool(causal)), resolve_scale(scale, D), ctypes.byref(opt),
+                                      _ptr(workspace), wsb, _stream(q.device))
     if st != 0:
         _raise(st, "attn_decode_paged")
     return out, lse

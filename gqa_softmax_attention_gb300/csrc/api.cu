@@ -103,9 +103,36 @@ constexpr long kMaxSeq = 1L << 30;
 
 extern "C" {
 
+// Checks the optional terms and turns them into their kernel form.
+static gqa_status make_extras(const gqa_options* op, float scale, gqa::Extras* x) {
+    x->wl = x->wr = -1;
+    x->cap_in = x->cap_out = 0.f;
+    x->sinks = nullptr;
+    if (!op) return GQA_OK;
+    if (op->window_left < -1 || op->window_right < -1) return GQA_ERR_INVALID_ARG;
+    if (!std::isfinite(op->softcap) || op->softcap < 0.f) return GQA_ERR_INVALID_ARG;
+    if (op->sinks && !aligned4(op->sinks)) return GQA_ERR_MISALIGNED;
+    x->wl = op->window_left;
+    x->wr = op->window_right;
+    if (op->softcap > 0.f) {
+        const double log2e = 1.4426950408889634074;
+        x->cap_in = (float)(2.0 * log2e * (double)scale / (double)op->softcap);
+        x->cap_out = (float)((double)op->softcap * log2e);
+    }
+    x->sinks = op->sinks;
+    return GQA_OK;
+}
+
 gqa_status attn_fwd_dense(const void* q, const void* k, const void* v, const uint8_t* key_padding_mask,
                           void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int D, int causal,
                           float scale, gqa_stream_t stream) {
+    return attn_fwd_dense_ex(q, k, v, key_padding_mask, o, lse, B, Hq, Hkv, Sq, Skv, D, causal, scale, nullptr,
+                             stream);
+}
+
+gqa_status attn_fwd_dense_ex(const void* q, const void* k, const void* v, const uint8_t* key_padding_mask,
+                             void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                             float scale, const gqa_options* opts, gqa_stream_t stream) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Sq < 0 || Skv < 0) return GQA_ERR_INVALID_ARG;
     if (Sq >= kMaxSeq || Skv >= kMaxSeq) return GQA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
@@ -115,6 +142,9 @@ gqa_status attn_fwd_dense(const void* q, const void* k, const void* v, const uin
     if (!q || !o || (Skv > 0 && (!k || !v))) return GQA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(o) || (Skv > 0 && (!aligned16(k) || !aligned16(v)))) return GQA_ERR_MISALIGNED;
     if (lse && !aligned4(lse)) return GQA_ERR_MISALIGNED;
+    gqa::Extras ex;
+    const gqa_status es = make_extras(opts, scale, &ex);
+    if (es != GQA_OK) return es;
     const long n_qtiles = ((long)Sq + 127) / 128;
     if (n_qtiles * B * Hq >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -134,6 +164,7 @@ gqa_status attn_fwd_dense(const void* q, const void* k, const void* v, const uin
     a.causal = causal ? 1 : 0;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     a.num_sms = sm_count();
+    a.x = ex;
     return gqa::launch_prefill(tq, tk, tv, to, a, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -148,6 +179,15 @@ gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_c
                              const int32_t* block_table, int page_size, void* o, float* lse, int B, int Sq, int Hq,
                              int Hkv, int D, int num_pages, int max_pages, int causal, float scale,
                              void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
+    return attn_decode_paged_ex(q, k_cache, v_cache, real_seqlen_kv, block_table, page_size, o, lse, B, Sq, Hq, Hkv,
+                                D, num_pages, max_pages, causal, scale, nullptr, workspace, workspace_bytes, stream);
+}
+
+gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* real_seqlen_kv, const int32_t* block_table, int page_size, void* o,
+                                float* lse, int B, int Sq, int Hq, int Hkv, int D, int num_pages, int max_pages,
+                                int causal, float scale, const gqa_options* opts, void* workspace,
+                                size_t workspace_bytes, gqa_stream_t stream) {
     if (B <= 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || page_size <= 0 || num_pages < 0 || max_pages <= 0)
         return GQA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
@@ -159,6 +199,9 @@ gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_c
     if (!q || !k_cache || !v_cache || !real_seqlen_kv || !block_table || !o) return GQA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return GQA_ERR_MISALIGNED;
     if (!aligned4(real_seqlen_kv) || !aligned4(block_table) || (lse && !aligned4(lse))) return GQA_ERR_MISALIGNED;
+    gqa::Extras ex;
+    const gqa_status es = make_extras(opts, scale, &ex);
+    if (es != GQA_OK) return es;
     DecodePlan p;
     if (!gqa::plan_decode(B, Sq, Hq, Hkv, D, page_size, max_pages, sm_count(), &p)) return GQA_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < p.workspace_bytes) return GQA_ERR_WORKSPACE;
@@ -178,6 +221,7 @@ gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_c
     a.seg_table = nullptr;
     a.n_part = 0;
     a.tc_grid = 0;
+    a.x = ex;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // KV groups of 32..128 query rows run on the balanced tensor-core decode
     // kernel, whose workspace holds per-piece partials and the segment table.

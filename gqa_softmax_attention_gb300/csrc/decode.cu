@@ -100,7 +100,7 @@ struct Work {
 };
 
 template <class C>
-__device__ __forceinline__ bool work_of(const DecodeArgs& a, int R, int n_rowblk, Work& w) {
+__device__ __forceinline__ bool work_of(const DecodeArgs& a, int R, int g, int n_rowblk, Work& w) {
     w.split = blockIdx.x;
     w.hkv = blockIdx.y;
     w.b = blockIdx.z / n_rowblk;
@@ -108,12 +108,20 @@ __device__ __forceinline__ bool work_of(const DecodeArgs& a, int R, int n_rowblk
     // Lengths are clamped to the table's capacity so a bad length cannot send
     // a load past block_table.
     w.L = min(max(a.seqlens[w.b], 0), a.max_pages * a.page_size);
+    w.row0 = w.rb * C::ROWS;
+    w.rows_here = min(C::ROWS, R - w.row0);
     w.t_begin = w.split * a.chunk;
     if (w.t_begin >= w.L) return false;            // nothing here; the combine skips it
     w.t_end = min(w.L, w.t_begin + a.chunk);
+    if (a.x.wl >= 0) {
+        // keys left of every row's window are never read: start at the tile
+        // holding the first row's lower bound (the combine reads no split
+        // before the one holding a row's lower bound)
+        const long lo = (long)(w.row0 / g) + w.L - a.Sq - a.x.wl;
+        if (lo > w.t_begin) w.t_begin = (int)min((long)w.t_end, lo / C::TK * C::TK);
+        if (w.t_begin >= w.t_end) return false;
+    }
     w.n_tiles = (w.t_end - w.t_begin + C::TK - 1) / C::TK;
-    w.row0 = w.rb * C::ROWS;
-    w.rows_here = min(C::ROWS, R - w.row0);
     return true;
 }
 
@@ -125,11 +133,13 @@ struct Consumer {
     uint8_t* smem;
     int ctid, warp, lane, mf, wk, srow, ssub;
     int lim[2];             // exclusive visibility limit of the two fragment rows this lane holds
+    int lo[2];              // their inclusive lower limit (left window)
+    float cap_in, cap_out;  // softcap, or cap_out == 0
     uint32_t qf[C::KSTEPS][4];
     float m_run, l_run;
     float acc[C::NFD][4];
 
-    __device__ void init(uint8_t* s, uint32_t base, const DecodeArgs& a, const Work& w, int g) {
+    __device__ __forceinline__ void init(uint8_t* s, uint32_t base, const DecodeArgs& a, const Work& w, int g) {
         smem = s;
         sb = base;
         ctid = threadIdx.x;
@@ -143,17 +153,24 @@ struct Consumer {
         l_run = 0.f;
 #pragma unroll
         for (int n = 0; n < C::NFD; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        cap_in = a.x.cap_in;
+        cap_out = a.x.cap_out;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int rl = mf * 16 + (lane >> 2) + 8 * h;
             const int r = w.row0 + rl;
+            lo[h] = 0;
             if (rl >= w.rows_here) {
                 lim[h] = -1;
-            } else if (a.causal) {
-                const long p = (long)(r / g) + w.L - a.Sq;          // key position of query r / g
-                lim[h] = (int)min((long)w.t_end, p + 1);
             } else {
-                lim[h] = w.t_end;
+                // keys [lo, lim) of query r / g at key position p (TileOPs
+                // GQAPagedFwdOp: causal j <= p, window p - wL <= j <= p + wR)
+                const long p = (long)(r / g) + w.L - a.Sq;
+                long hi = w.t_end;
+                if (a.causal) hi = min(hi, p + 1);
+                if (a.x.wr >= 0) hi = min(hi, p + a.x.wr + 1);
+                lim[h] = (int)max(-1L, hi);
+                if (a.x.wl >= 0) lo[h] = (int)max(0L, min((long)w.L, p - a.x.wl));
             }
         }
     }
@@ -161,7 +178,7 @@ struct Consumer {
     // Q rows r = i * g + hl (query i, head hkv * g + hl) -> shared memory with
     // cp.async (padded rows zero), then into registers.  `bar` syncs consumers.
     template <class Bar>
-    __device__ void load_q(const DecodeArgs& a, const Work& w, int g, Bar bar) {
+    __device__ __forceinline__ void load_q(const DecodeArgs& a, const Work& w, int g, Bar bar) {
         const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(a.q);
         for (int idx = ctid; idx < C::ROWS * CHUNKS; idx += C::NCT) {
             const int rr = idx / CHUNKS, c = idx % CHUNKS;
@@ -186,7 +203,7 @@ struct Consumer {
     }
 
     // S = Q K^T for this warp's rows and keys, scaled and masked, into smem.
-    __device__ void qk(uint32_t sK, int t0, float sl) {
+    __device__ __forceinline__ void qk(uint32_t sK, int t0, float sl) {
         float sacc[C::NFK][4];
 #pragma unroll
         for (int n = 0; n < C::NFK; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
@@ -210,9 +227,14 @@ struct Consumer {
                 const int rl = mf * 16 + (lane >> 2) + 8 * h;
                 const int kl = wk * C::KEYS_PER_WARP + n * 8 + 2 * (lane & 3);
                 const int t = t0 + kl;
-                float2 v;
-                v.x = t < lim[h] ? sacc[n][2 * h] * sl : -INFINITY;        // the select drops stale rows
-                v.y = t + 1 < lim[h] ? sacc[n][2 * h + 1] * sl : -INFINITY;
+                float x0 = sacc[n][2 * h] * sl, x1 = sacc[n][2 * h + 1] * sl;
+                if (cap_out != 0.f) {
+                    x0 = softcap_log2(sacc[n][2 * h], cap_in, cap_out);
+                    x1 = softcap_log2(sacc[n][2 * h + 1], cap_in, cap_out);
+                }
+                float2 v;                                                 // the select drops stale rows
+                v.x = t >= lo[h] && t < lim[h] ? x0 : -INFINITY;
+                v.y = t + 1 >= lo[h] && t + 1 < lim[h] ? x1 : -INFINITY;
                 *reinterpret_cast<float2*>(sS + rl * C::S_STRIDE + kl) = v;
             }
         }
@@ -220,7 +242,7 @@ struct Consumer {
 
     // Online softmax over the tile, TPR threads per row; P (bf16) and the
     // rescale factor alpha go to smem.
-    __device__ void softmax() {
+    __device__ __forceinline__ void softmax() {
         const float* sS = reinterpret_cast<const float*>(smem + C::OFF_S);
         float* sAlpha = reinterpret_cast<float*>(smem + C::OFF_A);
         float x[C::KPT];
@@ -261,7 +283,7 @@ struct Consumer {
     }
 
     // O = O * alpha + P V for this warp's rows and head-dim slice.
-    __device__ void pv(uint32_t sV) {
+    __device__ __forceinline__ void pv(uint32_t sV) {
         const float* sAlpha = reinterpret_cast<const float*>(smem + C::OFF_A);
         const float a0 = sAlpha[mf * 16 + (lane >> 2)];
         const float a1 = sAlpha[mf * 16 + (lane >> 2) + 8];
@@ -292,7 +314,7 @@ struct Consumer {
 
     // Normalised partial O (FP32) and base-2 LSE of this split.  `bar` syncs consumers.
     template <class Bar>
-    __device__ void store(const DecodeArgs& a, const Work& w, int R, Bar bar) {
+    __device__ __forceinline__ void store(const DecodeArgs& a, const Work& w, int R, Bar bar) {
         float* sL = reinterpret_cast<float*>(smem + C::OFF_L);
         float* sM = reinterpret_cast<float*>(smem + C::OFF_M);
         if (ssub == 0) {
@@ -331,7 +353,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
     Work w;
-    if (!work_of<C>(a, R, n_rowblk, w)) return;
+    if (!work_of<C>(a, R, g, n_rowblk, w)) return;
 
     const uint32_t bar0 = sb + C::OFF_BAR;
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -444,7 +466,7 @@ decode_gather_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
     Work w;
-    if (!work_of<C>(a, R, n_rowblk, w)) return;
+    if (!work_of<C>(a, R, g, n_rowblk, w)) return;
     const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
     const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
     const int32_t* trow = a.table + (size_t)w.b * a.max_pages;
@@ -531,6 +553,13 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
     } else {
         n = L > 0 ? (L + a.chunk - 1) / a.chunk : 0;
         base = (size_t)(b * a.Hkv + hkv) * a.max_splits * R + r;
+        if (a.x.wl >= 0 && n > 0) {
+            // splits wholly left of this row's window were not run
+            const long lo = (long)i + L - a.Sq - a.x.wl;
+            const int s0 = lo > 0 ? (int)min((long)n, lo / a.chunk) : 0;
+            base += (size_t)s0 * R;
+            n -= s0;
+        }
     }
 
     float M = -INFINITY;
@@ -540,6 +569,20 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
 
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o) + (size_t)row * D;
     constexpr int PER = D / 128 > 0 ? D / 128 : 1;     // float4 groups per lane
+    // A sink joins the denominator once per row (GQAPagedFwdOp sinks): the
+    // weights are taken against max(M, s); +inf zeroes the row.  A row no
+    // split saw stays zero with LSE -inf.
+    const float s2 = (a.x.sinks && M != -INFINITY) ? a.x.sinks[h] * 1.4426950408889634f : -INFINITY;
+    if (s2 == INFINITY) {
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int d = (q * 32 + lane) * 4;
+            if (d < D) *reinterpret_cast<uint2*>(out + d) = make_uint2(0u, 0u);
+        }
+        if (lane == 0 && a.lse) a.lse[row] = INFINITY;
+        return;
+    }
+    M = fmaxf(M, s2);
     if (M == -INFINITY) {
 #pragma unroll
         for (int q = 0; q < PER; ++q) {
@@ -550,7 +593,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
         return;
     }
     float accv[PER][4] = {};
-    float den = 0.f;
+    float den = s2 == -INFINITY ? 0.f : fast_exp2(s2 - M);
     for (int s = 0; s < n; ++s) {
         const size_t pr = base + (size_t)s * R;
         const float w = fast_exp2(a.part_lse[pr] - M);

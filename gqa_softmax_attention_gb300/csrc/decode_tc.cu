@@ -107,16 +107,25 @@ struct Range {
     int s0, lt0;      // segment and tile within it of the first tile
 };
 
-// A position in the tile sequence: segment s = b * Hkv + h holds
-// ceil(L_b / 64) tiles; lt is the tile within the segment.
+// First 64-key tile of request b that any query can see: with a left window
+// the keys before the first query's lower bound L - Sq - wL are never read.
+__device__ __forceinline__ int first_tile(const DecodeArgs& a, int L) {
+    if (a.x.wl < 0 || L <= 0) return 0;
+    const long lo = (long)L - a.Sq - a.x.wl;
+    return lo > 0 ? (int)(lo / BN) : 0;
+}
+
+// A position in the tile sequence: segment s = b * Hkv + h holds the
+// ceil(L_b / 64) - tf tiles from tile tf on; lt is the tile within the segment.
 struct Cursor {
-    int s, b, h, L, nt, lt;
+    int s, b, h, L, tf, nt, lt;
     __device__ __forceinline__ void set(const DecodeArgs& a, int seg) {
         s = seg;
         b = seg / a.Hkv;
         h = seg % a.Hkv;
         L = seg < a.B * a.Hkv ? min(max(a.seqlens[b], 0), a.max_pages * a.page_size) : 0;
-        nt = (L + BN - 1) / BN;
+        tf = first_tile(a, L);
+        nt = (L + BN - 1) / BN - tf;
     }
     // The next tile, skipping empty segments (never past the last segment).
     __device__ __forceinline__ void next(const DecodeArgs& a) {
@@ -136,7 +145,9 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
 }
 
 __device__ __forceinline__ int request_tiles(const DecodeArgs& a, int b) {
-    return b < a.B ? (min(max(a.seqlens[b], 0), a.max_pages * a.page_size) + BN - 1) / BN : 0;
+    if (b >= a.B) return 0;
+    const int L = min(max(a.seqlens[b], 0), a.max_pages * a.page_size);
+    return (L + BN - 1) / BN - first_tile(a, L);
 }
 
 // Query row r of (b, h) (bf16 [B, Sq, Hq, D]) into this thread's TMEM lane,
@@ -277,7 +288,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 win = -(1 << 30);
             }
             const int32_t* trow = a.table + (size_t)cur.b * a.max_pages;
-            const int t = cur.lt * BN + lane * box_tokens;
+            const int t = (cur.tf + cur.lt) * BN + lane * box_tokens;
             const int lp = t / a.page_size;
             const int lp_first = __shfl_sync(0xffffffffu, lp, 0);
             const int lp_last = __shfl_sync(0xffffffffu, lp, nbox - 1);
@@ -384,7 +395,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (!ok) break;
             const uint32_t vb = sb + C::OFF_V + vs * C::KV_TILE;
             const bool fresh = i == 0 || cp.lt == 0;   // first tile of a piece: O starts over
-            const int nvalid = min(BN, cp.L - cp.lt * BN);
+            const int nvalid = min(BN, cp.L - (cp.tf + cp.lt) * BN);
             if (nvalid < BN) {
                 // Value rows past the request's end hold stale data: zero them
                 // before the tensor core reads the tile.
@@ -439,18 +450,29 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         Cursor c;
         c.set(a, rg.s0);
         c.lt = rg.lt0;
-        int lim = 0, lim_first = 0;                // visibility limit of this row / of every row
+        // visible keys of this row: [lo, lim); lim_first / lo_last bound every row's
+        int lim = 0, lo = 0, lim_first = 0, lo_last = 0;
+        auto key_hi = [&](long p, int L) {
+            long hi = L;
+            if (a.causal) hi = min(hi, p + 1);
+            if (a.x.wr >= 0) hi = min(hi, p + a.x.wr + 1);
+            return (int)max(0L, hi);
+        };
+        auto key_lo = [&](long p, int L) { return a.x.wl >= 0 ? (int)max(0L, min((long)L, p - a.x.wl)) : 0; };
         auto piece_setup = [&]() {
             const int L = c.L;
-            lim = row_ok ? (a.causal ? (int)min((long)L, (long)(r / g) + L - a.Sq + 1) : L) : 0;
-            lim_first = a.causal ? max(0, min(L, L - a.Sq + 1)) : L;
+            const long p = (long)(r / g) + L - a.Sq;       // key position of this row's query
+            lim = row_ok ? key_hi(p, L) : 0;
+            lo = row_ok ? key_lo(p, L) : 0;
+            lim_first = key_hi((long)L - a.Sq, L);
+            lo_last = key_lo((long)L - 1, L);
         };
         piece_setup();
         int piece_lt0 = rg.lt0;                    // tile of the segment the piece starts at
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int it = 0; it < n; ++it) {
-            const int t0 = c.lt * BN;
+            const int t0 = (c.tf + c.lt) * BN;
             const bool first = it == 0 || c.lt == 0;
             const bool last = c.lt == c.nt - 1 || it == n - 1;
             Cursor nx = c;
@@ -471,7 +493,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const uint32_t scol = (it & 1) ? C::COL_S1 : C::COL_S0;
             float s[BN];
             tmem_ld64(tmem + lane_addr + scol, s);
-            const bool fast = t0 + BN <= lim_first && sl > 0.f;
+            const bool capped = a.x.cap_out != 0.f;
+            const bool fast = t0 + BN <= lim_first && t0 >= lo_last && sl > 0.f && !capped;
             float mx8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
@@ -481,7 +504,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             } else {
 #pragma unroll
                 for (int cc = 0; cc < BN; ++cc) {
-                    const float x = t0 + cc < lim ? s[cc] * sl : -INFINITY;   // the select drops stale rows
+                    const float lg = capped ? softcap_log2(s[cc], a.x.cap_in, a.x.cap_out) : s[cc] * sl;
+                    const float x = t0 + cc >= lo && t0 + cc < lim ? lg : -INFINITY;   // the select drops stale rows
                     s[cc] = x;
                     mx8[cc & 7] = fmaxf(mx8[cc & 7], x);
                 }

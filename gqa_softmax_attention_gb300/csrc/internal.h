@@ -7,6 +7,15 @@
 
 namespace gqa {
 
+// Optional terms of a call in kernel form (TileOPs "Attention Operators",
+// GQADenseFwdOp stages 5-6; GQAPagedFwdOp sinks).
+struct Extras {
+    int wl, wr;             // window sizes; -1 = unlimited
+    float cap_in;           // softcap c: 2 * log2(e) * scale / c, multiplying a raw score (0 = off)
+    float cap_out;          // c * log2(e)
+    const float* sinks;     // [Hq] natural-log logits joining the denominator only, or nullptr
+};
+
 struct PrefillArgs {
     const uint8_t* mask;  // [B, Skv] or nullptr
     void* o;              // [B, Sq, Hq, D] bf16
@@ -15,6 +24,7 @@ struct PrefillArgs {
     int causal;
     float scale_log2;     // scale * log2(e)
     int num_sms;          // persistent grid size
+    Extras x;
 };
 
 // Launches the tcgen05 prefill kernel.  The tensor maps describe q, k, v as
@@ -48,6 +58,7 @@ struct DecodeArgs {
     int* seg_table;         // [B * Hkv, 2]
     int n_part;             // partial slots in part_o / part_lse
     int tc_grid;            // persistent CTAs (one per SM)
+    Extras x;
 };
 
 struct DecodePlan {

@@ -98,37 +98,52 @@ struct Cfg {
 struct TileInfo {
     int q0;          // first query row of the tile
     int rows_valid;  // rows of the tile that exist (ragged tail; may be 0)
-    int lim_first;   // keys [0, lim_first) are causally visible to every row of the tile
+    int lim_first;   // keys below lim_first are inside every row's upper bound
+    int lo_last;     // keys from lo_last on are inside every row's lower (window) bound
+    int kv_begin;    // no row of the tile sees a key < kv_begin
     int kv_end;      // no row of the tile sees a key >= kv_end
     int n_tiles;     // key tiles in [0, kv_end)
 };
 
-__device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causal) {
+// Visible keys of the query at key position p: [lo, hi) (TileOPs "Attention
+// Operators", GQADenseFwdOp stage 5: causal j <= p, window p - wL <= j <= p + wR).
+__device__ __forceinline__ long key_hi(long p, int Skv, int causal, int wr) {
+    long hi = Skv;
+    if (causal) hi = min(hi, p + 1);
+    if (wr >= 0) hi = min(hi, p + wr + 1);
+    return max(0L, hi);
+}
+__device__ __forceinline__ long key_lo(long p, int Skv, int wl) {
+    return wl >= 0 ? min((long)Skv, max(0L, p - wl)) : 0L;
+}
+
+__device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causal, int wl, int wr) {
     TileInfo t;
     t.q0 = q0;
     t.rows_valid = max(0, min(BM, Sq - q0));
     if (t.rows_valid == 0) {
-        t.kv_end = t.lim_first = 0;
-    } else if (causal) {
+        t.kv_begin = t.kv_end = t.lim_first = t.lo_last = 0;
+    } else {
         const long p_first = (long)q0 + Skv - Sq;        // key position of the first row
         const long p_last = p_first + t.rows_valid - 1;
-        t.kv_end = (int)max(0L, min((long)Skv, p_last + 1));
-        t.lim_first = (int)max(0L, min((long)Skv, p_first + 1));
-    } else {
-        t.kv_end = Skv;
-        t.lim_first = Skv;
+        t.kv_end = (int)key_hi(p_last, Skv, causal, wr);
+        t.lim_first = (int)key_hi(p_first, Skv, causal, wr);
+        t.kv_begin = (int)key_lo(p_first, Skv, wl);
+        t.lo_last = (int)key_lo(p_last, Skv, wl);
+        if (t.kv_begin >= t.kv_end) t.kv_begin = t.kv_end = t.lim_first = t.lo_last = 0;
     }
     t.n_tiles = (t.kv_end + BN - 1) / BN;
     return t;
 }
 
 // Warp-collective.  Bit l of the result is set when key tile 32 * chunk + l
-// (below n_tiles) holds a key below kv_end that the padding mask keeps; lane l
+// (in [first, n_tiles)) holds a key below kv_end that the padding mask keeps; lane l
 // scans that tile, so 32 tiles cost one pass.  Without a mask every tile
 // below n_tiles counts.
-__device__ __forceinline__ uint32_t tile_flags(const uint8_t* mrow, int chunk, int n_tiles, int kv_end, int lane) {
+__device__ __forceinline__ uint32_t tile_flags(const uint8_t* mrow, int chunk, int first, int n_tiles, int kv_end,
+                                               int lane) {
     const int j = chunk * 32 + lane;
-    bool any = j < n_tiles;
+    bool any = j >= first && j < n_tiles;
     if (mrow && any) {
         const int k0 = j * BN, k1 = min(k0 + BN, kv_end);
         const uint8_t* p = mrow + k0;
@@ -149,19 +164,19 @@ __device__ __forceinline__ uint32_t tile_flags(const uint8_t* mrow, int chunk, i
     return __ballot_sync(0xffffffffu, any);
 }
 
-// Walks the visited key tiles (non-empty ones below n_tiles) in increasing
+// Walks the visited key tiles (non-empty ones in [first, n_tiles)) in increasing
 // order, 32 tiles per scan.  Warp-collective; every lane sees the same tiles.
 struct TileIter {
     const uint8_t* mrow;
-    int n_tiles, kv_end, lane, chunk;
+    int first, n_tiles, kv_end, lane, chunk;
     uint32_t f;
-    __device__ __forceinline__ TileIter(const uint8_t* m, int n, int e, int l)
-        : mrow(m), n_tiles(n), kv_end(e), lane(l), chunk(-1), f(0) {}
+    __device__ __forceinline__ TileIter(const uint8_t* m, int fst, int n, int e, int l)
+        : mrow(m), first(fst), n_tiles(n), kv_end(e), lane(l), chunk(fst / 32 - 1), f(0) {}
     __device__ __forceinline__ int next() {   // next visited tile, or -1
         while (f == 0) {
             ++chunk;
             if (chunk * 32 >= n_tiles) return -1;
-            f = tile_flags(mrow, chunk, n_tiles, kv_end, lane);
+            f = tile_flags(mrow, chunk, first, n_tiles, kv_end, lane);
         }
         const int l = __ffs(f) - 1;
         f &= f - 1;
@@ -233,7 +248,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         return w < n_items ? (int)w : -1;
     };
     struct Item {
-        int b, hq, hkv, q0, n_all, kv_end_all;
+        int b, hq, hkv, q0, first, n_all, kv_end_all;
         TileInfo t0, t1;
         const uint8_t* mrow;
     };
@@ -245,20 +260,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         it.b = rem / a.Hq;
         it.hkv = it.hq / (a.Hq / a.Hkv);
         it.q0 = qp * (NQ * BM);
-        it.t0 = tile_info(it.q0, a.Sq, a.Skv, a.causal);
-        it.t1 = tile_info(it.q0 + BM, a.Sq, a.Skv, a.causal);
+        it.t0 = tile_info(it.q0, a.Sq, a.Skv, a.causal, a.x.wl, a.x.wr);
+        it.t1 = tile_info(it.q0 + BM, a.Sq, a.Skv, a.causal, a.x.wl, a.x.wr);
         it.n_all = max(it.t0.n_tiles, it.t1.n_tiles);
         it.kv_end_all = max(it.t0.kv_end, it.t1.kv_end);
+        // both Q tiles walk the tiles from the first one either needs (Q1's
+        // window starts later: its extra leading tiles are fully masked)
+        it.first = (it.t0.n_tiles > 0 ? it.t0.kv_begin : it.t1.kv_begin) / BN;
         it.mrow = a.mask ? a.mask + (size_t)it.b * a.Skv : nullptr;
         return it;
     };
-    // Visited key tiles of an item (non-empty, below kv_end of either Q tile)
-    // are numbered i = 0, 1, ...; Q_k takes part in the first c_k of them.
-    // Warp-collective.
+    // Visited key tiles of an item (non-empty, from its first tile to kv_end of
+    // either Q tile) are numbered i = 0, 1, ...; Q_k takes part in the first c_k
+    // of them.  Warp-collective.
     auto count_tiles = [&](const Item& it, int& c0, int& c1, int& c_all) {
         c0 = c1 = c_all = 0;
-        for (int chunk = 0; chunk * 32 < it.n_all; ++chunk) {
-            const uint32_t f = tile_flags(it.mrow, chunk, it.n_all, it.kv_end_all, lane);
+        for (int chunk = it.first / 32; chunk * 32 < it.n_all; ++chunk) {
+            const uint32_t f = tile_flags(it.mrow, chunk, it.first, it.n_all, it.kv_end_all, lane);
             c_all += __popc(f);
             c0 += __popc(f & below_bits(it.t0.n_tiles, chunk));
             c1 += __popc(f & below_bits(it.t1.n_tiles, chunk));
@@ -344,7 +362,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 nq0 = __shfl_sync(0xffffffffu, nq0, 0);
                 nq1 = __shfl_sync(0xffffffffu, nq1, 0);
                 if (!ok) break;
-                TileIter tiles(it.mrow, it.n_all, it.kv_end_all, lane);
+                TileIter tiles(it.mrow, it.first, it.n_all, it.kv_end_all, lane);
                 for (int j = tiles.next(); j >= 0; j = tiles.next()) {
                     if (lane == 0) {
                         const int ks = nk % C::NK;
@@ -522,12 +540,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint8_t* mrow = itm.mrow;
             const int row_q = ti.q0 + r;
             const long p_row = (long)row_q + a.Skv - a.Sq;
-            const int lim = a.causal ? (int)max(0L, min((long)a.Skv, p_row + 1)) : a.Skv;
+            const int lim = (int)key_hi(p_row, a.Skv, a.causal, a.x.wr);   // visible keys: [lo, lim)
+            const int lo = (int)key_lo(p_row, a.Skv, a.x.wl);
             float m_ref = -INFINITY;     // reference max (log2 units, scaled)
             float l_run = 0.f;
             int it = 0;
             // The mask bytes of the next visited tile are fetched one tile ahead.
-            TileIter tiles(mrow, itm.n_all, itm.kv_end_all, lane);
+            TileIter tiles(mrow, itm.first, itm.n_all, itm.kv_end_all, lane);
             auto fetch = [&](int j, uint8_t* mb) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -550,7 +569,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     all_kept = all_kept && (mw[q] == 0xffffffffu);
                 }
                 const int kbase = j * BN;
-                const bool need_mask = (kbase + BN > ti.lim_first) || !all_kept;
+                const bool need_mask = (kbase + BN > ti.lim_first) || kbase < ti.lo_last || !all_kept;
 
                 ok = __all_sync(0xffffffffu, mbar_wait(s_full(k), sf & 1, abort_flag));
                 ++sf;
@@ -561,10 +580,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 float* s = reinterpret_cast<float*>(sr);
 
                 // Row max over 8 independent chains (short dependency chains).
-                // Fast path (no mask in this tile, positive scale): the max is taken
-                // on raw scores and the scale is folded into the exp2 argument;
-                // otherwise scores are scaled first and masked ones set to -inf.
-                const bool fast = !need_mask && sl > 0.f;
+                // Fast path (no mask in this tile, positive scale, no cap): the max
+                // is taken on raw scores and the scale is folded into the exp2
+                // argument; otherwise scores become logits (log2 units, capped
+                // when a softcap is set) and masked ones -inf.
+                const bool capped = a.x.cap_out != 0.f;
+                const bool fast = !need_mask && sl > 0.f && !capped;
                 float mx8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
@@ -572,15 +593,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int c = 0; c < BN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
                 } else {
+                    if (capped) {
+#pragma unroll
+                        for (int c = 0; c < BN; ++c) s[c] = softcap_log2(s[c], a.x.cap_in, a.x.cap_out);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BN; ++c) s[c] *= sl;
+                    }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        // keys of this 32-column group below the row's causal limit
+                        // keys of this 32-column group inside the row's [lo, lim)
                         const int rel = lim - (kbase + 32 * q);
                         const uint32_t below = rel >= 32 ? 0xffffffffu : (rel <= 0 ? 0u : ((1u << rel) - 1u));
-                        const uint32_t vis = mw[q] & below;
+                        const int rlo = lo - (kbase + 32 * q);
+                        const uint32_t above = rlo <= 0 ? 0xffffffffu : (rlo >= 32 ? 0u : ~((1u << rlo) - 1u));
+                        const uint32_t vis = mw[q] & below & above;
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
-                            const float x = ((vis >> c) & 1u) ? s[32 * q + c] * sl : -INFINITY;
+                            const float x = ((vis >> c) & 1u) ? s[32 * q + c] : -INFINITY;
                             s[32 * q + c] = x;
                             mx8[c & 7] = fmaxf(mx8[c & 7], x);
                         }
@@ -635,7 +665,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             ++n_done;
             const bool row_ok = r < ti.rows_valid;
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            // O / l, and the LSE in log2 units; a sink adds exp(s) to l only
+            // (GQAPagedFwdOp sinks), taken against max(m_ref, s) so nothing
+            // overflows; +inf zeroes the row
+            float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            float lse2 = l_run > 0.f ? m_ref + log2f(l_run) : -INFINITY;
+            if (a.x.sinks && l_run > 0.f) {
+                const float s2 = a.x.sinks[itm.hq] * 1.4426950408889634f;
+                if (s2 == INFINITY) {
+                    inv = 0.f;
+                    lse2 = INFINITY;
+                } else {
+                    const float M = fmaxf(m_ref, s2);
+                    const float keep = fast_exp2(m_ref - M);
+                    const float l_tot = l_run * keep + fast_exp2(s2 - M);
+                    inv = keep / l_tot;
+                    lse2 = M + log2f(l_tot);
+                }
+            }
             // O / l as bf16 goes, one 64-column box at a time, into this
             // warpgroup's staging buffer in the 128-byte-swizzled box layout of
             // the output map, and one thread stores each box with TMA: whole
@@ -676,9 +723,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
             }
-            if (row_ok && a.lse)
-                a.lse[((size_t)itm.b * a.Sq + row_q) * a.Hq + itm.hq] =
-                    l_run > 0.f ? (m_ref + log2f(l_run)) * kLn2 : -INFINITY;
+            if (row_ok && a.lse) a.lse[((size_t)itm.b * a.Sq + row_q) * a.Hq + itm.hq] = lse2 * kLn2;
             tc_fence_before();
             if (!named_bar_and(3 + k, BM, ok)) break;     // the whole warpgroup stops together
         }

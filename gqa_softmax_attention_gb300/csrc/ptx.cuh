@@ -318,6 +318,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Softcapped logit in log2 units from a raw score s (TileOPs "Attention
+// Operators", GQADenseFwdOp stage 6: z = scale * s, logit c * tanh(z / c)):
+// tanh(y) = 1 - 2 / (e^(2y) + 1), with cap_in = 2 * log2(e) * scale / c and
+// cap_out = c * log2(e).  e^(2y) overflowing to +inf gives 1, underflowing to
+// 0 gives -1; near 0 the absolute error stays about c * 1e-7.
+__device__ __forceinline__ float softcap_log2(float s, float cap_in, float cap_out) {
+    const float e = fast_exp2(s * cap_in);
+    return cap_out - 2.f * cap_out * rcp_approx(e + 1.f);
+}
+
 // Three-input maximum.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;

@@ -58,6 +58,33 @@ typedef enum {
 } gqa_status;
 
 /*
+ * Optional terms of a call (TileOPs "Attention Operators", GQADenseFwdOp stages
+ * 5-6, and GQAPagedFwdOp's sinks).  Pass NULL for none; a zeroed struct with
+ * both windows at -1 is the same.
+ *   window_left   keys admitted left of the query's key position p_i (key j is
+ *                 visible only if j >= p_i - window_left); -1 = unlimited
+ *   window_right  keys admitted right of p_i (j <= p_i + window_right); -1 =
+ *                 unlimited; with the causal mask (j <= p_i already) a
+ *                 window_right >= 0 changes nothing
+ *   softcap       c > 0 replaces each visible scaled score z with c*tanh(z/c);
+ *                 0 disables capping; negative or non-finite is refused
+ *   sinks         NULL, or a DEVICE array of Hq float32 logits, one per query
+ *                 head, that join the softmax denominator only (not scaled,
+ *                 not capped): weight_j = exp(z_j) / (sum_j exp(z_j) +
+ *                 exp(sink_h)); the LSE includes exp(sink_h).  -inf disables a
+ *                 sink; +inf makes that head's output zero (LSE +inf).  A row
+ *                 with no visible key outputs zeros with LSE -inf either way.
+ *                 4-byte aligned; read on the device, never copied.
+ * Window values below -1 or a bad softcap return GQA_ERR_INVALID_ARG.
+ */
+typedef struct {
+    int window_left;
+    int window_right;
+    float softcap;
+    const float* sinks;
+} gqa_options;
+
+/*
  * Dense prefill / chunked prefill (TileOPs GQADenseFwdOp; RL-Kernel
  * "Prefill / Decode / KV-cache Shared Contract": one expression covers
  * Sq == Skv, chunked prefill and Sq < Skv).
@@ -79,6 +106,13 @@ gqa_status attn_fwd_dense(const void* q, const void* k, const void* v,
                           const uint8_t* key_padding_mask, void* o, float* lse,
                           int B, int Hq, int Hkv, int Sq, int Skv, int D,
                           int causal, float scale, gqa_stream_t stream);
+
+/* attn_fwd_dense with optional terms (opts may be NULL). */
+gqa_status attn_fwd_dense_ex(const void* q, const void* k, const void* v,
+                             const uint8_t* key_padding_mask, void* o, float* lse,
+                             int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                             int causal, float scale, const gqa_options* opts,
+                             gqa_stream_t stream);
 
 /*
  * Paged decode (TileOPs MHADecodePagedWithKVCacheFwdOp and GQAPagedFwdOp;
@@ -114,6 +148,19 @@ gqa_status attn_decode_paged(const void* q, const void* k_cache, const void* v_c
                              int num_pages, int max_pages, int causal, float scale,
                              void* workspace, size_t workspace_bytes,
                              gqa_stream_t stream);
+
+/*
+ * attn_decode_paged with optional terms (opts may be NULL).  A left window
+ * also bounds what is read: keys left of every query's window are not loaded.
+ * Same workspace size.
+ */
+gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* real_seqlen_kv, const int32_t* block_table,
+                                int page_size, void* o, float* lse,
+                                int B, int Sq, int Hq, int Hkv, int D,
+                                int num_pages, int max_pages, int causal, float scale,
+                                const gqa_options* opts, void* workspace, size_t workspace_bytes,
+                                gqa_stream_t stream);
 
 /*
  * Bytes of workspace attn_decode_paged needs for these sizes on the current

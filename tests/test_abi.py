@@ -102,3 +102,39 @@ def test_python_layer_rejects_cpu_tensors():
     q = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         g.attention(q, q, q)
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int), ("softcap", ctypes.c_float),
+                ("sinks", ctypes.c_void_p)]
+
+
+def test_option_checks(lib):
+    # refused before anything is launched (TileOPs GQADenseFwdOp: window -1 = unlimited, softcap >= 0)
+    def dense_ex(o):
+        return lib.attn_fwd_dense_ex(A16, A16, A16, None, A16b, None, 1, 4, 2, 8, 8, 64, 1, 0.125, ctypes.byref(o),
+                                     None)
+
+    def paged_ex(o):
+        return lib.attn_decode_paged_ex(A16, A16, A16, A16, A16, 16, A16b, None, 2, 1, 8, 2, 128, 10, 4, 1, 0.1,
+                                        ctypes.byref(o), A16, 1 << 30, None)
+
+    for call in (dense_ex, paged_ex):
+        assert call(Opts(-2, -1, 0.0, None)) == INVALID
+        assert call(Opts(-1, -5, 0.0, None)) == INVALID
+        assert call(Opts(-1, -1, -1.0, None)) == INVALID
+        assert call(Opts(-1, -1, float("nan"), None)) == INVALID
+        assert call(Opts(-1, -1, float("inf"), None)) == INVALID
+        assert call(Opts(-1, -1, 0.0, (1 << 20) + 2)) == MISALIGNED
+
+
+def test_python_layer_option_checks():
+    import torch
+    import gqa_softmax_attention_gb300.api as api
+    with pytest.raises(ValueError, match="window_left"):
+        api._options(-3, -1, None, None, 4, "cpu")
+    with pytest.raises(ValueError, match="softcap"):
+        api._options(-1, -1, -0.5, None, 4, "cpu")
+    with pytest.raises(ValueError, match="sinks"):
+        api._options(-1, -1, None, torch.zeros(3), 4, "cpu")
+    assert api._options(-1, -1, None, None, 4, "cpu") == (None, None)
