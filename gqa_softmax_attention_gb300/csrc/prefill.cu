@@ -221,12 +221,20 @@ __device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, 
     return (r0 + r1) + (r2 + r3);
 }
 
-template <int D>
+// OPTS: the call has a window, a softcap or sinks.  Without them every option
+// term is a compile-time constant and the code is the plain causal / padded
+// kernel.
+template <int D, bool OPTS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const PrefillArgs a, int n_qpairs) {
     using C = Cfg<D>;
+    const int wl = OPTS ? a.x.wl : -1;
+    const int wr = OPTS ? a.x.wr : -1;
+    const float cap_in = OPTS ? a.x.cap_in : 0.f;
+    const float cap_out = OPTS ? a.x.cap_out : 0.f;
+    const float* sinks = OPTS ? a.x.sinks : nullptr;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw_base & 1023)) & 1023);
@@ -260,8 +268,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         it.b = rem / a.Hq;
         it.hkv = it.hq / (a.Hq / a.Hkv);
         it.q0 = qp * (NQ * BM);
-        it.t0 = tile_info(it.q0, a.Sq, a.Skv, a.causal, a.x.wl, a.x.wr);
-        it.t1 = tile_info(it.q0 + BM, a.Sq, a.Skv, a.causal, a.x.wl, a.x.wr);
+        it.t0 = tile_info(it.q0, a.Sq, a.Skv, a.causal, wl, wr);
+        it.t1 = tile_info(it.q0 + BM, a.Sq, a.Skv, a.causal, wl, wr);
         it.n_all = max(it.t0.n_tiles, it.t1.n_tiles);
         it.kv_end_all = max(it.t0.kv_end, it.t1.kv_end);
         // both Q tiles walk the tiles from the first one either needs (Q1's
@@ -540,8 +548,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint8_t* mrow = itm.mrow;
             const int row_q = ti.q0 + r;
             const long p_row = (long)row_q + a.Skv - a.Sq;
-            const int lim = (int)key_hi(p_row, a.Skv, a.causal, a.x.wr);   // visible keys: [lo, lim)
-            const int lo = (int)key_lo(p_row, a.Skv, a.x.wl);
+            const int lim = (int)key_hi(p_row, a.Skv, a.causal, wr);   // visible keys: [lo, lim)
+            const int lo = (int)key_lo(p_row, a.Skv, wl);
             float m_ref = -INFINITY;     // reference max (log2 units, scaled)
             float l_run = 0.f;
             int it = 0;
@@ -584,7 +592,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // is taken on raw scores and the scale is folded into the exp2
                 // argument; otherwise scores become logits (log2 units, capped
                 // when a softcap is set) and masked ones -inf.
-                const bool capped = a.x.cap_out != 0.f;
+                const bool capped = cap_out != 0.f;
                 const bool fast = !need_mask && sl > 0.f && !capped;
                 float mx8[8];
 #pragma unroll
@@ -593,13 +601,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int c = 0; c < BN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
                 } else {
-                    if (capped) {
-#pragma unroll
-                        for (int c = 0; c < BN; ++c) s[c] = softcap_log2(s[c], a.x.cap_in, a.x.cap_out);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < BN; ++c) s[c] *= sl;
-                    }
+                    uint32_t vis[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         // keys of this 32-column group inside the row's [lo, lim)
@@ -607,11 +609,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         const uint32_t below = rel >= 32 ? 0xffffffffu : (rel <= 0 ? 0u : ((1u << rel) - 1u));
                         const int rlo = lo - (kbase + 32 * q);
                         const uint32_t above = rlo <= 0 ? 0xffffffffu : (rlo >= 32 ? 0u : ~((1u << rlo) - 1u));
-                        const uint32_t vis = mw[q] & below & above;
+                        vis[q] = mw[q] & below & above;
+                    }
+                    if (capped) {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const float x = ((vis >> c) & 1u) ? s[32 * q + c] : -INFINITY;
-                            s[32 * q + c] = x;
+                        for (int c = 0; c < BN; ++c) {
+                            const float x = ((vis[c / 32] >> (c % 32)) & 1u)
+                                                ? softcap_log2(s[c], cap_in, cap_out) : -INFINITY;
+                            s[c] = x;
+                            mx8[c & 7] = fmaxf(mx8[c & 7], x);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BN; ++c) {
+                            const float x = ((vis[c / 32] >> (c % 32)) & 1u) ? s[c] * sl : -INFINITY;
+                            s[c] = x;
                             mx8[c & 7] = fmaxf(mx8[c & 7], x);
                         }
                     }
@@ -670,8 +682,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // overflows; +inf zeroes the row
             float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             float lse2 = l_run > 0.f ? m_ref + log2f(l_run) : -INFINITY;
-            if (a.x.sinks && l_run > 0.f) {
-                const float s2 = a.x.sinks[itm.hq] * 1.4426950408889634f;
+            if (sinks && l_run > 0.f) {
+                const float s2 = sinks[itm.hq] * 1.4426950408889634f;
                 if (s2 == INFINITY) {
                     inv = 0.f;
                     lse2 = INFINITY;
@@ -749,18 +761,19 @@ __global__ void empty_rows_kernel(__nv_bfloat16* o, float* lse, long rows, int D
     }
 }
 
-template <int D>
+template <int D, bool OPTS>
 cudaError_t launch_prefill_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream) {
     using C = Cfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, OPTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_qpairs = (a.Sq + NQ * BM - 1) / (NQ * BM);
     const long n_items = (long)n_qpairs * a.B * a.Hq;
     const long sms = a.num_sms > 0 ? a.num_sms : 148;
     const long grid = n_items < sms ? n_items : sms;    // persistent: one CTA per SM
-    prefill_kernel<D><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, tm_o, a, n_qpairs);
+    prefill_kernel<D, OPTS><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, tm_o, a,
+                                                                                   n_qpairs);
     return cudaGetLastError();
 }
 
@@ -768,9 +781,14 @@ cudaError_t launch_prefill_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
 
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream) {
+    const bool opts = a.x.wl >= 0 || a.x.wr >= 0 || a.x.cap_out != 0.f || a.x.sinks != nullptr;
     switch (a.D) {
-        case 64: return launch_prefill_t<64>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        case 128: return launch_prefill_t<128>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 64:
+            return opts ? launch_prefill_t<64, true>(tm_q, tm_k, tm_v, tm_o, a, stream)
+                        : launch_prefill_t<64, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 128:
+            return opts ? launch_prefill_t<128, true>(tm_q, tm_k, tm_v, tm_o, a, stream)
+                        : launch_prefill_t<128, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
         default: return cudaErrorInvalidValue;
     }
 }
