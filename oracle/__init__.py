@@ -6,8 +6,8 @@ no code with the CUDA library and the product path never calls it.
 
 The arithmetic lives in ``oracle_fp64.c`` (plain C, double precision, one row
 at a time); this module only marshals arrays.  Inputs may be torch tensors
-(bfloat16, float32 or float64, any device-less CPU tensor) or numpy arrays;
-bfloat16 and float32 values widen to double exactly.  Outputs are float64
+(bfloat16, float16, float32 or float64, any device-less CPU tensor) or numpy
+arrays; 16- and 32-bit values widen to double exactly.  Outputs are float64
 torch tensors: ``o`` shaped like ``q`` and ``lse`` shaped ``q.shape[:-1]``.
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``.
@@ -20,7 +20,7 @@ import torch
 
 from . import build as _build
 
-_F64, _BF16 = 0, 1
+_F64, _BF16, _F16 = 0, 1, 2
 
 
 def _bind(lib):
@@ -106,6 +106,8 @@ def _tensor_in(x):
         x = x.detach().cpu().contiguous()
         if x.dtype == torch.bfloat16:
             return x.view(torch.int16).numpy().view(np.uint16), _BF16
+        if x.dtype == torch.float16:
+            return x.view(torch.int16).numpy().view(np.uint16), _F16
         return x.to(torch.float64).numpy(), _F64
     a = np.ascontiguousarray(x)
     if a.dtype == np.uint16:
@@ -124,6 +126,8 @@ def _same_kind(arrs):
 def _to_f64(a, code):
     if code == _F64:
         return a
+    if code == _F16:
+        return a.view(np.float16).astype(np.float64)
     return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 

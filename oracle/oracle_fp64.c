@@ -47,9 +47,12 @@
  * LSE = M + log Z.  Subtracting M changes nothing mathematically; it only
  * keeps exp() finite.
  *
- * Inputs may be given as IEEE double or as bfloat16 bit patterns (uint16);
- * a bfloat16 value widens to double exactly (its bits are the top half of a
- * float).  Outputs are always double.
+ * Inputs may be given as IEEE double, as bfloat16 bit patterns or as IEEE
+ * half (float16) bit patterns (uint16); both 16-bit types widen to double
+ * exactly: a bfloat16 is the top half of a float, and a half is
+ * (-1)^s * 2^(e-15) * (1 + m/1024) for a biased exponent e in 1..30,
+ * (-1)^s * 2^-14 * (m/1024) for e = 0 (zero and subnormals), and an infinity
+ * or NaN for e = 31.  Outputs are always double.
  *
  * Build: gcc -O2 -ffp-contract=off -fopenmp -fPIC -shared (OpenMP optional).
  */
@@ -61,11 +64,20 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F64 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F64 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
 
 /* Exact widening of one element of an input array to double. */
 static double load_elem(const void* base, size_t idx, int dtype) {
     if (dtype == ORACLE_F64) return ((const double*)base)[idx];
+    if (dtype == ORACLE_F16) {
+        const uint16_t h = ((const uint16_t*)base)[idx];
+        const int sign = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+        double mag;
+        if (e == 0) mag = ldexp((double)m, -24);                  /* 2^-14 * m / 1024 */
+        else if (e == 31) mag = m ? NAN : INFINITY;
+        else mag = ldexp(1024.0 + m, e - 25);                    /* 2^(e-15) * (1024 + m) / 1024 */
+        return sign ? -mag : mag;
+    }
     uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
     float f;
     memcpy(&f, &bits, sizeof f);

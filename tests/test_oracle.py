@@ -438,13 +438,30 @@ def pin_options_paged_equals_dense():
     assert (ld - lp).abs().max().item() < 1e-14
 
 
+def pin_half_inputs_widen_exactly():
+    # IEEE half inputs (the float16 calls of TileOPs GQAPagedFwdOp) widen to double
+    # exactly: the oracle on float16 tensors equals the oracle on the same values
+    # converted by torch to float64, bit for bit, including subnormals, signed
+    # zeros and the largest finite half
+    q, k, v, mask = _rand_case(2, 4, 2, 5, 9, 8, seed=26, mask_p=0.8)
+    q16, k16, v16 = q.float().half(), k.float().half(), v.float().half()
+    specials = torch.tensor([6.0e-8, -6.0e-8, 3.0e-6, -0.0, 0.0, 65504.0, -65504.0, 1.0 / 3.0],
+                            dtype=torch.float16)
+    v16[0, 0, 0, :] = specials
+    k16[1, 2, 1, :] = specials * 1e-4
+    for causal in (True, False):
+        oh, lh = oracle.attn_dense(q16, k16, v16, key_padding_mask=mask, causal=causal)
+        od, ld = oracle.attn_dense(q16.double(), k16.double(), v16.double(), key_padding_mask=mask, causal=causal)
+        assert torch.equal(oh, od) and torch.equal(lh, ld)
+
+
 PINS = [pin_golden_closed_form, pin_matches_torch_sdpa, pin_lse_matches_torch_logsumexp,
         pin_single_visible_key_exact, pin_zero_query_is_mean_of_visible_values,
         pin_gqa_equals_repeat_interleave_mha, pin_paged_equals_dense,
         pin_rows_without_visible_keys, pin_invariants, pin_chunked_prefill_and_row_independence,
         pin_noncausal_key_permutation, pin_high_precision_rows, pin_window_single_key_exact,
         pin_window_equals_key_slice, pin_softcap_closed_forms, pin_softcap_large_cap_limit,
-        pin_sinks_identity, pin_options_paged_equals_dense]
+        pin_sinks_identity, pin_options_paged_equals_dense, pin_half_inputs_widen_exactly]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -493,6 +510,8 @@ MUTANTS = {
     "softcap_scale_dropped": ("opt->softcap * tanh(z[j] / opt->softcap)", "tanh(z[j] / opt->softcap)"),
     "sink_ignored": ("double Z = sink == -INFINITY ? 0.0 : exp(sink - M);", "double Z = 0.0;"),
     "sink_plus_inf_unhandled": ("if (sink == INFINITY) {", "if (0) {"),
+    "half_exponent_bias": ("ldexp(1024.0 + m, e - 25)", "ldexp(1024.0 + m, e - 24)"),
+    "half_subnormal_scale": ("ldexp((double)m, -24)", "ldexp((double)m, -23)"),
     "mask_ignored": ("mask[(size_t)b * Skv + j] != 0", "1"),
     "scale_dropped": ("z[j] = scale * dot;", "z[j] = dot;"),
     "lse_missing_log": ("*lse_out = M + log(Z);", "*lse_out = M + Z;"),
