@@ -68,7 +68,7 @@ def load() -> ctypes.CDLL:
 class Options(ctypes.Structure):
     """gqa_options of include/gqa_attn.h."""
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int), ("softcap", ctypes.c_float),
-                ("sinks", ctypes.c_void_p)]
+                ("sinks", ctypes.c_void_p), ("dtype", ctypes.c_int)]
 
 
 def status_name(code: int) -> str:

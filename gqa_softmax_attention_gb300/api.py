@@ -33,11 +33,15 @@ def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def _check_bf16_cuda(name, t, ndim):
+_DTYPES = {torch.bfloat16: 0, torch.float16: 1}      # gqa_dtype
+
+
+def _check_16_cuda(name, t, ndim, dtypes=(torch.bfloat16, torch.float16)):
+    """A CUDA tensor of ndim dimensions and one of the given dtypes."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
-    if t.dtype != torch.bfloat16:
-        raise ValueError("%s must be bfloat16, got %s" % (name, t.dtype))
+    if t.dtype not in dtypes:
+        raise ValueError("%s must be %s, got %s" % (name, " or ".join(str(d) for d in dtypes), t.dtype))
     if t.dim() != ndim:
         raise ValueError("%s must have %d dimensions, got %d" % (name, ndim, t.dim()))
 
@@ -47,10 +51,11 @@ def resolve_scale(scale, D):
     return 1.0 / math.sqrt(D) if scale is None else float(scale)
 
 
-def _options(window_left, window_right, softcap, sinks, Hq, device):
-    """gqa_options for the optional terms, or None when none is set (the sinks
-    tensor is returned too, to keep it alive for the call)."""
-    if window_left == -1 and window_right == -1 and not softcap and sinks is None:
+def _options(window_left, window_right, softcap, sinks, Hq, device, dtype=0):
+    """gqa_options for the optional terms and the element type, or None when
+    none is set (the sinks tensor is returned too, to keep it alive for the
+    call)."""
+    if window_left == -1 and window_right == -1 and not softcap and sinks is None and dtype == 0:
         return None, None
     for n, w in (("window_left", window_left), ("window_right", window_right)):
         if int(w) < -1:
@@ -63,7 +68,8 @@ def _options(window_left, window_right, softcap, sinks, Hq, device):
         sk = torch.as_tensor(sinks).to(device=device, dtype=torch.float32).contiguous()
         if tuple(sk.shape) != (Hq,):
             raise ValueError("sinks must be [Hq] = [%d]" % Hq)
-    opt = _lib.Options(int(window_left), int(window_right), cap, sk.data_ptr() if sk is not None else None)
+    opt = _lib.Options(int(window_left), int(window_right), cap, sk.data_ptr() if sk is not None else None,
+                       int(dtype))
     return opt, sk
 
 
@@ -71,7 +77,8 @@ def attn_fwd_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, out=
                    window_left=-1, window_right=-1, softcap=None, sinks=None):
     """Dense / chunked-prefill GQA attention.
 
-    q [B,Sq,Hq,D], k/v [B,Skv,Hkv,D] bfloat16 CUDA tensors (BSHD);
+    q [B,Sq,Hq,D], k/v [B,Skv,Hkv,D] CUDA tensors (BSHD), all bfloat16 or all
+    float16 (the output takes the same type);
     key_padding_mask [B,Skv] bool (True = keep) or None.
     window_left / window_right: keys admitted left / right of each query's key
     position (-1 unlimited); softcap: c > 0 caps each scaled score to
@@ -79,8 +86,9 @@ def attn_fwd_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, out=
     softmax denominator only, or None.
     Returns (o [B,Sq,Hq,D] bf16, lse [B,Sq,Hq] float32, natural log).
     """
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _check_bf16_cuda(n, t, 4)
+    _check_16_cuda("q", q, 4)
+    for n, t in (("k", k), ("v", v)):
+        _check_16_cuda(n, t, 4, (q.dtype,))
     B, Sq, Hq, D = q.shape
     Bk, Skv, Hkv, Dk = k.shape
     if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
@@ -94,10 +102,10 @@ def attn_fwd_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, out=
             raise ValueError("key_padding_mask must be [B, Skv] = [%d, %d]" % (B, Skv))
         m = key_padding_mask.to(device=q.device, dtype=torch.bool).contiguous().view(torch.uint8)
     if out is None:
-        out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device)
-    opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device)
+    opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device, _DTYPES[q.dtype])
     lib = _lib.load()
     if opt is None:
         st = lib.attn_fwd_dense(_ptr(q), _ptr(k), _ptr(v), _ptr(m), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
@@ -121,15 +129,15 @@ def attn_decode_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=T
                       sinks=None):
     """Paged decode.
 
-    q [B,Sq,Hq,D] bf16; k_cache/v_cache [num_pages,page_size,Hkv,D] bf16;
+    q [B,Sq,Hq,D]; k_cache/v_cache [num_pages,page_size,Hkv,D], all bfloat16 or all float16;
     real_seqlen_kv [B] int32 (query tokens included); block_table [B,max_pages] int32.
     workspace: optional uint8 CUDA tensor of at least attn_decode_paged_workspace_size bytes.
     window_left / window_right / softcap / sinks as in attn_fwd_dense.
     Returns (o [B,Sq,Hq,D] bf16, lse [B,Sq,Hq] float32).
     """
-    _check_bf16_cuda("q", q, 4)
-    _check_bf16_cuda("k_cache", k_cache, 4)
-    _check_bf16_cuda("v_cache", v_cache, 4)
+    _check_16_cuda("q", q, 4)
+    _check_16_cuda("k_cache", k_cache, 4, (q.dtype,))
+    _check_16_cuda("v_cache", v_cache, 4, (q.dtype,))
     B, Sq, Hq, D = q.shape
     num_pages, page_size, Hkv, Dk = k_cache.shape
     if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
@@ -148,10 +156,10 @@ def attn_decode_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=T
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     if out is None:
-        out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device)
-    opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device)
+    opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device, _DTYPES[q.dtype])
     lib = _lib.load()
     wsb = workspace.numel() * workspace.element_size()
     if opt is None:
@@ -178,9 +186,10 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, real_seqlen_kv, block_table, 
     calls (calls overlapping on the GPU race).  Sizes whose partials do not fit
     raise ValueError.  Outputs are allocated here only when not passed in.
     """
-    _check_bf16_cuda("q", q, 4)
-    _check_bf16_cuda("k_cache", k_cache, 4)
-    _check_bf16_cuda("v_cache", v_cache, 4)
+    bf16 = (torch.bfloat16,)
+    _check_16_cuda("q", q, 4, bf16)
+    _check_16_cuda("k_cache", k_cache, 4, bf16)
+    _check_16_cuda("v_cache", v_cache, 4, bf16)
     B, Sq, Hq, D = q.shape
     num_pages, page_size, Hkv, _ = k_cache.shape
     max_pages = block_table.shape[1]

@@ -33,14 +33,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [B, S, H, D] bf16, D contiguous, as a 4-D tensor map {D, S, H, B} with a
 // {64, 128, 1, 1} box and 128-byte swizzle.  Rows past S read as zero.
-bool make_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D) {
+// The tensor maps only move 16-bit elements; the type names the data.
+CUtensorMapDataType elem_type(bool f16) {
+    return f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
+bool make_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, bool f16) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)H * D * 2, (cuuint64_t)D * 2, (cuuint64_t)S * H * D * 2};
     const cuuint32_t box[4] = {64, 128, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+    const CUresult r = fn(map, elem_type(f16), 4, const_cast<void*>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -48,14 +53,14 @@ bool make_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D
 
 // Paged cache [pages * page_size, Hkv, D] bf16 as a 3-D map {D, Hkv, rows}
 // with a {64, 1, box_tokens} box and 128-byte swizzle.
-bool make_cache_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D, int box_tokens) {
+bool make_cache_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D, int box_tokens, bool f16) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
     const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_tokens};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+    const CUresult r = fn(map, elem_type(f16), 3, const_cast<void*>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -68,7 +73,8 @@ bool make_cache_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D
 // shared memory as [group][slice][8 rows][128 bytes] (128-byte swizzle), so
 // consecutive boxes of a tile keep one uniform 8-row-group stride (D / 64 KB)
 // for every slice, which lets one MMA descriptor span the tile's 64 keys.
-bool make_cache_page_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D, int box_tokens) {
+bool make_cache_page_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D, int box_tokens,
+                         bool f16) {
     auto fn = encode_fn();
     if (!fn || rows % 8 != 0 || box_tokens % 8 != 0) return false;
     const cuuint64_t row_bytes = (cuuint64_t)Hkv * D * 2;
@@ -76,7 +82,7 @@ bool make_cache_page_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, 
     const cuuint64_t strides[4] = {row_bytes, 128, 8 * row_bytes, (cuuint64_t)D * 2};
     const cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), (cuuint32_t)(box_tokens / 8), 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(ptr), dims, strides, box,
+    const CUresult r = fn(map, elem_type(f16), 5, const_cast<void*>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -112,6 +118,7 @@ static gqa_status make_extras(const gqa_options* op, float scale, gqa::Extras* x
     if (op->window_left < -1 || op->window_right < -1) return GQA_ERR_INVALID_ARG;
     if (!std::isfinite(op->softcap) || op->softcap < 0.f) return GQA_ERR_INVALID_ARG;
     if (op->sinks && !aligned4(op->sinks)) return GQA_ERR_MISALIGNED;
+    if (op->dtype != GQA_BF16 && op->dtype != GQA_FP16) return GQA_ERR_INVALID_ARG;
     x->wl = op->window_left;
     x->wr = op->window_right;
     if (op->softcap > 0.f) {
@@ -153,8 +160,9 @@ gqa_status attn_fwd_dense_ex(const void* q, const void* k, const void* v, const 
         return gqa::launch_empty_rows(o, lse, (long)B * Sq * Hq, D, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 
     CUtensorMap tq, tk, tv, to;
-    if (!make_bshd_map(&tq, q, B, Sq, Hq, D) || !make_bshd_map(&tk, k, B, Skv, Hkv, D) ||
-        !make_bshd_map(&tv, v, B, Skv, Hkv, D) || !make_bshd_map(&to, o, B, Sq, Hq, D))
+    const bool f16 = opts && opts->dtype == GQA_FP16;
+    if (!make_bshd_map(&tq, q, B, Sq, Hq, D, f16) || !make_bshd_map(&tk, k, B, Skv, Hkv, D, f16) ||
+        !make_bshd_map(&tv, v, B, Skv, Hkv, D, f16) || !make_bshd_map(&to, o, B, Sq, Hq, D, f16))
         return GQA_ERR_CUDA;
     PrefillArgs a;
     a.mask = key_padding_mask;
@@ -164,6 +172,7 @@ gqa_status attn_fwd_dense_ex(const void* q, const void* k, const void* v, const 
     a.causal = causal ? 1 : 0;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     a.num_sms = sm_count();
+    a.f16 = f16 ? 1 : 0;
     a.x = ex;
     return gqa::launch_prefill(tq, tk, tv, to, a, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -221,6 +230,7 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
     a.seg_table = nullptr;
     a.n_part = 0;
     a.tc_grid = 0;
+    a.f16 = opts && opts->dtype == GQA_FP16 ? 1 : 0;
     a.x = ex;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // KV groups of 32..128 query rows run on the balanced tensor-core decode
@@ -228,8 +238,8 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
     if (num_pages > 0 && p.tc) {
         const int tbox = gqa::decode_tc_box_tokens(page_size);
         CUtensorMap tk, tv;
-        if (make_cache_page_map(&tk, k_cache, (long)num_pages * page_size, Hkv, D, tbox) &&
-            make_cache_page_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, tbox)) {
+        if (make_cache_page_map(&tk, k_cache, (long)num_pages * page_size, Hkv, D, tbox, a.f16) &&
+            make_cache_page_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, tbox, a.f16)) {
             char* ws = static_cast<char*>(workspace);
             const size_t o_bytes = (p.tc_part_o_bytes + 255) / 256 * 256;
             const size_t l_bytes = (p.tc_part_lse_bytes + 255) / 256 * 256;
@@ -246,8 +256,8 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
     const int box = gqa::decode_box_tokens(D, page_size);
     CUtensorMap tk, tv;
     const bool use_tma = box > 0 && num_pages > 0 &&
-                         make_cache_map(&tk, k_cache, (long)num_pages * page_size, Hkv, D, box) &&
-                         make_cache_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, box);
+                         make_cache_map(&tk, k_cache, (long)num_pages * page_size, Hkv, D, box, a.f16) &&
+                         make_cache_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, box, a.f16);
     return gqa::launch_decode(a, use_tma ? &tk : nullptr, use_tma ? &tv : nullptr, box, st) == cudaSuccess
                ? GQA_OK
                : GQA_ERR_CUDA;

@@ -49,8 +49,9 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 constexpr int key_tile(int D) { return D == 256 ? 32 : 64; }
 
-template <int D, int MF, bool TMA>
+template <int D, int MF, bool TMA, bool F16_ = false>
 struct DCfg {
+    static constexpr bool F16 = F16_;                        // float16 data (else bfloat16)
     static constexpr int TK = key_tile(D);                   // tokens per key tile
     static constexpr int KSPLIT = (MF == 1 && TK == 64) ? 4 : 2;   // consumer warps per 16-row fragment
     static constexpr int NC = MF * KSPLIT;                   // consumer warps
@@ -215,8 +216,8 @@ struct Consumer {
                 const int chunk = kk * 2 + ((lane >> 3) & 1);
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(sK + sw_off(key, chunk, C::SUB_BYTES), b0, b1, b2, b3);
-                mma_16816(sacc[2 * np], qf[kk], b0, b1);
-                mma_16816(sacc[2 * np + 1], qf[kk], b2, b3);
+                mma16816<C::F16>(sacc[2 * np], qf[kk], b0, b1);
+                mma16816<C::F16>(sacc[2 * np + 1], qf[kk], b2, b3);
             }
         }
         float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
@@ -267,7 +268,7 @@ struct Consumer {
             const float p0 = fast_exp2(x[2 * e] - m_use);
             const float p1 = fast_exp2(x[2 * e + 1] - m_use);
             sum += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
+            pk[e] = pack2<C::F16>(p0, p1);
         }
 #pragma unroll
         for (int o = C::TPR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -306,8 +307,8 @@ struct Consumer {
                 const int dchunk = (wk * C::DSL + np * 16) / 8 + (lane >> 4);
                 uint32_t v0, v1, v2, v3;
                 ldsm_x4_t(sV + sw_off(key, dchunk, C::SUB_BYTES), v0, v1, v2, v3);
-                mma_16816(acc[2 * np], pa, v0, v1);
-                mma_16816(acc[2 * np + 1], pa, v2, v3);
+                mma16816<C::F16>(acc[2 * np], pa, v0, v1);
+                mma16816<C::F16>(acc[2 * np + 1], pa, v2, v3);
             }
         }
     }
@@ -343,11 +344,11 @@ struct Consumer {
     }
 };
 
-template <int D, int MF>
-__global__ void __launch_bounds__(DCfg<D, MF, true>::NT)
+template <int D, int MF, bool F16>
+__global__ void __launch_bounds__(DCfg<D, MF, true, F16>::NT)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeArgs a, int R, int g, int n_rowblk, int box_tokens) {
-    using C = DCfg<D, MF, true>;
+    using C = DCfg<D, MF, true, F16>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -457,10 +458,10 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_decode_error, (int)kErrDecodeWait);
 }
 
-template <int D, int MF>
-__global__ void __launch_bounds__(DCfg<D, MF, false>::NT)
+template <int D, int MF, bool F16>
+__global__ void __launch_bounds__(DCfg<D, MF, false, F16>::NT)
 decode_gather_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
-    using C = DCfg<D, MF, false>;
+    using C = DCfg<D, MF, false, F16>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -524,7 +525,7 @@ decode_gather_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
     c.store(a, w, R, bar);
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a, int R, int g) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const long row = (long)blockIdx.x * 4 + warp;
@@ -613,8 +614,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
         const int d = (q * 32 + lane) * 4;
         if (d < D)
             *reinterpret_cast<uint2*>(out + d) =
-                make_uint2(pack_bf16x2(accv[q][0] * inv, accv[q][1] * inv),
-                           pack_bf16x2(accv[q][2] * inv, accv[q][3] * inv));
+                make_uint2(pack2<F16>(accv[q][0] * inv, accv[q][1] * inv),
+                           pack2<F16>(accv[q][2] * inv, accv[q][3] * inv));
     }
     if (lane == 0 && a.lse) a.lse[row] = (M + log2f(den)) * kLn2;
 }
@@ -624,22 +625,22 @@ int choose_mf(int R) {
     return blocks16 >= 4 ? 4 : blocks16;
 }
 
-template <int D, int MF>
+template <int D, int MF, bool F16>
 cudaError_t launch_split(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int box_tokens,
                          int R, int g, int n_rowblk, cudaStream_t stream) {
     dim3 grid(a.max_splits, a.Hkv, a.B * n_rowblk);
     if (tm_k) {
-        using C = DCfg<D, MF, true>;
-        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<D, MF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM);
-        if (e != cudaSuccess) return e;
-        decode_tma_kernel<D, MF><<<grid, C::NT, C::SMEM, stream>>>(*tm_k, *tm_v, a, R, g, n_rowblk, box_tokens);
-    } else {
-        using C = DCfg<D, MF, false>;
-        cudaError_t e = cudaFuncSetAttribute(decode_gather_kernel<D, MF>,
+        using C = DCfg<D, MF, true, F16>;
+        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<D, MF, F16>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        decode_gather_kernel<D, MF><<<grid, C::NT, C::SMEM, stream>>>(a, R, g, n_rowblk);
+        decode_tma_kernel<D, MF, F16><<<grid, C::NT, C::SMEM, stream>>>(*tm_k, *tm_v, a, R, g, n_rowblk, box_tokens);
+    } else {
+        using C = DCfg<D, MF, false, F16>;
+        cudaError_t e = cudaFuncSetAttribute(decode_gather_kernel<D, MF, F16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        decode_gather_kernel<D, MF, F16><<<grid, C::NT, C::SMEM, stream>>>(a, R, g, n_rowblk);
     }
     return cudaGetLastError();
 }
@@ -652,11 +653,15 @@ cudaError_t launch_d(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtenso
     const int mf = choose_mf(R);
     const int n_rowblk = (R + 16 * mf - 1) / (16 * mf);
     cudaError_t e;
-    switch (mf) {
-        case 1: e = launch_split<D, 1>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
-        case 2: e = launch_split<D, 2>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
-        case 3: e = launch_split<D, 3>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
-        default: e = launch_split<D, 4>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+    switch (mf * 2 + (a.f16 ? 1 : 0)) {
+        case 2: e = launch_split<D, 1, false>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        case 3: e = launch_split<D, 1, true>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        case 4: e = launch_split<D, 2, false>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        case 5: e = launch_split<D, 2, true>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        case 6: e = launch_split<D, 3, false>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        case 7: e = launch_split<D, 3, true>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        case 8: e = launch_split<D, 4, false>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
+        default: e = launch_split<D, 4, true>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream); break;
     }
     if (e != cudaSuccess) return e;
     return launch_decode_combine(a, stream);
@@ -728,9 +733,18 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream) {
     const long rows = (long)a.B * a.Sq * a.Hq;
     const unsigned blocks = (unsigned)((rows + 3) / 4);
     switch (a.D) {
-        case 64: decode_combine_kernel<64><<<blocks, 128, 0, stream>>>(a, R, g); break;
-        case 128: decode_combine_kernel<128><<<blocks, 128, 0, stream>>>(a, R, g); break;
-        case 256: decode_combine_kernel<256><<<blocks, 128, 0, stream>>>(a, R, g); break;
+        case 64:
+            if (a.f16) decode_combine_kernel<64, true><<<blocks, 128, 0, stream>>>(a, R, g);
+            else decode_combine_kernel<64, false><<<blocks, 128, 0, stream>>>(a, R, g);
+            break;
+        case 128:
+            if (a.f16) decode_combine_kernel<128, true><<<blocks, 128, 0, stream>>>(a, R, g);
+            else decode_combine_kernel<128, false><<<blocks, 128, 0, stream>>>(a, R, g);
+            break;
+        case 256:
+            if (a.f16) decode_combine_kernel<256, true><<<blocks, 128, 0, stream>>>(a, R, g);
+            else decode_combine_kernel<256, false><<<blocks, 128, 0, stream>>>(a, R, g);
+            break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -94,8 +94,6 @@ struct TCfg {
     // TMEM: S0 | S1 | O | Q (Q rows as bf16 pairs, the A operand of S = Q K^T)
     static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN, COL_Q = 2 * BN + D;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t IDESC_QK = make_idesc_bf16(BM, BN, false, false);
-    static constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, D, false, true);
     static_assert(COL_Q + D / 2 <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -169,11 +167,14 @@ __device__ __forceinline__ void q_row_to_tmem(const DecodeArgs& a, uint32_t tadd
     for (int c = 0; c < D / 64; ++c) tmem_st32(taddr + 32 * c, w + 32 * c);
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const DecodeArgs a, int R, int g, int box_tokens) {
     using C = TCfg<D>;
+    // both MMA operands of the call's 16-bit type (P is packed to it as well)
+    constexpr uint32_t IDESC_QK = make_idesc_16<F16>(BM, BN, false, false);
+    constexpr uint32_t IDESC_PV = make_idesc_16<F16>(BM, D, false, true);
     const int cta = blockIdx.x;
 
     extern __shared__ uint8_t smem_raw[];
@@ -374,7 +375,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_bf16_ts(d, tmem + C::COL_Q + kk * 8,
-                                kdesc + (uint64_t)((((kk / 4) * 1024 + (kk % 4) * 32)) >> 4), C::IDESC_QK,
+                                kdesc + (uint64_t)((((kk / 4) * 1024 + (kk % 4) * 32)) >> 4), IDESC_QK,
                                 kk > 0 ? 1u : 0u);
                 mma_commit(s_full(i & 1));
                 mma_commit(k_empty(ks));
@@ -417,7 +418,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_bf16_ts(tmem + C::COL_O, tmem + pcol + kk * 8,
-                                vdesc + (uint64_t)((2 * kk * C::GROUP_STRIDE) >> 4), C::IDESC_PV,
+                                vdesc + (uint64_t)((2 * kk * C::GROUP_STRIDE) >> 4), IDESC_PV,
                                 (!fresh || kk > 0) ? 1u : 0u);
                 mma_commit(o_done);
                 mma_commit(v_empty(vs));
@@ -532,7 +533,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 f32x2_split(ffma2(f32x2(s[2 * cc], s[2 * cc + 1]), fa2, nm2), x0, x1);
                 const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
                 rs4[cc & 3] = fadd2(rs4[cc & 3], f32x2(p0, p1));
-                pk[cc] = pack_bf16x2(p0, p1);
+                pk[cc] = pack2<F16>(p0, p1);
             }
             rs4[0] = fadd2(rs4[0], rs4[2]);
             rs4[1] = fadd2(rs4[1], rs4[3]);
@@ -617,16 +618,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_decode_tc_error, (int)kErrDecodeWait);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_t(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecodeArgs& a,
                      int box_tokens, cudaStream_t stream) {
     using C = TCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int g = a.Hq / a.Hkv;
     const int R = g * a.Sq;
-    decode_tc_kernel<D><<<a.tc_grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_k, tm_v, a, R, g, box_tokens);
+    decode_tc_kernel<D, F16><<<a.tc_grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_k, tm_v, a, R, g, box_tokens);
     return cudaGetLastError();
 }
 
@@ -648,8 +649,10 @@ cudaError_t launch_decode_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const DecodeArgs& a, int box_tokens, cudaStream_t stream) {
     cudaError_t e;
     switch (a.D) {
-        case 128: e = launch_t<128>(tm_k, tm_v, a, box_tokens, stream); break;
-        case 256: e = launch_t<256>(tm_k, tm_v, a, box_tokens, stream); break;
+        case 128: e = a.f16 ? launch_t<128, true>(tm_k, tm_v, a, box_tokens, stream)
+                            : launch_t<128, false>(tm_k, tm_v, a, box_tokens, stream); break;
+        case 256: e = a.f16 ? launch_t<256, true>(tm_k, tm_v, a, box_tokens, stream)
+                            : launch_t<256, false>(tm_k, tm_v, a, box_tokens, stream); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;

@@ -24,6 +24,7 @@ struct PrefillArgs {
     int causal;
     float scale_log2;     // scale * log2(e)
     int num_sms;          // persistent grid size
+    int f16;              // inputs and output are float16 (else bfloat16)
     Extras x;
 };
 
@@ -58,6 +59,7 @@ struct DecodeArgs {
     int* seg_table;         // [B * Hkv, 2]
     int n_part;             // partial slots in part_o / part_lse
     int tc_grid;            // persistent CTAs (one per SM)
+    int f16;                // q, caches and o are float16 (else bfloat16)
     Extras x;
 };
 

@@ -89,8 +89,6 @@ struct Cfg {
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128;
     static constexpr uint32_t COL_O0 = 256, COL_O1 = 256 + D;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t IDESC_QK = make_idesc_bf16(BM, BN, false, false);
-    static constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, D, false, true);
     static_assert(COL_O1 + D <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -193,7 +191,7 @@ __device__ __forceinline__ uint32_t below_bits(int n, int chunk) {
 // p[c] = 2^(s[c] * fa - m_use) for one 128-column row: P packed to bf16x2 in
 // pk, the row sum returned.  Two columns per paired FMA / add; with POLY > 0,
 // one column pair in POLY is evaluated on the FMA pipe instead of the MUFU.
-template <int POLY>
+template <int POLY, bool F16>
 __device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, uint32_t* pk) {
     const uint64_t fa2 = f32x2(fa, fa);
     const uint64_t nm2 = f32x2(-m_use, -m_use);
@@ -211,7 +209,7 @@ __device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, 
             p1 = fast_exp2(x1);
         }
         rs4[c & 3] = fadd2(rs4[c & 3], f32x2(p0, p1));
-        pk[c] = pack_bf16x2(p0, p1);
+        pk[c] = pack2<F16>(p0, p1);
     }
     rs4[0] = fadd2(rs4[0], rs4[2]);
     rs4[1] = fadd2(rs4[1], rs4[3]);
@@ -224,12 +222,15 @@ __device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, 
 // OPTS: the call has a window, a softcap or sinks.  Without them every option
 // term is a compile-time constant and the code is the plain causal / padded
 // kernel.
-template <int D, bool OPTS>
+template <int D, bool OPTS, bool F16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const PrefillArgs a, int n_qpairs) {
     using C = Cfg<D>;
+    // both MMA operands of the call's 16-bit type (P is packed to it as well)
+    constexpr uint32_t IDESC_QK = make_idesc_16<F16>(BM, BN, false, false);
+    constexpr uint32_t IDESC_PV = make_idesc_16<F16>(BM, D, false, true);
     const int wl = OPTS ? a.x.wl : -1;
     const int wr = OPTS ? a.x.wr : -1;
     const float cap_in = OPTS ? a.x.cap_in : 0.f;
@@ -432,7 +433,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             const uint32_t koff = (kk / 4) * C::SUB_BYTES + (kk % 4) * 32;
                             mma_bf16_ss(tmem + (k == 0 ? C::COL_S0 : C::COL_S1),
                                         make_sdesc_sw128(qbase + koff, 16, 1024),
-                                        make_sdesc_sw128(kbase + koff, 16, 1024), C::IDESC_QK, kk > 0 ? 1u : 0u);
+                                        make_sdesc_sw128(kbase + koff, 16, 1024), IDESC_QK, kk > 0 ? 1u : 0u);
                         }
                         mma_commit(s_full(k));
                     };
@@ -443,7 +444,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             // keys 16kk..16kk+15 of V: rows 16kk.. of every 64-column box
                             const uint64_t bdesc = make_sdesc_sw128(vbase + kk * 16 * 128, C::SUB_BYTES, 1024);
                             mma_bf16_ts(tmem + (k == 0 ? C::COL_O0 : C::COL_O1),
-                                        tmem + (k == 0 ? C::COL_S0 : C::COL_S1) + kk * 8, bdesc, C::IDESC_PV,
+                                        tmem + (k == 0 ? C::COL_S0 : C::COL_S1) + kk * 8, bdesc, IDESC_PV,
                                         (i > 0 || kk > 0) ? 1u : 0u);
                         }
                     };
@@ -644,8 +645,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const float fa = fast ? sl : 1.f;
                 uint32_t pk[BN / 2];
                 float rs;
-                if (fast) rs = exp_row<kPolyEvery>(s, fa, m_use, pk);
-                else rs = exp_row<0>(s, fa, m_use, pk);
+                if (fast) rs = exp_row<kPolyEvery, F16>(s, fa, m_use, pk);
+                else rs = exp_row<0, F16>(s, fa, m_use, pk);
                 tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
                 l_run = l_run * alpha + rs;
 
@@ -717,9 +718,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {              // 16-byte chunk q of the box row
                         const float* f = reinterpret_cast<const float*>(ow + 64 * sub + 8 * q);
-                        st_shared_v4(stage + r * 128 + ((q ^ (r & 7)) << 4), pack_bf16x2(f[0] * inv, f[1] * inv),
-                                     pack_bf16x2(f[2] * inv, f[3] * inv), pack_bf16x2(f[4] * inv, f[5] * inv),
-                                     pack_bf16x2(f[6] * inv, f[7] * inv));
+                        st_shared_v4(stage + r * 128 + ((q ^ (r & 7)) << 4), pack2<F16>(f[0] * inv, f[1] * inv),
+                                     pack2<F16>(f[2] * inv, f[3] * inv), pack2<F16>(f[4] * inv, f[5] * inv),
+                                     pack2<F16>(f[6] * inv, f[7] * inv));
                     }
                     fence_proxy_async_smem();
                     named_bar_sync(3 + k, BM);
@@ -761,19 +762,19 @@ __global__ void empty_rows_kernel(__nv_bfloat16* o, float* lse, long rows, int D
     }
 }
 
-template <int D, bool OPTS>
+template <int D, bool OPTS, bool F16>
 cudaError_t launch_prefill_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream) {
     using C = Cfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, OPTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, OPTS, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_qpairs = (a.Sq + NQ * BM - 1) / (NQ * BM);
     const long n_items = (long)n_qpairs * a.B * a.Hq;
     const long sms = a.num_sms > 0 ? a.num_sms : 148;
     const long grid = n_items < sms ? n_items : sms;    // persistent: one CTA per SM
-    prefill_kernel<D, OPTS><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, tm_o, a,
-                                                                                   n_qpairs);
+    prefill_kernel<D, OPTS, F16><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, tm_o, a,
+                                                                                        n_qpairs);
     return cudaGetLastError();
 }
 
@@ -782,13 +783,16 @@ cudaError_t launch_prefill_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream) {
     const bool opts = a.x.wl >= 0 || a.x.wr >= 0 || a.x.cap_out != 0.f || a.x.sinks != nullptr;
-    switch (a.D) {
-        case 64:
-            return opts ? launch_prefill_t<64, true>(tm_q, tm_k, tm_v, tm_o, a, stream)
-                        : launch_prefill_t<64, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        case 128:
-            return opts ? launch_prefill_t<128, true>(tm_q, tm_k, tm_v, tm_o, a, stream)
-                        : launch_prefill_t<128, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
+    const int sel = (opts ? 1 : 0) + (a.f16 ? 2 : 0);
+    switch (a.D * 4 + sel) {
+        case 64 * 4 + 0: return launch_prefill_t<64, false, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 64 * 4 + 1: return launch_prefill_t<64, true, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 64 * 4 + 2: return launch_prefill_t<64, false, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 64 * 4 + 3: return launch_prefill_t<64, true, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 128 * 4 + 0: return launch_prefill_t<128, false, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 128 * 4 + 1: return launch_prefill_t<128, true, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 128 * 4 + 2: return launch_prefill_t<128, false, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
+        case 128 * 4 + 3: return launch_prefill_t<128, true, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -229,6 +229,15 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 }
 
 // Instruction descriptor, kind::f16: bf16 x bf16 -> f32, M x N, operand majors.
+// Instruction descriptor, kind::f16: f16 x f16 -> f32 (A and B format 0).
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4)                                // D format: f32
+           | ((a_mn_major ? 1u : 0u) << 15)         // A major
+           | ((b_mn_major ? 1u : 0u) << 16)         // B major
+           | ((uint32_t)(N >> 3) << 17)             // N / 8
+           | ((uint32_t)(M >> 4) << 24);            // M / 16
+}
+
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
     return (1u << 4)                                // D format: f32
            | (1u << 7)                              // A format: bf16
@@ -237,6 +246,12 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_m
            | ((b_mn_major ? 1u : 0u) << 16)         // B major
            | ((uint32_t)(N >> 3) << 17)             // N / 8
            | ((uint32_t)(M >> 4) << 24);            // M / 16
+}
+
+// The call's 16-bit type: both operands f16 (F16) or both bf16.
+template <bool F16>
+__host__ __device__ constexpr uint32_t make_idesc_16(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return F16 ? make_idesc_f16(M, N, a_mn_major, b_mn_major) : make_idesc_bf16(M, N, a_mn_major, b_mn_major);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
@@ -396,6 +411,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two FP32 values rounded (nearest even) to the call's 16-bit type, lo in the
+// low half.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (F16) return pack_f16x2(lo, hi);
+    else return pack_bf16x2(lo, hi);
+}
+
 // ---------------------------------------------------------------- cp.async / ldmatrix / mma.sync
 // 16-byte async copy global -> shared; src_bytes == 0 writes 16 zero bytes.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -428,6 +457,21 @@ __device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t 
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_16816_f16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D (FP32) += A * B on 16-bit operands of the call's type.
+template <bool F16>
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    if constexpr (F16) mma_16816_f16(c, a, b0, b1);
+    else mma_16816(c, a, b0, b1);
 }
 
 }  // namespace gqa

@@ -75,13 +75,22 @@ typedef enum {
  *                 sink; +inf makes that head's output zero (LSE +inf).  A row
  *                 with no visible key outputs zeros with LSE -inf either way.
  *                 4-byte aligned; read on the device, never copied.
- * Window values below -1 or a bad softcap return GQA_ERR_INVALID_ARG.
+ *   dtype         GQA_BF16 (default) or GQA_FP16 (TileOPs GQAPagedFwdOp serves
+ *                 "a float16 or bfloat16 dtype" shared by Q and the cache):
+ *                 q, k, v / the caches and o all have this type; products and
+ *                 sums stay FP32, P is rounded to the same type before P V.
+ * Window values below -1, a bad softcap or another dtype return
+ * GQA_ERR_INVALID_ARG.
  */
+/* Element type of q, k, v (or the caches) and o. */
+typedef enum { GQA_BF16 = 0, GQA_FP16 = 1 } gqa_dtype;
+
 typedef struct {
     int window_left;
     int window_right;
     float softcap;
     const float* sinks;
+    int dtype;            /* gqa_dtype: every 16-bit tensor of the call; 0 = bfloat16 */
 } gqa_options;
 
 /*
