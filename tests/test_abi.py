@@ -106,7 +106,7 @@ def test_python_layer_rejects_cpu_tensors():
 
 class Opts(ctypes.Structure):
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int), ("softcap", ctypes.c_float),
-                ("sinks", ctypes.c_void_p)]
+                ("sinks", ctypes.c_void_p), ("dtype", ctypes.c_int)]
 
 
 def test_option_checks(lib):
@@ -126,6 +126,7 @@ def test_option_checks(lib):
         assert call(Opts(-1, -1, float("nan"), None)) == INVALID
         assert call(Opts(-1, -1, float("inf"), None)) == INVALID
         assert call(Opts(-1, -1, 0.0, (1 << 20) + 2)) == MISALIGNED
+        assert call(Opts(-1, -1, 0.0, None, 2)) == INVALID       # neither GQA_BF16 nor GQA_FP16
 
 
 def test_python_layer_option_checks():
