@@ -32,18 +32,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [B, S, H, D] bf16, D contiguous, as a 4-D tensor map {D, S, H, B} with a
-// {64, 128, 1, 1} box and 128-byte swizzle.  Rows past S read as zero.
+// {64, box_rows, 1, 1} box and 128-byte swizzle.  Rows past S read as zero.
 // The tensor maps only move 16-bit elements; the type names the data.
 CUtensorMapDataType elem_type(bool f16) {
     return f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
-bool make_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, bool f16) {
+bool make_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, bool f16, int box_rows = 128) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)H * D * 2, (cuuint64_t)D * 2, (cuuint64_t)S * H * D * 2};
-    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUresult r = fn(map, elem_type(f16), 4, const_cast<void*>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -144,7 +144,7 @@ gqa_status attn_fwd_dense_ex(const void* q, const void* k, const void* v, const 
     if (Sq >= kMaxSeq || Skv >= kMaxSeq) return GQA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
-    if (!head_dim_ok(D) || D == 256) return GQA_ERR_UNSUPPORTED;
+    if (!head_dim_ok(D)) return GQA_ERR_UNSUPPORTED;
     if (Sq == 0) return GQA_OK;
     if (!q || !o || (Skv > 0 && (!k || !v))) return GQA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(o) || (Skv > 0 && (!aligned16(k) || !aligned16(v)))) return GQA_ERR_MISALIGNED;
@@ -162,7 +162,7 @@ gqa_status attn_fwd_dense_ex(const void* q, const void* k, const void* v, const 
     CUtensorMap tq, tk, tv, to;
     const bool f16 = opts && opts->dtype == GQA_FP16;
     if (!make_bshd_map(&tq, q, B, Sq, Hq, D, f16) || !make_bshd_map(&tk, k, B, Skv, Hkv, D, f16) ||
-        !make_bshd_map(&tv, v, B, Skv, Hkv, D, f16) || !make_bshd_map(&to, o, B, Sq, Hq, D, f16))
+        !make_bshd_map(&tv, v, B, Skv, Hkv, D, f16, D == 256 ? 64 : 128) || !make_bshd_map(&to, o, B, Sq, Hq, D, f16))
         return GQA_ERR_CUDA;
     PrefillArgs a;
     a.mask = key_padding_mask;
@@ -174,7 +174,9 @@ gqa_status attn_fwd_dense_ex(const void* q, const void* k, const void* v, const 
     a.num_sms = sm_count();
     a.f16 = f16 ? 1 : 0;
     a.x = ex;
-    return gqa::launch_prefill(tq, tk, tv, to, a, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    const cudaError_t e = D == 256 ? gqa::launch_prefill_d256(tq, tk, tv, to, a, st)
+                                   : gqa::launch_prefill(tq, tk, tv, to, a, st);
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 size_t attn_decode_paged_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_pages) {
@@ -303,10 +305,11 @@ const char* gqa_status_string(gqa_status s) {
 gqa_status gqa_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
     const int e = gqa::prefill_take_device_error();
+    const int e2 = gqa::prefill_d256_take_device_error();
     const int d = gqa::decode_take_device_error();
     const int t = gqa::decode_tc_take_device_error();
-    if (e < 0 || d < 0 || t < 0) return GQA_ERR_CUDA;
-    return (e || d || t) ? GQA_ERR_TIMEOUT : GQA_OK;
+    if (e < 0 || e2 < 0 || d < 0 || t < 0) return GQA_ERR_CUDA;
+    return (e || e2 || d || t) ? GQA_ERR_TIMEOUT : GQA_OK;
 }
 
 gqa_status gqa_exp2_poly(const float* x, float* y, long n, gqa_stream_t stream) {

@@ -36,6 +36,11 @@ cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
 // Rows with no key at all (Skv == 0): O = 0, LSE = -inf.
 cudaError_t launch_empty_rows(void* o, float* lse, long rows, int D, cudaStream_t stream);
 int prefill_take_device_error();
+// Head dim 256 (prefill_d256.cu): one query tile per CTA.  tm_q, tm_k, tm_o as
+// above; tm_v with a {64, 64, 1, 1} box (64-key halves of a V tile).
+cudaError_t launch_prefill_d256(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream);
+int prefill_d256_take_device_error();
 // y[i] = 2^x[i] by the prefill kernel's FMA-pipe exp2 (diagnostic).
 cudaError_t launch_exp2_poly(const float* x, float* y, long n, cudaStream_t stream);
 

@@ -40,6 +40,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "prefill_tiles.cuh"
 #include "ptx.cuh"
 
 namespace gqa {
@@ -47,9 +48,8 @@ namespace {
 
 __device__ int g_prefill_error;
 
-constexpr int BM = 128;            // query rows per Q tile (= TMEM lanes)
+using namespace pf;
 constexpr int NQ = 2;              // Q tiles per CTA
-constexpr int BN = 128;            // keys per tile
 constexpr int NUM_THREADS = 384;   // warps 0-7 softmax, 8 producer, 9 MMA, 10-11 idle
 constexpr int WARP_LOAD = 8;
 constexpr int WARP_MMA = 9;
@@ -60,8 +60,6 @@ constexpr int kRegsLaunch = 168;
 constexpr int kRegsSoftmax = 208;
 constexpr int kRegsOther = 88;
 static_assert(kRegsSoftmax * 256 + kRegsOther * 128 <= kRegsLaunch * NUM_THREADS, "register split");
-constexpr float kLn2 = 0.693147180559945309f;
-constexpr float kRescaleThreshold = 8.f;   // log2 units: P <= 256 between rescales
 // One exponential pair in kPolyEvery goes to the FMA-pipe exp2 on unmasked
 // tiles (0: all on the MUFU).
 constexpr int kPolyEvery = 0;
@@ -92,132 +90,6 @@ struct Cfg {
     static_assert(COL_O1 + D <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
-
-struct TileInfo {
-    int q0;          // first query row of the tile
-    int rows_valid;  // rows of the tile that exist (ragged tail; may be 0)
-    int lim_first;   // keys below lim_first are inside every row's upper bound
-    int lo_last;     // keys from lo_last on are inside every row's lower (window) bound
-    int kv_begin;    // no row of the tile sees a key < kv_begin
-    int kv_end;      // no row of the tile sees a key >= kv_end
-    int n_tiles;     // key tiles in [0, kv_end)
-};
-
-// Visible keys of the query at key position p: [lo, hi) (TileOPs "Attention
-// Operators", GQADenseFwdOp stage 5: causal j <= p, window p - wL <= j <= p + wR).
-__device__ __forceinline__ long key_hi(long p, int Skv, int causal, int wr) {
-    long hi = Skv;
-    if (causal) hi = min(hi, p + 1);
-    if (wr >= 0) hi = min(hi, p + wr + 1);
-    return max(0L, hi);
-}
-__device__ __forceinline__ long key_lo(long p, int Skv, int wl) {
-    return wl >= 0 ? min((long)Skv, max(0L, p - wl)) : 0L;
-}
-
-__device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causal, int wl, int wr) {
-    TileInfo t;
-    t.q0 = q0;
-    t.rows_valid = max(0, min(BM, Sq - q0));
-    if (t.rows_valid == 0) {
-        t.kv_begin = t.kv_end = t.lim_first = t.lo_last = 0;
-    } else {
-        const long p_first = (long)q0 + Skv - Sq;        // key position of the first row
-        const long p_last = p_first + t.rows_valid - 1;
-        t.kv_end = (int)key_hi(p_last, Skv, causal, wr);
-        t.lim_first = (int)key_hi(p_first, Skv, causal, wr);
-        t.kv_begin = (int)key_lo(p_first, Skv, wl);
-        t.lo_last = (int)key_lo(p_last, Skv, wl);
-        if (t.kv_begin >= t.kv_end) t.kv_begin = t.kv_end = t.lim_first = t.lo_last = 0;
-    }
-    t.n_tiles = (t.kv_end + BN - 1) / BN;
-    return t;
-}
-
-// Warp-collective.  Bit l of the result is set when key tile 32 * chunk + l
-// (in [first, n_tiles)) holds a key below kv_end that the padding mask keeps; lane l
-// scans that tile, so 32 tiles cost one pass.  Without a mask every tile
-// below n_tiles counts.
-__device__ __forceinline__ uint32_t tile_flags(const uint8_t* mrow, int chunk, int first, int n_tiles, int kv_end,
-                                               int lane) {
-    const int j = chunk * 32 + lane;
-    bool any = j >= first && j < n_tiles;
-    if (mrow && any) {
-        const int k0 = j * BN, k1 = min(k0 + BN, kv_end);
-        const uint8_t* p = mrow + k0;
-        any = false;
-        if (k1 - k0 == BN && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
-            const uint4* q = reinterpret_cast<const uint4*>(p);
-            uint32_t acc = 0;
-#pragma unroll
-            for (int e = 0; e < BN / 16; ++e) {
-                const uint4 v = __ldg(q + e);
-                acc |= v.x | v.y | v.z | v.w;
-            }
-            any = acc != 0;
-        } else {
-            for (int k = 0; k < k1 - k0 && !any; ++k) any = p[k] != 0;
-        }
-    }
-    return __ballot_sync(0xffffffffu, any);
-}
-
-// Walks the visited key tiles (non-empty ones in [first, n_tiles)) in increasing
-// order, 32 tiles per scan.  Warp-collective; every lane sees the same tiles.
-struct TileIter {
-    const uint8_t* mrow;
-    int first, n_tiles, kv_end, lane, chunk;
-    uint32_t f;
-    __device__ __forceinline__ TileIter(const uint8_t* m, int fst, int n, int e, int l)
-        : mrow(m), first(fst), n_tiles(n), kv_end(e), lane(l), chunk(fst / 32 - 1), f(0) {}
-    __device__ __forceinline__ int next() {   // next visited tile, or -1
-        while (f == 0) {
-            ++chunk;
-            if (chunk * 32 >= n_tiles) return -1;
-            f = tile_flags(mrow, chunk, first, n_tiles, kv_end, lane);
-        }
-        const int l = __ffs(f) - 1;
-        f &= f - 1;
-        return chunk * 32 + l;
-    }
-};
-
-// Bits of the tiles of chunk `chunk` whose index is below n.
-__device__ __forceinline__ uint32_t below_bits(int n, int chunk) {
-    const int rel = n - chunk * 32;
-    return rel >= 32 ? 0xffffffffu : (rel <= 0 ? 0u : ((1u << rel) - 1u));
-}
-
-// p[c] = 2^(s[c] * fa - m_use) for one 128-column row: P packed to bf16x2 in
-// pk, the row sum returned.  Two columns per paired FMA / add; with POLY > 0,
-// one column pair in POLY is evaluated on the FMA pipe instead of the MUFU.
-template <int POLY, bool F16>
-__device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, uint32_t* pk) {
-    const uint64_t fa2 = f32x2(fa, fa);
-    const uint64_t nm2 = f32x2(-m_use, -m_use);
-    uint64_t rs4[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) rs4[e] = f32x2(0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < BN / 2; ++c) {
-        float x0, x1, p0, p1;
-        f32x2_split(ffma2(f32x2(s[2 * c], s[2 * c + 1]), fa2, nm2), x0, x1);
-        if (POLY > 0 && c % (POLY > 0 ? POLY : 1) == (POLY > 0 ? POLY : 1) - 1) {
-            exp2_poly_x2(x0, x1, p0, p1);
-        } else {
-            p0 = fast_exp2(x0);
-            p1 = fast_exp2(x1);
-        }
-        rs4[c & 3] = fadd2(rs4[c & 3], f32x2(p0, p1));
-        pk[c] = pack2<F16>(p0, p1);
-    }
-    rs4[0] = fadd2(rs4[0], rs4[2]);
-    rs4[1] = fadd2(rs4[1], rs4[3]);
-    float r0, r1, r2, r3;
-    f32x2_split(rs4[0], r0, r1);
-    f32x2_split(rs4[1], r2, r3);
-    return (r0 + r1) + (r2 + r3);
-}
 
 // OPTS: the call has a window, a softcap or sinks.  Without them every option
 // term is a compile-time constant and the code is the plain causal / padded

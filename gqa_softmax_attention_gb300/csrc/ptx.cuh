@@ -139,6 +139,10 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// The same, allowing the most recent committed group to be still reading.
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses of the same memory.

@@ -22,9 +22,10 @@ round-to-nearest-even):
   entries of the permutation, in request order; unused block_table entries are
   -1.  Streams 0, 1, 2 are q, k_cache, v_cache.
 
-The five named workloads are the shapes of the pages' examples: a tiny GQA
-case, a Qwen3-8B-shaped prefill (Hq=32, Hkv=8, D=128), a paged decode batch of
-the same geometry, a 24/2/D256 multi-query decode and a long chunked prefill.
+The named workloads are the shapes of the pages' examples: a tiny GQA case, a
+Qwen3-8B-shaped prefill (Hq=32, Hkv=8, D=128), a paged decode batch of the same
+geometry, a 24/2/D256 multi-query decode, a long chunked prefill, and a dense
+causal prefill of the 24/2/D256 geometry.
 """
 import math
 from concurrent.futures import ThreadPoolExecutor
@@ -44,6 +45,8 @@ WORKLOADS = {
                               causal=True, sigma=1.0, lengths=(512, 32768), spare=0.10),
     "long_chunked_prefill": dict(kind="dense", B=4, Hq=64, Hkv=8, Sq=2048, Skv=32768, D=128,
                                  causal=True, sigma=0.5, mask_lengths=None),
+    "wide_group_prefill": dict(kind="dense", B=2, Hq=24, Hkv=2, Sq=8192, Skv=8192, D=256,
+                               causal=True, sigma=1.0, mask_lengths=None),
 }
 
 

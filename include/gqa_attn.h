@@ -109,7 +109,8 @@ typedef struct {
  *
  * B, Hq, Hkv, D > 0; Sq >= 0, Skv >= 0.  Sq > Skv with causal is accepted:
  * rows i < Sq - Skv see no key and get zeros.  Skv == 0 gives all-zero O.
- * D == 256 is not yet served here (GQA_ERR_UNSUPPORTED).
+ * D = 64 and 128 run two 128-row query tiles per CTA; D = 256 (the 24/2/D256
+ * geometry of MATE "QSA") one tile per CTA with double-buffered scores.
  */
 gqa_status attn_fwd_dense(const void* q, const void* k, const void* v,
                           const uint8_t* key_padding_mask, void* o, float* lse,

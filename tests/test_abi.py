@@ -59,7 +59,7 @@ def test_dense_argument_checks(lib):
     assert dense(lib, Sq=-1) == INVALID
     assert dense(lib, Skv=-3) == INVALID
     assert dense(lib, D=96) == UNSUPPORTED
-    assert dense(lib, D=256) == UNSUPPORTED                      # dense D=256 not served yet
+    assert dense(lib, D=512) == UNSUPPORTED
     assert dense(lib, scale=float("nan")) == INVALID
     assert dense(lib, scale=float("inf")) == INVALID
     assert dense(lib, q=MIS) == MISALIGNED
