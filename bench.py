@@ -15,7 +15,8 @@ beside it.  Between timed steps a buffer twice the L2 size is overwritten so
 every step starts with a cold L2.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload step|qwen3_8b_prefill|paged_decode|wide_group_decode|long_chunked_prefill]
+                       [--workload step|qwen3_8b_prefill|paged_decode|wide_group_decode|long_chunked_prefill|
+                                   wide_group_prefill]
 Prints exactly one JSON line (rank 0).
 """
 import argparse
@@ -83,6 +84,7 @@ TRAFFIC = {
     "paged_decode": ("ratio", (559.396864 + 5.465344) / 556.916736),
     "wide_group_decode": ("ratio", (233.606656 + 4.270080) / 232.683520),
     "qwen3_8b_prefill": ("bytes", (93.515776 + 30.323200) * 1e6),
+    "wide_group_prefill": ("bytes", (235.172608 + 160.694528) * 1e6),
 }
 
 
@@ -326,7 +328,8 @@ def bench_ours(args, world, rank, local):
             dom, dom_t = p, t
     if dom.kind == "dense":
         ach = dom.flops / dom_t / 1e12
-        roof = dict(kernel="prefill_kernel<128> (" + dom.name + ")", bound="tensor", achieved=ach,
+        kname = "prefill_d256_kernel" if dom.data["config"]["D"] == 256 else "prefill_kernel<%d>" % dom.data["config"]["D"]
+        roof = dict(kernel=kname + " (" + dom.name + ")", bound="tensor", achieved=ach,
                     peak=peaks["bf16_tflops"], unit="TFLOP/s", frac=ach / peaks["bf16_tflops"],
                     traffic=traffic_per_launch(dom), peak_source=peaks["source"] + " bf16 burst")
     else:
