@@ -42,6 +42,11 @@ def _bind(lib):
     lib.oracle_attn_paged_ex.argtypes = ([vp] * 3 + [ip] + [vp] * 2 + [ip] + [vp] * 3 + [ip] * 8
                                          + [dp, lp, lp, dp, vp, ip])
     lib.oracle_attn_paged_ex.restype = ip
+    lib.oracle_attn_varlen_ex.argtypes = ([vp] * 3 + [ip] + [vp] * 4 + [ip] * 7 + [dp, lp, lp, dp, vp, ip])
+    lib.oracle_attn_varlen_ex.restype = ip
+    lib.oracle_attn_paged_varlen_ex.argtypes = ([vp] * 3 + [ip] + [vp] * 3 + [ip] + [vp] * 2 + [ip] * 8
+                                                + [dp, lp, lp, dp, vp, ip])
+    lib.oracle_attn_paged_varlen_ex.restype = ip
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ip
     return lib
@@ -92,6 +97,7 @@ _ERRORS = {
     -6: "a block_table entry for a used page lies outside [0, num_pages)",
     -7: "a window size below -1",
     -8: "softcap must be finite and >= 0",
+    -9: "cu_seqlens must run from 0 up to the packed total without decreasing",
 }
 
 
@@ -235,5 +241,64 @@ def attn_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=True, sc
                                       _ptr(req), _ptr(o), _ptr(lse), B, Sq, Hq, Hkv, D, num_pages,
                                       max_pages, int(bool(causal)), float(scale), wl, wr, cap,
                                       _ptr(sk), int(nthreads))
+    _check(rc)
+    return torch.from_numpy(o), torch.from_numpy(lse)
+
+
+def _i32(x):
+    return np.ascontiguousarray(torch.as_tensor(x).cpu().numpy(), dtype=np.int32)
+
+
+def attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, causal=True, scale=None, nthreads=0,
+                window_left=-1, window_right=-1, softcap=0.0, sinks=None):
+    """Packed variable-length GQA attention in double (TileOPs GQAVarlenFwdOp).
+
+    q: [total_q, Hq, D]; k, v: [total_kv, Hkv, D]; cu_seqlens_q / cu_seqlens_kv:
+    [B + 1] request offsets.  Every request is dense attention over its own rows
+    with its own end-aligned causal mask.  Returns o [total_q, Hq, D] and
+    lse [total_q, Hq]."""
+    total_q, Hq, D = q.shape
+    total_kv, Hkv, _ = k.shape
+    if scale is None:
+        scale = default_scale(D)
+    (qa, c), (ka, _), (va, _) = _same_kind([_tensor_in(q), _tensor_in(k), _tensor_in(v)])
+    cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_kv)
+    if cq.shape != ck.shape or cq.ndim != 1 or cq.shape[0] < 1:
+        raise ValueError("oracle: cu_seqlens_q and cu_seqlens_kv must both hold B + 1 offsets")
+    B = cq.shape[0] - 1
+    o = np.zeros((total_q, Hq, D), dtype=np.float64)
+    lse = np.zeros((total_q, Hq), dtype=np.float64)
+    wl, wr, cap, sk = _opts(window_left, window_right, softcap, sinks, Hq)
+    rc = _load().oracle_attn_varlen_ex(_ptr(qa), _ptr(ka), _ptr(va), c, _ptr(cq), _ptr(ck), _ptr(o), _ptr(lse),
+                                       B, total_q, total_kv, Hq, Hkv, D, int(bool(causal)), float(scale),
+                                       wl, wr, cap, _ptr(sk), int(nthreads))
+    _check(rc)
+    return torch.from_numpy(o), torch.from_numpy(lse)
+
+
+def attn_paged_varlen(q, k_cache, v_cache, cu_seqlens_q, cache_seqlens, block_table, causal=True, scale=None,
+                      nthreads=0, window_left=-1, window_right=-1, softcap=0.0, sinks=None):
+    """Paged GQA attention over packed queries in double (TileOPs GQAPagedFwdOp).
+
+    q: [total_q, Hq, D]; k_cache, v_cache: [num_pages, page_size, Hkv, D];
+    cu_seqlens_q: [B + 1]; cache_seqlens: [B] (each request's query tokens
+    included); block_table: [B, max_pages].  Returns o [total_q, Hq, D] and
+    lse [total_q, Hq]."""
+    total_q, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    if scale is None:
+        scale = default_scale(D)
+    (qa, c), (ka, _), (va, _) = _same_kind([_tensor_in(q), _tensor_in(k_cache), _tensor_in(v_cache)])
+    cq, sl, bt = _i32(cu_seqlens_q), _i32(cache_seqlens), _i32(block_table)
+    B = sl.shape[0]
+    if cq.shape != (B + 1,) or bt.ndim != 2 or bt.shape[0] != B:
+        raise ValueError("oracle: cu_seqlens_q [B + 1], cache_seqlens [B] and block_table [B, pages] disagree")
+    o = np.zeros((total_q, Hq, D), dtype=np.float64)
+    lse = np.zeros((total_q, Hq), dtype=np.float64)
+    wl, wr, cap, sk = _opts(window_left, window_right, softcap, sinks, Hq)
+    rc = _load().oracle_attn_paged_varlen_ex(_ptr(qa), _ptr(ka), _ptr(va), c, _ptr(cq), _ptr(sl), _ptr(bt),
+                                             page_size, _ptr(o), _ptr(lse), B, total_q, Hq, Hkv, D, num_pages,
+                                             bt.shape[1], int(bool(causal)), float(scale), wl, wr, cap, _ptr(sk),
+                                             int(nthreads))
     _check(rc)
     return torch.from_numpy(o), torch.from_numpy(lse)

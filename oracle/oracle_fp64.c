@@ -396,3 +396,92 @@ int oracle_attn_paged_ex(const void* q, const void* k_cache, const void* v_cache
                      o, lse, B, Sq, Hq, Hkv, D, num_pages, max_pages, causal, scale, &opt,
                      nthreads);
 }
+
+/*
+ * Offsets of packed requests: non-decreasing from 0 up to total, B + 1 of them
+ * (TileOPs "Attention Operators", GQAVarlenFwdOp: cu_seqlens delimit each
+ * request).
+ */
+static int check_offsets(const int32_t* cu, int B, long total) {
+    if (cu[0] != 0 || (long)cu[B] != total) return -9;
+    for (int b = 0; b < B; ++b)
+        if (cu[b + 1] < cu[b]) return -9;
+    return 0;
+}
+
+/*
+ * Packed variable-length attention (TileOPs "Attention Operators",
+ * GQAVarlenFwdOp): request b owns the packed query rows
+ * [cu_q[b], cu_q[b + 1]) and the key / value rows [cu_kv[b], cu_kv[b + 1]);
+ * every request is the dense definition on its own rows, with its own
+ * bottom-right-aligned causal mask (Sq_b queries, Skv_b keys).
+ *   q : [total_q, Hq, D]      k, v : [total_kv, Hkv, D]
+ *   o : [total_q, Hq, D]      lse  : [total_q, Hq]
+ * Returns 0; -1 bad size; -2 Hq % Hkv != 0; -3 out of memory; -7 / -8 bad
+ * options; -9 offsets that do not run from 0 up to the total without
+ * decreasing.
+ */
+int oracle_attn_varlen_ex(const void* q, const void* k, const void* v, int dtype,
+                          const int32_t* cu_q, const int32_t* cu_kv, double* o,
+                          double* lse, int B, int total_q, int total_kv, int Hq,
+                          int Hkv, int D, int causal, double scale, long window_left,
+                          long window_right, double softcap, const double* sinks,
+                          int nthreads) {
+    int rc = check_opts(window_left, window_right, softcap);
+    if (rc) return rc;
+    rc = check_dense_args(B, Hq, Hkv, total_q, total_kv, D);
+    if (rc) return rc;
+    if (check_offsets(cu_q, B, total_q) || check_offsets(cu_kv, B, total_kv)) return -9;
+    const oracle_opts opt = {window_left, window_right, softcap, sinks};
+    const size_t es = dtype == ORACLE_F64 ? sizeof(double) : sizeof(uint16_t);
+    for (int b = 0; b < B; ++b) {
+        const int qs = cu_q[b], sq = cu_q[b + 1] - qs;
+        const int ks = cu_kv[b], skv = cu_kv[b + 1] - ks;
+        /* rows [qs, qs + sq) of a [total, H, D] tensor are a [1, sq, H, D] one */
+        rc = dense_all((const char*)q + (size_t)qs * Hq * D * es,
+                       (const char*)k + (size_t)ks * Hkv * D * es,
+                       (const char*)v + (size_t)ks * Hkv * D * es, dtype, NULL,
+                       o + (size_t)qs * Hq * D, lse + (size_t)qs * Hq, 1, Hq, Hkv, sq,
+                       skv, D, causal, scale, &opt, nthreads);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
+/*
+ * Paged attention over packed queries (TileOPs "Attention Operators",
+ * GQAPagedFwdOp): request b's queries are the packed rows
+ * [cu_q[b], cu_q[b + 1]); its cache holds cache_seqlens[b] tokens, its query
+ * tokens included, through block_table[b].  Every request is the paged
+ * definition above on its own query rows; a request without query rows
+ * produces nothing.
+ *   q : [total_q, Hq, D]      k_cache, v_cache : [num_pages, page_size, Hkv, D]
+ *   o : [total_q, Hq, D]      lse : [total_q, Hq]
+ * Returns the codes of paged_all, -7 / -8 for bad options and -9 for bad
+ * query offsets.
+ */
+int oracle_attn_paged_varlen_ex(const void* q, const void* k_cache, const void* v_cache,
+                                int dtype, const int32_t* cu_q, const int32_t* cache_seqlens,
+                                const int32_t* block_table, int page_size, double* o,
+                                double* lse, int B, int total_q, int Hq, int Hkv, int D,
+                                int num_pages, int max_pages, int causal, double scale,
+                                long window_left, long window_right, double softcap,
+                                const double* sinks, int nthreads) {
+    int rc = check_opts(window_left, window_right, softcap);
+    if (rc) return rc;
+    rc = check_dense_args(B, Hq, Hkv, total_q, 0, D);
+    if (rc) return rc;
+    if (check_offsets(cu_q, B, total_q)) return -9;
+    const oracle_opts opt = {window_left, window_right, softcap, sinks};
+    const size_t es = dtype == ORACLE_F64 ? sizeof(double) : sizeof(uint16_t);
+    for (int b = 0; b < B; ++b) {
+        const int qs = cu_q[b], sq = cu_q[b + 1] - qs;
+        if (sq == 0) continue;
+        rc = paged_all((const char*)q + (size_t)qs * Hq * D * es, k_cache, v_cache, dtype,
+                       cache_seqlens + b, block_table + (size_t)b * max_pages, page_size, NULL,
+                       o + (size_t)qs * Hq * D, lse + (size_t)qs * Hq, 1, sq, Hq, Hkv, D,
+                       num_pages, max_pages, causal, scale, &opt, nthreads);
+        if (rc) return rc;
+    }
+    return 0;
+}

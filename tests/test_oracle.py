@@ -11,7 +11,10 @@ same way: a zero left window leaves one key (exact value), a window equals the
 plain definition over the sliced keys, softcap has closed forms for two keys
 (tanh 40 = 1; 2 tanh(ln(3)/2) = 1) and vanishes for a huge cap, sinks obey the
 denominator identity O_s = O / (1 + exp(s - LSE)), and paged equals dense with
-all three.  The last test plants mistakes in copies of the oracle and checks
+all three.  Packed variable-length calls are checked request by request
+against torch's attention, against the BSHD batch for equal lengths, and the
+packed-query paged call against the packed call on gathered keys and against
+the [B, Sq] paged call.  The last test plants mistakes in copies of the oracle and checks
 that the pins catch every one.
 """
 import math
@@ -455,13 +458,93 @@ def pin_half_inputs_widen_exactly():
         assert torch.equal(oh, od) and torch.equal(lh, ld)
 
 
+def _pack(lengths, H, D, seed, stream):
+    """A packed [sum(lengths), H, D] bf16 tensor and its [B + 1] offsets."""
+    total = int(sum(lengths))
+    x = W.randn_bf16((max(total, 1), H, D), seed=seed, stream=stream)[:total]
+    cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int32)
+    return x, cu
+
+
+def pin_varlen_matches_sdpa_per_request():
+    # TileOPs GQAVarlenFwdOp: each request is attention over its own rows with
+    # its own end-aligned causal mask; checked request by request against
+    # torch's library attention (a request without queries, one with Sq > Skv)
+    sq, skv = [3, 0, 5, 3, 1], [4, 2, 5, 1, 9]
+    Hq, Hkv, D, scale = 4, 2, 8, 0.4
+    q, cq = _pack(sq, Hq, D, seed=61, stream=0)
+    k, ck = _pack(skv, Hkv, D, seed=61, stream=1)
+    v, _ = _pack(skv, Hkv, D, seed=61, stream=2)
+    o, lse = oracle.attn_varlen(q, k, v, cq, ck, causal=True, scale=scale)
+    for b in range(len(sq)):
+        qs, ks = int(cq[b]), int(ck[b])
+        if sq[b] == 0:
+            continue
+        vis = _visible(1, sq[b], skv[b], True, None)[0].any(-1)          # rows with a visible key
+        ref = _sdpa_fp64(q[None, qs:qs + sq[b]], k[None, ks:ks + skv[b]], v[None, ks:ks + skv[b]], None, True,
+                         scale)[0]
+        ob, lb = o[qs:qs + sq[b]], lse[qs:qs + sq[b]]
+        assert torch.allclose(ob[vis], ref[vis], rtol=1e-12, atol=1e-12)
+        assert torch.equal(ob[~vis], torch.zeros_like(ob[~vis])) and bool(torch.all(lb[~vis] == float("-inf")))
+        assert bool(torch.all(torch.isfinite(lb[vis])))
+
+
+def pin_varlen_equals_dense_batch():
+    # equal lengths: the packed call is the BSHD batch, options included
+    B, S, Skv, Hq, Hkv, D = 3, 6, 9, 6, 2, 8
+    q, k, v, _ = _rand_case(B, Hq, Hkv, S, Skv, D, seed=62)
+    cq = torch.arange(0, (B + 1) * S, S, dtype=torch.int32)
+    ck = torch.arange(0, (B + 1) * Skv, Skv, dtype=torch.int32)
+    sinks = torch.tensor([0.5, -1.0, float("-inf"), 2.0, 0.0, 1.0], dtype=torch.float64)
+    for kw in ({}, dict(window_left=3, window_right=1, softcap=2.5, sinks=sinks)):
+        o, lse = oracle.attn_varlen(q.reshape(B * S, Hq, D), k.reshape(B * Skv, Hkv, D), v.reshape(B * Skv, Hkv, D),
+                                    cq, ck, causal=True, **kw)
+        od, ld = oracle.attn_dense(q, k, v, causal=True, **kw)
+        assert torch.equal(o, od.reshape(B * S, Hq, D)) and torch.equal(lse, ld.reshape(B * S, Hq))
+
+
+def pin_paged_varlen_equals_gathered_varlen():
+    # TileOPs GQAPagedFwdOp: packed queries over a paged cache whose lengths
+    # include the query tokens equal the packed call on the gathered keys
+    sq, L = [1, 0, 7, 1, 4], [13, 5, 7, 30, 11]
+    Hq, Hkv, D, ps = 6, 2, 8, 4
+    q, cq = _pack(sq, Hq, D, seed=63, stream=0)
+    k, ck = _pack(L, Hkv, D, seed=63, stream=1)
+    v, _ = _pack(L, Hkv, D, seed=63, stream=2)
+    kd = torch.zeros(len(L), max(L), Hkv, D, dtype=k.dtype)
+    vd = torch.zeros_like(kd)
+    for b in range(len(L)):
+        kd[b, :L[b]] = k[int(ck[b]):int(ck[b + 1])]
+        vd[b, :L[b]] = v[int(ck[b]):int(ck[b + 1])]
+    kc, vc, table = _scatter_to_pages(kd, vd, L, ps, seed=64)
+    sl = torch.tensor(L, dtype=torch.int32)
+    o, lse = oracle.attn_paged_varlen(q, kc, vc, cq, sl, table, causal=True)
+    od, ld = oracle.attn_varlen(q, k, v, cq, ck, causal=True)
+    assert torch.equal(o, od) and torch.equal(lse, ld)
+
+
+def pin_paged_varlen_uniform_equals_paged():
+    # every request with the same query count: the packed call is the [B, Sq] one
+    B, Sq, Hq, Hkv, D, ps = 4, 2, 4, 1, 8, 3
+    L = [2, 9, 17, 5]
+    q, k, v, _ = _rand_case(B, Hq, Hkv, Sq, max(L), D, seed=65)
+    kc, vc, table = _scatter_to_pages(k, v, L, ps, seed=66)
+    sl = torch.tensor(L, dtype=torch.int32)
+    cq = torch.arange(0, (B + 1) * Sq, Sq, dtype=torch.int32)
+    o, lse = oracle.attn_paged_varlen(q.reshape(B * Sq, Hq, D), kc, vc, cq, sl, table, causal=True, softcap=3.0)
+    op, lp = oracle.attn_paged(q, kc, vc, sl, table, causal=True, softcap=3.0)
+    assert torch.equal(o, op.reshape(B * Sq, Hq, D)) and torch.equal(lse, lp.reshape(B * Sq, Hq))
+
+
 PINS = [pin_golden_closed_form, pin_matches_torch_sdpa, pin_lse_matches_torch_logsumexp,
         pin_single_visible_key_exact, pin_zero_query_is_mean_of_visible_values,
         pin_gqa_equals_repeat_interleave_mha, pin_paged_equals_dense,
         pin_rows_without_visible_keys, pin_invariants, pin_chunked_prefill_and_row_independence,
         pin_noncausal_key_permutation, pin_high_precision_rows, pin_window_single_key_exact,
         pin_window_equals_key_slice, pin_softcap_closed_forms, pin_softcap_large_cap_limit,
-        pin_sinks_identity, pin_options_paged_equals_dense, pin_half_inputs_widen_exactly]
+        pin_sinks_identity, pin_options_paged_equals_dense, pin_half_inputs_widen_exactly,
+        pin_varlen_matches_sdpa_per_request, pin_varlen_equals_dense_batch,
+        pin_paged_varlen_equals_gathered_varlen, pin_paged_varlen_uniform_equals_paged]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -521,6 +604,12 @@ MUTANTS = {
                            "block_table[(size_t)b * max_pages + t % page_size]"),
     "weights_unnormalised": ("exp(z[j] - M) / Z;", "exp(z[j] - M);"),
     "query_row_transposed": ("(((size_t)b * Sq + i) * Hq + h)", "(((size_t)b * Hq + h) * Sq + i)"),
+    "varlen_key_offset_ignored": ("(const char*)k + (size_t)ks * Hkv * D * es,", "(const char*)k,"),
+    "varlen_output_offset_ignored": ("o + (size_t)qs * Hq * D, lse + (size_t)qs * Hq, 1, Hq, Hkv, sq,",
+                                     "o, lse, 1, Hq, Hkv, sq,"),
+    "paged_varlen_table_row_ignored": ("block_table + (size_t)b * max_pages, page_size, NULL,",
+                                       "block_table, page_size, NULL,"),
+    "paged_varlen_first_length": ("cache_seqlens + b,", "cache_seqlens,"),
 }
 
 
