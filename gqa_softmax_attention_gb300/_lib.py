@@ -51,6 +51,12 @@ def load() -> ctypes.CDLL:
     lib.attn_decode_paged_noalloc.restype = i
     lib.attn_decode_paged_noalloc_max_workspace.argtypes = []
     lib.attn_decode_paged_noalloc_max_workspace.restype = sz
+    lib.attn_fwd_varlen.argtypes = [vp] * 7 + [i] * 7 + [f, vp, vp, sz, vp]
+    lib.attn_fwd_varlen.restype = i
+    lib.attn_fwd_paged.argtypes = [vp] * 6 + [i, vp, vp] + [i] * 8 + [f, vp, vp, sz, vp]
+    lib.attn_fwd_paged.restype = i
+    lib.attn_varlen_workspace_size.argtypes = [i] * 4
+    lib.attn_varlen_workspace_size.restype = sz
     lib.attn_validate_paged.argtypes = [vp, vp] + [i] * 6 + [vp]
     lib.attn_validate_paged.restype = i
     lib.gqa_status_string.argtypes = [i]

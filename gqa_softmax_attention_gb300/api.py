@@ -207,6 +207,109 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, real_seqlen_kv, block_table, 
     return out, lse
 
 
+def attn_varlen_workspace_size(B, total_q, Hq, Hkv):
+    """Workspace bytes of attn_fwd_varlen / attn_fwd_paged."""
+    return int(_lib.load().attn_varlen_workspace_size(B, total_q, Hq, Hkv))
+
+
+def _check_offsets(name, t, n):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32 or tuple(t.shape) != (n,):
+        raise ValueError("%s must be an int32 CUDA tensor of shape [%d]" % (name, n))
+    return t.contiguous()
+
+
+def _varlen_outputs(q, out, lse, workspace, B):
+    total_q, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    return out, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, causal=True, scale=None, out=None, lse=None,
+                    window_left=-1, window_right=-1, softcap=None, sinks=None, workspace=None):
+    """Packed variable-length GQA attention (TileOPs GQAVarlenFwdOp).
+
+    q [total_q, Hq, D], k / v [total_kv, Hkv, D] CUDA tensors (THD), all
+    bfloat16 or all float16; cu_seqlens_q / cu_seqlens_kv [B + 1] int32 CUDA
+    offsets (request b owns rows cu[b]:cu[b+1]; they stay on the device).
+    Options as in attn_fwd_dense.  Returns (o [total_q, Hq, D], lse [total_q, Hq]).
+    """
+    _check_16_cuda("q", q, 3)
+    for n, t in (("k", k), ("v", v)):
+        _check_16_cuda(n, t, 3, (q.dtype,))
+    total_q, Hq, D = q.shape
+    total_kv, Hkv, Dk = k.shape
+    if Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch: q %s, k %s, v %s" % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    if Hq % Hkv != 0:
+        raise ValueError("Hq (%d) must be divisible by Hkv (%d)" % (Hq, Hkv))
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape[0] < 2:
+        raise ValueError("cu_seqlens_q must hold B + 1 >= 2 offsets")
+    B = cu_seqlens_q.shape[0] - 1
+    cq = _check_offsets("cu_seqlens_q", cu_seqlens_q, B + 1)
+    ck = _check_offsets("cu_seqlens_kv", cu_seqlens_kv, B + 1)
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    out, lse = _varlen_outputs(q, out, lse, workspace, B)
+    need = attn_varlen_workspace_size(B, total_q, Hq, Hkv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device, _DTYPES[q.dtype])
+    st = _lib.load().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck), _ptr(out), _ptr(lse), B, total_q,
+                                     total_kv, Hq, Hkv, D, int(bool(causal)), resolve_scale(scale, D),
+                                     ctypes.byref(opt) if opt is not None else None, _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(q.device))
+    if st != 0:
+        _raise(st, "attn_fwd_varlen")
+    return out, lse
+
+
+def attn_fwd_paged(q, k_cache, v_cache, cu_seqlens_q, cache_seqlens, block_table, causal=True, scale=None,
+                   out=None, lse=None, window_left=-1, window_right=-1, softcap=None, sinks=None, workspace=None):
+    """Packed queries over a paged cache: prefill chunks and decode steps in one
+    launch (TileOPs GQAPagedFwdOp).
+
+    q [total_q, Hq, D]; k_cache / v_cache [num_pages, page_size, Hkv, D], all
+    bfloat16 or all float16; cu_seqlens_q [B + 1], cache_seqlens [B] (query
+    tokens included) and block_table [B, max_pages] int32 CUDA tensors.
+    page_size must be a multiple of 8.  Options as in attn_fwd_dense.
+    Returns (o [total_q, Hq, D], lse [total_q, Hq]).
+    """
+    _check_16_cuda("q", q, 3)
+    _check_16_cuda("k_cache", k_cache, 4, (q.dtype,))
+    _check_16_cuda("v_cache", v_cache, 4, (q.dtype,))
+    total_q, Hq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shape mismatch: k %s, v %s, D %d" % (tuple(k_cache.shape), tuple(v_cache.shape), D))
+    if Hq % Hkv != 0:
+        raise ValueError("Hq (%d) must be divisible by Hkv (%d)" % (Hq, Hkv))
+    if cache_seqlens.dim() != 1:
+        raise ValueError("cache_seqlens must be [B]")
+    B = cache_seqlens.shape[0]
+    cq = _check_offsets("cu_seqlens_q", cu_seqlens_q, B + 1)
+    sl = _check_offsets("cache_seqlens", cache_seqlens, B)
+    if not block_table.is_cuda or block_table.dtype != torch.int32 or block_table.dim() != 2 \
+            or block_table.shape[0] != B:
+        raise ValueError("block_table must be an int32 CUDA tensor [B, max_pages]")
+    bt = block_table.contiguous()
+    q, k_cache, v_cache = q.contiguous(), k_cache.contiguous(), v_cache.contiguous()
+    out, lse = _varlen_outputs(q, out, lse, workspace, B)
+    need = attn_varlen_workspace_size(B, total_q, Hq, Hkv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device, _DTYPES[q.dtype])
+    st = _lib.load().attn_fwd_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cq), _ptr(sl), _ptr(bt), page_size,
+                                    _ptr(out), _ptr(lse), B, total_q, Hq, Hkv, D, num_pages, bt.shape[1],
+                                    int(bool(causal)), resolve_scale(scale, D),
+                                    ctypes.byref(opt) if opt is not None else None, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(q.device))
+    if st != 0:
+        _raise(st, "attn_fwd_paged")
+    return out, lse
+
+
 def attn_validate_paged(real_seqlen_kv, block_table, Sq, page_size, num_pages, causal=True):
     """Host-side range check of paged metadata (synchronises the stream)."""
     B, max_pages = block_table.shape
@@ -227,3 +330,5 @@ def gqa_device_error():
 # Short aliases in the style of the pages' op APIs.
 attention = attn_fwd_dense
 decode_paged = attn_decode_paged
+varlen = attn_fwd_varlen
+paged = attn_fwd_paged

@@ -14,8 +14,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libgqa_attn.so")
-SOURCES = ["api.cu", "prefill.cu", "prefill_d256.cu", "decode.cu", "decode_tc.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "prefill_tiles.cuh"]
+SOURCES = ["api.cu", "prefill.cu", "prefill_d256.cu", "varlen_packed.cu", "varlen_paged.cu", "decode.cu",
+           "decode_tc.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "prefill_tiles.cuh", "onetile.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

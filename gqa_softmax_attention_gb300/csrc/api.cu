@@ -74,18 +74,44 @@ bool make_cache_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D
 // consecutive boxes of a tile keep one uniform 8-row-group stride (D / 64 KB)
 // for every slice, which lets one MMA descriptor span the tile's 64 keys.
 bool make_cache_page_map(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D, int box_tokens,
-                         bool f16) {
+                         bool f16, int box_slices = 0) {
     auto fn = encode_fn();
     if (!fn || rows % 8 != 0 || box_tokens % 8 != 0) return false;
     const cuuint64_t row_bytes = (cuuint64_t)Hkv * D * 2;
     const cuuint64_t dims[5] = {64, 8, (cuuint64_t)(D / 64), (cuuint64_t)(rows / 8), (cuuint64_t)Hkv};
     const cuuint64_t strides[4] = {row_bytes, 128, 8 * row_bytes, (cuuint64_t)D * 2};
-    const cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), (cuuint32_t)(box_tokens / 8), 1};
+    const cuuint32_t box[5] = {64, 8, (cuuint32_t)(box_slices > 0 ? box_slices : D / 64), (cuuint32_t)(box_tokens / 8),
+                               1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     const CUresult r = fn(map, elem_type(f16), 5, const_cast<void*>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Packed [total, H, D] rows (THD) as a 3-D map {D, H, total} with a
+// {64, box_h, box_t} box and 128-byte swizzle: box_h heads of box_t
+// consecutive tokens land as box_t * box_h rows of 128 bytes.
+bool make_thd_map(CUtensorMap* map, const void* ptr, long total, int H, int D, int box_h, int box_t, bool f16) {
+    auto fn = encode_fn();
+    if (!fn || total <= 0) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_h, (cuuint32_t)box_t};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, elem_type(f16), 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int gcd_int(int a, int b) {
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
 }
 
 int sm_count() {
@@ -164,7 +190,7 @@ gqa_status attn_fwd_dense_ex(const void* q, const void* k, const void* v, const 
     if (!make_bshd_map(&tq, q, B, Sq, Hq, D, f16) || !make_bshd_map(&tk, k, B, Skv, Hkv, D, f16) ||
         !make_bshd_map(&tv, v, B, Skv, Hkv, D, f16, D == 256 ? 64 : 128) || !make_bshd_map(&to, o, B, Sq, Hq, D, f16))
         return GQA_ERR_CUDA;
-    PrefillArgs a;
+    PrefillArgs a{};
     a.mask = key_padding_mask;
     a.o = o;
     a.lse = lse;
@@ -265,6 +291,128 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
                : GQA_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- packed calls
+// Workspace of a packed call: a 16-byte header holding the entry count, then
+// up to max_entries row-block entries of 32 bytes.
+static int varlen_max_entries(int B, int total_q, int qpb) { return total_q / qpb + B + 1; }
+
+static size_t varlen_ws_bytes(int B, int total_q, int Hq, int Hkv) {
+    if (B <= 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > 128) return 0;
+    const int qpb = 128 / (Hq / Hkv);
+    return 16 + (size_t)varlen_max_entries(B, total_q, qpb) * 32;
+}
+
+size_t attn_varlen_workspace_size(int B, int total_q, int Hq, int Hkv) {
+    return varlen_ws_bytes(B, total_q, Hq, Hkv);
+}
+
+// Shared checks and set-up of the two packed entry points.
+static gqa_status varlen_common(const void* q, void* o, float* lse, const int32_t* cu_q, int B, int total_q,
+                                int Hq, int Hkv, int D, int causal, float scale, const gqa_options* opts,
+                                void* workspace, size_t workspace_bytes, PrefillArgs* a, CUtensorMap* tq,
+                                CUtensorMap* to) {
+    if (B <= 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return GQA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || total_q >= kMaxSeq) return GQA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+    if (!head_dim_ok(D) || Hq / Hkv > 128) return GQA_ERR_UNSUPPORTED;
+    if (!q || !o || !cu_q) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o)) return GQA_ERR_MISALIGNED;
+    if (!aligned4(cu_q) || (lse && !aligned4(lse))) return GQA_ERR_MISALIGNED;
+    gqa::Extras ex;
+    const gqa_status es = make_extras(opts, scale, &ex);
+    if (es != GQA_OK) return es;
+    const size_t need = varlen_ws_bytes(B, total_q, Hq, Hkv);
+    if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return GQA_ERR_MISALIGNED;
+    const bool f16 = opts && opts->dtype == GQA_FP16;
+    const int g = Hq / Hkv, qpb = 128 / g;
+    if (total_q > 0 && (!make_thd_map(tq, q, total_q, Hq, D, g, qpb, f16) ||
+                        !make_thd_map(to, o, total_q, Hq, D, g, qpb, f16)))
+        return GQA_ERR_CUDA;
+    a->mask = nullptr;
+    a->o = o;
+    a->lse = lse;
+    a->B = B; a->Hq = Hq; a->Hkv = Hkv; a->Sq = 0; a->Skv = 0; a->D = D;
+    a->causal = causal ? 1 : 0;
+    a->scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    a->num_sms = sm_count();
+    a->f16 = f16 ? 1 : 0;
+    a->x = ex;
+    a->n_entries = static_cast<const int32_t*>(workspace);
+    a->entries = reinterpret_cast<const int32_t*>(static_cast<char*>(workspace) + 16);
+    a->g = g;
+    a->qpb = qpb;
+    a->table = nullptr;
+    a->page_size = a->max_pages = a->bt_k = a->bt_v = 0;
+    return GQA_OK;
+}
+
+gqa_status attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                           const int32_t* cu_seqlens_kv, void* o, float* lse, int B, int total_q, int total_kv,
+                           int Hq, int Hkv, int D, int causal, float scale, const gqa_options* opts,
+                           void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
+    PrefillArgs a{};
+    CUtensorMap tq, tk, tv, to;
+    if (total_kv < 0 || total_kv >= kMaxSeq) return GQA_ERR_INVALID_ARG;
+    gqa_status st = varlen_common(q, o, lse, cu_seqlens_q, B, total_q, Hq, Hkv, D, causal, scale, opts, workspace,
+                                  workspace_bytes, &a, &tq, &to);
+    if (st != GQA_OK) return st;
+    if (!cu_seqlens_kv || (total_kv > 0 && (!k || !v))) return GQA_ERR_INVALID_ARG;
+    if (!aligned4(cu_seqlens_kv) || (total_kv > 0 && (!aligned16(k) || !aligned16(v)))) return GQA_ERR_MISALIGNED;
+    if (total_q == 0) return GQA_OK;
+    // with no key at all the maps are never read; they then describe q
+    const void* kb = total_kv > 0 ? k : q;
+    const void* vb = total_kv > 0 ? v : q;
+    const long kv_rows = total_kv > 0 ? total_kv : 1;
+    if (!make_thd_map(&tk, kb, kv_rows, Hkv, D, 1, 128, a.f16) ||
+        !make_thd_map(&tv, vb, kv_rows, Hkv, D, 1, D == 256 ? 64 : 128, a.f16))
+        return GQA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int max_e = varlen_max_entries(B, total_q, a.qpb);
+    int32_t* ws = static_cast<int32_t*>(workspace);
+    if (gqa::launch_varlen_plan(cu_seqlens_q, cu_seqlens_kv, false, B, a.qpb, total_q, total_kv, ws + 4, ws, max_e,
+                                s) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    return gqa::launch_varlen_packed(tq, tk, tv, to, a, (long)max_e * Hkv, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+                          const int32_t* cache_seqlens, const int32_t* block_table, int page_size, void* o,
+                          float* lse, int B, int total_q, int Hq, int Hkv, int D, int num_pages, int max_pages,
+                          int causal, float scale, const gqa_options* opts, void* workspace,
+                          size_t workspace_bytes, gqa_stream_t stream) {
+    PrefillArgs a{};
+    CUtensorMap tq, tk, tv, to;
+    if (page_size <= 0 || num_pages <= 0 || max_pages <= 0) return GQA_ERR_INVALID_ARG;
+    if ((long)max_pages * page_size >= kMaxSeq) return GQA_ERR_INVALID_ARG;
+    if ((long)num_pages * page_size >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
+    if (page_size % 8 != 0) return GQA_ERR_UNSUPPORTED;      // pages move as 8-row TMA blocks
+    gqa_status st = varlen_common(q, o, lse, cu_seqlens_q, B, total_q, Hq, Hkv, D, causal, scale, opts, workspace,
+                                  workspace_bytes, &a, &tq, &to);
+    if (st != GQA_OK) return st;
+    if (!k_cache || !v_cache || !cache_seqlens || !block_table) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return GQA_ERR_MISALIGNED;
+    if (!aligned4(cache_seqlens) || !aligned4(block_table)) return GQA_ERR_MISALIGNED;
+    if (total_q == 0) return GQA_OK;
+    a.table = block_table;
+    a.page_size = page_size;
+    a.max_pages = max_pages;
+    const int vkeys = D == 256 ? 64 : 128;
+    a.bt_k = gcd_int(page_size, 128);
+    a.bt_v = gcd_int(page_size, vkeys);
+    const long rows = (long)num_pages * page_size;
+    if (!make_cache_page_map(&tk, k_cache, rows, Hkv, D, a.bt_k, a.f16, D == 256 ? 2 : D / 64) ||
+        !make_cache_page_map(&tv, v_cache, rows, Hkv, D, a.bt_v, a.f16))
+        return GQA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int max_e = varlen_max_entries(B, total_q, a.qpb);
+    int32_t* ws = static_cast<int32_t*>(workspace);
+    if (gqa::launch_varlen_plan(cu_seqlens_q, cache_seqlens, true, B, a.qpb, total_q, (long)max_pages * page_size,
+                                ws + 4, ws, max_e, s) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    return gqa::launch_varlen_paged(tq, tk, tv, to, a, (long)max_e * Hkv, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
 gqa_status attn_validate_paged(const int32_t* real_seqlen_kv, const int32_t* block_table, int B, int Sq,
                                int page_size, int num_pages, int max_pages, int causal, gqa_stream_t stream) {
     (void)causal;
@@ -306,10 +454,12 @@ gqa_status gqa_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
     const int e = gqa::prefill_take_device_error();
     const int e2 = gqa::prefill_d256_take_device_error();
+    const int v1 = gqa::varlen_packed_take_device_error();
+    const int v2 = gqa::varlen_paged_take_device_error();
     const int d = gqa::decode_take_device_error();
     const int t = gqa::decode_tc_take_device_error();
-    if (e < 0 || e2 < 0 || d < 0 || t < 0) return GQA_ERR_CUDA;
-    return (e || e2 || d || t) ? GQA_ERR_TIMEOUT : GQA_OK;
+    if (e < 0 || e2 < 0 || v1 < 0 || v2 < 0 || d < 0 || t < 0) return GQA_ERR_CUDA;
+    return (e || e2 || v1 || v2 || d || t) ? GQA_ERR_TIMEOUT : GQA_OK;
 }
 
 gqa_status gqa_exp2_poly(const float* x, float* y, long n, gqa_stream_t stream) {

@@ -26,6 +26,15 @@ struct PrefillArgs {
     int num_sms;          // persistent grid size
     int f16;              // inputs and output are float16 (else bfloat16)
     Extras x;
+    // Packed calls (onetile.cuh): q / o [total_q, Hq, D]; row blocks listed by
+    // the plan kernel.  Unused by the BSHD kernels.
+    const int32_t* entries;   // [max_entries, 8]: b, q0, qs, sq, ks, L, -, -
+    const int32_t* n_entries; // number of entries (device)
+    int g;                    // query heads per KV head
+    int qpb;                  // queries per row block: floor(128 / g)
+    const int32_t* table;     // paged: block_table [B, max_pages]
+    int page_size, max_pages;
+    int bt_k, bt_v;           // paged: tokens per TMA box of a K / V chunk
 };
 
 // Launches the tcgen05 prefill kernel.  The tensor maps describe q, k, v as
@@ -41,6 +50,26 @@ int prefill_take_device_error();
 cudaError_t launch_prefill_d256(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream);
 int prefill_d256_take_device_error();
+
+// Packed calls (varlen_packed.cu, varlen_paged.cu; onetile.cuh).  The plan
+// kernel lists the (request, row block) entries of a call into `entries`
+// ([max_entries, 8] int32) and their count into *n_entries; kv holds
+// cu_seqlens_kv [B + 1] (packed keys) or cache_seqlens [B] (paged), and kv_cap
+// bounds a request's key count (total_kv, or max_pages * page_size).
+cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int total_q,
+                               long kv_cap, int32_t* entries, int32_t* n_entries, int max_entries,
+                               cudaStream_t stream);
+// tm_q / tm_o: {D, Hq, total_q} with a {64, g, qpb} box.  Packed: tm_k / tm_v
+// {D, Hkv, total_kv} with {64, 1, 128} and {64, 1, 128 or 64 (D = 256)} boxes.
+// Paged: the caches as {64, 8, D / 64, pages * page_size / 8, Hkv} with
+// {64, 8, D / 64 / (D == 256 ? 2 : 1), bt_k / 8, 1} (K) and
+// {64, 8, D / 64, bt_v / 8, 1} (V) boxes.  max_items bounds entries * Hkv.
+cudaError_t launch_varlen_packed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                 const CUtensorMap& tm_o, const PrefillArgs& a, long max_items, cudaStream_t stream);
+cudaError_t launch_varlen_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                const CUtensorMap& tm_o, const PrefillArgs& a, long max_items, cudaStream_t stream);
+int varlen_packed_take_device_error();
+int varlen_paged_take_device_error();
 // y[i] = 2^x[i] by the prefill kernel's FMA-pipe exp2 (diagnostic).
 cudaError_t launch_exp2_poly(const float* x, float* y, long n, cudaStream_t stream);
 

@@ -36,10 +36,12 @@ __device__ __forceinline__ long key_lo(long p, int Skv, int wl) {
     return wl >= 0 ? min((long)Skv, max(0L, p - wl)) : 0L;
 }
 
-__device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causal, int wl, int wr) {
+// Bounds of a block of up to nq queries starting at query q0 (rows_valid
+// counts the queries of the block that exist).
+__device__ __forceinline__ TileInfo tile_info_n(int q0, int nq, int Sq, int Skv, int causal, int wl, int wr) {
     TileInfo t;
     t.q0 = q0;
-    t.rows_valid = max(0, min(BM, Sq - q0));
+    t.rows_valid = max(0, min(nq, Sq - q0));
     if (t.rows_valid == 0) {
         t.kv_begin = t.kv_end = t.lim_first = t.lo_last = 0;
     } else {
@@ -53,6 +55,10 @@ __device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causa
     }
     t.n_tiles = (t.kv_end + BN - 1) / BN;
     return t;
+}
+
+__device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causal, int wl, int wr) {
+    return tile_info_n(q0, BM, Sq, Skv, causal, wl, wr);
 }
 
 // Warp-collective.  Bit l of the result is set when key tile 32 * chunk + l

@@ -1,0 +1,97 @@
+// Packed variable-length calls (TileOPs "Attention Operators",
+// GQAVarlenFwdOp): q [total_q, Hq, D], k / v [total_kv, Hkv, D], request b
+// owning query rows [cu_seqlens_q[b], cu_seqlens_q[b + 1]) and key rows
+// [cu_seqlens_kv[b], cu_seqlens_kv[b + 1]).  Also the plan kernel shared with
+// the paged calls: it lists the (request, row block) entries on the device,
+// so the host never reads the offsets back.
+#include "onetile.cuh"
+
+namespace gqa {
+namespace {
+
+// One CTA of 1024 threads.  Request b gets ceil(Sq_b / qpb) entries, last
+// block first (its rows see the most keys); entries are laid out request by
+// request.  Offsets are clamped into [0, total] and lengths into [0, kv_cap],
+// so malformed metadata can give wrong results but no access out of range;
+// entries past max_entries are dropped.
+__global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, const int32_t* kv, int paged,
+                                                          int B, int qpb, int total_q, long kv_cap,
+                                                          int32_t* entries, int32_t* n_entries, int max_entries) {
+    __shared__ int warp_sum[32];
+    __shared__ int base;
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    if (threadIdx.x == 0) base = 0;
+    __syncthreads();
+    for (int b0 = 0; b0 < B; b0 += 1024) {
+        const int b = b0 + threadIdx.x;
+        int qs = 0, sq = 0, ks = 0, L = 0, nrb = 0;
+        if (b < B) {
+            qs = min(max(cu_q[b], 0), total_q);
+            sq = min(max(cu_q[b + 1], qs), total_q) - qs;
+            if (paged) {
+                L = (int)min((long)max(kv[b], 0), kv_cap);
+            } else {
+                ks = (int)min((long)max(kv[b], 0), kv_cap);
+                L = (int)min((long)max(kv[b + 1], ks), kv_cap) - ks;
+            }
+            nrb = (sq + qpb - 1) / qpb;
+        }
+        int x = nrb;                                   // inclusive scan within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int s = warp_sum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += y;
+            }
+            warp_sum[lane] = s;
+        }
+        __syncthreads();
+        const int first = base + (warp > 0 ? warp_sum[warp - 1] : 0) + x - nrb;
+        for (int k = 0; k < nrb; ++k) {
+            const int e = first + k;
+            if (e >= max_entries) break;
+            int4* dst = reinterpret_cast<int4*>(entries + (size_t)e * ot::ENTRY_INTS);
+            dst[0] = make_int4(b, (nrb - 1 - k) * qpb, qs, sq);
+            dst[1] = make_int4(ks, L, 0, 0);
+        }
+        __syncthreads();
+        if (threadIdx.x == 1023) base = first + nrb;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *n_entries = min(base, max_entries);
+}
+
+}  // namespace
+
+cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int total_q,
+                               long kv_cap, int32_t* entries, int32_t* n_entries, int max_entries,
+                               cudaStream_t stream) {
+    varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_q, kv, paged ? 1 : 0, B, qpb, total_q, kv_cap, entries, n_entries,
+                                               max_entries);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_packed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                 const CUtensorMap& tm_o, const PrefillArgs& a, long max_items, cudaStream_t stream) {
+    switch (a.D * 2 + (a.f16 ? 1 : 0)) {
+        case 64 * 2: return ot::launch_onetile<64, ot::kPacked, true, false>(tm_q, tm_k, tm_v, tm_o, a, max_items, 0, stream);
+        case 64 * 2 + 1: return ot::launch_onetile<64, ot::kPacked, true, true>(tm_q, tm_k, tm_v, tm_o, a, max_items, 0, stream);
+        case 128 * 2: return ot::launch_onetile<128, ot::kPacked, true, false>(tm_q, tm_k, tm_v, tm_o, a, max_items, 0, stream);
+        case 128 * 2 + 1: return ot::launch_onetile<128, ot::kPacked, true, true>(tm_q, tm_k, tm_v, tm_o, a, max_items, 0, stream);
+        case 256 * 2: return ot::launch_onetile<256, ot::kPacked, true, false>(tm_q, tm_k, tm_v, tm_o, a, max_items, 0, stream);
+        case 256 * 2 + 1: return ot::launch_onetile<256, ot::kPacked, true, true>(tm_q, tm_k, tm_v, tm_o, a, max_items, 0, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int varlen_packed_take_device_error() { return ot::take_error(); }
+
+}  // namespace gqa

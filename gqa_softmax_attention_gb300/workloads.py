@@ -128,6 +128,38 @@ def paged_inputs(B, Sq, Hq, Hkv, D, page_size, lengths, spare=0.10, sigma=1.0, s
                 block_table=table, num_pages=pool, max_pages=max_pages, page_size=page_size)
 
 
+def _offsets(lengths):
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def varlen_inputs(q_lens, kv_lens, Hq, Hkv, D, sigma=1.0, seed=0, **_):
+    """Packed (THD) inputs: q [sum(q_lens), Hq, D], k / v [sum(kv_lens), Hkv, D]
+    (streams 0, 1, 2) and their [B + 1] offsets."""
+    cq, ck = _offsets(q_lens), _offsets(kv_lens)
+    tq, tk = int(cq[-1]), int(ck[-1])
+    q = randn_bf16((max(tq, 1), Hq, D), sigma, seed, 0)[:tq]
+    k = randn_bf16((max(tk, 1), Hkv, D), sigma, seed, 1)[:tk]
+    v = randn_bf16((max(tk, 1), Hkv, D), sigma, seed, 2)[:tk]
+    return dict(q=q, k=k, v=v, cu_seqlens_q=cq, cu_seqlens_kv=ck)
+
+
+def varlen_paged_inputs(q_lens, lengths, Hq, Hkv, D, page_size, spare=0.10, sigma=1.0, seed=0, **_):
+    """Packed queries over a paged cache: the cache, lengths and table of
+    paged_inputs(lengths) plus q [sum(q_lens), Hq, D] (stream 3) and its
+    [B + 1] offsets; cache_seqlens = lengths (query tokens included)."""
+    B = len(lengths)
+    p = paged_inputs(B, 1, Hq, Hkv, D, page_size, list(lengths), spare=spare, sigma=sigma, seed=seed)
+    cq = _offsets(q_lens)
+    tq = int(cq[-1])
+    p["q"] = randn_bf16((max(tq, 1), Hq, D), sigma, seed, 3)[:tq]
+    p["cu_seqlens_q"] = cq
+    p["cache_seqlens"] = p.pop("real_seqlen_kv")
+    return p
+
+
 def make(name, seed=0):
     """Inputs of a named workload plus its shape description."""
     cfg = dict(WORKLOADS[name])

@@ -211,6 +211,69 @@ gqa_status attn_decode_paged_noalloc(const void* q, const void* k_cache, const v
 size_t attn_decode_paged_noalloc_max_workspace(void);
 
 /*
+ * Packed variable-length attention (TileOPs "Attention Operators",
+ * GQAVarlenFwdOp), one launch for any mix of request lengths.
+ *
+ *   q    [total_q, Hq, D]    k, v  [total_kv, Hkv, D]     (THD, 16-bit)
+ *   cu_seqlens_q, cu_seqlens_kv  [B + 1] int32 device offsets: request b
+ *        owns query rows [cu_seqlens_q[b], cu_seqlens_q[b + 1]) and key /
+ *        value rows [cu_seqlens_kv[b], cu_seqlens_kv[b + 1]); a request may
+ *        have no query row or no key
+ *   o    [total_q, Hq, D] (written); lse [total_q, Hq] float or NULL
+ *   causal  nonzero: query i of request b sees its keys j <= i + Skv_b - Sq_b
+ *   opts    window, softcap, sinks and dtype as for attn_fwd_dense_ex
+ *   workspace / workspace_bytes: device scratch of at least
+ *        attn_varlen_workspace_size(B, total_q, Hq, Hkv) bytes, 16-byte
+ *        aligned; calls that share one must not overlap on the GPU.
+ *
+ * The offsets stay on the device (no host read-back; the call can be
+ * captured in a CUDA graph with the offsets as live inputs).  The caller
+ * guarantees cu[0] = 0, non-decreasing offsets and cu[B] = total; the device
+ * clamps every offset into [0, total], so malformed offsets give wrong
+ * results but no access outside q, k, v, o and lse; query rows outside every
+ * request are not written.  The g = Hq / Hkv query heads of a KV group share
+ * one tile (g <= 128, GQA_ERR_UNSUPPORTED otherwise).
+ */
+gqa_status attn_fwd_varlen(const void* q, const void* k, const void* v,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                           void* o, float* lse, int B, int total_q, int total_kv,
+                           int Hq, int Hkv, int D, int causal, float scale,
+                           const gqa_options* opts, void* workspace, size_t workspace_bytes,
+                           gqa_stream_t stream);
+
+/*
+ * Packed queries over a paged cache (TileOPs "Attention Operators",
+ * GQAPagedFwdOp): prefill chunks and decode steps of many requests in one
+ * launch.
+ *
+ *   q    [total_q, Hq, D]; request b owns rows [cu_seqlens_q[b], cu_seqlens_q[b + 1])
+ *   k_cache, v_cache  [num_pages, page_size, Hkv, D]
+ *   cache_seqlens     [B] int32: request b's cache length L_b, its query
+ *                     tokens included; query i of request b sits at key
+ *                     position i + L_b - Sq_b
+ *   block_table       [B, max_pages] int32, as for attn_decode_paged
+ *   o    [total_q, Hq, D] (written); lse [total_q, Hq] float or NULL
+ *   workspace         attn_varlen_workspace_size(B, total_q, Hq, Hkv) bytes,
+ *                     16-byte aligned
+ *
+ * page_size must be a multiple of 8 (GQA_ERR_UNSUPPORTED otherwise; pages
+ * move as 8-row TMA blocks) and num_pages >= 1.  Caller obligations on the
+ * table as for attn_decode_paged; lengths are clamped to
+ * [0, max_pages * page_size] and a page id outside [0, num_pages) reads as
+ * zeros.  Cache slots past L_b and pages past a request's end never reach
+ * the result.
+ */
+gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* cu_seqlens_q, const int32_t* cache_seqlens,
+                          const int32_t* block_table, int page_size, void* o, float* lse,
+                          int B, int total_q, int Hq, int Hkv, int D, int num_pages,
+                          int max_pages, int causal, float scale, const gqa_options* opts,
+                          void* workspace, size_t workspace_bytes, gqa_stream_t stream);
+
+/* Workspace bytes of attn_fwd_varlen / attn_fwd_paged (0 for invalid sizes). */
+size_t attn_varlen_workspace_size(int B, int total_q, int Hq, int Hkv);
+
+/*
  * Optional host-side check of the paged metadata (the TileOPs
  * validate_inputs=True analogue).  Copies real_seqlen_kv and block_table to
  * the host (synchronising `stream`) and checks every length and every needed

@@ -29,6 +29,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("attn_fwd_dense", "attn_decode_paged", "attn_decode_paged_workspace_size", "attn_validate_paged",
+              "attn_fwd_varlen", "attn_fwd_paged", "attn_varlen_workspace_size",
               "gqa_status_string", "gqa_device_error", "gqa_version"):
         assert n in names
 
@@ -86,6 +87,44 @@ def test_paged_argument_checks(lib):
     assert paged(lib, ws=None, ws_bytes=0) == WORKSPACE          # workspace is required
     assert paged(lib, ws=A16, ws_bytes=16) == WORKSPACE          # and must be large enough
     assert paged(lib, Sq=0) == OK
+
+
+def varlen(lib, q=A16, o=A16b, cu=A16, cukv=A16, B=2, total_q=8, total_kv=16, Hq=4, Hkv=2, D=64, ws=A16,
+           ws_bytes=1 << 20, opts=None):
+    return lib.attn_fwd_varlen(q, A16, A16, cu, cukv, o, None, B, total_q, total_kv, Hq, Hkv, D, 1, 0.125, opts, ws,
+                               ws_bytes, None)
+
+
+def paged_varlen(lib, q=A16, cu=A16, B=2, total_q=8, Hq=4, Hkv=2, D=64, ps=16, num_pages=4, max_pages=2, ws=A16,
+                 ws_bytes=1 << 20):
+    return lib.attn_fwd_paged(q, A16, A16, cu, A16, A16, ps, A16b, None, B, total_q, Hq, Hkv, D, num_pages, max_pages,
+                              1, 0.125, None, ws, ws_bytes, None)
+
+
+def test_varlen_argument_checks(lib):
+    # TileOPs GQAVarlenFwdOp / GQAPagedFwdOp: refused before anything is launched
+    assert varlen(lib, B=0) == INVALID
+    assert varlen(lib, Hq=6, Hkv=4) == INVALID
+    assert varlen(lib, total_q=-1) == INVALID
+    assert varlen(lib, D=96) == UNSUPPORTED
+    assert varlen(lib, Hq=258, Hkv=1) == UNSUPPORTED              # more than 128 heads per KV head
+    assert varlen(lib, q=MIS) == MISALIGNED
+    assert varlen(lib, cu=ctypes.c_void_p((1 << 20) + 2)) == MISALIGNED
+    assert varlen(lib, cu=None) == INVALID
+    assert varlen(lib, ws=None, ws_bytes=0) == WORKSPACE
+    assert varlen(lib, ws_bytes=lib.attn_varlen_workspace_size(2, 8, 4, 2) - 1) == WORKSPACE
+    assert varlen(lib, ws=ctypes.c_void_p((1 << 20) + 8)) == MISALIGNED
+    assert varlen(lib, total_q=0) == OK                          # nothing to do, nothing launched
+    assert paged_varlen(lib, ps=12) == UNSUPPORTED                # pages move as 8-row blocks
+    assert paged_varlen(lib, ps=0) == INVALID
+    assert paged_varlen(lib, num_pages=0) == INVALID
+    assert paged_varlen(lib, D=80) == UNSUPPORTED
+    assert paged_varlen(lib, ws=None, ws_bytes=0) == WORKSPACE
+    assert paged_varlen(lib, total_q=0) == OK
+    # workspace: a header and one 32-byte entry per possible row block
+    assert lib.attn_varlen_workspace_size(2, 8, 4, 2) == 16 + 32 * (8 // 64 + 2 + 1)
+    assert lib.attn_varlen_workspace_size(3, 1000, 24, 2) == 16 + 32 * (1000 // 10 + 3 + 1)   # g = 12: 10 queries
+    assert lib.attn_varlen_workspace_size(2, 8, 6, 4) == 0
 
 
 def test_workspace_size_is_positive_and_monotone(lib):
