@@ -163,6 +163,7 @@ __device__ __forceinline__ void q_row_to_tmem(const DecodeArgs& a, uint32_t tadd
         const uint4 v = src ? __ldg(src + e) : make_uint4(0u, 0u, 0u, 0u);
         w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
     }
+    __syncwarp();                                  // tcgen05.st is warp-collective
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) tmem_st32(taddr + 32 * c, w + 32 * c);
 }
@@ -578,6 +579,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     float o[32];
+                    __syncwarp();                          // tcgen05.ld is warp-collective: reconverge
                     tmem_ld32(tmem + lane_addr + C::COL_O + 32 * cc, o);
                     if (row_ok) {
                         float4* dst = reinterpret_cast<float4*>(a.part_o + part_row * D + 32 * cc);

@@ -419,15 +419,19 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!take(C::CK)) return false;
                 if (lane == 0) {
                     const uint32_t d = tmem + COL_S0 + (gi & 1) * BN;
+                    // descriptors of the Q tile and of each K chunk, advanced by
+                    // constant offsets (>> 4) per step
+                    const uint64_t qdesc = make_sdesc_sw128(sb + C::OFF_Q, 16, 1024);
+                    uint64_t kdesc[C::CK];
+#pragma unroll
+                    for (int c = 0; c < C::CK; ++c) kdesc[c] = make_sdesc_sw128(chunk_addr(c), 16, C::K_GROUP);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         constexpr int PER = D / 16 / C::CK;       // steps per K chunk
                         const int kl = kk % PER;
                         const uint32_t qoff = (kk / 4) * BOX + (kk % 4) * 32;
                         const uint32_t koff = (kl / 4) * C::K_SLICE + (kl % 4) * 32;
-                        mma_bf16_ss(d, make_sdesc_sw128(sb + C::OFF_Q + qoff, 16, 1024),
-                                    make_sdesc_sw128(chunk_addr(kk / PER) + koff, 16, C::K_GROUP), IDESC_QK,
-                                    kk > 0 ? 1u : 0u);
+                        mma_bf16_ss(d, qdesc + (qoff >> 4), kdesc[kk / PER] + (koff >> 4), IDESC_QK, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(s_full(gi & 1));
                 }
@@ -455,13 +459,15 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 if (lane == 0) {
                     const uint32_t p = tmem + COL_S0 + (gi & 1) * BN;
+                    uint64_t vdesc[C::CV];
+#pragma unroll
+                    for (int c = 0; c < C::CV; ++c) vdesc[c] = make_sdesc_sw128(chunk_addr(c), C::V_SLICE, C::V_GROUP);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
                         constexpr int PER = BN / 16 / C::CV;       // steps per V chunk
                         const int kc = (kk % PER) * 16;
-                        const uint64_t bdesc = make_sdesc_sw128(chunk_addr(kk / PER) + (kc / 8) * C::V_GROUP,
-                                                                C::V_SLICE, C::V_GROUP);
-                        mma_bf16_ts(tmem + COL_O, p + kk * 8, bdesc, IDESC_PV, (!fresh || kk > 0) ? 1u : 0u);
+                        mma_bf16_ts(tmem + COL_O, p + kk * 8, vdesc[kk / PER] + (((kc / 8) * C::V_GROUP) >> 4), IDESC_PV,
+                                    (!fresh || kk > 0) ? 1u : 0u);
                     }
                 }
                 release(C::CV);
@@ -666,7 +672,10 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (w < 0) break;
             const Item itm = describe(w);
             const TileInfo ti = itm.t;
-            ok = mbar_wait(stats_full, n & 1, abort_flag) && mbar_wait(o_final, n & 1, abort_flag);
+            // warp-collective waits: the warp must be converged at the
+            // .aligned barrier below and at every tcgen05.ld
+            ok = __all_sync(0xffffffffu, mbar_wait(stats_full, n & 1, abort_flag));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final, n & 1, abort_flag));
             if (!named_bar_and(3, BM, ok)) break;     // the whole warpgroup stops together
             tc_fence_after();
             const int cnt = *st_cnt;
@@ -692,52 +701,64 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     lse2 = M + log2f(l_tot);
                 }
             }
-            // whole blocks go out with TMA; a packed block cut by its request's
-            // end is written row by row (its box would reach the next request)
+            // Whole blocks go out with TMA; a packed block cut by its request's
+            // end is written row by row (its box would reach the next request).
+            // The choice is the same for every thread of the item.
             const bool boxed = !PACKED || ti.rows_valid == qpb;
-            if (cnt > 0) {
-                // O / l packed to 16 bits, 128 columns at a time; O is free once
-                // the last columns are read
-                constexpr int HALF = D < 128 ? D : 128;
+            constexpr int HALF = D < 128 ? D : 128;     // O columns read per pass
+            // O / l packed to 16 bits, HALF columns at a time; O is free once the
+            // last columns are read
+            auto read_o = [&](int half, uint32_t* ow) {
+                // tcgen05.ld is warp-collective (.sync.aligned): reconverge first
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < HALF / 32; ++c) {
+                    float f[32];
+                    tmem_ld32(tmem + lane_addr + COL_O + HALF * half + 32 * c, f);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) ow[16 * c + e] = pack2<F16>(f[2 * e] * inv, f[2 * e + 1] * inv);
+                }
+                if (half == D / HALF - 1) {
+                    tc_fence_before();
+                    mbar_arrive(stats_empty);
+                    mbar_arrive(o_empty);
+                }
+            };
+            if (cnt > 0 && boxed) {
 #pragma unroll
                 for (int half = 0; half < D / HALF; ++half) {
                     uint32_t ow[HALF / 2];
+                    read_o(half, ow);
+                    // 64-column boxes through the alternating staging buffers
 #pragma unroll
-                    for (int c = 0; c < HALF / 32; ++c) {
-                        float f[32];
-                        tmem_ld32(tmem + lane_addr + COL_O + HALF * half + 32 * c, f);
+                    for (int sub = 0; sub < HALF / 64; ++sub, ++nb) {
+                        const uint32_t stage = sb + C::OFF_STAGE + (nb & 1) * BOX;
+                        if (r == 0) bulk_wait_read_1();       // the store two boxes back has read this buffer
+                        __syncwarp();
+                        named_bar_sync(3, BM);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) ow[16 * c + e] = pack2<F16>(f[2 * e] * inv, f[2 * e + 1] * inv);
-                    }
-                    if (half == D / HALF - 1) {
-                        tc_fence_before();
-                        mbar_arrive(stats_empty);
-                        mbar_arrive(o_empty);
-                    }
-                    if (boxed) {
-                        // 64-column boxes through the alternating staging buffers
-#pragma unroll
-                        for (int sub = 0; sub < HALF / 64; ++sub, ++nb) {
-                            const uint32_t stage = sb + C::OFF_STAGE + (nb & 1) * BOX;
-                            if (r == 0) bulk_wait_read_1();   // the store two boxes back has read this buffer
-                            named_bar_sync(3, BM);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const uint32_t* u = ow + 32 * sub + 4 * q;
-                                st_shared_v4(stage + r * 128 + ((q ^ (r & 7)) << 4), u[0], u[1], u[2], u[3]);
-                            }
-                            fence_proxy_async_smem();
-                            named_bar_sync(3, BM);
-                            if (r == 0) {
-                                const int col = HALF * half + 64 * sub;
-                                if constexpr (PACKED)
-                                    tma_store_3d(&tm_o, stage, col, itm.hq, itm.qs + ti.q0);
-                                else
-                                    tma_store_4d(&tm_o, stage, col, ti.q0, itm.hq, itm.b);
-                                bulk_commit_group();
-                            }
+                        for (int q = 0; q < 8; ++q) {
+                            const uint32_t* u = ow + 32 * sub + 4 * q;
+                            st_shared_v4(stage + r * 128 + ((q ^ (r & 7)) << 4), u[0], u[1], u[2], u[3]);
                         }
-                    } else if (row_ok) {
+                        fence_proxy_async_smem();
+                        named_bar_sync(3, BM);
+                        if (r == 0) {
+                            const int col = HALF * half + 64 * sub;
+                            if constexpr (PACKED)
+                                tma_store_3d(&tm_o, stage, col, itm.hq, itm.qs + ti.q0);
+                            else
+                                tma_store_4d(&tm_o, stage, col, ti.q0, itm.hq, itm.b);
+                            bulk_commit_group();
+                        }
+                    }
+                }
+            } else if (cnt > 0) {
+#pragma unroll
+                for (int half = 0; half < D / HALF; ++half) {
+                    uint32_t ow[HALF / 2];
+                    read_o(half, ow);
+                    if (row_ok) {
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + orow * D + HALF * half);
 #pragma unroll
                         for (int e = 0; e < HALF / 8; ++e)

@@ -586,6 +586,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
 #pragma unroll
                 for (int sub = 0; sub < C::KSUB; ++sub) {
+                    __syncwarp();                              // converged at the .aligned barriers
                     if (sub > 0) named_bar_sync(3 + k, BM);   // the previous box has been read out
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {              // 16-byte chunk q of the box row
