@@ -266,17 +266,21 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tma_prefetch_desc(&tm_k);
                 tma_prefetch_desc(&tm_v);
             }
-            // Lane 0: waits for the next ring slot and arms its barrier for
-            // `bytes`; every lane learns the slot's address.  Warp-collective.
+            // Waits for the next ring slot and arms its barrier for `bytes`.
+            // TMA-tensor layouts: lane 0 alone (it issues every copy).  Paged:
+            // warp-collective, every lane learning the slot (lanes copy one
+            // page block each).
             auto take_slot = [&](uint32_t& dst, uint32_t& full, uint32_t bytes) -> bool {
                 const int s = nc % C::NS;
                 bool good = true;
-                if (lane == 0) {
+                if (MODE != kPaged || lane == 0) {
                     good = mbar_wait(r_empty(s), ((nc / C::NS) & 1) ^ 1, abort_flag);
                     if (good) mbar_arrive_expect_tx(r_full(s), bytes);
                 }
-                good = __shfl_sync(0xffffffffu, good, 0);
-                __syncwarp();                        // the expect-tx precedes every lane's copy
+                if constexpr (MODE == kPaged) {
+                    good = __shfl_sync(0xffffffffu, good, 0);
+                    __syncwarp();                    // the expect-tx precedes every lane's copy
+                }
                 full = r_full(s);
                 dst = sb + C::OFF_RING + s * SLOT;
                 if (good) ++nc;
@@ -307,17 +311,15 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         const int rows = paged_blocks(it, j * BN, a.bt_k, n);
                         if (!take_slot(dst, full, (uint32_t)(rows * 128 * C::KSL_C))) return false;
                         paged_copy(it, &tm_k, dst, full, j * BN, a.bt_k, n, C::K_GROUP, c * C::KSL_C);
-                    } else {
+                    } else {                        // lane 0 only
                         if (!take_slot(dst, full, C::K_CHUNK)) return false;
-                        if (lane == 0) {
 #pragma unroll
-                            for (int s = 0; s < C::KSL_C; ++s) {
-                                const int col = 64 * (c * C::KSL_C + s);
-                                if constexpr (MODE == kPacked)
-                                    tma_load_3d(dst + s * C::K_SLICE, &tm_k, full, col, it.hkv, it.ks + j * BN);
-                                else
-                                    tma_load_4d(dst + s * C::K_SLICE, &tm_k, full, col, j * BN, it.hkv, it.b);
-                            }
+                        for (int s = 0; s < C::KSL_C; ++s) {
+                            const int col = 64 * (c * C::KSL_C + s);
+                            if constexpr (MODE == kPacked)
+                                tma_load_3d(dst + s * C::K_SLICE, &tm_k, full, col, it.hkv, it.ks + j * BN);
+                            else
+                                tma_load_4d(dst + s * C::K_SLICE, &tm_k, full, col, j * BN, it.hkv, it.b);
                         }
                     }
                 }
@@ -332,16 +334,14 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         const int rows = paged_blocks(it, key0, a.bt_v, n);
                         if (!take_slot(dst, full, (uint32_t)(rows * 128 * C::KSL))) return false;
                         paged_copy(it, &tm_v, dst, full, key0, a.bt_v, n, C::V_GROUP, 0);
-                    } else {
+                    } else {                        // lane 0 only
                         if (!take_slot(dst, full, C::V_CHUNK)) return false;
-                        if (lane == 0) {
 #pragma unroll
-                            for (int s = 0; s < C::KSL; ++s) {
-                                if constexpr (MODE == kPacked)
-                                    tma_load_3d(dst + s * C::V_SLICE, &tm_v, full, 64 * s, it.hkv, it.ks + key0);
-                                else
-                                    tma_load_4d(dst + s * C::V_SLICE, &tm_v, full, 64 * s, key0, it.hkv, it.b);
-                            }
+                        for (int s = 0; s < C::KSL; ++s) {
+                            if constexpr (MODE == kPacked)
+                                tma_load_3d(dst + s * C::V_SLICE, &tm_v, full, 64 * s, it.hkv, it.ks + key0);
+                            else
+                                tma_load_4d(dst + s * C::V_SLICE, &tm_v, full, 64 * s, key0, it.hkv, it.b);
                         }
                     }
                 }
@@ -376,11 +376,15 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // K of tile 0, then (K of tile i+1, V of tile i) for each tile i
                 TileIter tiles(it.mrow, it.first, it.t.n_tiles, it.t.kv_end, lane);
                 int j = tiles.next();
-                ok = load_k(it, j);
+                if (MODE == kPaged || lane == 0) ok = load_k(it, j);
+                if (MODE != kPaged) ok = __shfl_sync(0xffffffffu, ok, 0);
                 while (ok && j >= 0) {
                     const int jn = tiles.next();
-                    if (jn >= 0) ok = load_k(it, jn);
-                    if (ok) ok = load_v(it, j);
+                    if (MODE == kPaged || lane == 0) {
+                        if (jn >= 0) ok = load_k(it, jn);
+                        if (ok) ok = load_v(it, j);
+                    }
+                    if (MODE != kPaged) ok = __shfl_sync(0xffffffffu, ok, 0);
                     j = jn;
                 }
             }
@@ -394,91 +398,73 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         } else if (warp == WARP_MMA) {
             // ------------------------------------------------------------ MMA issuer
-            // Every lane runs the loop and waits; lane 0 issues and commits.
+            // Lane 0 alone issues every MMA of an item but its last P V (a
+            // single polling lane keeps the issue loop short); the whole warp
+            // takes the last P V, whose value rows past the request's end it
+            // zeroes first (packed layouts).
             int nc = 0, nq = 0;     // ring chunks and Q blocks consumed
             int g_t = 0;            // visited tiles of earlier items (S buffer / p_full parity)
             int oe = 0;             // o_empty phases waited
             bool ok = true;
-            auto wait_all = [&](uint32_t bar, uint32_t parity) {
-                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
-            };
             auto chunk_addr = [&](int k) { return sb + C::OFF_RING + ((nc + k) % C::NS) * SLOT; };
-            auto take = [&](int n) -> bool {        // the next n ring chunks have landed
+            auto take = [&](int n) -> bool {        // lane 0: the next n ring chunks have landed
                 for (int k = 0; k < n; ++k)
-                    if (!wait_all(r_full((nc + k) % C::NS), ((nc + k) / C::NS) & 1)) return false;
+                    if (!mbar_wait(r_full((nc + k) % C::NS), ((nc + k) / C::NS) & 1, abort_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            auto release = [&](int n) {
-                if (lane == 0)
-                    for (int k = 0; k < n; ++k) mma_commit(r_empty((nc + k) % C::NS));
+            auto release = [&](int n) {             // lane 0
+                for (int k = 0; k < n; ++k) mma_commit(r_empty((nc + k) % C::NS));
                 nc += n;
             };
-            // S of visited tile gi = Q K^T over D / 16 steps of 16 columns
+            // S of visited tile gi = Q K^T over D / 16 steps of 16 columns (lane 0)
             auto issue_qk = [&](int gi) -> bool {
                 if (!take(C::CK)) return false;
-                if (lane == 0) {
-                    const uint32_t d = tmem + COL_S0 + (gi & 1) * BN;
-                    // descriptors of the Q tile and of each K chunk, advanced by
-                    // constant offsets (>> 4) per step
-                    const uint64_t qdesc = make_sdesc_sw128(sb + C::OFF_Q, 16, 1024);
-                    uint64_t kdesc[C::CK];
+                const uint32_t d = tmem + COL_S0 + (gi & 1) * BN;
+                // descriptors of the Q tile and of each K chunk, advanced by
+                // constant offsets (>> 4) per step
+                const uint64_t qdesc = make_sdesc_sw128(sb + C::OFF_Q, 16, 1024);
+                uint64_t kdesc[C::CK];
 #pragma unroll
-                    for (int c = 0; c < C::CK; ++c) kdesc[c] = make_sdesc_sw128(chunk_addr(c), 16, C::K_GROUP);
+                for (int c = 0; c < C::CK; ++c) kdesc[c] = make_sdesc_sw128(chunk_addr(c), 16, C::K_GROUP);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        constexpr int PER = D / 16 / C::CK;       // steps per K chunk
-                        const int kl = kk % PER;
-                        const uint32_t qoff = (kk / 4) * BOX + (kk % 4) * 32;
-                        const uint32_t koff = (kl / 4) * C::K_SLICE + (kl % 4) * 32;
-                        mma_bf16_ss(d, qdesc + (qoff >> 4), kdesc[kk / PER] + (koff >> 4), IDESC_QK, kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(s_full(gi & 1));
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    constexpr int PER = D / 16 / C::CK;       // steps per K chunk
+                    const int kl = kk % PER;
+                    const uint32_t qoff = (kk / 4) * BOX + (kk % 4) * 32;
+                    const uint32_t koff = (kl / 4) * C::K_SLICE + (kl % 4) * 32;
+                    mma_bf16_ss(d, qdesc + (qoff >> 4), kdesc[kk / PER] + (koff >> 4), IDESC_QK, kk > 0 ? 1u : 0u);
                 }
+                mma_commit(s_full(gi & 1));
                 release(C::CK);
-                __syncwarp();
                 return true;
             };
-            // O (+)= P V of visited tile gi: 8 steps of 16 keys.  nvalid < BN:
-            // value rows from nvalid on are zeroed first.
-            auto issue_pv = [&](int gi, bool fresh, int nvalid) -> bool {
-                if (!wait_all(p_full(gi & 1), (gi >> 1) & 1)) return false;
-                if (!take(C::CV)) return false;
-                if (PACKED && nvalid < BN) {
-                    for (int idx = lane; idx < (BN - nvalid) * 8 * C::KSL; idx += 32) {
-                        const int key = nvalid + idx / (8 * C::KSL);
-                        const int s = (idx / 8) % C::KSL, q = idx % 8;
-                        const int kc = key % C::VKEYS;
-                        const uint32_t off = chunk_addr(key / C::VKEYS) - sb + s * C::V_SLICE +
-                                             (kc / 8) * C::V_GROUP + (kc % 8) * 128 + q * 16;
-                        *reinterpret_cast<uint4*>(smem + off) = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    tc_fence_after();
-                }
-                if (lane == 0) {
-                    const uint32_t p = tmem + COL_S0 + (gi & 1) * BN;
-                    uint64_t vdesc[C::CV];
+            // O (+)= P V of visited tile gi: 8 steps of 16 keys (lane 0)
+            auto mma_pv = [&](int gi, bool fresh) {
+                const uint32_t p = tmem + COL_S0 + (gi & 1) * BN;
+                uint64_t vdesc[C::CV];
 #pragma unroll
-                    for (int c = 0; c < C::CV; ++c) vdesc[c] = make_sdesc_sw128(chunk_addr(c), C::V_SLICE, C::V_GROUP);
+                for (int c = 0; c < C::CV; ++c) vdesc[c] = make_sdesc_sw128(chunk_addr(c), C::V_SLICE, C::V_GROUP);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        constexpr int PER = BN / 16 / C::CV;       // steps per V chunk
-                        const int kc = (kk % PER) * 16;
-                        mma_bf16_ts(tmem + COL_O, p + kk * 8, vdesc[kk / PER] + (((kc / 8) * C::V_GROUP) >> 4), IDESC_PV,
-                                    (!fresh || kk > 0) ? 1u : 0u);
-                    }
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    constexpr int PER = BN / 16 / C::CV;       // steps per V chunk
+                    const int kc = (kk % PER) * 16;
+                    mma_bf16_ts(tmem + COL_O, p + kk * 8, vdesc[kk / PER] + (((kc / 8) * C::V_GROUP) >> 4), IDESC_PV,
+                                (!fresh || kk > 0) ? 1u : 0u);
                 }
                 release(C::CV);
-                if (lane == 0) mma_commit(o_ready);
-                __syncwarp();
+                mma_commit(o_ready);
+            };
+            auto issue_pv = [&](int gi, bool fresh) -> bool {      // lane 0
+                if (!mbar_wait(p_full(gi & 1), (gi >> 1) & 1, abort_flag)) return false;
+                if (!take(C::CV)) return false;
+                mma_pv(gi, fresh);
                 return true;
             };
-            // the epilogue of every earlier item has read O
+            // lane 0: the epilogue of every earlier item has read O
             auto wait_o_empty = [&](int n_item) -> bool {
                 for (; oe < n_item; ++oe)
-                    if (!wait_all(o_empty, oe & 1)) return false;
+                    if (!mbar_wait(o_empty, oe & 1, abort_flag)) return false;
                 return true;
             };
             for (int r = 0, n_item = 0; ok; ++r, ++n_item) {
@@ -486,24 +472,56 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (w < 0) break;
                 const Item it = describe(w);
                 const int c = count_tiles(it);
-                if (c > 0) {
-                    // value rows of the last tile past the request's end (packed layouts)
-                    const int last_valid = PACKED ? min(BN, it.skv - (it.t.n_tiles - 1) * BN) : BN;
-                    ok = wait_all(q_full, nq++ & 1);
-                    if (ok) ok = issue_qk(g_t);
-                    if (ok && c > 1) ok = issue_qk(g_t + 1);
-                    if (ok) ok = wait_o_empty(n_item);
-                    if (ok) ok = issue_pv(g_t, true, c == 1 ? last_valid : BN);
-                    for (int i = 1; i + 1 < c && ok; ++i) {
-                        ok = issue_qk(g_t + i + 1);
-                        if (ok) ok = issue_pv(g_t + i, false, BN);
+                if (lane == 0) {
+                    if (c > 0) {
+                        ok = mbar_wait(q_full, nq++ & 1, abort_flag);
+                        if (ok) ok = issue_qk(g_t);
+                        if (ok && c > 1) ok = issue_qk(g_t + 1);
+                        if (ok) ok = wait_o_empty(n_item);
+                        if (ok && c > 1) ok = issue_pv(g_t, true);
+                        for (int i = 1; i + 1 < c && ok; ++i) {
+                            ok = issue_qk(g_t + i + 1);
+                            if (ok) ok = issue_pv(g_t + i, false);
+                        }
+                        if (ok) mma_commit(q_empty);               // every S of the item is issued
+                        // BSHD: no value row to zero, lane 0 issues the last P V too
+                        if (!PACKED && ok) ok = issue_pv(g_t + c - 1, c == 1);
+                    } else {
+                        ok = wait_o_empty(n_item);
                     }
-                    if (ok && lane == 0) mma_commit(q_empty);       // every S of the item is issued
-                    if (ok && c > 1) ok = issue_pv(g_t + c - 1, false, last_valid);
-                    g_t += c;
-                } else {
-                    ok = wait_o_empty(n_item);
                 }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                nc = __shfl_sync(0xffffffffu, nc, 0);
+                nq = __shfl_sync(0xffffffffu, nq, 0);
+                oe = __shfl_sync(0xffffffffu, oe, 0);
+                if (PACKED && ok && c > 0) {
+                    // the item's last P V, by the whole warp
+                    const int gi = g_t + c - 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait(p_full(gi & 1), (gi >> 1) & 1, abort_flag));
+                    for (int k = 0; k < C::CV && ok; ++k)
+                        ok = __all_sync(0xffffffffu,
+                                        mbar_wait(r_full((nc + k) % C::NS), ((nc + k) / C::NS) & 1, abort_flag));
+                    if (ok) {
+                        tc_fence_after();
+                        const int nvalid = PACKED ? min(BN, it.skv - (it.t.n_tiles - 1) * BN) : BN;
+                        if (PACKED && nvalid < BN) {
+                            for (int idx = lane; idx < (BN - nvalid) * 8 * C::KSL; idx += 32) {
+                                const int key = nvalid + idx / (8 * C::KSL);
+                                const int s = (idx / 8) % C::KSL, q = idx % 8;
+                                const int kc = key % C::VKEYS;
+                                const uint32_t off = chunk_addr(key / C::VKEYS) - sb + s * C::V_SLICE +
+                                                     (kc / 8) * C::V_GROUP + (kc % 8) * 128 + q * 16;
+                                *reinterpret_cast<uint4*>(smem + off) = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            tc_fence_after();
+                        }
+                        if (lane == 0) mma_pv(gi, c == 1);
+                        nc = __shfl_sync(0xffffffffu, nc, 0);
+                    }
+                }
+                g_t += c;
                 // one phase per item: every MMA of the item has completed
                 if (ok && lane == 0) mma_commit(o_final);
                 __syncwarp();
