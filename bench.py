@@ -16,7 +16,7 @@ every step starts with a cold L2.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload step|qwen3_8b_prefill|paged_decode|wide_group_decode|long_chunked_prefill|
-                                   wide_group_prefill]
+                                   wide_group_prefill|varlen_prefill|mixed_serving_batch]
 Prints exactly one JSON line (rank 0).
 """
 import argparse
@@ -64,6 +64,29 @@ def decode_bytes(p):
     return float(p["real_seqlen_kv"].to(torch.int64).sum()) * 2 * c["Hkv"] * c["D"] * 2
 
 
+def packed_pairs(cu_q, kv_lens):
+    """Visible (query, key) pairs of a packed causal call, one head: query i of
+    request b sees min(L_b, i + L_b - Sq_b + 1) keys (end-aligned)."""
+    total = 0
+    for b in range(len(kv_lens)):
+        sq, L = int(cu_q[b + 1] - cu_q[b]), int(kv_lens[b])
+        i = torch.arange(sq, dtype=torch.int64)
+        total += int((i + L - sq + 1).clamp(0, L).sum())
+    return total
+
+
+def packed_work(d):
+    """(FLOPs, pairs per head, K/V bytes read once) of a packed call."""
+    c = d["config"]
+    if c["kind"] == "varlen":
+        lens = (d["cu_seqlens_kv"][1:] - d["cu_seqlens_kv"][:-1]).tolist()
+    else:
+        lens = d["cache_seqlens"].tolist()
+    pairs = packed_pairs(d["cu_seqlens_q"], lens)
+    kv_bytes = float(sum(lens)) * 2 * c["Hkv"] * c["D"] * 2
+    return 4.0 * c["D"] * c["Hq"] * pairs, pairs, kv_bytes
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -105,17 +128,35 @@ class Part:
         if self.kind == "dense":
             self.flops, self.pairs = prefill_work(data)
             self.bytes = 0.0
+        elif self.kind == "varlen":
+            self.flops, self.pairs, _ = packed_work(data)      # tensor-bound: FLOPs only
+            self.bytes = 0.0
+        elif self.kind == "paged_varlen":
+            # prefill chunks and decode steps together: both terms count
+            self.flops, self.pairs, self.bytes = packed_work(data)
         else:
             self.flops, self.pairs = 0.0, 0
             self.bytes = decode_bytes(data)
 
     def ideal_s(self, peaks):
-        if self.kind == "dense":
-            return self.flops / (peaks["bf16_tflops"] * 1e12)
-        return self.bytes / (peaks["hbm_gbs"] * 1e9)
+        return self.flops / (peaks["bf16_tflops"] * 1e12) + self.bytes / (peaks["hbm_gbs"] * 1e9)
 
     def to_device(self, dev):
         d = self.data
+        if self.kind in ("varlen", "paged_varlen"):
+            import gqa_softmax_attention_gb300 as g
+            c = d["config"]
+            if self.kind == "varlen":
+                names = ("q", "k", "v", "cu_seqlens_q", "cu_seqlens_kv")
+            else:
+                names = ("q", "k_cache", "v_cache", "cu_seqlens_q", "cache_seqlens", "block_table")
+            self.dev = {n: d[n].to(dev) for n in names}
+            tq = d["q"].shape[0]
+            need = g.attn_varlen_workspace_size(len(d["cu_seqlens_q"]) - 1, tq, c["Hq"], c["Hkv"])
+            self.dev["ws"] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            self.dev["o"] = torch.empty_like(self.dev["q"])
+            self.dev["lse"] = torch.empty((tq, c["Hq"]), dtype=torch.float32, device=dev)
+            return
         if self.kind == "dense":
             self.dev = dict(q=d["q"].to(dev), k=d["k"].to(dev), v=d["v"].to(dev),
                             m=d["key_padding_mask"].to(dev) if d["key_padding_mask"] is not None else None)
@@ -134,12 +175,18 @@ class Part:
             self.dev["lse"] = torch.empty((c["B"], c["Sq"], c["Hq"]), dtype=torch.float32, device=dev)
 
     def launches(self):
-        return 1 if self.kind == "dense" else 2
+        return 1 if self.kind == "dense" else 2           # packed calls: plan + attention
 
     def run(self):
         import gqa_softmax_attention_gb300 as g
         x = self.dev
-        if self.kind == "dense":
+        if self.kind == "varlen":
+            g.attn_fwd_varlen(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_kv"], causal=True,
+                              out=x["o"], lse=x["lse"], workspace=x["ws"])
+        elif self.kind == "paged_varlen":
+            g.attn_fwd_paged(x["q"], x["k_cache"], x["v_cache"], x["cu_seqlens_q"], x["cache_seqlens"],
+                             x["block_table"], causal=True, out=x["o"], lse=x["lse"], workspace=x["ws"])
+        elif self.kind == "dense":
             g.attn_fwd_dense(x["q"], x["k"], x["v"], key_padding_mask=x["m"], causal=True, out=x["o"], lse=x["lse"])
         else:
             g.attn_decode_paged(x["q"], x["kc"], x["vc"], x["sl"], x["bt"], causal=True, workspace=x["ws"],
@@ -148,7 +195,11 @@ class Part:
     # host-resident copies for the end-to-end measurement
     def pin(self):
         d = self.data
-        if self.kind == "dense":
+        if self.kind == "varlen":
+            names = [(n, d[n]) for n in ("q", "k", "v", "cu_seqlens_q", "cu_seqlens_kv")]
+        elif self.kind == "paged_varlen":
+            names = [(n, d[n]) for n in ("q", "k_cache", "v_cache", "cu_seqlens_q", "cache_seqlens", "block_table")]
+        elif self.kind == "dense":
             names = [("q", d["q"]), ("k", d["k"]), ("v", d["v"])]
             if d["key_padding_mask"] is not None:
                 names.append(("m", d["key_padding_mask"]))
@@ -183,6 +234,8 @@ def make_parts(workload, batch=None):
             parts.append(Part(n, W.make(n)))
             continue
         cfg = dict(W.WORKLOADS[n], B=batch)
+        if cfg["kind"] not in ("dense", "paged"):
+            raise SystemExit("--batch applies to the dense and paged-decode workloads")
         data = W.dense_inputs(**cfg) if cfg["kind"] == "dense" else W.paged_inputs(**cfg)
         data["config"] = cfg
         parts.append(Part(n, data))
@@ -316,7 +369,10 @@ def bench_ours(args, world, rank, local):
     dom, dom_t = None, -1.0
     for p, ts in zip(parts, per_part):
         t = statistics.mean(ts)
-        if p.kind == "dense":
+        if p.kind == "paged_varlen":
+            detail[p.name] = dict(ms=1e3 * t, ms_min=1e3 * min(ts), tflops=p.flops / t / 1e12, gbs=p.bytes / t / 1e9,
+                                  frac=p.ideal_s(peaks) / t, gflop=p.flops / 1e9, gbytes=p.bytes / 1e9)
+        elif p.kind in ("dense", "varlen"):
             ach = p.flops / t / 1e12
             detail[p.name] = dict(ms=1e3 * t, ms_min=1e3 * min(ts), tflops=ach,
                                   frac=ach / peaks["bf16_tflops"], gflop=p.flops / 1e9)
@@ -326,7 +382,29 @@ def bench_ours(args, world, rank, local):
                                   gbytes=p.bytes / 1e9)
         if t > dom_t:
             dom, dom_t = p, t
-    if dom.kind == "dense":
+    if dom.kind == "paged_varlen":
+        # one launch serving prefill chunks and decode steps: the roofline is
+        # the sum of the FLOP term and the K/V byte term; the dominant one names it
+        c = dom.data["config"]
+        t_tensor = dom.flops / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = dom.bytes / (peaks["hbm_gbs"] * 1e9)
+        if t_hbm >= t_tensor:
+            roof = dict(bound="hbm", achieved=dom.bytes / dom_t / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
+                        frac=dom.bytes / dom_t / 1e9 / peaks["hbm_gbs"])
+        else:
+            roof = dict(bound="tensor", achieved=dom.flops / dom_t / 1e12, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                        frac=dom.flops / dom_t / 1e12 / peaks["bf16_tflops"])
+        roof.update(kernel="onetile_kernel<%d,kPaged> + varlen_plan_kernel (%s)" % (c["D"], dom.name),
+                    traffic=traffic_per_launch(dom), peak_source=peaks["source"],
+                    mixed=dict(tflops=dom.flops / dom_t / 1e12, gbs=dom.bytes / dom_t / 1e9,
+                               frac_of_summed_roofline=(t_tensor + t_hbm) / dom_t))
+    elif dom.kind == "varlen":
+        ach = dom.flops / dom_t / 1e12
+        roof = dict(kernel="onetile_kernel<%d,kPacked> + varlen_plan_kernel (%s)" % (dom.data["config"]["D"], dom.name),
+                    bound="tensor", achieved=ach, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                    frac=ach / peaks["bf16_tflops"], traffic=traffic_per_launch(dom),
+                    peak_source=peaks["source"] + " bf16 burst")
+    elif dom.kind == "dense":
         ach = dom.flops / dom_t / 1e12
         kname = "prefill_d256_kernel" if dom.data["config"]["D"] == 256 else "prefill_kernel<%d>" % dom.data["config"]["D"]
         roof = dict(kernel=kname + " (" + dom.name + ")", bound="tensor", achieved=ach,
@@ -412,6 +490,36 @@ def oracle_sample(parts, prefill_rows, decode_requests, seed=0):
             est += dt * total_pairs / max(pairs, 1)
             desc.append("%s: %d random rows (%.2f%% of its pairs) in %.2fs" % (p.name, n, 100.0 * pairs / total_pairs,
                                                                               dt))
+        elif p.kind in ("varlen", "paged_varlen"):
+            # random packed query rows, each as a one-query call whose keys end
+            # at that query's position (end-aligned causal)
+            n = max(1, prefill_rows // 64)
+            cu = d["cu_seqlens_q"]
+            tq = int(cu[-1])
+            one = torch.tensor([0, 1], dtype=torch.int32)
+            rows = torch.randint(0, tq, (n,), generator=gen).tolist()
+            pairs, dt = 0, 0.0
+            for t in rows:
+                b = int(torch.searchsorted(cu, torch.tensor(t), right=True)) - 1
+                sq, i = int(cu[b + 1] - cu[b]), t - int(cu[b])
+                if p.kind == "varlen":
+                    ks, L = int(d["cu_seqlens_kv"][b]), int(d["cu_seqlens_kv"][b + 1] - d["cu_seqlens_kv"][b])
+                    vis = max(0, min(L, i + L - sq + 1))
+                    t0 = time.perf_counter()
+                    oracle.attn_varlen(d["q"][t:t + 1], d["k"][ks:ks + vis], d["v"][ks:ks + vis], one,
+                                       torch.tensor([0, vis], dtype=torch.int32), causal=True)
+                else:
+                    L = int(d["cache_seqlens"][b])
+                    vis = max(0, min(L, i + L - sq + 1))
+                    t0 = time.perf_counter()
+                    oracle.attn_paged_varlen(d["q"][t:t + 1], d["k_cache"], d["v_cache"], one,
+                                             torch.tensor([vis], dtype=torch.int32), d["block_table"][b:b + 1],
+                                             causal=True)
+                dt += time.perf_counter() - t0
+                pairs += vis
+            est += dt * p.pairs / max(pairs, 1)
+            desc.append("%s: %d random query rows (%.3f%% of its pairs) in %.2fs" % (p.name, n, 100.0 * pairs / p.pairs,
+                                                                                    dt))
         else:
             n = min(decode_requests, c["B"])
             reqs = torch.randperm(c["B"], generator=gen)[:n].tolist()
@@ -434,6 +542,11 @@ def oracle_whole(parts):
         d = p.data
         if p.kind == "dense":
             oracle.attn_dense(d["q"], d["k"], d["v"], key_padding_mask=d["key_padding_mask"], causal=True)
+        elif p.kind == "varlen":
+            oracle.attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_kv"], causal=True)
+        elif p.kind == "paged_varlen":
+            oracle.attn_paged_varlen(d["q"], d["k_cache"], d["v_cache"], d["cu_seqlens_q"], d["cache_seqlens"],
+                                     d["block_table"], causal=True)
         else:
             oracle.attn_paged(d["q"], d["k_cache"], d["v_cache"], d["real_seqlen_kv"], d["block_table"], causal=True)
     return time.perf_counter() - t0
@@ -442,7 +555,8 @@ def oracle_whole(parts):
 def cpu_baseline(args, parts, peaks):
     import oracle
     ideal = sum(p.ideal_s(peaks) for p in parts)
-    if sum(p.flops for p in parts) < 2e12:       # the whole step takes seconds on the host cores
+    if sum(p.flops for p in parts) < 2e12 and all(p.kind in ("dense", "paged") for p in parts):
+        # the whole step takes seconds on the host cores
         est = oracle_whole(parts)
         desc = "the whole step (%s), every row, once" % " + ".join(p.name for p in parts)
     else:

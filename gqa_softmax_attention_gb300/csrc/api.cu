@@ -293,13 +293,14 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
 
 // ---------------------------------------------------------------- packed calls
 // Workspace of a packed call: a 16-byte header holding the entry count, then
-// up to max_entries row-block entries of 32 bytes.
+// two arrays of up to max_entries row-block entries of 32 bytes (as listed,
+// and ordered by cost).
 static int varlen_max_entries(int B, int total_q, int qpb) { return total_q / qpb + B + 1; }
 
 static size_t varlen_ws_bytes(int B, int total_q, int Hq, int Hkv) {
     if (B <= 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > 128) return 0;
     const int qpb = 128 / (Hq / Hkv);
-    return 16 + (size_t)varlen_max_entries(B, total_q, qpb) * 32;
+    return 16 + 2 * (size_t)varlen_max_entries(B, total_q, qpb) * 32;
 }
 
 size_t attn_varlen_workspace_size(int B, int total_q, int Hq, int Hkv) {
@@ -370,8 +371,8 @@ gqa_status attn_fwd_varlen(const void* q, const void* k, const void* v, const in
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int max_e = varlen_max_entries(B, total_q, a.qpb);
     int32_t* ws = static_cast<int32_t*>(workspace);
-    if (gqa::launch_varlen_plan(cu_seqlens_q, cu_seqlens_kv, false, B, a.qpb, total_q, total_kv, ws + 4, ws, max_e,
-                                s) != cudaSuccess)
+    if (gqa::launch_varlen_plan(cu_seqlens_q, cu_seqlens_kv, false, B, a.qpb, a.g, a.causal, total_q, total_kv,
+                                ws + 4 + (size_t)max_e * 8, ws + 4, ws, max_e, s) != cudaSuccess)
         return GQA_ERR_CUDA;
     return gqa::launch_varlen_packed(tq, tk, tv, to, a, (long)max_e * Hkv, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -407,8 +408,9 @@ gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cach
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int max_e = varlen_max_entries(B, total_q, a.qpb);
     int32_t* ws = static_cast<int32_t*>(workspace);
-    if (gqa::launch_varlen_plan(cu_seqlens_q, cache_seqlens, true, B, a.qpb, total_q, (long)max_pages * page_size,
-                                ws + 4, ws, max_e, s) != cudaSuccess)
+    if (gqa::launch_varlen_plan(cu_seqlens_q, cache_seqlens, true, B, a.qpb, a.g, a.causal, total_q,
+                                (long)max_pages * page_size, ws + 4 + (size_t)max_e * 8, ws + 4, ws, max_e,
+                                s) != cudaSuccess)
         return GQA_ERR_CUDA;
     return gqa::launch_varlen_paged(tq, tk, tv, to, a, (long)max_e * Hkv, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }

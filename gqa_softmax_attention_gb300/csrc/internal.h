@@ -52,13 +52,14 @@ cudaError_t launch_prefill_d256(const CUtensorMap& tm_q, const CUtensorMap& tm_k
 int prefill_d256_take_device_error();
 
 // Packed calls (varlen_packed.cu, varlen_paged.cu; onetile.cuh).  The plan
-// kernel lists the (request, row block) entries of a call into `entries`
-// ([max_entries, 8] int32) and their count into *n_entries; kv holds
-// cu_seqlens_kv [B + 1] (packed keys) or cache_seqlens [B] (paged), and kv_cap
-// bounds a request's key count (total_kv, or max_pages * page_size).
-cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int total_q,
-                               long kv_cap, int32_t* entries, int32_t* n_entries, int max_entries,
-                               cudaStream_t stream);
+// kernel lists the (request, row block) entries of a call into `tmp`, then
+// into `entries` ([max_entries, 8] int32 each) ordered by estimated cost,
+// heaviest first, and their count into *n_entries; kv holds cu_seqlens_kv
+// [B + 1] (packed keys) or cache_seqlens [B] (paged), and kv_cap bounds a
+// request's key count (total_kv, or max_pages * page_size).
+cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int g, int causal,
+                               int total_q, long kv_cap, int32_t* tmp, int32_t* entries, int32_t* n_entries,
+                               int max_entries, cudaStream_t stream);
 // tm_q / tm_o: {D, Hq, total_q} with a {64, g, qpb} box.  Packed: tm_k / tm_v
 // {D, Hkv, total_kv} with {64, 1, 128} and {64, 1, 128 or 64 (D = 256)} boxes.
 // Paged: the caches as {64, 8, D / 64, pages * page_size / 8, Hkv} with

@@ -149,10 +149,9 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int qpb = PACKED ? a.qpb : BM;         // queries per block
     const int n_e = PACKED ? *a.n_entries : 0;
     // Work items.  kBSHD: heaviest (last) query tiles first, adjacent items on
-    // one KV head.  Packed: item w = (KV head w / n_e, row block w % n_e); a
-    // request's row blocks are listed last-first, so adjacent items share
-    // the request's keys.  Round r takes item r * G + cta (even r) or
-    // r * G + G - 1 - cta (odd r).
+    // one KV head.  Packed: item w = (row block w / Hkv, KV head w % Hkv), the
+    // row blocks ordered by estimated cost, heaviest first.  Round r takes
+    // item r * G + cta (even r) or r * G + G - 1 - cta (odd r).
     const int n_items = PACKED ? n_e * a.Hkv : n_qtiles * a.B * a.Hq;
     const int G = gridDim.x;
     const int cta = blockIdx.x;
@@ -171,10 +170,10 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto describe = [&](int w) {
         Item it;
         if constexpr (PACKED) {
-            const int4* e = reinterpret_cast<const int4*>(a.entries + (size_t)(w % n_e) * ENTRY_INTS);
+            const int4* e = reinterpret_cast<const int4*>(a.entries + (size_t)(w / a.Hkv) * ENTRY_INTS);
             const int4 e0 = e[0], e1 = e[1];
             it.b = e0.x;
-            it.hkv = w / n_e;
+            it.hkv = w % a.Hkv;
             it.hq = it.hkv * g;
             it.qs = e0.z;
             it.sq = e0.w;

@@ -9,19 +9,37 @@
 namespace gqa {
 namespace {
 
-// One CTA of 1024 threads.  Request b gets ceil(Sq_b / qpb) entries, last
-// block first (its rows see the most keys); entries are laid out request by
-// request.  Offsets are clamped into [0, total] and lengths into [0, kv_cap],
-// so malformed metadata can give wrong results but no access out of range;
-// entries past max_entries are dropped.
+// One CTA of 1024 threads.  Request b gets ceil(Sq_b / qpb) entries
+// {b, q0, qs, Sq_b, ks, L_b}.  Offsets are clamped into [0, total] and
+// lengths into [0, kv_cap], so malformed metadata can give wrong results but
+// no access out of range; entries past max_entries are dropped.  The entries
+// are then ordered by estimated cost, heaviest first (a counting sort over
+// NBUCKET cost buckets), so that the persistent grid's snake order hands
+// out long decode streams and late causal blocks before short ones.
+constexpr int NBUCKET = 2048;
+
+__device__ __forceinline__ int entry_cost(const int4 e0, const int4 e1, int qpb, int g, int causal) {
+    const int q0 = e0.y, sq = e0.w, L = e1.y;
+    const int nq = min(qpb, sq - q0);
+    const int last = q0 + nq - 1;                         // last query of the block
+    const int keys = causal ? max(0, min(L, last + L - sq + 1)) : L;
+    const int tiles = (keys + 127) / 128;
+    // a block with few rows streams its keys at memory speed: weigh its tiles more
+    return min(NBUCKET - 1, tiles * (nq * g >= 64 ? 2 : 3));
+}
+
 __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, const int32_t* kv, int paged,
-                                                          int B, int qpb, int total_q, long kv_cap,
-                                                          int32_t* entries, int32_t* n_entries, int max_entries) {
+                                                          int B, int qpb, int g, int causal, int total_q,
+                                                          long kv_cap, int32_t* tmp, int32_t* entries,
+                                                          int32_t* n_entries, int max_entries) {
     __shared__ int warp_sum[32];
     __shared__ int base;
+    __shared__ int bucket[NBUCKET];
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
     if (threadIdx.x == 0) base = 0;
+    for (int i = threadIdx.x; i < NBUCKET; i += 1024) bucket[i] = 0;
     __syncthreads();
+    // 1. entries in request order
     for (int b0 = 0; b0 < B; b0 += 1024) {
         const int b = b0 + threadIdx.x;
         int qs = 0, sq = 0, ks = 0, L = 0, nrb = 0;
@@ -58,24 +76,69 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
         for (int k = 0; k < nrb; ++k) {
             const int e = first + k;
             if (e >= max_entries) break;
-            int4* dst = reinterpret_cast<int4*>(entries + (size_t)e * ot::ENTRY_INTS);
-            dst[0] = make_int4(b, (nrb - 1 - k) * qpb, qs, sq);
+            int4* dst = reinterpret_cast<int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
+            dst[0] = make_int4(b, k * qpb, qs, sq);
             dst[1] = make_int4(ks, L, 0, 0);
         }
         __syncthreads();
         if (threadIdx.x == 1023) base = first + nrb;
         __syncthreads();
     }
-    if (threadIdx.x == 0) *n_entries = min(base, max_entries);
+    const int n = min(base, max_entries);
+    // 2. counting sort by cost, heaviest first
+    for (int e = threadIdx.x; e < n; e += 1024) {
+        const int4* src = reinterpret_cast<const int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
+        atomicAdd(&bucket[entry_cost(src[0], src[1], qpb, g, causal)], 1);
+    }
+    __syncthreads();
+    {
+        // bucket starts in descending cost order: thread t owns buckets
+        // NBUCKET-1-2t and NBUCKET-2-2t; an exclusive block scan over threads
+        static_assert(NBUCKET == 2 * 1024, "two buckets per thread");
+        const int c1 = NBUCKET - 1 - 2 * threadIdx.x, c2 = c1 - 1;
+        const int n1 = bucket[c1], n2 = bucket[c2];
+        int x = n1 + n2;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        __syncthreads();                               // warp_sum is free again
+        if (lane == 31) warp_sum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int t = warp_sum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o) t += y;
+            }
+            warp_sum[lane] = t;
+        }
+        __syncthreads();
+        const int start = (warp > 0 ? warp_sum[warp - 1] : 0) + x - n1 - n2;
+        bucket[c1] = start;
+        bucket[c2] = start + n1;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < n; e += 1024) {
+        const int4* src = reinterpret_cast<const int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
+        const int4 e0 = src[0], e1 = src[1];
+        const int pos = atomicAdd(&bucket[entry_cost(e0, e1, qpb, g, causal)], 1);
+        int4* dst = reinterpret_cast<int4*>(entries + (size_t)pos * ot::ENTRY_INTS);
+        dst[0] = e0;
+        dst[1] = e1;
+    }
+    if (threadIdx.x == 0) *n_entries = n;
 }
 
 }  // namespace
 
-cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int total_q,
-                               long kv_cap, int32_t* entries, int32_t* n_entries, int max_entries,
-                               cudaStream_t stream) {
-    varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_q, kv, paged ? 1 : 0, B, qpb, total_q, kv_cap, entries, n_entries,
-                                               max_entries);
+cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int g, int causal,
+                               int total_q, long kv_cap, int32_t* tmp, int32_t* entries, int32_t* n_entries,
+                               int max_entries, cudaStream_t stream) {
+    varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_q, kv, paged ? 1 : 0, B, qpb, g, causal, total_q, kv_cap, tmp,
+                                               entries, n_entries, max_entries);
     return cudaGetLastError();
 }
 

@@ -47,6 +47,15 @@ WORKLOADS = {
                                  causal=True, sigma=0.5, mask_lengths=None),
     "wide_group_prefill": dict(kind="dense", B=2, Hq=24, Hkv=2, Sq=8192, Skv=8192, D=256,
                                causal=True, sigma=1.0, mask_lengths=None),
+    # packed (THD) self-attention prefill of 16 requests of mixed length
+    "varlen_prefill": dict(kind="varlen", B=16, Hq=32, Hkv=8, D=128, causal=True, sigma=1.0,
+                           lengths=(256, 8192)),
+    # one serving step over a paged cache: 60 decode steps (one query each,
+    # cache lengths U[1024, 16384]) and 4 prefill chunks of 1024 queries whose
+    # caches hold U[0, 8192] earlier tokens plus the chunk
+    "mixed_serving_batch": dict(kind="paged_varlen", B=64, Hq=32, Hkv=8, D=128, page_size=64, causal=True,
+                                sigma=1.0, decode_lengths=(1024, 16384), prefill_chunks=4, chunk=1024,
+                                context=(0, 8192)),
 }
 
 
@@ -160,11 +169,35 @@ def varlen_paged_inputs(q_lens, lengths, Hq, Hkv, D, page_size, spare=0.10, sigm
     return p
 
 
+def mixed_lengths(cfg, seed=0):
+    """Per-request query counts and cache lengths of a paged_varlen workload:
+    requests 0 .. chunks-1 are prefill chunks, the rest single decode steps
+    (lengths on Generator().manual_seed(seed + 1))."""
+    g = torch.Generator().manual_seed(seed + 1)
+    B, nc, chunk = cfg["B"], cfg["prefill_chunks"], cfg["chunk"]
+    lo, hi = cfg["decode_lengths"]
+    clo, chi = cfg["context"]
+    dec = torch.randint(lo, hi + 1, (B - nc,), generator=g).tolist()
+    ctx = torch.randint(clo, chi + 1, (nc,), generator=g).tolist()
+    q_lens = [chunk] * nc + [1] * (B - nc)
+    lengths = [c + chunk for c in ctx] + dec
+    return q_lens, lengths
+
+
 def make(name, seed=0):
     """Inputs of a named workload plus its shape description."""
     cfg = dict(WORKLOADS[name])
     if cfg["kind"] == "dense":
         data = dense_inputs(seed=seed, **cfg)
+    elif cfg["kind"] == "varlen":
+        g = torch.Generator().manual_seed(seed + 1)
+        lo, hi = cfg["lengths"]
+        lens = torch.randint(lo, hi + 1, (cfg["B"],), generator=g).tolist()
+        data = varlen_inputs(lens, lens, cfg["Hq"], cfg["Hkv"], cfg["D"], sigma=cfg["sigma"], seed=seed)
+    elif cfg["kind"] == "paged_varlen":
+        q_lens, lengths = mixed_lengths(cfg, seed)
+        data = varlen_paged_inputs(q_lens, lengths, cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["page_size"],
+                                   sigma=cfg["sigma"], seed=seed)
     else:
         data = paged_inputs(seed=seed, **cfg)
     data["config"] = cfg

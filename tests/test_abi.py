@@ -121,9 +121,9 @@ def test_varlen_argument_checks(lib):
     assert paged_varlen(lib, D=80) == UNSUPPORTED
     assert paged_varlen(lib, ws=None, ws_bytes=0) == WORKSPACE
     assert paged_varlen(lib, total_q=0) == OK
-    # workspace: a header and one 32-byte entry per possible row block
-    assert lib.attn_varlen_workspace_size(2, 8, 4, 2) == 16 + 32 * (8 // 64 + 2 + 1)
-    assert lib.attn_varlen_workspace_size(3, 1000, 24, 2) == 16 + 32 * (1000 // 10 + 3 + 1)   # g = 12: 10 queries
+    # workspace: a header and two 32-byte entries per possible row block
+    assert lib.attn_varlen_workspace_size(2, 8, 4, 2) == 16 + 64 * (8 // 64 + 2 + 1)
+    assert lib.attn_varlen_workspace_size(3, 1000, 24, 2) == 16 + 64 * (1000 // 10 + 3 + 1)   # g = 12: 10 queries
     assert lib.attn_varlen_workspace_size(2, 8, 6, 4) == 0
 
 
