@@ -577,14 +577,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const size_t part_row = (size_t)id * R + r;
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    float o[32];
-                    __syncwarp();                          // tcgen05.ld is warp-collective: reconverge
+                for (int cc = 0; cc < D / 32; cc += 2) {
+                    float o[64];
+                    __syncwarp();                          // tcgen05.ld is warp-collective: reconverge (two loads per pass)
                     tmem_ld32(tmem + lane_addr + C::COL_O + 32 * cc, o);
+                    tmem_ld32(tmem + lane_addr + C::COL_O + 32 * cc + 32, o + 32);
                     if (row_ok) {
                         float4* dst = reinterpret_cast<float4*>(a.part_o + part_row * D + 32 * cc);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
+                        for (int e = 0; e < 16; ++e)
                             dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv,
                                                  o[4 * e + 3] * inv);
                     }
