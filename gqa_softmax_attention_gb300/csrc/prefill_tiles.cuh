@@ -115,10 +115,10 @@ __device__ __forceinline__ uint32_t below_bits(int n, int chunk) {
     return rel >= 32 ? 0xffffffffu : (rel <= 0 ? 0u : ((1u << rel) - 1u));
 }
 
-// p[c] = 2^(s[c] * fa - m_use) for one 128-column row: P packed to bf16x2 in
+// p[c] = 2^(s[c] * fa - m_use) for NCOL (default 128) columns of a row: P packed to bf16x2 in
 // pk, the row sum returned.  Two columns per paired FMA / add; with POLY > 0,
 // one column pair in POLY is evaluated on the FMA pipe instead of the MUFU.
-template <int POLY, bool F16>
+template <int POLY, bool F16, int NCOL = BN>
 __device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, uint32_t* pk) {
     const uint64_t fa2 = f32x2(fa, fa);
     const uint64_t nm2 = f32x2(-m_use, -m_use);
@@ -126,7 +126,7 @@ __device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, 
 #pragma unroll
     for (int e = 0; e < 4; ++e) rs4[e] = f32x2(0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < BN / 2; ++c) {
+    for (int c = 0; c < NCOL / 2; ++c) {
         float x0, x1, p0, p1;
         f32x2_split(ffma2(f32x2(s[2 * c], s[2 * c + 1]), fa2, nm2), x0, x1);
         if (POLY > 0 && c % (POLY > 0 ? POLY : 1) == (POLY > 0 ? POLY : 1) - 1) {
