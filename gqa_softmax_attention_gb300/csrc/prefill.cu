@@ -54,11 +54,12 @@ constexpr int NUM_THREADS = 384;   // warps 0-7 softmax, 8 producer, 9 MMA, 10-1
 constexpr int WARP_LOAD = 8;
 constexpr int WARP_MMA = 9;
 // Registers per thread: the launch gives 168 to all 384 threads (64,512); the
-// producer/MMA warpgroup gives back 80 each, which the two softmax
-// warpgroups take: 208 * 256 + 88 * 128 = 64,512, the launch total.
+// two softmax warpgroups take 192 each and the producer/MMA warpgroup keeps
+// 120 (its peeled issue loop needs them; measured best of 208/88 ... 176/152):
+// 192 * 256 + 120 * 128 = 64,512, the launch total.
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsSoftmax = 208;
-constexpr int kRegsOther = 88;
+constexpr int kRegsSoftmax = 192;
+constexpr int kRegsOther = 120;
 static_assert(kRegsSoftmax * 256 + kRegsOther * 128 <= kRegsLaunch * NUM_THREADS, "register split");
 // One exponential pair in kPolyEvery goes to the FMA-pipe exp2 on unmasked
 // tiles (0: all on the MUFU).
@@ -329,10 +330,73 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         if (c1 > 0) issue_s(1, kt % C::NK);
                         mma_commit(k_empty(kt % C::NK));
                     }
+                    // Common causal case (Q1 sees Q0's tiles, plus at most one more):
+                    // the loop is peeled where Q0 ends, so that o_final(0) is
+                    // committed right after Q0's last P V and Q0's epilogue
+                    // overlaps Q1's last tile, with no conditional in the loop.
+                    const bool peel = c0 >= 1 && c1 == c_all && (c1 == c0 || c1 == c0 + 1);
+                    if (peel && ok) {
+                        auto pv = [&](int k, int vs, int i) -> bool {
+                            const int pc = k == 0 ? pc0++ : pc1++;
+                            if (!mbar_wait(p_full(k), pc & 1, abort_flag)) return false;
+                            tc_fence_after();
+                            issue_pv(k, vs, i);
+                            return true;
+                        };
+                        auto wait_k = [&](int kn) -> bool {
+                            if (!mbar_wait(k_full(kn % C::NK), (kn / C::NK) & 1, abort_flag)) return false;
+                            tc_fence_after();
+                            return true;
+                        };
+                        // tiles 0 .. c0-2: both Q tiles take P V of tile i and S of tile i+1
+                        for (int i = 0; i + 1 < c0 && ok; ++i) {
+                            const int vs = (vt + i) % C::NV;
+                            const int kn = kt + i + 1;
+                            ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
+                            if (ok) ok = pv(0, vs, i);
+                            if (ok) ok = wait_k(kn);
+                            if (!ok) break;
+                            issue_s(0, kn % C::NK);
+                            if (!pv(1, vs, i)) { ok = false; break; }
+                            issue_s(1, kn % C::NK);
+                            mma_commit(v_empty(vs));
+                            mma_commit(k_empty(kn % C::NK));
+                        }
+                        // tile c0-1: Q0's last P V, then its epilogue may start
+                        const int i = c0 - 1;
+                        const int vs = (vt + i) % C::NV;
+                        if (ok) ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
+                        if (ok) ok = pv(0, vs, i);
+                        if (ok) mma_commit(o_final(0));
+                        if (ok && c1 == c0 + 1) {
+                            const int kn = kt + c0;
+                            ok = wait_k(kn);
+                            if (ok) ok = pv(1, vs, i);
+                            if (ok) {
+                                issue_s(1, kn % C::NK);
+                                mma_commit(v_empty(vs));
+                                mma_commit(k_empty(kn % C::NK));
+                                mma_commit(q_empty(0));
+                                mma_commit(q_empty(1));
+                                const int vs2 = (vt + c0) % C::NV;
+                                ok = mbar_wait(v_full(vs2), ((vt + c0) / C::NV) & 1, abort_flag);
+                                if (ok) ok = pv(1, vs2, c0);
+                                if (ok) mma_commit(v_empty(vs2));
+                            }
+                        } else if (ok) {
+                            mma_commit(q_empty(0));
+                            mma_commit(q_empty(1));
+                            ok = pv(1, vs, i);
+                            if (ok) mma_commit(v_empty(vs));
+                        }
+                        if (ok) mma_commit(o_final(1));
+                        kt += c_all;
+                        vt += c_all;
+                    }
                     // Visited tiles 0 .. c_all-2: P V of tile i, then S of tile i+1.
                     // The item's commits of q_empty / o_final come after the loop:
                     // conditional commits inside it slowed the steady state.
-                    for (int i = 0; i + 1 < c_all && ok; ++i) {
+                    for (int i = 0; !peel && i + 1 < c_all && ok; ++i) {
                         const int vs = (vt + i) % C::NV;
                         ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
                         if (!ok) break;
@@ -359,12 +423,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         mma_commit(k_empty(kn % C::NK));
                     }
                     // every S of the item is issued: its Q tiles may be replaced
-                    if (ok) {
+                    if (!peel && ok) {
                         if (c0 > 0) mma_commit(q_empty(0));
                         if (c1 > 0) mma_commit(q_empty(1));
                     }
                     // the last visited tile: P V only
-                    if (ok) {
+                    if (!peel && ok) {
                         const int i = c_all - 1;
                         const int vs = (vt + i) % C::NV;
                         ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
@@ -379,13 +443,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             }
                         }
                         if (ok) mma_commit(v_empty(vs));
+                        kt += c_all;
+                        vt += c_all;
+                        if (ok) {
+                            mma_commit(o_final(0));
+                            mma_commit(o_final(1));
+                        }
                     }
-                    kt += c_all;
-                    vt += c_all;
                 }
                 // one o_final phase per Q tile and item (also for a tile with no key):
                 // arrives when every MMA of the item has completed
-                if (lane == 0 && ok) {
+                if (lane == 0 && ok && c_all == 0) {
                     mma_commit(o_final(0));
                     mma_commit(o_final(1));
                 }
