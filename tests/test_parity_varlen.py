@@ -181,3 +181,33 @@ def test_mixed_serving_batch_sampled(g):
             ro, rl = oracle.attn_paged_varlen(p["q"][qs + i:qs + i + 1], p["k_cache"], p["v_cache"], one, Li,
                                               p["block_table"][b:b + 1], causal=True)
             compare(o[qs + i:qs + i + 1], lse[qs + i:qs + i + 1], ro, rl, "request %d row %d" % (b, i))
+
+
+def test_many_requests_plan(g):
+    """More requests than the plan kernel's 1024 threads (its scan runs in
+    chunks) and a cache shorter than the query count (leading rows see no key)."""
+    gen = torch.Generator().manual_seed(21)
+    B = 1500
+    ql = torch.randint(0, 3, (B,), generator=gen).tolist()
+    L = [max(1, int(x)) for x in torch.randint(1, 200, (B,), generator=gen)]
+    L[7], ql[7] = 2, 3                                   # Sq > L: the first query sees nothing
+    p = W.varlen_paged_inputs(ql, L, 4, 2, 64, 8, seed=3)
+    o, lse = g.paged(p["q"].cuda(), p["k_cache"].cuda(), p["v_cache"].cuda(), p["cu_seqlens_q"].cuda(),
+                     p["cache_seqlens"].cuda(), p["block_table"].cuda(), causal=True)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn_paged_varlen(p["q"], p["k_cache"], p["v_cache"], p["cu_seqlens_q"], p["cache_seqlens"],
+                                      p["block_table"], causal=True)
+    compare(o.cpu(), lse.cpu(), ro, rl, "1500 requests")
+    qs = int(p["cu_seqlens_q"][7])
+    assert bool(torch.isneginf(lse[qs, :].cpu()).all())
+
+
+def test_varlen_two_sided_window_noncausal(g):
+    ql, kl, Hq, Hkv, D = [60, 200, 5], [300, 200, 90], 6, 3, 128
+    d = W.varlen_inputs(ql, kl, Hq, Hkv, D, seed=12)
+    o, lse = g.varlen(*[d[n].cuda() for n in ("q", "k", "v", "cu_seqlens_q", "cu_seqlens_kv")], causal=False,
+                      window_left=40, window_right=17)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_kv"], causal=False,
+                                window_left=40, window_right=17)
+    compare(o.cpu(), lse.cpu(), ro, rl, "two-sided window")
