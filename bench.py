@@ -104,10 +104,14 @@ def load_peaks():
 # workloads as a ratio to the algorithmic K/V bytes (their captures ran at a
 # reduced batch), for the prefill as bytes per launch of the same workload.
 TRAFFIC = {
-    "paged_decode": ("ratio", (559.396864 + 5.465344) / 556.916736),
-    "wide_group_decode": ("ratio", (233.606656 + 4.270080) / 232.683520),
-    "qwen3_8b_prefill": ("bytes", (93.515776 + 30.323200) * 1e6),
-    "wide_group_prefill": ("bytes", (235.172608 + 160.694528) * 1e6),
+    "paged_decode": ("ratio", (559.378944 + 5.455360) / 556.916736),
+    "wide_group_decode": ("ratio", (233.700096 + 3.488000) / 232.683520),
+    "qwen3_8b_prefill": ("bytes", (94.945280 + 31.452928) * 1e6),
+    "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
+    # captured at B=1 of 4 independent batches: traffic scales by 4
+    "long_chunked_prefill": ("bytes", 4 * (537.318144 + 34.280704) * 1e6),
+    "mixed_serving_batch": ("bytes", (2583.485 + 24.447744) * 1e6),
+    "varlen_prefill": ("bytes", (6572.479 + 507.1168) * 1e6),
 }
 
 
@@ -406,7 +410,8 @@ def bench_ours(args, world, rank, local):
                     peak_source=peaks["source"] + " bf16 burst")
     elif dom.kind == "dense":
         ach = dom.flops / dom_t / 1e12
-        kname = "prefill_d256_kernel" if dom.data["config"]["D"] == 256 else "prefill_kernel<%d>" % dom.data["config"]["D"]
+        kname = ("onetile_kernel<256,kBSHD>" if dom.data["config"]["D"] == 256
+                 else "prefill_kernel<%d>" % dom.data["config"]["D"])
         roof = dict(kernel=kname + " (" + dom.name + ")", bound="tensor", achieved=ach,
                     peak=peaks["bf16_tflops"], unit="TFLOP/s", frac=ach / peaks["bf16_tflops"],
                     traffic=traffic_per_launch(dom), peak_source=peaks["source"] + " bf16 burst")
