@@ -1,0 +1,77 @@
+"""The paged calls keep their metadata on the device and allocate nothing when
+given their buffers, so they can be captured in a CUDA graph once and
+replayed with new lengths and tables (TileOPs GQAPagedFwdOp: device lengths
+stay live replay inputs; choosing and preparing the path needs no host
+read-back).  Each replay is checked against the FP64 oracle."""
+import pytest
+import torch
+
+import oracle
+from gqa_softmax_attention_gb300 import workloads as W
+
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from gqa_softmax_attention_gb300 import build
+    build.build()
+    import gqa_softmax_attention_gb300 as m
+    yield m
+    m.gqa_device_error()
+
+
+def test_paged_decode_graph_replay(g):
+    B, Sq, Hq, Hkv, D, ps = 8, 1, 32, 8, 128, 64
+    p = W.paged_inputs(B, Sq, Hq, Hkv, D, ps, lengths=[4000] * B, seed=1)
+    dev = {n: p[n].cuda() for n in ("q", "k_cache", "v_cache", "real_seqlen_kv", "block_table")}
+    ws = torch.empty(g.attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, ps, p["block_table"].shape[1]),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dev["q"])
+    lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device="cuda")
+    run = lambda: g.decode_paged(dev["q"], dev["k_cache"], dev["v_cache"], dev["real_seqlen_kv"],
+                                 dev["block_table"], causal=True, workspace=ws, out=out, lse=lse)
+    run()                                      # first call outside capture (loads the library, sets attributes)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    gen = torch.Generator().manual_seed(2)
+    for _ in range(3):
+        lens = torch.randint(1, 4001, (B,), generator=gen, dtype=torch.int32)
+        dev["real_seqlen_kv"].copy_(lens)
+        graph.replay()
+        torch.cuda.synchronize()
+        ro, rl = oracle.attn_paged(p["q"], p["k_cache"], p["v_cache"], lens, p["block_table"], causal=True)
+        compare(out.cpu(), lse.cpu(), ro, rl, "decode replay")
+
+
+def test_mixed_paged_graph_replay(g):
+    ql, L = [1, 300, 1, 4], [2000, 700, 50, 1000]
+    Hq, Hkv, D, ps = 8, 2, 128, 16
+    p = W.varlen_paged_inputs(ql, L, Hq, Hkv, D, ps, seed=4)
+    names = ("q", "k_cache", "v_cache", "cu_seqlens_q", "cache_seqlens", "block_table")
+    dev = {n: p[n].cuda() for n in names}
+    ws = torch.empty(g.attn_varlen_workspace_size(len(ql), p["q"].shape[0], Hq, Hkv), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dev["q"])
+    lse = torch.empty((p["q"].shape[0], Hq), dtype=torch.float32, device="cuda")
+    run = lambda: g.paged(*[dev[n] for n in names], causal=True, out=out, lse=lse, workspace=ws)
+    run()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    # new cache lengths (still >= each request's query count) and a new query split
+    for lens, cu in (([2000, 700, 50, 1000], [0, 1, 301, 302, 306]), ([17, 400, 1, 999], [0, 1, 301, 302, 306]),
+                     ([1500, 305, 30, 10], [0, 0, 300, 302, 306])):
+        dev["cache_seqlens"].copy_(torch.tensor(lens, dtype=torch.int32))
+        dev["cu_seqlens_q"].copy_(torch.tensor(cu, dtype=torch.int32))
+        graph.replay()
+        torch.cuda.synchronize()
+        ro, rl = oracle.attn_paged_varlen(p["q"], p["k_cache"], p["v_cache"], torch.tensor(cu, dtype=torch.int32),
+                                          torch.tensor(lens, dtype=torch.int32), p["block_table"], causal=True)
+        compare(out.cpu(), lse.cpu(), ro, rl, "mixed replay %s" % lens)
