@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(DCfg<D, MF, true, F16>::NT)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeArgs a, int R, int g, int n_rowblk, int box_tokens) {
     using C = DCfg<D, MF, true, F16>;
+    griddep_launch_dependents();                 // the combine may be scheduled (it waits for this grid)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -462,6 +463,7 @@ template <int D, int MF, bool F16>
 __global__ void __launch_bounds__(DCfg<D, MF, false, F16>::NT)
 decode_gather_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
     using C = DCfg<D, MF, false, F16>;
+    griddep_launch_dependents();                 // the combine may be scheduled (it waits for this grid)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -527,6 +529,9 @@ decode_gather_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
 
 template <int D, bool F16>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a, int R, int g) {
+    // launched as a programmatic dependent of the split kernel: its partials
+    // are complete and visible past this point
+    griddep_wait();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const long row = (long)blockIdx.x * 4 + warp;
     const long total = (long)a.B * a.Sq * a.Hq;
@@ -595,6 +600,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
     }
     float accv[PER][4] = {};
     float den = s2 == -INFINITY ? 0.f : fast_exp2(s2 - M);
+    // four pieces per pass so that their loads are in flight together
+#pragma unroll 4
     for (int s = 0; s < n; ++s) {
         const size_t pr = base + (size_t)s * R;
         const float w = fast_exp2(a.part_lse[pr] - M);
@@ -727,27 +734,41 @@ bool plan_decode(int B, int Sq, int Hq, int Hkv, int D, int page_size, int max_p
     return true;
 }
 
+namespace {
+// The combine runs as a programmatic dependent launch of the split kernel:
+// its blocks are scheduled while the split kernel finishes (every split kernel
+// lets its dependents go at its start) and wait in griddep_wait(), so no launch
+// gap separates the two.
+template <int D, bool F16>
+cudaError_t launch_combine_t(const DecodeArgs& a, int R, int g, unsigned blocks, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, F16>, a, R, g);
+}
+}  // namespace
+
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream) {
     const int g = a.Hq / a.Hkv;
     const int R = g * a.Sq;
     const long rows = (long)a.B * a.Sq * a.Hq;
     const unsigned blocks = (unsigned)((rows + 3) / 4);
-    switch (a.D) {
-        case 64:
-            if (a.f16) decode_combine_kernel<64, true><<<blocks, 128, 0, stream>>>(a, R, g);
-            else decode_combine_kernel<64, false><<<blocks, 128, 0, stream>>>(a, R, g);
-            break;
-        case 128:
-            if (a.f16) decode_combine_kernel<128, true><<<blocks, 128, 0, stream>>>(a, R, g);
-            else decode_combine_kernel<128, false><<<blocks, 128, 0, stream>>>(a, R, g);
-            break;
-        case 256:
-            if (a.f16) decode_combine_kernel<256, true><<<blocks, 128, 0, stream>>>(a, R, g);
-            else decode_combine_kernel<256, false><<<blocks, 128, 0, stream>>>(a, R, g);
-            break;
+    switch (a.D * 2 + (a.f16 ? 1 : 0)) {
+        case 64 * 2: return launch_combine_t<64, false>(a, R, g, blocks, stream);
+        case 64 * 2 + 1: return launch_combine_t<64, true>(a, R, g, blocks, stream);
+        case 128 * 2: return launch_combine_t<128, false>(a, R, g, blocks, stream);
+        case 128 * 2 + 1: return launch_combine_t<128, true>(a, R, g, blocks, stream);
+        case 256 * 2: return launch_combine_t<256, false>(a, R, g, blocks, stream);
+        case 256 * 2 + 1: return launch_combine_t<256, true>(a, R, g, blocks, stream);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int box_tokens,

@@ -177,6 +177,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     constexpr uint32_t IDESC_QK = make_idesc_16<F16>(BM, BN, false, false);
     constexpr uint32_t IDESC_PV = make_idesc_16<F16>(BM, D, false, true);
     const int cta = blockIdx.x;
+    griddep_launch_dependents();                 // the combine may be scheduled (it waits for this grid)
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
