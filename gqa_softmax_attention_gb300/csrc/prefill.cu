@@ -78,10 +78,12 @@ struct Cfg {
     static constexpr int OFF_STAGE = OFF_V + NV * TILE_BYTES;   // one 64-column output box per Q tile
     static constexpr int OFF_BAR = OFF_STAGE + NQ * SUB_BYTES;
     // q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-    // s_full[2], p_full[2], o_final[2], drain
-    static constexpr int NBAR = 4 + 2 * NK + 2 * NV + 6 + 1;
+    // s_full[2], p_full[2], o_final[2], drain, info_full[2], info_empty[2]
+    static constexpr int NBAR = 4 + 2 * NK + 2 * NV + 6 + 1 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_USED = OFF_MISC + 16;
+    // two 32-byte item records (tile counts, first flag word, first tile's mask words)
+    static constexpr int OFF_INFO = OFF_MISC + 16;
+    static constexpr int SMEM_USED = OFF_INFO + 2 * 32;
     // 1 KB alignment slack; at least 120 KB so that one CTA holds an SM (it
     // takes all 512 TMEM columns).
     static constexpr int SMEM_BYTES = SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
@@ -155,10 +157,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // Visited key tiles of an item (non-empty, from its first tile to kv_end of
     // either Q tile) are numbered i = 0, 1, ...; Q_k takes part in the first c_k
     // of them.  Warp-collective.
-    auto count_tiles = [&](const Item& it, int& c0, int& c1, int& c_all) {
+    auto count_tiles = [&](const Item& it, int& c0, int& c1, int& c_all, uint32_t& f0) {
         c0 = c1 = c_all = 0;
+        f0 = 0;
         for (int chunk = it.first / 32; chunk * 32 < it.n_all; ++chunk) {
             const uint32_t f = tile_flags(it.mrow, chunk, it.first, it.n_all, it.kv_end_all, lane);
+            if (chunk == it.first / 32) f0 = f;
             c_all += __popc(f);
             c0 += __popc(f & below_bits(it.t0.n_tiles, chunk));
             c1 += __popc(f & below_bits(it.t1.n_tiles, chunk));
@@ -176,6 +180,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto p_full = [&](int k) { return bar0 + 8u * (6 + 2 * C::NK + 2 * C::NV + k); };
     auto o_final = [&](int k) { return bar0 + 8u * (8 + 2 * C::NK + 2 * C::NV + k); };
     const uint32_t drain = bar0 + 8u * (10 + 2 * C::NK + 2 * C::NV);
+    auto info_full = [&](int i) { return bar0 + 8u * (11 + 2 * C::NK + 2 * C::NV + i); };
+    auto info_empty = [&](int i) { return bar0 + 8u * (13 + 2 * C::NK + 2 * C::NV + i); };
+    // Item records, written by the producer one item ahead of its consumers:
+    // c0, c1, c_all, the flag word of the first 32-tile chunk and the mask
+    // words of the first visited tile, so that no consumer scans the padding
+    // mask in global memory at an item boundary.
+    uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -190,6 +201,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int i = 0; i < C::NK; ++i) { mbar_init(k_full(i), 1); mbar_init(k_empty(i), 1); }
         for (int i = 0; i < C::NV; ++i) { mbar_init(v_full(i), 1); mbar_init(v_empty(i), 1); }
         mbar_init(drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(info_full(i), 1);
+            mbar_init(info_empty(i), 1 + 8);   // the MMA thread and the eight softmax warps
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -221,31 +236,50 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (w < 0) break;
                 const Item it = describe(w);
                 int c0, c1, c_all;
-                count_tiles(it, c0, c1, c_all);
-                if (c_all == 0) continue;
+                uint32_t f0;
+                count_tiles(it, c0, c1, c_all, f0);
+                TileIter tiles(it.mrow, it.first, it.n_all, it.kv_end_all, lane, f0);
+                int j = tiles.next();                  // first visited tile, -1 if none
+                uint32_t mw0[4];                       // its kept keys, as the softmax forms them
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int key = j * BN + q * 32 + lane;
+                    const bool keep = it.mrow ? (j >= 0 && key < it.kv_end_all && it.mrow[key] != 0) : true;
+                    mw0[q] = __ballot_sync(0xffffffffu, keep);
+                }
                 if (lane == 0) {
-                    // Q_k of this item once the last S of the previous Q_k is done
+                    const int slot = r & 1;
+                    ok = mbar_wait(info_empty(slot), ((r >> 1) & 1) ^ 1, abort_flag);
+                    if (ok) {
+                        uint32_t* rec = info + 8 * slot;
+                        rec[0] = (uint32_t)c0;
+                        rec[1] = (uint32_t)c1;
+                        rec[2] = (uint32_t)c_all;
+                        rec[3] = f0;
 #pragma unroll
-                    for (int k = 0; k < NQ; ++k) {
-                        const int ck = k == 0 ? c0 : c1;
-                        const int nq = k == 0 ? nq0 : nq1;
-                        if (ck == 0 || !ok) continue;
-                        ok = mbar_wait(q_empty(k), (nq & 1) ^ 1, abort_flag);
-                        if (!ok) break;
-                        mbar_arrive_expect_tx(q_full(k), C::TILE_BYTES);
-#pragma unroll
-                        for (int s = 0; s < C::KSUB; ++s)
-                            tma_load_4d(sb + C::OFF_Q + k * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, q_full(k),
-                                        s * 64, it.q0 + k * BM, it.hq, it.b);
-                        if (k == 0) ++nq0; else ++nq1;
+                        for (int q = 0; q < 4; ++q) rec[4 + q] = mw0[q];
+                        mbar_arrive(info_full(slot));
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                nq0 = __shfl_sync(0xffffffffu, nq0, 0);
-                nq1 = __shfl_sync(0xffffffffu, nq1, 0);
-                if (!ok) break;
-                TileIter tiles(it.mrow, it.first, it.n_all, it.kv_end_all, lane);
-                for (int j = tiles.next(); j >= 0; j = tiles.next()) {
+                if (!ok || c_all == 0) continue;
+                // Load order Q0, K(first), Q1, V(first), K, V, ...: S0 of the first
+                // tile can start before Q1 has landed.  Q_k is loaded once the last
+                // S of the previous Q_k is done.
+                auto load_q = [&](int k) -> bool {   // lane 0
+                    const int nq = k == 0 ? nq0 : nq1;
+                    if (!mbar_wait(q_empty(k), (nq & 1) ^ 1, abort_flag)) return false;
+                    mbar_arrive_expect_tx(q_full(k), C::TILE_BYTES);
+#pragma unroll
+                    for (int s = 0; s < C::KSUB; ++s)
+                        tma_load_4d(sb + C::OFF_Q + k * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, q_full(k),
+                                    s * 64, it.q0 + k * BM, it.hq, it.b);
+                    if (k == 0) ++nq0; else ++nq1;
+                    return true;
+                };
+                if (lane == 0 && c0 > 0) ok = load_q(0);
+                bool q1_due = c1 > 0;
+                for (; j >= 0 && __shfl_sync(0xffffffffu, ok, 0); j = tiles.next()) {
                     if (lane == 0) {
                         const int ks = nk % C::NK;
                         ok = mbar_wait(k_empty(ks), ((nk / C::NK) & 1) ^ 1, abort_flag);
@@ -256,6 +290,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 tma_load_4d(sb + C::OFF_K + ks * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k,
                                             k_full(ks), s * 64, j * BN, it.hkv, it.b);
                             ++nk;
+                        }
+                        if (ok && q1_due) ok = load_q(1);
+                        if (ok) {
                             const int vs = nv % C::NV;
                             ok = mbar_wait(v_empty(vs), ((nv / C::NV) & 1) ^ 1, abort_flag);
                             if (ok) {
@@ -268,9 +305,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             }
                         }
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) break;
+                    q1_due = false;
                 }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
             }
             if (lane == 0 && *abort_flag) {
                 // Let copies already in flight land before the CTA goes away:
@@ -292,12 +329,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             int nq0 = 0, nq1 = 0, pc0 = 0, pc1 = 0;   // Q loads consumed, P tiles taken
             bool ok = true;
             for (int r = 0; ok; ++r) {
-                const int w = item_of(r);
-                if (w < 0) break;
-                const Item it = describe(w);
-                int c0, c1, c_all;
-                count_tiles(it, c0, c1, c_all);
-                if (lane == 0 && c_all > 0) {
+                if (item_of(r) < 0) break;
+                int c0 = 0, c1 = 0, c_all = 0;         // lane 0 holds the item's tile counts
+                if (lane == 0) {
+                    const int slot = r & 1;
+                    ok = mbar_wait(info_full(slot), (r >> 1) & 1, abort_flag);
+                    if (ok) {
+                        c0 = (int)info[8 * slot];
+                        c1 = (int)info[8 * slot + 1];
+                        c_all = (int)info[8 * slot + 2];
+                        mbar_arrive(info_empty(slot));
+                    }
+                }
+                if (lane == 0 && ok && c_all > 0) {
                     auto issue_s = [&](int k, int slot) {
                         const uint32_t kbase = sb + C::OFF_K + slot * C::TILE_BYTES;
                         const uint32_t qbase = sb + C::OFF_Q + k * C::TILE_BYTES;
@@ -321,15 +365,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                         (i > 0 || kk > 0) ? 1u : 0u);
                         }
                     };
+                    // first tile: S0 once Q0 and K are in, S1 once Q1 is (loaded after K)
                     if (c0 > 0) ok = mbar_wait(q_full(0), nq0++ & 1, abort_flag);
-                    if (ok && c1 > 0) ok = mbar_wait(q_full(1), nq1++ & 1, abort_flag);
                     if (ok) ok = mbar_wait(k_full(kt % C::NK), (kt / C::NK) & 1, abort_flag);
                     if (ok) {
                         tc_fence_after();
                         if (c0 > 0) issue_s(0, kt % C::NK);
-                        if (c1 > 0) issue_s(1, kt % C::NK);
-                        mma_commit(k_empty(kt % C::NK));
                     }
+                    if (ok && c1 > 0) {
+                        ok = mbar_wait(q_full(1), nq1++ & 1, abort_flag);
+                        if (ok) {
+                            tc_fence_after();
+                            issue_s(1, kt % C::NK);
+                        }
+                    }
+                    if (ok) mma_commit(k_empty(kt % C::NK));
                     // Common causal case (Q1 sees Q0's tiles, plus at most one more):
                     // the loop is peeled where Q0 ends, so that o_final(0) is
                     // committed right after Q0's last P V and Q0's epilogue
@@ -362,6 +412,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             mma_commit(v_empty(vs));
                             mma_commit(k_empty(kn % C::NK));
                         }
+                        // every S0 of the item is issued: Q0 may be replaced
+                        if (ok) mma_commit(q_empty(0));
                         // tile c0-1: Q0's last P V, then its epilogue may start
                         const int i = c0 - 1;
                         const int vs = (vt + i) % C::NV;
@@ -376,7 +428,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 issue_s(1, kn % C::NK);
                                 mma_commit(v_empty(vs));
                                 mma_commit(k_empty(kn % C::NK));
-                                mma_commit(q_empty(0));
                                 mma_commit(q_empty(1));
                                 const int vs2 = (vt + c0) % C::NV;
                                 ok = mbar_wait(v_full(vs2), ((vt + c0) / C::NV) & 1, abort_flag);
@@ -384,7 +435,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 if (ok) mma_commit(v_empty(vs2));
                             }
                         } else if (ok) {
-                            mma_commit(q_empty(0));
                             mma_commit(q_empty(1));
                             ok = pv(1, vs, i);
                             if (ok) mma_commit(v_empty(vs));
@@ -494,8 +544,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             float m_ref = -INFINITY;     // reference max (log2 units, scaled)
             float l_run = 0.f;
             int it = 0;
-            // The mask bytes of the next visited tile are fetched one tile ahead.
-            TileIter tiles(mrow, itm.first, itm.n_all, itm.kv_end_all, lane);
+            // The item record gives the first chunk's tile flags and the first
+            // visited tile's kept keys; the mask bytes of each later tile are
+            // fetched one tile ahead.
+            const int slot = rr & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(info_full(slot), (rr >> 1) & 1, abort_flag));
+            uint32_t mw[4];              // kept keys of the current tile, 32 per word
+            uint32_t f0 = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mw[q] = ok ? info[8 * slot + 4 + q] : 0u;
+            if (ok) f0 = info[8 * slot + 3];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(info_empty(slot));
+            __syncwarp();
+            TileIter tiles(mrow, itm.first, itm.n_all, itm.kv_end_all, lane, f0);
             auto fetch = [&](int j, uint8_t* mb) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -503,20 +565,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     mb[q] = (mrow && j >= 0 && key < itm.kv_end_all) ? mrow[key] : (uint8_t)(mrow ? 0 : 1);
                 }
             };
-            int j = tiles.next();
-            uint8_t mb[4];
-            fetch(j, mb);
+            int j = ok ? tiles.next() : -1;
             for (; j >= 0 && j < ti.n_tiles;) {
                 const int jn = tiles.next();
                 uint8_t mbn[4];
                 fetch(jn, mbn);
-                uint32_t mw[4];
                 bool all_kept = true;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    mw[q] = __ballot_sync(0xffffffffu, mb[q] != 0);
-                    all_kept = all_kept && (mw[q] == 0xffffffffu);
-                }
+                for (int q = 0; q < 4; ++q) all_kept = all_kept && (mw[q] == 0xffffffffu);
                 const int kbase = j * BN;
                 const bool need_mask = (kbase + BN > ti.lim_first) || kbase < ti.lo_last || !all_kept;
 
@@ -607,7 +663,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ++it;
                 j = jn;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) mb[q] = mbn[q];
+                for (int q = 0; q < 4; ++q) mw[q] = __ballot_sync(0xffffffffu, mbn[q] != 0);
             }
             // ---- epilogue of this Q tile: the last P V done.  It runs even after
             // a wait gave up, so that the warpgroup's named barriers below see

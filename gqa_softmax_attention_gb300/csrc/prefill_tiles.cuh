@@ -97,6 +97,9 @@ struct TileIter {
     uint32_t f;
     __device__ __forceinline__ TileIter(const uint8_t* m, int fst, int n, int e, int l)
         : mrow(m), first(fst), n_tiles(n), kv_end(e), lane(l), chunk(fst / 32 - 1), f(0) {}
+    // Primed with the flag word of the first chunk (fst / 32), already scanned.
+    __device__ __forceinline__ TileIter(const uint8_t* m, int fst, int n, int e, int l, uint32_t f_first)
+        : mrow(m), first(fst), n_tiles(n), kv_end(e), lane(l), chunk(fst / 32), f(f_first) {}
     __device__ __forceinline__ int next() {   // next visited tile, or -1
         while (f == 0) {
             ++chunk;
