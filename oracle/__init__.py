@@ -47,6 +47,11 @@ def _bind(lib):
     lib.oracle_attn_paged_varlen_ex.argtypes = ([vp] * 3 + [ip] + [vp] * 3 + [ip] + [vp] * 2 + [ip] * 8
                                                 + [dp, lp, lp, dp, vp, ip])
     lib.oracle_attn_paged_varlen_ex.restype = ip
+    lib.oracle_e4m3_decode.argtypes = [vp, vp, lp]
+    lib.oracle_e4m3_decode.restype = ip
+    lib.oracle_attn_paged_fp8kv_ex.argtypes = ([vp, ip] + [vp] * 6 + [ip] + [vp] * 3 + [ip] * 8
+                                               + [dp, lp, lp, dp, vp, ip])
+    lib.oracle_attn_paged_fp8kv_ex.restype = ip
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ip
     return lib
@@ -300,5 +305,66 @@ def attn_paged_varlen(q, k_cache, v_cache, cu_seqlens_q, cache_seqlens, block_ta
                                              page_size, _ptr(o), _ptr(lse), B, total_q, Hq, Hkv, D, num_pages,
                                              bt.shape[1], int(bool(causal)), float(scale), wl, wr, cap, _ptr(sk),
                                              int(nthreads))
+    _check(rc)
+    return torch.from_numpy(o), torch.from_numpy(lse)
+
+
+def _u8(x):
+    """e4m3fn codes (a torch float8_e4m3fn or uint8 tensor, or a numpy array) as uint8."""
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().contiguous()
+        if x.dtype != torch.uint8:
+            x = x.view(torch.uint8)
+        return x.numpy()
+    return np.ascontiguousarray(x, dtype=np.uint8)
+
+
+def e4m3_decode(codes):
+    """float8_e4m3fn codes -> float64 values (same shape)."""
+    a = _u8(codes)
+    out = np.zeros(a.shape, dtype=np.float64)
+    _check(_load().oracle_e4m3_decode(_ptr(a), _ptr(out), int(a.size)))
+    return torch.from_numpy(out)
+
+
+def attn_paged_fp8kv(q, k_cache, v_cache, k_scale, v_scale, real_seqlen_kv, block_table, causal=True,
+                     scale=None, requests=None, nthreads=0, window_left=-1, window_right=-1, softcap=0.0,
+                     sinks=None):
+    """Paged GQA attention over float8_e4m3fn key/value caches, in double.
+
+    q: [B,Sq,Hq,D] (16-bit or float); k_cache, v_cache: [num_pages, page_size,
+    Hkv, D] e4m3fn codes (torch.float8_e4m3fn or uint8); k_scale, v_scale:
+    [B, Hkv] dequantization scales (None: ones).  Key j of KV head r in
+    request b is K * k_scale[b, r], its value V * v_scale[b, r] (TileOPs
+    GQADenseFwdOp, FP8 dequantization).  Other arguments as attn_paged."""
+    B, Sq, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    if scale is None:
+        scale = default_scale(D)
+    qa, c = _tensor_in(q)
+    ka, va = _u8(k_cache), _u8(v_cache)
+
+    def sc(x):
+        if x is None:
+            return None
+        a = np.ascontiguousarray(torch.as_tensor(x).detach().cpu().to(torch.float64).numpy().reshape(-1))
+        if a.shape[0] != B * Hkv:
+            raise ValueError("oracle: k_scale / v_scale must hold one value per request and KV head")
+        return a
+    ks, vs = sc(k_scale), sc(v_scale)
+    sl = np.ascontiguousarray(torch.as_tensor(real_seqlen_kv).cpu().numpy(), dtype=np.int32)
+    bt = np.ascontiguousarray(torch.as_tensor(block_table).cpu().numpy(), dtype=np.int32)
+    max_pages = bt.shape[1] if bt.ndim == 2 else 0
+    req = None
+    if requests is not None:
+        req = np.zeros((B,), dtype=np.uint8)
+        req[np.asarray(list(requests), dtype=np.int64)] = 1
+    o = np.zeros((B, Sq, Hq, D), dtype=np.float64)
+    lse = np.zeros((B, Sq, Hq), dtype=np.float64)
+    wl, wr, cap, sk = _opts(window_left, window_right, softcap, sinks, Hq)
+    rc = _load().oracle_attn_paged_fp8kv_ex(_ptr(qa), c, _ptr(ka), _ptr(va), _ptr(ks), _ptr(vs), _ptr(sl),
+                                            _ptr(bt), page_size, _ptr(req), _ptr(o), _ptr(lse), B, Sq, Hq, Hkv,
+                                            D, num_pages, max_pages, int(bool(causal)), float(scale), wl, wr,
+                                            cap, _ptr(sk), int(nthreads))
     _check(rc)
     return torch.from_numpy(o), torch.from_numpy(lse)

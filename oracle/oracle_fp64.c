@@ -42,6 +42,11 @@
  *            fix the zero output; -inf keeps "zero row <=> -inf" whether a
  *            sink is given or not).
  *
+ * FP8 keys and values (TileOPs "Attention Operators", GQADenseFwdOp stage 2):
+ * float8_e4m3fn caches are widened exactly and multiplied by one scale per
+ * request and KV head, K^ = K * k_scale[b, r], V' = V * v_scale[b, r], before
+ * the definition above (oracle_attn_paged_fp8kv_ex).
+ *
  * softmax_j(z) is written out as its definition: with M = max_{j in V_i} z_j
  * and Z = sum_{j in V_i} exp(z_j - M), weight_j = exp(z_j - M) / Z and
  * LSE = M + log Z.  Subtracting M changes nothing mathematically; it only
@@ -395,6 +400,99 @@ int oracle_attn_paged_ex(const void* q, const void* k_cache, const void* v_cache
     return paged_all(q, k_cache, v_cache, dtype, seqlens, block_table, page_size, req_mask,
                      o, lse, B, Sq, Hq, Hkv, D, num_pages, max_pages, causal, scale, &opt,
                      nthreads);
+}
+
+/*
+ * float8_e4m3fn, the 8-bit type the pages name for FP8 keys and values
+ * (TileOPs "Attention Operators", GQAVarlenFwdOp), widened to double: sign s,
+ * 4-bit exponent e with bias 7, 3-bit mantissa m, no infinities:
+ *   e in 1..15 (except e = 15, m = 7):  (-1)^s * 2^(e-7) * (1 + m/8)
+ *   e = 0:                              (-1)^s * 2^-6 * (m/8)   (zero, subnormals)
+ *   e = 15, m = 7:                      NaN
+ */
+static double e4m3_to_double(uint8_t x) {
+    const int s = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    double mag;
+    if (e == 15 && m == 7) mag = NAN;
+    else if (e == 0) mag = ldexp((double)m, -9);
+    else mag = ldexp(8.0 + m, e - 10);
+    return s ? -mag : mag;
+}
+
+/* e4m3fn codes widened to double, for the tests' check of the table. */
+int oracle_e4m3_decode(const uint8_t* codes, double* out, long n) {
+    if (n < 0) return -1;
+    for (long i = 0; i < n; ++i) out[i] = e4m3_to_double(codes[i]);
+    return 0;
+}
+
+/*
+ * Paged attention over float8_e4m3fn key and value caches (TileOPs "Attention
+ * Operators", GQADenseFwdOp stage 2, FP8 dequantization): with per-(request,
+ * KV head) scales, K^_{j,r} = K_{j,r} * k_scale[b, r] and
+ * V'_{j,r} = V_{j,r} * v_scale[b, r]; Q stays 16-bit (its scale is one).
+ * The dequantized request is then the dense definition above, in double.
+ *   q            : [B, Sq, Hq, D], dtype ORACLE_BF16 or ORACLE_F16 (or F64)
+ *   k/v_cache    : [num_pages, page_size, Hkv, D] e4m3fn codes
+ *   k/v_scale    : [B, Hkv] doubles, or NULL for all ones
+ * Other arguments and return codes as oracle_attn_paged_ex.
+ */
+int oracle_attn_paged_fp8kv_ex(const void* q, int q_dtype, const uint8_t* k_cache,
+                               const uint8_t* v_cache, const double* k_scale,
+                               const double* v_scale, const int32_t* seqlens,
+                               const int32_t* block_table, int page_size,
+                               const uint8_t* req_mask, double* o, double* lse, int B,
+                               int Sq, int Hq, int Hkv, int D, int num_pages, int max_pages,
+                               int causal, double scale, long window_left, long window_right,
+                               double softcap, const double* sinks, int nthreads) {
+    int rc = check_opts(window_left, window_right, softcap);
+    if (rc) return rc;
+    rc = check_dense_args(B, Hq, Hkv, Sq, 0, D);
+    if (rc) return rc;
+    if (page_size <= 0 || num_pages < 0 || max_pages < 0) return -1;
+    for (int b = 0; b < B; ++b) {
+        if (req_mask && !req_mask[b]) continue;
+        const int L = seqlens[b];
+        if (L < 0 || (long)L > (long)max_pages * page_size) return -5;
+        const int npages = (L + page_size - 1) / page_size;
+        for (int lp = 0; lp < npages; ++lp) {
+            const int32_t phys = block_table[(size_t)b * max_pages + lp];
+            if (phys < 0 || phys >= num_pages) return -6;
+        }
+    }
+    const oracle_opts opt = {window_left, window_right, softcap, sinks};
+    const size_t tok_elems = (size_t)Hkv * D;
+    const size_t q_elems = (size_t)Sq * Hq * D;
+    for (int b = 0; b < B; ++b) {
+        if (req_mask && !req_mask[b]) continue;
+        const int L = seqlens[b];
+        /* request b: Q widened, K and V gathered token by token and dequantized */
+        double* qd = (double*)malloc(sizeof(double) * (q_elems > 0 ? q_elems : 1));
+        double* kd = (double*)malloc(sizeof(double) * tok_elems * (size_t)(L > 0 ? L : 1));
+        double* vd = (double*)malloc(sizeof(double) * tok_elems * (size_t)(L > 0 ? L : 1));
+        if (!qd || !kd || !vd) { free(qd); free(kd); free(vd); return -3; }
+        for (size_t e = 0; e < q_elems; ++e) qd[e] = load_elem(q, (size_t)b * q_elems + e, q_dtype);
+        const int32_t* trow = block_table + (size_t)b * max_pages;   /* request b's pages */
+        for (int t = 0; t < L; ++t) {
+            const size_t src = ((size_t)trow[t / page_size] * page_size + t % page_size) * tok_elems;
+            for (int r = 0; r < Hkv; ++r) {
+                const double ks = k_scale ? k_scale[(size_t)b * Hkv + r] : 1.0;
+                const double vs = v_scale ? v_scale[(size_t)b * Hkv + r] : 1.0;
+                for (int d = 0; d < D; ++d) {
+                    const size_t e = (size_t)r * D + d;
+                    kd[(size_t)t * tok_elems + e] = e4m3_to_double(k_cache[src + e]) * ks;
+                    vd[(size_t)t * tok_elems + e] = e4m3_to_double(v_cache[src + e]) * vs;
+                }
+            }
+        }
+        rc = dense_all(qd, kd, vd, ORACLE_F64, NULL, o + (size_t)b * q_elems, lse + (size_t)b * Sq * Hq,
+                       1, Hq, Hkv, Sq, L, D, causal, scale, &opt, nthreads);
+        free(qd);
+        free(kd);
+        free(vd);
+        if (rc) return rc;
+    }
+    return 0;
 }
 
 /*

@@ -536,6 +536,78 @@ def pin_paged_varlen_uniform_equals_paged():
     assert torch.equal(o, op.reshape(B * Sq, Hq, D)) and torch.equal(lse, lp.reshape(B * Sq, Hq))
 
 
+
+# ----------------------------------------------------------------------------- float8_e4m3fn key/value caches
+def _fp8_paged_case(B, Sq, Hq, Hkv, D, lengths, ps, seed):
+    """Q (bf16), K/V as e4m3fn codes of N(0, 1) draws in a shuffled page pool
+    (unused slots hold the NaN code), the table and the lengths."""
+    q, k, v, _ = _rand_case(B, Hq, Hkv, Sq, max(lengths), D, seed=seed)
+    k8 = k.float().to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = v.float().to(torch.float8_e4m3fn).view(torch.uint8)
+    npages = [(L + ps - 1) // ps for L in lengths]
+    pool = sum(npages) + 2
+    perm = torch.randperm(pool, generator=torch.Generator().manual_seed(seed + 500))
+    table = torch.full((B, max(1, max(npages))), -1, dtype=torch.int32)
+    kc = torch.full((pool, ps, Hkv, D), 0x7F, dtype=torch.uint8)
+    vc = torch.full((pool, ps, Hkv, D), 0x7F, dtype=torch.uint8)
+    off = 0
+    for b in range(B):
+        for lp in range(npages[b]):
+            phys = int(perm[off + lp])
+            table[b, lp] = phys
+            n = min(ps, lengths[b] - lp * ps)
+            kc[phys, :n] = k8[b, lp * ps: lp * ps + n]
+            vc[phys, :n] = v8[b, lp * ps: lp * ps + n]
+        off += npages[b]
+    return q, kc, vc, table, torch.tensor(lengths, dtype=torch.int32)
+
+
+def pin_e4m3_table_matches_library():
+    # every e4m3fn code against torch's own float8_e4m3fn conversion (a library
+    # routine): 0x7F and 0xFF are the only NaNs, everything else is exact
+    codes = torch.arange(256, dtype=torch.uint8)
+    mine = oracle.e4m3_decode(codes)
+    lib = codes.view(torch.float8_e4m3fn).to(torch.float64)
+    nan = torch.isnan(lib)
+    assert torch.equal(torch.isnan(mine), nan) and int(nan.sum()) == 2
+    assert torch.equal(mine[~nan], lib[~nan])
+    assert mine[0x7E] == 448.0 and mine[0x01] == 2.0 ** -9 and mine[0x08] == 2.0 ** -6 and mine[0xB8] == -1.0
+
+
+def pin_fp8kv_unit_scales_equals_paged():
+    # unit scales: the FP8 call is the paged definition on the decoded values
+    # (decoded here by torch), options included
+    q, kc, vc, table, sl = _fp8_paged_case(3, 2, 6, 2, 16, [9, 0, 23], 4, seed=70)
+    kd = kc.view(torch.float8_e4m3fn).to(torch.float64)
+    vd = vc.view(torch.float8_e4m3fn).to(torch.float64)
+    sinks = torch.tensor([0.5, -1.0, float("-inf"), 2.0, 0.0, 1.0], dtype=torch.float64)
+    for kw in ({}, dict(window_left=5, window_right=0, softcap=4.0, sinks=sinks)):
+        o, lse = oracle.attn_paged_fp8kv(q, kc, vc, None, None, sl, table, causal=True, **kw)
+        op, lp = oracle.attn_paged(q.to(torch.float64), kd, vd, sl, table, causal=True, **kw)
+        assert torch.equal(o, op) and torch.equal(lse, lp)
+
+
+def pin_fp8kv_scale_roles():
+    # k_scale[b, r] multiplies every score of KV head r in request b (the same
+    # as that factor on the softmax scale), v_scale[b, r] multiplies its output
+    # rows and leaves the log-sum-exp alone
+    B, Sq, Hq, Hkv, D = 3, 2, 6, 3, 16
+    q, kc, vc, table, sl = _fp8_paged_case(B, Sq, Hq, Hkv, D, [11, 17, 6], 4, seed=71)
+    g = torch.Generator().manual_seed(72)
+    ks = torch.rand(B, Hkv, generator=g, dtype=torch.float64) * 1.5 + 0.25
+    vs = torch.rand(B, Hkv, generator=g, dtype=torch.float64) * 1.5 + 0.25
+    scale = 0.3
+    o, lse = oracle.attn_paged_fp8kv(q, kc, vc, ks, vs, sl, table, causal=True, scale=scale)
+    gsz = Hq // Hkv
+    for b in range(B):
+        for r in range(Hkv):
+            heads = slice(r * gsz, (r + 1) * gsz)
+            o1, l1 = oracle.attn_paged_fp8kv(q, kc, vc, None, None, sl, table, causal=True,
+                                             scale=scale * float(ks[b, r]))
+            assert torch.allclose(o[b, :, heads], o1[b, :, heads] * float(vs[b, r]), rtol=1e-12, atol=1e-13)
+            assert torch.allclose(lse[b, :, heads], l1[b, :, heads], rtol=1e-12, atol=1e-13)
+
+
 PINS = [pin_golden_closed_form, pin_matches_torch_sdpa, pin_lse_matches_torch_logsumexp,
         pin_single_visible_key_exact, pin_zero_query_is_mean_of_visible_values,
         pin_gqa_equals_repeat_interleave_mha, pin_paged_equals_dense,
@@ -544,7 +616,8 @@ PINS = [pin_golden_closed_form, pin_matches_torch_sdpa, pin_lse_matches_torch_lo
         pin_window_equals_key_slice, pin_softcap_closed_forms, pin_softcap_large_cap_limit,
         pin_sinks_identity, pin_options_paged_equals_dense, pin_half_inputs_widen_exactly,
         pin_varlen_matches_sdpa_per_request, pin_varlen_equals_dense_batch,
-        pin_paged_varlen_equals_gathered_varlen, pin_paged_varlen_uniform_equals_paged]
+        pin_paged_varlen_equals_gathered_varlen, pin_paged_varlen_uniform_equals_paged,
+        pin_e4m3_table_matches_library, pin_fp8kv_unit_scales_equals_paged, pin_fp8kv_scale_roles]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -610,6 +683,11 @@ MUTANTS = {
     "paged_varlen_table_row_ignored": ("block_table + (size_t)b * max_pages, page_size, NULL,",
                                        "block_table, page_size, NULL,"),
     "paged_varlen_first_length": ("cache_seqlens + b,", "cache_seqlens,"),
+    "e4m3_exponent_bias": ("ldexp(8.0 + m, e - 10)", "ldexp(8.0 + m, e - 9)"),
+    "e4m3_subnormal_scale": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    "e4m3_nan_missed": ("if (e == 15 && m == 7) mag = NAN;", "if (0) mag = NAN;"),
+    "fp8_scales_swapped": ("e4m3_to_double(k_cache[src + e]) * ks;", "e4m3_to_double(k_cache[src + e]) * vs;"),
+    "fp8_scale_request_ignored": ("k_scale[(size_t)b * Hkv + r]", "k_scale[r]"),
 }
 
 
