@@ -8,7 +8,7 @@ One step = one pass of the whole path over one batch of synthetic input:
     U[1024, 16384], pages shuffled through block_table.
 Inputs are resident in HBM before timing.  Work is counted algorithmically:
 prefill FLOPs = 4 * D * Hq * (visible query/key pairs), decode bytes = the K
-and V bytes of the real tokens.  The reported value is the step's roofline
+and V bytes of the real tokens (one byte per element for e4m3fn caches).  The reported value is the step's roofline
 efficiency, 100 * (FLOPs / tensor peak + bytes / HBM peak) / step time, with
 the measured peaks of this machine; per-kernel TFLOP/s and GB/s are reported
 beside it.  Between timed steps a buffer twice the L2 size is overwritten so
@@ -16,7 +16,7 @@ every step starts with a cold L2.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload step|qwen3_8b_prefill|paged_decode|wide_group_decode|long_chunked_prefill|
-                                   wide_group_prefill|varlen_prefill|mixed_serving_batch]
+                                   wide_group_prefill|varlen_prefill|mixed_serving_batch|paged_decode_fp8kv]
 Prints exactly one JSON line (rank 0).
 """
 import argparse
@@ -60,8 +60,10 @@ def prefill_work(d):
 
 
 def decode_bytes(p):
+    """K/V bytes of the real tokens: 2 bytes per element, 1 for e4m3fn caches."""
     c = p["config"]
-    return float(p["real_seqlen_kv"].to(torch.int64).sum()) * 2 * c["Hkv"] * c["D"] * 2
+    elem = 1 if c["kind"] == "paged_fp8" else 2
+    return float(p["real_seqlen_kv"].to(torch.int64).sum()) * 2 * c["Hkv"] * c["D"] * elem
 
 
 def packed_pairs(cu_q, kv_lens):
@@ -172,6 +174,8 @@ class Part:
             c = d["config"]
             self.dev = dict(q=d["q"].to(dev), kc=d["k_cache"].to(dev), vc=d["v_cache"].to(dev),
                             sl=d["real_seqlen_kv"].to(dev), bt=d["block_table"].to(dev))
+            if self.kind == "paged_fp8":
+                self.dev.update(ks=d["k_scale"].to(dev), vs=d["v_scale"].to(dev))
             need = g.attn_decode_paged_workspace_size(c["B"], c["Sq"], c["Hq"], c["Hkv"], c["D"], c["page_size"],
                                                       d["max_pages"])
             self.dev["ws"] = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
@@ -192,6 +196,9 @@ class Part:
                              x["block_table"], causal=True, out=x["o"], lse=x["lse"], workspace=x["ws"])
         elif self.kind == "dense":
             g.attn_fwd_dense(x["q"], x["k"], x["v"], key_padding_mask=x["m"], causal=True, out=x["o"], lse=x["lse"])
+        elif self.kind == "paged_fp8":
+            g.attn_decode_paged_fp8kv(x["q"], x["kc"], x["vc"], x["ks"], x["vs"], x["sl"], x["bt"], causal=True,
+                                      workspace=x["ws"], out=x["o"], lse=x["lse"])
         else:
             g.attn_decode_paged(x["q"], x["kc"], x["vc"], x["sl"], x["bt"], causal=True, workspace=x["ws"],
                                 out=x["o"], lse=x["lse"])
@@ -210,6 +217,8 @@ class Part:
         else:
             names = [("q", d["q"]), ("kc", d["k_cache"]), ("vc", d["v_cache"]), ("sl", d["real_seqlen_kv"]),
                      ("bt", d["block_table"])]
+            if self.kind == "paged_fp8":
+                names += [("ks", d["k_scale"]), ("vs", d["v_scale"])]
         self.host_in = [(n, t.contiguous().pin_memory()) for n, t in names]
         self.host_out = [("o", torch.empty(self.dev["o"].shape, dtype=self.dev["o"].dtype).pin_memory()),
                          ("lse", torch.empty(self.dev["lse"].shape, dtype=torch.float32).pin_memory())]
@@ -238,9 +247,10 @@ def make_parts(workload, batch=None):
             parts.append(Part(n, W.make(n)))
             continue
         cfg = dict(W.WORKLOADS[n], B=batch)
-        if cfg["kind"] not in ("dense", "paged"):
+        if cfg["kind"] not in ("dense", "paged", "paged_fp8"):
             raise SystemExit("--batch applies to the dense and paged-decode workloads")
-        data = W.dense_inputs(**cfg) if cfg["kind"] == "dense" else W.paged_inputs(**cfg)
+        make_in = {"dense": W.dense_inputs, "paged": W.paged_inputs, "paged_fp8": W.paged_fp8_inputs}[cfg["kind"]]
+        data = make_in(**cfg)
         data["config"] = cfg
         parts.append(Part(n, data))
     return parts
@@ -421,7 +431,10 @@ def bench_ours(args, world, rank, local):
         rows = c["Hq"] // c["Hkv"] * c["Sq"]
         tc = c["D"] in (128, 256) and 32 <= rows <= 128 and c["page_size"] % 8 == 0 and (
             c["page_size"] >= 64 or 64 % c["page_size"] == 0)
-        split = "decode_tc_kernel<%d>" % c["D"] if tc else "decode_tma_kernel<%d,%d>" % (c["D"], min(4, (rows + 15) // 16))
+        mf = min(4, (rows + 15) // 16)
+        split = "decode_tc_kernel<%d>" % c["D"] if tc else "decode_tma_kernel<%d,%d>" % (c["D"], mf)
+        if dom.kind == "paged_fp8":
+            split = "decode_fp8_kernel<%d,%d>" % (c["D"], mf)
         roof = dict(kernel=split + " + decode_combine_kernel<%d> (%s)" % (c["D"], dom.name), bound="hbm",
                     achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s", frac=ach / peaks["hbm_gbs"],
                     traffic=traffic_per_launch(dom),
@@ -433,7 +446,9 @@ def bench_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        # the arithmetic type: e4m3fn caches widened to float16 products, else bf16
+        "dtype": "e4m3kv-f16" if any(p.kind == "paged_fp8" for p in parts) else "bf16", "data": "synthetic",
         "config": {"workload": "serving step: qwen3_8b_prefill + paged_decode" if args.workload == "step"
                    else args.workload,
                    "parts": {p.name: p.data["config"] for p in parts}, "parallelism": "replicas",
@@ -528,10 +543,15 @@ def oracle_sample(parts, prefill_rows, decode_requests, seed=0):
         else:
             n = min(decode_requests, c["B"])
             reqs = torch.randperm(c["B"], generator=gen)[:n].tolist()
-            sel_bytes = float(d["real_seqlen_kv"][reqs].to(torch.int64).sum()) * 2 * c["Hkv"] * c["D"] * 2
+            elem = 1 if p.kind == "paged_fp8" else 2
+            sel_bytes = float(d["real_seqlen_kv"][reqs].to(torch.int64).sum()) * 2 * c["Hkv"] * c["D"] * elem
             t0 = time.perf_counter()
-            oracle.attn_paged(d["q"], d["k_cache"], d["v_cache"], d["real_seqlen_kv"], d["block_table"],
-                              causal=True, requests=reqs)
+            if p.kind == "paged_fp8":
+                oracle.attn_paged_fp8kv(d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
+                                        d["real_seqlen_kv"], d["block_table"], causal=True, requests=reqs)
+            else:
+                oracle.attn_paged(d["q"], d["k_cache"], d["v_cache"], d["real_seqlen_kv"], d["block_table"],
+                                  causal=True, requests=reqs)
             dt = time.perf_counter() - t0
             est += dt * p.bytes / max(sel_bytes, 1.0)
             desc.append("%s: %d whole requests (%.2f%% of its bytes) in %.2fs" % (p.name, n, 100.0 * sel_bytes / p.bytes,
@@ -552,6 +572,9 @@ def oracle_whole(parts):
         elif p.kind == "paged_varlen":
             oracle.attn_paged_varlen(d["q"], d["k_cache"], d["v_cache"], d["cu_seqlens_q"], d["cache_seqlens"],
                                      d["block_table"], causal=True)
+        elif p.kind == "paged_fp8":
+            oracle.attn_paged_fp8kv(d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
+                                    d["real_seqlen_kv"], d["block_table"], causal=True)
         else:
             oracle.attn_paged(d["q"], d["k_cache"], d["v_cache"], d["real_seqlen_kv"], d["block_table"], causal=True)
     return time.perf_counter() - t0
@@ -560,7 +583,7 @@ def oracle_whole(parts):
 def cpu_baseline(args, parts, peaks):
     import oracle
     ideal = sum(p.ideal_s(peaks) for p in parts)
-    if sum(p.flops for p in parts) < 2e12 and all(p.kind in ("dense", "paged") for p in parts):
+    if sum(p.flops for p in parts) < 2e12 and all(p.kind in ("dense", "paged", "paged_fp8") for p in parts):
         # the whole step takes seconds on the host cores
         est = oracle_whole(parts)
         desc = "the whole step (%s), every row, once" % " + ".join(p.name for p in parts)

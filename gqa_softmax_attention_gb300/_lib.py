@@ -45,6 +45,8 @@ def load() -> ctypes.CDLL:
     lib.attn_fwd_dense_ex.restype = i
     lib.attn_decode_paged_ex.argtypes = [vp, vp, vp, vp, vp, i, vp, vp] + [i] * 8 + [f, vp, vp, sz, vp]
     lib.attn_decode_paged_ex.restype = i
+    lib.attn_decode_paged_fp8kv.argtypes = [vp] * 7 + [i, vp, vp] + [i] * 8 + [f, vp, vp, sz, vp]
+    lib.attn_decode_paged_fp8kv.restype = i
     lib.attn_decode_paged_workspace_size.argtypes = [i] * 7
     lib.attn_decode_paged_workspace_size.restype = sz
     lib.attn_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, i, vp, vp] + [i] * 8 + [f, vp]

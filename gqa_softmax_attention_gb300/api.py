@@ -177,6 +177,61 @@ def attn_decode_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=T
     return out, lse
 
 
+def attn_decode_paged_fp8kv(q, k_cache, v_cache, k_scale, v_scale, real_seqlen_kv, block_table, causal=True,
+                            scale=None, workspace=None, out=None, lse=None, window_left=-1, window_right=-1,
+                            softcap=None, sinks=None):
+    """Paged decode over float8_e4m3fn key/value caches.
+
+    q [B,Sq,Hq,D] bfloat16 or float16; k_cache/v_cache [num_pages,page_size,Hkv,D]
+    torch.float8_e4m3fn (or uint8 holding e4m3fn codes); k_scale/v_scale [B,Hkv]
+    float32 CUDA tensors or None (ones): key t of KV head r in request b is
+    K * k_scale[b, r] and its value V * v_scale[b, r].  D is 128 or 256.  Other
+    arguments as attn_decode_paged.  Returns (o like q, lse [B,Sq,Hq] float32).
+    """
+    _check_16_cuda("q", q, 4)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or \
+                t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise ValueError("%s must be a 4-D float8_e4m3fn (or uint8) CUDA tensor" % n)
+    B, Sq, Hq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shape mismatch: k %s, v %s, D %d" % (tuple(k_cache.shape), tuple(v_cache.shape), D))
+    if Hq % Hkv != 0:
+        raise ValueError("Hq (%d) must be divisible by Hkv (%d)" % (Hq, Hkv))
+    for n, t in (("real_seqlen_kv", real_seqlen_kv), ("block_table", block_table)):
+        if not t.is_cuda or t.dtype != torch.int32:
+            raise ValueError("%s must be an int32 CUDA tensor" % n)
+    if tuple(real_seqlen_kv.shape) != (B,) or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("real_seqlen_kv must be [B] and block_table [B, max_pages]")
+    scales = []
+    for n, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is not None:
+            if not t.is_cuda or t.dtype != torch.float32 or t.numel() != B * Hkv:
+                raise ValueError("%s must be a float32 CUDA tensor of B * Hkv values" % n)
+            t = t.contiguous()
+        scales.append(t)
+    max_pages = block_table.shape[1]
+    q, k_cache, v_cache = q.contiguous(), k_cache.contiguous(), v_cache.contiguous()
+    sl, bt = real_seqlen_kv.contiguous(), block_table.contiguous()
+    need = attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, page_size, max_pages)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device)
+    opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device, _DTYPES[q.dtype])
+    st = _lib.load().attn_decode_paged_fp8kv(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(scales[0]), _ptr(scales[1]), _ptr(sl), _ptr(bt), page_size,
+        _ptr(out), _ptr(lse), B, Sq, Hq, Hkv, D, num_pages, max_pages, int(bool(causal)), resolve_scale(scale, D),
+        ctypes.byref(opt) if opt is not None else None, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(q.device))
+    if st != 0:
+        _raise(st, "attn_decode_paged_fp8kv")
+    return out, lse
+
+
 def attn_decode_paged_noalloc(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=True, scale=None, out=None,
                               lse=None):
     """Paged decode through the entry point that allocates nothing in the library.

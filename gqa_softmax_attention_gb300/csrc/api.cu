@@ -244,7 +244,7 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
     if (!workspace || workspace_bytes < p.workspace_bytes) return GQA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GQA_ERR_MISALIGNED;
 
-    DecodeArgs a;
+    DecodeArgs a{};
     a.q = q; a.k_cache = k_cache; a.v_cache = v_cache;
     a.seqlens = real_seqlen_kv; a.table = block_table;
     a.o = o; a.lse = lse;
@@ -287,6 +287,77 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
                          make_cache_map(&tk, k_cache, (long)num_pages * page_size, Hkv, D, box, a.f16) &&
                          make_cache_map(&tv, v_cache, (long)num_pages * page_size, Hkv, D, box, a.f16);
     return gqa::launch_decode(a, use_tma ? &tk : nullptr, use_tma ? &tv : nullptr, box, st) == cudaSuccess
+               ? GQA_OK
+               : GQA_ERR_CUDA;
+}
+
+// Paged cache of e4m3fn bytes [pages * page_size, Hkv, D] as a 3-D byte map
+// {D, Hkv, rows} with a {128, 1, box_tokens} box (128-byte rows, 128-byte swizzle).
+static bool make_cache_map_fp8(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D, int box_tokens) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)Hkv * D};
+    const cuuint32_t box[3] = {128, 1, (cuuint32_t)box_tokens};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+gqa_status attn_decode_paged_fp8kv(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                                   const float* v_scale, const int32_t* real_seqlen_kv, const int32_t* block_table,
+                                   int page_size, void* o, float* lse, int B, int Sq, int Hq, int Hkv, int D,
+                                   int num_pages, int max_pages, int causal, float scale, const gqa_options* opts,
+                                   void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
+    if (B <= 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || page_size <= 0 || num_pages < 0 || max_pages <= 0)
+        return GQA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+    if ((long)max_pages * page_size >= kMaxSeq) return GQA_ERR_INVALID_ARG;
+    if ((long)num_pages * page_size >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+    if (D != 128 && D != 256) return GQA_ERR_UNSUPPORTED;
+    const int box = gqa::decode_box_tokens(D, page_size);
+    if (box <= 0) return GQA_ERR_UNSUPPORTED;
+    if (Sq == 0) return GQA_OK;
+    if (!q || !k_cache || !v_cache || !real_seqlen_kv || !block_table || !o) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return GQA_ERR_MISALIGNED;
+    if (!aligned4(real_seqlen_kv) || !aligned4(block_table) || (lse && !aligned4(lse)) ||
+        (k_scale && !aligned4(k_scale)) || (v_scale && !aligned4(v_scale)))
+        return GQA_ERR_MISALIGNED;
+    gqa::Extras ex;
+    const gqa_status es = make_extras(opts, scale, &ex);
+    if (es != GQA_OK) return es;
+    DecodePlan p;
+    if (!gqa::plan_decode(B, Sq, Hq, Hkv, D, page_size, max_pages, sm_count(), &p)) return GQA_ERR_UNSUPPORTED;
+    // the split path's partials: never more than attn_decode_paged_workspace_size
+    const size_t need = (p.part_o_bytes + 255) / 256 * 256 + (p.part_lse_bytes + 255) / 256 * 256;
+    if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GQA_ERR_MISALIGNED;
+
+    DecodeArgs a{};
+    a.q = q; a.k_cache = k_cache; a.v_cache = v_cache;
+    a.seqlens = real_seqlen_kv; a.table = block_table;
+    a.o = o; a.lse = lse;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + (p.part_o_bytes + 255) / 256 * 256);
+    a.B = B; a.Sq = Sq; a.Hq = Hq; a.Hkv = Hkv; a.D = D;
+    a.page_size = page_size; a.max_pages = max_pages; a.num_pages = num_pages; a.causal = causal ? 1 : 0;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    a.chunk = p.chunk;
+    a.max_splits = p.max_splits;
+    a.seg_table = nullptr;
+    a.f16 = opts && opts->dtype == GQA_FP16 ? 1 : 0;
+    a.x = ex;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    // with an empty pool no page is ever loaded; the maps then describe one page
+    const long rows = (long)(num_pages > 0 ? num_pages : 1) * page_size;
+    CUtensorMap tk, tv;
+    if (!make_cache_map_fp8(&tk, k_cache, rows, Hkv, D, box) || !make_cache_map_fp8(&tv, v_cache, rows, Hkv, D, box))
+        return GQA_ERR_CUDA;
+    return gqa::launch_decode_fp8(a, tk, tv, box, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? GQA_OK
                : GQA_ERR_CUDA;
 }

@@ -33,6 +33,9 @@
 //
 // The path is bound by HBM bandwidth; the MMAs are small and hidden under the
 // loads, so warp-level mma.sync is used rather than tcgen05.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <cmath>
 #include <mutex>
 
@@ -136,6 +139,7 @@ struct Consumer {
     int lim[2];             // exclusive visibility limit of the two fragment rows this lane holds
     int lo[2];              // their inclusive lower limit (left window)
     float cap_in, cap_out;  // softcap, or cap_out == 0
+    float out_scale;        // multiplies the stored partial O (FP8 value scale; else 1)
     uint32_t qf[C::KSTEPS][4];
     float m_run, l_run;
     float acc[C::NFD][4];
@@ -156,6 +160,7 @@ struct Consumer {
         for (int n = 0; n < C::NFD; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
         cap_in = a.x.cap_in;
         cap_out = a.x.cap_out;
+        out_scale = 1.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int rl = mf * 16 + (lane >> 2) + 8 * h;
@@ -220,6 +225,11 @@ struct Consumer {
                 mma16816<C::F16>(sacc[2 * np + 1], qf[kk], b2, b3);
             }
         }
+        write_s(sacc, t0, sl);
+    }
+
+    // Scaled (or capped) and masked scores of this warp's keys into smem.
+    __device__ __forceinline__ void write_s(const float (&sacc)[C::NFK][4], int t0, float sl) {
         float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
 #pragma unroll
         for (int n = 0; n < C::NFK; ++n) {
@@ -329,7 +339,7 @@ struct Consumer {
             const int rl = mf * 16 + (lane >> 2) + 8 * h;
             if (rl < w.rows_here) {
                 const float l = sL[rl];
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = l > 0.f ? out_scale / l : 0.f;
                 float* dst = a.part_o + (part_row0 + rl) * (CHUNKS * 8) + wk * C::DSL + 2 * (lane & 3);
 #pragma unroll
                 for (int n = 0; n < C::NFD; ++n)
@@ -525,6 +535,310 @@ decode_gather_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
     }
     cp_async_wait<0>();
     c.store(a, w, R, bar);
+}
+
+// ---------------------------------------------------------------------------
+// float8_e4m3fn caches (TileOPs "Attention Operators", GQADenseFwdOp stage 2:
+// K^ = K * k_scale and V' = V * v_scale, one scale per request and KV head).
+// The producer brings the cache bytes in with TMA (128-byte rows, 128-byte
+// swizzle); the consumer warps take their K and V fragments straight from
+// those tiles with ldmatrix (two e4m3 per 16-bit element) and widen them to
+// float16 in registers (exact: every e4m3fn value is a float16), then run
+// float16 MMAs with FP32 accumulation.  Q is rounded to float16 once (a
+// bfloat16 Q keeps every bit for magnitudes in [2^-14, 65504]) and P is packed
+// to float16; k_scale joins the softmax scale and the softcap's input, v_scale
+// the stored partial O.
+//   S = Q K^T: ldmatrix gives lane t four consecutive dims 4(t%4)..4(t%4)+3 of
+//     a key in each 16-dim k-step; the first two serve as k = 2(t%4), 2(t%4)+1
+//     of the m16n8k16 fragment and the last two as k = 2(t%4)+8, +9, and Q's
+//     fragments are loaded under the same map, so every dot product is the
+//     same sum in another order.
+//   O += P V: ldmatrix.trans gives lane t, for keys 2(t%4) and 2(t%4)+1, the
+//     two dims 2(t/4), 2(t/4)+1 of a 16-dim chunk; a byte permute splits them
+//     into an even-dim and an odd-dim n8 block, and the stored O interleaves
+//     the two blocks back into dim order.
+template <int D, int MF>
+struct F8Cfg : DCfg<D, MF, true, true> {
+    using B16 = DCfg<D, MF, true, true>;
+    static constexpr int SUB8 = B16::TK * 128;                 // 128 e4m3 columns of a tile
+    static constexpr int NSUB8 = D / 128;
+    static constexpr int TILE8 = NSUB8 * SUB8;                 // one K or V tile of bytes
+    static constexpr int FIXED8 = B16::Q_BYTES + B16::ROWS * B16::S_STRIDE * 4 + B16::ROWS * 128 +
+                                  3 * B16::ROWS * 4 + 1024 + 256;
+    // three CTAs per SM for the small row blocks at D = 128, else two
+    static constexpr int BUDGET = (D == 128 && MF <= 2) ? 75 * 1024 : 113 * 1024;
+    static constexpr int NS_FIT8 = (BUDGET - FIXED8) / (2 * TILE8);
+    static constexpr int NS = NS_FIT8 < 6 ? NS_FIT8 : 6;
+    static constexpr int OFF_KV = 0;                           // 1024-aligned byte ring first
+    static constexpr int OFF_Q = OFF_KV + NS * 2 * TILE8;
+    static constexpr int OFF_S = OFF_Q + B16::Q_BYTES;
+    static constexpr int OFF_P = OFF_S + B16::ROWS * B16::S_STRIDE * 4;
+    static constexpr int OFF_A = OFF_P + B16::ROWS * 128;
+    static constexpr int OFF_L = OFF_A + B16::ROWS * 4;
+    static constexpr int OFF_M = OFF_L + B16::ROWS * 4;
+    static constexpr int OFF_BAR = OFF_M + B16::ROWS * 4;      // full[NS], empty[NS]
+    static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
+    static constexpr int SMEM = OFF_FLAG + 16 + 1024;
+    static_assert(D == 128 || D == 256, "e4m3 rows of 128 or 256 bytes");
+    static_assert(B16::DSL % 32 == 0, "P V takes 32-dim groups");
+    static_assert(NS >= 2, "pipeline depth");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+// Two e4m3fn codes (low byte first) -> two float16 (low half first), exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// A bfloat16 pair -> a float16 pair (round to nearest even).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <class C>
+struct Consumer8 : Consumer<C> {
+    // Byte offset of 16-byte chunk c (16 dims) of key row r in an e4m3 tile.
+    static __device__ __forceinline__ uint32_t off8(int r, int c) {
+        return (uint32_t)((c >> 3) * C::SUB8 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    }
+
+    // Q's fragments under the dim map of the S products (Q already in smem).
+    __device__ __forceinline__ void q_fragments(bool qbf) {
+        const int t4 = this->lane & 3;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            const int chunk = 2 * kk + (t4 >> 1);              // 8-element chunk holding dims 16kk + 4(t%4)..
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = this->mf * 16 + (this->lane >> 2) + 8 * h;
+                const uint2 v = *reinterpret_cast<const uint2*>(this->smem + C::OFF_Q +
+                                                                 sw_off(row, chunk, C::ROWS * 128) + (t4 & 1) * 8);
+                this->qf[kk][h] = qbf ? bf16x2_to_f16x2(v.x) : v.x;       // k = 2(t%4), +1
+                this->qf[kk][2 + h] = qbf ? bf16x2_to_f16x2(v.y) : v.y;   // k = 2(t%4) + 8, +9
+            }
+        }
+    }
+
+    // S = Q K^T for this warp's rows and keys from the e4m3 key tile at sK.
+    __device__ __forceinline__ void qk8(uint32_t sK, int t0, float sl) {
+        float sacc[C::NFK][4];
+#pragma unroll
+        for (int n = 0; n < C::NFK; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+        const int m = this->lane >> 3;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; kk += 2) {
+#pragma unroll
+            for (int nb = 0; nb < C::NFK; nb += 2) {
+                // matrices: (block nb, step kk), (nb, kk+1), (nb+1, kk), (nb+1, kk+1)
+                const int key = this->wk * C::KEYS_PER_WARP + (nb + (m >> 1)) * 8 + (this->lane & 7);
+                uint32_t r[4];
+                ldsm_x4(sK + off8(key, kk + (m & 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma16816<true>(sacc[nb + (j >> 1)], this->qf[kk + (j & 1)], e4m3x2_to_f16x2(r[j]),
+                                   e4m3x2_to_f16x2(r[j] >> 16));
+            }
+        }
+        this->write_s(sacc, t0, sl);
+    }
+
+    // O = O * alpha + P V for this warp's rows and dims from the e4m3 value tile
+    // at sV.  acc[4q + 2i + e]: dims of 16-dim chunk i of group q with parity e.
+    __device__ __forceinline__ void pv8(uint32_t sV) {
+        const float* sAlpha = reinterpret_cast<const float*>(this->smem + C::OFF_A);
+        const int lane = this->lane, mf = this->mf;
+        const float a0 = sAlpha[mf * 16 + (lane >> 2)];
+        const float a1 = sAlpha[mf * 16 + (lane >> 2) + 8];
+#pragma unroll
+        for (int n = 0; n < C::NFD; ++n) {
+            this->acc[n][0] *= a0; this->acc[n][1] *= a0;
+            this->acc[n][2] *= a1; this->acc[n][3] *= a1;
+        }
+        const int m = lane >> 3;
+#pragma unroll
+        for (int kk = 0; kk < C::TK / 16; ++kk) {
+            uint32_t pa[4];
+            {
+                const int row = mf * 16 + (lane & 15);
+                const int chunk = kk * 2 + (lane >> 4);
+                ldsm_x4(this->sb + C::OFF_P + row * 128 + ((chunk ^ (row & 7)) << 4), pa[0], pa[1], pa[2], pa[3]);
+            }
+#pragma unroll
+            for (int q = 0; q < C::DSL / 32; ++q) {
+                // matrices: (keys 0-7, chunk c0), (keys 8-15, c0), (keys 0-7, c0+1), (keys 8-15, c0+1)
+                const int c0 = (this->wk * C::DSL + 32 * q) / 16;
+                const int key = kk * 16 + (m & 1) * 8 + (lane & 7);
+                uint32_t r[4];
+                ldsm_x4_t(sV + off8(key, c0 + (m >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    // bytes: V[k0][d], V[k0][d+1], V[k1][d], V[k1][d+1] (d even)
+                    mma16816<true>(this->acc[4 * q + 2 * i], pa, e4m3x2_to_f16x2(__byte_perm(r[2 * i], 0, 0x0020)),
+                                   e4m3x2_to_f16x2(__byte_perm(r[2 * i + 1], 0, 0x0020)));
+                    mma16816<true>(this->acc[4 * q + 2 * i + 1], pa,
+                                   e4m3x2_to_f16x2(__byte_perm(r[2 * i], 0, 0x0031)),
+                                   e4m3x2_to_f16x2(__byte_perm(r[2 * i + 1], 0, 0x0031)));
+                }
+            }
+        }
+    }
+
+    // Normalised partial O (FP32, dims back in order) and base-2 LSE of this split.
+    template <class Bar>
+    __device__ __forceinline__ void store8(const DecodeArgs& a, const Work& w, int R, Bar bar) {
+        float* sL = reinterpret_cast<float*>(this->smem + C::OFF_L);
+        float* sM = reinterpret_cast<float*>(this->smem + C::OFF_M);
+        if (this->ssub == 0) {
+            sL[this->srow] = this->l_run;
+            sM[this->srow] = this->m_run;
+        }
+        bar();
+        const int lane = this->lane;
+        const size_t part_row0 = ((size_t)(w.b * a.Hkv + w.hkv) * a.max_splits + w.split) * R + w.row0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int rl = this->mf * 16 + (lane >> 2) + 8 * h;
+            if (rl < w.rows_here) {
+                const float l = sL[rl];
+                const float inv = l > 0.f ? this->out_scale / l : 0.f;
+                float* dst = a.part_o + (part_row0 + rl) * (C::NSUB * 64) + this->wk * C::DSL + 4 * (lane & 3);
+#pragma unroll
+                for (int q = 0; q < C::DSL / 32; ++q)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const float* e = this->acc[4 * q + 2 * i];
+                        const float* o = this->acc[4 * q + 2 * i + 1];
+                        *reinterpret_cast<float4*>(dst + 32 * q + 16 * i) =
+                            make_float4(e[2 * h] * inv, o[2 * h] * inv, e[2 * h + 1] * inv, o[2 * h + 1] * inv);
+                    }
+            }
+        }
+        if (this->ctid < w.rows_here) {
+            const float l = sL[this->ctid];
+            a.part_lse[part_row0 + this->ctid] = l > 0.f ? sM[this->ctid] + log2f(l) : -INFINITY;
+        }
+    }
+};
+
+template <int D, int MF, bool QBF>
+__global__ void __launch_bounds__(F8Cfg<D, MF>::NT)
+decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DecodeArgs a, int R, int g, int n_rowblk, int box_tokens) {
+    using C = F8Cfg<D, MF>;
+    griddep_launch_dependents();                 // the combine may be scheduled (it waits for this grid)
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+    Work w;
+    if (!work_of<C>(a, R, g, n_rowblk, w)) return;
+
+    const uint32_t bar0 = sb + C::OFF_BAR;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (C::NS + s); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), C::NC);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x / 32;
+    if (warp == C::NC) {
+        // ------------------------------------------------------------ TMA producer
+        if ((threadIdx.x & 31) == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            const int32_t* trow = a.table + (size_t)w.b * a.max_pages;
+            const int nbox = C::TK / box_tokens;
+            const uint32_t box_bytes = (uint32_t)box_tokens * 128;
+            int issued = 0;
+            for (int it = 0; it < w.n_tiles; ++it) {
+                const int s = it % C::NS;
+                if (!mbar_wait(empty(s), ((it / C::NS) & 1) ^ 1, abort_flag)) break;
+                const int t0 = w.t_begin + it * C::TK;
+                int rows[8];        // first cache row of each box, or -1
+                int n = 0;
+                for (int i = 0; i < nbox; ++i) {
+                    const int t = t0 + i * box_tokens;
+                    int row = -1;
+                    if (t < w.t_end) {
+                        const int page = trow[t / a.page_size];
+                        // a page id outside the pool (a caller error) is not loaded
+                        if (page >= 0 && page < a.num_pages) row = page * a.page_size + t % a.page_size;
+                    }
+                    rows[i] = row;
+                    n += row >= 0;
+                }
+                mbar_arrive_expect_tx(full(s), (uint32_t)n * box_bytes * C::NSUB8 * 2);
+                const uint32_t sK = sb + C::OFF_KV + s * 2 * C::TILE8;
+                const uint32_t sV = sK + C::TILE8;
+                for (int i = 0; i < nbox; ++i) {
+                    if (rows[i] < 0) continue;
+#pragma unroll
+                    for (int sub = 0; sub < C::NSUB8; ++sub) {
+                        const uint32_t off = sub * C::SUB8 + i * box_tokens * 128;
+                        tma_load_3d(sK + off, &tm_k, full(s), sub * 128, w.hkv, rows[i]);
+                        tma_load_3d(sV + off, &tm_v, full(s), sub * 128, w.hkv, rows[i]);
+                    }
+                }
+                issued = it + 1;
+            }
+            if (*abort_flag) {
+                // let copies already in flight land before the CTA goes away
+                for (int it = issued - C::NS > 0 ? issued - C::NS : 0; it < issued; ++it)
+                    mbar_drain(full(it % C::NS), (it / C::NS) & 1);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        Consumer8<C> c;
+        c.init(smem, sb, a, w, g);
+        const int kv = w.b * a.Hkv + w.hkv;
+        const float ks = a.k_scale ? a.k_scale[kv] : 1.f;
+        c.out_scale = a.v_scale ? a.v_scale[kv] : 1.f;
+        c.cap_in *= ks;
+        auto bar = [] { named_bar_sync(1, C::NCT); };
+        c.load_q(a, w, g, bar);
+        c.q_fragments(QBF);
+        const float sl = a.scale_log2 * ks;
+        for (int it = 0; it < w.n_tiles; ++it) {
+            const int s = it % C::NS;
+            const int t0 = w.t_begin + it * C::TK;
+            const uint32_t sK = sb + C::OFF_KV + s * 2 * C::TILE8;
+            const uint32_t sV = sK + C::TILE8;
+            const bool ok = mbar_wait(full(s), (it / C::NS) & 1, abort_flag);
+            if (ok) {
+                const int nvalid = w.t_end - t0;
+                if (nvalid < C::TK) {
+                    // Value rows past the request's end hold stale bytes: zero them.
+                    const int per_sub = (C::TK - nvalid) * 8;
+                    for (int idx = c.ctid; idx < per_sub * C::NSUB8; idx += C::NCT) {
+                        const int sub = idx / per_sub;
+                        const int rem = idx % per_sub;
+                        *reinterpret_cast<uint4*>(smem + (sV - sb) + sub * C::SUB8 + (nvalid + rem / 8) * 128 +
+                                                  (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                c.qk8(sK, t0, sl);
+            }
+            if (!named_bar_and(1, C::NCT, ok)) break;   // every consumer leaves together
+            c.softmax();
+            named_bar_sync(1, C::NCT);
+            c.pv8(sV);
+            __syncwarp();
+            if (c.lane == 0) mbar_arrive(empty(s));
+        }
+        c.store8(a, w, R, bar);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_decode_error, (int)kErrDecodeWait);
 }
 
 template <int D, bool F16>
@@ -779,6 +1093,52 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CU
         case 256: return launch_d<256>(a, tm_k, tm_v, box_tokens, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+namespace {
+template <int D, int MF, bool QBF>
+cudaError_t launch_fp8_t(const DecodeArgs& a, const CUtensorMap& tm_k, const CUtensorMap& tm_v, int box_tokens,
+                         int R, int g, int n_rowblk, cudaStream_t stream) {
+    using C = F8Cfg<D, MF>;
+    cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<D, MF, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(a.max_splits, a.Hkv, a.B * n_rowblk);
+    decode_fp8_kernel<D, MF, QBF><<<grid, C::NT, C::SMEM, stream>>>(tm_k, tm_v, a, R, g, n_rowblk, box_tokens);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fp8_d(const DecodeArgs& a, const CUtensorMap& tm_k, const CUtensorMap& tm_v, int box_tokens,
+                         int R, int g, cudaStream_t stream) {
+    const int mf = choose_mf(R);
+    const int n_rowblk = (R + 16 * mf - 1) / (16 * mf);
+    const bool qbf = !a.f16;
+    switch (mf * 2 + (qbf ? 1 : 0)) {
+        case 2: return launch_fp8_t<D, 1, false>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);
+        case 3: return launch_fp8_t<D, 1, true>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);
+        case 4: return launch_fp8_t<D, 2, false>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);
+        case 5: return launch_fp8_t<D, 2, true>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);
+        case 6: return launch_fp8_t<D, 3, false>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);
+        case 7: return launch_fp8_t<D, 3, true>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);
+        case 8: return launch_fp8_t<D, 4, false>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);
+        default: return launch_fp8_t<D, 4, true>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);
+    }
+}
+}  // namespace
+
+cudaError_t launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& tm_k, const CUtensorMap& tm_v, int box_tokens,
+                              cudaStream_t stream) {
+    const int g = a.Hq / a.Hkv;
+    const int R = g * a.Sq;
+    cudaError_t e;
+    switch (a.D) {
+        case 128: e = launch_fp8_d<128>(a, tm_k, tm_v, box_tokens, R, g, stream); break;
+        case 256: e = launch_fp8_d<256>(a, tm_k, tm_v, box_tokens, R, g, stream); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    return launch_decode_combine(a, stream);
 }
 
 int decode_take_device_error() {

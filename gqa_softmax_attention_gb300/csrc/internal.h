@@ -96,6 +96,10 @@ struct DecodeArgs {
     int tc_grid;            // persistent CTAs (one per SM)
     int f16;                // q, caches and o are float16 (else bfloat16)
     Extras x;
+    // float8_e4m3fn caches (attn_decode_paged_fp8kv): per-(request, KV head)
+    // dequantization scales [B, Hkv], nullptr meaning 1
+    const float* k_scale;
+    const float* v_scale;
 };
 
 struct DecodePlan {
@@ -122,6 +126,11 @@ int decode_box_tokens(int D, int page_size);
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int box_tokens,
                           cudaStream_t stream);
 int decode_take_device_error();
+// Split decode over float8_e4m3fn caches (decode_fp8_kernel): tm_k / tm_v are
+// 3-D byte maps {D, Hkv, pages * page_size} with a {128, 1, box_tokens} box;
+// D is 128 or 256 and g * Sq at most 64.  Launches the combine as well.
+cudaError_t launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                              int box_tokens, cudaStream_t stream);
 // Merge of the split partials (decode_combine_kernel).
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream);
 

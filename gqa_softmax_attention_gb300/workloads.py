@@ -50,6 +50,9 @@ WORKLOADS = {
     # packed (THD) self-attention prefill of 16 requests of mixed length
     "varlen_prefill": dict(kind="varlen", B=16, Hq=32, Hkv=8, D=128, causal=True, sigma=1.0,
                            lengths=(256, 8192)),
+    # the paged decode batch over float8_e4m3fn caches with per-(request, KV head) scales
+    "paged_decode_fp8kv": dict(kind="paged_fp8", B=64, Sq=1, Hq=32, Hkv=8, D=128, page_size=64, causal=True,
+                               sigma=1.0, lengths=(1024, 16384), spare=0.10, scale_range=(0.25, 1.0)),
     # one serving step over a paged cache: 60 decode steps (one query each,
     # cache lengths U[1024, 16384]) and 4 prefill chunks of 1024 queries whose
     # caches hold U[0, 8192] earlier tokens plus the chunk
@@ -137,6 +140,24 @@ def paged_inputs(B, Sq, Hq, Hkv, D, page_size, lengths, spare=0.10, sigma=1.0, s
                 block_table=table, num_pages=pool, max_pages=max_pages, page_size=page_size)
 
 
+def paged_fp8_inputs(B, Sq, Hq, Hkv, D, page_size, lengths, spare=0.10, sigma=1.0, seed=0,
+                     scale_range=(0.25, 1.0), max_pages=None, **_):
+    """Paged decode inputs with float8_e4m3fn caches: the paged_inputs draw,
+    each bf16 cache value rounded to e4m3fn by torch (round to nearest even),
+    and k_scale / v_scale [B, Hkv] float32 drawn uniformly from scale_range
+    (stream 3, K first).  Returns the paged_inputs dict with k_cache / v_cache
+    as torch.float8_e4m3fn and k_scale / v_scale added."""
+    p = paged_inputs(B, Sq, Hq, Hkv, D, page_size, lengths, spare=spare, sigma=sigma, seed=seed,
+                     max_pages=max_pages)
+    p["k_cache"] = p["k_cache"].float().to(torch.float8_e4m3fn)
+    p["v_cache"] = p["v_cache"].float().to(torch.float8_e4m3fn)
+    g = torch.Generator().manual_seed(seed * 2**32 + 3 * 2**20)
+    lo, hi = scale_range
+    p["k_scale"] = lo + (hi - lo) * torch.rand(B, Hkv, generator=g, dtype=torch.float32)
+    p["v_scale"] = lo + (hi - lo) * torch.rand(B, Hkv, generator=g, dtype=torch.float32)
+    return p
+
+
 def _offsets(lengths):
     cu = [0]
     for n in lengths:
@@ -198,6 +219,8 @@ def make(name, seed=0):
         q_lens, lengths = mixed_lengths(cfg, seed)
         data = varlen_paged_inputs(q_lens, lengths, cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["page_size"],
                                    sigma=cfg["sigma"], seed=seed)
+    elif cfg["kind"] == "paged_fp8":
+        data = paged_fp8_inputs(seed=seed, **cfg)
     else:
         data = paged_inputs(seed=seed, **cfg)
     data["config"] = cfg

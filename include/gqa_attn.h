@@ -173,6 +173,39 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
                                 gqa_stream_t stream);
 
 /*
+ * Paged decode over float8_e4m3fn key and value caches (TileOPs "Attention
+ * Operators", GQADenseFwdOp stage 2, FP8 dequantization, and GQAVarlenFwdOp's
+ * one scale per request and KV head): key t of KV head r in request b is
+ * K * k_scale[b * Hkv + r], its value V * v_scale[b * Hkv + r]; Q is 16-bit.
+ * The result is the attn_decode_paged_ex definition on those keys and values.
+ *
+ *   k_cache, v_cache  [num_pages, page_size, Hkv, D] e4m3fn bytes (sign, 4
+ *                     exponent bits with bias 7, 3 mantissa bits; 0x7F and 0xFF
+ *                     are NaN and must not occur), 16-byte aligned
+ *   k_scale, v_scale  [B, Hkv] float device arrays, or NULL for all ones
+ *   q, o              16-bit: bfloat16, or float16 with opts->dtype = GQA_FP16
+ *   other arguments   as attn_decode_paged_ex; the same workspace size
+ *                     (attn_decode_paged_workspace_size) is enough.
+ *
+ * The keys and values are widened exactly to float16 on the GPU and the
+ * products run in float16 with FP32 accumulation, so Q is rounded to float16
+ * once: a bfloat16 Q keeps every bit for magnitudes in [2^-14, 65504] and must
+ * stay below 65504.  Supported: D = 128 or 256, and page sizes that are a
+ * multiple of 8 and divide, or are divided by, the key tile (64 tokens at
+ * D = 128, 32 at D = 256); other sizes return GQA_ERR_UNSUPPORTED.  Caller
+ * obligations and the handling of bad page ids and lengths are those of
+ * attn_decode_paged.
+ */
+gqa_status attn_decode_paged_fp8kv(const void* q, const void* k_cache, const void* v_cache,
+                                   const float* k_scale, const float* v_scale,
+                                   const int32_t* real_seqlen_kv, const int32_t* block_table,
+                                   int page_size, void* o, float* lse,
+                                   int B, int Sq, int Hq, int Hkv, int D,
+                                   int num_pages, int max_pages, int causal, float scale,
+                                   const gqa_options* opts, void* workspace, size_t workspace_bytes,
+                                   gqa_stream_t stream);
+
+/*
  * Bytes of workspace attn_decode_paged needs for these sizes on the current
  * device (0 for invalid sizes).  A pure function of its arguments and the
  * device's SM count.

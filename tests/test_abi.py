@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("attn_fwd_dense", "attn_decode_paged", "attn_decode_paged_workspace_size", "attn_validate_paged",
-              "attn_fwd_varlen", "attn_fwd_paged", "attn_varlen_workspace_size",
+              "attn_fwd_varlen", "attn_fwd_paged", "attn_varlen_workspace_size", "attn_decode_paged_fp8kv",
               "gqa_status_string", "gqa_device_error", "gqa_version"):
         assert n in names
 
@@ -87,6 +87,24 @@ def test_paged_argument_checks(lib):
     assert paged(lib, ws=None, ws_bytes=0) == WORKSPACE          # workspace is required
     assert paged(lib, ws=A16, ws_bytes=16) == WORKSPACE          # and must be large enough
     assert paged(lib, Sq=0) == OK
+
+
+def paged_fp8(lib, ws=None, ws_bytes=0, q=A16, kc=A16, ks=None, vs=None, B=2, Sq=1, Hq=8, Hkv=2, D=128, ps=16,
+              num_pages=10, max_pages=4):
+    return lib.attn_decode_paged_fp8kv(q, kc, A16, ks, vs, A16, A16, ps, A16b, None, B, Sq, Hq, Hkv, D, num_pages,
+                                       max_pages, 1, 0.1, None, ws, ws_bytes, None)
+
+
+def test_paged_fp8kv_argument_checks(lib):
+    assert paged_fp8(lib, B=0) == INVALID
+    assert paged_fp8(lib, Hq=6, Hkv=4) == INVALID
+    assert paged_fp8(lib, D=64) == UNSUPPORTED                  # e4m3 rows of 128 or 256 bytes only
+    assert paged_fp8(lib, ps=12) == UNSUPPORTED                 # pages must tile the key tile in 8-row blocks
+    assert paged_fp8(lib, kc=MIS) == MISALIGNED
+    assert paged_fp8(lib, ks=ctypes.c_void_p((1 << 20) + 2)) == MISALIGNED
+    assert paged_fp8(lib, ws=None, ws_bytes=0) == WORKSPACE
+    assert paged_fp8(lib, ws=A16, ws_bytes=16) == WORKSPACE
+    assert paged_fp8(lib, Sq=0) == OK
 
 
 def varlen(lib, q=A16, o=A16b, cu=A16, cukv=A16, B=2, total_q=8, total_kv=16, Hq=4, Hkv=2, D=64, ws=A16,
