@@ -106,9 +106,10 @@ def load_peaks():
 # workloads as a ratio to the algorithmic K/V bytes (their captures ran at a
 # reduced batch), for the prefill as bytes per launch of the same workload.
 TRAFFIC = {
-    "paged_decode": ("ratio", (559.378944 + 5.455360) / 556.916736),
-    "wide_group_decode": ("ratio", (233.700096 + 3.488000) / 232.683520),
-    "qwen3_8b_prefill": ("bytes", (94.945280 + 31.452928) * 1e6),
+    "paged_decode": ("ratio", (559.379712 + 6.031616) / 556.916736),
+    "wide_group_decode": ("ratio", (233.671424 + 4.135424) / 232.683520),
+    "paged_decode_fp8kv": ("ratio", (279.800320 + 4.730368) / 278.458368),
+    "qwen3_8b_prefill": ("bytes", (95.003136 + 31.002112) * 1e6),
     "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
     # captured at B=1 of 4 independent batches: traffic scales by 4
     "long_chunked_prefill": ("bytes", 4 * (537.318144 + 34.280704) * 1e6),
