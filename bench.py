@@ -112,7 +112,7 @@ TRAFFIC = {
     "qwen3_8b_prefill": ("bytes", (95.003136 + 31.002112) * 1e6),
     "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
     # captured at B=1 of 4 independent batches: traffic scales by 4
-    "long_chunked_prefill": ("bytes", 4 * (537.318144 + 34.280704) * 1e6),
+    "long_chunked_prefill": ("bytes", 4 * (534.633984 + 31.650048) * 1e6),
     "mixed_serving_batch": ("bytes", (2583.485 + 24.447744) * 1e6),
     "varlen_prefill": ("bytes", (6572.479 + 507.1168) * 1e6),
 }

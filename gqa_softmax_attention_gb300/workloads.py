@@ -21,6 +21,9 @@ round-to-nearest-even):
   ones; request b's logical pages take the next ``ceil(L_b / page_size)``
   entries of the permutation, in request order; unused block_table entries are
   -1.  Streams 0, 1, 2 are q, k_cache, v_cache.
+* Paged FP8: the paged draw, each bf16 cache value rounded to float8_e4m3fn
+  by torch, then ``k_scale`` and ``v_scale`` [B, Hkv] uniform on the workload's
+  scale range from ``Generator().manual_seed(seed * 2**32 + 3 * 2**20)``.
 
 The named workloads are the shapes of the pages' examples: a tiny GQA case, a
 Qwen3-8B-shaped prefill (Hq=32, Hkv=8, D=128), a paged decode batch of the same

@@ -75,3 +75,36 @@ def test_mixed_paged_graph_replay(g):
         ro, rl = oracle.attn_paged_varlen(p["q"], p["k_cache"], p["v_cache"], torch.tensor(cu, dtype=torch.int32),
                                           torch.tensor(lens, dtype=torch.int32), p["block_table"], causal=True)
         compare(out.cpu(), lse.cpu(), ro, rl, "mixed replay %s" % lens)
+
+
+def test_fp8kv_decode_graph_replay(g):
+    """The FP8-KV decode replays with new lengths and new scales."""
+    B, Sq, Hq, Hkv, D, ps = 6, 1, 32, 8, 128, 64
+    p = W.paged_fp8_inputs(B, Sq, Hq, Hkv, D, ps, lengths=[3000] * B, seed=9)
+    dev = {n: p[n].cuda() for n in ("q", "k_cache", "v_cache", "k_scale", "v_scale", "real_seqlen_kv",
+                                    "block_table")}
+    ws = torch.empty(g.attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, ps, p["block_table"].shape[1]),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dev["q"])
+    lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device="cuda")
+    run = lambda: g.attn_decode_paged_fp8kv(dev["q"], dev["k_cache"], dev["v_cache"], dev["k_scale"], dev["v_scale"],
+                                            dev["real_seqlen_kv"], dev["block_table"], causal=True, workspace=ws,
+                                            out=out, lse=lse)
+    run()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    gen = torch.Generator().manual_seed(10)
+    for _ in range(3):
+        lens = torch.randint(1, 3001, (B,), generator=gen, dtype=torch.int32)
+        ks = torch.rand(B, Hkv, generator=gen) + 0.1
+        vs = torch.rand(B, Hkv, generator=gen) + 0.1
+        dev["real_seqlen_kv"].copy_(lens)
+        dev["k_scale"].copy_(ks)
+        dev["v_scale"].copy_(vs)
+        graph.replay()
+        torch.cuda.synchronize()
+        ro, rl = oracle.attn_paged_fp8kv(p["q"], p["k_cache"], p["v_cache"], ks, vs, lens, p["block_table"],
+                                         causal=True)
+        compare(out.cpu(), lse.cpu(), ro, rl, "fp8 decode replay")
