@@ -697,7 +697,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // the output map, and one thread stores each box with TMA: whole
             // 128-byte rows instead of 16-byte pieces strided by Hq * D.  Rows
             // past Sq lie outside the map and are not written.  A tile with no
-            // visited key, or a wait that gave up, writes zeros directly.
+            // visited key, or a wait that gave up, writes zeros directly.  The
+            // last box of an item is left reading while the warpgroup moves on;
+            // the storing thread waits for it before the buffer is written again.
+            if (r == 0) bulk_wait_read_all();
+            __syncwarp();
             const bool staged = named_bar_and(3 + k, BM, ok && it > 0);
             if (staged) {
                 uint32_t ow[D];
@@ -724,7 +728,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (r == 0) {
                         tma_store_4d(&tm_o, stage, sub * 64, ti.q0, itm.hq, itm.b);
                         bulk_commit_group();
-                        bulk_wait_read_all();
+                        if (sub + 1 < C::KSUB) bulk_wait_read_all();
                     }
                 }
             } else if (row_ok) {
@@ -737,6 +741,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_before();
             if (!named_bar_and(3 + k, BM, ok)) break;     // the whole warpgroup stops together
         }
+        if (r == 0) bulk_wait_all();                    // the last stores are done before the CTA ends
+        __syncwarp();
         named_bar_arrive(2, 8 * 32 + 32);
         if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_prefill_error, (int)kErrPrefillWait);
     }

@@ -145,6 +145,8 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// Wait until every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // The same, allowing the most recent committed group to be still reading.
 __device__ __forceinline__ void bulk_wait_read_1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
