@@ -50,7 +50,7 @@ typedef struct CUstream_st* gqa_stream_t;
 typedef enum {
     GQA_OK = 0,
     GQA_ERR_INVALID_ARG = 1,  /* a size or pointer argument is out of range */
-    GQA_ERR_UNSUPPORTED = 2,  /* a valid combination this build has no kernel for */
+    GQA_ERR_UNSUPPORTED = 2,  /* a valid combination the library has no kernel for */
     GQA_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
     GQA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
     GQA_ERR_CUDA = 5,         /* a CUDA call or kernel launch failed */
