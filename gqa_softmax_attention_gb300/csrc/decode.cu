@@ -540,49 +540,61 @@ decode_gather_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
 // ---------------------------------------------------------------------------
 // float8_e4m3fn caches (TileOPs "Attention Operators", GQADenseFwdOp stage 2:
 // K^ = K * k_scale and V' = V * v_scale, one scale per request and KV head).
-// The producer brings the cache bytes in with TMA (128-byte rows, 128-byte
-// swizzle); the consumer warps take their K and V fragments straight from
-// those tiles with ldmatrix (two e4m3 per 16-bit element) and widen them to
-// float16 in registers (exact: every e4m3fn value is a float16), then run
-// float16 MMAs with FP32 accumulation.  Q is rounded to float16 once (a
-// bfloat16 Q keeps every bit for magnitudes in [2^-14, 65504]) and P is packed
-// to float16; k_scale joins the softmax scale and the softcap's input, v_scale
-// the stored partial O.
+// One CTA per (split, KV head, request, row block), as in the 16-bit split
+// path.  The producer brings the cache bytes in with TMA (128-byte rows,
+// 128-byte swizzle).  Each consumer warp owns one 16-row fragment and a fixed
+// share of every key tile (16 or 32 keys) and keeps its own online softmax
+// over those keys, with scores, P and O in its registers: no barrier joins the
+// warps while the tiles stream, and the warps sharing a fragment merge their
+// (max, sum, O) once, through shared memory, after the last tile.  K and V
+// fragments come straight from the e4m3 tiles by ldmatrix (two e4m3 per
+// 16-bit element) and are widened to float16 in registers (exact: every e4m3fn
+// value is a float16); the MMAs run in float16 with FP32 accumulation.  Q is
+// rounded to float16 once (a bfloat16 Q keeps every bit for magnitudes in
+// [2^-14, 65504]) and P is packed to float16; k_scale joins the softmax scale
+// and the softcap's input, v_scale the stored partial O.
 //   S = Q K^T: ldmatrix gives lane t four consecutive dims 4(t%4)..4(t%4)+3 of
 //     a key in each 16-dim k-step; the first two serve as k = 2(t%4), 2(t%4)+1
 //     of the m16n8k16 fragment and the last two as k = 2(t%4)+8, +9, and Q's
 //     fragments are loaded under the same map, so every dot product is the
 //     same sum in another order.
+//   P: the score accumulators of key blocks 2j and 2j+1 are the A fragment of
+//     P V's k-step j, packed in place.
 //   O += P V: ldmatrix.trans gives lane t, for keys 2(t%4) and 2(t%4)+1, the
 //     two dims 2(t/4), 2(t/4)+1 of a 16-dim chunk; a byte permute splits them
 //     into an even-dim and an odd-dim n8 block, and the stored O interleaves
 //     the two blocks back into dim order.
 template <int D, int MF>
-struct F8Cfg : DCfg<D, MF, true, true> {
-    using B16 = DCfg<D, MF, true, true>;
-    static constexpr int SUB8 = B16::TK * 128;                 // 128 e4m3 columns of a tile
+struct F8Cfg {
+    static constexpr int TK = key_tile(D);                  // keys per tile (64, or 32 at D = 256)
+    static constexpr int ROWS = 16 * MF;                    // padded rows per CTA
+    static constexpr int KSPLIT = MF == 1 ? TK / 16 : TK / 32;   // warps per fragment, splitting each tile
+    static constexpr int KPW = TK / KSPLIT;                 // keys of a tile per warp (16 or 32)
+    static constexpr int NC = MF * KSPLIT;                  // consumer warps
+    static constexpr int NCT = NC * 32;
+    static constexpr int NT = NCT + 32;                     // + producer warp
+    static constexpr int SUB8 = TK * 128;                   // 128 e4m3 columns of a tile
     static constexpr int NSUB8 = D / 128;
-    static constexpr int TILE8 = NSUB8 * SUB8;                 // one K or V tile of bytes
-    static constexpr int FIXED8 = B16::Q_BYTES + B16::ROWS * B16::S_STRIDE * 4 + B16::ROWS * 128 +
-                                  3 * B16::ROWS * 4 + 1024 + 256;
-    // three CTAs per SM for the small row blocks at D = 128, else two
+    static constexpr int TILE8 = NSUB8 * SUB8;              // one K or V tile of bytes
+    static constexpr int KSTEPS = D / 16;
+    static constexpr int NFK = KPW / 8;                     // key blocks of a warp's S
+    static constexpr int NFD = D / 8;                       // dim blocks of O
+    static constexpr int MROW = D + 4;                      // merge row: O, max, sum (16-byte rows)
+    static constexpr int MERGE = KSPLIT > 1 ? NC * 16 * MROW * 4 : 0;
+    // byte ring: up to three CTAs per SM by shared memory at D = 128 with one or two fragments
     static constexpr int BUDGET = (D == 128 && MF <= 2) ? 75 * 1024 : 113 * 1024;
-    static constexpr int NS_FIT8 = (BUDGET - FIXED8) / (2 * TILE8);
-    static constexpr int NS = NS_FIT8 < 6 ? NS_FIT8 : 6;
-    static constexpr int OFF_KV = 0;                           // 1024-aligned byte ring first
-    static constexpr int OFF_Q = OFF_KV + NS * 2 * TILE8;
-    static constexpr int OFF_S = OFF_Q + B16::Q_BYTES;
-    static constexpr int OFF_P = OFF_S + B16::ROWS * B16::S_STRIDE * 4;
-    static constexpr int OFF_A = OFF_P + B16::ROWS * 128;
-    static constexpr int OFF_L = OFF_A + B16::ROWS * 4;
-    static constexpr int OFF_M = OFF_L + B16::ROWS * 4;
-    static constexpr int OFF_BAR = OFF_M + B16::ROWS * 4;      // full[NS], empty[NS]
+    static constexpr int NS_FIT = (BUDGET - 2048) / (2 * TILE8);
+    static constexpr int NS = NS_FIT < 6 ? NS_FIT : 6;
+    static constexpr int RING = NS * 2 * TILE8;
+    static constexpr int MINB = (D == 128 && MF == 1) ? 2 : 1;   // CTAs per SM the registers must allow
+    static constexpr int OFF_KV = 0;                        // byte ring; the merge reuses it
+    static constexpr int OFF_BAR = RING > MERGE ? RING : MERGE;   // full[NS], empty[NS]
     static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
     static constexpr int SMEM = OFF_FLAG + 16 + 1024;
     static_assert(D == 128 || D == 256, "e4m3 rows of 128 or 256 bytes");
-    static_assert(B16::DSL % 32 == 0, "P V takes 32-dim groups");
-    static_assert(NS >= 2, "pipeline depth");
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(KPW % 16 == 0 && NFK % 2 == 0, "whole P V k-steps per warp");
+    static_assert((MROW * 4) % 16 == 0, "float4 rows in the merge area");
+    static_assert(NS >= 2 && SMEM <= 227 * 1024, "pipeline depth / shared memory budget");
 };
 
 // Two e4m3fn codes (low byte first) -> two float16 (low half first), exactly.
@@ -597,133 +609,14 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <class C>
-struct Consumer8 : Consumer<C> {
-    // Byte offset of 16-byte chunk c (16 dims) of key row r in an e4m3 tile.
-    static __device__ __forceinline__ uint32_t off8(int r, int c) {
-        return (uint32_t)((c >> 3) * C::SUB8 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-    }
-
-    // Q's fragments under the dim map of the S products (Q already in smem).
-    __device__ __forceinline__ void q_fragments(bool qbf) {
-        const int t4 = this->lane & 3;
-#pragma unroll
-        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            const int chunk = 2 * kk + (t4 >> 1);              // 8-element chunk holding dims 16kk + 4(t%4)..
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = this->mf * 16 + (this->lane >> 2) + 8 * h;
-                const uint2 v = *reinterpret_cast<const uint2*>(this->smem + C::OFF_Q +
-                                                                 sw_off(row, chunk, C::ROWS * 128) + (t4 & 1) * 8);
-                this->qf[kk][h] = qbf ? bf16x2_to_f16x2(v.x) : v.x;       // k = 2(t%4), +1
-                this->qf[kk][2 + h] = qbf ? bf16x2_to_f16x2(v.y) : v.y;   // k = 2(t%4) + 8, +9
-            }
-        }
-    }
-
-    // S = Q K^T for this warp's rows and keys from the e4m3 key tile at sK.
-    __device__ __forceinline__ void qk8(uint32_t sK, int t0, float sl) {
-        float sacc[C::NFK][4];
-#pragma unroll
-        for (int n = 0; n < C::NFK; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-        const int m = this->lane >> 3;
-#pragma unroll
-        for (int kk = 0; kk < C::KSTEPS; kk += 2) {
-#pragma unroll
-            for (int nb = 0; nb < C::NFK; nb += 2) {
-                // matrices: (block nb, step kk), (nb, kk+1), (nb+1, kk), (nb+1, kk+1)
-                const int key = this->wk * C::KEYS_PER_WARP + (nb + (m >> 1)) * 8 + (this->lane & 7);
-                uint32_t r[4];
-                ldsm_x4(sK + off8(key, kk + (m & 1)), r[0], r[1], r[2], r[3]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    mma16816<true>(sacc[nb + (j >> 1)], this->qf[kk + (j & 1)], e4m3x2_to_f16x2(r[j]),
-                                   e4m3x2_to_f16x2(r[j] >> 16));
-            }
-        }
-        this->write_s(sacc, t0, sl);
-    }
-
-    // O = O * alpha + P V for this warp's rows and dims from the e4m3 value tile
-    // at sV.  acc[4q + 2i + e]: dims of 16-dim chunk i of group q with parity e.
-    __device__ __forceinline__ void pv8(uint32_t sV) {
-        const float* sAlpha = reinterpret_cast<const float*>(this->smem + C::OFF_A);
-        const int lane = this->lane, mf = this->mf;
-        const float a0 = sAlpha[mf * 16 + (lane >> 2)];
-        const float a1 = sAlpha[mf * 16 + (lane >> 2) + 8];
-#pragma unroll
-        for (int n = 0; n < C::NFD; ++n) {
-            this->acc[n][0] *= a0; this->acc[n][1] *= a0;
-            this->acc[n][2] *= a1; this->acc[n][3] *= a1;
-        }
-        const int m = lane >> 3;
-#pragma unroll
-        for (int kk = 0; kk < C::TK / 16; ++kk) {
-            uint32_t pa[4];
-            {
-                const int row = mf * 16 + (lane & 15);
-                const int chunk = kk * 2 + (lane >> 4);
-                ldsm_x4(this->sb + C::OFF_P + row * 128 + ((chunk ^ (row & 7)) << 4), pa[0], pa[1], pa[2], pa[3]);
-            }
-#pragma unroll
-            for (int q = 0; q < C::DSL / 32; ++q) {
-                // matrices: (keys 0-7, chunk c0), (keys 8-15, c0), (keys 0-7, c0+1), (keys 8-15, c0+1)
-                const int c0 = (this->wk * C::DSL + 32 * q) / 16;
-                const int key = kk * 16 + (m & 1) * 8 + (lane & 7);
-                uint32_t r[4];
-                ldsm_x4_t(sV + off8(key, c0 + (m >> 1)), r[0], r[1], r[2], r[3]);
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    // bytes: V[k0][d], V[k0][d+1], V[k1][d], V[k1][d+1] (d even)
-                    mma16816<true>(this->acc[4 * q + 2 * i], pa, e4m3x2_to_f16x2(__byte_perm(r[2 * i], 0, 0x0020)),
-                                   e4m3x2_to_f16x2(__byte_perm(r[2 * i + 1], 0, 0x0020)));
-                    mma16816<true>(this->acc[4 * q + 2 * i + 1], pa,
-                                   e4m3x2_to_f16x2(__byte_perm(r[2 * i], 0, 0x0031)),
-                                   e4m3x2_to_f16x2(__byte_perm(r[2 * i + 1], 0, 0x0031)));
-                }
-            }
-        }
-    }
-
-    // Normalised partial O (FP32, dims back in order) and base-2 LSE of this split.
-    template <class Bar>
-    __device__ __forceinline__ void store8(const DecodeArgs& a, const Work& w, int R, Bar bar) {
-        float* sL = reinterpret_cast<float*>(this->smem + C::OFF_L);
-        float* sM = reinterpret_cast<float*>(this->smem + C::OFF_M);
-        if (this->ssub == 0) {
-            sL[this->srow] = this->l_run;
-            sM[this->srow] = this->m_run;
-        }
-        bar();
-        const int lane = this->lane;
-        const size_t part_row0 = ((size_t)(w.b * a.Hkv + w.hkv) * a.max_splits + w.split) * R + w.row0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int rl = this->mf * 16 + (lane >> 2) + 8 * h;
-            if (rl < w.rows_here) {
-                const float l = sL[rl];
-                const float inv = l > 0.f ? this->out_scale / l : 0.f;
-                float* dst = a.part_o + (part_row0 + rl) * (C::NSUB * 64) + this->wk * C::DSL + 4 * (lane & 3);
-#pragma unroll
-                for (int q = 0; q < C::DSL / 32; ++q)
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const float* e = this->acc[4 * q + 2 * i];
-                        const float* o = this->acc[4 * q + 2 * i + 1];
-                        *reinterpret_cast<float4*>(dst + 32 * q + 16 * i) =
-                            make_float4(e[2 * h] * inv, o[2 * h] * inv, e[2 * h + 1] * inv, o[2 * h + 1] * inv);
-                    }
-            }
-        }
-        if (this->ctid < w.rows_here) {
-            const float l = sL[this->ctid];
-            a.part_lse[part_row0 + this->ctid] = l > 0.f ? sM[this->ctid] + log2f(l) : -INFINITY;
-        }
-    }
-};
+// Byte offset of 16-byte chunk c (16 dims) of key row r in an e4m3 tile.
+template <int SUB8>
+__device__ __forceinline__ uint32_t off8(int r, int c) {
+    return (uint32_t)((c >> 3) * SUB8 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
 
 template <int D, int MF, bool QBF>
-__global__ void __launch_bounds__(F8Cfg<D, MF>::NT)
+__global__ void __launch_bounds__(F8Cfg<D, MF>::NT, F8Cfg<D, MF>::MINB)
 decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeArgs a, int R, int g, int n_rowblk, int box_tokens) {
     using C = F8Cfg<D, MF>;
@@ -750,9 +643,10 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __syncthreads();
 
     const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
     if (warp == C::NC) {
         // ------------------------------------------------------------ TMA producer
-        if ((threadIdx.x & 31) == 0) {
+        if (lane == 0) {
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             const int32_t* trow = a.table + (size_t)w.b * a.max_pages;
@@ -797,46 +691,233 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             }
         }
     } else {
-        // ------------------------------------------------------------ consumers
-        Consumer8<C> c;
-        c.init(smem, sb, a, w, g);
+        // ------------------------------------------------------------ consumer warps
+        const int mf = warp / C::KSPLIT;            // row fragment
+        const int wk = warp % C::KSPLIT;            // share of each key tile
+        const int kw0 = wk * C::KPW;                // this warp's first key of a tile
+        const int t4 = lane & 3;
         const int kv = w.b * a.Hkv + w.hkv;
         const float ks = a.k_scale ? a.k_scale[kv] : 1.f;
-        c.out_scale = a.v_scale ? a.v_scale[kv] : 1.f;
-        c.cap_in *= ks;
-        auto bar = [] { named_bar_sync(1, C::NCT); };
-        c.load_q(a, w, g, bar);
-        c.q_fragments(QBF);
+        const float vs = a.v_scale ? a.v_scale[kv] : 1.f;
         const float sl = a.scale_log2 * ks;
+        const float cap_in = a.x.cap_in * ks, cap_out = a.x.cap_out;
+        // rows g and g + 8 of the fragment: key range [lo, lim) and Q fragments
+        int lim[2], lo[2];
+        uint32_t qf[C::KSTEPS][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int rl = mf * 16 + (lane >> 2) + 8 * h;
+            const int r = w.row0 + rl;
+            const bool valid = rl < w.rows_here;
+            lo[h] = 0;
+            lim[h] = -1;
+            if (valid) {
+                // keys [lo, lim) of query r / g at key position p (TileOPs
+                // GQAPagedFwdOp: causal j <= p, window p - wL <= j <= p + wR)
+                const long p = (long)(r / g) + w.L - a.Sq;
+                long hi = w.t_end;
+                if (a.causal) hi = min(hi, p + 1);
+                if (a.x.wr >= 0) hi = min(hi, p + a.x.wr + 1);
+                lim[h] = (int)max(-1L, hi);
+                if (a.x.wl >= 0) lo[h] = (int)max(0L, min((long)w.L, p - a.x.wl));
+            }
+            const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.q) +
+                                   (((size_t)w.b * a.Sq + r / g) * a.Hq + w.hkv * g + r % g) * D;
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                uint2 v = make_uint2(0u, 0u);
+                if (valid) v = *reinterpret_cast<const uint2*>(qrow + 16 * kk + 4 * t4);
+                qf[kk][h] = QBF ? bf16x2_to_f16x2(v.x) : v.x;          // k = 2(t%4), +1
+                qf[kk][2 + h] = QBF ? bf16x2_to_f16x2(v.y) : v.y;      // k = 2(t%4) + 8, +9
+            }
+        }
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+        float acc[C::NFD][4];
+#pragma unroll
+        for (int n = 0; n < C::NFD; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        const int m = lane >> 3;                    // ldmatrix: this lane addresses matrix m
         for (int it = 0; it < w.n_tiles; ++it) {
             const int s = it % C::NS;
             const int t0 = w.t_begin + it * C::TK;
             const uint32_t sK = sb + C::OFF_KV + s * 2 * C::TILE8;
             const uint32_t sV = sK + C::TILE8;
-            const bool ok = mbar_wait(full(s), (it / C::NS) & 1, abort_flag);
-            if (ok) {
-                const int nvalid = w.t_end - t0;
-                if (nvalid < C::TK) {
-                    // Value rows past the request's end hold stale bytes: zero them.
-                    const int per_sub = (C::TK - nvalid) * 8;
-                    for (int idx = c.ctid; idx < per_sub * C::NSUB8; idx += C::NCT) {
-                        const int sub = idx / per_sub;
-                        const int rem = idx % per_sub;
-                        *reinterpret_cast<uint4*>(smem + (sV - sb) + sub * C::SUB8 + (nvalid + rem / 8) * 128 +
-                                                  (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
-                }
-                c.qk8(sK, t0, sl);
+            if (!__all_sync(0xffffffffu, mbar_wait(full(s), (it / C::NS) & 1, abort_flag))) break;
+            const int nvalid = w.t_end - t0;
+            if (nvalid < kw0 + C::KPW) {
+                // This warp's value rows past the request's end hold stale bytes:
+                // zero them (no other warp reads them).
+                const int r0 = nvalid > kw0 ? nvalid : kw0;
+                const int per_sub = (kw0 + C::KPW - r0) * 8;
+                for (int idx = lane; idx < per_sub * C::NSUB8; idx += 32)
+                    *reinterpret_cast<uint4*>(smem + (sV - sb) + (idx / per_sub) * C::SUB8 +
+                                              (r0 + (idx % per_sub) / 8) * 128 + (idx % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                __syncwarp();
             }
-            if (!named_bar_and(1, C::NCT, ok)) break;   // every consumer leaves together
-            c.softmax();
-            named_bar_sync(1, C::NCT);
-            c.pv8(sV);
+            // ---- S = Q K^T over this warp's keys of the tile
+            float sc[C::NFK][4];
+#pragma unroll
+            for (int n = 0; n < C::NFK; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; kk += 2) {
+#pragma unroll
+                for (int nb = 0; nb < C::NFK; nb += 2) {
+                    // matrices: (block nb, step kk), (nb, kk+1), (nb+1, kk), (nb+1, kk+1)
+                    uint32_t r[4];
+                    ldsm_x4(sK + off8<C::SUB8>(kw0 + (nb + (m >> 1)) * 8 + (lane & 7), kk + (m & 1)), r[0], r[1],
+                            r[2], r[3]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma16816<true>(sc[nb + (j >> 1)], qf[kk + (j & 1)], e4m3x2_to_f16x2(r[j]),
+                                       e4m3x2_to_f16x2(r[j] >> 16));
+                }
+            }
+            // ---- scaled, masked logits (log2 units) and the rows' maxima
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int n = 0; n < C::NFK; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = e >> 1;
+                    const int t = t0 + kw0 + 8 * n + 2 * t4 + (e & 1);
+                    float x = cap_out != 0.f ? softcap_log2(sc[n][e], cap_in, cap_out) : sc[n][e] * sl;
+                    x = t >= lo[h] && t < lim[h] ? x : -INFINITY;       // the select drops stale keys
+                    sc[n][e] = x;
+                    mx[h] = fmaxf(mx[h], x);
+                }
+            float alpha[2], m_use[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                const float m_new = fmaxf(m_run[h], mx[h]);
+                m_use[h] = m_new == -INFINITY ? 0.f : m_new;           // no -inf - -inf
+                alpha[h] = fast_exp2(m_run[h] - m_use[h]);
+                m_run[h] = m_new;
+            }
+            // ---- P (float16) as P V's A fragments, this lane's share of the row sums
+            uint32_t pa[C::KPW / 16][4];
+            float rs[2] = {0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < C::KPW / 16; ++j)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const float* x = sc[2 * j + half];
+                    const float p0 = fast_exp2(x[0] - m_use[0]), p1 = fast_exp2(x[1] - m_use[0]);
+                    const float p2 = fast_exp2(x[2] - m_use[1]), p3 = fast_exp2(x[3] - m_use[1]);
+                    rs[0] += p0 + p1;
+                    rs[1] += p2 + p3;
+                    pa[j][2 * half] = pack2<true>(p0, p1);         // row g, keys 16j + 8 half + 2(t%4), +1
+                    pa[j][2 * half + 1] = pack2<true>(p2, p3);     // row g + 8
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + rs[h];
+#pragma unroll
+            for (int n = 0; n < C::NFD; ++n) {
+                acc[n][0] *= alpha[0]; acc[n][1] *= alpha[0];
+                acc[n][2] *= alpha[1]; acc[n][3] *= alpha[1];
+            }
+            // ---- O += P V over all dims; acc[4q + 2i + e]: chunk i of the 32-dim
+            // group q, dims of parity e
+#pragma unroll
+            for (int kk = 0; kk < C::KPW / 16; ++kk) {
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    // matrices: (keys 0-7, chunk 2q), (keys 8-15, 2q), (keys 0-7, 2q+1), (keys 8-15, 2q+1)
+                    uint32_t r[4];
+                    ldsm_x4_t(sV + off8<C::SUB8>(kw0 + kk * 16 + (m & 1) * 8 + (lane & 7), 2 * q + (m >> 1)), r[0],
+                              r[1], r[2], r[3]);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        // bytes: V[k0][d], V[k0][d+1], V[k1][d], V[k1][d+1] (d even)
+                        mma16816<true>(acc[4 * q + 2 * i], pa[kk], e4m3x2_to_f16x2(__byte_perm(r[2 * i], 0, 0x0020)),
+                                       e4m3x2_to_f16x2(__byte_perm(r[2 * i + 1], 0, 0x0020)));
+                        mma16816<true>(acc[4 * q + 2 * i + 1], pa[kk],
+                                       e4m3x2_to_f16x2(__byte_perm(r[2 * i], 0, 0x0031)),
+                                       e4m3x2_to_f16x2(__byte_perm(r[2 * i + 1], 0, 0x0031)));
+                    }
+                }
+            }
             __syncwarp();
-            if (c.lane == 0) mbar_arrive(empty(s));
+            if (lane == 0) mbar_arrive(empty(s));      // this warp is done with the stage
         }
-        c.store8(a, w, R, bar);
+        // ---- merge the warps of a fragment and store the split's partial O (FP32,
+        // dims in order, normalised) and base-2 LSE
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+        }
+        const size_t part_row0 = ((size_t)(w.b * a.Hkv + w.hkv) * a.max_splits + w.split) * R + w.row0;
+        if constexpr (C::KSPLIT == 1) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int rl = mf * 16 + (lane >> 2) + 8 * h;
+                if (rl >= w.rows_here) continue;
+                const float l = l_run[h];
+                const float inv = l > 0.f ? vs / l : 0.f;
+                float* dst = a.part_o + (part_row0 + rl) * D + 4 * t4;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const float* ev = acc[4 * q + 2 * i];
+                        const float* od = acc[4 * q + 2 * i + 1];
+                        *reinterpret_cast<float4*>(dst + 32 * q + 16 * i) =
+                            make_float4(ev[2 * h] * inv, od[2 * h] * inv, ev[2 * h + 1] * inv, od[2 * h + 1] * inv);
+                    }
+                if (t4 == 0) a.part_lse[part_row0 + rl] = l > 0.f ? m_run[h] + log2f(l) : -INFINITY;
+            }
+        } else {
+            named_bar_sync(1, C::NCT);                  // every consumer warp is done with the ring
+            float* mg = reinterpret_cast<float*>(smem + C::OFF_KV);
+            float* mine = mg + (size_t)warp * 16 * C::MROW;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int rr = (lane >> 2) + 8 * h;     // row within the fragment
+                float* row = mine + rr * C::MROW;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const float* ev = acc[4 * q + 2 * i];
+                        const float* od = acc[4 * q + 2 * i + 1];
+                        *reinterpret_cast<float4*>(row + 32 * q + 16 * i + 4 * t4) =
+                            make_float4(ev[2 * h], od[2 * h], ev[2 * h + 1], od[2 * h + 1]);
+                    }
+                if (t4 == 0) {
+                    row[D] = m_run[h];
+                    row[D + 1] = l_run[h];
+                }
+            }
+            named_bar_sync(1, C::NCT);
+            // warp (mf, wk) merges dims [wk * D / KSPLIT, (wk + 1) * D / KSPLIT) of fragment mf
+            const float* frag = mg + (size_t)(mf * C::KSPLIT) * 16 * C::MROW;
+            constexpr int DW = D / C::KSPLIT;
+            for (int rr = 0; rr < 16; ++rr) {
+                const int rl = mf * 16 + rr;
+                if (rl >= w.rows_here) break;
+                float M = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < C::KSPLIT; ++u) M = fmaxf(M, frag[(u * 16 + rr) * C::MROW + D]);
+                const float M_use = M == -INFINITY ? 0.f : M;
+                float wgt[C::KSPLIT], L = 0.f;
+#pragma unroll
+                for (int u = 0; u < C::KSPLIT; ++u) {
+                    wgt[u] = fast_exp2(frag[(u * 16 + rr) * C::MROW + D] - M_use);
+                    L += wgt[u] * frag[(u * 16 + rr) * C::MROW + D + 1];
+                }
+                const float inv = L > 0.f ? vs / L : 0.f;
+                for (int d = wk * DW + lane; d < (wk + 1) * DW; d += 32) {
+                    float o = 0.f;
+#pragma unroll
+                    for (int u = 0; u < C::KSPLIT; ++u) o += wgt[u] * frag[(u * 16 + rr) * C::MROW + d];
+                    a.part_o[(part_row0 + rl) * D + d] = o * inv;
+                }
+                if (wk == 0 && lane == 0) a.part_lse[part_row0 + rl] = L > 0.f ? M + log2f(L) : -INFINITY;
+            }
+        }
     }
     if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_decode_error, (int)kErrDecodeWait);
 }

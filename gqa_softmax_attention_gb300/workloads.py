@@ -56,6 +56,8 @@ WORKLOADS = {
     # the paged decode batch over float8_e4m3fn caches with per-(request, KV head) scales
     "paged_decode_fp8kv": dict(kind="paged_fp8", B=64, Sq=1, Hq=32, Hkv=8, D=128, page_size=64, causal=True,
                                sigma=1.0, lengths=(1024, 16384), spare=0.10, scale_range=(0.25, 1.0)),
+    "wide_group_decode_fp8kv": dict(kind="paged_fp8", B=32, Sq=4, Hq=24, Hkv=2, D=256, page_size=16, causal=True,
+                                    sigma=1.0, lengths=(512, 32768), spare=0.10, scale_range=(0.25, 1.0)),
     # one serving step over a paged cache: 60 decode steps (one query each,
     # cache lengths U[1024, 16384]) and 4 prefill chunks of 1024 queries whose
     # caches hold U[0, 8192] earlier tokens plus the chunk
