@@ -124,8 +124,9 @@ def test_matches_16bit_path_on_widened_cache(g):
     compare(o8, l8, o16.cpu().double(), l16.cpu().double(), "fp8 vs fp16 path")
 
 
-def test_full_size_workload(g):
-    p = W.make("paged_decode_fp8kv")
+@pytest.mark.parametrize("name", ["paged_decode_fp8kv", "wide_group_decode_fp8kv"])
+def test_full_size_workload(g, name):
+    p = W.make(name)
     o, lse = run(g, p)
     L = p["real_seqlen_kv"]
     order = torch.argsort(L)
@@ -135,5 +136,5 @@ def test_full_size_workload(g):
     ro, rl = oracle.attn_paged_fp8kv(p["q"], p["k_cache"], p["v_cache"], p["k_scale"], p["v_scale"], L,
                                      p["block_table"], requests=reqs)
     sel = torch.tensor(reqs)
-    compare(o[sel], lse[sel], ro[sel], rl[sel], "paged_decode_fp8kv")
+    compare(o[sel], lse[sel], ro[sel], rl[sel], name)
     assert not torch.isnan(o.float()).any() and bool(torch.isfinite(lse).all())
