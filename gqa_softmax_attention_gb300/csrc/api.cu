@@ -306,6 +306,23 @@ static bool make_cache_map_fp8(CUtensorMap* map, const void* ptr, long rows, int
     return r == CUDA_SUCCESS;
 }
 
+// Paged cache of e4m3fn bytes as a 5-D map {128, 8, D / 128, pages * page_size / 8,
+// Hkv}: a {128, 8, D / 128, box_tokens / 8, 1} box brings one page block of
+// one head and lands as [8-row group][128-column half][8 rows][128 bytes].
+static bool make_cache_page_map_fp8(CUtensorMap* map, const void* ptr, long rows, int Hkv, int D, int box_tokens) {
+    auto fn = encode_fn();
+    if (!fn || rows % 8 != 0 || box_tokens % 8 != 0) return false;
+    const cuuint64_t row_bytes = (cuuint64_t)Hkv * D;
+    const cuuint64_t dims[5] = {128, 8, (cuuint64_t)(D / 128), (cuuint64_t)(rows / 8), (cuuint64_t)Hkv};
+    const cuuint64_t strides[4] = {row_bytes, 128, 8 * row_bytes, (cuuint64_t)D};
+    const cuuint32_t box[5] = {128, 8, (cuuint32_t)(D / 128), (cuuint32_t)(box_tokens / 8), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 gqa_status attn_decode_paged_fp8kv(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                                    const float* v_scale, const int32_t* real_seqlen_kv, const int32_t* block_table,
                                    int page_size, void* o, float* lse, int B, int Sq, int Hq, int Hkv, int D,
@@ -331,9 +348,8 @@ gqa_status attn_decode_paged_fp8kv(const void* q, const void* k_cache, const voi
     if (es != GQA_OK) return es;
     DecodePlan p;
     if (!gqa::plan_decode(B, Sq, Hq, Hkv, D, page_size, max_pages, sm_count(), &p)) return GQA_ERR_UNSUPPORTED;
-    // the split path's partials: never more than attn_decode_paged_workspace_size
-    const size_t need = (p.part_o_bytes + 255) / 256 * 256 + (p.part_lse_bytes + 255) / 256 * 256;
-    if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+    // the partials of whichever path the sizes select (attn_decode_paged_workspace_size)
+    if (!workspace || workspace_bytes < p.workspace_bytes) return GQA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GQA_ERR_MISALIGNED;
 
     DecodeArgs a{};
@@ -354,12 +370,28 @@ gqa_status attn_decode_paged_fp8kv(const void* q, const void* k_cache, const voi
     a.v_scale = v_scale;
     // with an empty pool no page is ever loaded; the maps then describe one page
     const long rows = (long)(num_pages > 0 ? num_pages : 1) * page_size;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     CUtensorMap tk, tv;
+    // KV groups of 32..128 query rows: the balanced tensor-core decode, its
+    // byte tiles widened in shared memory
+    if (p.tc) {
+        const int tbox = gqa::decode_tc_box_tokens(page_size);
+        if (!make_cache_page_map_fp8(&tk, k_cache, rows, Hkv, D, tbox) ||
+            !make_cache_page_map_fp8(&tv, v_cache, rows, Hkv, D, tbox))
+            return GQA_ERR_CUDA;
+        char* ws = static_cast<char*>(workspace);
+        const size_t o_bytes = (p.tc_part_o_bytes + 255) / 256 * 256;
+        const size_t l_bytes = (p.tc_part_lse_bytes + 255) / 256 * 256;
+        a.part_o = reinterpret_cast<float*>(ws);
+        a.part_lse = reinterpret_cast<float*>(ws + o_bytes);
+        a.seg_table = reinterpret_cast<int*>(ws + o_bytes + l_bytes);
+        a.n_part = p.n_part;
+        a.tc_grid = p.tc_grid;
+        return gqa::launch_decode_tc_fp8(tk, tv, a, tbox, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    }
     if (!make_cache_map_fp8(&tk, k_cache, rows, Hkv, D, box) || !make_cache_map_fp8(&tv, v_cache, rows, Hkv, D, box))
         return GQA_ERR_CUDA;
-    return gqa::launch_decode_fp8(a, tk, tv, box, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? GQA_OK
-               : GQA_ERR_CUDA;
+    return gqa::launch_decode_fp8(a, tk, tv, box, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------- packed calls

@@ -51,6 +51,9 @@
 // Rows past g * Sq in the 128-row M dimension are padding; their results are
 // never stored.  Value rows past a request's end are zeroed in shared memory
 // before P V reads them.  Every wait is bounded (ptx.cuh).
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <cmath>
 
 #include "internal.h"
@@ -66,9 +69,14 @@ constexpr int BN = 64;             // keys per tile
 constexpr int NUM_THREADS = 192;   // warps 0-3 softmax, 4 producer, 5 MMA
 constexpr int WARP_LOAD = 4;
 constexpr int WARP_MMA = 5;
+// e4m3 caches: warps 6-7 widen each byte tile into the 16-bit rings
+constexpr int WARP_W0 = 6;
+constexpr int NUM_W = 2;
+template <bool KV8>
+constexpr int num_threads() { return NUM_THREADS + (KV8 ? 32 * NUM_W : 0); }
 constexpr float kRescaleThreshold = 8.f;
 
-template <int D>
+template <int D, bool KV8 = false>
 struct TCfg {
     static constexpr int NSUB = D / 64;
     // Shared-memory layout of a 64-key K or V tile: [8-key group][64-column
@@ -81,14 +89,25 @@ struct TCfg {
     // flight per SM covers the memory latency at full bandwidth.  V tiles are
     // consumed about two tiles after their K (P V follows the softmax), so the
     // V ring is deeper.
-    static constexpr int NK = D == 256 ? 3 : 4;
-    static constexpr int NV = D == 256 ? 4 : 6;
-    static constexpr int OFF_K = 0;
+    // With e4m3 caches the byte tiles (TMA, 3-D boxes of 128-byte rows) come
+    // first and the 16-bit rings the wideners fill are shallower.
+    static constexpr int NK = KV8 ? (D == 256 ? 2 : 3) : (D == 256 ? 3 : 4);
+    static constexpr int NV = KV8 ? (D == 256 ? 3 : 4) : (D == 256 ? 4 : 6);
+    static constexpr int NSUB8 = D / 128;                  // 128-column halves of an e4m3 row
+    // e4m3 tile: [8-key group][128-column half][8 keys][128 bytes], 128-byte swizzle
+    static constexpr int GROUP8 = NSUB8 * 1024;
+    static constexpr int TILE8 = KV8 ? NSUB8 * BN * 128 : 0;   // one K or V tile of bytes
+    static constexpr int NK8 = KV8 ? (D == 256 ? 2 : 4) : 0;
+    static constexpr int NV8 = NK8;
+    static constexpr int OFF_K8 = 0;
+    static constexpr int OFF_V8 = OFF_K8 + NK8 * TILE8;
+    static constexpr int OFF_K = OFF_V8 + NV8 * TILE8;
     static constexpr int OFF_V = OFF_K + NK * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
     // q_ready, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
-    // p_full[2], o_done, drain, q_next
-    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 1 + 1 + 1;
+    // p_full[2], o_done, drain, q_next, then k8_full[NK8], k8_empty[NK8],
+    // v8_full[NV8], v8_empty[NV8]
+    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 1 + 1 + 1 + 2 * NK8 + 2 * NV8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
     // TMEM: S0 | S1 | O | Q (Q rows as bf16 pairs, the A operand of S = Q K^T)
@@ -150,9 +169,11 @@ __device__ __forceinline__ int request_tiles(const DecodeArgs& a, int b) {
 
 // Query row r of (b, h) (bf16 [B, Sq, Hq, D]) into this thread's TMEM lane,
 // columns COL_Q.., zeros for padding rows; the whole warp calls it.
+// to_f16: the row is bfloat16 and goes into TMEM as float16 (the e4m3 path's
+// MMAs run in float16).
 template <int D>
 __device__ __forceinline__ void q_row_to_tmem(const DecodeArgs& a, uint32_t taddr, int r, int R, int g, int b,
-                                              int h) {
+                                              int h, bool to_f16) {
     const uint4* src = nullptr;
     if (r < R)
         src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q) +
@@ -163,16 +184,32 @@ __device__ __forceinline__ void q_row_to_tmem(const DecodeArgs& a, uint32_t tadd
         const uint4 v = src ? __ldg(src + e) : make_uint4(0u, 0u, 0u, 0u);
         w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
     }
+    if (to_f16) {
+#pragma unroll
+        for (int e = 0; e < D / 2; ++e) {
+            const __half2 hh = __floats2half2_rn(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+            w[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+    }
     __syncwarp();                                  // tcgen05.st is warp-collective
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) tmem_st32(taddr + 32 * c, w + 32 * c);
 }
 
-template <int D, bool F16>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// Two e4m3fn codes (low byte first) -> two float16 (low half first), exactly.
+__device__ __forceinline__ uint32_t tc_e4m3x2_to_f16x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// F16: the MMA operand type (float16 for e4m3 caches, widened exactly).  KV8:
+// float8_e4m3fn caches with per-(request, KV head) scales (a bfloat16 Q is
+// then rounded to float16 once, when it goes into TMEM).
+template <int D, bool F16, bool KV8>
+__global__ void __launch_bounds__(num_threads<KV8>(), 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const DecodeArgs a, int R, int g, int box_tokens) {
-    using C = TCfg<D>;
+    using C = TCfg<D, KV8>;
     // both MMA operands of the call's 16-bit type (P is packed to it as well)
     constexpr uint32_t IDESC_QK = make_idesc_16<F16>(BM, BN, false, false);
     constexpr uint32_t IDESC_PV = make_idesc_16<F16>(BM, D, false, true);
@@ -198,14 +235,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const uint32_t o_done = bar0 + 8u * (5 + 2 * C::NK + 2 * C::NV);
     const uint32_t drain = bar0 + 8u * (6 + 2 * C::NK + 2 * C::NV);
     const uint32_t q_next = bar0 + 8u * (7 + 2 * C::NK + 2 * C::NV);
+    const uint32_t bar8 = bar0 + 8u * (8 + 2 * C::NK + 2 * C::NV);
+    auto k8_full = [&](int i) { return bar8 + 8u * i; };
+    auto k8_empty = [&](int i) { return bar8 + 8u * (C::NK8 + i); };
+    auto v8_full = [&](int i) { return bar8 + 8u * (2 * C::NK8 + i); };
+    auto v8_empty = [&](int i) { return bar8 + 8u * (2 * C::NK8 + C::NV8 + i); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     Range* range = reinterpret_cast<Range*>(smem + C::OFF_MISC + 16);
 
     if (threadIdx.x == 0) {
         mbar_init(q_ready, BM);
-        for (int i = 0; i < C::NK; ++i) { mbar_init(k_full(i), 1); mbar_init(k_empty(i), 1); }
-        for (int i = 0; i < C::NV; ++i) { mbar_init(v_full(i), 1); mbar_init(v_empty(i), 1); }
+        // the 16-bit tiles land by TMA (one arrival with its bytes) or from the
+        // wideners (one arrival per widener warp)
+        const int fill = KV8 ? NUM_W + (4 - n_sm_warps) : 1;
+        for (int i = 0; i < C::NK; ++i) { mbar_init(k_full(i), fill); mbar_init(k_empty(i), 1); }
+        for (int i = 0; i < C::NV; ++i) { mbar_init(v_full(i), fill); mbar_init(v_empty(i), 1); }
+        for (int i = 0; i < C::NK8; ++i) { mbar_init(k8_full(i), 1); mbar_init(k8_empty(i), fill); }
+        for (int i = 0; i < C::NV8; ++i) { mbar_init(v8_full(i), 1); mbar_init(v8_empty(i), fill); }
         for (int i = 0; i < 2; ++i) { mbar_init(s_full(i), 1); mbar_init(p_full(i), 32 * n_sm_warps); }
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
@@ -266,6 +313,59 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // ------------------------------------------------------------ wideners (e4m3 caches)
+    // Each byte tile becomes the 16-bit tile the MMAs read, in the order the
+    // producer loads them (K0, K1, V0, K2, V1, ...): rows [8-key group][64-
+    // column slice][8 keys][128 bytes] with the 128-byte swizzle, exactly as the
+    // 5-D page-block boxes land in the 16-bit path.  Warps 6-7 widen, and so do
+    // the warps of 0-3 that hold no query row once their (zero) Q rows are in.
+    const int n_w = NUM_W + (4 - n_sm_warps);
+    auto run_wideners = [&](int wt) {
+        int nk = 0, nv = 0;
+        auto widen = [&](bool is_v) -> bool {
+            const int cnt = is_v ? nv : nk;
+            const int r8 = is_v ? C::NV8 : C::NK8, r16 = is_v ? C::NV : C::NK;
+            const int s8 = cnt % r8, s16 = cnt % r16;
+            if (!__all_sync(0xffffffffu, mbar_wait(is_v ? v8_full(s8) : k8_full(s8), (cnt / r8) & 1, abort_flag)))
+                return false;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(is_v ? v_empty(s16) : k_empty(s16), ((cnt / r16) & 1) ^ 1, abort_flag)))
+                return false;
+            const uint8_t* src = smem + (is_v ? C::OFF_V8 : C::OFF_K8) + s8 * C::TILE8;
+            uint8_t* dst = smem + (is_v ? C::OFF_V : C::OFF_K) + s16 * C::KV_TILE;
+            constexpr int CH8 = D / 16;            // 16-byte e4m3 chunks of a row
+            for (int idx = wt; idx < BN * CH8; idx += 32 * n_w) {
+                const int k = idx / CH8, c8 = idx % CH8;
+                const uint4 x = *reinterpret_cast<const uint4*>(src + (k >> 3) * C::GROUP8 + (c8 >> 3) * 1024 +
+                                                                (k & 7) * 128 + (((c8 & 7) ^ (k & 7)) << 4));
+                const int c16 = 2 * c8;             // its two 8-dim chunks share one 64-column slice
+                uint8_t* row = dst + (k >> 3) * C::GROUP_STRIDE + (c16 >> 3) * 1024 + (k & 7) * 128;
+                *reinterpret_cast<uint4*>(row + (((c16 & 7) ^ (k & 7)) << 4)) =
+                    make_uint4(tc_e4m3x2_to_f16x2(x.x), tc_e4m3x2_to_f16x2(x.x >> 16), tc_e4m3x2_to_f16x2(x.y),
+                               tc_e4m3x2_to_f16x2(x.y >> 16));
+                *reinterpret_cast<uint4*>(row + ((((c16 + 1) & 7) ^ (k & 7)) << 4)) =
+                    make_uint4(tc_e4m3x2_to_f16x2(x.z), tc_e4m3x2_to_f16x2(x.z >> 16), tc_e4m3x2_to_f16x2(x.w),
+                               tc_e4m3x2_to_f16x2(x.w >> 16));
+            }
+            fence_proxy_async_smem();              // the tensor core reads what the warp wrote
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(is_v ? v8_empty(s8) : k8_empty(s8));
+                mbar_arrive(is_v ? v_full(s16) : k_full(s16));
+            }
+            __syncwarp();
+            if (is_v) ++nv; else ++nk;
+            return true;
+        };
+        bool ok = widen(false);
+        for (int it = 0; it < n && ok; ++it) {
+            if (it + 1 < n) {
+                ok = widen(false);
+                if (!ok) break;
+            }
+            ok = widen(true);
+        }
+    };
     if (warp == WARP_LOAD) {
         // ------------------------------------------------------------ producer
         const int nbox = BN / box_tokens;          // page blocks per tile; lane i loads block i
@@ -314,20 +414,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const int cnt_rows = (it & 1) ? n_ring1 : n_ring0;
             const int h = (it & 1) ? h_ring1 : h_ring0;
             const int cnt = is_v ? nv : nk;
-            const int ring = is_v ? C::NV : C::NK;
+            // e4m3 caches: byte tiles into their own rings, for the wideners
+            const int ring = KV8 ? (is_v ? C::NV8 : C::NK8) : (is_v ? C::NV : C::NK);
             const int slot = cnt % ring;
-            const uint32_t empty_bar = is_v ? v_empty(slot) : k_empty(slot);
-            const uint32_t full_bar = is_v ? v_full(slot) : k_full(slot);
+            const uint32_t empty_bar = KV8 ? (is_v ? v8_empty(slot) : k8_empty(slot))
+                                           : (is_v ? v_empty(slot) : k_empty(slot));
+            const uint32_t full_bar = KV8 ? (is_v ? v8_full(slot) : k8_full(slot))
+                                          : (is_v ? v_full(slot) : k_full(slot));
             bool ok = true;
             if (lane == 0) {
                 ok = mbar_wait(empty_bar, ((cnt / ring) & 1) ^ 1, abort_flag);
-                if (ok) mbar_arrive_expect_tx(full_bar, (uint32_t)cnt_rows * blk_bytes);
+                const uint32_t bytes = KV8 ? (uint32_t)box_tokens * 128 * C::NSUB8 : blk_bytes;
+                if (ok) mbar_arrive_expect_tx(full_bar, (uint32_t)cnt_rows * bytes);
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
             __syncwarp();                          // the expect-tx precedes every lane's copy
-            const uint32_t dst = sb + (is_v ? C::OFF_V : C::OFF_K) + slot * C::KV_TILE + lane * blk_bytes;
             const void* map = is_v ? (const void*)&tm_v : (const void*)&tm_k;
-            if (row >= 0) tma_load_5d(dst, map, full_bar, 0, 0, 0, row / 8, h);
+            if constexpr (KV8) {
+                // one {128, 8, D / 128, box_tokens / 8, 1} byte box per page block
+                const uint32_t dst = sb + (is_v ? C::OFF_V8 : C::OFF_K8) + slot * C::TILE8 +
+                                     lane * box_tokens * 128 * C::NSUB8;
+                if (row >= 0) tma_load_5d(dst, map, full_bar, 0, 0, 0, row / 8, h);
+            } else {
+                const uint32_t dst = sb + (is_v ? C::OFF_V : C::OFF_K) + slot * C::KV_TILE + lane * blk_bytes;
+                if (row >= 0) tma_load_5d(dst, map, full_bar, 0, 0, 0, row / 8, h);
+            }
             if (is_v) ++nv; else ++nk;
             return true;
         };
@@ -343,13 +454,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
         if (lane == 0) {
             if (*abort_flag) {
-                for (int s = 0; s < C::NK && s < nk; ++s) {
-                    const int last = nk - 1 - ((nk - 1 - s) % C::NK);
-                    mbar_drain(k_full(s), (last / C::NK) & 1);
+                // let the copies in flight land: the last load of each slot
+                constexpr int RK = KV8 ? C::NK8 : C::NK, RV = KV8 ? C::NV8 : C::NV;
+                for (int s = 0; s < RK && s < nk; ++s) {
+                    const int last = nk - 1 - ((nk - 1 - s) % RK);
+                    mbar_drain(KV8 ? k8_full(s) : k_full(s), (last / RK) & 1);
                 }
-                for (int s = 0; s < C::NV && s < nv; ++s) {
-                    const int last = nv - 1 - ((nv - 1 - s) % C::NV);
-                    mbar_drain(v_full(s), (last / C::NV) & 1);
+                for (int s = 0; s < RV && s < nv; ++s) {
+                    const int last = nv - 1 - ((nv - 1 - s) % RV);
+                    mbar_drain(KV8 ? v8_full(s) : v_full(s), (last / RV) & 1);
                 }
             }
         }
@@ -435,21 +548,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             mbar_drain(drain, 0);
         }
         __syncwarp();
+    } else if (KV8 && warp >= WARP_W0) {
+        run_wideners((4 - n_sm_warps) * 32 + (warp - WARP_W0) * 32 + lane);
     } else {
         // ------------------------------------------------------------ warps 0-3: first Q rows into TMEM
         // Row r = i * g + hl is query i of head h * g + hl; rows past g * Sq are zero.
         Cursor c0;
         c0.set(a, rg.s0);
-        q_row_to_tmem<D>(a, tmem + ((uint32_t)(warp * 32) << 16) + C::COL_Q, warp * 32 + lane, R, g, c0.b, c0.h);
+        q_row_to_tmem<D>(a, tmem + ((uint32_t)(warp * 32) << 16) + C::COL_Q, warp * 32 + lane, R, g, c0.b, c0.h,
+                         KV8 && !a.f16);
         tc_fence_before();
         mbar_arrive(q_ready);
     }
+    if (KV8 && warp < 4 && warp >= n_sm_warps) run_wideners((warp - n_sm_warps) * 32 + lane);
     if (warp < n_sm_warps) {
         // ------------------------------------------------------------ softmax warps
         const int r = warp * 32 + lane;            // padded row == TMEM lane
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
         const bool row_ok = r < R;
-        const float sl = a.scale_log2;
+        // softmax scale and softcap input of the piece (times its k_scale with
+        // e4m3 caches), and the factor of its stored O (its v_scale)
+        float sl = a.scale_log2, cap_in = a.x.cap_in, o_scale = 1.f;
         Cursor c;
         c.set(a, rg.s0);
         c.lt = rg.lt0;
@@ -463,6 +582,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         };
         auto key_lo = [&](long p, int L) { return a.x.wl >= 0 ? (int)max(0L, min((long)L, p - a.x.wl)) : 0; };
         auto piece_setup = [&]() {
+            if constexpr (KV8) {
+                const int kv = c.b * a.Hkv + c.h;
+                const float ks = a.k_scale ? a.k_scale[kv] : 1.f;
+                sl = a.scale_log2 * ks;
+                cap_in = a.x.cap_in * ks;
+                o_scale = a.v_scale ? a.v_scale[kv] : 1.f;
+            }
             const int L = c.L;
             const long p = (long)(r / g) + L - a.Sq;       // key position of this row's query
             lim = row_ok ? key_hi(p, L) : 0;
@@ -507,7 +633,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             } else {
 #pragma unroll
                 for (int cc = 0; cc < BN; ++cc) {
-                    const float lg = capped ? softcap_log2(s[cc], a.x.cap_in, a.x.cap_out) : s[cc] * sl;
+                    const float lg = capped ? softcap_log2(s[cc], cap_in, a.x.cap_out) : s[cc] * sl;
                     const float x = t0 + cc >= lo && t0 + cc < lim ? lg : -INFINITY;   // the select drops stale rows
                     s[cc] = x;
                     mx8[cc & 7] = fmaxf(mx8[cc & 7], x);
@@ -566,7 +692,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (last) {
                 if (it + 1 < n) {
                     // S of this tile is done, so Q is free: the next piece's rows
-                    q_row_to_tmem<D>(a, tmem + lane_addr + C::COL_Q, r, R, g, nx.b, nx.h);
+                    q_row_to_tmem<D>(a, tmem + lane_addr + C::COL_Q, r, R, g, nx.b, nx.h, KV8 && !a.f16);
                     tc_fence_before();
                     mbar_arrive(q_next);
                 }
@@ -576,7 +702,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 tc_fence_after();
                 const int id = c.s + cta;                  // partial id of this piece
                 const size_t part_row = (size_t)id * R + r;
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                const float inv = l_run > 0.f ? o_scale / l_run : 0.f;
 #pragma unroll 1
                 for (int cc = 0; cc < D / 32; cc += 2) {
                     float o[64];
@@ -622,16 +748,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_decode_tc_error, (int)kErrDecodeWait);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool KV8 = false>
 cudaError_t launch_t(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecodeArgs& a,
                      int box_tokens, cudaStream_t stream) {
-    using C = TCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    using C = TCfg<D, KV8>;
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, F16, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int g = a.Hq / a.Hkv;
     const int R = g * a.Sq;
-    decode_tc_kernel<D, F16><<<a.tc_grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_k, tm_v, a, R, g, box_tokens);
+    decode_tc_kernel<D, F16, KV8><<<a.tc_grid, num_threads<KV8>(), C::SMEM_BYTES, stream>>>(tm_k, tm_v, a, R, g,
+                                                                                           box_tokens);
     return cudaGetLastError();
 }
 
@@ -657,6 +784,18 @@ cudaError_t launch_decode_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             : launch_t<128, false>(tm_k, tm_v, a, box_tokens, stream); break;
         case 256: e = a.f16 ? launch_t<256, true>(tm_k, tm_v, a, box_tokens, stream)
                             : launch_t<256, false>(tm_k, tm_v, a, box_tokens, stream); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    return launch_decode_combine(a, stream);
+}
+
+cudaError_t launch_decode_tc_fp8(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecodeArgs& a,
+                                 int box_tokens, cudaStream_t stream) {
+    cudaError_t e;
+    switch (a.D) {
+        case 128: e = launch_t<128, true, true>(tm_k, tm_v, a, box_tokens, stream); break;
+        case 256: e = launch_t<256, true, true>(tm_k, tm_v, a, box_tokens, stream); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;

@@ -141,6 +141,12 @@ int decode_tc_box_tokens(int page_size);
 // {64, 8, D / 64, box_tokens / 8, 1} box (one page block of one head per box).
 cudaError_t launch_decode_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecodeArgs& a,
                              int box_tokens, cudaStream_t stream);
+// The same kernel over float8_e4m3fn caches (DecodeArgs k_scale / v_scale):
+// tm_k / tm_v are 5-D byte maps {128, 8, D / 128, pages * page_size / 8, Hkv}
+// with a {128, 8, D / 128, box_tokens / 8, 1} box (one page block of one head);
+// warps widen each byte tile into the 16-bit rings.
+cudaError_t launch_decode_tc_fp8(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecodeArgs& a,
+                                 int box_tokens, cudaStream_t stream);
 int decode_tc_take_device_error();
 
 }  // namespace gqa
