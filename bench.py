@@ -109,7 +109,7 @@ TRAFFIC = {
     "paged_decode": ("ratio", (559.379712 + 6.031616) / 556.916736),
     "wide_group_decode": ("ratio", (233.671424 + 4.135424) / 232.683520),
     "paged_decode_fp8kv": ("ratio", (279.809536 + 5.651200) / 278.458368),
-    "wide_group_decode_fp8kv": ("ratio", (116.981760 + 5.635072) / 116.341760),
+    "wide_group_decode_fp8kv": ("ratio", (117.055232 + 3.771392) / 116.341760),
     "qwen3_8b_prefill": ("bytes", (95.003136 + 31.002112) * 1e6),
     "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
     # captured at B=1 of 4 independent batches: traffic scales by 4
@@ -436,7 +436,7 @@ def bench_ours(args, world, rank, local):
         mf = min(4, (rows + 15) // 16)
         split = "decode_tc_kernel<%d>" % c["D"] if tc else "decode_tma_kernel<%d,%d>" % (c["D"], mf)
         if dom.kind == "paged_fp8":
-            split = "decode_fp8_kernel<%d,%d>" % (c["D"], mf)
+            split = ("decode_tc_kernel<%d,e4m3>" % c["D"]) if tc else "decode_fp8_kernel<%d,%d>" % (c["D"], mf)
         roof = dict(kernel=split + " + decode_combine_kernel<%d> (%s)" % (c["D"], dom.name), bound="hbm",
                     achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s", frac=ach / peaks["hbm_gbs"],
                     traffic=traffic_per_launch(dom),

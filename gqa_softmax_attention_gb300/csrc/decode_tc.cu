@@ -335,7 +335,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             uint8_t* dst = smem + (is_v ? C::OFF_V : C::OFF_K) + s16 * C::KV_TILE;
             constexpr int CH8 = D / 16;            // 16-byte e4m3 chunks of a row
             for (int idx = wt; idx < BN * CH8; idx += 32 * n_w) {
-                const int k = idx / CH8, c8 = idx % CH8;
+                const int k = idx % BN, c8 = idx / BN;   // 8-lane phases: eight keys, one chunk (no bank conflict)
                 const uint4 x = *reinterpret_cast<const uint4*>(src + (k >> 3) * C::GROUP8 + (c8 >> 3) * 1024 +
                                                                 (k & 7) * 128 + (((c8 & 7) ^ (k & 7)) << 4));
                 const int c16 = 2 * c8;             // its two 8-dim chunks share one 64-column slice
