@@ -111,6 +111,26 @@ def test_options_and_non_causal(g, D):
     compare(o, lse, ro, rl, "non-causal")
 
 
+@pytest.mark.parametrize("D", [128, 256])
+def test_wide_groups_options_and_fp16(g, D):
+    """32-128 rows per KV head take the tensor-core decode with widened tiles:
+    window + softcap + sinks, non-causal, and a float16 query there."""
+    p = W.paged_fp8_inputs(3, 4, 24, 2, D, 16, lengths=[700, 5, 2100], seed=11, scale_range=(0.1, 1.5))
+    sinks = torch.linspace(-2.0, 2.0, 24)
+    sinks[3] = float("-inf")
+    kw = dict(window_left=300, window_right=0, softcap=6.0, sinks=sinks)
+    o, lse = run(g, p, **kw)
+    ro, rl = reference(p, **kw)
+    compare(o, lse, ro, rl, "tc: window + softcap + sinks")
+    o, lse = run(g, p, causal=False, scale=0.04)
+    ro, rl = reference(p, causal=False, scale=0.04)
+    compare(o, lse, ro, rl, "tc: non-causal")
+    q16 = p["q"].to(torch.float16)
+    o, lse = run(g, p, q=q16)
+    ro, rl = reference(p, q=q16)
+    compare(o, lse, ro, rl, "tc: float16 query")
+
+
 def test_matches_16bit_path_on_widened_cache(g):
     """The FP8 call equals the 16-bit decode on the caches widened to float16
     (every e4m3fn value is a float16), unit scales, float16 query."""
