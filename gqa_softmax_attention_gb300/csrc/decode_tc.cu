@@ -248,11 +248,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         mbar_init(q_ready, BM);
         // the 16-bit tiles land by TMA (one arrival with its bytes) or from the
         // wideners (one arrival per widener warp)
-        const int fill = KV8 ? NUM_W + (4 - n_sm_warps) : 1;
-        for (int i = 0; i < C::NK; ++i) { mbar_init(k_full(i), fill); mbar_init(k_empty(i), 1); }
-        for (int i = 0; i < C::NV; ++i) { mbar_init(v_full(i), fill); mbar_init(v_empty(i), 1); }
-        for (int i = 0; i < C::NK8; ++i) { mbar_init(k8_full(i), 1); mbar_init(k8_empty(i), fill); }
-        for (int i = 0; i < C::NV8; ++i) { mbar_init(v8_full(i), 1); mbar_init(v8_empty(i), fill); }
+        const int nwt = NUM_W + (4 - n_sm_warps);
+        const int fill_k = KV8 ? (nwt + 1) / 2 : 1, fill_v = KV8 ? nwt / 2 : 1;
+        for (int i = 0; i < C::NK; ++i) { mbar_init(k_full(i), fill_k); mbar_init(k_empty(i), 1); }
+        for (int i = 0; i < C::NV; ++i) { mbar_init(v_full(i), fill_v); mbar_init(v_empty(i), 1); }
+        for (int i = 0; i < C::NK8; ++i) { mbar_init(k8_full(i), 1); mbar_init(k8_empty(i), fill_k); }
+        for (int i = 0; i < C::NV8; ++i) { mbar_init(v8_full(i), 1); mbar_init(v8_empty(i), fill_v); }
         for (int i = 0; i < 2; ++i) { mbar_init(s_full(i), 1); mbar_init(p_full(i), 32 * n_sm_warps); }
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
@@ -318,9 +319,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     // producer loads them (K0, K1, V0, K2, V1, ...): rows [8-key group][64-
     // column slice][8 keys][128 bytes] with the 128-byte swizzle, exactly as the
     // 5-D page-block boxes land in the 16-bit path.  Warps 6-7 widen, and so do
-    // the warps of 0-3 that hold no query row once their (zero) Q rows are in.
+    // the warps of 0-3 that hold no query row once their (zero) Q rows are in;
+    // they form a K team and a V team, so a value tile waiting for its slot
+    // never holds up the next key tile.
     const int n_w = NUM_W + (4 - n_sm_warps);
-    auto run_wideners = [&](int wt) {
+    auto run_wideners = [&](int wpos) {             // position among the widener warps
+        const bool team_v = wpos & 1;                // even positions widen K, odd ones V
+        const int team_n = team_v ? n_w / 2 : (n_w + 1) / 2;
+        const int wt = (wpos >> 1) * 32 + lane;
         int nk = 0, nv = 0;
         auto widen = [&](bool is_v) -> bool {
             const int cnt = is_v ? nv : nk;
@@ -334,7 +340,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const uint8_t* src = smem + (is_v ? C::OFF_V8 : C::OFF_K8) + s8 * C::TILE8;
             uint8_t* dst = smem + (is_v ? C::OFF_V : C::OFF_K) + s16 * C::KV_TILE;
             constexpr int CH8 = D / 16;            // 16-byte e4m3 chunks of a row
-            for (int idx = wt; idx < BN * CH8; idx += 32 * n_w) {
+            for (int idx = wt; idx < BN * CH8; idx += 32 * team_n) {
                 const int k = idx % BN, c8 = idx / BN;   // 8-lane phases: eight keys, one chunk (no bank conflict)
                 const uint4 x = *reinterpret_cast<const uint4*>(src + (k >> 3) * C::GROUP8 + (c8 >> 3) * 1024 +
                                                                 (k & 7) * 128 + (((c8 & 7) ^ (k & 7)) << 4));
@@ -357,14 +363,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (is_v) ++nv; else ++nk;
             return true;
         };
-        bool ok = widen(false);
-        for (int it = 0; it < n && ok; ++it) {
-            if (it + 1 < n) {
-                ok = widen(false);
-                if (!ok) break;
-            }
-            ok = widen(true);
-        }
+        for (int it = 0; it < n; ++it)
+            if (!widen(team_v)) break;
     };
     if (warp == WARP_LOAD) {
         // ------------------------------------------------------------ producer
@@ -549,7 +549,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
         __syncwarp();
     } else if (KV8 && warp >= WARP_W0) {
-        run_wideners((4 - n_sm_warps) * 32 + (warp - WARP_W0) * 32 + lane);
+        run_wideners((4 - n_sm_warps) + (warp - WARP_W0));
     } else {
         // ------------------------------------------------------------ warps 0-3: first Q rows into TMEM
         // Row r = i * g + hl is query i of head h * g + hl; rows past g * Sq are zero.
@@ -560,7 +560,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         tc_fence_before();
         mbar_arrive(q_ready);
     }
-    if (KV8 && warp < 4 && warp >= n_sm_warps) run_wideners((warp - n_sm_warps) * 32 + lane);
+    if (KV8 && warp < 4 && warp >= n_sm_warps) run_wideners(warp - n_sm_warps);
     if (warp < n_sm_warps) {
         // ------------------------------------------------------------ softmax warps
         const int r = warp * 32 + lane;            // padded row == TMEM lane
