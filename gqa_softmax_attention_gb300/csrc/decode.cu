@@ -786,15 +786,20 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     sc[n][e] = x;
                     mx[h] = fmaxf(mx[h], x);
                 }
+            // Lazy rescale: the reference max moves only when the tile max exceeds
+            // it by more than 2^8 (P stays below 2^8, far inside float16); O and
+            // the sum share the reference, so the result is unchanged.
             float alpha[2], m_use[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
                 mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                const float m_new = fmaxf(m_run[h], mx[h]);
-                m_use[h] = m_new == -INFINITY ? 0.f : m_new;           // no -inf - -inf
-                alpha[h] = fast_exp2(m_run[h] - m_use[h]);
-                m_run[h] = m_new;
+                alpha[h] = 1.f;
+                if (mx[h] > m_run[h] + 8.f) {
+                    alpha[h] = fast_exp2(m_run[h] - mx[h]);         // 0 while m_run is -inf
+                    m_run[h] = mx[h];
+                }
+                m_use[h] = m_run[h] == -INFINITY ? 0.f : m_run[h];  // no -inf - -inf
             }
             // ---- P (float16) as P V's A fragments, this lane's share of the row sums
             uint32_t pa[C::KPW / 16][4];
@@ -813,10 +818,12 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
 #pragma unroll
             for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + rs[h];
+            if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-            for (int n = 0; n < C::NFD; ++n) {
-                acc[n][0] *= alpha[0]; acc[n][1] *= alpha[0];
-                acc[n][2] *= alpha[1]; acc[n][3] *= alpha[1];
+                for (int n = 0; n < C::NFD; ++n) {
+                    acc[n][0] *= alpha[0]; acc[n][1] *= alpha[0];
+                    acc[n][2] *= alpha[1]; acc[n][3] *= alpha[1];
+                }
             }
             // ---- O += P V over all dims; acc[4q + 2i + e]: chunk i of the 32-dim
             // group q, dims of parity e
