@@ -36,6 +36,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -731,6 +732,21 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 qf[kk][2 + h] = QBF ? bf16x2_to_f16x2(v.y) : v.y;      // k = 2(t%4) + 8, +9
             }
         }
+        // keys every row of the fragment sees (rows past the block see all: their
+        // Q is zero and their results are never stored)
+        int lim_min = INT_MAX, lo_max = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (mf * 16 + (lane >> 2) + 8 * h < w.rows_here) {
+                lim_min = min(lim_min, lim[h]);
+                lo_max = max(lo_max, lo[h]);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lim_min = min(lim_min, __shfl_xor_sync(0xffffffffu, lim_min, o));
+            lo_max = max(lo_max, __shfl_xor_sync(0xffffffffu, lo_max, o));
+        }
         float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
         float acc[C::NFD][4];
 #pragma unroll
@@ -775,17 +791,28 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             }
             // ---- scaled, masked logits (log2 units) and the rows' maxima
             float mx[2] = {-INFINITY, -INFINITY};
+            const bool unmasked = t0 + kw0 + C::KPW <= lim_min && t0 + kw0 >= lo_max && cap_out == 0.f;
+            if (unmasked) {                             // every key of this warp's share is visible
 #pragma unroll
-            for (int n = 0; n < C::NFK; ++n)
+                for (int n = 0; n < C::NFK; ++n)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int h = e >> 1;
-                    const int t = t0 + kw0 + 8 * n + 2 * t4 + (e & 1);
-                    float x = cap_out != 0.f ? softcap_log2(sc[n][e], cap_in, cap_out) : sc[n][e] * sl;
-                    x = t >= lo[h] && t < lim[h] ? x : -INFINITY;       // the select drops stale keys
-                    sc[n][e] = x;
-                    mx[h] = fmaxf(mx[h], x);
-                }
+                    for (int e = 0; e < 4; ++e) {
+                        sc[n][e] *= sl;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], sc[n][e]);
+                    }
+            } else {
+#pragma unroll
+                for (int n = 0; n < C::NFK; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = e >> 1;
+                        const int t = t0 + kw0 + 8 * n + 2 * t4 + (e & 1);
+                        float x = cap_out != 0.f ? softcap_log2(sc[n][e], cap_in, cap_out) : sc[n][e] * sl;
+                        x = t >= lo[h] && t < lim[h] ? x : -INFINITY;       // the select drops stale keys
+                        sc[n][e] = x;
+                        mx[h] = fmaxf(mx[h], x);
+                    }
+            }
             // Lazy rescale: the reference max moves only when the tile max exceeds
             // it by more than 2^8 (P stays below 2^8, far inside float16); O and
             // the sum share the reference, so the result is unchanged.
