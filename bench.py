@@ -108,7 +108,7 @@ def load_peaks():
 TRAFFIC = {
     "paged_decode": ("ratio", (559.379712 + 6.031616) / 556.916736),
     "wide_group_decode": ("ratio", (233.671424 + 4.135424) / 232.683520),
-    "paged_decode_fp8kv": ("ratio", (279.809536 + 5.651200) / 278.458368),
+    "paged_decode_fp8kv": ("ratio", (279.805952 + 5.622016) / 278.458368),
     "wide_group_decode_fp8kv": ("ratio", (117.075456 + 3.785472) / 116.341760),
     "qwen3_8b_prefill": ("bytes", (95.003136 + 31.002112) * 1e6),
     "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
