@@ -249,7 +249,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         // the 16-bit tiles land by TMA (one arrival with its bytes) or from the
         // wideners (one arrival per widener warp)
         const int nwt = NUM_W + (4 - n_sm_warps);
-        const int fill_k = KV8 ? (nwt + 1) / 2 : 1, fill_v = KV8 ? nwt / 2 : 1;
+        int nwv = 0;                                  // widener positions in the V team (see team_of)
+        for (int q = 0; q < nwt; ++q) nwv += (q + (q >> 1)) & 1;
+        const int fill_k = KV8 ? nwt - nwv : 1, fill_v = KV8 ? nwv : 1;
         for (int i = 0; i < C::NK; ++i) { mbar_init(k_full(i), fill_k); mbar_init(k_empty(i), 1); }
         for (int i = 0; i < C::NV; ++i) { mbar_init(v_full(i), fill_v); mbar_init(v_empty(i), 1); }
         for (int i = 0; i < C::NK8; ++i) { mbar_init(k8_full(i), 1); mbar_init(k8_empty(i), fill_k); }
@@ -323,10 +325,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     // they form a K team and a V team, so a value tile waiting for its slot
     // never holds up the next key tile.
     const int n_w = NUM_W + (4 - n_sm_warps);
+    // Team of widener position p: positions 0, 3, 4, 7, ... widen K and 1, 2, 5,
+    // 6, ... V, so that with the row-less warps 2-3 and warps 6-7 each team
+    // spans two SM sub-partitions (warp w issues on sub-partition w % 4): the
+    // conversion pipe of one sub-partition does not carry a whole team.
+    auto team_of = [](int p) { return ((p + (p >> 1)) & 1) != 0; };
     auto run_wideners = [&](int wpos) {             // position among the widener warps
-        const bool team_v = wpos & 1;                // even positions widen K, odd ones V
-        const int team_n = team_v ? n_w / 2 : (n_w + 1) / 2;
-        const int wt = (wpos >> 1) * 32 + lane;
+        const bool team_v = team_of(wpos);
+        int team_n = 0, rank = 0;
+        for (int q = 0; q < n_w; ++q) {
+            if (team_of(q) != team_v) continue;
+            if (q < wpos) ++rank;
+            ++team_n;
+        }
+        const int wt = rank * 32 + lane;
         int nk = 0, nv = 0;
         auto widen = [&](bool is_v) -> bool {
             const int cnt = is_v ? nv : nk;
