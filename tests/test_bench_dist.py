@@ -64,3 +64,27 @@ def test_visible_pairs_brute_force():
             bf = sum(1 for b in range(2) for i in range(Sq) for j in range(Skv)
                      if (not causal or j <= i + Skv - Sq) and m[b, j])
             assert bf == bench.visible_pairs(2, Sq, Skv, causal, m[:, :Skv])
+
+
+def test_decode_bytes_count_the_element_size():
+    from gqa_softmax_attention_gb300 import workloads as W
+    for kind, gen, elem in (("paged", W.paged_inputs, 2), ("paged_fp8", W.paged_fp8_inputs, 1)):
+        cfg = dict(kind=kind, B=3, Sq=1, Hq=8, Hkv=2, D=128, page_size=16, lengths=[5, 0, 70])
+        d = gen(**cfg)
+        d["config"] = cfg
+        assert bench.decode_bytes(d) == (5 + 0 + 70) * 2 * 2 * 128 * elem
+
+
+def test_fp8_inputs_are_e4m3_with_scales_in_range():
+    from gqa_softmax_attention_gb300 import workloads as W
+    d = W.paged_fp8_inputs(4, 2, 8, 2, 128, 16, lengths=(1, 300), seed=3, scale_range=(0.25, 1.0))
+    assert d["k_cache"].dtype == torch.float8_e4m3fn and d["v_cache"].dtype == torch.float8_e4m3fn
+    for n in ("k_scale", "v_scale"):
+        s = d[n]
+        assert s.shape == (4, 2) and s.dtype == torch.float32
+        assert bool(((s >= 0.25) & (s < 1.0)).all())
+    codes = d["k_cache"].view(torch.uint8)
+    assert not bool(((codes & 0x7F) == 0x7F).any())          # no NaN code anywhere
+    # the same seed draws the same bytes and scales
+    e = W.paged_fp8_inputs(4, 2, 8, 2, 128, 16, lengths=(1, 300), seed=3, scale_range=(0.25, 1.0))
+    assert torch.equal(codes, e["k_cache"].view(torch.uint8)) and torch.equal(d["v_scale"], e["v_scale"])
