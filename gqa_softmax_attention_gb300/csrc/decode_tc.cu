@@ -352,18 +352,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const uint8_t* src = smem + (is_v ? C::OFF_V8 : C::OFF_K8) + s8 * C::TILE8;
             uint8_t* dst = smem + (is_v ? C::OFF_V : C::OFF_K) + s16 * C::KV_TILE;
             constexpr int CH8 = D / 16;            // 16-byte e4m3 chunks of a row
-            for (int idx = wt; idx < BN * CH8; idx += 32 * team_n) {
-                const int k = idx % BN, c8 = idx / BN;   // 8-lane phases: eight keys, one chunk (no bank conflict)
-                const uint4 x = *reinterpret_cast<const uint4*>(src + (k >> 3) * C::GROUP8 + (c8 >> 3) * 1024 +
-                                                                (k & 7) * 128 + (((c8 & 7) ^ (k & 7)) << 4));
-                const int c16 = 2 * c8;             // its two 8-dim chunks share one 64-column slice
-                uint8_t* row = dst + (k >> 3) * C::GROUP_STRIDE + (c16 >> 3) * 1024 + (k & 7) * 128;
-                *reinterpret_cast<uint4*>(row + (((c16 & 7) ^ (k & 7)) << 4)) =
-                    make_uint4(tc_e4m3x2_to_f16x2(x.x), tc_e4m3x2_to_f16x2(x.x >> 16), tc_e4m3x2_to_f16x2(x.y),
-                               tc_e4m3x2_to_f16x2(x.y >> 16));
-                *reinterpret_cast<uint4*>(row + ((((c16 + 1) & 7) ^ (k & 7)) << 4)) =
-                    make_uint4(tc_e4m3x2_to_f16x2(x.z), tc_e4m3x2_to_f16x2(x.z >> 16), tc_e4m3x2_to_f16x2(x.w),
-                               tc_e4m3x2_to_f16x2(x.w >> 16));
+            constexpr int U = 2;                   // chunks loaded before any is stored
+            const int step = 32 * team_n;
+            for (int base = wt; base < BN * CH8; base += U * step) {
+                // The loads of a batch are issued together: the stores cannot
+                // be proven apart from the next loads, so a one-chunk loop
+                // would wait out the shared-memory latency once per chunk.
+                uint4 x[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int idx = base + u * step;
+                    const int k = idx % BN, c8 = idx / BN;   // 8-lane phases: eight keys, one chunk (no bank conflict)
+                    if (idx < BN * CH8)
+                        x[u] = *reinterpret_cast<const uint4*>(src + (k >> 3) * C::GROUP8 + (c8 >> 3) * 1024 +
+                                                               (k & 7) * 128 + (((c8 & 7) ^ (k & 7)) << 4));
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int idx = base + u * step;
+                    if (idx >= BN * CH8) break;
+                    const int k = idx % BN, c16 = 2 * (idx / BN);   // two 8-dim chunks share one 64-column slice
+                    uint8_t* row = dst + (k >> 3) * C::GROUP_STRIDE + (c16 >> 3) * 1024 + (k & 7) * 128;
+                    *reinterpret_cast<uint4*>(row + (((c16 & 7) ^ (k & 7)) << 4)) =
+                        make_uint4(tc_e4m3x2_to_f16x2(x[u].x), tc_e4m3x2_to_f16x2(x[u].x >> 16),
+                                   tc_e4m3x2_to_f16x2(x[u].y), tc_e4m3x2_to_f16x2(x[u].y >> 16));
+                    *reinterpret_cast<uint4*>(row + ((((c16 + 1) & 7) ^ (k & 7)) << 4)) =
+                        make_uint4(tc_e4m3x2_to_f16x2(x[u].z), tc_e4m3x2_to_f16x2(x[u].z >> 16),
+                                   tc_e4m3x2_to_f16x2(x[u].w), tc_e4m3x2_to_f16x2(x[u].w >> 16));
+                }
             }
             fence_proxy_async_smem();              // the tensor core reads what the warp wrote
             __syncwarp();
