@@ -109,7 +109,7 @@ TRAFFIC = {
     "paged_decode": ("ratio", (559.379712 + 6.031616) / 556.916736),
     "wide_group_decode": ("ratio", (233.671424 + 4.135424) / 232.683520),
     "paged_decode_fp8kv": ("ratio", (279.805952 + 5.622016) / 278.458368),
-    "wide_group_decode_fp8kv": ("ratio", (117.075456 + 3.785472) / 116.341760),
+    "wide_group_decode_fp8kv": ("ratio", (117.060352 + 3.536896) / 116.341760),
     "qwen3_8b_prefill": ("bytes", (95.003136 + 31.002112) * 1e6),
     "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
     # captured at B=1 of 4 independent batches: traffic scales by 4
