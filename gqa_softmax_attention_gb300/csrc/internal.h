@@ -128,7 +128,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CU
 int decode_take_device_error();
 // Split decode over float8_e4m3fn caches (decode_fp8_kernel): tm_k / tm_v are
 // 3-D byte maps {D, Hkv, pages * page_size} with a {128, 1, box_tokens} box;
-// D is 128 or 256 and g * Sq at most 64.  Launches the combine as well.
+// D is 128 or 256; the g * Sq rows of a KV group go in blocks of up to 64.
+// Launches the combine as well.
 cudaError_t launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                               int box_tokens, cudaStream_t stream);
 // Merge of the split partials (decode_combine_kernel).

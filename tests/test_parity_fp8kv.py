@@ -65,6 +65,8 @@ SMALL = [
     (3, 3, 6, 2, 128, 16, [2, 3, 4]),                # 9 rows, L around Sq
     (2, 2, 32, 4, 128, 128, [50, 401]),              # pages longer than the key tile
     (3, 1, 32, 8, 128, 64, [64, 65, 1]),             # one-key and exact-tile tails
+    (2, 3, 64, 1, 128, 64, [700, 1500]),             # 192 rows: the split kernel, three row blocks
+    (2, 2, 48, 1, 256, 96, [500, 1000]),             # 96 rows, pages of no 64-key tiling: split, two row blocks
 ]
 
 
