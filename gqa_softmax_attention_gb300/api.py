@@ -185,7 +185,8 @@ def attn_decode_paged_fp8kv(q, k_cache, v_cache, k_scale, v_scale, real_seqlen_k
     q [B,Sq,Hq,D] bfloat16 or float16; k_cache/v_cache [num_pages,page_size,Hkv,D]
     torch.float8_e4m3fn (or uint8 holding e4m3fn codes); k_scale/v_scale [B,Hkv]
     float32 CUDA tensors or None (ones): key t of KV head r in request b is
-    K * k_scale[b, r] and its value V * v_scale[b, r].  D is 128 or 256.  Other
+    K * k_scale[b, r] and its value V * v_scale[b, r].  Every scale must be finite
+    and positive; they stay on the GPU and are not checked.  D is 128 or 256.  Other
     arguments as attn_decode_paged.  Returns (o like q, lse [B,Sq,Hq] float32).
     """
     _check_16_cuda("q", q, 4)

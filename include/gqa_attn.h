@@ -182,7 +182,13 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
  *   k_cache, v_cache  [num_pages, page_size, Hkv, D] e4m3fn bytes (sign, 4
  *                     exponent bits with bias 7, 3 mantissa bits; 0x7F and 0xFF
  *                     are NaN and must not occur), 16-byte aligned
- *   k_scale, v_scale  [B, Hkv] float device arrays, or NULL for all ones
+ *   k_scale, v_scale  [B, Hkv] float device arrays, or NULL for all ones;
+ *                     every scale finite and positive, a caller obligation as
+ *                     in TileOPs "Attention Operators",
+ *                     GQAPrefillPagedWithKVCacheFwdOp (validate_inputs): the
+ *                     library reads them on the GPU only and does not check
+ *                     them; another value corrupts the rows of that request
+ *                     and KV head
  *   q, o              16-bit: bfloat16, or float16 with opts->dtype = GQA_FP16
  *   other arguments   as attn_decode_paged_ex; the same workspace size
  *                     (attn_decode_paged_workspace_size) is enough.
