@@ -65,8 +65,6 @@ def load() -> ctypes.CDLL:
     lib.gqa_status_string.restype = ctypes.c_char_p
     lib.gqa_device_error.argtypes = []
     lib.gqa_device_error.restype = i
-    lib.gqa_exp2_poly.argtypes = [vp, vp, ctypes.c_long, vp]
-    lib.gqa_exp2_poly.restype = i
     lib.gqa_version.argtypes = []
     lib.gqa_version.restype = ctypes.c_char_p
     _handle = lib

@@ -119,6 +119,31 @@ def attn_fwd_dense(q, k, v, key_padding_mask=None, causal=True, scale=None, out=
     return out, lse
 
 
+def _check_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, dtypes=(torch.bfloat16, torch.float16)):
+    """Checks shared by the paged decode entry points: q [B,Sq,Hq,D] and the
+    caches [num_pages,page_size,Hkv,D] CUDA tensors of one 16-bit type, Hq a
+    multiple of Hkv, real_seqlen_kv [B] and block_table [B,max_pages] int32 CUDA
+    tensors.  Returns the five tensors made contiguous."""
+    _check_16_cuda("q", q, 4, dtypes)
+    _check_16_cuda("k_cache", k_cache, 4, (q.dtype,))
+    _check_16_cuda("v_cache", v_cache, 4, (q.dtype,))
+    B, Sq, Hq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shape mismatch: k %s, v %s, D %d" % (tuple(k_cache.shape), tuple(v_cache.shape), D))
+    if Hq % Hkv != 0:
+        raise ValueError("Hq (%d) must be divisible by Hkv (%d)" % (Hq, Hkv))
+    for n, t in (("real_seqlen_kv", real_seqlen_kv), ("block_table", block_table)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32:
+            raise ValueError("%s must be an int32 CUDA tensor" % n)
+        if t.device != q.device:
+            raise ValueError("%s must be on q's device %s, got %s" % (n, q.device, t.device))
+    if tuple(real_seqlen_kv.shape) != (B,) or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("real_seqlen_kv must be [B] and block_table [B, max_pages]")
+    return (q.contiguous(), k_cache.contiguous(), v_cache.contiguous(), real_seqlen_kv.contiguous(),
+            block_table.contiguous())
+
+
 def attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, page_size, max_pages):
     """Workspace bytes attn_decode_paged needs on the current device."""
     return int(_lib.load().attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, page_size, max_pages))
@@ -135,23 +160,10 @@ def attn_decode_paged(q, k_cache, v_cache, real_seqlen_kv, block_table, causal=T
     window_left / window_right / softcap / sinks as in attn_fwd_dense.
     Returns (o [B,Sq,Hq,D] bf16, lse [B,Sq,Hq] float32).
     """
-    _check_16_cuda("q", q, 4)
-    _check_16_cuda("k_cache", k_cache, 4, (q.dtype,))
-    _check_16_cuda("v_cache", v_cache, 4, (q.dtype,))
+    q, k_cache, v_cache, sl, bt = _check_paged(q, k_cache, v_cache, real_seqlen_kv, block_table)
     B, Sq, Hq, D = q.shape
-    num_pages, page_size, Hkv, Dk = k_cache.shape
-    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
-        raise ValueError("cache shape mismatch: k %s, v %s, D %d" % (tuple(k_cache.shape), tuple(v_cache.shape), D))
-    if Hq % Hkv != 0:
-        raise ValueError("Hq (%d) must be divisible by Hkv (%d)" % (Hq, Hkv))
-    for n, t in (("real_seqlen_kv", real_seqlen_kv), ("block_table", block_table)):
-        if not t.is_cuda or t.dtype != torch.int32:
-            raise ValueError("%s must be an int32 CUDA tensor" % n)
-    if tuple(real_seqlen_kv.shape) != (B,) or block_table.dim() != 2 or block_table.shape[0] != B:
-        raise ValueError("real_seqlen_kv must be [B] and block_table [B, max_pages]")
-    max_pages = block_table.shape[1]
-    q, k_cache, v_cache = q.contiguous(), k_cache.contiguous(), v_cache.contiguous()
-    sl, bt = real_seqlen_kv.contiguous(), block_table.contiguous()
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    max_pages = bt.shape[1]
     need = attn_decode_paged_workspace_size(B, Sq, Hq, Hkv, D, page_size, max_pages)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -242,10 +254,8 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, real_seqlen_kv, block_table, 
     calls (calls overlapping on the GPU race).  Sizes whose partials do not fit
     raise ValueError.  Outputs are allocated here only when not passed in.
     """
-    bf16 = (torch.bfloat16,)
-    _check_16_cuda("q", q, 4, bf16)
-    _check_16_cuda("k_cache", k_cache, 4, bf16)
-    _check_16_cuda("v_cache", v_cache, 4, bf16)
+    q, k_cache, v_cache, real_seqlen_kv, block_table = _check_paged(q, k_cache, v_cache, real_seqlen_kv,
+                                                                    block_table, (torch.bfloat16,))
     B, Sq, Hq, D = q.shape
     num_pages, page_size, Hkv, _ = k_cache.shape
     max_pages = block_table.shape[1]

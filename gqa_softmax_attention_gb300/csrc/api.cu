@@ -567,13 +567,6 @@ gqa_status gqa_device_error(void) {
     return (e || e2 || v1 || v2 || d || t) ? GQA_ERR_TIMEOUT : GQA_OK;
 }
 
-gqa_status gqa_exp2_poly(const float* x, float* y, long n, gqa_stream_t stream) {
-    if (n < 0 || (n > 0 && (!x || !y))) return GQA_ERR_INVALID_ARG;
-    if (!aligned4(x) || !aligned4(y)) return GQA_ERR_MISALIGNED;
-    return gqa::launch_exp2_poly(x, y, n, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? GQA_OK
-                                                                                                  : GQA_ERR_CUDA;
-}
-
 const char* gqa_version(void) { return "gqa_attn 0.1 sm_103a"; }
 
 }  // extern "C"

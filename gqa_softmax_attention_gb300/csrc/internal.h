@@ -72,7 +72,6 @@ cudaError_t launch_varlen_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_k
 int varlen_packed_take_device_error();
 int varlen_paged_take_device_error();
 // y[i] = 2^x[i] by the prefill kernel's FMA-pipe exp2 (diagnostic).
-cudaError_t launch_exp2_poly(const float* x, float* y, long n, cudaStream_t stream);
 
 struct DecodeArgs {
     const void* q;          // [B, Sq, Hq, D]

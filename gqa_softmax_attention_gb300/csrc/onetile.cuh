@@ -636,7 +636,7 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
                 const float fa = fast ? sl : 1.f;
                 uint32_t pk[BN / 2];
-                const float rs = exp_row<0, F16>(s, fa, m_use, pk);
+                const float rs = exp_row<F16>(s, fa, m_use, pk);
                 tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
                 l_run = l_run * alpha + rs;
 

@@ -61,9 +61,6 @@ constexpr int kRegsLaunch = 168;
 constexpr int kRegsSoftmax = 192;
 constexpr int kRegsOther = 120;
 static_assert(kRegsSoftmax * 256 + kRegsOther * 128 <= kRegsLaunch * NUM_THREADS, "register split");
-// One exponential pair in kPolyEvery goes to the FMA-pipe exp2 on unmasked
-// tiles (0: all on the MUFU).
-constexpr int kPolyEvery = 0;
 
 template <int D>
 struct Cfg {
@@ -640,9 +637,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // exp2 argument: s * fa - m_use (fa = scale on the fast path, 1 otherwise)
                 const float fa = fast ? sl : 1.f;
                 uint32_t pk[BN / 2];
-                float rs;
-                if (fast) rs = exp_row<kPolyEvery, F16>(s, fa, m_use, pk);
-                else rs = exp_row<0, F16>(s, fa, m_use, pk);
+                const float rs = exp_row<F16>(s, fa, m_use, pk);
                 tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
                 l_run = l_run * alpha + rs;
 
@@ -748,15 +743,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
 }
 
-__global__ void exp2_poly_kernel(const float* x, float* y, long n) {
-    const long i = 2 * ((long)blockIdx.x * blockDim.x + threadIdx.x);
-    if (i >= n) return;
-    float y0, y1;
-    exp2_poly_x2(x[i], i + 1 < n ? x[i + 1] : 0.f, y0, y1);
-    y[i] = y0;
-    if (i + 1 < n) y[i + 1] = y1;
-}
-
 __global__ void empty_rows_kernel(__nv_bfloat16* o, float* lse, long rows, int D) {
     const long n = rows * D;
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -807,13 +793,6 @@ cudaError_t launch_empty_rows(void* o, float* lse, long rows, int D, cudaStream_
     const long blocks = (n + threads - 1) / threads < 4096 ? (n + threads - 1) / threads : 4096;
     empty_rows_kernel<<<(unsigned)blocks, threads, 0, stream>>>(reinterpret_cast<__nv_bfloat16*>(o), lse,
                                                                  rows, D);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_exp2_poly(const float* x, float* y, long n, cudaStream_t stream) {
-    if (n <= 0) return cudaSuccess;
-    const long pairs = (n + 1) / 2;
-    exp2_poly_kernel<<<(unsigned)((pairs + 255) / 256), 256, 0, stream>>>(x, y, n);
     return cudaGetLastError();
 }
 

@@ -119,9 +119,8 @@ __device__ __forceinline__ uint32_t below_bits(int n, int chunk) {
 }
 
 // p[c] = 2^(s[c] * fa - m_use) for NCOL (default 128) columns of a row: P packed to bf16x2 in
-// pk, the row sum returned.  Two columns per paired FMA / add; with POLY > 0,
-// one column pair in POLY is evaluated on the FMA pipe instead of the MUFU.
-template <int POLY, bool F16, int NCOL = BN>
+// pk, the row sum returned.  Two columns per paired FMA / add.
+template <bool F16, int NCOL = BN>
 __device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, uint32_t* pk) {
     const uint64_t fa2 = f32x2(fa, fa);
     const uint64_t nm2 = f32x2(-m_use, -m_use);
@@ -132,12 +131,8 @@ __device__ __forceinline__ float exp_row(const float* s, float fa, float m_use, 
     for (int c = 0; c < NCOL / 2; ++c) {
         float x0, x1, p0, p1;
         f32x2_split(ffma2(f32x2(s[2 * c], s[2 * c + 1]), fa2, nm2), x0, x1);
-        if (POLY > 0 && c % (POLY > 0 ? POLY : 1) == (POLY > 0 ? POLY : 1) - 1) {
-            exp2_poly_x2(x0, x1, p0, p1);
-        } else {
-            p0 = fast_exp2(x0);
-            p1 = fast_exp2(x1);
-        }
+        p0 = fast_exp2(x0);
+        p1 = fast_exp2(x1);
         rs4[c & 3] = fadd2(rs4[c & 3], f32x2(p0, p1));
         pk[c] = pack2<F16>(p0, p1);
     }

@@ -396,34 +396,6 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
     return d;
 }
 
-// 2^x for two floats at once on the FMA pipe (no MUFU): Cody-Waite reduction
-// in base 2, 2^x = 2^j * 2^f with j = round(x) (via the 1.5 * 2^23 shifter)
-// and f = x - j in [-1/2, 1/2], then a degree-4 polynomial for 2^f whose
-// coefficients minimise the maximum relative error on [-1/2, 1/2] (Remez
-// exchange, csrc/fit_exp2.py), then j added into the exponent field.
-// Relative error <= 2.7e-6 for x in [-125, 127].  Arguments below -126 are
-// clamped to -126 (p(f) >= 2^-1/2 then keeps the exponent field at 0 or 1, so
-// it cannot wrap); the result there is below 2^-125.  Inputs must be finite.
-__device__ __forceinline__ void exp2_poly_x2(float x0, float x1, float& y0, float& y1) {
-    x0 = fmaxf(x0, -126.f);
-    x1 = fmaxf(x1, -126.f);
-    const uint64_t shifter = f32x2(12582912.f, 12582912.f);          // 1.5 * 2^23
-    const uint64_t x = f32x2(x0, x1);
-    const uint64_t t = fadd2(x, shifter);                              // round(x) in the low mantissa bits
-    const uint64_t j = fadd2(t, f32x2(-12582912.f, -12582912.f));      // round(x) as a float
-    const uint64_t f = ffma2(j, f32x2(-1.f, -1.f), x);                 // x - round(x)
-    uint64_t p = ffma2(f32x2(9.570102207e-03f, 9.570102207e-03f), f, f32x2(5.591785908e-02f, 5.591785908e-02f));
-    p = ffma2(p, f, f32x2(2.402474433e-01f, 2.402474433e-01f));
-    p = ffma2(p, f, f32x2(6.931217909e-01f, 6.931217909e-01f));
-    p = ffma2(p, f, f32x2(9.999992847e-01f, 9.999992847e-01f));
-    float p0, p1, t0, t1;
-    f32x2_split(p, p0, p1);
-    f32x2_split(t, t0, t1);
-    // bits(t) = bits(1.5 * 2^23) + j and bits(1.5 * 2^23) << 23 vanishes mod 2^32
-    y0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
-    y1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
-}
-
 // Pack two floats into bf16x2 (round to nearest even); `lo` goes to the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;

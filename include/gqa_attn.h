@@ -333,16 +333,6 @@ const char* gqa_status_string(gqa_status status);
  */
 gqa_status gqa_device_error(void);
 
-/*
- * Diagnostic: y[i] = 2^x[i] (device arrays of n floats) computed by the
- * FMA-pipe exp2 routine the prefill kernel uses for part of its softmax
- * exponentials (base-2 Cody-Waite reduction plus a fitted degree-4 minimax
- * polynomial; relative error <= 2.7e-6 for x in [-125, 127], arguments below
- * -126 clamped).  Exposed so the routine can be checked against exp2f; not
- * part of the attention path.
- */
-gqa_status gqa_exp2_poly(const float* x, float* y, long n, gqa_stream_t stream);
-
 /* Library version string. */
 const char* gqa_version(void);
 

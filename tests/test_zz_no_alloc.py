@@ -5,9 +5,9 @@ serving engine whose memory is all pre-reserved by its own pool, a plugin in a
 host framework that forbids allocation while it runs, a loop that cannot pay
 for cudaMalloc's implicit synchronisation): its split partials live in a fixed
 array inside the library.  Here it is called through the C ABI and must match
-attn_decode_paged (caller workspace) within the parity tolerances, on two calls
-in a row with different inputs, so a stale array from the first call would
-show.  This file sorts last so that a run stopping at the first failure has
+attn_decode_paged (caller workspace) within the parity tolerances, with each
+of its two decode routes called twice in a row on different inputs, so a stale
+array from the first call would show.  This file sorts last so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process.
 """
 import ctypes
@@ -68,14 +68,54 @@ def _close(a, b):
 
 
 def test_noalloc_matches_workspace_entry_point_twice(lib):
-    first = W.paged_inputs(6, 1, 32, 8, 128, 64, lengths=[1500, 0, 7000, 64, 3333, 12000], seed=11)
-    second = W.paged_inputs(3, 4, 24, 2, 256, 16, lengths=[900, 2, 5000], seed=12)
-    for p in (first, second):
+    # Each of the two decode routes runs twice in a row on the shared array,
+    # the second call with other inputs and shorter requests (one of them
+    # empty), so partials or segment-table entries left by the first call
+    # would show in the second.
+    split_path = [  # 4 query rows per KV head: the split-KV kernel and its partials
+        W.paged_inputs(6, 1, 32, 8, 128, 64, lengths=[1500, 0, 7000, 64, 3333, 12000], seed=11),
+        W.paged_inputs(5, 1, 32, 8, 128, 64, lengths=[700, 9000, 0, 1, 2100], seed=13),
+    ]
+    tensor_core_path = [  # 48 rows per KV head: the balanced tensor-core kernel and its segment table
+        W.paged_inputs(3, 4, 24, 2, 256, 16, lengths=[900, 2, 5000], seed=12),
+        W.paged_inputs(4, 4, 24, 2, 256, 16, lengths=[300, 0, 4, 1200], seed=14),
+    ]
+    for p in split_path + tensor_core_path:
         na = _call(lib, lib.attn_decode_paged_noalloc, p)
         assert na[0] == 0, lib.gqa_status_string(na[0])
         ref = _with_workspace(lib, p)
         assert ref[0] == 0
         _close(na, ref)
+
+
+def test_noalloc_python_wrapper_checks_its_arguments(lib):
+    import gqa_softmax_attention_gb300 as g
+    p = W.paged_inputs(2, 1, 8, 2, 128, 16, lengths=[40, 17], seed=15)
+    dev = "cuda"
+    q, kc, vc = p["q"].to(dev), p["k_cache"].to(dev), p["v_cache"].to(dev)
+    sl, bt = p["real_seqlen_kv"].to(dev), p["block_table"].to(dev)
+    o, lse = g.attn_decode_paged_noalloc(q, kc, vc, sl, bt)
+    ref = _with_workspace(lib, p)
+    torch.cuda.synchronize()
+    _close((0, o.cpu(), lse.cpu()), ref)
+    bad = [
+        dict(real_seqlen_kv=sl.cpu()),                       # lengths on the host
+        dict(block_table=bt.to(torch.int64)),                # wrong index type
+        dict(v_cache=vc[:, :8].contiguous()),                # smaller value cache
+        dict(k_cache=kc[..., :64].contiguous()),             # head dim differs from q's
+        dict(real_seqlen_kv=sl[:1]),                         # not [B]
+    ]
+    for change in bad:
+        args = dict(q=q, k_cache=kc, v_cache=vc, real_seqlen_kv=sl, block_table=bt)
+        args.update(change)
+        with pytest.raises(ValueError):
+            g.attn_decode_paged_noalloc(**args)
+    # a strided block table is made contiguous, not read with the wrong stride
+    wide = torch.full((bt.shape[0], 2 * bt.shape[1]), -1, dtype=torch.int32, device=dev)
+    wide[:, ::2] = bt
+    o2, lse2 = g.attn_decode_paged_noalloc(q, kc, vc, sl, wide[:, ::2])
+    torch.cuda.synchronize()
+    _close((0, o2.cpu(), lse2.cpu()), ref)
 
 
 def test_noalloc_refuses_sizes_beyond_its_array(lib):
