@@ -1,22 +1,28 @@
 #!/usr/bin/env python
 """Benchmark of the causal GQA attention forward hot path on GB300.
 
-One step = one pass of the whole path over one batch of synthetic input:
-  * dense prefill, Qwen3-8B-shaped: B=2, Sq=Skv=4096, Hq=32, Hkv=8, D=128,
+One step = one pass of the whole path over the five synthetic workloads, each
+through its own entry point (inputs resident in HBM before timing):
+  * tiny_dense: B=1, Hq=4, Hkv=2, Sq=Skv=128, D=64, causal (latency only);
+  * qwen3_8b_prefill: dense prefill, B=2, Sq=Skv=4096, Hq=32, Hkv=8, D=128,
     causal, key_padding_mask with per-batch valid lengths U[2048, 4096];
-  * paged decode of the same geometry: B=64, Sq=1, ps=64, lengths
-    U[1024, 16384], pages shuffled through block_table.
-Inputs are resident in HBM before timing.  Work is counted algorithmically:
-prefill FLOPs = 4 * D * Hq * (visible query/key pairs), decode bytes = the K
-and V bytes of the real tokens (one byte per element for e4m3fn caches).  The reported value is the step's roofline
-efficiency, 100 * (FLOPs / tensor peak + bytes / HBM peak) / step time, with
-the measured peaks of this machine; per-kernel TFLOP/s and GB/s are reported
-beside it.  Between timed steps a buffer twice the L2 size is overwritten so
-every step starts with a cold L2.
+  * paged_decode: B=64, Sq=1, Hq=32, Hkv=8, D=128, pages of 64 tokens, lengths
+    U[1024, 16384], pages shuffled through block_table;
+  * wide_group_decode: B=32, Sq=4 causal, Hq=24, Hkv=2, D=256, pages of 16
+    tokens, lengths U[512, 32768];
+  * long_chunked_prefill: B=4, Sq=2048 queries at the end of Skv=32768 keys,
+    Hq=64, Hkv=8, D=128, causal, values N(0, 0.5^2).
+Work is counted algorithmically: prefill FLOPs = 4 * D * Hq * (visible
+query/key pairs), decode bytes = the K and V bytes of the real tokens (one byte
+per element for e4m3fn caches).  The reported value is the step's roofline
+efficiency, 100 * sum(FLOPs / tensor peak + bytes / HBM peak) / step time, with
+the measured peaks of this machine; per-workload TFLOP/s or GB/s and their
+fractions of the measured (and of the nominal) peaks are reported beside it.
+Between timed steps a buffer twice the L2 size is overwritten so every step
+starts with a cold L2.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload step|qwen3_8b_prefill|paged_decode|wide_group_decode|long_chunked_prefill|
-                                   wide_group_prefill|varlen_prefill|mixed_serving_batch|paged_decode_fp8kv]
+                       [--workload step|serving_step|<one workload name>]
 Prints exactly one JSON line (rank 0).
 """
 import argparse
@@ -37,6 +43,17 @@ from gqa_softmax_attention_gb300 import workloads as W  # noqa: E402
 METRIC = "prefill TFLOP/s and paged-decode HBM GB/s, as % of GB300 roofline"
 UNIT = "% of roofline"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal GB300 figures: dense bf16 tensor peak and HBM3e bandwidth
+NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
+STEPS = {
+    "step": ["tiny_dense", "qwen3_8b_prefill", "paged_decode", "wide_group_decode", "long_chunked_prefill"],
+    "serving_step": ["qwen3_8b_prefill", "paged_decode"],
+}
+# Roofline targets per workload, judged on the measured peaks: causal prefill
+# at least 60 % of the dense bf16 tensor peak, paged decode at least 75 % of
+# the HBM bandwidth.  tiny_dense is latency-bound and has none.
+TARGETS = {"qwen3_8b_prefill": 0.60, "long_chunked_prefill": 0.60, "paged_decode": 0.75,
+           "wide_group_decode": 0.75}
 
 
 # --------------------------------------------------------------------------- work accounting
@@ -185,7 +202,30 @@ class Part:
             self.dev["lse"] = torch.empty((c["B"], c["Sq"], c["Hq"]), dtype=torch.float32, device=dev)
 
     def launches(self):
-        return 1 if self.kind == "dense" else 2           # packed calls: plan + attention
+        return 1 if self.kind == "dense" else 2           # packed calls: plan + attention; decode: split + combine
+
+    def bound(self, peaks):
+        """"tensor" or "hbm": the larger of the FLOP and byte terms."""
+        return "tensor" if self.flops / peaks["bf16_tflops"] / 1e12 >= self.bytes / peaks["hbm_gbs"] / 1e9 else "hbm"
+
+    def kernel_name(self):
+        """The kernels this part launches, as the profiler lists them."""
+        c = self.data["config"]
+        if self.kind == "dense":
+            return "onetile_kernel<256,kBSHD>" if c["D"] == 256 else "prefill_kernel<%d>" % c["D"]
+        if self.kind == "varlen":
+            return "onetile_kernel<%d,kPacked> + varlen_plan_kernel" % c["D"]
+        if self.kind == "paged_varlen":
+            return "onetile_kernel<%d,kPaged> + varlen_plan_kernel" % c["D"]
+        rows = c["Hq"] // c["Hkv"] * c["Sq"]
+        tc = c["D"] in (128, 256) and 32 <= rows <= 128 and c["page_size"] % 8 == 0 and (
+            c["page_size"] >= 64 or 64 % c["page_size"] == 0)
+        mf = min(4, (rows + 15) // 16)
+        if self.kind == "paged_fp8":
+            split = ("decode_tc_kernel<%d,e4m3>" % c["D"]) if tc else "decode_fp8_kernel<%d,%d>" % (c["D"], mf)
+        else:
+            split = "decode_tc_kernel<%d>" % c["D"] if tc else "decode_tma_kernel<%d,%d>" % (c["D"], mf)
+        return split + " + decode_combine_kernel<%d>" % c["D"]
 
     def run(self):
         import gqa_softmax_attention_gb300 as g
@@ -242,7 +282,7 @@ class Part:
 
 def make_parts(workload, batch=None):
     """The step's parts; `batch` shrinks a single named workload's B (for profiling captures)."""
-    names = ["qwen3_8b_prefill", "paged_decode"] if workload == "step" else [workload]
+    names = STEPS.get(workload, [workload])
     parts = []
     for n in names:
         if batch is None:
@@ -258,8 +298,81 @@ def make_parts(workload, batch=None):
     return parts
 
 
+def workload_label(workload):
+    if workload in STEPS:
+        return "%s: %s" % ("five-workload step" if workload == "step" else "serving step",
+                           " + ".join(STEPS[workload]))
+    return workload
+
+
 # --------------------------------------------------------------------------- clocks
-class ClockSampler:
+class NvmlClocks:
+    """SM clock, its maximum, power and the clock-event reasons, read through
+    NVML (read-only queries) every few milliseconds on a host thread while the
+    timed loop runs."""
+    # nvml.h clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index, period_s=0.002):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.period = period_s
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for " + uuid)
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.sm_max = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 \
+            else None
+        self.rows = []
+        self.stop_ev = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _sample(self):
+        ct = self.ct
+        clk, rs, pw = ct.c_uint(), ct.c_ulonglong(), ct.c_uint()
+        ok = self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) == 0      # NVML_CLOCK_SM
+        ok = ok and self.reason_fn(self.h, ct.byref(rs)) == 0
+        p = pw.value / 1e3 if self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw)) == 0 else None
+        if ok:
+            self.rows.append((time.perf_counter(), float(clk.value), int(rs.value), p))
+
+    def _run(self):
+        while not self.stop_ev.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        self._sample()
+        self.thread.start()
+
+    def stop(self, t0, t1):
+        self.stop_ev.set()
+        self.thread.join()
+        rows = [r for r in self.rows if t0 <= r[0] <= t1] or self.rows[-1:]
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for bit, name in self.REASONS.items():
+                if r[2] & bit:
+                    reasons.add(name)
+        pw = [r[3] for r in rows if r[3] is not None]
+        return dict(sm_mhz=statistics.median(r[1] for r in rows), sm_max_mhz=self.sm_max,
+                    sm_mhz_min=min(r[1] for r in rows), reasons=sorted(reasons), samples=len(rows),
+                    power_w_max=max(pw) if pw else None, source="NVML, every %g ms" % (1e3 * self.period))
+
+
+class SmiClocks:
+    """Fallback sampler: nvidia-smi every 50 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -281,7 +394,7 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -302,7 +415,14 @@ class ClockSampler:
                 if r[col].strip().lower() == "active":
                     reasons.add(name)
         return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
-                    reasons=sorted(reasons), samples=len(rows))
+                    reasons=sorted(reasons), samples=len(rows), source="nvidia-smi, every 50 ms")
+
+
+def clock_sampler(device_index):
+    try:
+        return NvmlClocks(device_index)
+    except Exception:
+        return SmiClocks(device_index)
 
 
 # --------------------------------------------------------------------------- distributed
@@ -335,6 +455,50 @@ def barrier(world):
 
 
 # --------------------------------------------------------------------------- our arm
+def part_detail(p, ts, peaks):
+    """Per-part timing: mean and min launch-group time, achieved rate and its
+    fraction of the measured and of the nominal peak, the target if any."""
+    t = statistics.mean(ts)
+    d = dict(kernel=p.kernel_name(), ms=1e3 * t, ms_min=1e3 * min(ts), bound=p.bound(peaks))
+    if p.kind == "paged_varlen":
+        d.update(tflops=p.flops / t / 1e12, gbs=p.bytes / t / 1e9, frac=p.ideal_s(peaks) / t,
+                 gflop=p.flops / 1e9, gbytes=p.bytes / 1e9)
+    elif p.flops > 0:
+        ach = p.flops / t / 1e12
+        d.update(tflops=ach, frac=ach / peaks["bf16_tflops"], frac_nominal=ach / NOMINAL["bf16_tflops"],
+                 gflop=p.flops / 1e9)
+    else:
+        ach = p.bytes / t / 1e9
+        d.update(gbs=ach, frac=ach / peaks["hbm_gbs"], frac_nominal=ach / NOMINAL["hbm_gbs"], gbytes=p.bytes / 1e9)
+    if p.name in TARGETS:
+        d.update(target=TARGETS[p.name], met=d["frac"] >= TARGETS[p.name])
+    tr = traffic_per_launch(p)
+    d["dram_traffic_bytes"] = tr
+    return d
+
+
+def roofline_of(p, t, peaks):
+    """The roofline object of the dominant part (largest mean time)."""
+    t_tensor = p.flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = p.bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        ach = p.flops / t / 1e12
+        roof = dict(bound="tensor", achieved=ach, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                    frac=ach / peaks["bf16_tflops"], peak_source=peaks["source"] + " bf16 burst",
+                    frac_of_sustained=ach / peaks["bf16_tflops_sustained"],
+                    frac_nominal=ach / NOMINAL["bf16_tflops"])
+    else:
+        ach = p.bytes / t / 1e9
+        roof = dict(bound="hbm", achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s", frac=ach / peaks["hbm_gbs"],
+                    peak_source=peaks["source"] + " copy bandwidth", frac_nominal=ach / NOMINAL["hbm_gbs"])
+    roof.update(kernel="%s (%s)" % (p.kernel_name(), p.name), traffic=traffic_per_launch(p),
+                algorithmic=dict(flops=p.flops, bytes=p.bytes))
+    if p.kind == "paged_varlen":
+        roof["mixed"] = dict(tflops=p.flops / t / 1e12, gbs=p.bytes / t / 1e9,
+                             frac_of_summed_roofline=(t_tensor + t_hbm) / t)
+    return roof
+
+
 def bench_ours(args, world, rank, local):
     import gqa_softmax_attention_gb300 as g
     from gqa_softmax_attention_gb300 import _lib
@@ -358,7 +522,7 @@ def bench_ours(args, world, rank, local):
 
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
           for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    clocks = clock_sampler(local)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -370,9 +534,10 @@ def bench_ours(args, world, rank, local):
             p.run()
             ev[s][j][1].record(stream)
     torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
     barrier(world)
     wall = time.perf_counter() - t0
-    clk = clocks.stop()
+    clk = clocks.stop(t0, t1)
     g.gqa_device_error()
 
     per_part = [[ev[s][j][0].elapsed_time(ev[s][j][1]) / 1e3 for s in range(args.steps)] for j in range(len(parts))]
@@ -381,66 +546,9 @@ def bench_ours(args, world, rank, local):
     ideal = sum(p.ideal_s(peaks) for p in parts)
     value = job_value(ideal, step_s_max, world)
 
-    detail = {}
-    dom, dom_t = None, -1.0
-    for p, ts in zip(parts, per_part):
-        t = statistics.mean(ts)
-        if p.kind == "paged_varlen":
-            detail[p.name] = dict(ms=1e3 * t, ms_min=1e3 * min(ts), tflops=p.flops / t / 1e12, gbs=p.bytes / t / 1e9,
-                                  frac=p.ideal_s(peaks) / t, gflop=p.flops / 1e9, gbytes=p.bytes / 1e9)
-        elif p.kind in ("dense", "varlen"):
-            ach = p.flops / t / 1e12
-            detail[p.name] = dict(ms=1e3 * t, ms_min=1e3 * min(ts), tflops=ach,
-                                  frac=ach / peaks["bf16_tflops"], gflop=p.flops / 1e9)
-        else:
-            ach = p.bytes / t / 1e9
-            detail[p.name] = dict(ms=1e3 * t, ms_min=1e3 * min(ts), gbs=ach, frac=ach / peaks["hbm_gbs"],
-                                  gbytes=p.bytes / 1e9)
-        if t > dom_t:
-            dom, dom_t = p, t
-    if dom.kind == "paged_varlen":
-        # one launch serving prefill chunks and decode steps: the roofline is
-        # the sum of the FLOP term and the K/V byte term; the dominant one names it
-        c = dom.data["config"]
-        t_tensor = dom.flops / (peaks["bf16_tflops"] * 1e12)
-        t_hbm = dom.bytes / (peaks["hbm_gbs"] * 1e9)
-        if t_hbm >= t_tensor:
-            roof = dict(bound="hbm", achieved=dom.bytes / dom_t / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
-                        frac=dom.bytes / dom_t / 1e9 / peaks["hbm_gbs"])
-        else:
-            roof = dict(bound="tensor", achieved=dom.flops / dom_t / 1e12, peak=peaks["bf16_tflops"], unit="TFLOP/s",
-                        frac=dom.flops / dom_t / 1e12 / peaks["bf16_tflops"])
-        roof.update(kernel="onetile_kernel<%d,kPaged> + varlen_plan_kernel (%s)" % (c["D"], dom.name),
-                    traffic=traffic_per_launch(dom), peak_source=peaks["source"],
-                    mixed=dict(tflops=dom.flops / dom_t / 1e12, gbs=dom.bytes / dom_t / 1e9,
-                               frac_of_summed_roofline=(t_tensor + t_hbm) / dom_t))
-    elif dom.kind == "varlen":
-        ach = dom.flops / dom_t / 1e12
-        roof = dict(kernel="onetile_kernel<%d,kPacked> + varlen_plan_kernel (%s)" % (dom.data["config"]["D"], dom.name),
-                    bound="tensor", achieved=ach, peak=peaks["bf16_tflops"], unit="TFLOP/s",
-                    frac=ach / peaks["bf16_tflops"], traffic=traffic_per_launch(dom),
-                    peak_source=peaks["source"] + " bf16 burst")
-    elif dom.kind == "dense":
-        ach = dom.flops / dom_t / 1e12
-        kname = ("onetile_kernel<256,kBSHD>" if dom.data["config"]["D"] == 256
-                 else "prefill_kernel<%d>" % dom.data["config"]["D"])
-        roof = dict(kernel=kname + " (" + dom.name + ")", bound="tensor", achieved=ach,
-                    peak=peaks["bf16_tflops"], unit="TFLOP/s", frac=ach / peaks["bf16_tflops"],
-                    traffic=traffic_per_launch(dom), peak_source=peaks["source"] + " bf16 burst")
-    else:
-        ach = dom.bytes / dom_t / 1e9
-        c = dom.data["config"]
-        rows = c["Hq"] // c["Hkv"] * c["Sq"]
-        tc = c["D"] in (128, 256) and 32 <= rows <= 128 and c["page_size"] % 8 == 0 and (
-            c["page_size"] >= 64 or 64 % c["page_size"] == 0)
-        mf = min(4, (rows + 15) // 16)
-        split = "decode_tc_kernel<%d>" % c["D"] if tc else "decode_tma_kernel<%d,%d>" % (c["D"], mf)
-        if dom.kind == "paged_fp8":
-            split = ("decode_tc_kernel<%d,e4m3>" % c["D"]) if tc else "decode_fp8_kernel<%d,%d>" % (c["D"], mf)
-        roof = dict(kernel=split + " + decode_combine_kernel<%d> (%s)" % (c["D"], dom.name), bound="hbm",
-                    achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s", frac=ach / peaks["hbm_gbs"],
-                    traffic=traffic_per_launch(dom),
-                    peak_source=peaks["source"] + " copy bandwidth")
+    detail = {p.name: part_detail(p, ts, peaks) for p, ts in zip(parts, per_part)}
+    dom_j = max(range(len(parts)), key=lambda j: statistics.mean(per_part[j]))
+    roof = roofline_of(parts[dom_j], statistics.mean(per_part[dom_j]), peaks)
 
     e2e = bench_e2e(args, parts, peaks, dev, stream, world)
     cpu = cpu_baseline(args, parts, peaks) if (rank == 0 and world == 1 and not args.no_cpu) else None
@@ -451,11 +559,13 @@ def bench_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None,
         # the arithmetic type: e4m3fn caches widened to float16 products, else bf16
         "dtype": "e4m3kv-f16" if any(p.kind == "paged_fp8" for p in parts) else "bf16", "data": "synthetic",
-        "config": {"workload": "serving step: qwen3_8b_prefill + paged_decode" if args.workload == "step"
-                   else args.workload,
+        "config": {"workload": workload_label(args.workload),
                    "parts": {p.name: p.data["config"] for p in parts}, "parallelism": "replicas",
                    "l2": "flushed between steps (%d MB write)" % (flush.numel() * 4 >> 20)},
         "parts": detail, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+        "targets": {"judged_on": "measured peaks (MEASURED_PEAKS.json); frac_nominal uses %g TFLOP/s and %g GB/s"
+                                 % (NOMINAL["bf16_tflops"], NOMINAL["hbm_gbs"]),
+                    "met": {n: d["met"] for n, d in detail.items() if "met" in d}},
         "gpu_launches": args.steps * sum(p.launches() for p in parts),
         "peaks": peaks, "wall_s_timed_loop": wall,
     }
@@ -487,142 +597,193 @@ def bench_e2e(args, parts, peaks, dev, stream, world):
 
 
 # --------------------------------------------------------------------------- oracle timing
-def oracle_sample(parts, prefill_rows, decode_requests, seed=0):
-    """Time the FP64 oracle on a bounded sample of each part; returns the
-    estimated seconds for the whole step and a description of the sample."""
+def _draw_sample(p, frac, gen):
+    """A bounded random sample of part p: about `frac` of its work, at least
+    one unit.  Units are query rows (b, i, h) of a dense call, query rows of
+    a packed call, and (request, query head) pairs of a paged decode, whose K/V
+    bytes count 1/g of that request's KV-head bytes (g query heads share them).
+    Returns (kind of unit, units, sampled FLOPs, sampled bytes)."""
+    d, c = p.data, p.data["config"]
+    if p.kind == "dense":
+        total = c["B"] * c["Sq"] * c["Hq"]
+        n = max(1, min(total, int(round(frac * total))))
+        flat = torch.randperm(total, generator=gen)[:n]
+        rows = torch.stack([flat // (c["Sq"] * c["Hq"]), (flat // c["Hq"]) % c["Sq"], flat % c["Hq"]], 1).tolist()
+        m = d["key_padding_mask"]
+        pairs = 0
+        for b, i, _h in rows:
+            lim = max(0, min(c["Skv"], i + c["Skv"] - c["Sq"] + 1)) if c["causal"] else c["Skv"]
+            pairs += int(m[b, :lim].sum()) if m is not None else lim
+        return "rows", rows, 4.0 * c["D"] * pairs, 0.0
+    if p.kind in ("varlen", "paged_varlen"):
+        cu = d["cu_seqlens_q"]
+        tq = int(cu[-1])
+        n = max(1, int(round(frac * tq)))
+        toks = torch.randperm(tq, generator=gen)[:n].tolist()
+        units, flops, kvb = [], 0.0, 0.0
+        for t in toks:
+            b = int(torch.searchsorted(cu, torch.tensor(t), right=True)) - 1
+            sq, i = int(cu[b + 1] - cu[b]), t - int(cu[b])
+            L = (int(d["cu_seqlens_kv"][b + 1] - d["cu_seqlens_kv"][b]) if p.kind == "varlen"
+                 else int(d["cache_seqlens"][b]))
+            vis = max(0, min(L, i + L - sq + 1))
+            units.append((t, b, vis))
+            flops += 4.0 * c["D"] * c["Hq"] * vis
+            if p.kind == "paged_varlen" and sq == 1:
+                kvb += vis * 2 * c["Hkv"] * c["D"] * 2
+        return "query rows", units, flops, kvb
+    elem = 1 if p.kind == "paged_fp8" else 2
+    g = c["Hq"] // c["Hkv"]
+    lens = d["real_seqlen_kv"].tolist()
+    want = frac * p.bytes
+    units, got = [], 0.0
+    for u in torch.randperm(c["B"] * c["Hq"], generator=gen).tolist():
+        if units and got >= want:
+            break
+        b, h = divmod(u, c["Hq"])
+        units.append((b, h))
+        got += lens[b] * 2 * c["D"] * elem / g
+    return "(request, query head) pairs", units, 0.0, got
+
+
+def _decode_units(p, units):
+    """The sampled (request, query head) pairs of a paged decode as one
+    compact paged call with one query head and one KV head per request: each
+    pair's pages (its KV head only) copied into a small pool in logical
+    order.  Same arithmetic per row as the full call."""
+    d, c = p.data, p.data["config"]
+    ps, g = c["page_size"], c["Hq"] // c["Hkv"]
+    lens = d["real_seqlen_kv"].tolist()
+    kp, vp, tables, sl, qs, ks, vs = [], [], [], [], [], [], []
+    first = 0
+    for b, h in units:
+        r = h // g
+        n = max(1, -(-lens[b] // ps))
+        pages = d["block_table"][b, :n].clamp(min=0).to(torch.int64)
+        kp.append(d["k_cache"][pages][:, :, r:r + 1, :])
+        vp.append(d["v_cache"][pages][:, :, r:r + 1, :])
+        tables.append(list(range(first, first + n)))
+        first += n
+        sl.append(lens[b])
+        qs.append(d["q"][b:b + 1, :, h:h + 1, :])
+        if p.kind == "paged_fp8":
+            ks.append(float(d["k_scale"][b, r]))
+            vs.append(float(d["v_scale"][b, r]))
+    width = max(len(t) for t in tables)
+    bt = torch.full((len(units), width), -1, dtype=torch.int32)
+    for i, t in enumerate(tables):
+        bt[i, :len(t)] = torch.tensor(t, dtype=torch.int32)
+    out = dict(q=torch.cat(qs).contiguous(), k_cache=torch.cat(kp).contiguous(), v_cache=torch.cat(vp).contiguous(),
+               real_seqlen_kv=torch.tensor(sl, dtype=torch.int32), block_table=bt)
+    if p.kind == "paged_fp8":
+        out.update(k_scale=torch.tensor(ks).view(-1, 1), v_scale=torch.tensor(vs).view(-1, 1))
+    return out
+
+
+def _run_sample(p, unit, units, nthreads=0):
+    """Run the FP64 oracle on a drawn sample; returns the seconds it took (the
+    copy that gathers a decode sample's pages is not timed)."""
     import oracle
-    est, desc = 0.0, []
-    gen = torch.Generator().manual_seed(seed)
-    for p in parts:
-        d, c = p.data, p.data["config"]
-        if p.kind == "dense":
-            n = prefill_rows
-            rows = torch.stack([torch.randint(0, c["B"], (n,), generator=gen),
-                                torch.randint(0, c["Sq"], (n,), generator=gen),
-                                torch.randint(0, c["Hq"], (n,), generator=gen)], 1)
-            m = d["key_padding_mask"]
-            pairs = 0
-            for b, i, _h in rows.tolist():
-                lim = max(0, min(c["Skv"], i + c["Skv"] - c["Sq"] + 1))
-                pairs += int(m[b, :lim].sum()) if m is not None else lim
-            t0 = time.perf_counter()
-            oracle.attn_dense_rows(d["q"], d["k"], d["v"], rows.tolist(), key_padding_mask=m, causal=True)
-            dt = time.perf_counter() - t0
-            total_pairs = p.pairs * c["Hq"]            # p.pairs counts one head
-            est += dt * total_pairs / max(pairs, 1)
-            desc.append("%s: %d random rows (%.2f%% of its pairs) in %.2fs" % (p.name, n, 100.0 * pairs / total_pairs,
-                                                                              dt))
-        elif p.kind in ("varlen", "paged_varlen"):
-            # random packed query rows, each as a one-query call whose keys end
-            # at that query's position (end-aligned causal)
-            n = max(1, prefill_rows // 64)
-            cu = d["cu_seqlens_q"]
-            tq = int(cu[-1])
-            one = torch.tensor([0, 1], dtype=torch.int32)
-            rows = torch.randint(0, tq, (n,), generator=gen).tolist()
-            pairs, dt = 0, 0.0
-            for t in rows:
-                b = int(torch.searchsorted(cu, torch.tensor(t), right=True)) - 1
-                sq, i = int(cu[b + 1] - cu[b]), t - int(cu[b])
-                if p.kind == "varlen":
-                    ks, L = int(d["cu_seqlens_kv"][b]), int(d["cu_seqlens_kv"][b + 1] - d["cu_seqlens_kv"][b])
-                    vis = max(0, min(L, i + L - sq + 1))
-                    t0 = time.perf_counter()
-                    oracle.attn_varlen(d["q"][t:t + 1], d["k"][ks:ks + vis], d["v"][ks:ks + vis], one,
-                                       torch.tensor([0, vis], dtype=torch.int32), causal=True)
-                else:
-                    L = int(d["cache_seqlens"][b])
-                    vis = max(0, min(L, i + L - sq + 1))
-                    t0 = time.perf_counter()
-                    oracle.attn_paged_varlen(d["q"][t:t + 1], d["k_cache"], d["v_cache"], one,
-                                             torch.tensor([vis], dtype=torch.int32), d["block_table"][b:b + 1],
-                                             causal=True)
-                dt += time.perf_counter() - t0
-                pairs += vis
-            est += dt * p.pairs / max(pairs, 1)
-            desc.append("%s: %d random query rows (%.3f%% of its pairs) in %.2fs" % (p.name, n, 100.0 * pairs / p.pairs,
-                                                                                    dt))
+    d, c = p.data, p.data["config"]
+    if p.kind in ("paged", "paged_fp8"):
+        u = _decode_units(p, units)
+        t0 = time.perf_counter()
+        if p.kind == "paged_fp8":
+            oracle.attn_paged_fp8kv(u["q"], u["k_cache"], u["v_cache"], u["k_scale"], u["v_scale"],
+                                    u["real_seqlen_kv"], u["block_table"], causal=c["causal"], nthreads=nthreads)
         else:
-            n = min(decode_requests, c["B"])
-            reqs = torch.randperm(c["B"], generator=gen)[:n].tolist()
-            elem = 1 if p.kind == "paged_fp8" else 2
-            sel_bytes = float(d["real_seqlen_kv"][reqs].to(torch.int64).sum()) * 2 * c["Hkv"] * c["D"] * elem
-            t0 = time.perf_counter()
-            if p.kind == "paged_fp8":
-                oracle.attn_paged_fp8kv(d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
-                                        d["real_seqlen_kv"], d["block_table"], causal=True, requests=reqs)
-            else:
-                oracle.attn_paged(d["q"], d["k_cache"], d["v_cache"], d["real_seqlen_kv"], d["block_table"],
-                                  causal=True, requests=reqs)
-            dt = time.perf_counter() - t0
-            est += dt * p.bytes / max(sel_bytes, 1.0)
-            desc.append("%s: %d whole requests (%.2f%% of its bytes) in %.2fs" % (p.name, n, 100.0 * sel_bytes / p.bytes,
-                                                                                  dt))
-    return est, "; ".join(desc)
-
-
-def oracle_whole(parts):
-    """Time the FP64 oracle on the whole step (every row of every part)."""
-    import oracle
+            oracle.attn_paged(u["q"], u["k_cache"], u["v_cache"], u["real_seqlen_kv"], u["block_table"],
+                              causal=c["causal"], nthreads=nthreads)
+        return time.perf_counter() - t0
     t0 = time.perf_counter()
-    for p in parts:
-        d = p.data
-        if p.kind == "dense":
-            oracle.attn_dense(d["q"], d["k"], d["v"], key_padding_mask=d["key_padding_mask"], causal=True)
-        elif p.kind == "varlen":
-            oracle.attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_kv"], causal=True)
-        elif p.kind == "paged_varlen":
-            oracle.attn_paged_varlen(d["q"], d["k_cache"], d["v_cache"], d["cu_seqlens_q"], d["cache_seqlens"],
-                                     d["block_table"], causal=True)
-        elif p.kind == "paged_fp8":
-            oracle.attn_paged_fp8kv(d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
-                                    d["real_seqlen_kv"], d["block_table"], causal=True)
-        else:
-            oracle.attn_paged(d["q"], d["k_cache"], d["v_cache"], d["real_seqlen_kv"], d["block_table"], causal=True)
+    if unit == "rows":
+        oracle.attn_dense_rows(d["q"], d["k"], d["v"], units, key_padding_mask=d["key_padding_mask"],
+                               causal=c["causal"], nthreads=nthreads)
+    else:
+        one = torch.tensor([0, 1], dtype=torch.int32)
+        for t, b, vis in units:
+            if p.kind == "varlen":
+                ks = int(d["cu_seqlens_kv"][b])
+                oracle.attn_varlen(d["q"][t:t + 1], d["k"][ks:ks + vis], d["v"][ks:ks + vis], one,
+                                   torch.tensor([0, vis], dtype=torch.int32), causal=True, nthreads=nthreads)
+            else:
+                oracle.attn_paged_varlen(d["q"][t:t + 1], d["k_cache"], d["v_cache"], one,
+                                         torch.tensor([vis], dtype=torch.int32), d["block_table"][b:b + 1],
+                                         causal=True, nthreads=nthreads)
     return time.perf_counter() - t0
 
 
+def oracle_sample(parts, peaks, frac, seed, nthreads=0):
+    """Time the FP64 oracle on a bounded random sample of every part (about
+    `frac` of each part's rows or K/V bytes).  Returns the sample's ideal
+    seconds (its FLOPs and bytes at the measured peaks), the oracle's seconds
+    on it, and per-part records."""
+    gen = torch.Generator().manual_seed(seed)
+    ideal, secs, recs = 0.0, 0.0, {}
+    for p in parts:
+        unit, units, flops, nbytes = _draw_sample(p, frac, gen)
+        dt = _run_sample(p, unit, units, nthreads)
+        i = flops / (peaks["bf16_tflops"] * 1e12) + nbytes / (peaks["hbm_gbs"] * 1e9)
+        share = (flops / p.flops) if p.flops > 0 else (nbytes / p.bytes if p.bytes > 0 else 0.0)
+        recs[p.name] = dict(sample="%d %s" % (len(units), unit), share_of_part=share, seconds=dt,
+                            gflops_per_s=flops / dt / 1e9 if flops else None,
+                            gbs=nbytes / dt / 1e9 if nbytes else None,
+                            whole_part_s_est=dt / share if share > 0 else None)
+        ideal += i
+        secs += dt
+    return ideal, secs, recs
+
+
 def cpu_baseline(args, parts, peaks):
+    """The FP64 oracle on the host cores, on a bounded sample of the step."""
     import oracle
-    ideal = sum(p.ideal_s(peaks) for p in parts)
-    if sum(p.flops for p in parts) < 2e12 and all(p.kind in ("dense", "paged", "paged_fp8") for p in parts):
-        # the whole step takes seconds on the host cores
-        est = oracle_whole(parts)
-        desc = "the whole step (%s), every row, once" % " + ".join(p.name for p in parts)
-    else:
-        est, desc = oracle_sample(parts, args.cpu_rows, args.cpu_requests)
-        desc = "sample scaled to the whole step: " + desc
-    return dict(value=100.0 * ideal / est, unit=UNIT, cores=oracle.max_threads(), kind="oracle", sample=desc,
-                step_s=est)
+    ideal, secs, recs = oracle_sample(parts, peaks, args.cpu_frac, seed=1)
+    line = dict(value=100.0 * ideal / secs, unit=UNIT, cores=oracle.max_threads(), kind="oracle",
+                sample="%.2f%% of each workload's rows or K/V bytes, drawn at random: %s" % (
+                    100 * args.cpu_frac, "; ".join("%s %s" % (n, r["sample"]) for n, r in recs.items())),
+                seconds=secs, step_s_est=secs * sum(p.ideal_s(peaks) for p in parts) / ideal, parts=recs)
+    # one core against all cores on the same small sample of one prefill
+    pf = [p for p in parts if p.kind == "dense" and p.flops > 1e9]
+    if pf:
+        p = pf[0]
+        unit, units, flops, _ = _draw_sample(p, args.cpu_frac / 8, torch.Generator().manual_seed(2))
+        t_all = _run_sample(p, unit, units, 0)
+        t_one = _run_sample(p, unit, units, 1)
+        line["one_core"] = dict(part=p.name, sample="%d %s" % (len(units), unit), gflop=flops / 1e9,
+                                seconds_1_core=t_one, seconds_all_cores=t_all,
+                                gflops_per_s_1_core=flops / t_one / 1e9, speedup=t_one / t_all)
+    return line
 
 
 def bench_reference(args, world, rank):
-    """The FP64 oracle as the reference arm: each step times a bounded sample of
-    the workload on the host cores and scales it to the whole step."""
+    """The FP64 oracle as the reference arm: each step times the oracle on a
+    bounded random sample of the step's work (a fresh draw per step); the
+    value is the sample's ideal time over the oracle's measured time, and
+    ms_per_step is that measured time."""
     if rank != 0:
         return None
     import oracle
     peaks = load_peaks()
     parts = make_parts(args.workload)
-    for _ in range(args.warmup):
-        oracle_sample(parts, 16, 1, seed=1000)
-    ests = []
-    descs = []
+    for w in range(args.warmup):
+        oracle_sample(parts, peaks, args.ref_frac / 8, seed=1000 + w)
+    ideals, secs, descs = [], [], None
     for s in range(args.steps):
-        est, desc = oracle_sample(parts, args.ref_rows, 1, seed=s)
-        ests.append(est)
-        descs.append(desc)
-    est = statistics.mean(ests)
-    ideal = sum(p.ideal_s(peaks) for p in parts)
-    value = 100.0 * ideal / est
+        i, t, recs = oracle_sample(parts, peaks, args.ref_frac, seed=s)
+        ideals.append(i)
+        secs.append(t)
+        descs = descs or recs
+    value = 100.0 * sum(ideals) / sum(secs)
+    ms = 1e3 * statistics.mean(secs)
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * est, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "serving step: qwen3_8b_prefill + paged_decode" if args.workload == "step"
-                   else args.workload, "parts": {p.name: p.data["config"] for p in parts}},
+        "config": {"workload": workload_label(args.workload), "parts": {p.name: p.data["config"] for p in parts}},
         "cpu_baseline": dict(kind="oracle", cores=oracle.max_threads(), value=value, unit=UNIT,
-                             sample="per step: " + descs[0]),
+                             sample="per step, a fresh random draw of %.2f%% of each workload's rows or K/V "
+                                    "bytes (first step: %s)" % (100 * args.ref_frac, "; ".join(
+                                        "%s %s" % (n, r["sample"]) for n, r in descs.items()))),
         "e2e": dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0),
         "gpu_launches": 0,
     }
@@ -631,20 +792,21 @@ def bench_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="step", choices=["step"] + sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="step", choices=sorted(STEPS) + sorted(W.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-rows", type=int, default=4096)
-    ap.add_argument("--cpu-requests", type=int, default=8)
-    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--cpu-frac", type=float, default=0.02,
+                    help="share of each workload the cpu_baseline times on the oracle")
+    ap.add_argument("--ref-frac", type=float, default=0.004,
+                    help="share of each workload one reference-arm step times on the oracle")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B of a single named workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.batch is not None and args.workload == "step":
+    if args.batch is not None and args.workload in STEPS:
         ap.error("--batch applies to a single named workload")
     world, rank, local = dist_env()
     if world > 1:

@@ -88,3 +88,51 @@ def test_fp8_inputs_are_e4m3_with_scales_in_range():
     # the same seed draws the same bytes and scales
     e = W.paged_fp8_inputs(4, 2, 8, 2, 128, 16, lengths=(1, 300), seed=3, scale_range=(0.25, 1.0))
     assert torch.equal(codes, e["k_cache"].view(torch.uint8)) and torch.equal(d["v_scale"], e["v_scale"])
+
+
+def _part(kind, gen, cfg):
+    d = gen(**cfg)
+    d["config"] = dict(cfg, kind=kind)
+    return bench.Part("probe", d)
+
+
+def test_oracle_sample_of_a_dense_part_counts_its_rows_flops():
+    from gqa_softmax_attention_gb300 import workloads as W
+    cfg = dict(B=2, Hq=4, Hkv=2, Sq=40, Skv=70, D=64, causal=True, sigma=1.0, mask_lengths=(30, 70), seed=5)
+    p = _part("dense", W.dense_inputs, cfg)
+    unit, rows, flops, nbytes = bench._draw_sample(p, 0.25, torch.Generator().manual_seed(0))
+    assert unit == "rows" and len(rows) == 80 and nbytes == 0.0
+    m = p.data["key_padding_mask"]
+    pairs = sum(1 for b, i, _h in rows for j in range(70) if j <= i + 70 - 40 and m[b, j])
+    assert flops == 4.0 * 64 * pairs
+    assert bench._run_sample(p, unit, rows) >= 0.0
+
+
+def test_decode_sample_units_reproduce_the_full_call():
+    # the compact call built from sampled (request, query head) pairs gives the
+    # oracle's own rows of the full paged call, bit for bit
+    import oracle
+    from gqa_softmax_attention_gb300 import workloads as W
+    for kind, gen in (("paged", W.paged_inputs), ("paged_fp8", W.paged_fp8_inputs)):
+        cfg = dict(B=4, Sq=3, Hq=6, Hkv=2, D=64, page_size=8, lengths=[19, 0, 2, 33], seed=7)
+        if kind == "paged_fp8":
+            cfg["scale_range"] = (0.25, 1.0)
+        p = _part(kind, gen, cfg)
+        d = p.data
+        unit, units, flops, nbytes = bench._draw_sample(p, 0.5, torch.Generator().manual_seed(1))
+        assert flops == 0.0 and len(units) >= 1
+        elem = 1 if kind == "paged_fp8" else 2
+        want = sum(d["real_seqlen_kv"][b].item() * 2 * 64 * elem / 3 for b, _h in units)
+        assert nbytes == pytest.approx(want)
+        u = bench._decode_units(p, units)
+        if kind == "paged":
+            full = oracle.attn_paged(d["q"], d["k_cache"], d["v_cache"], d["real_seqlen_kv"], d["block_table"])
+            part = oracle.attn_paged(u["q"], u["k_cache"], u["v_cache"], u["real_seqlen_kv"], u["block_table"])
+        else:
+            full = oracle.attn_paged_fp8kv(d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
+                                           d["real_seqlen_kv"], d["block_table"])
+            part = oracle.attn_paged_fp8kv(u["q"], u["k_cache"], u["v_cache"], u["k_scale"], u["v_scale"],
+                                           u["real_seqlen_kv"], u["block_table"])
+        for i, (b, h) in enumerate(units):
+            assert torch.equal(part[0][i, :, 0], full[0][b, :, h])
+            assert torch.equal(part[1][i, :, 0], full[1][b, :, h])
