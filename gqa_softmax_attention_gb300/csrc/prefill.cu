@@ -27,11 +27,14 @@
 // first 64 columns of S_k.
 //
 // The O rescale is lazy: the reference max of a row only moves when the tile
-// max exceeds it by more than kRescaleThreshold (log2 units), so P stays below
-// 2^threshold and most tiles touch no O at all.  The result is exact: O and l
-// are accumulated against the same reference max.  A rescale of O_k before PV
-// of tile i needs PV of tile i-1 complete; that is implied by S_k of tile i
-// having landed, since its commit follows that PV in the MMA thread's order.
+// max exceeds it by more than kRescaleThreshold (log2 units), so most tiles
+// touch no O at all.  Once every row of a warp has a reference, a tile is
+// exponentiated against it without taking its row max; only a row sum above
+// kSumLimit (2^32) sends the warp back to the scores in TMEM for the max.  The
+// result is exact either way: O and l are accumulated against the same
+// reference.  A rescale of O_k before PV of tile i needs PV of tile i-1
+// complete; that is implied by S_k of tile i having landed, since its commit
+// follows that PV in the MMA thread's order.
 //
 // Key tiles holding no visible key (beyond the causal bound or fully padded)
 // are never loaded, and tiles past Q0's causal bound are skipped for Q0.
@@ -581,20 +584,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tmem_ld128(tmem + lane_addr + col_s, sr);
                 float* s = reinterpret_cast<float*>(sr);
 
-                // Row max over 8 independent chains (short dependency chains).
-                // Fast path (no mask in this tile, positive scale, no cap): the max
-                // is taken on raw scores and the scale is folded into the exp2
-                // argument; otherwise scores become logits (log2 units, capped
-                // when a softcap is set) and masked ones -inf.
+                // Scores to exp2 arguments.  Fast path (no mask in this tile,
+                // positive scale, no cap): raw scores, the scale folded into the
+                // exp2 argument; otherwise scores become logits (log2 units,
+                // capped when a softcap is set) and masked ones -inf.
                 const bool capped = cap_out != 0.f;
                 const bool fast = !need_mask && sl > 0.f && !capped;
-                float mx8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-                if (fast) {
-#pragma unroll
-                    for (int c = 0; c < BN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
-                } else {
+                auto to_logits = [&]() {
+                    if (fast) return;
                     uint32_t vis[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -607,38 +604,57 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                     if (capped) {
 #pragma unroll
-                        for (int c = 0; c < BN; ++c) {
-                            const float x = ((vis[c / 32] >> (c % 32)) & 1u)
-                                                ? softcap_log2(s[c], cap_in, cap_out) : -INFINITY;
-                            s[c] = x;
-                            mx8[c & 7] = fmaxf(mx8[c & 7], x);
-                        }
+                        for (int c = 0; c < BN; ++c)
+                            s[c] = ((vis[c / 32] >> (c % 32)) & 1u) ? softcap_log2(s[c], cap_in, cap_out) : -INFINITY;
                     } else {
 #pragma unroll
-                        for (int c = 0; c < BN; ++c) {
-                            const float x = ((vis[c / 32] >> (c % 32)) & 1u) ? s[c] * sl : -INFINITY;
-                            s[c] = x;
-                            mx8[c & 7] = fmaxf(mx8[c & 7], x);
-                        }
+                        for (int c = 0; c < BN; ++c) s[c] = ((vis[c / 32] >> (c % 32)) & 1u) ? s[c] * sl : -INFINITY;
+                    }
+                };
+                to_logits();
+                // exp2 argument: s * fa - m (fa = scale on the fast path, 1 otherwise)
+                const float fa = fast ? sl : 1.f;
+                float alpha = 1.f;
+                float rs = 0.f;
+                // Once every row of the warp has a reference max, the tile is
+                // exponentiated against it directly, with no row max: P and l
+                // stay exact relative to the reference, and fp32 / 16-bit P hold
+                // values up to the row-sum limit.  A row whose sum passes the
+                // limit (or is not finite) sends the warp to the path below.
+                bool done = false;
+                if (__all_sync(0xffffffffu, m_ref != -INFINITY)) {
+                    uint32_t pk[BN / 2];
+                    rs = exp_row<F16>(s, fa, m_ref, pk);
+                    if (!__any_sync(0xffffffffu, !(rs <= kSumLimit))) {
+                        tmem_st64(tmem + lane_addr + col_s, pk);   // P over the first 64 columns of S
+                        done = true;
                     }
                 }
+                if (!done) {
+                    // The tile's row max, from the scores still in TMEM (P is not
+                    // written yet), over 8 independent chains; the reference max
+                    // moves only when the tile max exceeds it by more than the
+                    // rescale threshold (lazy rescale).
+                    tmem_ld128(tmem + lane_addr + col_s, sr);
+                    to_logits();
+                    float mx8[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + 4]);
-                const float mx_raw = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
-                const float mx = fast ? mx_raw * sl : mx_raw;          // scaled (log2 units)
-                // Lazy rescale: move the reference max only when the tile max
-                // exceeds it by more than the threshold.
-                float alpha = 1.f;
-                if (mx > m_ref + kRescaleThreshold) {
-                    alpha = fast_exp2(m_ref - mx);                  // 0 when m_ref is -inf
-                    m_ref = mx;
+                    for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < BN; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], s[c], s[c + 1]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + 4]);
+                    const float mx_raw = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+                    const float mx = fast ? mx_raw * sl : mx_raw;      // scaled (log2 units)
+                    if (mx > m_ref + kRescaleThreshold) {
+                        alpha = fast_exp2(m_ref - mx);              // 0 when m_ref is -inf
+                        m_ref = mx;
+                    }
+                    const float m_use = m_ref == -INFINITY ? 0.f : m_ref;   // no -inf - -inf
+                    uint32_t pk[BN / 2];
+                    rs = exp_row<F16>(s, fa, m_use, pk);
+                    tmem_st64(tmem + lane_addr + col_s, pk);       // P over the first 64 columns of S
                 }
-                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;   // no -inf - -inf
-                // exp2 argument: s * fa - m_use (fa = scale on the fast path, 1 otherwise)
-                const float fa = fast ? sl : 1.f;
-                uint32_t pk[BN / 2];
-                const float rs = exp_row<F16>(s, fa, m_use, pk);
-                tmem_st64(tmem + lane_addr + col_s, pk);          // P over the first 64 columns of S
                 l_run = l_run * alpha + rs;
 
                 // PV of the previous tile is complete (S of this tile landed after

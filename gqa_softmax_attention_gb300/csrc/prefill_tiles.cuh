@@ -13,6 +13,10 @@ constexpr int BM = 128;            // query rows per Q tile (= TMEM lanes)
 constexpr int BN = 128;            // keys per tile
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P <= 256 between rescales
+// Row-sum limit of a tile exponentiated against a stale reference max (no
+// row max taken): 2^32.  A row's sum stays below tiles x 2^32, far from the
+// fp32 range, and its P values below 2^32 (16-bit P holds them).
+constexpr float kSumLimit = 4294967296.f;
 
 struct TileInfo {
     int q0;          // first query row of the tile
