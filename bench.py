@@ -121,13 +121,14 @@ def load_peaks():
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
 # kernel, taken once with ncu on the kernel as it stands: for the decode
 # workloads as a ratio to the algorithmic K/V bytes (their captures ran at a
-# reduced batch), for the prefill as bytes per launch of the same workload.
-# A workload whose dominant kernel changed after its capture has no entry (its
-# traffic is reported as null until it is captured again): qwen3_8b_prefill and
-# long_chunked_prefill (prefill_kernel, epilogue store wait moved) and
-# wide_group_decode (decode_tc_kernel, shared with the e4m3 route since).
+# reduced batch), for the prefill as bytes per launch of the same workload
+# (long_chunked_prefill captured at B=1 of its four independent batches and
+# scaled by 4).
 TRAFFIC = {
+    "qwen3_8b_prefill": ("bytes", (93.504512 + 30.836480) * 1e6),
+    "long_chunked_prefill": ("bytes", 4 * (534.100480 + 31.266816) * 1e6),
     "paged_decode": ("ratio", (559.379712 + 6.031616) / 556.916736),
+    "wide_group_decode": ("ratio", (233.683200 + 3.794688) / 232.683520),
     "paged_decode_fp8kv": ("ratio", (279.805952 + 5.622016) / 278.458368),
     "wide_group_decode_fp8kv": ("ratio", (117.060352 + 3.536896) / 116.341760),
     "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
@@ -137,10 +138,14 @@ TRAFFIC = {
 
 
 def traffic_per_launch(part):
+    """DRAM bytes per launch from TRAFFIC; a fixed byte count holds only at the
+    workload's own batch size."""
     t = TRAFFIC.get(part.name)
     if t is None:
         return None
-    return t[1] * part.bytes if t[0] == "ratio" else t[1]
+    if t[0] == "ratio":
+        return t[1] * part.bytes
+    return t[1] if part.data["config"].get("B") == W.WORKLOADS[part.name].get("B") else None
 
 
 class Part:

@@ -71,7 +71,6 @@ cudaError_t launch_varlen_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_k
                                 const CUtensorMap& tm_o, const PrefillArgs& a, long max_items, cudaStream_t stream);
 int varlen_packed_take_device_error();
 int varlen_paged_take_device_error();
-// y[i] = 2^x[i] by the prefill kernel's FMA-pipe exp2 (diagnostic).
 
 struct DecodeArgs {
     const void* q;          // [B, Sq, Hq, D]
