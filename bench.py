@@ -132,7 +132,6 @@ TRAFFIC = {
     "paged_decode_fp8kv": ("ratio", (279.805952 + 5.622016) / 278.458368),
     "wide_group_decode_fp8kv": ("ratio", (117.060352 + 3.536896) / 116.341760),
     "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
-    "mixed_serving_batch": ("bytes", (2583.485 + 24.447744) * 1e6),
     "varlen_prefill": ("bytes", (6572.479 + 507.1168) * 1e6),
 }
 
@@ -182,7 +181,11 @@ class Part:
                 names = ("q", "k_cache", "v_cache", "cu_seqlens_q", "cache_seqlens", "block_table")
             self.dev = {n: d[n].to(dev) for n in names}
             tq = d["q"].shape[0]
-            need = g.attn_varlen_workspace_size(len(d["cu_seqlens_q"]) - 1, tq, c["Hq"], c["Hkv"])
+            if self.kind == "varlen":
+                need = g.attn_varlen_workspace_size(len(d["cu_seqlens_q"]) - 1, tq, c["Hq"], c["Hkv"])
+            else:
+                need = g.attn_paged_workspace_size(len(d["cu_seqlens_q"]) - 1, tq, c["Hq"], c["Hkv"], c["D"],
+                                                   c["page_size"], d["block_table"].shape[1])
             self.dev["ws"] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
             self.dev["o"] = torch.empty_like(self.dev["q"])
             self.dev["lse"] = torch.empty((tq, c["Hq"]), dtype=torch.float32, device=dev)
@@ -206,8 +209,18 @@ class Part:
             self.dev["o"] = torch.empty_like(self.dev["q"])
             self.dev["lse"] = torch.empty((c["B"], c["Sq"], c["Hq"]), dtype=torch.float32, device=dev)
 
+    def _routes_decode(self):
+        """A mixed paged call whose one-query requests run on the split decode
+        kernel (KV groups of fewer than 32 query heads)."""
+        c = self.data["config"]
+        return self.kind == "paged_varlen" and c["Hq"] // c["Hkv"] < 32
+
     def launches(self):
-        return 1 if self.kind == "dense" else 2           # packed calls: plan + attention; decode: split + combine
+        # dense: one; packed: plan + attention (+ split decode + combine for a
+        # mixed paged call); decode: split + combine
+        if self.kind == "dense":
+            return 1
+        return 4 if self._routes_decode() else 2
 
     def bound(self, peaks):
         """"tensor" or "hbm": the larger of the FLOP and byte terms."""
@@ -221,7 +234,11 @@ class Part:
         if self.kind == "varlen":
             return "onetile_kernel<%d,kPacked> + varlen_plan_kernel" % c["D"]
         if self.kind == "paged_varlen":
-            return "onetile_kernel<%d,kPaged> + varlen_plan_kernel" % c["D"]
+            name = "onetile_kernel<%d,kPaged> + varlen_plan_kernel" % c["D"]
+            if self._routes_decode():
+                mf = min(4, (c["Hq"] // c["Hkv"] + 15) // 16)
+                name = "decode_tma_kernel<%d,%d> + decode_combine_kernel<%d> + " % (c["D"], mf, c["D"]) + name
+            return name
         rows = c["Hq"] // c["Hkv"] * c["Sq"]
         tc = c["D"] in (128, 256) and 32 <= rows <= 128 and c["page_size"] % 8 == 0 and (
             c["page_size"] >= 64 or 64 % c["page_size"] == 0)

@@ -11,5 +11,6 @@ is an error: there is no CPU fallback.
 
 from .api import (attention, attn_decode_paged, attn_decode_paged_fp8kv, attn_decode_paged_noalloc,  # noqa: F401
                   attn_decode_paged_workspace_size, attn_fwd_paged, attn_fwd_varlen,
-                  attn_fwd_dense, attn_validate_paged, attn_varlen_workspace_size, decode_paged,
+                  attn_fwd_dense, attn_paged_workspace_size, attn_validate_paged, attn_varlen_workspace_size,
+                  decode_paged,
                   gqa_device_error, paged, resolve_scale, varlen)

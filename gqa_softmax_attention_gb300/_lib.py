@@ -59,6 +59,8 @@ def load() -> ctypes.CDLL:
     lib.attn_fwd_paged.restype = i
     lib.attn_varlen_workspace_size.argtypes = [i] * 4
     lib.attn_varlen_workspace_size.restype = sz
+    lib.attn_paged_workspace_size.argtypes = [i] * 7
+    lib.attn_paged_workspace_size.restype = sz
     lib.attn_validate_paged.argtypes = [vp, vp] + [i] * 6 + [vp]
     lib.attn_validate_paged.restype = i
     lib.gqa_status_string.argtypes = [i]

@@ -278,6 +278,13 @@ def attn_varlen_workspace_size(B, total_q, Hq, Hkv):
     return int(_lib.load().attn_varlen_workspace_size(B, total_q, Hq, Hkv))
 
 
+def attn_paged_workspace_size(B, total_q, Hq, Hkv, D, page_size, max_pages):
+    """Workspace bytes of attn_fwd_paged with its single-query requests on the
+    split-KV decode kernel (equal to attn_varlen_workspace_size when the sizes
+    keep every request on the packed kernel)."""
+    return int(_lib.load().attn_paged_workspace_size(B, total_q, Hq, Hkv, D, page_size, max_pages))
+
+
 def _check_offsets(name, t, n):
     if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32 or tuple(t.shape) != (n,):
         raise ValueError("%s must be an int32 CUDA tensor of shape [%d]" % (name, n))
@@ -332,14 +339,18 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, causal=True, scale=Non
 
 
 def attn_fwd_paged(q, k_cache, v_cache, cu_seqlens_q, cache_seqlens, block_table, causal=True, scale=None,
-                   out=None, lse=None, window_left=-1, window_right=-1, softcap=None, sinks=None, workspace=None):
+                   out=None, lse=None, window_left=-1, window_right=-1, softcap=None, sinks=None, workspace=None,
+                   split_decode=True):
     """Packed queries over a paged cache: prefill chunks and decode steps in one
-    launch (TileOPs GQAPagedFwdOp).
+    call (TileOPs GQAPagedFwdOp).
 
     q [total_q, Hq, D]; k_cache / v_cache [num_pages, page_size, Hkv, D], all
     bfloat16 or all float16; cu_seqlens_q [B + 1], cache_seqlens [B] (query
     tokens included) and block_table [B, max_pages] int32 CUDA tensors.
     page_size must be a multiple of 8.  Options as in attn_fwd_dense.
+    split_decode: give the call the workspace that sends requests with one
+    query to the split-KV decode kernel (False: every request on the packed
+    kernel).  A caller's workspace decides by its size instead.
     Returns (o [total_q, Hq, D], lse [total_q, Hq]).
     """
     _check_16_cuda("q", q, 3)
@@ -362,7 +373,10 @@ def attn_fwd_paged(q, k_cache, v_cache, cu_seqlens_q, cache_seqlens, block_table
     bt = block_table.contiguous()
     q, k_cache, v_cache = q.contiguous(), k_cache.contiguous(), v_cache.contiguous()
     out, lse = _varlen_outputs(q, out, lse, workspace, B)
-    need = attn_varlen_workspace_size(B, total_q, Hq, Hkv)
+    if split_decode:
+        need = attn_paged_workspace_size(B, total_q, Hq, Hkv, D, page_size, bt.shape[1])
+    else:
+        need = attn_varlen_workspace_size(B, total_q, Hq, Hkv)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     opt, _keep = _options(window_left, window_right, softcap, sinks, Hq, q.device, _DTYPES[q.dtype])

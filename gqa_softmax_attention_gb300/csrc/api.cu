@@ -410,6 +410,22 @@ size_t attn_varlen_workspace_size(int B, int total_q, int Hq, int Hkv) {
     return varlen_ws_bytes(B, total_q, Hq, Hkv);
 }
 
+// Split-decode plan for the single-query requests of a paged call (B requests
+// of one query each); false when the sizes leave them on the one-tile kernel
+// (KV groups of 32 rows or more, whose decode runs on the tensor-core kernel).
+static bool paged_decode_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages, DecodePlan* p) {
+    if (!head_dim_ok(D) || page_size <= 0 || max_pages <= 0) return false;
+    if (!gqa::plan_decode(B, 1, Hq, Hkv, D, page_size, max_pages, sm_count(), p)) return false;
+    return !p->tc;
+}
+
+size_t attn_paged_workspace_size(int B, int total_q, int Hq, int Hkv, int D, int page_size, int max_pages) {
+    const size_t v = varlen_ws_bytes(B, total_q, Hq, Hkv);
+    DecodePlan p;
+    if (v == 0 || !paged_decode_plan(B, Hq, Hkv, D, page_size, max_pages, &p)) return v;
+    return (v + 255) / 256 * 256 + p.workspace_bytes;
+}
+
 // Shared checks and set-up of the two packed entry points.
 static gqa_status varlen_common(const void* q, void* o, float* lse, const int32_t* cu_q, int B, int total_q,
                                 int Hq, int Hkv, int D, int causal, float scale, const gqa_options* opts,
@@ -511,10 +527,44 @@ gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cach
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int max_e = varlen_max_entries(B, total_q, a.qpb);
     int32_t* ws = static_cast<int32_t*>(workspace);
+    // Requests with exactly one query (decode steps) run on the split decode
+    // kernel when the workspace also holds its partials: there all g heads of a
+    // KV group share one MMA fragment and the keys stream at memory speed,
+    // instead of g rows taking a 128-row tensor-core tile.  The prefill chunks
+    // stay on the one-tile kernel; the two launches write disjoint rows.
+    DecodePlan dp;
+    char* wsc = static_cast<char*>(workspace);
+    const size_t d_off = (varlen_ws_bytes(B, total_q, Hq, Hkv) + 255) / 256 * 256;
+    const bool route = paged_decode_plan(B, Hq, Hkv, D, page_size, max_pages, &dp) &&
+                       workspace_bytes >= d_off + dp.workspace_bytes &&
+                       (reinterpret_cast<uintptr_t>(wsc + d_off) & 255u) == 0;
     if (gqa::launch_varlen_plan(cu_seqlens_q, cache_seqlens, true, B, a.qpb, a.g, a.causal, total_q,
                                 (long)max_pages * page_size, ws + 4 + (size_t)max_e * 8, ws + 4, ws, max_e,
-                                s) != cudaSuccess)
+                                s, route) != cudaSuccess)
         return GQA_ERR_CUDA;
+    if (route) {
+        DecodeArgs da{};
+        da.q = q; da.k_cache = k_cache; da.v_cache = v_cache;
+        da.seqlens = cache_seqlens; da.table = block_table;
+        da.o = o; da.lse = lse;
+        da.part_o = reinterpret_cast<float*>(wsc + d_off);
+        da.part_lse = reinterpret_cast<float*>(wsc + d_off + (dp.part_o_bytes + 255) / 256 * 256);
+        da.B = B; da.Sq = 1; da.Hq = Hq; da.Hkv = Hkv; da.D = D;
+        da.page_size = page_size; da.max_pages = max_pages; da.num_pages = num_pages; da.causal = a.causal;
+        da.scale_log2 = a.scale_log2;
+        da.chunk = dp.chunk;
+        da.max_splits = dp.max_splits;
+        da.f16 = a.f16;
+        da.x = a.x;
+        da.q_rows = cu_seqlens_q;
+        da.q_total = total_q;
+        const int box = gqa::decode_box_tokens(D, page_size);
+        CUtensorMap dk, dv;
+        const bool use_tma = box > 0 && make_cache_map(&dk, k_cache, rows, Hkv, D, box, a.f16) &&
+                             make_cache_map(&dv, v_cache, rows, Hkv, D, box, a.f16);
+        if (gqa::launch_decode(da, use_tma ? &dk : nullptr, use_tma ? &dv : nullptr, box, s) != cudaSuccess)
+            return GQA_ERR_CUDA;
+    }
     return gqa::launch_varlen_paged(tq, tk, tv, to, a, (long)max_e * Hkv, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 

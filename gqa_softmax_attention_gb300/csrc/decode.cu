@@ -102,7 +102,17 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c, int sub_bytes) {
 
 struct Work {
     int split, hkv, b, rb, L, t_begin, t_end, n_tiles, row0, rows_here;
+    long qrow0;     // row of query 0 of request b in q ([B * Sq] rows, or packed)
 };
+
+// Packed call (a.q_rows set): whether request b has exactly one query row, and
+// that row (offsets clamped into [0, q_total] like the packed plan kernel's).
+__device__ __forceinline__ bool packed_single(const DecodeArgs& a, int b, long& row) {
+    const int qs = min(max(a.q_rows[b], 0), a.q_total);
+    const int qe = min(max(a.q_rows[b + 1], qs), a.q_total);
+    row = qs;
+    return qe - qs == 1;
+}
 
 template <class C>
 __device__ __forceinline__ bool work_of(const DecodeArgs& a, int R, int g, int n_rowblk, Work& w) {
@@ -110,6 +120,8 @@ __device__ __forceinline__ bool work_of(const DecodeArgs& a, int R, int g, int n
     w.hkv = blockIdx.y;
     w.b = blockIdx.z / n_rowblk;
     w.rb = blockIdx.z % n_rowblk;
+    w.qrow0 = (long)w.b * a.Sq;
+    if (a.q_rows && !packed_single(a, w.b, w.qrow0)) return false;   // not a decode step: not ours
     // Lengths are clamped to the table's capacity so a bad length cannot send
     // a load past block_table.
     w.L = min(max(a.seqlens[w.b], 0), a.max_pages * a.page_size);
@@ -193,7 +205,7 @@ struct Consumer {
             if (rr < w.rows_here) {
                 const int r = w.row0 + rr;
                 const int i = r / g, hl = r % g;
-                cp_async16(dst, qg + (((size_t)w.b * a.Sq + i) * a.Hq + w.hkv * g + hl) * (CHUNKS * 8) + c * 8, 16);
+                cp_async16(dst, qg + (((size_t)w.qrow0 + i) * a.Hq + w.hkv * g + hl) * (CHUNKS * 8) + c * 8, 16);
             } else {
                 cp_async16(dst, qg, 0);
             }
@@ -723,7 +735,7 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (a.x.wl >= 0) lo[h] = (int)max(0L, min((long)w.L, p - a.x.wl));
             }
             const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.q) +
-                                   (((size_t)w.b * a.Sq + r / g) * a.Hq + w.hkv * g + r % g) * D;
+                                   (((size_t)w.qrow0 + r / g) * a.Hq + w.hkv * g + r % g) * D;
 #pragma unroll
             for (int kk = 0; kk < C::KSTEPS; ++kk) {
                 uint2 v = make_uint2(0u, 0u);
@@ -969,6 +981,12 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
     const int i = (int)((row / a.Hq) % a.Sq);
     const int b = (int)(row / ((long)a.Hq * a.Sq));
     const int hkv = h / g, r = i * g + h % g;
+    long orow = row;        // row of o [.., D] and lse
+    if (a.q_rows) {
+        long qr;
+        if (!packed_single(a, b, qr)) return;       // rows of a prefill chunk are not ours
+        orow = qr * a.Hq + h;
+    }
     const int L = min(max(a.seqlens[b], 0), a.max_pages * a.page_size);
     int n;
     size_t base;
@@ -1002,7 +1020,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o) + (size_t)row * D;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o) + (size_t)orow * D;
     constexpr int PER = D / 128 > 0 ? D / 128 : 1;     // float4 groups per lane
     // A sink joins the denominator once per row (GQAPagedFwdOp sinks): the
     // weights are taken against max(M, s); +inf zeroes the row.  A row no
@@ -1014,7 +1032,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
             const int d = (q * 32 + lane) * 4;
             if (d < D) *reinterpret_cast<uint2*>(out + d) = make_uint2(0u, 0u);
         }
-        if (lane == 0 && a.lse) a.lse[row] = INFINITY;
+        if (lane == 0 && a.lse) a.lse[orow] = INFINITY;
         return;
     }
     M = fmaxf(M, s2);
@@ -1024,7 +1042,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
             const int d = (q * 32 + lane) * 4;
             if (d < D) *reinterpret_cast<uint2*>(out + d) = make_uint2(0u, 0u);
         }
-        if (lane == 0 && a.lse) a.lse[row] = -INFINITY;
+        if (lane == 0 && a.lse) a.lse[orow] = -INFINITY;
         return;
     }
     float accv[PER][4] = {};
@@ -1053,7 +1071,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a,
                 make_uint2(pack2<F16>(accv[q][0] * inv, accv[q][1] * inv),
                            pack2<F16>(accv[q][2] * inv, accv[q][3] * inv));
     }
-    if (lane == 0 && a.lse) a.lse[row] = (M + log2f(den)) * kLn2;
+    if (lane == 0 && a.lse) a.lse[orow] = (M + log2f(den)) * kLn2;
 }
 
 int choose_mf(int R) {

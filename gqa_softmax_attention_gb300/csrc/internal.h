@@ -57,9 +57,11 @@ int prefill_d256_take_device_error();
 // heaviest first, and their count into *n_entries; kv holds cu_seqlens_kv
 // [B + 1] (packed keys) or cache_seqlens [B] (paged), and kv_cap bounds a
 // request's key count (total_kv, or max_pages * page_size).
+// skip_single leaves requests with exactly one query out of the list (they
+// run on the split decode kernel instead).
 cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int g, int causal,
                                int total_q, long kv_cap, int32_t* tmp, int32_t* entries, int32_t* n_entries,
-                               int max_entries, cudaStream_t stream);
+                               int max_entries, cudaStream_t stream, bool skip_single = false);
 // tm_q / tm_o: {D, Hq, total_q} with a {64, g, qpb} box.  Packed: tm_k / tm_v
 // {D, Hkv, total_kv} with {64, 1, 128} and {64, 1, 128 or 64 (D = 256)} boxes.
 // Paged: the caches as {64, 8, D / 64, pages * page_size / 8, Hkv} with
@@ -98,6 +100,14 @@ struct DecodeArgs {
     // dequantization scales [B, Hkv], nullptr meaning 1
     const float* k_scale;
     const float* v_scale;
+    // Packed queries (the single-query requests of attn_fwd_paged; split
+    // kernels only): q_rows = cu_seqlens_q [B + 1] over q / o [q_total, Hq, D]
+    // and lse [q_total, Hq]; with Sq = 1, request b takes part only when it
+    // has exactly one query row, at row q_rows[b] (offsets clamped into
+    // [0, q_total] as by the packed plan kernel).  nullptr: q, o and lse are
+    // [B, Sq, Hq, ...].
+    const int32_t* q_rows;
+    int q_total;
 };
 
 struct DecodePlan {

@@ -46,13 +46,14 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
         if (b < B) {
             qs = min(max(cu_q[b], 0), total_q);
             sq = min(max(cu_q[b + 1], qs), total_q) - qs;
-            if (paged) {
+            if (paged & 1) {
                 L = (int)min((long)max(kv[b], 0), kv_cap);
             } else {
                 ks = (int)min((long)max(kv[b], 0), kv_cap);
                 L = (int)min((long)max(kv[b + 1], ks), kv_cap) - ks;
             }
             nrb = (sq + qpb - 1) / qpb;
+            if ((paged & 2) && sq == 1) nrb = 0;      // a decode step, run by the split decode kernel
         }
         int x = nrb;                                   // inclusive scan within the warp
 #pragma unroll
@@ -136,8 +137,10 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
 
 cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int g, int causal,
                                int total_q, long kv_cap, int32_t* tmp, int32_t* entries, int32_t* n_entries,
-                               int max_entries, cudaStream_t stream) {
-    varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_q, kv, paged ? 1 : 0, B, qpb, g, causal, total_q, kv_cap, tmp,
+                               int max_entries, cudaStream_t stream, bool skip_single) {
+    // flags: bit 0 paged (kv holds cache lengths), bit 1 skip single-query requests
+    const int flags = (paged ? 1 : 0) | (skip_single ? 2 : 0);
+    varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_q, kv, flags, B, qpb, g, causal, total_q, kv_cap, tmp,
                                                entries, n_entries, max_entries);
     return cudaGetLastError();
 }

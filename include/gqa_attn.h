@@ -292,8 +292,17 @@ gqa_status attn_fwd_varlen(const void* q, const void* k, const void* v,
  *                     position i + L_b - Sq_b
  *   block_table       [B, max_pages] int32, as for attn_decode_paged
  *   o    [total_q, Hq, D] (written); lse [total_q, Hq] float or NULL
- *   workspace         attn_varlen_workspace_size(B, total_q, Hq, Hkv) bytes,
- *                     16-byte aligned
+ *   workspace         at least attn_varlen_workspace_size(B, total_q, Hq, Hkv)
+ *                     bytes, 16-byte aligned.  With
+ *                     attn_paged_workspace_size(B, total_q, Hq, Hkv, D,
+ *                     page_size, max_pages) bytes, 256-byte aligned, the
+ *                     requests with exactly one query (decode steps) run on
+ *                     the split-KV decode kernel of attn_decode_paged (where
+ *                     Hq / Hkv < 32) and the rest on the packed kernel, in
+ *                     two launches on `stream`; with less, every request runs
+ *                     on the packed kernel.  Results agree within the usual
+ *                     tolerance either way.  Calls sharing a workspace must
+ *                     not overlap on the GPU.
  *
  * page_size must be a multiple of 8 (GQA_ERR_UNSUPPORTED otherwise; pages
  * move as 8-row TMA blocks) and num_pages >= 1.  Caller obligations on the
@@ -311,6 +320,15 @@ gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cach
 
 /* Workspace bytes of attn_fwd_varlen / attn_fwd_paged (0 for invalid sizes). */
 size_t attn_varlen_workspace_size(int B, int total_q, int Hq, int Hkv);
+
+/*
+ * Workspace bytes of attn_fwd_paged with its single-query requests on the
+ * split-KV decode kernel: the packed plan's bytes, then, from a 256-byte
+ * boundary, the split partials of B one-query requests (attn_decode_paged's
+ * workspace for Sq = 1).  Equals attn_varlen_workspace_size when the sizes
+ * keep every request on the packed kernel; 0 for invalid sizes.
+ */
+size_t attn_paged_workspace_size(int B, int total_q, int Hq, int Hkv, int D, int page_size, int max_pages);
 
 /*
  * Optional host-side check of the paged metadata (the TileOPs

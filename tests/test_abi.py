@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("attn_fwd_dense", "attn_decode_paged", "attn_decode_paged_workspace_size", "attn_validate_paged",
-              "attn_fwd_varlen", "attn_fwd_paged", "attn_varlen_workspace_size", "attn_decode_paged_fp8kv",
+              "attn_fwd_varlen", "attn_fwd_paged", "attn_varlen_workspace_size", "attn_paged_workspace_size",
+              "attn_decode_paged_fp8kv",
               "gqa_status_string", "gqa_device_error", "gqa_version"):
         assert n in names
 
@@ -143,6 +144,19 @@ def test_varlen_argument_checks(lib):
     assert lib.attn_varlen_workspace_size(2, 8, 4, 2) == 16 + 64 * (8 // 64 + 2 + 1)
     assert lib.attn_varlen_workspace_size(3, 1000, 24, 2) == 16 + 64 * (1000 // 10 + 3 + 1)   # g = 12: 10 queries
     assert lib.attn_varlen_workspace_size(2, 8, 6, 4) == 0
+
+
+def test_paged_workspace_holds_the_decode_partials(lib):
+    """attn_fwd_paged's larger workspace: the packed plan's bytes, a 256-byte
+    boundary, then attn_decode_paged's workspace for B one-query requests; the
+    packed size alone when the group is too wide for the split decode kernel."""
+    for B, tq, Hq, Hkv, D, ps, mp in ((64, 4156, 32, 8, 128, 64, 257), (3, 10, 24, 2, 256, 16, 40)):
+        v = lib.attn_varlen_workspace_size(B, tq, Hq, Hkv)
+        d = lib.attn_decode_paged_workspace_size(B, 1, Hq, Hkv, D, ps, mp)
+        assert lib.attn_paged_workspace_size(B, tq, Hq, Hkv, D, ps, mp) == (v + 255) // 256 * 256 + d
+    # 64 query heads per KV head: the decode rows would take the tensor-core kernel
+    assert lib.attn_paged_workspace_size(4, 8, 64, 1, 128, 64, 8) == lib.attn_varlen_workspace_size(4, 8, 64, 1)
+    assert lib.attn_paged_workspace_size(2, 8, 6, 4, 128, 64, 8) == 0
 
 
 def test_workspace_size_is_positive_and_monotone(lib):

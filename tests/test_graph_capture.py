@@ -50,13 +50,20 @@ def test_paged_decode_graph_replay(g):
         compare(out.cpu(), lse.cpu(), ro, rl, "decode replay")
 
 
-def test_mixed_paged_graph_replay(g):
+@pytest.mark.parametrize("split_decode", [False, True], ids=["packed_only", "split_decode"])
+def test_mixed_paged_graph_replay(g, split_decode):
+    """A mixed call replays with new cache lengths and a new query split; with
+    the larger workspace its one-query requests (which change between
+    replays) run on the split decode kernel."""
     ql, L = [1, 300, 1, 4], [2000, 700, 50, 1000]
     Hq, Hkv, D, ps = 8, 2, 128, 16
     p = W.varlen_paged_inputs(ql, L, Hq, Hkv, D, ps, seed=4)
     names = ("q", "k_cache", "v_cache", "cu_seqlens_q", "cache_seqlens", "block_table")
     dev = {n: p[n].cuda() for n in names}
-    ws = torch.empty(g.attn_varlen_workspace_size(len(ql), p["q"].shape[0], Hq, Hkv), dtype=torch.uint8, device="cuda")
+    tq = p["q"].shape[0]
+    size = (g.attn_paged_workspace_size(len(ql), tq, Hq, Hkv, D, ps, p["block_table"].shape[1]) if split_decode
+            else g.attn_varlen_workspace_size(len(ql), tq, Hq, Hkv))
+    ws = torch.empty(size, dtype=torch.uint8, device="cuda")
     out = torch.empty_like(dev["q"])
     lse = torch.empty((p["q"].shape[0], Hq), dtype=torch.float32, device="cuda")
     run = lambda: g.paged(*[dev[n] for n in names], causal=True, out=out, lse=lse, workspace=ws)

@@ -107,31 +107,37 @@ PAGED = [
     ([3, 100, 1], [77, 100, 1000], 4, 2, 64, 8),
     ([1, 40, 2], [500, 300, 2], 8, 2, 128, 24),                            # 24-token pages: 8-token blocks
     ([5, 1, 130], [900, 600, 130], 16, 2, 256, 256),                       # pages larger than a key tile
+    ([1, 1, 20, 1], [0, 700, 40, 1], 8, 2, 128, 16),                       # a decode step with an empty cache
 ]
 
 
+@pytest.mark.parametrize("split_decode", [True, False], ids=["split_decode", "packed_only"])
 @pytest.mark.parametrize("case", PAGED, ids=[str(c[:2]) + "/ps%d" % c[5] for c in PAGED])
-def test_paged(g, case):
+def test_paged(g, case, split_decode):
+    """With the larger workspace the one-query requests run on the split decode
+    kernel and the rest on the packed kernel; with the packed workspace every
+    request runs on the packed kernel.  Both against the oracle."""
     ql, L, Hq, Hkv, D, ps = case
     p = W.varlen_paged_inputs(ql, L, Hq, Hkv, D, ps, seed=sum(L) % 97)
     kc, vc = poison(p)
     o, lse = g.paged(p["q"].cuda(), kc.cuda(), vc.cuda(), p["cu_seqlens_q"].cuda(), p["cache_seqlens"].cuda(),
-                     p["block_table"].cuda(), causal=True)
+                     p["block_table"].cuda(), causal=True, split_decode=split_decode)
     torch.cuda.synchronize()
     ro, rl = oracle.attn_paged_varlen(p["q"], p["k_cache"], p["v_cache"], p["cu_seqlens_q"], p["cache_seqlens"],
                                       p["block_table"], causal=True)
     check(o, lse, ro, rl, str(case))
 
 
-def test_paged_options_float16(g):
-    ql, L, Hq, Hkv, D, ps = [1, 200, 4], [2000, 450, 40], 24, 2, 256, 32
+@pytest.mark.parametrize("split_decode", [True, False], ids=["split_decode", "packed_only"])
+def test_paged_options_float16(g, split_decode):
+    ql, L, Hq, Hkv, D, ps = [1, 200, 4, 1], [2000, 450, 40, 90], 24, 2, 256, 32
     p = W.varlen_paged_inputs(ql, L, Hq, Hkv, D, ps, seed=5)
     sinks = sinks_for(Hq, 9)
     for dtype in (torch.bfloat16, torch.float16):
         q, kc, vc = (p[n].to(dtype) for n in ("q", "k_cache", "v_cache"))
         kw = dict(window_left=300, softcap=20.0)
         o, lse = g.paged(q.cuda(), kc.cuda(), vc.cuda(), p["cu_seqlens_q"].cuda(), p["cache_seqlens"].cuda(),
-                         p["block_table"].cuda(), causal=True, sinks=sinks.cuda(), **kw)
+                         p["block_table"].cuda(), causal=True, sinks=sinks.cuda(), split_decode=split_decode, **kw)
         torch.cuda.synchronize()
         assert o.dtype == dtype
         ro, rl = oracle.attn_paged_varlen(q, kc, vc, p["cu_seqlens_q"], p["cache_seqlens"], p["block_table"],
