@@ -12,10 +12,10 @@ namespace {
 // One CTA of 1024 threads.  Request b gets ceil(Sq_b / qpb) entries
 // {b, q0, qs, Sq_b, ks, L_b}.  Offsets are clamped into [0, total] and
 // lengths into [0, kv_cap], so malformed metadata can give wrong results but
-// no access out of range; entries past max_entries are dropped.  The entries
-// are then ordered by estimated cost, heaviest first (a counting sort over
-// NBUCKET cost buckets), so that the persistent grid's snake order hands
-// out long decode streams and late causal blocks before short ones.
+// no access out of range; entries past max_entries are dropped.  The
+// requests are then ordered by estimated cost, heaviest first (a counting
+// sort over NBUCKET cost buckets), each request's blocks together and its
+// heaviest (last) block first.
 constexpr int NBUCKET = 2048;
 
 __device__ __forceinline__ int entry_cost(const int4 e0, const int4 e1, int qpb, int g, int causal) {
@@ -74,22 +74,35 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
         }
         __syncthreads();
         const int first = base + (warp > 0 ? warp_sum[warp - 1] : 0) + x - nrb;
+        // the request's estimated cost: the sum of its blocks' costs
+        int total = 0;
+        for (int k = 0; k < nrb; ++k)
+            total += entry_cost(make_int4(b, k * qpb, qs, sq), make_int4(ks, L, 0, 0), qpb, g, causal);
+        const int key = min(NBUCKET - 1, total / 16);
         for (int k = 0; k < nrb; ++k) {
             const int e = first + k;
             if (e >= max_entries) break;
             int4* dst = reinterpret_cast<int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
             dst[0] = make_int4(b, k * qpb, qs, sq);
-            dst[1] = make_int4(ks, L, 0, 0);
+            dst[1] = make_int4(ks, L, key, 0);             // .w: the request's start once placed
         }
         __syncthreads();
         if (threadIdx.x == 1023) base = first + nrb;
         __syncthreads();
     }
     const int n = min(base, max_entries);
-    // 2. counting sort by cost, heaviest first
+    // 2. requests ordered by estimated cost, heaviest first (a counting sort of
+    // their total costs), each request's blocks kept together and placed from
+    // its last block (the most keys under a causal mask) to its first: the
+    // grid's snake order then works through one request's keys at a time,
+    // which stay in L2 while its blocks need them.  A request's first entry
+    // (q0 = 0) stands for the whole request.
     for (int e = threadIdx.x; e < n; e += 1024) {
         const int4* src = reinterpret_cast<const int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
-        atomicAdd(&bucket[entry_cost(src[0], src[1], qpb, g, causal)], 1);
+        const int4 e0 = src[0], e1 = src[1];
+        // blocks of the request that made the list (all of them unless the
+        // cap cut it short), so that the placed entries fill [0, n)
+        if (e0.y == 0) atomicAdd(&bucket[e1.z], min((e0.w + qpb - 1) / qpb, n - e));
     }
     __syncthreads();
     {
@@ -122,13 +135,24 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
         bucket[c2] = start + n1;
     }
     __syncthreads();
+    // 3. each request reserves its range; then every block takes its place
+    for (int e = threadIdx.x; e < n; e += 1024) {
+        int4* src = reinterpret_cast<int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
+        const int4 e0 = src[0], e1 = src[1];
+        if (e0.y == 0) src[1].w = atomicAdd(&bucket[e1.z], min((e0.w + qpb - 1) / qpb, n - e));
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < n; e += 1024) {
         const int4* src = reinterpret_cast<const int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
         const int4 e0 = src[0], e1 = src[1];
-        const int pos = atomicAdd(&bucket[entry_cost(e0, e1, qpb, g, causal)], 1);
+        const int k = e0.y / qpb;
+        const int cnt = min((e0.w + qpb - 1) / qpb, n - (e - k));
+        const int start = reinterpret_cast<const int4*>(tmp + (size_t)(e - k) * ot::ENTRY_INTS)[1].w;
+        const int pos = start + cnt - 1 - k;
+        if (pos < 0 || pos >= n) continue;
         int4* dst = reinterpret_cast<int4*>(entries + (size_t)pos * ot::ENTRY_INTS);
         dst[0] = e0;
-        dst[1] = e1;
+        dst[1] = make_int4(e1.x, e1.y, 0, 0);
     }
     if (threadIdx.x == 0) *n_entries = n;
 }
