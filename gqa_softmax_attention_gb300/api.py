@@ -347,7 +347,8 @@ def attn_fwd_paged(q, k_cache, v_cache, cu_seqlens_q, cache_seqlens, block_table
     q [total_q, Hq, D]; k_cache / v_cache [num_pages, page_size, Hkv, D], all
     bfloat16 or all float16; cu_seqlens_q [B + 1], cache_seqlens [B] (query
     tokens included) and block_table [B, max_pages] int32 CUDA tensors.
-    page_size must be a multiple of 8.  Options as in attn_fwd_dense.
+    Any page size (multiples of 8 move by TMA, others are gathered row by
+    row).  Options as in attn_fwd_dense.
     split_decode: give the call the workspace that sends requests with one
     query to the split-KV decode kernel (False: every request on the packed
     kernel).  A caller's workspace decides by its size instead.

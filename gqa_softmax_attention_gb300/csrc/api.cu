@@ -506,7 +506,6 @@ gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cach
     if (page_size <= 0 || num_pages <= 0 || max_pages <= 0) return GQA_ERR_INVALID_ARG;
     if ((long)max_pages * page_size >= kMaxSeq) return GQA_ERR_INVALID_ARG;
     if ((long)num_pages * page_size >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
-    if (page_size % 8 != 0) return GQA_ERR_UNSUPPORTED;      // pages move as 8-row TMA blocks
     gqa_status st = varlen_common(q, o, lse, cu_seqlens_q, B, total_q, Hq, Hkv, D, causal, scale, opts, workspace,
                                   workspace_bytes, &a, &tq, &to);
     if (st != GQA_OK) return st;
@@ -518,12 +517,23 @@ gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cach
     a.page_size = page_size;
     a.max_pages = max_pages;
     const int vkeys = D == 256 ? 64 : 128;
-    a.bt_k = gcd_int(page_size, 128);
-    a.bt_v = gcd_int(page_size, vkeys);
     const long rows = (long)num_pages * page_size;
-    if (!make_cache_page_map(&tk, k_cache, rows, Hkv, D, a.bt_k, a.f16, D == 256 ? 2 : D / 64) ||
-        !make_cache_page_map(&tv, v_cache, rows, Hkv, D, a.bt_v, a.f16))
-        return GQA_ERR_CUDA;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.num_pages = num_pages;
+    if (page_size % 8 == 0) {
+        // pages move as 8-row TMA blocks
+        a.bt_k = gcd_int(page_size, 128);
+        a.bt_v = gcd_int(page_size, vkeys);
+        if (!make_cache_page_map(&tk, k_cache, rows, Hkv, D, a.bt_k, a.f16, D == 256 ? 2 : D / 64) ||
+            !make_cache_page_map(&tv, v_cache, rows, Hkv, D, a.bt_v, a.f16))
+            return GQA_ERR_CUDA;
+    } else {
+        // other page sizes: rows gathered with cp.async (the maps go unused)
+        a.bt_k = a.bt_v = 0;
+        tk = tq;
+        tv = tq;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int max_e = varlen_max_entries(B, total_q, a.qpb);
     int32_t* ws = static_cast<int32_t*>(workspace);

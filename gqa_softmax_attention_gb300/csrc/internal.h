@@ -34,7 +34,12 @@ struct PrefillArgs {
     int qpb;                  // queries per row block: floor(128 / g)
     const int32_t* table;     // paged: block_table [B, max_pages]
     int page_size, max_pages;
-    int bt_k, bt_v;           // paged: tokens per TMA box of a K / V chunk
+    int bt_k, bt_v;           // paged: tokens per TMA box of a K / V chunk; 0: rows gathered with cp.async
+    // paged, gathered rows (page sizes that are not a multiple of 8): the
+    // caches [num_pages, page_size, Hkv, D] themselves
+    const void* k_cache;
+    const void* v_cache;
+    int num_pages;
 };
 
 // Launches the tcgen05 prefill kernel.  The tensor maps describe q, k, v as

@@ -269,12 +269,17 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // TMA-tensor layouts: lane 0 alone (it issues every copy).  Paged:
             // warp-collective, every lane learning the slot (lanes copy one
             // page block each).
+            // Paged caches whose page size is not a multiple of 8 are gathered
+            // row by row with cp.async into the same layout the page-block
+            // boxes give; a slot's full barrier then takes lane 0's plain
+            // arrival once that slot's copies have landed.
+            const bool gather = MODE == kPaged && a.bt_k == 0;
             auto take_slot = [&](uint32_t& dst, uint32_t& full, uint32_t bytes) -> bool {
                 const int s = nc % C::NS;
                 bool good = true;
                 if (MODE != kPaged || lane == 0) {
                     good = mbar_wait(r_empty(s), ((nc / C::NS) & 1) ^ 1, abort_flag);
-                    if (good) mbar_arrive_expect_tx(r_full(s), bytes);
+                    if (good && !gather) mbar_arrive_expect_tx(r_full(s), bytes);
                 }
                 if constexpr (MODE == kPaged) {
                     good = __shfl_sync(0xffffffffu, good, 0);
@@ -302,10 +307,46 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 it.hkv);
                 }
             };
+            // Gathered rows: keys key0 .. key0 + nkeys - 1 (those below the
+            // request's end), 64-column slices slice0 .. slice0 + nsl - 1, as
+            // [8-key group][slice][8 keys][128 B] with the 128-byte swizzle; a
+            // page id outside the pool reads as zeros.  The copies are
+            // committed as one group; the previous slot's barrier is then
+            // released once its group has landed (one slot stays in flight).
+            uint32_t pend = 0;                      // full barrier of the slot still in flight
+            auto release = [&](int keep) {
+                if (pend == 0) return;
+                if (keep) cp_async_wait<1>(); else cp_async_wait<0>();
+                fence_proxy_async_smem();           // cp.async writes, read by the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pend);
+                pend = 0;
+            };
+            auto gather_copy = [&](const Item& it, const void* cache, uint32_t dst, uint32_t full, int key0,
+                                   int nkeys, int slice0, int nsl, int group_stride) {
+                const uint16_t* base = static_cast<const uint16_t*>(cache);
+                for (int idx = lane; idx < nkeys * nsl * 8; idx += 32) {
+                    const int r = idx / (nsl * 8), s = (idx / 8) % nsl, q = idx % 8;
+                    const int key = key0 + r;
+                    if (key >= it.skv) continue;
+                    const int page = __ldg(a.table + (size_t)it.b * a.max_pages + key / a.page_size);
+                    const bool in_pool = page >= 0 && page < a.num_pages;
+                    const long row = in_pool ? (long)page * a.page_size + key % a.page_size : 0;
+                    const uint16_t* src = base + (row * a.Hkv + it.hkv) * D + 64 * (slice0 + s) + 8 * q;
+                    cp_async16(dst + (r / 8) * group_stride + s * 1024 + (r % 8) * 128 + ((q ^ (r % 8)) << 4), src,
+                               in_pool ? 16u : 0u);
+                }
+                cp_async_commit();
+                release(1);
+                pend = full;
+            };
             auto load_k = [&](const Item& it, int j) -> bool {
                 for (int c = 0; c < C::CK; ++c) {
                     uint32_t dst, full;
-                    if constexpr (MODE == kPaged) {
+                    if (gather) {
+                        if (!take_slot(dst, full, 0)) return false;
+                        gather_copy(it, a.k_cache, dst, full, j * BN, BN, c * C::KSL_C, C::KSL_C, C::K_GROUP);
+                    } else if constexpr (MODE == kPaged) {
                         const int n = BN / a.bt_k;
                         const int rows = paged_blocks(it, j * BN, a.bt_k, n);
                         if (!take_slot(dst, full, (uint32_t)(rows * 128 * C::KSL_C))) return false;
@@ -328,7 +369,10 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int c = 0; c < C::CV; ++c) {
                     uint32_t dst, full;
                     const int key0 = j * BN + c * C::VKEYS;
-                    if constexpr (MODE == kPaged) {
+                    if (gather) {
+                        if (!take_slot(dst, full, 0)) return false;
+                        gather_copy(it, a.v_cache, dst, full, key0, C::VKEYS, 0, C::KSL, C::V_GROUP);
+                    } else if constexpr (MODE == kPaged) {
                         const int n = C::VKEYS / a.bt_v;
                         const int rows = paged_blocks(it, key0, a.bt_v, n);
                         if (!take_slot(dst, full, (uint32_t)(rows * 128 * C::KSL))) return false;
@@ -386,8 +430,12 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (MODE != kPaged) ok = __shfl_sync(0xffffffffu, ok, 0);
                     j = jn;
                 }
+                // the item's last gathered slot, before the next item's waits
+                // (its Q slot frees only once this item's MMAs have run)
+                if (gather) release(0);
             }
-            if (lane == 0 && *abort_flag) {
+            if (gather) cp_async_wait<0>();         // no copy outlives the loop
+            if (lane == 0 && *abort_flag && !gather) {
                 // let the copies in flight land: the last load of each slot
                 for (int s = 0; s < C::NS && s < nc; ++s) {
                     const int last = nc - 1 - ((nc - 1 - s) % C::NS);

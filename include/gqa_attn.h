@@ -304,8 +304,9 @@ gqa_status attn_fwd_varlen(const void* q, const void* k, const void* v,
  *                     tolerance either way.  Calls sharing a workspace must
  *                     not overlap on the GPU.
  *
- * page_size must be a multiple of 8 (GQA_ERR_UNSUPPORTED otherwise; pages
- * move as 8-row TMA blocks) and num_pages >= 1.  Caller obligations on the
+ * Any page_size >= 1 and num_pages >= 1: pages whose size is a multiple of 8
+ * move as 8-row TMA blocks, other page sizes are gathered row by row (slower
+ * loads, the same results).  Caller obligations on the
  * table as for attn_decode_paged; lengths are clamped to
  * [0, max_pages * page_size] and a page id outside [0, num_pages) reads as
  * zeros.  Cache slots past L_b and pages past a request's end never reach

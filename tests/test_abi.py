@@ -134,7 +134,6 @@ def test_varlen_argument_checks(lib):
     assert varlen(lib, ws_bytes=lib.attn_varlen_workspace_size(2, 8, 4, 2) - 1) == WORKSPACE
     assert varlen(lib, ws=ctypes.c_void_p((1 << 20) + 8)) == MISALIGNED
     assert varlen(lib, total_q=0) == OK                          # nothing to do, nothing launched
-    assert paged_varlen(lib, ps=12) == UNSUPPORTED                # pages move as 8-row blocks
     assert paged_varlen(lib, ps=0) == INVALID
     assert paged_varlen(lib, num_pages=0) == INVALID
     assert paged_varlen(lib, D=80) == UNSUPPORTED

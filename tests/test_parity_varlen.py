@@ -3,7 +3,7 @@ the C ABI: attn_fwd_varlen (TileOPs "Attention Operators", GQAVarlenFwdOp)
 and attn_fwd_paged (GQAPagedFwdOp: prefill chunks and decode steps over a
 paged cache in one launch).  Request mixes with empty requests, requests
 without keys, Sq > Skv, group sizes that do not divide the 128-row tile,
-every head dim, page sizes from 8 to 256, the optional terms, float16, and
+every head dim, page sizes from 1 to 256, the optional terms, float16, and
 cache slots the call must not read poisoned with NaN."""
 import pytest
 import torch
@@ -108,6 +108,11 @@ PAGED = [
     ([1, 40, 2], [500, 300, 2], 8, 2, 128, 24),                            # 24-token pages: 8-token blocks
     ([5, 1, 130], [900, 600, 130], 16, 2, 256, 256),                       # pages larger than a key tile
     ([1, 1, 20, 1], [0, 700, 40, 1], 8, 2, 128, 16),                       # a decode step with an empty cache
+    # page sizes that are not a multiple of 8: rows gathered with cp.async
+    ([1, 37, 3], [300, 200, 3], 8, 2, 128, 1),
+    ([2, 1, 150], [41, 500, 400], 8, 2, 64, 3),
+    ([1, 129, 4], [777, 129, 260], 24, 2, 256, 5),
+    ([200, 1, 1], [1000, 13, 1200], 32, 8, 128, 12),
 ]
 
 
