@@ -335,8 +335,8 @@ gqa_status attn_decode_paged_fp8kv(const void* q, const void* k_cache, const voi
     if ((long)num_pages * page_size >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
     if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
     if (D != 128 && D != 256) return GQA_ERR_UNSUPPORTED;
+    // pages the byte boxes tile move by TMA; others are gathered row by row
     const int box = gqa::decode_box_tokens(D, page_size);
-    if (box <= 0) return GQA_ERR_UNSUPPORTED;
     if (Sq == 0) return GQA_OK;
     if (!q || !k_cache || !v_cache || !real_seqlen_kv || !block_table || !o) return GQA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return GQA_ERR_MISALIGNED;
@@ -389,8 +389,14 @@ gqa_status attn_decode_paged_fp8kv(const void* q, const void* k_cache, const voi
         a.tc_grid = p.tc_grid;
         return gqa::launch_decode_tc_fp8(tk, tv, a, tbox, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
     }
-    if (!make_cache_map_fp8(&tk, k_cache, rows, Hkv, D, box) || !make_cache_map_fp8(&tv, v_cache, rows, Hkv, D, box))
-        return GQA_ERR_CUDA;
+    if (box > 0) {
+        if (!make_cache_map_fp8(&tk, k_cache, rows, Hkv, D, box) ||
+            !make_cache_map_fp8(&tv, v_cache, rows, Hkv, D, box))
+            return GQA_ERR_CUDA;
+    } else {
+        tk = CUtensorMap{};                         // unused by the gather producer
+        tv = CUtensorMap{};
+    }
     return gqa::launch_decode_fp8(a, tk, tv, box, st) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 

@@ -657,7 +657,51 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    if (warp == C::NC) {
+    if (warp == C::NC && box_tokens == 0) {
+        // ------------------------------------------------------------ gather producer
+        // Page sizes the byte boxes cannot tile: all 32 lanes copy each tile's
+        // e4m3 rows with 16-byte cp.async into the same swizzled layout (rows
+        // past the split's end are left to the consumers, a page id outside
+        // the pool reads as zeros).  A slot's full barrier takes lane 0's
+        // arrival once the slot's copies have landed; one slot stays in flight.
+        const int32_t* trow = a.table + (size_t)w.b * a.max_pages;
+        const uint8_t* kc = static_cast<const uint8_t*>(a.k_cache);
+        const uint8_t* vc = static_cast<const uint8_t*>(a.v_cache);
+        constexpr int CPR = D / 16;                 // 16-byte chunks per row
+        int pend = -1;                              // slot whose copies are in flight
+        bool good = true;
+        for (int it = 0; it < w.n_tiles; ++it) {
+            const int s = it % C::NS;
+            if (lane == 0) good = mbar_wait(empty(s), ((it / C::NS) & 1) ^ 1, abort_flag);
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) break;
+            const int t0 = w.t_begin + it * C::TK;
+            const uint32_t sK = sb + C::OFF_KV + s * 2 * C::TILE8;
+            const uint32_t sV = sK + C::TILE8;
+            for (int idx = lane; idx < C::TK * CPR; idx += 32) {
+                const int r = idx / CPR, c = idx % CPR;
+                const int t = t0 + r;
+                if (t >= w.t_end) continue;
+                const int page = trow[t / a.page_size];
+                const bool in_pool = page >= 0 && page < a.num_pages;
+                const long row = in_pool ? (long)page * a.page_size + t % a.page_size : 0;
+                const size_t src = ((size_t)row * a.Hkv + w.hkv) * D + c * 16;
+                const uint32_t off = off8<C::SUB8>(r, c);
+                cp_async16(sK + off, kc + src, in_pool ? 16u : 0u);
+                cp_async16(sV + off, vc + src, in_pool ? 16u : 0u);
+            }
+            cp_async_commit();
+            if (pend >= 0) {
+                cp_async_wait<1>();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full(pend));
+            }
+            pend = s;
+        }
+        cp_async_wait<0>();                         // no copy outlives the CTA
+        __syncwarp();
+        if (good && pend >= 0 && lane == 0) mbar_arrive(full(pend));
+    } else if (warp == C::NC) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);

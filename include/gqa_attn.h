@@ -196,9 +196,11 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_cache, const void* 
  * The keys and values are widened exactly to float16 on the GPU and the
  * products run in float16 with FP32 accumulation, so Q is rounded to float16
  * once: a bfloat16 Q keeps every bit for magnitudes in [2^-14, 65504] and must
- * stay below 65504.  Supported: D = 128 or 256, and page sizes that are a
- * multiple of 8 and divide, or are divided by, the key tile (64 tokens at
- * D = 128, 32 at D = 256); other sizes return GQA_ERR_UNSUPPORTED.  Caller
+ * stay below 65504.  Supported: D = 128 or 256 (GQA_ERR_UNSUPPORTED
+ * otherwise) and any page size: pages that are a multiple of 8 and divide,
+ * or are divided by, the key tile (64 tokens at D = 128, 32 at D = 256) move
+ * by TMA, other sizes are gathered row by row (slower loads, the same
+ * results; KV groups of 32 or more rows then take the split kernel).  Caller
  * obligations and the handling of bad page ids and lengths are those of
  * attn_decode_paged.
  */

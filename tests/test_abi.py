@@ -100,7 +100,6 @@ def test_paged_fp8kv_argument_checks(lib):
     assert paged_fp8(lib, B=0) == INVALID
     assert paged_fp8(lib, Hq=6, Hkv=4) == INVALID
     assert paged_fp8(lib, D=64) == UNSUPPORTED                  # e4m3 rows of 128 or 256 bytes only
-    assert paged_fp8(lib, ps=12) == UNSUPPORTED                 # pages must tile the key tile in 8-row blocks
     assert paged_fp8(lib, kc=MIS) == MISALIGNED
     assert paged_fp8(lib, ks=ctypes.c_void_p((1 << 20) + 2)) == MISALIGNED
     assert paged_fp8(lib, ws=None, ws_bytes=0) == WORKSPACE

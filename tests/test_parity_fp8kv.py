@@ -67,6 +67,11 @@ SMALL = [
     (3, 1, 32, 8, 128, 64, [64, 65, 1]),             # one-key and exact-tile tails
     (2, 3, 64, 1, 128, 64, [700, 1500]),             # 192 rows: the split kernel, three row blocks
     (2, 2, 48, 1, 256, 96, [500, 1000]),             # 96 rows, pages of no 64-key tiling: split, two row blocks
+    # page sizes the byte boxes cannot tile: rows gathered with cp.async
+    (3, 1, 8, 2, 128, 1, [1, 77, 300]),              # one-token pages
+    (2, 4, 24, 2, 256, 5, [3, 901]),                 # 48 rows per KV head (split kernel, not tensor cores)
+    (4, 1, 32, 8, 128, 12, [12, 13, 0, 600]),        # 12-token pages, an empty request
+    (2, 2, 16, 2, 128, 24, [500, 49]),               # a multiple of 8 that does not tile the 64-key tile
 ]
 
 
