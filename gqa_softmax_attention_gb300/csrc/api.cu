@@ -465,6 +465,7 @@ static gqa_status varlen_common(const void* q, void* o, float* lse, const int32_
     a->f16 = f16 ? 1 : 0;
     a->x = ex;
     a->n_entries = static_cast<const int32_t*>(workspace);
+    a->work = static_cast<int32_t*>(workspace) + 1;
     a->entries = reinterpret_cast<const int32_t*>(static_cast<char*>(workspace) + 16);
     a->g = g;
     a->qpb = qpb;

@@ -30,6 +30,7 @@ struct PrefillArgs {
     // the plan kernel.  Unused by the BSHD kernels.
     const int32_t* entries;   // [max_entries, 8]: b, q0, qs, sq, ks, L, -, -
     const int32_t* n_entries; // number of entries (device)
+    int32_t* work;            // packed: item counter, zeroed by the plan kernel
     int g;                    // query heads per KV head
     int qpb;                  // queries per row block: floor(128 / g)
     const int32_t* table;     // paged: block_table [B, max_pages]

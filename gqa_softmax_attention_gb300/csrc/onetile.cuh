@@ -112,8 +112,8 @@ struct Cfg {
     static constexpr int OFF_STATS = OFF_STAGE + 2 * BOX;    // m[128], l[128], visited-tile count
     static constexpr int OFF_BAR = OFF_STATS + 2 * BM * 4 + 16;
     // q_full, q_empty, r_full[NS], r_empty[NS], s_full[2], p_full[2], o_ready,
-    // o_final, o_empty, stats_full, stats_empty, drain
-    static constexpr int NBAR = 2 + 2 * NS + 4 + 6;
+    // o_final, o_empty, stats_full, stats_empty, drain, item_full[2], item_empty[2]
+    static constexpr int NBAR = 2 + 2 * NS + 4 + 6 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;        // 1 KB alignment slack
@@ -149,9 +149,11 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int qpb = PACKED ? a.qpb : BM;         // queries per block
     const int n_e = PACKED ? *a.n_entries : 0;
     // Work items.  kBSHD: heaviest (last) query tiles first, adjacent items on
-    // one KV head.  Packed: item w = (row block w / Hkv, KV head w % Hkv), the
-    // row blocks ordered by estimated cost, heaviest first.  Round r takes
-    // item r * G + cta (even r) or r * G + G - 1 - cta (odd r).
+    // one KV head; round r takes item r * G + cta (even r) or r * G + G - 1 -
+    // cta (odd r).  Packed: item w = (row block w / Hkv, KV head w % Hkv), the
+    // requests ordered by estimated cost, heaviest first; items are claimed
+    // in that order from a counter in the workspace (the plan kernel zeroes
+    // it), so that a CTA whose items ran long takes fewer of them.
     const int n_items = PACKED ? n_e * a.Hkv : n_qtiles * a.B * a.Hq;
     const int G = gridDim.x;
     const int cta = blockIdx.x;
@@ -215,11 +217,46 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t o_ready = bar0 + 8u * (6 + 2 * C::NS);
     const uint32_t o_final = o_ready + 8, o_empty = o_ready + 16;
     const uint32_t stats_full = o_ready + 24, stats_empty = o_ready + 32, drain = o_ready + 40;
+    auto item_full = [&](int k) { return o_ready + 48u + 8u * k; };
+    auto item_empty = [&](int k) { return o_ready + 64u + 8u * k; };
     float* st_m = reinterpret_cast<float*>(smem + C::OFF_STATS);
     float* st_l = st_m + BM;
     volatile int* st_cnt = reinterpret_cast<volatile int*>(st_l + BM);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    volatile int* item_rec = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);   // two claimed items
+    // Packed: the producer claims items and hands each one's index to the
+    // MMA warp and the eight softmax / epilogue warps through a two-slot
+    // record; the last record it writes is -1.  Warp-collective.
+    auto claim_item = [&](int r) -> int {
+        if constexpr (!PACKED) {
+            return item_of(r);
+        } else {
+            int w = -1;
+            if (lane == 0) {
+                const int slot = r & 1;
+                if (mbar_wait(item_empty(slot), ((r >> 1) & 1) ^ 1, abort_flag)) {
+                    w = atomicAdd(a.work, 1);
+                    if (w >= n_items) w = -1;
+                    item_rec[slot] = w;
+                    mbar_arrive(item_full(slot));
+                }
+            }
+            return __shfl_sync(0xffffffffu, w, 0);
+        }
+    };
+    auto next_item = [&](int r) -> int {
+        if constexpr (!PACKED) {
+            return item_of(r);
+        } else {
+            const int slot = r & 1;
+            const bool got = __all_sync(0xffffffffu, mbar_wait(item_full(slot), (r >> 1) & 1, abort_flag));
+            const int w = got ? item_rec[slot] : -1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(item_empty(slot));
+            return w;
+        }
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -232,6 +269,10 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(stats_full, BM);
         mbar_init(stats_empty, BM);
         mbar_init(drain, 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(item_full(k), 1);
+            mbar_init(item_empty(k), 1 + 8);   // the MMA warp and the eight softmax / epilogue warps
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -391,7 +432,7 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 return true;
             };
             for (int r = 0; ok; ++r) {
-                const int w = item_of(r);
+                const int w = claim_item(r);
                 if (w < 0) break;
                 const Item it = describe(w);
                 const int c = count_tiles(it);
@@ -515,7 +556,7 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 return true;
             };
             for (int r = 0, n_item = 0; ok; ++r, ++n_item) {
-                const int w = item_of(r);
+                const int w = next_item(r);
                 if (w < 0) break;
                 const Item it = describe(w);
                 const int c = count_tiles(it);
@@ -593,7 +634,7 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         int n = 0;                   // items finished
         bool ok = true;
         for (int rr = 0; ok; ++rr) {
-            const int w = item_of(rr);
+            const int w = next_item(rr);
             if (w < 0) break;
             const Item itm = describe(w);
             const TileInfo ti = itm.t;
@@ -733,7 +774,7 @@ onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         int nb = 0;                  // output boxes stored (staging buffer alternation)
         bool ok = true;
         for (int rr = 0;; ++rr) {
-            const int w = item_of(rr);
+            const int w = next_item(rr);
             if (w < 0) break;
             const Item itm = describe(w);
             const TileInfo ti = itm.t;

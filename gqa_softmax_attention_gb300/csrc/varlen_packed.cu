@@ -154,7 +154,10 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
         dst[0] = e0;
         dst[1] = make_int4(e1.x, e1.y, 0, 0);
     }
-    if (threadIdx.x == 0) *n_entries = n;
+    if (threadIdx.x == 0) {
+        n_entries[0] = n;
+        n_entries[1] = 0;                              // the attention kernel's item counter
+    }
 }
 
 }  // namespace
