@@ -132,6 +132,7 @@ TRAFFIC = {
     "paged_decode_fp8kv": ("ratio", (279.805952 + 5.622016) / 278.458368),
     "wide_group_decode_fp8kv": ("ratio", (117.060352 + 3.536896) / 116.341760),
     "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
+    "varlen_prefill": ("bytes", (798.223872 + 504.861952) * 1e6),
 }
 
 
