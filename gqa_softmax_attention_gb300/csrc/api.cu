@@ -497,10 +497,15 @@ gqa_status attn_fwd_varlen(const void* q, const void* k, const void* v, const in
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int max_e = varlen_max_entries(B, total_q, a.qpb);
     int32_t* ws = static_cast<int32_t*>(workspace);
+    // D = 64 and 128 run on the two-Q-tile kernel (items of two consecutive
+    // row blocks sharing each K/V tile); D = 256 on the one-tile kernel
+    const bool two = D <= 128;
     if (gqa::launch_varlen_plan(cu_seqlens_q, cu_seqlens_kv, false, B, a.qpb, a.g, a.causal, total_q, total_kv,
-                                ws + 4 + (size_t)max_e * 8, ws + 4, ws, max_e, s) != cudaSuccess)
+                                ws + 4 + (size_t)max_e * 8, ws + 4, ws, max_e, s, false, two) != cudaSuccess)
         return GQA_ERR_CUDA;
-    return gqa::launch_varlen_packed(tq, tk, tv, to, a, (long)max_e * Hkv, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    const cudaError_t e = two ? gqa::launch_prefill_packed(tq, tk, tv, to, a, (long)max_e * Hkv, s)
+                              : gqa::launch_varlen_packed(tq, tk, tv, to, a, (long)max_e * Hkv, s);
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,

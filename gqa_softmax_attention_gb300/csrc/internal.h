@@ -48,6 +48,13 @@ struct PrefillArgs {
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, const CUtensorMap& tm_o, const PrefillArgs& a,
                            cudaStream_t stream);
+// The same two-Q-tile kernel over packed THD calls (D = 64 or 128): items are
+// pairs of consecutive row blocks of one request, listed by the plan kernel
+// with pairs set; tm_q / tm_o as for launch_varlen_packed, tm_k / tm_v
+// {D, Hkv, total_kv} with {64, 1, 128} boxes.  max_items bounds pair entries
+// * Hkv.
+cudaError_t launch_prefill_packed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                  const CUtensorMap& tm_o, const PrefillArgs& a, long max_items, cudaStream_t stream);
 // Rows with no key at all (Skv == 0): O = 0, LSE = -inf.
 cudaError_t launch_empty_rows(void* o, float* lse, long rows, int D, cudaStream_t stream);
 int prefill_take_device_error();
@@ -65,9 +72,11 @@ int prefill_d256_take_device_error();
 // request's key count (total_kv, or max_pages * page_size).
 // skip_single leaves requests with exactly one query out of the list (they
 // run on the split decode kernel instead).
+// pairs lists pairs of consecutive row blocks (q0 = 2k * qpb) for the
+// two-Q-tile kernel.
 cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int g, int causal,
                                int total_q, long kv_cap, int32_t* tmp, int32_t* entries, int32_t* n_entries,
-                               int max_entries, cudaStream_t stream, bool skip_single = false);
+                               int max_entries, cudaStream_t stream, bool skip_single = false, bool pairs = false);
 // tm_q / tm_o: {D, Hq, total_q} with a {64, g, qpb} box.  Packed: tm_k / tm_v
 // {D, Hkv, total_kv} with {64, 1, 128} and {64, 1, 128 or 64 (D = 256)} boxes.
 // Paged: the caches as {64, 8, D / 64, pages * page_size / 8, Hkv} with

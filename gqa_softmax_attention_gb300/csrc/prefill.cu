@@ -10,7 +10,11 @@
 // (MATE "QSA", Core Attention).
 //
 // One CTA owns two 128-row query tiles (Q0, Q1) of one (b, h); both read the
-// same K/V tiles.  Warp roles:
+// same K/V tiles.  The same kernel serves packed THD calls (variable-length
+// requests laid end to end): there a query tile holds the g query heads of one
+// KV head for 128 / g consecutive queries of one request, the two tiles are
+// consecutive row blocks of that request, and the CTAs claim such items from a
+// counter in the call's workspace in the order a plan kernel wrote.  Warp roles:
 //   warp 8     TMA producer: Q0 and Q1 once, then K_j and V_j tiles through two
 //              shared-memory rings (128-byte swizzle, 64-column boxes);
 //   warp 9     MMA issuer (one thread): S_k = Q_k K_j^T into TMEM, then
@@ -22,9 +26,10 @@
 //              S row, rescales its O row when needed, and finally normalises O
 //              into its Q tile's shared-memory buffer, from which one thread
 //              stores the tile with TMA, and writes the LSE.
-// Warps 10-11 only complete the third warpgroup (register rebalancing works
-// per warpgroup).  TMEM (512 columns): S0 | S1 | O0 | O1; P_k occupies the
-// first 64 columns of S_k.
+// Warps 10-11 complete the third warpgroup (register rebalancing works per
+// warpgroup); in packed calls they zero the value rows past a request's end in
+// its last key tile before that tile's P V.  TMEM (512 columns): S0 | S1 |
+// O0 | O1; P_k occupies the first 64 columns of S_k.
 //
 // The O rescale is lazy: the reference max of a row only moves when the tile
 // max exceeds it by more than kRescaleThreshold (log2 units), so most tiles
@@ -52,6 +57,9 @@ namespace {
 __device__ int g_prefill_error;
 
 using namespace pf;
+// Layouts: dense BSHD calls (attn_fwd_dense) and packed THD rows
+// (attn_fwd_varlen).
+constexpr int kModeDense = 0, kModePacked = 1;
 constexpr int NQ = 2;              // Q tiles per CTA
 constexpr int NUM_THREADS = 384;   // warps 0-7 softmax, 8 producer, 9 MMA, 10-11 idle
 constexpr int WARP_LOAD = 8;
@@ -78,12 +86,14 @@ struct Cfg {
     static constexpr int OFF_STAGE = OFF_V + NV * TILE_BYTES;   // one 64-column output box per Q tile
     static constexpr int OFF_BAR = OFF_STAGE + NQ * SUB_BYTES;
     // q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-    // s_full[2], p_full[2], o_final[2], drain, info_full[2], info_empty[2]
-    static constexpr int NBAR = 4 + 2 * NK + 2 * NV + 6 + 1 + 4;
+    // s_full[2], p_full[2], o_final[2], drain, info_full[2], info_empty[2],
+    // v_landed, v_fixed
+    static constexpr int NBAR = 4 + 2 * NK + 2 * NV + 6 + 1 + 4 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    // two 32-byte item records (tile counts, first flag word, first tile's mask words)
+    // two 64-byte item records (tile counts, first flag word, first tile's mask
+    // words, the item's index)
     static constexpr int OFF_INFO = OFF_MISC + 16;
-    static constexpr int SMEM_USED = OFF_INFO + 2 * 32;
+    static constexpr int SMEM_USED = OFF_INFO + 2 * 64;
     // 1 KB alignment slack; at least 120 KB so that one CTA holds an SM (it
     // takes all 512 TMEM columns).
     static constexpr int SMEM_BYTES = SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
@@ -97,12 +107,13 @@ struct Cfg {
 // OPTS: the call has a window, a softcap or sinks.  Without them every option
 // term is a compile-time constant and the code is the plain causal / padded
 // kernel.
-template <int D, bool OPTS, bool F16>
+template <int D, int MODE, bool OPTS, bool F16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const PrefillArgs a, int n_qpairs) {
     using C = Cfg<D>;
+    constexpr bool PACKED = MODE != kModeDense;
     // both MMA operands of the call's 16-bit type (P is packed to it as well)
     constexpr uint32_t IDESC_QK = make_idesc_16<F16>(BM, BN, false, false);
     constexpr uint32_t IDESC_PV = make_idesc_16<F16>(BM, D, false, true);
@@ -119,12 +130,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    // Work items w = 0 .. n_items-1, heaviest (last) query tiles first and
-    // adjacent items on one KV head; round r of this persistent CTA takes
-    // item r * G + cta (even r) or r * G + G - 1 - cta (odd r), so heavy and
-    // light items alternate across rounds.
+    // Work items.  Dense: w = 0 .. n_items-1, heaviest (last) query tiles
+    // first and adjacent items on one KV head; round r of this persistent CTA
+    // takes item r * G + cta (even r) or r * G + G - 1 - cta (odd r), so heavy
+    // and light items alternate across rounds.  Packed: item w = (pair entry
+    // w / Hkv of the plan, KV head w % Hkv), two consecutive row blocks of one
+    // request, claimed in the plan's order from the workspace's counter.  The
+    // producer hands every item's index to the other roles in its record.
     const int bh = a.B * a.Hq;
-    const int n_items = n_qpairs * bh;
+    const int g = PACKED ? a.g : 1;              // query rows per query (heads of a KV group)
+    const int qpb = PACKED ? a.qpb : BM;         // queries per Q tile
+    const int n_items = PACKED ? *a.n_entries * a.Hkv : n_qpairs * bh;
     const int G = gridDim.x;
     const int cta = blockIdx.x;
     auto item_of = [&](int r) -> int {
@@ -133,25 +149,44 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     };
     struct Item {
         int b, hq, hkv, q0, first, n_all, kv_end_all;
-        TileInfo t0, t1;
+        int qs, ks, sq, skv;    // packed: first query / key row of the request, its queries and keys
+        TileInfo t0, t1;        // t_k.q0: first query of Q tile k (within the request)
         const uint8_t* mrow;
     };
     auto describe = [&](int w) {
         Item it;
-        const int qp = n_qpairs - 1 - w / bh;
-        const int rem = w % bh;
-        it.hq = rem % a.Hq;
-        it.b = rem / a.Hq;
-        it.hkv = it.hq / (a.Hq / a.Hkv);
-        it.q0 = qp * (NQ * BM);
-        it.t0 = tile_info(it.q0, a.Sq, a.Skv, a.causal, wl, wr);
-        it.t1 = tile_info(it.q0 + BM, a.Sq, a.Skv, a.causal, wl, wr);
+        if constexpr (PACKED) {
+            const int4* e = reinterpret_cast<const int4*>(a.entries + (size_t)(w / a.Hkv) * 8);
+            const int4 e0 = e[0], e1 = e[1];
+            it.b = e0.x;
+            it.hkv = w % a.Hkv;
+            it.hq = it.hkv * g;
+            it.q0 = e0.y;
+            it.qs = e0.z;
+            it.sq = e0.w;
+            it.ks = e1.x;
+            it.skv = e1.y;
+            it.t0 = tile_info_n(it.q0, qpb, it.sq, it.skv, a.causal, wl, wr);
+            it.t1 = tile_info_n(it.q0 + qpb, qpb, it.sq, it.skv, a.causal, wl, wr);
+        } else {
+            const int qp = n_qpairs - 1 - w / bh;
+            const int rem = w % bh;
+            it.hq = rem % a.Hq;
+            it.b = rem / a.Hq;
+            it.hkv = it.hq / (a.Hq / a.Hkv);
+            it.q0 = qp * (NQ * BM);
+            it.qs = it.ks = 0;
+            it.sq = a.Sq;
+            it.skv = a.Skv;
+            it.t0 = tile_info(it.q0, a.Sq, a.Skv, a.causal, wl, wr);
+            it.t1 = tile_info(it.q0 + BM, a.Sq, a.Skv, a.causal, wl, wr);
+        }
         it.n_all = max(it.t0.n_tiles, it.t1.n_tiles);
         it.kv_end_all = max(it.t0.kv_end, it.t1.kv_end);
         // both Q tiles walk the tiles from the first one either needs (Q1's
         // window starts later: its extra leading tiles are fully masked)
         it.first = (it.t0.n_tiles > 0 ? it.t0.kv_begin : it.t1.kv_begin) / BN;
-        it.mrow = a.mask ? a.mask + (size_t)it.b * a.Skv : nullptr;
+        it.mrow = (!PACKED && a.mask) ? a.mask + (size_t)it.b * a.Skv : nullptr;
         return it;
     };
     // Visited key tiles of an item (non-empty, from its first tile to kv_end of
@@ -182,11 +217,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t drain = bar0 + 8u * (10 + 2 * C::NK + 2 * C::NV);
     auto info_full = [&](int i) { return bar0 + 8u * (11 + 2 * C::NK + 2 * C::NV + i); };
     auto info_empty = [&](int i) { return bar0 + 8u * (13 + 2 * C::NK + 2 * C::NV + i); };
+    // packed: the value rows past the request's end in an item's last tile are
+    // zeroed (warps 10-11) before its P V: the MMA thread, which takes the
+    // tiles in order, signals v_landed once that tile is in and waits for
+    // v_fixed
+    const uint32_t v_landed = bar0 + 8u * (15 + 2 * C::NK + 2 * C::NV);
+    const uint32_t v_fixed = bar0 + 8u * (16 + 2 * C::NK + 2 * C::NV);
     // Item records, written by the producer one item ahead of its consumers:
     // c0, c1, c_all, the flag word of the first 32-tile chunk and the mask
     // words of the first visited tile, so that no consumer scans the padding
     // mask in global memory at an item boundary.
     uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);
+    constexpr int REC = PACKED ? 16 : 8;   // words per record (packed: the item's index in word 8)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -203,10 +245,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(drain, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(info_full(i), 1);
-            mbar_init(info_empty(i), 1 + 8);   // the MMA thread and the eight softmax warps
+            // the MMA thread and the eight softmax warps (packed: and warps 10-11)
+            mbar_init(info_empty(i), PACKED ? 1 + 8 + 2 : 1 + 8);
         }
+        mbar_init(v_landed, 1);
+        mbar_init(v_fixed, 2);
         *abort_flag = 0;
         fence_mbar_init();
+    }
+    if constexpr (PACKED) {
+        // Q rows past g * qpb are never loaded: zero them once (finite rows,
+        // whose results are never stored)
+        const int rows = g * qpb;
+        const int per = (BM - rows) * 8 * C::KSUB;   // 16-byte chunks per Q tile
+        for (int x = threadIdx.x; x < NQ * per; x += NUM_THREADS) {
+            const int kq = x / per, y = x % per;
+            const int row = rows + y / (8 * C::KSUB), sl = (y / 8) % C::KSUB, q = y % 8;
+            *reinterpret_cast<uint4*>(smem + C::OFF_Q + kq * C::TILE_BYTES + sl * C::SUB_BYTES + row * 128 + q * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
     }
     if (warp == WARP_MMA) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -232,8 +290,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tma_prefetch_desc(&tm_v);
             }
             for (int r = 0; ok; ++r) {
-                const int w = item_of(r);
-                if (w < 0) break;
+                int w;
+                if constexpr (PACKED) {
+                    w = -1;
+                    if (lane == 0) {
+                        w = atomicAdd(a.work, 1);
+                        if (w >= n_items) w = -1;
+                    }
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                } else {
+                    w = item_of(r);
+                }
+                if (w < 0) {
+                    // packed: a last record with no item (dense consumers
+                    // know the item count)
+                    if (PACKED && lane == 0) {
+                        const int slot = r & 1;
+                        if (mbar_wait(info_empty(slot), ((r >> 1) & 1) ^ 1, abort_flag)) {
+                            info[REC * slot + 8] = 0xffffffffu;
+                            mbar_arrive(info_full(slot));
+                        }
+                    }
+                    break;
+                }
                 const Item it = describe(w);
                 int c0, c1, c_all;
                 uint32_t f0;
@@ -251,7 +330,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     const int slot = r & 1;
                     ok = mbar_wait(info_empty(slot), ((r >> 1) & 1) ^ 1, abort_flag);
                     if (ok) {
-                        uint32_t* rec = info + 8 * slot;
+                        uint32_t* rec = info + REC * slot;
+                        if constexpr (PACKED) rec[8] = (uint32_t)w;
                         rec[0] = (uint32_t)c0;
                         rec[1] = (uint32_t)c1;
                         rec[2] = (uint32_t)c_all;
@@ -269,11 +349,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 auto load_q = [&](int k) -> bool {   // lane 0
                     const int nq = k == 0 ? nq0 : nq1;
                     if (!mbar_wait(q_empty(k), (nq & 1) ^ 1, abort_flag)) return false;
-                    mbar_arrive_expect_tx(q_full(k), C::TILE_BYTES);
+                    if constexpr (PACKED) {
+                        // {64, g, qpb} boxes: row q * g + h of the tile is query q, head hq + h
+                        mbar_arrive_expect_tx(q_full(k), (uint32_t)(C::KSUB * g * qpb * 128));
 #pragma unroll
-                    for (int s = 0; s < C::KSUB; ++s)
-                        tma_load_4d(sb + C::OFF_Q + k * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, q_full(k),
-                                    s * 64, it.q0 + k * BM, it.hq, it.b);
+                        for (int s = 0; s < C::KSUB; ++s)
+                            tma_load_3d(sb + C::OFF_Q + k * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, q_full(k),
+                                        s * 64, it.hq, it.qs + it.q0 + k * qpb);
+                    } else {
+                        mbar_arrive_expect_tx(q_full(k), C::TILE_BYTES);
+#pragma unroll
+                        for (int s = 0; s < C::KSUB; ++s)
+                            tma_load_4d(sb + C::OFF_Q + k * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, q_full(k),
+                                        s * 64, it.q0 + k * BM, it.hq, it.b);
+                    }
                     if (k == 0) ++nq0; else ++nq1;
                     return true;
                 };
@@ -286,9 +375,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         if (ok) {
                             mbar_arrive_expect_tx(k_full(ks), C::TILE_BYTES);
 #pragma unroll
-                            for (int s = 0; s < C::KSUB; ++s)
-                                tma_load_4d(sb + C::OFF_K + ks * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k,
-                                            k_full(ks), s * 64, j * BN, it.hkv, it.b);
+                            for (int s = 0; s < C::KSUB; ++s) {
+                                const uint32_t dst = sb + C::OFF_K + ks * C::TILE_BYTES + s * C::SUB_BYTES;
+                                if constexpr (PACKED)
+                                    tma_load_3d(dst, &tm_k, k_full(ks), s * 64, it.hkv, it.ks + j * BN);
+                                else
+                                    tma_load_4d(dst, &tm_k, k_full(ks), s * 64, j * BN, it.hkv, it.b);
+                            }
                             ++nk;
                         }
                         if (ok && q1_due) ok = load_q(1);
@@ -298,9 +391,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             if (ok) {
                                 mbar_arrive_expect_tx(v_full(vs), C::TILE_BYTES);
 #pragma unroll
-                                for (int s = 0; s < C::KSUB; ++s)
-                                    tma_load_4d(sb + C::OFF_V + vs * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v,
-                                                v_full(vs), s * 64, j * BN, it.hkv, it.b);
+                                for (int s = 0; s < C::KSUB; ++s) {
+                                    const uint32_t dst = sb + C::OFF_V + vs * C::TILE_BYTES + s * C::SUB_BYTES;
+                                    if constexpr (PACKED)
+                                        tma_load_3d(dst, &tm_v, v_full(vs), s * 64, it.hkv, it.ks + j * BN);
+                                    else
+                                        tma_load_4d(dst, &tm_v, v_full(vs), s * 64, j * BN, it.hkv, it.b);
+                                }
                                 ++nv;
                             }
                         }
@@ -327,19 +424,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // ------------------------------------------------------------ MMA issuer
             int kt = 0, vt = 0;                    // K and V tiles consumed by earlier items
             int nq0 = 0, nq1 = 0, pc0 = 0, pc1 = 0;   // Q loads consumed, P tiles taken
+            int nfix = 0;                          // v_fixed phases waited (packed)
             bool ok = true;
             for (int r = 0; ok; ++r) {
-                if (item_of(r) < 0) break;
+                if (!PACKED && item_of(r) < 0) break;  // dense: no record past the last item
                 int c0 = 0, c1 = 0, c_all = 0;         // lane 0 holds the item's tile counts
+                int w = 0;
                 if (lane == 0) {
                     const int slot = r & 1;
                     ok = mbar_wait(info_full(slot), (r >> 1) & 1, abort_flag);
                     if (ok) {
-                        c0 = (int)info[8 * slot];
-                        c1 = (int)info[8 * slot + 1];
-                        c_all = (int)info[8 * slot + 2];
+                        if constexpr (PACKED) w = (int)info[REC * slot + 8];
+                        c0 = (int)info[REC * slot];
+                        c1 = (int)info[REC * slot + 1];
+                        c_all = (int)info[REC * slot + 2];
                         mbar_arrive(info_empty(slot));
                     }
+                }
+                if constexpr (PACKED) {
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (__shfl_sync(0xffffffffu, w, 0) < 0) break;  // the last record (or a wait gave up)
                 }
                 if (lane == 0 && ok && c_all > 0) {
                     auto issue_s = [&](int k, int slot) {
@@ -364,6 +468,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                         tmem + (k == 0 ? C::COL_S0 : C::COL_S1) + kk * 8, bdesc, IDESC_PV,
                                         (i > 0 || kk > 0) ? 1u : 0u);
                         }
+                    };
+                    // V of visited tile i (ring slot vs); packed: the item's last tile
+                    // also waits for its value rows past the request's end to be zeroed
+                    auto wait_v = [&](int i, int vs) -> bool {
+                        if (!mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag)) return false;
+                        if (PACKED && i == c_all - 1) {
+                            mbar_arrive(v_landed);
+                            if (!mbar_wait(v_fixed, nfix & 1, abort_flag)) return false;
+                            ++nfix;
+                        }
+                        return true;
                     };
                     // first tile: S0 once Q0 and K are in, S1 once Q1 is (loaded after K)
                     if (c0 > 0) ok = mbar_wait(q_full(0), nq0++ & 1, abort_flag);
@@ -402,7 +517,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         for (int i = 0; i + 1 < c0 && ok; ++i) {
                             const int vs = (vt + i) % C::NV;
                             const int kn = kt + i + 1;
-                            ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
+                            ok = wait_v(i, vs);
                             if (ok) ok = pv(0, vs, i);
                             if (ok) ok = wait_k(kn);
                             if (!ok) break;
@@ -417,7 +532,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         // tile c0-1: Q0's last P V, then its epilogue may start
                         const int i = c0 - 1;
                         const int vs = (vt + i) % C::NV;
-                        if (ok) ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
+                        if (ok) ok = wait_v(i, vs);
                         if (ok) ok = pv(0, vs, i);
                         if (ok) mma_commit(o_final(0));
                         if (ok && c1 == c0 + 1) {
@@ -430,7 +545,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 mma_commit(k_empty(kn % C::NK));
                                 mma_commit(q_empty(1));
                                 const int vs2 = (vt + c0) % C::NV;
-                                ok = mbar_wait(v_full(vs2), ((vt + c0) / C::NV) & 1, abort_flag);
+                                ok = wait_v(c0, vs2);
                                 if (ok) ok = pv(1, vs2, c0);
                                 if (ok) mma_commit(v_empty(vs2));
                             }
@@ -448,7 +563,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // conditional commits inside it slowed the steady state.
                     for (int i = 0; !peel && i + 1 < c_all && ok; ++i) {
                         const int vs = (vt + i) % C::NV;
-                        ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
+                        ok = wait_v(i, vs);
                         if (!ok) break;
                         const int kn = kt + i + 1;     // K tile of visited tile i+1
                         for (int k = 0; k < NQ && ok; ++k) {
@@ -481,7 +596,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (!peel && ok) {
                         const int i = c_all - 1;
                         const int vs = (vt + i) % C::NV;
-                        ok = mbar_wait(v_full(vs), ((vt + i) / C::NV) & 1, abort_flag);
+                        ok = wait_v(i, vs);
                         for (int k = 0; k < NQ && ok; ++k) {
                             const int cnt = k == 0 ? c0 : c1;
                             if (i < cnt) {
@@ -517,6 +632,48 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             named_bar_sync(2, 8 * 32 + 32);          // softmax warps are done with TMEM
             tc_fence_after();
             tmem_dealloc(tmem, C::TMEM_COLS);
+        } else if constexpr (PACKED) {
+            // ------------------------------------------------------------ warps 10-11
+            // In an item's last visited tile, the value rows past the request's
+            // end hold the next request's rows, where 0 * NaN would not vanish: zero them once the tile
+            // has landed, before its P V (the MMA thread waits on v_fixed).
+            const int t = (warp - 10) * 32 + lane;     // 0 .. 63
+            int vt = 0;                                // V tiles of earlier items
+            int nl = 0;                                // v_landed phases waited
+            for (int r = 0;; ++r) {
+                const int slot = r & 1;
+                const bool got = __all_sync(0xffffffffu, mbar_wait(info_full(slot), (r >> 1) & 1, abort_flag));
+                const int w = got ? (int)info[REC * slot + 8] : -1;
+                const int c_all = got ? (int)info[REC * slot + 2] : 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(info_empty(slot));
+                if (w < 0) break;
+                if (c_all == 0) continue;
+                const Item it = describe(w);
+                // packed items visit the tiles [first, n_all) without gaps
+                const int jl = it.n_all - 1;
+                const int i = vt + c_all - 1;
+                vt += c_all;
+                // v_landed first (one phase per item, in order): the slot's phase
+                // for this tile is then the current one and stays so until the
+                // MMA thread has seen v_fixed
+                if (!__all_sync(0xffffffffu, mbar_wait(v_landed, nl & 1, abort_flag))) break;
+                ++nl;
+                if (!__all_sync(0xffffffffu, mbar_wait(v_full(i % C::NV), (i / C::NV) & 1, abort_flag))) break;
+                const int r0 = it.skv - jl * BN;           // first row past the request's end (> 0)
+                if (r0 < BN) {
+                    const uint32_t base = C::OFF_V + (i % C::NV) * C::TILE_BYTES;
+                    const int n = (BN - r0) * C::KSUB * 8;  // 16-byte chunks
+                    for (int x = t; x < n; x += 64) {
+                        const int row = r0 + x / (C::KSUB * 8), sl = (x / 8) % C::KSUB, q = x % 8;
+                        *reinterpret_cast<uint4*>(smem + base + sl * C::SUB_BYTES + row * 128 + q * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();       // generic writes, read by the tensor core
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_fixed);
+            }
         }
     } else {
         regs_inc<kRegsSoftmax>();
@@ -532,31 +689,46 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         int n_done = 0;              // items finished (o_final parity)
         bool ok = true;
         for (int rr = 0;; ++rr) {
-            const int w = item_of(rr);
-            if (w < 0) break;
-            const Item itm = describe(w);
-            const TileInfo ti = k == 0 ? itm.t0 : itm.t1;
-            const uint8_t* mrow = itm.mrow;
-            const int row_q = ti.q0 + r;
-            const long p_row = (long)row_q + a.Skv - a.Sq;
-            const int lim = (int)key_hi(p_row, a.Skv, a.causal, wr);   // visible keys: [lo, lim)
-            const int lo = (int)key_lo(p_row, a.Skv, wl);
-            float m_ref = -INFINITY;     // reference max (log2 units, scaled)
-            float l_run = 0.f;
-            int it = 0;
-            // The item record gives the first chunk's tile flags and the first
-            // visited tile's kept keys; the mask bytes of each later tile are
-            // fetched one tile ahead.
+            // The item record: the first chunk's tile flags, the first visited
+            // tile's kept keys (the mask bytes of each later tile are fetched one
+            // tile ahead) and, for packed calls, the claimed item's index.  A
+            // dense item is known before its record arrives; a packed one only
+            // from it, and the warpgroup agrees that the record arrived before
+            // anything is taken from it.
+            Item itm;
+            if constexpr (!PACKED) {
+                const int wd = item_of(rr);
+                if (wd < 0) break;
+                itm = describe(wd);
+            }
             const int slot = rr & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(info_full(slot), (rr >> 1) & 1, abort_flag));
             uint32_t mw[4];              // kept keys of the current tile, 32 per word
             uint32_t f0 = 0;
+            int w = -1;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) mw[q] = ok ? info[8 * slot + 4 + q] : 0u;
-            if (ok) f0 = info[8 * slot + 3];
+            for (int q = 0; q < 4; ++q) mw[q] = ok ? info[REC * slot + 4 + q] : 0u;
+            if (ok) {
+                f0 = info[REC * slot + 3];
+                if constexpr (PACKED) w = (int)info[REC * slot + 8];
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(info_empty(slot));
             __syncwarp();
+            if constexpr (PACKED) {
+                if (!named_bar_and(3 + k, BM, ok) || w < 0) break;
+                itm = describe(w);
+            }
+            const TileInfo ti = k == 0 ? itm.t0 : itm.t1;
+            const uint8_t* mrow = itm.mrow;
+            const int row_q = ti.q0 + r / g;             // this row's query (within the request)
+            const int skv = PACKED ? itm.skv : a.Skv, sq = PACKED ? itm.sq : a.Sq;
+            const long p_row = (long)row_q + skv - sq;
+            const int lim = (int)key_hi(p_row, skv, a.causal, wr);   // visible keys: [lo, lim)
+            const int lo = (int)key_lo(p_row, skv, wl);
+            float m_ref = -INFINITY;     // reference max (log2 units, scaled)
+            float l_run = 0.f;
+            int it = 0;
             TileIter tiles(mrow, itm.first, itm.n_all, itm.kv_end_all, lane, f0);
             auto fetch = [&](int j, uint8_t* mb) {
 #pragma unroll
@@ -684,14 +856,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (ok) tc_fence_after();
             }
             ++n_done;
-            const bool row_ok = r < ti.rows_valid;
+            const bool row_ok = PACKED ? (r < g * qpb && r / g < ti.rows_valid) : r < ti.rows_valid;
+            // this row's place in o [.., D] and lse
+            const size_t orow = PACKED ? (size_t)(itm.qs + row_q) * a.Hq + itm.hq + r % g
+                                       : ((size_t)itm.b * a.Sq + row_q) * a.Hq + itm.hq;
             // O / l, and the LSE in log2 units; a sink adds exp(s) to l only
             // (GQAPagedFwdOp sinks), taken against max(m_ref, s) so nothing
             // overflows; +inf zeroes the row
             float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             float lse2 = l_run > 0.f ? m_ref + log2f(l_run) : -INFINITY;
             if (sinks && l_run > 0.f) {
-                const float s2 = sinks[itm.hq] * 1.4426950408889634f;
+                const float s2 = sinks[itm.hq + r % g] * 1.4426950408889634f;
                 if (s2 == INFINITY) {
                     inv = 0.f;
                     lse2 = INFINITY;
@@ -711,9 +886,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // visited key, or a wait that gave up, writes zeros directly.  The
             // last box of an item is left reading while the warpgroup moves on;
             // the storing thread waits for it before the buffer is written again.
+            // A packed block that the request's end cuts short is stored row by
+            // row (its box would reach the next request's rows).
+            const bool whole = !PACKED || ti.rows_valid == qpb;
             if (r == 0) bulk_wait_read_all();
             __syncwarp();
-            const bool staged = named_bar_and(3 + k, BM, ok && it > 0);
+            const bool staged = named_bar_and(3 + k, BM, ok && it > 0 && whole);
             if (staged) {
                 uint32_t ow[D];
                 if constexpr (D == 128) {
@@ -737,18 +915,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     fence_proxy_async_smem();
                     named_bar_sync(3 + k, BM);
                     if (r == 0) {
-                        tma_store_4d(&tm_o, stage, sub * 64, ti.q0, itm.hq, itm.b);
+                        if constexpr (PACKED)
+                            tma_store_3d(&tm_o, stage, sub * 64, itm.hq, itm.qs + ti.q0);
+                        else
+                            tma_store_4d(&tm_o, stage, sub * 64, ti.q0, itm.hq, itm.b);
                         bulk_commit_group();
                         if (sub + 1 < C::KSUB) bulk_wait_read_all();
                     }
                 }
+            } else if (PACKED && !whole && ok && it > 0) {
+                // the rows of a cut block, 16 bytes at a time
+                uint32_t ow[D];
+                if constexpr (D == 128) {
+                    tmem_ld128(tmem + lane_addr + col_o, ow);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c)
+                        tmem_ld32(tmem + lane_addr + col_o + 32 * c, reinterpret_cast<float*>(ow + 32 * c));
+                }
+                if (row_ok) {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + orow * D);
+#pragma unroll
+                    for (int e = 0; e < D / 8; ++e) {
+                        const float* f = reinterpret_cast<const float*>(ow + 8 * e);
+                        dst[e] = make_uint4(pack2<F16>(f[0] * inv, f[1] * inv), pack2<F16>(f[2] * inv, f[3] * inv),
+                                            pack2<F16>(f[4] * inv, f[5] * inv), pack2<F16>(f[6] * inv, f[7] * inv));
+                    }
+                }
             } else if (row_ok) {
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
-                                                      (((size_t)itm.b * a.Sq + row_q) * a.Hq + itm.hq) * D);
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + orow * D);
 #pragma unroll
                 for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
             }
-            if (row_ok && a.lse) a.lse[((size_t)itm.b * a.Sq + row_q) * a.Hq + itm.hq] = lse2 * kLn2;
+            if (row_ok && a.lse) a.lse[orow] = lse2 * kLn2;
             tc_fence_before();
             if (!named_bar_and(3 + k, BM, ok)) break;     // the whole warpgroup stops together
         }
@@ -767,39 +966,51 @@ __global__ void empty_rows_kernel(__nv_bfloat16* o, float* lse, long rows, int D
     }
 }
 
-template <int D, bool OPTS, bool F16>
+template <int D, int MODE, bool OPTS, bool F16>
 cudaError_t launch_prefill_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                             const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream) {
+                             const CUtensorMap& tm_o, const PrefillArgs& a, long max_items, cudaStream_t stream) {
     using C = Cfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, OPTS, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MODE, OPTS, F16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int n_qpairs = (a.Sq + NQ * BM - 1) / (NQ * BM);
-    const long n_items = (long)n_qpairs * a.B * a.Hq;
+    const int n_qpairs = MODE == kModeDense ? (a.Sq + NQ * BM - 1) / (NQ * BM) : 0;
+    const long n_items = MODE == kModeDense ? (long)n_qpairs * a.B * a.Hq : max_items;
     const long sms = a.num_sms > 0 ? a.num_sms : 148;
     const long grid = n_items < sms ? n_items : sms;    // persistent: one CTA per SM
-    prefill_kernel<D, OPTS, F16><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, tm_o, a,
-                                                                                        n_qpairs);
+    if (grid <= 0) return cudaSuccess;
+    prefill_kernel<D, MODE, OPTS, F16><<<(unsigned)grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v,
+                                                                                              tm_o, a, n_qpairs);
     return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_prefill_mode(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                const CUtensorMap& tm_o, const PrefillArgs& a, long max_items, cudaStream_t stream) {
+    const bool opts = a.x.wl >= 0 || a.x.wr >= 0 || a.x.cap_out != 0.f || a.x.sinks != nullptr;
+    const int sel = (opts ? 1 : 0) + (a.f16 ? 2 : 0);
+    switch (a.D * 4 + sel) {
+        case 64 * 4 + 0: return launch_prefill_t<64, MODE, false, false>(tm_q, tm_k, tm_v, tm_o, a, max_items, stream);
+        case 64 * 4 + 1: return launch_prefill_t<64, MODE, true, false>(tm_q, tm_k, tm_v, tm_o, a, max_items, stream);
+        case 64 * 4 + 2: return launch_prefill_t<64, MODE, false, true>(tm_q, tm_k, tm_v, tm_o, a, max_items, stream);
+        case 64 * 4 + 3: return launch_prefill_t<64, MODE, true, true>(tm_q, tm_k, tm_v, tm_o, a, max_items, stream);
+        case 128 * 4 + 0: return launch_prefill_t<128, MODE, false, false>(tm_q, tm_k, tm_v, tm_o, a, max_items, stream);
+        case 128 * 4 + 1: return launch_prefill_t<128, MODE, true, false>(tm_q, tm_k, tm_v, tm_o, a, max_items, stream);
+        case 128 * 4 + 2: return launch_prefill_t<128, MODE, false, true>(tm_q, tm_k, tm_v, tm_o, a, max_items, stream);
+        case 128 * 4 + 3: return launch_prefill_t<128, MODE, true, true>(tm_q, tm_k, tm_v, tm_o, a, max_items, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_o, const PrefillArgs& a, cudaStream_t stream) {
-    const bool opts = a.x.wl >= 0 || a.x.wr >= 0 || a.x.cap_out != 0.f || a.x.sinks != nullptr;
-    const int sel = (opts ? 1 : 0) + (a.f16 ? 2 : 0);
-    switch (a.D * 4 + sel) {
-        case 64 * 4 + 0: return launch_prefill_t<64, false, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        case 64 * 4 + 1: return launch_prefill_t<64, true, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        case 64 * 4 + 2: return launch_prefill_t<64, false, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        case 64 * 4 + 3: return launch_prefill_t<64, true, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        case 128 * 4 + 0: return launch_prefill_t<128, false, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        case 128 * 4 + 1: return launch_prefill_t<128, true, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        case 128 * 4 + 2: return launch_prefill_t<128, false, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        case 128 * 4 + 3: return launch_prefill_t<128, true, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return launch_prefill_mode<kModeDense>(tm_q, tm_k, tm_v, tm_o, a, 0, stream);
+}
+
+cudaError_t launch_prefill_packed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                  const CUtensorMap& tm_o, const PrefillArgs& a, long max_items, cudaStream_t stream) {
+    return launch_prefill_mode<kModePacked>(tm_q, tm_k, tm_v, tm_o, a, max_items, stream);
 }
 
 cudaError_t launch_empty_rows(void* o, float* lse, long rows, int D, cudaStream_t stream) {

@@ -36,6 +36,14 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
     __shared__ int base;
     __shared__ int bucket[NBUCKET];
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    // pairs (flag bit 2): an entry covers two consecutive row blocks
+    const bool pairs = (paged & 4) != 0;
+    const int span = pairs ? 2 * qpb : qpb;            // queries per entry
+    auto cost_of = [&](int b, int q0, int qs, int sq, int ks, int L) {
+        int c = entry_cost(make_int4(b, q0, qs, sq), make_int4(ks, L, 0, 0), qpb, g, causal);
+        if (pairs && q0 + qpb < sq) c += entry_cost(make_int4(b, q0 + qpb, qs, sq), make_int4(ks, L, 0, 0), qpb, g, causal);
+        return c;
+    };
     if (threadIdx.x == 0) base = 0;
     for (int i = threadIdx.x; i < NBUCKET; i += 1024) bucket[i] = 0;
     __syncthreads();
@@ -52,7 +60,7 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
                 ks = (int)min((long)max(kv[b], 0), kv_cap);
                 L = (int)min((long)max(kv[b + 1], ks), kv_cap) - ks;
             }
-            nrb = (sq + qpb - 1) / qpb;
+            nrb = (sq + span - 1) / span;
             if ((paged & 2) && sq == 1) nrb = 0;      // a decode step, run by the split decode kernel
         }
         int x = nrb;                                   // inclusive scan within the warp
@@ -76,14 +84,13 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
         const int first = base + (warp > 0 ? warp_sum[warp - 1] : 0) + x - nrb;
         // the request's estimated cost: the sum of its blocks' costs
         int total = 0;
-        for (int k = 0; k < nrb; ++k)
-            total += entry_cost(make_int4(b, k * qpb, qs, sq), make_int4(ks, L, 0, 0), qpb, g, causal);
+        for (int k = 0; k < nrb; ++k) total += cost_of(b, k * span, qs, sq, ks, L);
         const int key = min(NBUCKET - 1, total / 16);
         for (int k = 0; k < nrb; ++k) {
             const int e = first + k;
             if (e >= max_entries) break;
             int4* dst = reinterpret_cast<int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
-            dst[0] = make_int4(b, k * qpb, qs, sq);
+            dst[0] = make_int4(b, k * span, qs, sq);
             dst[1] = make_int4(ks, L, key, 0);             // .w: the request's start once placed
         }
         __syncthreads();
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
         const int4 e0 = src[0], e1 = src[1];
         // blocks of the request that made the list (all of them unless the
         // cap cut it short), so that the placed entries fill [0, n)
-        if (e0.y == 0) atomicAdd(&bucket[e1.z], min((e0.w + qpb - 1) / qpb, n - e));
+        if (e0.y == 0) atomicAdd(&bucket[e1.z], min((e0.w + span - 1) / span, n - e));
     }
     __syncthreads();
     {
@@ -139,14 +146,14 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
     for (int e = threadIdx.x; e < n; e += 1024) {
         int4* src = reinterpret_cast<int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
         const int4 e0 = src[0], e1 = src[1];
-        if (e0.y == 0) src[1].w = atomicAdd(&bucket[e1.z], min((e0.w + qpb - 1) / qpb, n - e));
+        if (e0.y == 0) src[1].w = atomicAdd(&bucket[e1.z], min((e0.w + span - 1) / span, n - e));
     }
     __syncthreads();
     for (int e = threadIdx.x; e < n; e += 1024) {
         const int4* src = reinterpret_cast<const int4*>(tmp + (size_t)e * ot::ENTRY_INTS);
         const int4 e0 = src[0], e1 = src[1];
-        const int k = e0.y / qpb;
-        const int cnt = min((e0.w + qpb - 1) / qpb, n - (e - k));
+        const int k = e0.y / span;
+        const int cnt = min((e0.w + span - 1) / span, n - (e - k));
         const int start = reinterpret_cast<const int4*>(tmp + (size_t)(e - k) * ot::ENTRY_INTS)[1].w;
         const int pos = start + cnt - 1 - k;
         if (pos < 0 || pos >= n) continue;
@@ -164,9 +171,10 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
 
 cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int g, int causal,
                                int total_q, long kv_cap, int32_t* tmp, int32_t* entries, int32_t* n_entries,
-                               int max_entries, cudaStream_t stream, bool skip_single) {
-    // flags: bit 0 paged (kv holds cache lengths), bit 1 skip single-query requests
-    const int flags = (paged ? 1 : 0) | (skip_single ? 2 : 0);
+                               int max_entries, cudaStream_t stream, bool skip_single, bool pairs) {
+    // flags: bit 0 paged (kv holds cache lengths), bit 1 skip single-query
+    // requests, bit 2 pairs of row blocks
+    const int flags = (paged ? 1 : 0) | (skip_single ? 2 : 0) | (pairs ? 4 : 0);
     varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_q, kv, flags, B, qpb, g, causal, total_q, kv_cap, tmp,
                                                entries, n_entries, max_entries);
     return cudaGetLastError();
