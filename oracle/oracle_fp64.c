@@ -308,6 +308,20 @@ int oracle_attn_dense_rows_ex(const void* q, const void* k, const void* v,
 }
 
 /*
+ * Physical page holding token t of a request whose block_table row is trow
+ * (max_pages entries): trow[t / page_size], the token sitting in slot
+ * t % page_size of it (the page addressing of the paged ops on the TileOPs
+ * page).  -1 when the logical page lies past the row or the page id lies
+ * outside [0, num_pages), so that no read leaves the table or the pool.
+ */
+static long page_of_token(const int32_t* trow, int max_pages, int page_size, int num_pages, int t) {
+    const long lp = t / page_size;
+    if (lp < 0 || lp >= max_pages) return -1;
+    const int32_t phys = trow[lp];
+    return (phys < 0 || phys >= num_pages) ? -1 : (long)phys;
+}
+
+/*
  * Paged attention, written as "gather the request's cache into a dense
  * sequence, then apply the dense definition" (the paged ops on the TileOPs
  * page read the same logical sequence through block_table).
@@ -356,7 +370,8 @@ static int paged_all(const void* q, const void* k_cache, const void* v_cache,
         char* vd = (char*)malloc(es * tok_elems * (size_t)(L > 0 ? L : 1));
         if (!kd || !vd) { free(kd); free(vd); return -3; }
         for (int t = 0; t < L; ++t) {
-            const int32_t phys = block_table[(size_t)b * max_pages + t / page_size];
+            const long phys = page_of_token(block_table + (size_t)b * max_pages, max_pages, page_size, num_pages, t);
+            if (phys < 0) { free(kd); free(vd); return -6; }
             const size_t src = ((size_t)phys * page_size + t % page_size) * tok_elems;
             memcpy(kd + (size_t)t * tok_elems * es, (const char*)k_cache + src * es,
                    tok_elems * es);
@@ -474,7 +489,9 @@ int oracle_attn_paged_fp8kv_ex(const void* q, int q_dtype, const uint8_t* k_cach
         for (size_t e = 0; e < q_elems; ++e) qd[e] = load_elem(q, (size_t)b * q_elems + e, q_dtype);
         const int32_t* trow = block_table + (size_t)b * max_pages;   /* request b's pages */
         for (int t = 0; t < L; ++t) {
-            const size_t src = ((size_t)trow[t / page_size] * page_size + t % page_size) * tok_elems;
+            const long phys = page_of_token(trow, max_pages, page_size, num_pages, t);
+            if (phys < 0) { free(qd); free(kd); free(vd); return -6; }
+            const size_t src = ((size_t)phys * page_size + t % page_size) * tok_elems;
             for (int r = 0; r < Hkv; ++r) {
                 const double ks = k_scale ? k_scale[(size_t)b * Hkv + r] : 1.0;
                 const double vs = v_scale ? v_scale[(size_t)b * Hkv + r] : 1.0;

@@ -673,8 +673,7 @@ MUTANTS = {
     "lse_missing_log": ("*lse_out = M + log(Z);", "*lse_out = M + Z;"),
     "values_from_keys": ("w * load_elem(v, v_off + d, dtype)", "w * load_elem(k, v_off + d, dtype)"),
     "empty_row_lse_zero": ("*lse_out = -INFINITY;\n        return;", "*lse_out = 0;\n        return;"),
-    "page_index_swapped": ("block_table[(size_t)b * max_pages + t / page_size]",
-                           "block_table[(size_t)b * max_pages + t % page_size]"),
+    "page_index_swapped": ("const long lp = t / page_size;", "const long lp = t % page_size;"),
     "weights_unnormalised": ("exp(z[j] - M) / Z;", "exp(z[j] - M);"),
     "query_row_transposed": ("(((size_t)b * Sq + i) * Hq + h)", "(((size_t)b * Hq + h) * Sq + i)"),
     "varlen_key_offset_ignored": ("(const char*)k + (size_t)ks * Hkv * D * es,", "(const char*)k,"),
