@@ -351,7 +351,10 @@ def attn_fwd_paged(q, k_cache, v_cache, cu_seqlens_q, cache_seqlens, block_table
     row).  Options as in attn_fwd_dense.
     split_decode: give the call the workspace that sends requests with one
     query to the split-KV decode kernel (False: every request on the packed
-    kernel).  A caller's workspace decides by its size instead.
+    kernel).  A caller's workspace decides by its size instead.  With the
+    split, the packed kernel runs beside the decode kernel on a library-owned
+    high-priority stream, forked from and joined back into the current stream
+    inside the call.
     Returns (o [total_q, Hq, D], lse [total_q, Hq]).
     """
     _check_16_cuda("q", q, 3)

@@ -508,6 +508,49 @@ gqa_status attn_fwd_varlen(const void* q, const void* k, const void* v, const in
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
+// A second stream per device and host thread, of the highest priority, with a
+// fork and a join event.  The prefill chunks of a mixed paged call run on it
+// beside the decode steps on the caller's stream: the chunks are tensor-bound
+// and the decode steps memory-bound, so side by side on separate SMs they take
+// less than one after the other.  Created on first use outside a stream
+// capture and kept (a capture uses one created by an earlier call); nullptr if
+// there is none (the call then runs everything on the caller's stream).
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static SideStream* side_stream(cudaStream_t caller) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+    thread_local std::vector<SideStream> per_dev;
+    if ((int)per_dev.size() <= dev) per_dev.resize(dev + 1);
+    SideStream& ss = per_dev[dev];
+    if (ss.s == nullptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+        int least = 0, greatest = 0;
+        cudaStream_t st = nullptr;
+        cudaEvent_t f = nullptr, j = nullptr;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+            if (f) cudaEventDestroy(f);
+            cudaStreamDestroy(st);
+            cudaGetLastError();
+            return nullptr;
+        }
+        ss.s = st;
+        ss.fork = f;
+        ss.join = j;
+    }
+    return &ss;
+}
+
 gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
                           const int32_t* cache_seqlens, const int32_t* block_table, int page_size, void* o,
                           float* lse, int B, int total_q, int Hq, int Hkv, int D, int num_pages, int max_pages,
@@ -560,10 +603,23 @@ gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cach
     const bool route = paged_decode_plan(B, Hq, Hkv, D, page_size, max_pages, &dp) &&
                        workspace_bytes >= d_off + dp.workspace_bytes &&
                        (reinterpret_cast<uintptr_t>(wsc + d_off) & 255u) == 0;
+    // With decode steps routed, the chunks run on the side stream beside them,
+    // keeping the share of the persistent CTAs the plan kernel computes (ws[2])
+    SideStream* side = route ? side_stream(s) : nullptr;
+    if (side) a.g_eff = ws + 2;
     if (gqa::launch_varlen_plan(cu_seqlens_q, cache_seqlens, true, B, a.qpb, a.g, a.causal, total_q,
                                 (long)max_pages * page_size, ws + 4 + (size_t)max_e * 8, ws + 4, ws, max_e,
-                                s, route) != cudaSuccess)
+                                s, route, false, side ? a.num_sms : 0) != cudaSuccess)
         return GQA_ERR_CUDA;
+    if (side) {
+        // fork after the plan: the chunks (highest priority, so their CTAs
+        // take their SMs first) and the decode steps become ready together
+        if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+            return GQA_ERR_CUDA;
+        if (gqa::launch_varlen_paged(tq, tk, tv, to, a, (long)max_e * Hkv, side->s) != cudaSuccess ||
+            cudaEventRecord(side->join, side->s) != cudaSuccess)
+            return GQA_ERR_CUDA;
+    }
     if (route) {
         DecodeArgs da{};
         da.q = q; da.k_cache = k_cache; da.v_cache = v_cache;
@@ -587,6 +643,7 @@ gqa_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cach
         if (gqa::launch_decode(da, use_tma ? &dk : nullptr, use_tma ? &dv : nullptr, box, s) != cudaSuccess)
             return GQA_ERR_CUDA;
     }
+    if (side) return cudaStreamWaitEvent(s, side->join, 0) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;   // join
     return gqa::launch_varlen_paged(tq, tk, tv, to, a, (long)max_e * Hkv, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 

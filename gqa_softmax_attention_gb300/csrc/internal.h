@@ -31,6 +31,10 @@ struct PrefillArgs {
     const int32_t* entries;   // [max_entries, 8]: b, q0, qs, sq, ks, L, -, -
     const int32_t* n_entries; // number of entries (device)
     int32_t* work;            // packed: item counter, zeroed by the plan kernel
+    // paged calls whose decode steps run beside them on the split decode
+    // kernel: CTAs at or past *g_eff exit at once, leaving their SMs to it
+    // (written by the plan kernel); nullptr: every CTA works
+    const int32_t* g_eff;
     int g;                    // query heads per KV head
     int qpb;                  // queries per row block: floor(128 / g)
     const int32_t* table;     // paged: block_table [B, max_pages]
@@ -73,10 +77,14 @@ int prefill_d256_take_device_error();
 // skip_single leaves requests with exactly one query out of the list (they
 // run on the split decode kernel instead).
 // pairs lists pairs of consecutive row blocks (q0 = 2k * qpb) for the
-// two-Q-tile kernel.
+// two-Q-tile kernel.  With skip_single, n_entries[2] receives how many of
+// `grid` persistent CTAs the listed blocks should keep so that they and the
+// left-out decode steps, run at the same time, end together (grid when there
+// is no decode step).
 cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int g, int causal,
                                int total_q, long kv_cap, int32_t* tmp, int32_t* entries, int32_t* n_entries,
-                               int max_entries, cudaStream_t stream, bool skip_single = false, bool pairs = false);
+                               int max_entries, cudaStream_t stream, bool skip_single = false, bool pairs = false,
+                               int grid = 0);
 // tm_q / tm_o: {D, Hq, total_q} with a {64, g, qpb} box.  Packed: tm_k / tm_v
 // {D, Hkv, total_kv} with {64, 1, 128} and {64, 1, 128 or 64 (D = 256)} boxes.
 // Paged: the caches as {64, 8, D / 64, pages * page_size / 8, Hkv} with

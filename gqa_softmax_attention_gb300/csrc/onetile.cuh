@@ -127,6 +127,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const PrefillArgs a, int n_qtiles) {
+    // CTAs past the share the plan gave this launch leave their SMs to the
+    // decode steps running beside it (uniform per CTA, before any set-up)
+    if (a.g_eff != nullptr && (int)blockIdx.x >= *a.g_eff) return;
     using C = Cfg<D, MODE>;
     constexpr bool PACKED = MODE != kBSHD;
     constexpr uint32_t IDESC_QK = make_idesc_16<F16>(BM, BN, false, false);

@@ -17,6 +17,15 @@ namespace {
 // sort over NBUCKET cost buckets), each request's blocks together and its
 // heaviest (last) block first.
 constexpr int NBUCKET = 2048;
+// SM time of one cached key of a decode step against one plan cost unit (see
+// the end of varlen_plan_kernel), as the two kernels run side by side: the
+// split decode kernel streams about 70 GB/s per SM on a share of the SMs, the
+// one-tile kernel about 7.2 TFLOP/s per SM, so (4 bytes / 70 GB/s) / (2^15
+// FLOP / 7.2 TFLOP/s) = 0.0126.  Set a little below: the chunks' persistent
+// grid cannot grow into SMs the decode steps leave, while the decode CTAs do
+// fill the SMs the chunks leave (measured on the mixed serving batch: 0.622,
+// 0.606 and 0.683 ms at 0.009, 0.0126 and 0.016).
+constexpr double kDecPerKey = 0.011;
 
 __device__ __forceinline__ int entry_cost(const int4 e0, const int4 e1, int qpb, int g, int causal) {
     const int q0 = e0.y, sq = e0.w, L = e1.y;
@@ -31,8 +40,9 @@ __device__ __forceinline__ int entry_cost(const int4 e0, const int4 e1, int qpb,
 __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, const int32_t* kv, int paged,
                                                           int B, int qpb, int g, int causal, int total_q,
                                                           long kv_cap, int32_t* tmp, int32_t* entries,
-                                                          int32_t* n_entries, int max_entries) {
+                                                          int32_t* n_entries, int max_entries, int grid) {
     __shared__ int warp_sum[32];
+    __shared__ unsigned long long pre_cost, dec_keys;   // listed blocks' cost; decode steps' cached keys
     __shared__ int base;
     __shared__ int bucket[NBUCKET];
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
@@ -44,7 +54,11 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
         if (pairs && q0 + qpb < sq) c += entry_cost(make_int4(b, q0 + qpb, qs, sq), make_int4(ks, L, 0, 0), qpb, g, causal);
         return c;
     };
-    if (threadIdx.x == 0) base = 0;
+    if (threadIdx.x == 0) {
+        base = 0;
+        pre_cost = 0;
+        dec_keys = 0;
+    }
     for (int i = threadIdx.x; i < NBUCKET; i += 1024) bucket[i] = 0;
     __syncthreads();
     // 1. entries in request order
@@ -85,6 +99,8 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
         // the request's estimated cost: the sum of its blocks' costs
         int total = 0;
         for (int k = 0; k < nrb; ++k) total += cost_of(b, k * span, qs, sq, ks, L);
+        if (total > 0) atomicAdd(&pre_cost, (unsigned long long)total);
+        if ((paged & 2) && sq == 1 && b < B && L > 0) atomicAdd(&dec_keys, (unsigned long long)L);
         const int key = min(NBUCKET - 1, total / 16);
         for (int k = 0; k < nrb; ++k) {
             const int e = first + k;
@@ -164,6 +180,19 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
     if (threadIdx.x == 0) {
         n_entries[0] = n;
         n_entries[1] = 0;                              // the attention kernel's item counter
+        // The listed blocks' share of `grid` persistent CTAs when decode steps
+        // run beside them: their estimated SM time against the decode steps',
+        // so that both end together.  A cost unit is half a 128-key tile of a
+        // full 128-row block (128 x 128 x D x 2 FLOP per KV head); a cached key
+        // of a decode step is 4 D bytes per KV head (16-bit K and V); D and
+        // Hkv cancel, and kDecPerKey converts the second into the first.
+        int ge = grid;
+        if (grid > 0 && pre_cost > 0 && dec_keys > 0) {
+            const double tp = (double)pre_cost, td = (double)dec_keys * kDecPerKey;
+            ge = (int)lrint((double)grid * tp / (tp + td));
+            ge = min(grid, max(ge, min(grid, 8)));
+        }
+        n_entries[2] = ge;
     }
 }
 
@@ -171,12 +200,12 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* cu_q, 
 
 cudaError_t launch_varlen_plan(const int32_t* cu_q, const int32_t* kv, bool paged, int B, int qpb, int g, int causal,
                                int total_q, long kv_cap, int32_t* tmp, int32_t* entries, int32_t* n_entries,
-                               int max_entries, cudaStream_t stream, bool skip_single, bool pairs) {
+                               int max_entries, cudaStream_t stream, bool skip_single, bool pairs, int grid) {
     // flags: bit 0 paged (kv holds cache lengths), bit 1 skip single-query
     // requests, bit 2 pairs of row blocks
     const int flags = (paged ? 1 : 0) | (skip_single ? 2 : 0) | (pairs ? 4 : 0);
     varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_q, kv, flags, B, qpb, g, causal, total_q, kv_cap, tmp,
-                                               entries, n_entries, max_entries);
+                                               entries, n_entries, max_entries, grid);
     return cudaGetLastError();
 }
 

@@ -300,11 +300,21 @@ gqa_status attn_fwd_varlen(const void* q, const void* k, const void* v,
  *                     page_size, max_pages) bytes, 256-byte aligned, the
  *                     requests with exactly one query (decode steps) run on
  *                     the split-KV decode kernel of attn_decode_paged (where
- *                     Hq / Hkv < 32) and the rest on the packed kernel, in
- *                     two launches on `stream`; with less, every request runs
- *                     on the packed kernel.  Results agree within the usual
- *                     tolerance either way.  Calls sharing a workspace must
- *                     not overlap on the GPU.
+ *                     Hq / Hkv < 32) and the rest on the packed kernel; with
+ *                     less, every request runs on the packed kernel.  Results
+ *                     agree within the usual tolerance either way.  Calls
+ *                     sharing a workspace must not overlap on the GPU.
+ *
+ * Streams: with the decode steps on the split kernel, the packed kernel runs
+ * beside them on a second stream of the highest priority that the library
+ * keeps per device and host thread (created on the first such call that is
+ * not inside a stream capture), forked from `stream` after the plan kernel
+ * and joined back into `stream` with events before the call returns: work
+ * queued on `stream` afterwards sees both parts complete, and a captured call
+ * records the fork and join in the graph.  The packed kernel then keeps the
+ * share of the SMs that the plan kernel estimates, on the device, from the
+ * requests' lengths; the decode CTAs take the rest.  If the second stream
+ * cannot be had, both parts run one after the other on `stream`.
  *
  * Any page_size >= 1 and num_pages >= 1: pages whose size is a multiple of 8
  * move as 8-row TMA blocks, other page sizes are gathered row by row (slower

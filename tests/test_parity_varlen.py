@@ -150,6 +150,33 @@ def test_paged_options_float16(g, split_decode):
         check(o, lse, ro, rl, "paged options " + str(dtype))
 
 
+def test_paged_decode_heavy_split(g):
+    """Decode steps over long caches beside one short chunk: the plan leaves
+    the chunk the fewest CTAs (the rest of the SMs go to the split decode
+    kernel, which runs beside it on the caller's stream), and both parts match
+    the oracle.  Then a chunk with no decode step keeps every CTA."""
+    for ql, L in (([1] * 40 + [300], [6000 + 37 * i for i in range(40)] + [500]), ([300, 700], [500, 900])):
+        Hq, Hkv, D, ps = 32, 8, 128, 64
+        p = W.varlen_paged_inputs(ql, L, Hq, Hkv, D, ps, seed=len(ql))
+        kc, vc = poison(p)
+        tq = p["q"].shape[0]
+        ws = torch.zeros(g.attn_paged_workspace_size(len(ql), tq, Hq, Hkv, D, ps, p["block_table"].shape[1]),
+                         dtype=torch.uint8, device="cuda")
+        o, lse = g.paged(p["q"].cuda(), kc.cuda(), vc.cuda(), p["cu_seqlens_q"].cuda(), p["cache_seqlens"].cuda(),
+                         p["block_table"].cuda(), causal=True, workspace=ws)
+        torch.cuda.synchronize()
+        ro, rl = oracle.attn_paged_varlen(p["q"], p["k_cache"], p["v_cache"], p["cu_seqlens_q"], p["cache_seqlens"],
+                                          p["block_table"], causal=True)
+        check(o, lse, ro, rl, "decode-heavy split %d requests" % len(ql))
+        # the plan's share of the persistent CTAs (third word of the workspace header)
+        share = int(ws[:16].view(torch.int32)[2])
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        if ql[0] == 1:
+            assert 8 <= share < sms // 4, share
+        else:
+            assert share == sms, share
+
+
 def test_paged_equals_uniform_decode(g):
     """One query per request through the packed call equals the [B, 1] decode
     entry point (different kernels, same definition)."""
