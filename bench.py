@@ -130,12 +130,12 @@ def load_peaks():
 # (long_chunked_prefill captured at B=1 of its four independent batches and
 # scaled by 4).
 TRAFFIC = {
-    "qwen3_8b_prefill": ("bytes", (93.504512 + 30.836480) * 1e6),
-    "long_chunked_prefill": ("bytes", 4 * (534.100480 + 31.266816) * 1e6),
+    "qwen3_8b_prefill": ("bytes", (94.029056 + 31.439360) * 1e6),
+    "long_chunked_prefill": ("bytes", 4 * (534.310144 + 31.316480) * 1e6),
     "paged_decode": ("ratio", (559.379712 + 6.031616) / 556.916736),
     "wide_group_decode": ("ratio", (233.683200 + 3.794688) / 232.683520),
     "paged_decode_fp8kv": ("ratio", (279.805952 + 5.622016) / 278.458368),
-    "wide_group_decode_fp8kv": ("ratio", (117.060352 + 3.536896) / 116.341760),
+    "wide_group_decode_fp8kv": ("ratio", (117.059840 + 3.576832) / 116.341760),
     "wide_group_prefill": ("bytes", (235.505152 + 160.755456) * 1e6),
     "varlen_prefill": ("bytes", (799.823872 + 502.045696) * 1e6),
 }
