@@ -577,10 +577,15 @@ decode_gather_kernel(const DecodeArgs a, int R, int g, int n_rowblk) {
 //     two dims 2(t/4), 2(t/4)+1 of a 16-dim chunk; a byte permute splits them
 //     into an even-dim and an odd-dim n8 block, and the stored O interleaves
 //     the two blocks back into dim order.
-template <int D, int MF>
+// SW: the swapped form for at most 8 query rows per KV head (one fragment):
+// the keys and dims take the MMAs' M side and the rows their N = 8 side
+// (fp8_swap_consumer).
+template <int D, int MF, bool SW = false>
 struct F8Cfg {
+    static_assert(!SW || MF == 1, "the swapped form holds one block of 8 rows");
     static constexpr int TK = key_tile(D);                  // keys per tile (64, or 32 at D = 256)
-    static constexpr int ROWS = 16 * MF;                    // padded rows per CTA
+    static constexpr int ROWS = SW ? 8 : 16 * MF;           // padded rows per CTA
+    static constexpr int RW = SW ? 8 : 16;                  // rows of a warp's merge block
     static constexpr int KSPLIT = MF == 1 ? TK / 16 : TK / 32;   // warps per fragment, splitting each tile
     static constexpr int KPW = TK / KSPLIT;                 // keys of a tile per warp (16 or 32)
     static constexpr int NC = MF * KSPLIT;                  // consumer warps
@@ -593,13 +598,16 @@ struct F8Cfg {
     static constexpr int NFK = KPW / 8;                     // key blocks of a warp's S
     static constexpr int NFD = D / 8;                       // dim blocks of O
     static constexpr int MROW = D + 4;                      // merge row: O, max, sum (16-byte rows)
-    static constexpr int MERGE = KSPLIT > 1 ? NC * 16 * MROW * 4 : 0;
-    // byte ring: up to three CTAs per SM by shared memory at D = 128 with one or two fragments
-    static constexpr int BUDGET = (D == 128 && MF <= 2) ? 75 * 1024 : 113 * 1024;
+    static constexpr int MERGE = KSPLIT > 1 ? NC * RW * MROW * 4 : 0;
+    // byte ring: up to three CTAs per SM by shared memory at D = 128 with one
+    // or two fragments, and in the swapped form
+    static constexpr int BUDGET = (SW || (D == 128 && MF <= 2)) ? 75 * 1024 : 113 * 1024;
     static constexpr int NS_FIT = (BUDGET - 2048) / (2 * TILE8);
     static constexpr int NS = NS_FIT < 6 ? NS_FIT : 6;
     static constexpr int RING = NS * 2 * TILE8;
-    static constexpr int MINB = (D == 128 && MF == 1) ? 2 : 1;   // CTAs per SM the registers must allow
+    // CTAs per SM the registers must allow (the swapped form's accumulators
+    // are half as large)
+    static constexpr int MINB = SW ? 3 : (D == 128 && MF == 1) ? 2 : 1;
     static constexpr int OFF_KV = 0;                        // byte ring; the merge reuses it
     static constexpr int OFF_BAR = RING > MERGE ? RING : MERGE;   // full[NS], empty[NS]
     static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
@@ -628,11 +636,262 @@ __device__ __forceinline__ uint32_t off8(int r, int c) {
     return (uint32_t)((c >> 3) * SUB8 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-template <int D, int MF, bool QBF>
-__global__ void __launch_bounds__(F8Cfg<D, MF>::NT, F8Cfg<D, MF>::MINB)
+// Four e4m3fn codes (byte order) -> two float16 pairs, exactly: bytes 0, 1
+// into lo and bytes 2, 3 into hi (low half first).  Two conversions on the
+// register's 16-bit halves.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
+// movmatrix: the transpose of an 8x8 matrix of 16-bit elements held one
+// register per lane (lane l: row l / 4, columns 2 (l % 4), +1), same layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Consumer warps of the swapped form (at most 8 query rows per KV head, a
+// whole row block per CTA).  With 4 rows, S = Q K^T and O += P V as m16n8k16
+// MMAs with the rows on M would use 4 of 16 rows; here the transposes are
+// computed instead, the keys (S) and the dims (O) on M and the rows on N = 8:
+//   S^T = K Q^T: A = 16 keys x 16 dims of the e4m3 tile (ldmatrix, the four
+//     bytes a lane receives widened as the k = 2t, 2t+1 and 2t+8, 2t+9 pairs,
+//     t = lane % 4), B = Q^T under the same map of dims (a permutation of the
+//     summation order); lane l holds keys l / 4 and l / 4 + 8 of rows 2t, 2t+1.
+//   The online softmax runs per row over the keys of the warp's share: the
+//     row max across the eight lanes of one t (shuffles), the lazy reference
+//     max as elsewhere, each lane's partial row sums kept apart until the end.
+//   O^T += V^T P^T: P^T (B, keys on k, rows on n) is the S^T accumulator
+//     packed to float16 and transposed in registers (movmatrix); V^T (A) comes
+//     from ldmatrix.trans of the value tile, whose 16-bit elements are dim
+//     pairs: a byte permute splits them so that M row g takes dim 2g and row
+//     g + 8 dim 2g + 1 of each 16-dim chunk.
+// The warps of a CTA split each key tile and merge their (max, sum, O) once,
+// as in the unswapped form.  Half the MMAs, and O takes 4 D / 16 registers.
+template <int D, bool QBF, class C>
+__device__ __forceinline__ void fp8_swap_consumer(const DecodeArgs& a, const Work& w, uint8_t* smem, uint32_t sb,
+                                                  uint32_t bar0, volatile int* abort_flag, int warp, int lane, int R,
+                                                  int g) {
+    static_assert(C::KSPLIT > 1 && C::KPW == 16 && C::ROWS == 8, "16 keys of each tile per warp, 8 rows");
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (C::NS + s); };
+    const int wk = warp;                           // share of each key tile
+    const int kw0 = wk * C::KPW;                   // this warp's first key of a tile
+    const int gq = lane >> 2, t4 = lane & 3;
+    const int kv = w.b * a.Hkv + w.hkv;
+    const float ks = a.k_scale ? a.k_scale[kv] : 1.f;
+    const float vs = a.v_scale ? a.v_scale[kv] : 1.f;
+    const float sl = a.scale_log2 * ks;
+    const float cap_in = a.x.cap_in * ks, cap_out = a.x.cap_out;
+    // Q^T fragments: row gq of the block (zero past it), dims 16 kk + 4t .. +3
+    uint32_t qf[C::KSTEPS][2];
+    {
+        const int r = w.row0 + gq;
+        const bool valid = gq < w.rows_here;
+        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.q) +
+                               (((size_t)w.qrow0 + r / g) * a.Hq + w.hkv * g + r % g) * D;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            uint2 v = make_uint2(0u, 0u);
+            if (valid) v = *reinterpret_cast<const uint2*>(qrow + 16 * kk + 4 * t4);
+            qf[kk][0] = QBF ? bf16x2_to_f16x2(v.x) : v.x;          // k = 2t, 2t+1
+            qf[kk][1] = QBF ? bf16x2_to_f16x2(v.y) : v.y;          // k = 2t+8, 2t+9
+        }
+    }
+    // rows 2t and 2t + 1 of the accumulators: key range [lo, lim)
+    int lim[2], lo[2];
+    int lim_min = INT_MAX, lo_max = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int rl = 2 * t4 + h;
+        lo[h] = 0;
+        lim[h] = -1;
+        if (rl < w.rows_here) {
+            // keys [lo, lim) of query r / g at key position p (TileOPs
+            // GQAPagedFwdOp: causal j <= p, window p - wL <= j <= p + wR)
+            const long p = (long)((w.row0 + rl) / g) + w.L - a.Sq;
+            long hi = w.t_end;
+            if (a.causal) hi = min(hi, p + 1);
+            if (a.x.wr >= 0) hi = min(hi, p + a.x.wr + 1);
+            lim[h] = (int)max(-1L, hi);
+            if (a.x.wl >= 0) lo[h] = (int)max(0L, min((long)w.L, p - a.x.wl));
+            lim_min = min(lim_min, lim[h]);
+            lo_max = max(lo_max, lo[h]);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lim_min = min(lim_min, __shfl_xor_sync(0xffffffffu, lim_min, o));
+        lo_max = max(lo_max, __shfl_xor_sync(0xffffffffu, lo_max, o));
+    }
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float acc[D / 16][4];                          // O^T: dims 16c + 2gq (+1), rows 2t, 2t+1
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+    const int m = lane >> 3;                       // ldmatrix: this lane addresses matrix m
+    for (int it = 0; it < w.n_tiles; ++it) {
+        const int s = it % C::NS;
+        const int t0 = w.t_begin + it * C::TK;
+        const uint32_t sK = sb + C::OFF_KV + s * 2 * C::TILE8;
+        const uint32_t sV = sK + C::TILE8;
+        if (!__all_sync(0xffffffffu, mbar_wait(full(s), (it / C::NS) & 1, abort_flag))) break;
+        const int nvalid = w.t_end - t0;
+        if (nvalid < kw0 + C::KPW) {
+            // This warp's value rows past the request's end hold stale bytes:
+            // zero them (no other warp reads them).
+            const int r0 = nvalid > kw0 ? nvalid : kw0;
+            const int per_sub = (kw0 + C::KPW - r0) * 8;
+            for (int idx = lane; idx < per_sub * C::NSUB8; idx += 32)
+                *reinterpret_cast<uint4*>(smem + (sV - sb) + (idx / per_sub) * C::SUB8 +
+                                          (r0 + (idx % per_sub) / 8) * 128 + (idx % 8) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        // ---- S^T = K Q^T over this warp's 16 keys (two accumulation chains)
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sz[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; kk += 2) {
+            // matrices: (keys 0-7, chunk kk), (keys 8-15, kk), (keys 0-7, kk+1), (keys 8-15, kk+1)
+            uint32_t r[4];
+            ldsm_x4(sK + off8<C::SUB8>(kw0 + (m & 1) * 8 + (lane & 7), kk + (m >> 1)), r[0], r[1], r[2], r[3]);
+            uint32_t a0[4], a1[4];
+            e4m3x4_to_f16x4(r[0], a0[0], a0[2]);
+            e4m3x4_to_f16x4(r[1], a0[1], a0[3]);
+            e4m3x4_to_f16x4(r[2], a1[0], a1[2]);
+            e4m3x4_to_f16x4(r[3], a1[1], a1[3]);
+            mma16816<true>(sa, a0, qf[kk][0], qf[kk][1]);
+            mma16816<true>(sz, a1, qf[kk + 1][0], qf[kk + 1][1]);
+        }
+        // element e: key gq + 8 (e >> 1) of the warp's share, row 2t + (e & 1)
+        float sc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = sa[e] + sz[e];
+        float mx[2] = {-INFINITY, -INFINITY};
+        const bool unmasked = t0 + kw0 + C::KPW <= lim_min && t0 + kw0 >= lo_max && cap_out == 0.f;
+        if (unmasked) {                             // every key of this warp's share is visible
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sc[e] *= sl;
+                mx[e & 1] = fmaxf(mx[e & 1], sc[e]);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int h = e & 1;
+                const int t = t0 + kw0 + gq + 8 * (e >> 1);
+                float x = cap_out != 0.f ? softcap_log2(sc[e], cap_in, cap_out) : sc[e] * sl;
+                x = t >= lo[h] && t < lim[h] ? x : -INFINITY;       // the select drops stale keys
+                sc[e] = x;
+                mx[h] = fmaxf(mx[h], x);
+            }
+        }
+        // Lazy rescale, as in the unswapped form (P stays below 2^8)
+        float alpha[2], m_use[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
+            alpha[h] = 1.f;
+            if (mx[h] > m_run[h] + 8.f) {
+                alpha[h] = fast_exp2(m_run[h] - mx[h]);             // 0 while m_run is -inf
+                m_run[h] = mx[h];
+            }
+            m_use[h] = m_run[h] == -INFINITY ? 0.f : m_run[h];      // no -inf - -inf
+        }
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pv[e] = fast_exp2(sc[e] - m_use[e & 1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + (pv[h] + pv[h + 2]);
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+                acc[c][0] *= alpha[0]; acc[c][1] *= alpha[1];
+                acc[c][2] *= alpha[0]; acc[c][3] *= alpha[1];
+            }
+        }
+        // P^T as the B fragments: keys 2t, 2t+1 (and + 8) of row gq
+        const uint32_t pb0 = movmatrix_t(pack2<true>(pv[0], pv[1]));
+        const uint32_t pb1 = movmatrix_t(pack2<true>(pv[2], pv[3]));
+        // ---- O^T += V^T P^T, two 16-dim chunks per ldmatrix
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+            // matrices: (keys 0-7, chunk 2q), (keys 8-15, 2q), (keys 0-7, 2q+1), (keys 8-15, 2q+1)
+            uint32_t r[4];
+            ldsm_x4_t(sV + off8<C::SUB8>(kw0 + (m & 1) * 8 + (lane & 7), 2 * q + (m >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                // bytes of r: V[k0][d], V[k0][d+1], V[k1][d], V[k1][d+1] (k0 = 2t, d = 2gq):
+                // widened to (k0: d, d+1) and (k1: d, d+1), then regrouped by dim
+                uint32_t k0a, k1a, k0b, k1b;
+                e4m3x4_to_f16x4(r[2 * i], k0a, k1a);
+                e4m3x4_to_f16x4(r[2 * i + 1], k0b, k1b);
+                const uint32_t av[4] = {__byte_perm(k0a, k1a, 0x5410), __byte_perm(k0a, k1a, 0x7632),
+                                        __byte_perm(k0b, k1b, 0x5410), __byte_perm(k0b, k1b, 0x7632)};
+                mma16816<true>(acc[2 * q + i], av, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));      // this warp is done with the stage
+    }
+    // ---- merge the warps and store the split's partial O (FP32, normalised) and base-2 LSE
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
+    }
+    const size_t part_row0 = ((size_t)(w.b * a.Hkv + w.hkv) * a.max_splits + w.split) * R + w.row0;
+    named_bar_sync(1, C::NCT);                     // every consumer warp is done with the ring
+    float* mg = reinterpret_cast<float*>(smem + C::OFF_KV);
+    float* mine = mg + (size_t)warp * C::RW * C::MROW;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float* row = mine + (2 * t4 + h) * C::MROW;
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c)
+            *reinterpret_cast<float2*>(row + 16 * c + 2 * gq) = make_float2(acc[c][h], acc[c][2 + h]);
+        if (gq == 0) {
+            row[D] = m_run[h];
+            row[D + 1] = l_run[h];
+        }
+    }
+    named_bar_sync(1, C::NCT);
+    // warp wk merges dims [wk * D / KSPLIT, (wk + 1) * D / KSPLIT)
+    constexpr int DW = D / C::KSPLIT;
+    for (int rr = 0; rr < w.rows_here; ++rr) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < C::KSPLIT; ++u) M = fmaxf(M, mg[(u * C::RW + rr) * C::MROW + D]);
+        const float M_use = M == -INFINITY ? 0.f : M;
+        float wgt[C::KSPLIT], L = 0.f;
+#pragma unroll
+        for (int u = 0; u < C::KSPLIT; ++u) {
+            wgt[u] = fast_exp2(mg[(u * C::RW + rr) * C::MROW + D] - M_use);
+            L += wgt[u] * mg[(u * C::RW + rr) * C::MROW + D + 1];
+        }
+        const float inv = L > 0.f ? vs / L : 0.f;
+        for (int d = wk * DW + lane; d < (wk + 1) * DW; d += 32) {
+            float o = 0.f;
+#pragma unroll
+            for (int u = 0; u < C::KSPLIT; ++u) o += wgt[u] * mg[(u * C::RW + rr) * C::MROW + d];
+            a.part_o[(part_row0 + rr) * D + d] = o * inv;
+        }
+        if (wk == 0 && lane == 0) a.part_lse[part_row0 + rr] = L > 0.f ? M + log2f(L) : -INFINITY;
+    }
+}
+
+template <int D, int MF, bool QBF, bool SW>
+__global__ void __launch_bounds__(F8Cfg<D, MF, SW>::NT, F8Cfg<D, MF, SW>::MINB)
 decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeArgs a, int R, int g, int n_rowblk, int box_tokens) {
-    using C = F8Cfg<D, MF>;
+    using C = F8Cfg<D, MF, SW>;
     griddep_launch_dependents();                 // the combine may be scheduled (it waits for this grid)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -747,6 +1006,9 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     mbar_drain(full(it % C::NS), (it / C::NS) & 1);
             }
         }
+    } else if constexpr (SW) {
+        // ------------------------------------------------------------ consumer warps (swapped form)
+        fp8_swap_consumer<D, QBF, C>(a, w, smem, sb, bar0, abort_flag, warp, lane, R, g);
     } else {
         // ------------------------------------------------------------ consumer warps
         const int mf = warp / C::KSPLIT;            // row fragment
@@ -1273,24 +1535,29 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CU
 }
 
 namespace {
-template <int D, int MF, bool QBF>
+template <int D, int MF, bool QBF, bool SW = false>
 cudaError_t launch_fp8_t(const DecodeArgs& a, const CUtensorMap& tm_k, const CUtensorMap& tm_v, int box_tokens,
                          int R, int g, int n_rowblk, cudaStream_t stream) {
-    using C = F8Cfg<D, MF>;
-    cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<D, MF, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
+    using C = F8Cfg<D, MF, SW>;
+    cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<D, MF, QBF, SW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid(a.max_splits, a.Hkv, a.B * n_rowblk);
-    decode_fp8_kernel<D, MF, QBF><<<grid, C::NT, C::SMEM, stream>>>(tm_k, tm_v, a, R, g, n_rowblk, box_tokens);
+    decode_fp8_kernel<D, MF, QBF, SW><<<grid, C::NT, C::SMEM, stream>>>(tm_k, tm_v, a, R, g, n_rowblk, box_tokens);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_fp8_d(const DecodeArgs& a, const CUtensorMap& tm_k, const CUtensorMap& tm_v, int box_tokens,
                          int R, int g, cudaStream_t stream) {
+    const bool qbf = !a.f16;
+    if (R <= 8) {
+        // at most 8 rows per KV head: the swapped form (rows on the MMAs' N side)
+        return qbf ? launch_fp8_t<D, 1, true, true>(a, tm_k, tm_v, box_tokens, R, g, 1, stream)
+                   : launch_fp8_t<D, 1, false, true>(a, tm_k, tm_v, box_tokens, R, g, 1, stream);
+    }
     const int mf = choose_mf(R);
     const int n_rowblk = (R + 16 * mf - 1) / (16 * mf);
-    const bool qbf = !a.f16;
     switch (mf * 2 + (qbf ? 1 : 0)) {
         case 2: return launch_fp8_t<D, 1, false>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);
         case 3: return launch_fp8_t<D, 1, true>(a, tm_k, tm_v, box_tokens, R, g, n_rowblk, stream);

@@ -72,6 +72,8 @@ SMALL = [
     (2, 4, 24, 2, 256, 5, [3, 901]),                 # 48 rows per KV head (split kernel, not tensor cores)
     (4, 1, 32, 8, 128, 12, [12, 13, 0, 600]),        # 12-token pages, an empty request
     (2, 2, 16, 2, 128, 24, [500, 49]),               # a multiple of 8 that does not tile the 64-key tile
+    (2, 2, 16, 4, 128, 64, [100, 2000]),             # 8 rows per KV head (4 heads x 2 queries): the swapped form
+    (2, 2, 6, 2, 256, 16, [40, 700]),                # 6 rows per KV head (3 heads x 2 queries), D 256
 ]
 
 
@@ -84,8 +86,9 @@ def test_small_shapes(g, case):
     compare(o, lse, ro, rl, str(case))
 
 
-def test_unit_scales_and_fp16_query(g):
-    p = W.paged_fp8_inputs(3, 2, 16, 2, 128, 16, lengths=[77, 1, 500], seed=5)
+@pytest.mark.parametrize("Sq", [2, 1], ids=["16rows", "8rows_swapped"])
+def test_unit_scales_and_fp16_query(g, Sq):
+    p = W.paged_fp8_inputs(3, Sq, 16, 2, 128, 16, lengths=[77, 1, 500], seed=5)
     o, lse = run(g, p, scales=False)
     ro, rl = reference(p, scales=False)
     compare(o, lse, ro, rl, "no scales")
@@ -105,9 +108,10 @@ def test_scales_reach_the_right_heads(g):
     compare(o, lse, ro, rl, "spread scales")
 
 
+@pytest.mark.parametrize("Sq", [4, 2], ids=["16rows", "8rows_swapped"])
 @pytest.mark.parametrize("D", [128, 256])
-def test_options_and_non_causal(g, D):
-    p = W.paged_fp8_inputs(3, 4, 8, 2, D, 16, lengths=[300, 17, 1200], seed=7)
+def test_options_and_non_causal(g, D, Sq):
+    p = W.paged_fp8_inputs(3, Sq, 8, 2, D, 16, lengths=[300, 17, 1200], seed=7)
     sinks = torch.tensor([0.5, -1.0, float("-inf"), 2.0, 0.0, 1.0, 3.0, -0.5])
     kw = dict(window_left=100, window_right=0, softcap=5.0, sinks=sinks)
     o, lse = run(g, p, **kw)
