@@ -33,8 +33,8 @@
 //
 // The path is bound by HBM bandwidth; the MMAs are small and hidden under the
 // loads, so warp-level mma.sync is used rather than tcgen05.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include <climits>
 #include <cmath>
@@ -618,12 +618,6 @@ struct F8Cfg {
     static_assert(NS >= 2 && SMEM <= 227 * 1024, "pipeline depth / shared memory budget");
 };
 
-// Two e4m3fn codes (low byte first) -> two float16 (low half first), exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
-
 // A bfloat16 pair -> a float16 pair (round to nearest even).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     const __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
@@ -634,16 +628,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
 template <int SUB8>
 __device__ __forceinline__ uint32_t off8(int r, int c) {
     return (uint32_t)((c >> 3) * SUB8 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
-
-// Four e4m3fn codes (byte order) -> two float16 pairs, exactly: bytes 0, 1
-// into lo and bytes 2, 3 into hi (low half first).  Two conversions on the
-// register's 16-bit halves.
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
-    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(x));
 }
 
 // movmatrix: the transpose of an 8x8 matrix of 16-bit elements held one
@@ -676,7 +660,8 @@ template <int D, bool QBF, class C>
 __device__ __forceinline__ void fp8_swap_consumer(const DecodeArgs& a, const Work& w, uint8_t* smem, uint32_t sb,
                                                   uint32_t bar0, volatile int* abort_flag, int warp, int lane, int R,
                                                   int g) {
-    static_assert(C::KSPLIT > 1 && C::KPW == 16 && C::ROWS == 8, "16 keys of each tile per warp, 8 rows");
+    static_assert(C::KSPLIT > 1 && C::KPW == 16 && C::ROWS == 8 && C::NFD == D / 8,
+                  "16 keys of each tile per warp, 8 rows, D / 16 accumulators of two dim blocks each");
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (C::NS + s); };
     const int wk = warp;                           // share of each key tile
@@ -827,13 +812,10 @@ __device__ __forceinline__ void fp8_swap_consumer(const DecodeArgs& a, const Wor
             ldsm_x4_t(sV + off8<C::SUB8>(kw0 + (m & 1) * 8 + (lane & 7), 2 * q + (m >> 1)), r[0], r[1], r[2], r[3]);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                // bytes of r: V[k0][d], V[k0][d+1], V[k1][d], V[k1][d+1] (k0 = 2t, d = 2gq):
-                // widened to (k0: d, d+1) and (k1: d, d+1), then regrouped by dim
-                uint32_t k0a, k1a, k0b, k1b;
-                e4m3x4_to_f16x4(r[2 * i], k0a, k1a);
-                e4m3x4_to_f16x4(r[2 * i + 1], k0b, k1b);
-                const uint32_t av[4] = {__byte_perm(k0a, k1a, 0x5410), __byte_perm(k0a, k1a, 0x7632),
-                                        __byte_perm(k0b, k1b, 0x5410), __byte_perm(k0b, k1b, 0x7632)};
+                // bytes of r: V[k0][d], V[k0][d+1], V[k1][d], V[k1][d+1] (k0 = 2t, d = 2gq)
+                uint32_t av[4];
+                e4m3x4_dim_split(r[2 * i], av[0], av[1]);
+                e4m3x4_dim_split(r[2 * i + 1], av[2], av[3]);
                 mma16816<true>(acc[2 * q + i], av, pb0, pb1);
             }
         }
@@ -1102,9 +1084,11 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     ldsm_x4(sK + off8<C::SUB8>(kw0 + (nb + (m >> 1)) * 8 + (lane & 7), kk + (m & 1)), r[0], r[1],
                             r[2], r[3]);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma16816<true>(sc[nb + (j >> 1)], qf[kk + (j & 1)], e4m3x2_to_f16x2(r[j]),
-                                       e4m3x2_to_f16x2(r[j] >> 16));
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t b0, b1;
+                        e4m3x4_to_f16x4(r[j], b0, b1);
+                        mma16816<true>(sc[nb + (j >> 1)], qf[kk + (j & 1)], b0, b1);
+                    }
                 }
             }
             // ---- scaled, masked logits (log2 units) and the rows' maxima
@@ -1183,11 +1167,11 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         // bytes: V[k0][d], V[k0][d+1], V[k1][d], V[k1][d+1] (d even)
-                        mma16816<true>(acc[4 * q + 2 * i], pa[kk], e4m3x2_to_f16x2(__byte_perm(r[2 * i], 0, 0x0020)),
-                                       e4m3x2_to_f16x2(__byte_perm(r[2 * i + 1], 0, 0x0020)));
-                        mma16816<true>(acc[4 * q + 2 * i + 1], pa[kk],
-                                       e4m3x2_to_f16x2(__byte_perm(r[2 * i], 0, 0x0031)),
-                                       e4m3x2_to_f16x2(__byte_perm(r[2 * i + 1], 0, 0x0031)));
+                        uint32_t e0, o0, e1, o1;
+                        e4m3x4_dim_split(r[2 * i], e0, o0);
+                        e4m3x4_dim_split(r[2 * i + 1], e1, o1);
+                        mma16816<true>(acc[4 * q + 2 * i], pa[kk], e0, e1);
+                        mma16816<true>(acc[4 * q + 2 * i + 1], pa[kk], o0, o1);
                     }
                 }
             }

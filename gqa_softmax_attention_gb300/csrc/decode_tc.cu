@@ -51,8 +51,8 @@
 // Rows past g * Sq in the 128-row M dimension are padding; their results are
 // never stored.  Value rows past a request's end are zeroed in shared memory
 // before P V reads them.  Every wait is bounded (ptx.cuh).
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include <cmath>
 
@@ -196,12 +196,6 @@ __device__ __forceinline__ void q_row_to_tmem(const DecodeArgs& a, uint32_t tadd
     __syncwarp();                                  // tcgen05.st is warp-collective
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) tmem_st32(taddr + 32 * c, w + 32 * c);
-}
-
-// Two e4m3fn codes (low byte first) -> two float16 (low half first), exactly.
-__device__ __forceinline__ uint32_t tc_e4m3x2_to_f16x2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
 // F16: the MMA operand type (float16 for e4m3 caches, widened exactly).  KV8:
@@ -375,12 +369,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     if (idx >= BN * CH8) break;
                     const int k = idx % BN, c16 = 2 * (idx / BN);   // two 8-dim chunks share one 64-column slice
                     uint8_t* row = dst + (k >> 3) * C::GROUP_STRIDE + (c16 >> 3) * 1024 + (k & 7) * 128;
-                    *reinterpret_cast<uint4*>(row + (((c16 & 7) ^ (k & 7)) << 4)) =
-                        make_uint4(tc_e4m3x2_to_f16x2(x[u].x), tc_e4m3x2_to_f16x2(x[u].x >> 16),
-                                   tc_e4m3x2_to_f16x2(x[u].y), tc_e4m3x2_to_f16x2(x[u].y >> 16));
+                    uint32_t h[8];
+                    e4m3x4_to_f16x4(x[u].x, h[0], h[1]);
+                    e4m3x4_to_f16x4(x[u].y, h[2], h[3]);
+                    e4m3x4_to_f16x4(x[u].z, h[4], h[5]);
+                    e4m3x4_to_f16x4(x[u].w, h[6], h[7]);
+                    *reinterpret_cast<uint4*>(row + (((c16 & 7) ^ (k & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
                     *reinterpret_cast<uint4*>(row + ((((c16 + 1) & 7) ^ (k & 7)) << 4)) =
-                        make_uint4(tc_e4m3x2_to_f16x2(x[u].z), tc_e4m3x2_to_f16x2(x[u].z >> 16),
-                                   tc_e4m3x2_to_f16x2(x[u].w), tc_e4m3x2_to_f16x2(x[u].w >> 16));
+                        make_uint4(h[4], h[5], h[6], h[7]);
                 }
             }
             fence_proxy_async_smem();              // the tensor core reads what the warp wrote

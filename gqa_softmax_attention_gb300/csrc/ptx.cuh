@@ -242,6 +242,26 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// Four e4m3fn codes (byte order) -> two float16 pairs, exactly: bytes 0, 1
+// into lo and bytes 2, 3 into hi (low half first).  Two conversions on the
+// register's 16-bit halves.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
+// Four e4m3fn codes laid out as ldmatrix.trans gives a 16-bit view of them,
+// V[k0][d], V[k0][d+1], V[k1][d], V[k1][d+1], -> the float16 pairs of dim d
+// (even: V[k0][d], V[k1][d]) and of dim d + 1 (odd), exactly.
+__device__ __forceinline__ void e4m3x4_dim_split(uint32_t x, uint32_t& even, uint32_t& odd) {
+    uint32_t k0, k1;
+    e4m3x4_to_f16x4(x, k0, k1);
+    even = __byte_perm(k0, k1, 0x5410);
+    odd = __byte_perm(k0, k1, 0x7632);
+}
+
 // Arrive on an mbarrier once every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
