@@ -84,6 +84,63 @@ def test_mixed_paged_graph_replay(g, split_decode):
         compare(out.cpu(), lse.cpu(), ro, rl, "mixed replay %s" % lens)
 
 
+def _mixed_case(seed):
+    ql, L = [1, 600, 1, 1, 300], [3000, 1800, 40, 7000, 700]
+    Hq, Hkv, D, ps = 32, 8, 128, 64
+    p = W.varlen_paged_inputs(ql, L, Hq, Hkv, D, ps, seed=seed)
+    names = ("q", "k_cache", "v_cache", "cu_seqlens_q", "cache_seqlens", "block_table")
+    dev = {n: p[n].cuda() for n in names}
+    return p, names, dev, (len(ql), p["q"].shape[0], Hq, Hkv, D, ps, p["block_table"].shape[1])
+
+
+def test_mixed_paged_on_side_stream_then_caller_work(g):
+    """A mixed call on a non-default stream runs its chunks on the library's
+    side stream and joins back: work queued on the caller's stream right after
+    the call (here a copy of the outputs) sees both parts complete."""
+    p, names, dev, sz = _mixed_case(6)
+    ws = torch.empty(g.attn_paged_workspace_size(*sz), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            out, lse = g.paged(*[dev[n] for n in names], causal=True, workspace=ws)
+            o_copy, l_copy = out.clone(), lse.clone()     # queued on st behind the call
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn_paged_varlen(p["q"], p["k_cache"], p["v_cache"], p["cu_seqlens_q"], p["cache_seqlens"],
+                                      p["block_table"], causal=True)
+    compare(o_copy.cpu(), l_copy.cpu(), ro, rl, "mixed call on a side stream, copied on the caller's stream")
+
+
+def test_mixed_paged_captured_in_fresh_thread(g):
+    """Captured in a host thread that has made no earlier mixed call (no side
+    stream yet, and none may be created during a capture): the call runs both
+    parts on the capturing stream, and the graph replays correctly."""
+    import threading
+    p, names, dev, sz = _mixed_case(8)
+    ws = torch.empty(g.attn_paged_workspace_size(*sz), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dev["q"])
+    lse = torch.empty((p["q"].shape[0], 32), dtype=torch.float32, device="cuda")
+    err = []
+
+    def body():
+        try:
+            torch.cuda.set_device(0)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                g.paged(*[dev[n] for n in names], causal=True, out=out, lse=lse, workspace=ws)
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception as e:          # reported in the main thread
+            err.append(e)
+
+    t = threading.Thread(target=body)
+    t.start()
+    t.join()
+    assert not err, err
+    ro, rl = oracle.attn_paged_varlen(p["q"], p["k_cache"], p["v_cache"], p["cu_seqlens_q"], p["cache_seqlens"],
+                                      p["block_table"], causal=True)
+    compare(out.cpu(), lse.cpu(), ro, rl, "mixed call captured in a fresh thread")
+
+
 def test_fp8kv_decode_graph_replay(g):
     """The FP8-KV decode replays with new lengths and new scales."""
     B, Sq, Hq, Hkv, D, ps = 6, 1, 32, 8, 128, 64
