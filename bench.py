@@ -134,7 +134,7 @@ TRAFFIC = {
     "long_chunked_prefill": ("bytes", 4 * (534.310144 + 31.316480) * 1e6),
     "paged_decode": ("ratio", (559.379712 + 6.031616) / 556.916736),
     "wide_group_decode": ("ratio", (233.683200 + 3.794688) / 232.683520),
-    "paged_decode_fp8kv": ("ratio", (279.812864 + 5.155840) / 278.458368),
+    "paged_decode_fp8kv": ("ratio", (279.798016 + 5.109504) / 278.458368),
     "wide_group_decode_fp8kv": ("ratio", (117.059840 + 3.576832) / 116.341760),
     "wide_group_prefill": ("bytes", (235.305216 + 159.707392) * 1e6),
     "varlen_prefill": ("bytes", (799.823872 + 502.045696) * 1e6),
