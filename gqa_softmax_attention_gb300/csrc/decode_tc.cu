@@ -89,17 +89,22 @@ struct TCfg {
     // flight per SM covers the memory latency at full bandwidth.  V tiles are
     // consumed about two tiles after their K (P V follows the softmax), so the
     // V ring is deeper.
-    // With e4m3 caches the byte tiles (TMA, 3-D boxes of 128-byte rows) come
-    // first and the 16-bit rings the wideners fill are shallower; the V ring
-    // keeps three tiles at D = 256 (P V of a tile follows its K by two tiles:
-    // with two, the 16-bit decode itself ran 35 % slower), the byte rings two.
-    static constexpr int NK = KV8 ? (D == 256 ? 2 : 3) : (D == 256 ? 3 : 4);
+    // With e4m3 caches the byte tiles (TMA, 5-D page-block boxes) come first
+    // and the 16-bit rings the wideners fill are shallower.  At D = 256 the V
+    // ring keeps three tiles (P V of a tile follows its K by two tiles: with
+    // two, the 16-bit decode itself ran 35 % slower) and the K ring one, since
+    // S = Q K^T frees its tile right after the wideners fill it; the byte
+    // rings get the rest, three tiles each.  A byte slot is held through the
+    // copy's latency and the widening after it, and with two per ring the
+    // wideners waited for bytes about a fifth of each tile (two K + two byte
+    // slots each: 0.267 ms; one K + three each: 0.236 ms at B = 32).
+    static constexpr int NK = KV8 ? (D == 256 ? 1 : 3) : (D == 256 ? 3 : 4);
     static constexpr int NV = KV8 ? (D == 256 ? 3 : 4) : (D == 256 ? 4 : 6);
     static constexpr int NSUB8 = D / 128;                  // 128-column halves of an e4m3 row
     // e4m3 tile: [8-key group][128-column half][8 keys][128 bytes], 128-byte swizzle
     static constexpr int GROUP8 = NSUB8 * 1024;
     static constexpr int TILE8 = KV8 ? NSUB8 * BN * 128 : 0;   // one K or V tile of bytes
-    static constexpr int NK8 = KV8 ? (D == 256 ? 2 : 4) : 0;
+    static constexpr int NK8 = KV8 ? (D == 256 ? 3 : 4) : 0;
     static constexpr int NV8 = NK8;
     static constexpr int OFF_K8 = 0;
     static constexpr int OFF_V8 = OFF_K8 + NK8 * TILE8;
