@@ -142,6 +142,18 @@ def test_wide_groups_options_and_fp16(g, D):
     compare(o, lse, ro, rl, "tc: float16 query")
 
 
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("Hq", [16, 40, 64], ids=["32rows", "80rows", "128rows"])
+def test_tensor_core_widener_teams(g, D, Hq):
+    """The tensor-core decode's widening warps split into a K and a V team whose
+    sizes follow the rows per KV head (32: three K warps and two V, 80: one and
+    two, 128: one and one); ragged tails and unread slots poisoned with NaN."""
+    p = poison_unread(W.paged_fp8_inputs(3, 4, Hq, 2, D, 16, lengths=[5, 333, 1500], seed=17))
+    o, lse = run(g, p)
+    ro, rl = reference(p)
+    compare(o, lse, ro, rl, "tc teams")
+
+
 def test_matches_16bit_path_on_widened_cache(g):
     """The FP8 call equals the 16-bit decode on the caches widened to float16
     (every e4m3fn value is a float16), unit scales, float16 query."""

@@ -58,6 +58,8 @@ SMALL = [
     (2, 4, 32, 1, 128, 16, [129, 2000]),             # 128 rows
     (4, 2, 48, 1, 256, 64, [64, 65, 0, 999]),        # 96 rows, empty request, one-key tile
     (2, 4, 24, 2, 256, 8, [1, 5000]),                # 48 rows, 8-token pages
+    (3, 4, 16, 2, 256, 16, [5, 333, 1500]),          # 32 rows at D 256 (one softmax warp)
+    (2, 4, 64, 2, 256, 32, [700, 1201]),             # 128 rows at D 256 (four softmax warps)
 ]
 
 
