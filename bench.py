@@ -130,6 +130,7 @@ def load_peaks():
 # (long_chunked_prefill captured at B=1 of its four independent batches and
 # scaled by 4).
 TRAFFIC = {
+    "tiny_dense": ("bytes", 236.54e3 + 0.0),
     "qwen3_8b_prefill": ("bytes", (94.029056 + 31.439360) * 1e6),
     "long_chunked_prefill": ("bytes", 4 * (534.310144 + 31.316480) * 1e6),
     "paged_decode": ("ratio", (559.379712 + 6.031616) / 556.916736),
