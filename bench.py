@@ -81,6 +81,31 @@ def prefill_work(d):
     return 4.0 * c["D"] * c["Hq"] * pairs, pairs
 
 
+def executed_work(d, tile=128):
+    """FLOPs the dense kernels execute: whole 128 x 128 (query, key) tiles, one
+    query head at a time, for every tile holding at least one visible pair
+    (the kernels skip the rest); the visible-pair count above is the work the
+    roofline fractions use."""
+    c = d["config"]
+    B, Sq, Skv = c["B"], c["Sq"], c["Skv"]
+    nq, nk = (Sq + tile - 1) // tile, (Skv + tile - 1) // tile
+    m = d["key_padding_mask"]
+    if m is None:
+        any_key = torch.ones(B, nk, dtype=torch.bool)
+    else:
+        pad = torch.zeros(B, nk * tile, dtype=torch.bool)
+        pad[:, :Skv] = m.to(torch.bool)
+        any_key = pad.view(B, nk, tile).any(-1)
+    kt = torch.arange(nk, dtype=torch.int64)
+    tiles = 0
+    for qt in range(nq):
+        last = min(Skv - 1, (qt + 1) * tile - 1 + Skv - Sq) if c["causal"] else Skv - 1
+        if last < 0:
+            continue
+        tiles += int((any_key & (kt * tile <= last)[None, :]).sum())
+    return 4.0 * tile * tile * c["D"] * c["Hq"] * tiles
+
+
 def decode_bytes(p):
     """K/V bytes of the real tokens: 2 bytes per element, 1 for e4m3fn caches."""
     c = p["config"]
@@ -489,7 +514,11 @@ def part_detail(p, ts, peaks):
     """Per-part timing: mean and min launch-group time, achieved rate and its
     fraction of the measured and of the nominal peak, the target if any."""
     t = statistics.mean(ts)
-    d = dict(kernel=p.kernel_name(), ms=1e3 * t, ms_min=1e3 * min(ts), bound=p.bound(peaks))
+    d = dict(kernel=p.kernel_name(), ms=1e3 * t, ms_median=1e3 * statistics.median(ts), ms_min=1e3 * min(ts),
+             bound=p.bound(peaks))
+    if p.kind == "dense":
+        ex = executed_work(p.data)
+        d.update(executed_gflop=ex / 1e9, executed_tflops=ex / t / 1e12)
     if p.kind == "paged_varlen":
         d.update(tflops=p.flops / t / 1e12, gbs=p.bytes / t / 1e9, frac=p.ideal_s(peaks) / t,
                  gflop=p.flops / 1e9, gbytes=p.bytes / 1e9)
@@ -580,6 +609,7 @@ def bench_ours(args, world, rank, local):
     dom_j = max(range(len(parts)), key=lambda j: statistics.mean(per_part[j]))
     roof = roofline_of(parts[dom_j], statistics.mean(per_part[dom_j]), peaks)
 
+    graph = bench_graph(args, parts, flush, stream, dev)
     e2e = bench_e2e(args, parts, peaks, dev, stream, world)
     cpu = cpu_baseline(args, parts, peaks) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
@@ -592,7 +622,7 @@ def bench_ours(args, world, rank, local):
         "config": {"workload": workload_label(args.workload),
                    "parts": {p.name: p.data["config"] for p in parts}, "parallelism": "replicas",
                    "l2": "flushed between steps (%d MB write)" % (flush.numel() * 4 >> 20)},
-        "parts": detail, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+        "parts": detail, "roofline": roof, "graph_replay": graph, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
         "targets": {"judged_on": "measured peaks (MEASURED_PEAKS.json); frac_nominal uses %g TFLOP/s and %g GB/s"
                                  % (NOMINAL["bf16_tflops"], NOMINAL["hbm_gbs"]),
                     "met": {n: d["met"] for n, d in detail.items() if "met" in d}},
@@ -600,6 +630,34 @@ def bench_ours(args, world, rank, local):
         "peaks": peaks, "wall_s_timed_loop": wall,
     }
     return line
+
+
+def bench_graph(args, parts, flush, stream, dev):
+    """The step's calls captured once in a CUDA graph and replayed `steps`
+    times, L2 flushed before each replay (outside the events).  Outside the
+    timed region of the headline value; a capture that fails is reported, not
+    raised."""
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for p in parts:
+                p.run()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        del graph
+        return dict(ms_per_step=statistics.mean(ts), ms_median=statistics.median(ts), ms_min=min(ts),
+                    replays=len(ts))
+    except RuntimeError as e:
+        return dict(error=str(e).splitlines()[0][:200])
 
 
 def bench_e2e(args, parts, peaks, dev, stream, world):
@@ -843,7 +901,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="step", choices=sorted(STEPS) + sorted(W.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)

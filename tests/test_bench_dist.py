@@ -66,6 +66,28 @@ def test_visible_pairs_brute_force():
             assert bf == bench.visible_pairs(2, Sq, Skv, causal, m[:, :Skv])
 
 
+def test_executed_work_counts_tiles_with_a_visible_pair():
+    """Brute force over 128 x 128 tiles: a tile counts when any (row, key) in
+    it is visible (causal, end-aligned, and the padding mask)."""
+    torch.manual_seed(3)
+    for B, Sq, Skv, causal in [(2, 200, 300, True), (1, 128, 128, True), (2, 130, 257, False), (1, 64, 400, True),
+                               (1, 300, 200, True)]:
+        mask = torch.rand(B, Skv) < 0.3
+        mask[0, 128:256] = False                       # a whole key tile masked out
+        d = dict(config=dict(B=B, Sq=Sq, Skv=Skv, D=64, Hq=3, causal=causal), key_padding_mask=mask)
+        tiles = 0
+        for b in range(B):
+            for q0 in range(0, Sq, 128):
+                for k0 in range(0, Skv, 128):
+                    rows = torch.arange(q0, min(q0 + 128, Sq))[:, None]
+                    keys = torch.arange(k0, min(k0 + 128, Skv))[None, :]
+                    vis = mask[b, k0:k0 + 128][None, :].expand(rows.shape[0], -1).clone()
+                    if causal:
+                        vis &= keys <= rows + Skv - Sq
+                    tiles += int(bool(vis.any()))
+        assert bench.executed_work(d) == 4.0 * 128 * 128 * 64 * 3 * tiles
+
+
 def test_decode_bytes_count_the_element_size():
     from gqa_softmax_attention_gb300 import workloads as W
     for kind, gen, elem in (("paged", W.paged_inputs, 2), ("paged_fp8", W.paged_fp8_inputs, 1)):
