@@ -161,7 +161,6 @@ TRAFFIC = {
     "paged_decode": ("ratio", (559.379712 + 6.031616) / 556.916736),
     "wide_group_decode": ("ratio", (233.683200 + 3.794688) / 232.683520),
     "paged_decode_fp8kv": ("ratio", (279.798016 + 5.109504) / 278.458368),
-    "wide_group_decode_fp8kv": ("ratio", (117.082368 + 3.994112) / 116.341760),
     "wide_group_prefill": ("bytes", (235.305216 + 159.707392) * 1e6),
     "varlen_prefill": ("bytes", (799.823872 + 502.045696) * 1e6),
 }

@@ -92,19 +92,19 @@ struct TCfg {
     // With e4m3 caches the byte tiles (TMA, 5-D page-block boxes) come first
     // and the 16-bit rings the wideners fill are shallower.  At D = 256 the V
     // ring keeps three tiles (P V of a tile follows its K by two tiles: with
-    // two, the 16-bit decode itself ran 35 % slower) and the K ring one, since
-    // S = Q K^T frees its tile right after the wideners fill it; the byte
-    // rings get the rest, three tiles each.  A byte slot is held through the
-    // copy's latency and the widening after it, and with two per ring the
-    // wideners waited for bytes about a fifth of each tile (two K + two byte
-    // slots each: 0.267 ms; one K + three each: 0.236 ms at B = 32).
-    static constexpr int NK = KV8 ? (D == 256 ? 1 : 3) : (D == 256 ? 3 : 4);
+    // two, the 16-bit decode itself ran 35 % slower), the K ring two (so that
+    // a tile is widened while S of the one before runs) and the byte rings two
+    // each.  The K and V byte copies are issued as two independent streams
+    // (see the producer): in one fixed order, a full V ring held back the next
+    // K copy, and every split with a two-deep K ring lost (0.236 ms with one
+    // K tile and three byte tiles a ring, 0.210 ms now, at B = 32).
+    static constexpr int NK = KV8 ? (D == 256 ? 2 : 3) : (D == 256 ? 3 : 4);
     static constexpr int NV = KV8 ? (D == 256 ? 3 : 4) : (D == 256 ? 4 : 6);
     static constexpr int NSUB8 = D / 128;                  // 128-column halves of an e4m3 row
     // e4m3 tile: [8-key group][128-column half][8 keys][128 bytes], 128-byte swizzle
     static constexpr int GROUP8 = NSUB8 * 1024;
     static constexpr int TILE8 = KV8 ? NSUB8 * BN * 128 : 0;   // one K or V tile of bytes
-    static constexpr int NK8 = KV8 ? (D == 256 ? 3 : 4) : 0;
+    static constexpr int NK8 = KV8 ? (D == 256 ? 2 : 4) : 0;
     static constexpr int NV8 = NK8;
     static constexpr int OFF_K8 = 0;
     static constexpr int OFF_V8 = OFF_K8 + NK8 * TILE8;
@@ -318,8 +318,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const uint32_t tmem = *tmem_slot;
 
     // ------------------------------------------------------------ wideners (e4m3 caches)
-    // Each byte tile becomes the 16-bit tile the MMAs read, in the order the
-    // producer loads them (K0, K1, V0, K2, V1, ...): rows [8-key group][64-
+    // Each byte tile becomes the 16-bit tile the MMAs read, each team in its
+    // own stream's tile order: rows [8-key group][64-
     // column slice][8 keys][128 bytes] with the 128-byte swizzle, exactly as the
     // 5-D page-block boxes land in the 16-bit path.  Warps 6-7 widen, and so do
     // the warps of 0-3 that hold no query row once their (zero) Q rows are in;
@@ -411,8 +411,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         Cursor cur;
         cur.set(a, rg.s0);
         cur.lt = rg.lt0;
-        // Loads are issued in the order the MMAs consume them: K0, K1, V0, K2,
-        // V1, ...  Lane i finds the first cache row of page block i of a tile
+        // 16-bit caches: loads are issued in the order the MMAs consume them: K0,
+        // K1, V0, K2, V1, ...  Lane i finds the first cache row of page block i of a tile
         // when the tile's K is issued (-1: not loaded) and keeps it, for two
         // tiles, for the tile's V, with the tile's KV head.
         int row_ring0 = -1, row_ring1 = -1, n_ring0 = 0, n_ring1 = 0, h_ring0 = 0, h_ring1 = 0;
@@ -473,15 +473,101 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (is_v) ++nv; else ++nk;
             return true;
         };
-        find_rows(0);
-        ok = load(0, false);
-        for (int it = 0; it < n && ok; ++it) {
-            if (it + 1 < n) {
-                find_rows(it + 1);
-                ok = load(it + 1, false);
-                if (!ok) break;
+        if constexpr (KV8) {
+            // e4m3 caches: K and V as two streams, each with its own cursor and
+            // block-table window, a stream's next copy issued as soon as its byte
+            // slot is free (polled without suspending), V(i) never before K(i).
+            // The wideners drain the two byte rings independently, so neither
+            // stream waits behind the other's full ring.
+            struct Stream { Cursor cur; int win, pid, win_b, it, cnt, row, rows, h; bool found; };
+            auto init = [&](Stream& S) {
+                S.cur.set(a, rg.s0);
+                S.cur.lt = rg.lt0;
+                S.win = -(1 << 30); S.pid = -1; S.win_b = -1; S.it = 0; S.cnt = 0; S.found = false;
+            };
+            auto find = [&](Stream& S) {           // the stream's next tile: rows as find_rows gives them
+                Cursor& c = S.cur;
+                if (c.b != S.win_b) { S.win_b = c.b; S.win = -(1 << 30); }
+                const int32_t* trow = a.table + (size_t)c.b * a.max_pages;
+                const int t = (c.tf + c.lt) * BN + lane * box_tokens;
+                const int lp = t / a.page_size;
+                const int lp_first = __shfl_sync(0xffffffffu, lp, 0);
+                const int lp_last = __shfl_sync(0xffffffffu, lp, nbox - 1);
+                if (lp_last - S.win >= 32 || lp_first < S.win) {
+                    S.win = lp_first;
+                    S.pid = S.win + lane < a.max_pages ? trow[S.win + lane] : -1;
+                }
+                const int page = __shfl_sync(0xffffffffu, S.pid, (lp - S.win) & 31);
+                int row = -1;
+                if (lane < nbox && t < c.L && page >= 0 && page < a.num_pages) row = page * a.page_size + t % a.page_size;
+                S.row = row;
+                S.rows = __popc(__ballot_sync(0xffffffffu, row >= 0));
+                S.h = c.h;
+                S.found = true;
+                if (S.it + 1 < n) c.next(a);
+            };
+            auto try_issue = [&](Stream& S, bool is_v) -> bool {   // whole warp; false: slot still busy
+                const int ring = is_v ? C::NV8 : C::NK8;
+                const int slot = S.cnt % ring;
+                const uint32_t empty_bar = is_v ? v8_empty(slot) : k8_empty(slot);
+                const uint32_t full_bar = is_v ? v8_full(slot) : k8_full(slot);
+                int free_slot = 0;
+                if (lane == 0) free_slot = mbar_test_wait(empty_bar, ((S.cnt / ring) & 1) ^ 1) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, free_slot, 0)) return false;
+                if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)S.rows * box_tokens * 128 * C::NSUB8);
+                __syncwarp();                      // the expect-tx precedes every lane's copy
+                // one {128, 8, D / 128, box_tokens / 8, 1} byte box per page block
+                const uint32_t dst = sb + (is_v ? C::OFF_V8 : C::OFF_K8) + slot * C::TILE8 +
+                                     lane * box_tokens * 128 * C::NSUB8;
+                if (S.row >= 0)
+                    tma_load_5d(dst, is_v ? (const void*)&tm_v : (const void*)&tm_k, full_bar, 0, 0, 0, S.row / 8, S.h);
+                ++S.cnt;
+                ++S.it;
+                S.found = false;
+                return true;
+            };
+            Stream sk, sv;
+            init(sk);
+            init(sv);
+            unsigned long long idle_since = 0;
+            while (sk.it < n || sv.it < n) {
+                bool did = false;
+                if (sk.it < n) {
+                    if (!sk.found) find(sk);
+                    did |= try_issue(sk, false);
+                }
+                if (sv.it < n && sv.it < sk.it) {
+                    if (!sv.found) find(sv);
+                    did |= try_issue(sv, true);
+                }
+                if (did) {
+                    idle_since = 0;
+                    continue;
+                }
+                // neither slot free: poll again shortly, within the wait limit
+                int stop = 0;
+                if (lane == 0) {
+                    const unsigned long long now = globaltimer_ns();
+                    if (idle_since == 0) idle_since = now;
+                    if (*abort_flag) stop = 1;
+                    else if (now - idle_since > kWaitTimeoutNs) { *abort_flag = 1; stop = 1; }
+                }
+                if (__shfl_sync(0xffffffffu, stop, 0)) break;
+                __nanosleep(64);
             }
-            ok = load(it, true);
+            nk = sk.cnt;
+            nv = sv.cnt;
+        } else {
+            find_rows(0);
+            ok = load(0, false);
+            for (int it = 0; it < n && ok; ++it) {
+                if (it + 1 < n) {
+                    find_rows(it + 1);
+                    ok = load(it + 1, false);
+                    if (!ok) break;
+                }
+                ok = load(it, true);
+            }
         }
         if (lane == 0) {
             if (*abort_flag) {
