@@ -36,7 +36,11 @@
 //              are issued in the order the MMAs consume them (K0, K1, V0, K2,
 //              V1, ...) through 3-4 deep K and 4-6 deep V rings (about 200 KB
 //              in flight, which the memory latency at full bandwidth needs);
-//              block-table entries are read 32 at a time by the warp;
+//              block-table entries are read 32 at a time by the warp.  With
+//              float8_e4m3fn caches it loads byte tiles into byte rings instead,
+//              K and V as two independent streams (each with its own cursor),
+//              and warps 6-7 with the row-less warps of 0-3 widen them into the
+//              16-bit rings as a K team and a V team;
 //   warp 5     MMA issuer: S = Q K^T (M = 128 rows, N = 64 keys, Q from TMEM)
 //              into one of two TMEM buffers, O += P V with P read from TMEM
 //              (N = D, 16 keys per step, a fresh accumulator at each piece);
