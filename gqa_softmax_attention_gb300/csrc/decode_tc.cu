@@ -444,36 +444,25 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             else { row_ring0 = row; n_ring0 = cnt; h_ring0 = cur.h; }
             if (it + 1 < n) cur.next(a);
         };
-        auto load = [&](int it, bool is_v) -> bool {   // whole warp
+        auto load = [&](int it, bool is_v) -> bool {   // whole warp; 16-bit caches
             const int row = (it & 1) ? row_ring1 : row_ring0;
             const int cnt_rows = (it & 1) ? n_ring1 : n_ring0;
             const int h = (it & 1) ? h_ring1 : h_ring0;
             const int cnt = is_v ? nv : nk;
-            // e4m3 caches: byte tiles into their own rings, for the wideners
-            const int ring = KV8 ? (is_v ? C::NV8 : C::NK8) : (is_v ? C::NV : C::NK);
+            const int ring = is_v ? C::NV : C::NK;
             const int slot = cnt % ring;
-            const uint32_t empty_bar = KV8 ? (is_v ? v8_empty(slot) : k8_empty(slot))
-                                           : (is_v ? v_empty(slot) : k_empty(slot));
-            const uint32_t full_bar = KV8 ? (is_v ? v8_full(slot) : k8_full(slot))
-                                          : (is_v ? v_full(slot) : k_full(slot));
+            const uint32_t empty_bar = is_v ? v_empty(slot) : k_empty(slot);
+            const uint32_t full_bar = is_v ? v_full(slot) : k_full(slot);
             bool ok = true;
             if (lane == 0) {
                 ok = mbar_wait(empty_bar, ((cnt / ring) & 1) ^ 1, abort_flag);
-                const uint32_t bytes = KV8 ? (uint32_t)box_tokens * 128 * C::NSUB8 : blk_bytes;
-                if (ok) mbar_arrive_expect_tx(full_bar, (uint32_t)cnt_rows * bytes);
+                if (ok) mbar_arrive_expect_tx(full_bar, (uint32_t)cnt_rows * blk_bytes);
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
             __syncwarp();                          // the expect-tx precedes every lane's copy
             const void* map = is_v ? (const void*)&tm_v : (const void*)&tm_k;
-            if constexpr (KV8) {
-                // one {128, 8, D / 128, box_tokens / 8, 1} byte box per page block
-                const uint32_t dst = sb + (is_v ? C::OFF_V8 : C::OFF_K8) + slot * C::TILE8 +
-                                     lane * box_tokens * 128 * C::NSUB8;
-                if (row >= 0) tma_load_5d(dst, map, full_bar, 0, 0, 0, row / 8, h);
-            } else {
-                const uint32_t dst = sb + (is_v ? C::OFF_V : C::OFF_K) + slot * C::KV_TILE + lane * blk_bytes;
-                if (row >= 0) tma_load_5d(dst, map, full_bar, 0, 0, 0, row / 8, h);
-            }
+            const uint32_t dst = sb + (is_v ? C::OFF_V : C::OFF_K) + slot * C::KV_TILE + lane * blk_bytes;
+            if (row >= 0) tma_load_5d(dst, map, full_bar, 0, 0, 0, row / 8, h);
             if (is_v) ++nv; else ++nk;
             return true;
         };
